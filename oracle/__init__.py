@@ -1,0 +1,290 @@
+"""Python access to the plain CPU oracle (``lkv_oracle.c``).
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` use this module; the product package never
+imports it. The oracle is single-threaded C built with
+``-O2 -ffp-contract=off`` (no FMA contraction; the fused multiply-adds the
+decision values need are explicit ``fmaf`` calls).
+
+Arrays cross as numpy buffers: bf16 tensors as ``uint16`` bit patterns, fp32 as
+``float32``. See ``lkv_oracle.h`` for each function's definition and the page
+passages it follows.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+FP32, BF16 = 0, 1
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "lkv_oracle.c")
+_HDR = os.path.join(_HERE, "lkv_oracle.h")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liblkv_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+CFLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
+          "-fno-fast-math", "-Wall", "-Wextra", "-Wno-unused-parameter"]
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (if missing or older than its sources)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    stale = (not os.path.exists(_LIB_PATH)) or force or any(
+        os.path.getmtime(p) > os.path.getmtime(_LIB_PATH) for p in (_SRC, _HDR))
+    if stale:
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.run(["gcc", *CFLAGS, "-o", tmp, _SRC, "-lm"], check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+class DecodeArgs(C.Structure):
+    _fields_ = [
+        ("dtype", C.c_int32), ("n_kv_heads", C.c_int32), ("group", C.c_int32),
+        ("head_dim", C.c_int32), ("n_prefill", C.c_int64),
+        ("n_clusters", C.c_int32), ("local_buf", C.c_int32),
+        ("n_steps", C.c_int32), ("tau", C.c_float), ("budget", C.c_int32),
+        ("keys", C.c_void_p), ("values", C.c_void_p), ("assign", C.c_void_p),
+        ("cent", C.c_void_p), ("q", C.c_void_p), ("k_new", C.c_void_p),
+        ("v_new", C.c_void_p), ("attn_mask", C.c_void_p),
+    ]
+
+
+class DecodeResult(C.Structure):
+    _fields_ = [
+        ("max_sel", C.c_int32), ("max_segs", C.c_int32), ("out", C.c_void_p),
+        ("flag", C.c_void_p), ("r32", C.c_void_p), ("r64", C.c_void_p),
+        ("n_sel", C.c_void_p), ("n_tok", C.c_void_p), ("sel", C.c_void_p),
+        ("win_start", C.c_void_p), ("n_units", C.c_void_p),
+        ("seg_start", C.c_void_p), ("seg_len", C.c_void_p),
+        ("seg_cent", C.c_void_p), ("n_evicted", C.c_int32),
+        ("n_forced", C.c_int32),
+    ]
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            L = C.CDLL(build())
+            vp, i32, i64, u64 = C.c_void_p, C.c_int32, C.c_int64, C.c_uint64
+            L.lkvo_init_indices.argtypes = [i64, i32, u64, vp]
+            L.lkvo_init_indices.restype = C.c_int
+            L.lkvo_splitmix64.argtypes = [u64, i32, vp]
+            L.lkvo_sqdist.argtypes = [vp, C.c_int, vp, i32]
+            L.lkvo_sqdist.restype = C.c_double
+            L.lkvo_assign.argtypes = [vp, C.c_int, i64, i32, vp, i32, vp, vp]
+            L.lkvo_update.argtypes = [vp, C.c_int, i64, i32, vp, i32, vp, vp, vp]
+            L.lkvo_operand.argtypes = [vp, i64, C.c_int, vp]
+            L.lkvo_objective.argtypes = [vp, C.c_int, i64, i32, vp, vp]
+            L.lkvo_objective.restype = C.c_double
+            L.lkvo_kmeans.argtypes = [vp, C.c_int, i64, i32, i32, i32, u64, vp, vp,
+                                      vp, vp, vp, vp]
+            L.lkvo_kmeans.restype = C.c_int
+            L.lkvo_boundary_r32.argtypes = [vp, vp, C.c_int, i32, i32]
+            L.lkvo_boundary_r32.restype = C.c_float
+            L.lkvo_boundary_r64.argtypes = [vp, vp, C.c_int, i32, i32]
+            L.lkvo_boundary_r64.restype = C.c_double
+            L.lkvo_group_scores.argtypes = [vp, C.c_int, i32, i32, vp, i32, vp]
+            L.lkvo_select.argtypes = [vp, vp, i32, i32, vp, vp]
+            L.lkvo_select.restype = i32
+            L.lkvo_attention.argtypes = [vp, C.c_int, i32, i32, vp, vp, i64, vp]
+            L.lkvo_decode.argtypes = [C.POINTER(DecodeArgs), C.POINTER(DecodeResult)]
+            L.lkvo_decode.restype = C.c_int
+            L.lkvo_f32_to_bf16.argtypes = [C.c_float]
+            L.lkvo_f32_to_bf16.restype = C.c_uint16
+            _lib = L
+    return _lib
+
+
+# ---------------------------------------------------------------- helpers
+
+def _arr(x, dtype):
+    return np.ascontiguousarray(x, dtype=dtype)
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data
+
+
+def dtype_of(a: np.ndarray) -> int:
+    if a.dtype == np.uint16:
+        return BF16
+    if a.dtype == np.float32:
+        return FP32
+    raise TypeError(f"oracle takes uint16 (bf16 bits) or float32, got {a.dtype}")
+
+
+def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    return (np.asarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round-to-nearest-even float32 -> bf16 bit patterns (same rule as the C)."""
+    u = np.ascontiguousarray(x, np.float32).view(np.uint32).astype(np.uint64)
+    nan = (u & 0x7FFFFFFF) > 0x7F800000
+    r = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+    r[nan] = ((u[nan] >> 16) | 0x40).astype(np.uint16)
+    return r
+
+
+def splitmix64(seed: int, count: int) -> np.ndarray:
+    out = np.zeros(count, np.uint64)
+    lib().lkvo_splitmix64(seed, count, _p(out))
+    return out
+
+
+def init_indices(n: int, c: int, seed: int) -> np.ndarray:
+    idx = np.zeros(c, np.int64)
+    if lib().lkvo_init_indices(n, c, seed, _p(idx)) != 0:
+        raise ValueError("bad init arguments")
+    return idx
+
+
+def operand(cent: np.ndarray, dtype: int) -> np.ndarray:
+    cent = _arr(cent, np.float32)
+    out = np.empty_like(cent)
+    lib().lkvo_operand(_p(cent), cent.size, dtype, _p(out))
+    return out
+
+
+def sqdist(key: np.ndarray, cent_row: np.ndarray) -> float:
+    key = np.ascontiguousarray(key)
+    c = _arr(cent_row, np.float32)
+    return lib().lkvo_sqdist(_p(key), dtype_of(key), _p(c), key.shape[-1])
+
+
+def assign(keys: np.ndarray, cent_op: np.ndarray, with_gap: bool = False):
+    keys = np.ascontiguousarray(keys)
+    cent_op = _arr(cent_op, np.float32)
+    n, d = keys.shape
+    a = np.zeros(n, np.int32)
+    gap = np.zeros(n, np.float64) if with_gap else None
+    lib().lkvo_assign(_p(keys), dtype_of(keys), n, d, _p(cent_op), cent_op.shape[0],
+                      _p(a), _p(gap))
+    return (a, gap) if with_gap else a
+
+
+def update(keys: np.ndarray, assign_: np.ndarray, cent: np.ndarray):
+    keys = np.ascontiguousarray(keys)
+    n, d = keys.shape
+    cent = _arr(cent, np.float32).copy()
+    a = _arr(assign_, np.int32)
+    cnt = np.zeros(cent.shape[0], np.int32)
+    inexact = C.c_int64(0)
+    lib().lkvo_update(_p(keys), dtype_of(keys), n, d, _p(a), cent.shape[0], _p(cent),
+                      _p(cnt), C.addressof(inexact))
+    return cent, cnt, inexact.value
+
+
+def objective(keys: np.ndarray, cent_op: np.ndarray, assign_: np.ndarray) -> float:
+    keys = np.ascontiguousarray(keys)
+    n, d = keys.shape
+    return lib().lkvo_objective(_p(keys), dtype_of(keys), n, d,
+                                _p(_arr(cent_op, np.float32)), _p(_arr(assign_, np.int32)))
+
+
+def kmeans(keys: np.ndarray, c: int, iters: int, seed: int, trace: bool = False):
+    """Returns dict(cent [c,d] fp32, assign [n], count [c], inexact, and with
+    trace: trace_cent [iters+1,c,d], trace_assign [iters,n])."""
+    keys = np.ascontiguousarray(keys)
+    n, d = keys.shape
+    cent = np.zeros((c, d), np.float32)
+    a = np.zeros(n, np.int32)
+    cnt = np.zeros(c, np.int32)
+    tc = np.zeros((iters + 1, c, d), np.float32) if trace else None
+    ta = np.zeros((iters, n), np.int32) if trace else None
+    inexact = C.c_int64(0)
+    rc = lib().lkvo_kmeans(_p(keys), dtype_of(keys), n, d, c, iters, seed, _p(cent),
+                           _p(a), _p(cnt), _p(tc), _p(ta), C.addressof(inexact))
+    if rc != 0:
+        raise ValueError("bad k-means arguments")
+    out = dict(cent=cent, assign=a, count=cnt, inexact=inexact.value)
+    if trace:
+        out.update(trace_cent=tc, trace_assign=ta)
+    return out
+
+
+def boundary_r(q_prev: np.ndarray, q_cur: np.ndarray):
+    """(r32 decision value, r64) for q of shape [H, d]."""
+    qp, qc = np.ascontiguousarray(q_prev), np.ascontiguousarray(q_cur)
+    h, d = qc.shape
+    dt = dtype_of(qc)
+    L = lib()
+    return (L.lkvo_boundary_r32(_p(qp), _p(qc), dt, h, d),
+            L.lkvo_boundary_r64(_p(qp), _p(qc), dt, h, d))
+
+
+def group_scores(q_group: np.ndarray, cent_op: np.ndarray) -> np.ndarray:
+    q = np.ascontiguousarray(q_group)
+    g, d = q.shape
+    cent_op = _arr(cent_op, np.float32)
+    s = np.zeros(cent_op.shape[0], np.float32)
+    lib().lkvo_group_scores(_p(q), dtype_of(q), g, d, _p(cent_op), cent_op.shape[0], _p(s))
+    return s
+
+
+def select(scores: np.ndarray, lens: np.ndarray, budget: int):
+    s = _arr(scores, np.float32)
+    ln = _arr(lens, np.int32)
+    sel = np.zeros(max(1, s.size), np.int32)
+    ntok = C.c_int32(0)
+    k = lib().lkvo_select(_p(s), _p(ln), s.size, budget, _p(sel), C.addressof(ntok))
+    return sel[:k].copy(), ntok.value
+
+
+def attention(q_group: np.ndarray, k_rows: np.ndarray, v_rows: np.ndarray) -> np.ndarray:
+    q = np.ascontiguousarray(q_group)
+    k, v = np.ascontiguousarray(k_rows), np.ascontiguousarray(v_rows)
+    g, d = q.shape
+    out = np.zeros((g, d), np.float64)
+    lib().lkvo_attention(_p(q), dtype_of(q), g, d, _p(k), _p(v), k.shape[0], _p(out))
+    return out
+
+
+def decode(keys, values, assign_, cent, q, k_new, v_new, *, n_clusters, local_buf,
+           tau, budget, attn_mask=None, want_seg_cent=False):
+    """Run one (sequence, layer) decode through the oracle.
+
+    keys/values [H_kv, N, d]; assign_ [H_kv, N]; cent [H_kv, C, d] fp32;
+    q [T, H, d]; k_new/v_new [T, H_kv, d]. Returns a dict of numpy arrays.
+    """
+    keys, values = np.ascontiguousarray(keys), np.ascontiguousarray(values)
+    q, k_new, v_new = (np.ascontiguousarray(x) for x in (q, k_new, v_new))
+    assign_ = _arr(assign_, np.int32)
+    cent = _arr(cent, np.float32)
+    hkv, n, d = keys.shape
+    T, h_all, _ = q.shape
+    g = h_all // hkv
+    dt = dtype_of(q)
+    c = n_clusters
+    ucap = c + T
+    mask = None if attn_mask is None else _arr(attn_mask, np.uint8)
+    args = DecodeArgs(dt, hkv, g, d, n, c, local_buf, T, tau, budget, _p(keys), _p(values),
+                      _p(assign_), _p(cent), _p(q), _p(k_new), _p(v_new), _p(mask))
+    res = dict(
+        out=np.zeros((T, h_all, d), np.float64), flag=np.zeros(T, np.uint8),
+        r32=np.zeros(T, np.float32), r64=np.zeros(T, np.float64),
+        n_sel=np.zeros((T, hkv), np.int32), n_tok=np.zeros((T, hkv), np.int32),
+        sel=np.full((T, hkv, ucap), -1, np.int32), win_start=np.zeros(T, np.int32),
+        n_units=np.zeros(T, np.int32), seg_start=np.zeros(max(T, 1), np.int32),
+        seg_len=np.zeros(max(T, 1), np.int32),
+        seg_cent=np.zeros((max(T, 1), hkv, d), np.float32) if want_seg_cent else None)
+    r = DecodeResult(ucap, max(T, 1), *(_p(res[k]) for k in (
+        "out", "flag", "r32", "r64", "n_sel", "n_tok", "sel", "win_start", "n_units",
+        "seg_start", "seg_len", "seg_cent")), 0, 0)
+    if lib().lkvo_decode(C.byref(args), C.byref(r)) != 0:
+        raise ValueError("oracle decode rejected its arguments")
+    ne = r.n_evicted
+    res["n_evicted"], res["n_forced"] = ne, r.n_forced
+    res["seg_start"], res["seg_len"] = res["seg_start"][:ne], res["seg_len"][:ne]
+    if want_seg_cent:
+        res["seg_cent"] = res["seg_cent"][:ne]
+    return res

@@ -1,0 +1,511 @@
+/*
+ * lkv_oracle.c -- plain, slow, single-threaded CPU oracle (test infrastructure
+ * only; see lkv_oracle.h for the sources, the precision rules and the build
+ * flags). Every loop runs in the order the definition states; there is no
+ * blocking, fusion or reordering.
+ */
+#include "lkv_oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------------ */
+/* element access                                                            */
+
+float lkvo_bf16_to_f32(uint16_t b) {
+  uint32_t u = (uint32_t)b << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return f;
+}
+
+uint16_t lkvo_f32_to_bf16(float f) {
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  if ((u & 0x7fffffffu) > 0x7f800000u) return (uint16_t)((u >> 16) | 0x40u);
+  u += 0x7fffu + ((u >> 16) & 1u); /* round to nearest, ties to even */
+  return (uint16_t)(u >> 16);
+}
+
+static float elem(const void *p, int dtype, int64_t i) {
+  if (dtype == LKVO_BF16) return lkvo_bf16_to_f32(((const uint16_t *)p)[i]);
+  return ((const float *)p)[i];
+}
+
+static size_t elem_size(int dtype) { return dtype == LKVO_BF16 ? 2u : 4u; }
+
+static const void *row_ptr(const void *base, int dtype, int64_t row, int32_t d) {
+  return (const char *)base + (size_t)row * (size_t)d * elem_size(dtype);
+}
+
+/* ------------------------------------------------------------------------ */
+/* seeded initialisation                                                     */
+
+/* splitmix64 (Steele, Lea and Flood, "Fast splittable pseudorandom number
+ * generators", OOPSLA 2014; constants as in Vigna's public-domain
+ * splitmix64.c): state += golden gamma, then the variant-13 mix. */
+static uint64_t splitmix64_next(uint64_t *state) {
+  uint64_t z = (*state += 0x9e3779b97f4a7c15ull);
+  z = (z ^ (z >> 30)) * 0xbf58476d1ce4e5b9ull;
+  z = (z ^ (z >> 27)) * 0x94d049bb133111ebull;
+  return z ^ (z >> 31);
+}
+
+void lkvo_splitmix64(uint64_t seed, int32_t count, uint64_t *out) {
+  uint64_t st = seed;
+  for (int32_t i = 0; i < count; ++i) out[i] = splitmix64_next(&st);
+}
+
+int lkvo_init_indices(int64_t n, int32_t c, uint64_t seed, int64_t *idx_out) {
+  if (c < 1 || (int64_t)c > n) return -1;
+  int64_t *perm = (int64_t *)malloc((size_t)n * sizeof *perm);
+  if (!perm) return -1;
+  for (int64_t i = 0; i < n; ++i) perm[i] = i;
+  uint64_t st = seed;
+  for (int32_t i = 0; i < c; ++i) {
+    uint64_t r = splitmix64_next(&st);
+    int64_t j = (int64_t)i + (int64_t)(r % (uint64_t)(n - i));
+    int64_t t = perm[i];
+    perm[i] = perm[j];
+    perm[j] = t;
+    idx_out[i] = perm[i];
+  }
+  free(perm);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* K-means [LouisKV notes, 关键设计 2: K-means over the prefill keys, centroid  */
+/* = mean of the cluster's keys, used as the retrieval index]                */
+
+double lkvo_sqdist(const void *key, int dtype, const float *cent, int32_t d) {
+  double acc = 0.0;
+  for (int32_t j = 0; j < d; ++j) {
+    double diff = (double)elem(key, dtype, j) - (double)cent[j];
+    double sq = diff * diff;
+    acc = acc + sq;
+  }
+  return acc;
+}
+
+void lkvo_assign(const void *keys, int dtype, int64_t n, int32_t d,
+                 const float *cent, int32_t c, int32_t *assign_out,
+                 double *gap_out) {
+  for (int64_t i = 0; i < n; ++i) {
+    const void *k = row_ptr(keys, dtype, i, d);
+    int32_t best = 0;
+    double d1 = lkvo_sqdist(k, dtype, cent, d);
+    double d2 = INFINITY;
+    for (int32_t j = 1; j < c; ++j) {
+      double dj = lkvo_sqdist(k, dtype, cent + (size_t)j * d, d);
+      if (dj < d1) {
+        d2 = d1;
+        d1 = dj;
+        best = j;
+      } else if (dj < d2) {
+        d2 = dj;
+      }
+    }
+    assign_out[i] = best;
+    if (gap_out) {
+      double kk = 0.0, cc = 0.0;
+      for (int32_t j = 0; j < d; ++j) {
+        double kv = elem(k, dtype, j), cv = cent[(size_t)best * d + j];
+        kk += kv * kv;
+        cc += cv * cv;
+      }
+      gap_out[i] = (c > 1) ? (d2 - d1) / (kk + cc) : INFINITY;
+    }
+  }
+}
+
+void lkvo_update(const void *keys, int dtype, int64_t n, int32_t d,
+                 const int32_t *assign, int32_t c, float *cent,
+                 int32_t *count_out, int64_t *inexact_out) {
+  double *sum = (double *)calloc((size_t)c * d, sizeof *sum);
+  int64_t inexact = 0;
+  for (int32_t j = 0; j < c; ++j) count_out[j] = 0;
+  /* token order: each cluster's members are added in increasing token index */
+  for (int64_t i = 0; i < n; ++i) {
+    int32_t j = assign[i];
+    count_out[j] += 1;
+    const void *k = row_ptr(keys, dtype, i, d);
+    for (int32_t t = 0; t < d; ++t) {
+      double a = sum[(size_t)j * d + t], b = (double)elem(k, dtype, t);
+      double s = a + b;
+      /* two-sum error term: nonzero iff the addition rounded */
+      double bb = s - a;
+      double err = (a - (s - bb)) + (b - bb);
+      if (err != 0.0) ++inexact;
+      sum[(size_t)j * d + t] = s;
+    }
+  }
+  for (int32_t j = 0; j < c; ++j) {
+    if (count_out[j] == 0) continue; /* empty cluster keeps its centroid */
+    for (int32_t t = 0; t < d; ++t)
+      cent[(size_t)j * d + t] =
+          (float)(sum[(size_t)j * d + t] / (double)count_out[j]);
+  }
+  free(sum);
+  if (inexact_out) *inexact_out += inexact;
+}
+
+void lkvo_operand(const float *cent, int64_t count, int dtype, float *out) {
+  for (int64_t i = 0; i < count; ++i)
+    out[i] = (dtype == LKVO_BF16) ? lkvo_bf16_to_f32(lkvo_f32_to_bf16(cent[i]))
+                                  : cent[i];
+}
+
+double lkvo_objective(const void *keys, int dtype, int64_t n, int32_t d,
+                      const float *cent, const int32_t *assign) {
+  double j = 0.0;
+  for (int64_t i = 0; i < n; ++i)
+    j += lkvo_sqdist(row_ptr(keys, dtype, i, d), dtype,
+                     cent + (size_t)assign[i] * d, d);
+  return j;
+}
+
+int lkvo_kmeans(const void *keys, int dtype, int64_t n, int32_t d, int32_t c,
+                int32_t iters, uint64_t seed, float *cent_out,
+                int32_t *assign_out, int32_t *count_out, float *trace_cent,
+                int32_t *trace_assign, int64_t *inexact_out) {
+  if (iters < 1 || c < 1 || (int64_t)c > n || d < 1) return -1;
+  int64_t *idx = (int64_t *)malloc((size_t)c * sizeof *idx);
+  float *op = (float *)malloc((size_t)c * d * sizeof *op);
+  if (!idx || !op) {
+    free(idx);
+    free(op);
+    return -1;
+  }
+  lkvo_init_indices(n, c, seed, idx);
+  for (int32_t j = 0; j < c; ++j)
+    for (int32_t t = 0; t < d; ++t)
+      cent_out[(size_t)j * d + t] = elem(keys, dtype, idx[j] * d + t);
+  if (inexact_out) *inexact_out = 0;
+  if (trace_cent) memcpy(trace_cent, cent_out, (size_t)c * d * sizeof(float));
+  for (int32_t it = 0; it < iters; ++it) {
+    lkvo_operand(cent_out, (int64_t)c * d, dtype, op);
+    lkvo_assign(keys, dtype, n, d, op, c, assign_out, NULL);
+    lkvo_update(keys, dtype, n, d, assign_out, c, cent_out, count_out,
+                inexact_out);
+    if (trace_assign)
+      memcpy(trace_assign + (size_t)it * n, assign_out, (size_t)n * sizeof(int32_t));
+    if (trace_cent)
+      memcpy(trace_cent + (size_t)(it + 1) * c * d, cent_out,
+             (size_t)c * d * sizeof(float));
+  }
+  free(idx);
+  free(op);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* semantic boundary [LouisKV notes, 关键设计 1]                              */
+
+float lkvo_boundary_r32(const void *q_prev, const void *q_cur, int dtype,
+                        int32_t h, int32_t d) {
+  float r = 0.0f;
+  for (int32_t head = 0; head < h; ++head) {
+    float dot = 0.0f, na = 0.0f, nb = 0.0f;
+    for (int32_t j = 0; j < d; ++j) {
+      float a = elem(q_prev, dtype, (int64_t)head * d + j);
+      float b = elem(q_cur, dtype, (int64_t)head * d + j);
+      dot = fmaf(a, b, dot);
+      na = fmaf(a, a, na);
+      nb = fmaf(b, b, nb);
+    }
+    float den = sqrtf(na) * sqrtf(nb);
+    float cs = (den > 0.0f) ? dot / den : 0.0f;
+    r = r + cs;
+  }
+  return r / (float)h;
+}
+
+double lkvo_boundary_r64(const void *q_prev, const void *q_cur, int dtype,
+                         int32_t h, int32_t d) {
+  double r = 0.0;
+  for (int32_t head = 0; head < h; ++head) {
+    double dot = 0.0, na = 0.0, nb = 0.0;
+    for (int32_t j = 0; j < d; ++j) {
+      double a = elem(q_prev, dtype, (int64_t)head * d + j);
+      double b = elem(q_cur, dtype, (int64_t)head * d + j);
+      dot += a * b;
+      na += a * a;
+      nb += b * b;
+    }
+    double den = sqrt(na) * sqrt(nb);
+    r += (den > 0.0) ? dot / den : 0.0;
+  }
+  return r / (double)h;
+}
+
+/* ------------------------------------------------------------------------ */
+/* group-consistent scoring and budgeted selection [LouisKV notes, 关键设计 3] */
+
+void lkvo_group_scores(const void *q, int dtype, int32_t g, int32_t d,
+                       const float *cent, int32_t u, float *scores_out) {
+  float *qbar = (float *)malloc((size_t)d * sizeof *qbar);
+  for (int32_t j = 0; j < d; ++j) {
+    float acc = elem(q, dtype, j);
+    for (int32_t h = 1; h < g; ++h) acc = acc + elem(q, dtype, (int64_t)h * d + j);
+    qbar[j] = acc;
+  }
+  for (int32_t k = 0; k < u; ++k) {
+    float s = 0.0f;
+    for (int32_t j = 0; j < d; ++j) s = fmaf(qbar[j], cent[(size_t)k * d + j], s);
+    scores_out[k] = s;
+  }
+  free(qbar);
+}
+
+/* (score descending, id ascending) */
+static int precedes(const float *s, int32_t a, int32_t b) {
+  if (s[a] != s[b]) return s[a] > s[b];
+  return a < b;
+}
+
+int32_t lkvo_select(const float *scores, const int32_t *len, int32_t u,
+                    int32_t budget, int32_t *sel_out, int32_t *n_tok_out) {
+  /* plain insertion sort of the ids by the selection order */
+  int32_t *order = (int32_t *)malloc((size_t)(u > 0 ? u : 1) * sizeof *order);
+  for (int32_t i = 0; i < u; ++i) {
+    int32_t x = i, p = i;
+    while (p > 0 && precedes(scores, x, order[p - 1])) {
+      order[p] = order[p - 1];
+      --p;
+    }
+    order[p] = x;
+  }
+  int32_t n_sel = 0, tok = 0;
+  for (int32_t i = 0; i < u; ++i) {
+    int32_t id = order[i];
+    if (tok + len[id] > budget) break; /* first unit that does not fit */
+    tok += len[id];
+    sel_out[n_sel++] = id;
+  }
+  free(order);
+  *n_tok_out = tok;
+  return n_sel;
+}
+
+/* ------------------------------------------------------------------------ */
+/* attention over the retrieved + local tokens [LouisKV notes, flowchart:     */
+/* Attention over retrieved or reused critical KV]                           */
+
+void lkvo_attention(const void *q, int dtype, int32_t g, int32_t d,
+                    const void *k_rows, const void *v_rows, int64_t n,
+                    double *out) {
+  double *logit = (double *)malloc((size_t)(n > 0 ? n : 1) * sizeof *logit);
+  double scale = 1.0 / sqrt((double)d);
+  for (int32_t h = 0; h < g; ++h) {
+    double m = -INFINITY;
+    for (int64_t i = 0; i < n; ++i) {
+      double dot = 0.0;
+      for (int32_t j = 0; j < d; ++j)
+        dot += (double)elem(q, dtype, (int64_t)h * d + j) *
+               (double)elem(k_rows, dtype, i * d + j);
+      logit[i] = dot * scale;
+      if (logit[i] > m) m = logit[i];
+    }
+    double z = 0.0;
+    for (int64_t i = 0; i < n; ++i) {
+      logit[i] = exp(logit[i] - m);
+      z += logit[i];
+    }
+    for (int32_t j = 0; j < d; ++j) {
+      double acc = 0.0;
+      for (int64_t i = 0; i < n; ++i)
+        acc += logit[i] * (double)elem(v_rows, dtype, i * d + j);
+      out[(size_t)h * d + j] = (n > 0) ? acc / z : 0.0;
+    }
+  }
+  free(logit);
+}
+
+/* ------------------------------------------------------------------------ */
+/* decode: boundary -> segment close -> append/evict -> retrieve -> attend   */
+
+int lkvo_decode(const lkvo_decode_args *a, lkvo_decode_result *r) {
+  const int dt = a->dtype;
+  const int32_t hkv = a->n_kv_heads, g = a->group, d = a->head_dim;
+  const int32_t h_all = hkv * g, c = a->n_clusters, L = a->local_buf;
+  const int32_t T = a->n_steps;
+  const int64_t n = a->n_prefill;
+  const size_t es = elem_size(dt);
+  if (hkv < 1 || g < 1 || d < 1 || c < 1 || L < 1 || T < 0 || n < 0) return -1;
+  const int32_t ucap = c + T; /* every eviction removes at least one token */
+
+  int rc = -1;
+  /* cluster membership in token order, per kv head */
+  int32_t *cnt = (int32_t *)calloc((size_t)hkv * c, sizeof *cnt);
+  int32_t *first = (int32_t *)malloc((size_t)hkv * (c + 1) * sizeof *first);
+  int64_t *member = (int64_t *)malloc((size_t)(hkv * n > 0 ? hkv * n : 1) * sizeof *member);
+  /* per kv head unit tables: operand centroid and length */
+  float *op = (float *)malloc((size_t)hkv * ucap * d * sizeof *op);
+  int32_t *ulen = (int32_t *)malloc((size_t)hkv * ucap * sizeof *ulen);
+  /* active selection per kv head */
+  int32_t *act = (int32_t *)malloc((size_t)hkv * ucap * sizeof *act);
+  int32_t *act_n = (int32_t *)calloc((size_t)hkv, sizeof *act_n);
+  int32_t *act_tok = (int32_t *)calloc((size_t)hkv, sizeof *act_tok);
+  /* closed, not yet evicted segments: FIFO of [start, end) */
+  int32_t *cl_s = (int32_t *)malloc((size_t)(T + 1) * sizeof *cl_s);
+  int32_t *cl_e = (int32_t *)malloc((size_t)(T + 1) * sizeof *cl_e);
+  float *scores = (float *)malloc((size_t)ucap * sizeof *scores);
+  float *segc = (float *)malloc((size_t)hkv * d * sizeof *segc);
+  double *segsum = (double *)malloc((size_t)d * sizeof *segsum);
+  char *kg = (char *)malloc((size_t)(n + T + 1) * d * es);
+  char *vg = (char *)malloc((size_t)(n + T + 1) * d * es);
+  if (!cnt || !first || !member || !op || !ulen || !act || !act_n ||
+      !act_tok || !cl_s || !cl_e || !scores || !segc || !segsum || !kg || !vg)
+    goto done;
+
+  for (int32_t kh = 0; kh < hkv; ++kh) {
+    const int32_t *as = a->assign + (size_t)kh * n;
+    int32_t *ct = cnt + (size_t)kh * c;
+    int32_t *fs = first + (size_t)kh * (c + 1);
+    for (int64_t i = 0; i < n; ++i) {
+      if (as[i] < 0 || as[i] >= c) goto done;
+      ct[as[i]] += 1;
+    }
+    fs[0] = 0;
+    for (int32_t j = 0; j < c; ++j) fs[j + 1] = fs[j] + ct[j];
+    int32_t *fill = (int32_t *)calloc((size_t)c, sizeof *fill);
+    if (!fill) goto done;
+    for (int64_t i = 0; i < n; ++i) {
+      int32_t j = as[i];
+      member[(size_t)kh * n + fs[j] + fill[j]++] = i;
+    }
+    free(fill);
+    lkvo_operand(a->cent + (size_t)kh * c * d, (int64_t)c * d, dt,
+                 op + (size_t)kh * ucap * d);
+    for (int32_t j = 0; j < c; ++j) ulen[(size_t)kh * ucap + j] = ct[j];
+  }
+
+  int32_t n_units = c, n_ev = 0, n_forced = 0;
+  int32_t win_start = 0, open_start = 0, cl_head = 0, cl_tail = 0;
+
+  for (int32_t t = 0; t < T; ++t) {
+    const void *qt = row_ptr(a->q, dt, (int64_t)t * h_all, d);
+    /* 1. boundary test */
+    int flag = 1;
+    float r32 = 0.0f;
+    double r64 = 0.0;
+    if (t > 0) {
+      const void *qp = row_ptr(a->q, dt, (int64_t)(t - 1) * h_all, d);
+      r32 = lkvo_boundary_r32(qp, qt, dt, h_all, d);
+      r64 = lkvo_boundary_r64(qp, qt, dt, h_all, d);
+      flag = r32 < a->tau;
+    }
+    /* 2. a boundary closes the open segment; token t starts the next one */
+    if (flag && t > 0 && open_start < t) {
+      cl_s[cl_tail] = open_start;
+      cl_e[cl_tail] = t;
+      ++cl_tail;
+      open_start = t;
+    }
+    /* 3. make room for token t: evict whole segments, oldest first; with no
+     *    closed segment left, cut the open one */
+    while ((t - win_start) + 1 > L) {
+      int32_t s0, s1;
+      if (cl_head < cl_tail) {
+        s0 = cl_s[cl_head];
+        s1 = cl_e[cl_head];
+        ++cl_head;
+      } else {
+        s0 = open_start;
+        s1 = t;
+        open_start = t;
+        ++n_forced;
+      }
+      if (n_ev >= r->max_segs) goto done;
+      for (int32_t kh = 0; kh < hkv; ++kh) {
+        for (int32_t j = 0; j < d; ++j) segsum[j] = 0.0;
+        for (int32_t tt = s0; tt < s1; ++tt)
+          for (int32_t j = 0; j < d; ++j)
+            segsum[j] = segsum[j] +
+                        (double)elem(a->k_new, dt, ((int64_t)tt * hkv + kh) * d + j);
+        for (int32_t j = 0; j < d; ++j)
+          segc[(size_t)kh * d + j] = (float)(segsum[j] / (double)(s1 - s0));
+        lkvo_operand(segc + (size_t)kh * d, d, dt,
+                     op + ((size_t)kh * ucap + n_units) * d);
+        ulen[(size_t)kh * ucap + n_units] = s1 - s0;
+      }
+      r->seg_start[n_ev] = s0;
+      r->seg_len[n_ev] = s1 - s0;
+      if (r->seg_cent)
+        memcpy(r->seg_cent + (size_t)n_ev * hkv * d, segc,
+               (size_t)hkv * d * sizeof(float));
+      ++n_ev;
+      ++n_units;
+      win_start = s1;
+    }
+    /* 4. token t enters the local buffer [win_start, t] */
+    /* 5. retrieval on a boundary step, against the pool after evictions */
+    if (flag) {
+      for (int32_t kh = 0; kh < hkv; ++kh) {
+        const void *qg = row_ptr(a->q, dt, (int64_t)t * h_all + (int64_t)kh * g, d);
+        lkvo_group_scores(qg, dt, g, d, op + (size_t)kh * ucap * d, n_units, scores);
+        act_n[kh] = lkvo_select(scores, ulen + (size_t)kh * ucap, n_units,
+                                a->budget, act + (size_t)kh * ucap, &act_tok[kh]);
+      }
+    }
+    /* 6. attention of each query head over its group's selection + buffer */
+    if (!a->attn_mask || a->attn_mask[t]) {
+      for (int32_t kh = 0; kh < hkv; ++kh) {
+        int64_t m = 0;
+        for (int32_t s = 0; s < act_n[kh]; ++s) {
+          int32_t u = act[(size_t)kh * ucap + s];
+          if (u < c) {
+            const int32_t *fs = first + (size_t)kh * (c + 1);
+            for (int32_t p = fs[u]; p < fs[u + 1]; ++p) {
+              int64_t i = member[(size_t)kh * n + p];
+              memcpy(kg + m * d * es, row_ptr(a->keys, dt, (int64_t)kh * n + i, d), d * es);
+              memcpy(vg + m * d * es, row_ptr(a->values, dt, (int64_t)kh * n + i, d), d * es);
+              ++m;
+            }
+          } else {
+            int32_t e = u - c;
+            for (int32_t tt = r->seg_start[e]; tt < r->seg_start[e] + r->seg_len[e]; ++tt) {
+              memcpy(kg + m * d * es, row_ptr(a->k_new, dt, (int64_t)tt * hkv + kh, d), d * es);
+              memcpy(vg + m * d * es, row_ptr(a->v_new, dt, (int64_t)tt * hkv + kh, d), d * es);
+              ++m;
+            }
+          }
+        }
+        for (int32_t tt = win_start; tt <= t; ++tt) {
+          memcpy(kg + m * d * es, row_ptr(a->k_new, dt, (int64_t)tt * hkv + kh, d), d * es);
+          memcpy(vg + m * d * es, row_ptr(a->v_new, dt, (int64_t)tt * hkv + kh, d), d * es);
+          ++m;
+        }
+        const void *qg = row_ptr(a->q, dt, (int64_t)t * h_all + (int64_t)kh * g, d);
+        lkvo_attention(qg, dt, g, d, kg, vg, m,
+                       r->out + ((size_t)t * h_all + (size_t)kh * g) * d);
+      }
+    }
+    /* per-step record */
+    if (r->flag) r->flag[t] = (uint8_t)flag;
+    if (r->r32) r->r32[t] = r32;
+    if (r->r64) r->r64[t] = r64;
+    if (r->win_start) r->win_start[t] = win_start;
+    if (r->n_units) r->n_units[t] = n_units;
+    for (int32_t kh = 0; kh < hkv; ++kh) {
+      if (r->n_sel) r->n_sel[(size_t)t * hkv + kh] = act_n[kh];
+      if (r->n_tok) r->n_tok[(size_t)t * hkv + kh] = act_tok[kh];
+      if (r->sel) {
+        if (act_n[kh] > r->max_sel) goto done;
+        memcpy(r->sel + ((size_t)t * hkv + kh) * r->max_sel, act + (size_t)kh * ucap,
+               (size_t)act_n[kh] * sizeof(int32_t));
+      }
+    }
+  }
+  r->n_evicted = n_ev;
+  r->n_forced = n_forced;
+  rc = 0;
+
+done:
+  free(cnt); free(first); free(member); free(op); free(ulen); free(act);
+  free(act_n); free(act_tok); free(cl_s); free(cl_e); free(scores);
+  free(segc); free(segsum); free(kg); free(vg);
+  return rc;
+}

@@ -1,0 +1,446 @@
+"""Pins of the CPU oracle against facts fixed outside the oracle itself:
+published generator outputs, closed forms, textbook properties of Lloyd's
+K-means and softmax attention, brute force on tiny inputs, and the FullCache
+special case (every step retrieves with a budget covering every token, so the
+sparse attention must equal full attention). No GPU needed."""
+import itertools
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+rng = np.random.default_rng(12345)
+
+
+def bf16(x):
+    return oracle.f32_to_bf16_bits(np.asarray(x, np.float32))
+
+
+def unbf16(b):
+    return oracle.bf16_bits_to_f32(b)
+
+
+# ------------------------------------------------------------------ splitmix64
+
+def test_splitmix64_published_vectors():
+    with open(os.path.join(GOLDEN, "splitmix64.txt")) as f:
+        lines = [l for l in f if l.strip() and not l.startswith("#")]
+    assert len(lines) == 2
+    for line in lines:
+        seed_s, outs = line.split(":")
+        seed = int(seed_s, 0)
+        want = [int(x, 0) for x in outs.split()]
+        got = [int(x) for x in oracle.splitmix64(seed, len(want))]
+        assert got == want
+
+
+def test_init_indices_distinct_and_full_shuffle_is_permutation():
+    for n, c, seed in [(10, 10, 7), (2048, 32, 1), (5, 1, 99), (131072, 8192, 3)]:
+        idx = oracle.init_indices(n, c, seed)
+        assert idx.min() >= 0 and idx.max() < n
+        assert len(set(idx.tolist())) == c
+    full = oracle.init_indices(1000, 1000, 5)
+    assert sorted(full.tolist()) == list(range(1000))
+    with pytest.raises(ValueError):
+        oracle.init_indices(4, 5, 1)
+
+
+def test_init_indices_first_draw_matches_generator():
+    # the first index is (first splitmix64 output) mod n
+    for seed in (1, 2, 0xDEADBEEF):
+        first = int(oracle.splitmix64(seed, 1)[0])
+        assert oracle.init_indices(1000, 3, seed)[0] == first % 1000
+
+
+# ------------------------------------------------------------------ bf16
+
+def test_bf16_rounding_matches_torch():
+    import torch
+    x = np.concatenate([rng.standard_normal(10000).astype(np.float32),
+                        np.array([0.0, -0.0, 1.0, 65504.0, 1e-30, 3.4e38, -2.5e-8],
+                                 np.float32)])
+    want = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(bf16(x), want)
+    # ties to even: 1 + 2^-8 is halfway between two bf16 values
+    assert unbf16(bf16(np.float32(1.0 + 2 ** -8)))[()] == 1.0
+    assert unbf16(bf16(np.float32(1.0 + 3 * 2 ** -8)))[()] == 1.0 + 2 ** -6
+
+
+# ------------------------------------------------------------------ K-means
+
+def test_sqdist_closed_form():
+    k = np.zeros(128, np.float32); k[0] = 3
+    c = np.zeros(128, np.float32); c[1] = 4
+    assert oracle.sqdist(k, c) == 25.0
+    kb = bf16(k)
+    assert oracle.sqdist(kb, c) == 25.0
+
+
+def test_assign_brute_force_and_ties():
+    d = 8
+    keys = rng.standard_normal((50, d)).astype(np.float32)
+    cent = rng.standard_normal((7, d)).astype(np.float32)
+    a = oracle.assign(keys, cent)
+    dist = ((keys[:, None, :].astype(np.float64) - cent[None].astype(np.float64)) ** 2).sum(-1)
+    assert np.array_equal(a, dist.argmin(1))
+    # exact tie between centroid 0 and 1 -> lowest id; 2 and 3 -> 2
+    k = np.zeros((2, d), np.float32)
+    k[1, 0] = 10
+    c = np.zeros((4, d), np.float32)
+    c[0, 1], c[1, 1] = 1, -1
+    c[2, 0], c[3, 0] = 11, 11
+    c[2, 2], c[3, 2] = 1, -1
+    assert oracle.assign(k, c).tolist() == [0, 2]
+
+
+def test_update_is_member_mean_and_empty_keeps_centroid():
+    d = 16
+    keys = rng.standard_normal((200, d)).astype(np.float32)
+    a = rng.integers(0, 5, 200).astype(np.int32)
+    a[a == 3] = 4  # cluster 3 empty
+    old = rng.standard_normal((5, d)).astype(np.float32)
+    cent, cnt, inexact = oracle.update(keys, a, old)
+    for j in range(5):
+        m = a == j
+        assert cnt[j] == m.sum()
+        if m.any():
+            want = keys[m].astype(np.float64).mean(0)
+            assert np.allclose(cent[j], want, atol=1e-6, rtol=0)
+        else:
+            assert np.array_equal(cent[j], old[j])
+    # bf16 keys: member sums are exact in double, so the centroid is the
+    # correctly rounded mean of the exact sum
+    kb = bf16(keys)
+    centb, _, inexact_b = oracle.update(kb, a, old)
+    assert inexact_b == 0
+    kf = unbf16(kb).astype(np.float64)
+    for j in (0, 1, 2, 4):
+        want = (kf[a == j].sum(0) / (a == j).sum()).astype(np.float32)
+        assert np.array_equal(centb[j], want)
+
+
+def test_well_separated_mixture_recovers_partition():
+    # textbook case: components far apart, one initial centroid per component
+    # -> one Lloyd round returns the generating partition and its means
+    d, C, per = 32, 6, 40
+    means = np.zeros((C, d), np.float32)
+    for j in range(C):
+        means[j, j] = 100.0
+    lab = np.repeat(np.arange(C), per)
+    rng.shuffle(lab)
+    keys = (means[lab] + rng.standard_normal((C * per, d)).astype(np.float32)).astype(np.float32)
+    init = np.stack([keys[np.flatnonzero(lab == j)[0]] for j in range(C)])
+    a = oracle.assign(keys, init)
+    assert np.array_equal(a, lab)
+    cent, cnt, _ = oracle.update(keys, a, init)
+    assert np.array_equal(cnt, np.full(C, per))
+    for j in range(C):
+        assert np.allclose(cent[j], keys[lab == j].astype(np.float64).mean(0), atol=1e-5)
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+def test_kmeans_objective_monotone_and_composition(dtype):
+    n, d, c, iters = 600, 16, 12, 8
+    keys = (rng.standard_normal((c, d))[rng.integers(0, c, n)] * 1.0
+            + 0.4 * rng.standard_normal((n, d))).astype(np.float32)
+    if dtype == "bf16":
+        keys = bf16(keys)
+    dt = oracle.dtype_of(keys)
+    r = oracle.kmeans(keys, c, iters, seed=11, trace=True)
+    tc, ta = r["trace_cent"], r["trace_assign"]
+    # the run is init + (assign with operand, update) repeated
+    idx = oracle.init_indices(n, c, 11)
+    kf = unbf16(keys) if dtype == "bf16" else keys
+    assert np.array_equal(tc[0], kf[idx])
+    cent = tc[0].copy()
+    for it in range(iters):
+        op = oracle.operand(cent, dt)
+        a = oracle.assign(keys, op)
+        assert np.array_equal(a, ta[it])
+        cent, cnt, _ = oracle.update(keys, a, cent)
+        assert np.array_equal(cent, tc[it + 1])
+    assert np.array_equal(r["assign"], ta[-1]) and np.array_equal(r["cent"], tc[-1])
+    # argmin step can only lower J for fixed centroids; mean step can only lower
+    # J for a fixed assignment (exact for the unrounded centroid up to the
+    # float rounding of the mean)
+    for it in range(1, iters):
+        op = oracle.operand(tc[it], dt)
+        j_new = oracle.objective(keys, op, ta[it])
+        j_old = oracle.objective(keys, op, ta[it - 1])
+        assert j_new <= j_old
+        j_mean = oracle.objective(keys, tc[it + 1], ta[it])
+        j_prev = oracle.objective(keys, tc[it], ta[it])
+        assert j_mean <= j_prev * (1 + 1e-9)
+    # end-to-end objective (with operand centroids) non-increasing
+    js = [oracle.objective(keys, oracle.operand(tc[it + 1], dt), ta[it]) for it in range(iters)]
+    tol = 1e-9 if dtype == "fp32" else 1e-3
+    for a_, b_ in zip(js, js[1:]):
+        assert b_ <= a_ * (1 + tol)
+
+
+def test_kmeans_centroids_are_member_means():
+    n, d, c = 500, 128, 20
+    keys = bf16(rng.standard_normal((n, d)))
+    r = oracle.kmeans(keys, c, 5, seed=3)
+    kf = unbf16(keys).astype(np.float64)
+    for j in range(c):
+        m = r["assign"] == j
+        assert r["count"][j] == m.sum()
+        if m.any():
+            assert np.array_equal(r["cent"][j], (kf[m].sum(0) / m.sum()).astype(np.float32))
+
+
+# ------------------------------------------------------------------ boundary
+
+def _boundary_case(rel, h, d=128):
+    qp = rng.standard_normal((h, d)).astype(np.float32)
+    qc = np.empty_like(qp)
+    for i, r in enumerate(rel):
+        if r == "same":
+            qc[i] = qp[i]
+        elif r == "neg":
+            qc[i] = -qp[i]
+        elif r == "scaled":
+            qc[i] = 3 * qp[i]
+        elif r == "orth":
+            # exactly orthogonal in float arithmetic: disjoint supports
+            qp[i, d // 2:] = 0
+            qc[i] = 0
+            qc[i, d // 2:] = rng.standard_normal(d - d // 2)
+    return qp, qc
+
+
+def test_boundary_golden_cases():
+    with open(os.path.join(GOLDEN, "boundary_cases.txt")) as f:
+        rows = [l for l in f if l.strip() and not l.startswith("#")]
+    assert len(rows) >= 7
+    for row in rows:
+        name, h, rel, want, tau, trig = (x.strip() for x in row.split("|"))
+        qp, qc = _boundary_case(rel.split(), int(h))
+        r32, r64 = oracle.boundary_r(qp, qc)
+        assert abs(r32 - float(want)) <= 2e-7, name
+        assert abs(r64 - float(want)) <= 1e-12, name
+        assert int(r32 < float(tau)) == int(trig), name
+
+
+def test_boundary_matches_mean_cosine_and_is_head_symmetric():
+    for dtype in ("fp32", "bf16"):
+        qp = rng.standard_normal((32, 128)).astype(np.float32)
+        qc = (qp + 0.3 * rng.standard_normal((32, 128))).astype(np.float32)
+        if dtype == "bf16":
+            qp, qc = bf16(qp), bf16(qc)
+        a = (unbf16(qp) if dtype == "bf16" else qp).astype(np.float64)
+        b = (unbf16(qc) if dtype == "bf16" else qc).astype(np.float64)
+        want = np.mean((a * b).sum(1) / np.linalg.norm(a, axis=1) / np.linalg.norm(b, axis=1))
+        r32, r64 = oracle.boundary_r(qp, qc)
+        assert abs(r64 - want) < 1e-12
+        assert abs(r32 - want) < 2e-6
+        perm = rng.permutation(32)
+        r32p, r64p = oracle.boundary_r(qp[perm], qc[perm])
+        assert abs(r64p - r64) < 1e-12 and abs(r32p - r32) < 2e-6
+    z = np.zeros((2, 128), np.float32)
+    o = rng.standard_normal((2, 128)).astype(np.float32)
+    assert oracle.boundary_r(z, o) == (0.0, 0.0)
+
+
+# ------------------------------------------------------------------ scoring + selection
+
+def test_group_scores_are_group_sum_dot_products():
+    G, d, U = 4, 128, 300
+    q = rng.standard_normal((G, d)).astype(np.float32)
+    cent = rng.standard_normal((U, d)).astype(np.float32)
+    s = oracle.group_scores(q, cent)
+    exact = cent.astype(np.float64) @ q.astype(np.float64).sum(0)
+    bound = 2 * (d + G) * 2.0 ** -24 * (np.abs(cent) @ np.abs(q).sum(0))
+    assert np.all(np.abs(s - exact) <= bound)
+    # single head, small integers: every intermediate is exact
+    qi = rng.integers(-8, 8, (1, d)).astype(np.float32)
+    ci = rng.integers(-8, 8, (U, d)).astype(np.float32)
+    assert np.array_equal(oracle.group_scores(qi, ci),
+                          (ci.astype(np.int64) @ qi[0].astype(np.int64)).astype(np.float32))
+
+
+def _selection_properties(s, ln, budget, sel, ntok):
+    order = sorted(range(len(s)), key=lambda u: (-float(s[u]), u))
+    k = len(sel)
+    assert list(sel) == order[:k]                      # a prefix of the order
+    assert ntok == sum(int(ln[u]) for u in sel) <= budget
+    if k < len(s):
+        assert ntok + int(ln[order[k]]) > budget       # stopped at first misfit
+
+
+def test_select_brute_force_unique_prefix():
+    for trial in range(300):
+        u = int(rng.integers(1, 8))
+        s = rng.integers(-3, 4, u).astype(np.float32)   # many score ties
+        ln = rng.integers(0, 6, u).astype(np.int32)
+        budget = int(rng.integers(0, 20))
+        sel, ntok = oracle.select(s, ln, budget)
+        _selection_properties(s, ln, budget, sel, ntok)
+        # brute force: exactly one (ordering, prefix) pair satisfies the rule
+        valid = []
+        for perm in itertools.permutations(range(u)):
+            if any((-s[a], a) > (-s[b], b) for a, b in zip(perm, perm[1:])):
+                continue
+            tok, take = 0, []
+            for x in perm:
+                if tok + ln[x] > budget:
+                    break
+                tok += ln[x]
+                take.append(x)
+            valid.append(take)
+        assert len(valid) == 1 and valid[0] == list(sel)
+
+
+def test_select_budget_covers_all_and_zero_budget():
+    s = rng.standard_normal(50).astype(np.float32)
+    ln = rng.integers(1, 30, 50).astype(np.int32)
+    sel, ntok = oracle.select(s, ln, int(ln.sum()))
+    assert sorted(sel.tolist()) == list(range(50)) and ntok == ln.sum()
+    sel0, ntok0 = oracle.select(s, ln, 0)
+    assert len(sel0) == 0 and ntok0 == 0
+    big = ln.copy(); big[int(np.argmax(s))] = 10 ** 6   # best unit never fits
+    selb, _ = oracle.select(s, big, 100)
+    assert len(selb) == 0
+
+
+# ------------------------------------------------------------------ attention
+
+def _softmax_attn(q, k, v):
+    q, k, v = (x.astype(np.float64) for x in (q, k, v))
+    lg = q @ k.T / math.sqrt(q.shape[1])
+    w = np.exp(lg - lg.max(1, keepdims=True))
+    return (w / w.sum(1, keepdims=True)) @ v
+
+
+def test_attention_closed_forms():
+    d = 128
+    q = rng.standard_normal((4, d)).astype(np.float32)
+    v1 = rng.standard_normal((1, d)).astype(np.float32)
+    k1 = rng.standard_normal((1, d)).astype(np.float32)
+    assert np.allclose(oracle.attention(q, k1, v1), np.repeat(v1, 4, 0), atol=1e-12)
+    kk = np.repeat(k1, 9, 0)
+    vv = rng.standard_normal((9, d)).astype(np.float32)
+    assert np.allclose(oracle.attention(q, kk, vv), np.repeat(vv.astype(np.float64).mean(0, keepdims=True), 4, 0), atol=1e-12)
+    k = rng.standard_normal((70, d)).astype(np.float32)
+    v = rng.standard_normal((70, d)).astype(np.float32)
+    assert np.allclose(oracle.attention(q, k, v), _softmax_attn(q, k, v), atol=1e-12)
+
+
+# ------------------------------------------------------------------ decode
+
+def _decode_inputs(dtype, hkv=2, g=4, d=128, n=300, c=10, T=60, jump=0.1, seed=0):
+    r = np.random.default_rng(seed)
+    comps = r.standard_normal((c, d))
+    keys = (comps[r.integers(0, c, (hkv, n))] + 0.3 * r.standard_normal((hkv, n, d))).astype(np.float32)
+    values = r.standard_normal((hkv, n, d)).astype(np.float32)
+    q = np.empty((T, hkv * g, d), np.float32)
+    cur = r.standard_normal((hkv * g, d))
+    for t in range(T):
+        if t and r.random() < jump:
+            cur = r.standard_normal((hkv * g, d))
+        elif t:
+            cur = cur + 0.2 * r.standard_normal(cur.shape)
+            cur = math.sqrt(d) * cur / np.linalg.norm(cur, axis=1, keepdims=True)
+        q[t] = cur
+    kn = r.standard_normal((T, hkv, d)).astype(np.float32)
+    vn = r.standard_normal((T, hkv, d)).astype(np.float32)
+    if dtype == "bf16":
+        keys, values, q, kn, vn = (bf16(x) for x in (keys, values, q, kn, vn))
+    assign = np.zeros((hkv, n), np.int32)
+    cent = np.zeros((hkv, c, d), np.float32)
+    for h in range(hkv):
+        km = oracle.kmeans(np.ascontiguousarray(keys[h]), c, 4, seed=h)
+        assign[h], cent[h] = km["assign"], km["cent"]
+    return keys, values, assign, cent, q, kn, vn
+
+
+def _f(x):
+    return unbf16(x).astype(np.float64) if x.dtype == np.uint16 else x.astype(np.float64)
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+def test_decode_fullcache_special_case(dtype):
+    """tau > 1 makes every step retrieve; a budget >= every token selects every
+    unit; the local buffer holds the rest: the output is full attention over
+    all prefill and decode tokens so far (the FullCache configuration)."""
+    hkv, g, n, c, T, L = 2, 4, 300, 10, 60, 8
+    keys, values, assign, cent, q, kn, vn = _decode_inputs(dtype, hkv, g, n=n, c=c, T=T)
+    res = oracle.decode(keys, values, assign, cent, q, kn, vn, n_clusters=c, local_buf=L,
+                        tau=1.5, budget=n + T, want_seg_cent=True)
+    assert res["flag"].all()
+    K, Vv, Q, KN, VN = (_f(x) for x in (keys, values, q, kn, vn))
+    for t in range(T):
+        for kh in range(hkv):
+            kk = np.concatenate([K[kh], KN[: t + 1, kh]])
+            vv = np.concatenate([Vv[kh], VN[: t + 1, kh]])
+            want = _softmax_attn(Q[t, kh * g:(kh + 1) * g], kk, vv)
+            assert np.allclose(res["out"][t, kh * g:(kh + 1) * g], want, atol=1e-10)
+    # every boundary closes a segment: all evicted segments have length 1 here
+    assert res["n_evicted"] == T - L and (res["seg_len"] == 1).all()
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+def test_decode_invariants(dtype):
+    hkv, g, n, c, T, L, budget = 2, 4, 300, 10, 200, 16, 90
+    keys, values, assign, cent, q, kn, vn = _decode_inputs(dtype, hkv, g, n=n, c=c, T=T,
+                                                           jump=0.15, seed=4)
+    tau = 0.9
+    res = oracle.decode(keys, values, assign, cent, q, kn, vn, n_clusters=c, local_buf=L,
+                        tau=tau, budget=budget, want_seg_cent=True)
+    flag, ws, nu = res["flag"], res["win_start"], res["n_units"]
+    assert flag[0] == 1
+    assert np.array_equal(flag[1:], (res["r32"][1:] < tau).astype(np.uint8))
+    assert 0 < flag[1:].sum() < T - 1
+    # the local buffer never exceeds L and always holds the current token
+    t = np.arange(T)
+    assert np.all(t - ws + 1 <= L) and np.all(ws <= t)
+    # evicted segments + buffer tile the decode tokens [0, t] in time order
+    ss, sl = res["seg_start"], res["seg_len"]
+    assert ss[0] == 0 and np.all(ss[1:] == ss[:-1] + sl[:-1])
+    assert ss[-1] + sl[-1] == ws[-1]
+    assert nu[-1] == c + res["n_evicted"]
+    # segment boundaries are boundary steps, except forced cuts
+    starts = set((ss + sl).tolist())
+    cuts_not_flagged = [s for s in starts if s < T and flag[s] == 0]
+    assert len(cuts_not_flagged) <= res["n_forced"]
+    # a segment's index vector is the mean of its keys
+    KN = _f(kn)
+    for e in range(res["n_evicted"]):
+        seg = KN[ss[e]: ss[e] + sl[e]]
+        for kh in range(hkv):
+            assert np.allclose(res["seg_cent"][e, kh], seg[:, kh].mean(0), atol=1e-6)
+    # selections: within budget, reused verbatim between boundaries
+    assert np.all(res["n_tok"] <= budget)
+    for step in range(1, T):
+        if not flag[step]:
+            assert np.array_equal(res["n_sel"][step], res["n_sel"][step - 1])
+            assert np.array_equal(res["sel"][step], res["sel"][step - 1])
+
+
+def test_decode_never_triggering_forces_cuts():
+    hkv, g, n, c, T, L = 1, 4, 200, 8, 100, 16
+    keys, values, assign, cent, q, kn, vn = _decode_inputs("fp32", hkv, g, n=n, c=c, T=T)
+    res = oracle.decode(keys, values, assign, cent, q, kn, vn, n_clusters=c, local_buf=L,
+                        tau=-2.0, budget=64)
+    assert res["flag"].sum() == 1
+    assert res["n_forced"] == res["n_evicted"] == (T - 1) // L
+    assert (res["seg_len"] == L).all()
+
+
+def test_decode_selection_is_group_scored_budget_prefix():
+    hkv, g, n, c, T, L, budget = 2, 4, 300, 10, 30, 8, 70
+    keys, values, assign, cent, q, kn, vn = _decode_inputs("bf16", hkv, g, n=n, c=c, T=T)
+    res = oracle.decode(keys, values, assign, cent, q, kn, vn, n_clusters=c, local_buf=L,
+                        tau=0.95, budget=budget)
+    step = 0  # only clusters exist at t = 0
+    for kh in range(hkv):
+        op = oracle.operand(cent[kh], oracle.BF16)
+        s = oracle.group_scores(q[step, kh * g:(kh + 1) * g], op)
+        ln = np.bincount(assign[kh], minlength=c).astype(np.int32)
+        k = res["n_sel"][step, kh]
+        _selection_properties(s, ln, budget, res["sel"][step, kh, :k], res["n_tok"][step, kh])
