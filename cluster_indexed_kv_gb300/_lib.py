@@ -1,0 +1,141 @@
+"""ctypes binding of liblkv (include/lkv.h): argument marshalling only.
+
+Every function here has the name of the C entry point it calls. There is no
+fallback: if liblkv.so has not been built, loading raises immediately.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import threading
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "liblkv.so")
+
+LKV_OK, LKV_EINVAL, LKV_ENOMEM, LKV_ECUDA, LKV_ECAPACITY, LKV_ESTATE, LKV_ETIMEOUT = range(7)
+STATUS_NAMES = {0: "LKV_OK", 1: "LKV_EINVAL", 2: "LKV_ENOMEM", 3: "LKV_ECUDA",
+                4: "LKV_ECAPACITY", 5: "LKV_ESTATE", 6: "LKV_ETIMEOUT"}
+LKV_DTYPE_FP32, LKV_DTYPE_BF16 = 0, 1
+
+EXPORTED = ("lkv_create", "lkv_destroy", "lkv_build_index", "lkv_load_index",
+            "lkv_decode_step", "lkv_get_index", "lkv_get_decode_state", "lkv_sync",
+            "lkv_last_error")
+
+
+class lkv_config(C.Structure):
+    _fields_ = [
+        ("batch", C.c_int32), ("n_layers", C.c_int32), ("n_kv_heads", C.c_int32),
+        ("group", C.c_int32), ("head_dim", C.c_int32), ("dtype", C.c_int32),
+        ("local_buf", C.c_int32), ("max_clusters", C.c_int32), ("max_prefill", C.c_int64),
+        ("max_steps", C.c_int32), ("max_budget", C.c_int32), ("offload", C.c_int32),
+        ("stream", C.c_void_p),
+    ]
+
+
+class lkv_decode_state(C.Structure):
+    _fields_ = [
+        ("t", C.c_int32), ("win_start", C.c_int32), ("open_start", C.c_int32),
+        ("n_clusters", C.c_int32), ("n_units", C.c_int32), ("n_closed", C.c_int32),
+        ("n_evicted", C.c_int32), ("n_forced", C.c_int32), ("n_refined", C.c_int64),
+        ("n_inexact", C.c_int64),
+    ]
+
+
+class LKVError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load liblkv.so (raises if it is missing: build it first)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"liblkv.so not found at {path}; build it with "
+                "`python -m cluster_indexed_kv_gb300.build` (needs nvcc)")
+        L = C.CDLL(path)
+        vp, i32, i64, u64, f32 = C.c_void_p, C.c_int32, C.c_int64, C.c_uint64, C.c_float
+        st = C.c_int
+        L.lkv_create.argtypes = [C.POINTER(lkv_config), C.POINTER(vp)]
+        L.lkv_create.restype = st
+        L.lkv_destroy.argtypes = [vp]
+        L.lkv_destroy.restype = None
+        L.lkv_build_index.argtypes = [vp, i32, vp, vp, i64, i32, i32, u64]
+        L.lkv_build_index.restype = st
+        L.lkv_load_index.argtypes = [vp, i32, vp, vp, i64, i32, vp, vp]
+        L.lkv_load_index.restype = st
+        L.lkv_decode_step.argtypes = [vp, i32, i32, vp, vp, vp, f32, i32, i32, vp, vp, vp, vp, vp]
+        L.lkv_decode_step.restype = st
+        L.lkv_get_index.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, C.POINTER(i32)]
+        L.lkv_get_index.restype = st
+        L.lkv_get_decode_state.argtypes = [vp, i32, i32, C.POINTER(lkv_decode_state)]
+        L.lkv_get_decode_state.restype = st
+        L.lkv_sync.argtypes = [vp]
+        L.lkv_sync.restype = st
+        L.lkv_last_error.argtypes = [vp]
+        L.lkv_last_error.restype = C.c_char_p
+        _lib = L
+        return L
+
+
+def _check(status: int, ctx) -> None:
+    if status != LKV_OK:
+        msg = load().lkv_last_error(ctx)
+        raise LKVError(status, msg.decode() if msg else "")
+
+
+def lkv_create(cfg: lkv_config):
+    h = C.c_void_p()
+    _check(load().lkv_create(C.byref(cfg), C.byref(h)), None)
+    return h
+
+
+def lkv_destroy(ctx) -> None:
+    load().lkv_destroy(ctx)
+
+
+def lkv_build_index(ctx, layer, keys_ptr, values_ptr, n_tokens, n_clusters, iters, seed):
+    _check(load().lkv_build_index(ctx, layer, keys_ptr, values_ptr, n_tokens, n_clusters,
+                                  iters, seed), ctx)
+
+
+def lkv_load_index(ctx, layer, keys_ptr, values_ptr, n_tokens, n_clusters, assign_ptr, cent_ptr):
+    _check(load().lkv_load_index(ctx, layer, keys_ptr, values_ptr, n_tokens, n_clusters,
+                                 assign_ptr, cent_ptr), ctx)
+
+
+def lkv_decode_step(ctx, layer, n_layers, q_ptr, k_ptr, v_ptr, tau, budget, local_buf,
+                    out_ptr, sel_ptr, nsel_ptr, boundary_ptr, r_ptr):
+    _check(load().lkv_decode_step(ctx, layer, n_layers, q_ptr, k_ptr, v_ptr, tau, budget,
+                                  local_buf, out_ptr, sel_ptr, nsel_ptr, boundary_ptr, r_ptr), ctx)
+
+
+def lkv_get_index(ctx, layer, seq, kv_head, capacity, cent_ptr, len_ptr, row_ptr, assign_ptr,
+                  perm_ptr) -> int:
+    n = C.c_int32(0)
+    _check(load().lkv_get_index(ctx, layer, seq, kv_head, capacity, cent_ptr, len_ptr, row_ptr,
+                                assign_ptr, perm_ptr, C.byref(n)), ctx)
+    return n.value
+
+
+def lkv_get_decode_state(ctx, layer, seq) -> lkv_decode_state:
+    s = lkv_decode_state()
+    _check(load().lkv_get_decode_state(ctx, layer, seq, C.byref(s)), ctx)
+    return s
+
+
+def lkv_sync(ctx) -> None:
+    _check(load().lkv_sync(ctx), ctx)
+
+
+def lkv_last_error(ctx) -> str:
+    m = load().lkv_last_error(ctx)
+    return m.decode() if m else ""

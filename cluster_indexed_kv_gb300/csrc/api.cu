@@ -1,0 +1,385 @@
+// api.cu -- the C ABI of liblkv (declared in include/lkv.h): context
+// allocation, argument checks, stream-ordered launches, blocking queries.
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/lkv.h"
+#include "lkv_internal.cuh"
+
+using lkv::CtxView;
+using lkv::DecState;
+using lkv::KmeansScratch;
+
+struct lkv_ctx {
+  lkv_config cfg{};
+  CtxView v{};
+  KmeansScratch ks{};
+  cudaStream_t stream = nullptr;
+  std::vector<void *> dev;
+  std::vector<void *> host;
+  std::vector<int32_t> steps;     // decode steps taken per layer
+  std::vector<int8_t> built;      // index present per layer
+  std::vector<int64_t> n_tokens;  // prefill tokens per layer
+  std::vector<int32_t> n_clusters;
+  std::string err;
+  bool broken = false;
+  int alloc_index = 0;
+  int fail_at = -1;               // host-side allocation-failure injection
+};
+
+static thread_local std::string g_create_error;
+
+static lkv_status fail(lkv_ctx *c, lkv_status s, const std::string &msg) {
+  if (c) c->err = msg;
+  else g_create_error = msg;
+  return s;
+}
+
+static lkv_status cuda_fail(lkv_ctx *c, cudaError_t e, const char *where) {
+  if (c) c->broken = true;
+  return fail(c, LKV_ECUDA, std::string(where) + ": " + cudaGetErrorString(e));
+}
+
+static void *dalloc(lkv_ctx *c, size_t bytes, lkv_status *st) {
+  if (*st != LKV_OK) return nullptr;
+  if (c->fail_at >= 0 && c->alloc_index++ == c->fail_at) {
+    *st = fail(c, LKV_ENOMEM, "injected allocation failure");
+    return nullptr;
+  }
+  void *p = nullptr;
+  if (cudaMalloc(&p, bytes < 16 ? 16 : bytes) != cudaSuccess) {
+    cudaGetLastError();
+    *st = fail(c, LKV_ENOMEM, "cudaMalloc of " + std::to_string(bytes) + " bytes failed");
+    return nullptr;
+  }
+  c->dev.push_back(p);
+  return p;
+}
+
+static void *halloc(lkv_ctx *c, size_t bytes, lkv_status *st) {
+  if (*st != LKV_OK) return nullptr;
+  if (c->fail_at >= 0 && c->alloc_index++ == c->fail_at) {
+    *st = fail(c, LKV_ENOMEM, "injected allocation failure");
+    return nullptr;
+  }
+  void *p = nullptr;
+  if (cudaHostAlloc(&p, bytes < 16 ? 16 : bytes, cudaHostAllocMapped | cudaHostAllocPortable) != cudaSuccess) {
+    cudaGetLastError();
+    *st = fail(c, LKV_ENOMEM, "pinned host allocation of " + std::to_string(bytes) + " bytes failed");
+    return nullptr;
+  }
+  c->host.push_back(p);
+  return p;
+}
+
+static void free_all(lkv_ctx *c) {
+  for (void *p : c->dev) cudaFree(p);
+  for (void *p : c->host) cudaFreeHost(p);
+  c->dev.clear();
+  c->host.clear();
+}
+
+// splitmix64 (Steele, Lea and Flood, OOPSLA 2014), the seeded source of the
+// K-means initialisation.
+static uint64_t splitmix64_next(uint64_t &state) {
+  uint64_t z = (state += 0x9e3779b97f4a7c15ull);
+  z = (z ^ (z >> 30)) * 0xbf58476d1ce4e5b9ull;
+  z = (z ^ (z >> 27)) * 0x94d049bb133111ebull;
+  return z ^ (z >> 31);
+}
+
+// First c entries of a partial Fisher-Yates shuffle of [0, n).
+static void init_indices(int64_t n, int32_t c, uint64_t seed, int64_t *out,
+                         std::vector<int64_t> &perm) {
+  perm.resize((size_t)n);
+  for (int64_t i = 0; i < n; ++i) perm[(size_t)i] = i;
+  uint64_t st = seed;
+  for (int32_t i = 0; i < c; ++i) {
+    const uint64_t r = splitmix64_next(st);
+    const int64_t j = (int64_t)i + (int64_t)(r % (uint64_t)(n - i));
+    std::swap(perm[(size_t)i], perm[(size_t)j]);
+    out[i] = perm[(size_t)i];
+  }
+}
+
+extern "C" {
+
+lkv_status lkv_create(const lkv_config *cfg, lkv_ctx **out) {
+  if (!cfg || !out) return fail(nullptr, LKV_EINVAL, "null argument");
+  *out = nullptr;
+  const lkv_config &k = *cfg;
+  if (k.head_dim != 128) return fail(nullptr, LKV_EINVAL, "head_dim must be 128");
+  if (!(k.group == 1 || k.group == 2 || k.group == 4 || k.group == 8))
+    return fail(nullptr, LKV_EINVAL, "group must be 1, 2, 4 or 8");
+  if (k.n_kv_heads < 1 || k.n_kv_heads > 16) return fail(nullptr, LKV_EINVAL, "n_kv_heads must be 1..16");
+  if (k.batch < 1 || k.n_layers < 1) return fail(nullptr, LKV_EINVAL, "batch and n_layers must be >= 1");
+  if (k.dtype != LKV_DTYPE_FP32 && k.dtype != LKV_DTYPE_BF16) return fail(nullptr, LKV_EINVAL, "bad dtype");
+  if (k.local_buf < 1) return fail(nullptr, LKV_EINVAL, "local_buf must be >= 1");
+  if (k.max_clusters < 1 || k.max_clusters > 12288) return fail(nullptr, LKV_EINVAL, "max_clusters must be 1..12288");
+  if (k.max_prefill < 1 || k.max_prefill > (int64_t(1) << 18)) return fail(nullptr, LKV_EINVAL, "max_prefill must be 1..2^18");
+  if (k.max_steps < 1 || k.max_budget < 0) return fail(nullptr, LKV_EINVAL, "max_steps >= 1 and max_budget >= 0 required");
+  if ((int64_t)k.max_clusters + k.max_steps >= (int64_t(1) << 30)) return fail(nullptr, LKV_EINVAL, "too many units");
+  if (k.max_budget > (int64_t(1) << 30)) return fail(nullptr, LKV_EINVAL, "max_budget too large");
+
+  lkv_ctx *c = new lkv_ctx();
+  c->cfg = k;
+  c->stream = (cudaStream_t)k.stream;
+  if (const char *e = std::getenv("LKV_FAIL_ALLOC_AFTER")) c->fail_at = std::atoi(e);
+  const int B = k.batch, NL = k.n_layers, Hkv = k.n_kv_heads, G = k.group, d = 128;
+  const int H = Hkv * G;
+  const size_t es = k.dtype == LKV_DTYPE_BF16 ? 2 : 4;
+  const int64_t n_cap = k.max_prefill;
+  const int32_t t_cap = k.max_steps, c_cap = k.max_clusters, u_cap = c_cap + t_cap;
+  const int64_t S_all = (int64_t)NL * B * Hkv, LB = (int64_t)NL * B, S = (int64_t)B * Hkv;
+  const int64_t pool_rows = n_cap + t_cap;
+  const int32_t max_chunks = (k.max_budget + k.local_buf + lkv::kAttnChunk - 1) / lkv::kAttnChunk;
+
+  lkv_status st = LKV_OK;
+  CtxView &v = c->v;
+  v.dtype = k.dtype;
+  v.B = B; v.Hkv = Hkv; v.G = G; v.d = d; v.L = k.local_buf;
+  v.n_cap = n_cap; v.t_cap = t_cap; v.u_cap = u_cap; v.bud_cap = k.max_budget;
+  v.offload = k.offload ? 1 : 0;
+  v.pool_rows = pool_rows;
+  if (!k.offload) {
+    v.pool_k = dalloc(c, S_all * pool_rows * d * es, &st);
+    v.pool_v = dalloc(c, S_all * pool_rows * d * es, &st);
+    if (st == LKV_OK) {
+      v.dec_k = (char *)v.pool_k + n_cap * d * es;
+      v.dec_v = (char *)v.pool_v + n_cap * d * es;
+    }
+    v.dec_rows = pool_rows;
+  } else {
+    v.pool_k = halloc(c, S_all * pool_rows * d * es, &st);
+    v.pool_v = halloc(c, S_all * pool_rows * d * es, &st);
+    v.dec_k = dalloc(c, S_all * t_cap * d * es, &st);
+    v.dec_v = dalloc(c, S_all * t_cap * d * es, &st);
+    v.dec_rows = t_cap;
+    v.stage_k = dalloc(c, S_all * (int64_t)k.max_budget * d * es, &st);
+    v.stage_v = dalloc(c, S_all * (int64_t)k.max_budget * d * es, &st);
+  }
+  v.cent_op = dalloc(c, S_all * u_cap * d * es, &st);
+  v.cent32 = (float *)dalloc(c, S_all * u_cap * d * 4, &st);
+  v.unit_row = (int32_t *)dalloc(c, S_all * u_cap * 4, &st);
+  v.unit_len = (int32_t *)dalloc(c, S_all * u_cap * 4, &st);
+  v.assign = (int32_t *)dalloc(c, S_all * n_cap * 4, &st);
+  v.perm = (int32_t *)dalloc(c, S_all * n_cap * 4, &st);
+  v.st = (DecState *)dalloc(c, LB * sizeof(DecState), &st);
+  v.q_prev = dalloc(c, LB * H * d * es, &st);
+  v.segsum = (int64_t *)dalloc(c, S_all * d * 8, &st);
+  v.scores = (float *)dalloc(c, S_all * u_cap * 4, &st);
+  v.sel = (int32_t *)dalloc(c, S_all * u_cap * 4, &st);
+  v.n_sel = (int32_t *)dalloc(c, S_all * 4, &st);
+  v.n_tok = (int32_t *)dalloc(c, S_all * 4, &st);
+  v.rng_row = (int32_t *)dalloc(c, S_all * u_cap * 4, &st);
+  v.rng_cum = (int32_t *)dalloc(c, S_all * (u_cap + 1) * 4, &st);
+  v.max_chunks = max_chunks;
+  v.part_acc = (float *)dalloc(c, S_all * max_chunks * G * d * 4, &st);
+  v.part_ml = (float *)dalloc(c, S_all * max_chunks * G * 2 * 4, &st);
+  v.attn_count = (int32_t *)dalloc(c, S_all * 4, &st);
+  v.err = (int32_t *)dalloc(c, 4, &st);
+
+  KmeansScratch &ks = c->ks;
+  ks.knorm = (float *)dalloc(c, S * n_cap * 4, &st);
+  ks.c2 = (float *)dalloc(c, S * c_cap * 4, &st);
+  ks.cstat = (float *)dalloc(c, S * 2 * 4, &st);
+  ks.cnt_part = (int32_t *)dalloc(c, S * lkv::kMaxParts * c_cap * 4, &st);
+  ks.count = (int32_t *)dalloc(c, S * c_cap * 4, &st);
+  ks.offs = (int32_t *)dalloc(c, S * c_cap * 4, &st);
+  ks.amb = (int4 *)dalloc(c, S * n_cap * sizeof(int4), &st);
+  ks.amb_count = (int32_t *)dalloc(c, 4, &st);
+  ks.n_refined = (int64_t *)dalloc(c, 8, &st);
+  ks.n_inexact = (int64_t *)dalloc(c, 8, &st);
+  ks.init_idx = (int64_t *)dalloc(c, S * c_cap * 8, &st);
+  if (st != LKV_OK) {
+    g_create_error = c->err;
+    free_all(c);
+    delete c;
+    return st;
+  }
+  cudaError_t e = cudaSuccess;
+  if (e == cudaSuccess) e = cudaMemsetAsync(v.st, 0, LB * sizeof(DecState), c->stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(v.attn_count, 0, S_all * 4, c->stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(v.err, 0, 4, c->stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(ks.n_refined, 0, 8, c->stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(ks.n_inexact, 0, 8, c->stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(c->stream);
+  if (e != cudaSuccess) {
+    g_create_error = std::string("initialisation: ") + cudaGetErrorString(e);
+    free_all(c);
+    delete c;
+    return LKV_ECUDA;
+  }
+  c->steps.assign(NL, 0);
+  c->built.assign(NL, 0);
+  c->n_tokens.assign(NL, 0);
+  c->n_clusters.assign(NL, 0);
+  *out = c;
+  return LKV_OK;
+}
+
+void lkv_destroy(lkv_ctx *c) {
+  if (!c) return;
+  cudaStreamSynchronize(c->stream);
+  free_all(c);
+  delete c;
+}
+
+static lkv_status check_usable(lkv_ctx *c) {
+  if (!c) return LKV_EINVAL;
+  if (c->broken) return fail(c, LKV_ESTATE, "context is unusable after a CUDA error");
+  return LKV_OK;
+}
+
+lkv_status lkv_build_index(lkv_ctx *c, int32_t layer, const void *keys, const void *values,
+                           int64_t n, int32_t nc, int32_t iters, uint64_t seed) {
+  lkv_status s = check_usable(c);
+  if (s != LKV_OK) return s;
+  if (layer < 0 || layer >= c->cfg.n_layers) return fail(c, LKV_EINVAL, "layer out of range");
+  if (!keys || !values) return fail(c, LKV_EINVAL, "null keys or values");
+  if (n < 1 || n > c->cfg.max_prefill) return fail(c, LKV_EINVAL, "n_tokens outside 1..max_prefill");
+  if (nc < 1 || nc > c->cfg.max_clusters || nc > n)
+    return fail(c, LKV_EINVAL, "n_clusters outside 1..min(max_clusters, n_tokens)");
+  if (iters < 1) return fail(c, LKV_EINVAL, "iters must be >= 1");
+  const int S = c->cfg.batch * c->cfg.n_kv_heads;
+  std::vector<int64_t> idx((size_t)S * nc), perm;
+  for (int sl = 0; sl < S; ++sl) init_indices(n, nc, seed + (uint64_t)sl, idx.data() + (size_t)sl * nc, perm);
+  cudaError_t e = cudaMemcpyAsync(c->ks.init_idx, idx.data(), idx.size() * 8, cudaMemcpyHostToDevice, c->stream);
+  if (e == cudaSuccess) e = lkv::launch_kmeans_build(c->v, layer, c->ks, keys, values, n, nc, iters, false, c->stream);
+  if (e != cudaSuccess) return cuda_fail(c, e, "lkv_build_index");
+  c->built[layer] = 1;
+  c->steps[layer] = 0;
+  c->n_tokens[layer] = n;
+  c->n_clusters[layer] = nc;
+  return LKV_OK;
+}
+
+lkv_status lkv_load_index(lkv_ctx *c, int32_t layer, const void *keys, const void *values,
+                          int64_t n, int32_t nc, const int32_t *assign, const float *cent) {
+  lkv_status s = check_usable(c);
+  if (s != LKV_OK) return s;
+  if (layer < 0 || layer >= c->cfg.n_layers) return fail(c, LKV_EINVAL, "layer out of range");
+  if (!keys || !values || !assign || !cent) return fail(c, LKV_EINVAL, "null argument");
+  if (n < 1 || n > c->cfg.max_prefill) return fail(c, LKV_EINVAL, "n_tokens outside 1..max_prefill");
+  if (nc < 1 || nc > c->cfg.max_clusters) return fail(c, LKV_EINVAL, "n_clusters outside 1..max_clusters");
+  cudaError_t e = lkv::launch_load_index(c->v, layer, c->ks, keys, values, n, nc, assign, cent, c->stream);
+  if (e != cudaSuccess) return cuda_fail(c, e, "lkv_load_index");
+  c->built[layer] = 1;
+  c->steps[layer] = 0;
+  c->n_tokens[layer] = n;
+  c->n_clusters[layer] = nc;
+  return LKV_OK;
+}
+
+lkv_status lkv_decode_step(lkv_ctx *c, int32_t layer, int32_t nl, const void *q,
+                           const void *k_new, const void *v_new, float tau, int32_t budget,
+                           int32_t local_buf, float *out, int32_t *selected_units,
+                           int32_t *n_selected, uint8_t *boundary, float *r_out) {
+  lkv_status s = check_usable(c);
+  if (s != LKV_OK) return s;
+  if (nl < 1 || layer < 0 || layer + nl > c->cfg.n_layers) return fail(c, LKV_EINVAL, "layer range out of bounds");
+  if (!q || !k_new || !v_new || !out) return fail(c, LKV_EINVAL, "null input or output");
+  if (budget < 0 || budget > c->cfg.max_budget) return fail(c, LKV_EINVAL, "budget outside 0..max_budget");
+  if (local_buf != c->cfg.local_buf) return fail(c, LKV_EINVAL, "local_buf differs from the context's");
+  if (tau != tau) return fail(c, LKV_EINVAL, "tau is NaN");
+  for (int l = layer; l < layer + nl; ++l) {
+    if (!c->built[l]) return fail(c, LKV_ESTATE, "layer " + std::to_string(l) + " has no index");
+    if (c->steps[l] >= c->cfg.max_steps) return fail(c, LKV_ECAPACITY, "max_steps reached");
+  }
+  lkv::StepArgs a{};
+  a.q = q; a.k_new = k_new; a.v_new = v_new;
+  a.tau = tau; a.budget = budget;
+  a.out = out; a.selected_units = selected_units; a.n_selected = n_selected;
+  a.boundary = boundary; a.r_out = r_out;
+  a.l0 = layer; a.nl = nl;
+  cudaError_t e = lkv::launch_decode_step(c->v, a, c->stream);
+  if (e != cudaSuccess) return cuda_fail(c, e, "lkv_decode_step");
+  for (int l = layer; l < layer + nl; ++l) c->steps[l] += 1;
+  return LKV_OK;
+}
+
+lkv_status lkv_sync(lkv_ctx *c) {
+  if (!c) return LKV_EINVAL;
+  if (c->broken) return fail(c, LKV_ESTATE, "context is unusable after a CUDA error");
+  cudaError_t e = cudaStreamSynchronize(c->stream);
+  if (e != cudaSuccess) return cuda_fail(c, e, "lkv_sync");
+  int32_t bits = 0;
+  e = cudaMemcpy(&bits, c->v.err, 4, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(c, e, "lkv_sync");
+  if (bits) {
+    cudaMemset(c->v.err, 0, 4);
+    if (bits & lkv::kErrTimeout) return fail(c, LKV_ETIMEOUT, "a device-side wait gave up");
+    if (bits & lkv::kErrCapacity) return fail(c, LKV_ECAPACITY, "device-side capacity exceeded");
+    return fail(c, LKV_ECUDA, "device-side invariant check failed");
+  }
+  return LKV_OK;
+}
+
+lkv_status lkv_get_index(lkv_ctx *c, int32_t layer, int32_t seq, int32_t kv_head,
+                         int32_t capacity, float *centroids, int32_t *unit_len,
+                         int32_t *unit_row, int32_t *assign, int32_t *perm, int32_t *n_units) {
+  lkv_status s = check_usable(c);
+  if (s != LKV_OK) return s;
+  if (layer < 0 || layer >= c->cfg.n_layers || seq < 0 || seq >= c->cfg.batch || kv_head < 0 ||
+      kv_head >= c->cfg.n_kv_heads || !n_units)
+    return fail(c, LKV_EINVAL, "index coordinates out of range");
+  if (!c->built[layer]) return fail(c, LKV_ESTATE, "layer has no index");
+  s = lkv_sync(c);
+  if (s != LKV_OK) return s;
+  const int64_t lb = (int64_t)layer * c->cfg.batch + seq;
+  const int64_t gs = lb * c->cfg.n_kv_heads + kv_head;
+  DecState st{};
+  cudaError_t e = cudaMemcpy(&st, c->v.st + lb, sizeof st, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(c, e, "lkv_get_index");
+  *n_units = st.n_units;
+  if (st.n_units > capacity) return fail(c, LKV_ECAPACITY, "capacity below n_units");
+  const int64_t u_cap = c->v.u_cap, n = c->n_tokens[layer];
+  if (centroids && e == cudaSuccess)
+    e = cudaMemcpy(centroids, c->v.cent32 + gs * u_cap * 128, (size_t)st.n_units * 128 * 4, cudaMemcpyDeviceToHost);
+  if (unit_len && e == cudaSuccess)
+    e = cudaMemcpy(unit_len, c->v.unit_len + gs * u_cap, (size_t)st.n_units * 4, cudaMemcpyDeviceToHost);
+  if (unit_row && e == cudaSuccess)
+    e = cudaMemcpy(unit_row, c->v.unit_row + gs * u_cap, (size_t)st.n_units * 4, cudaMemcpyDeviceToHost);
+  if (assign && e == cudaSuccess)
+    e = cudaMemcpy(assign, c->v.assign + gs * c->v.n_cap, (size_t)n * 4, cudaMemcpyDeviceToHost);
+  if (perm && e == cudaSuccess)
+    e = cudaMemcpy(perm, c->v.perm + gs * c->v.n_cap, (size_t)n * 4, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(c, e, "lkv_get_index");
+  return LKV_OK;
+}
+
+lkv_status lkv_get_decode_state(lkv_ctx *c, int32_t layer, int32_t seq, lkv_decode_state *out) {
+  lkv_status s = check_usable(c);
+  if (s != LKV_OK) return s;
+  if (!out || layer < 0 || layer >= c->cfg.n_layers || seq < 0 || seq >= c->cfg.batch)
+    return fail(c, LKV_EINVAL, "state coordinates out of range");
+  s = lkv_sync(c);
+  if (s != LKV_OK) return s;
+  DecState st{};
+  int64_t refined = 0, inexact = 0;
+  cudaError_t e = cudaMemcpy(&st, c->v.st + (int64_t)layer * c->cfg.batch + seq, sizeof st, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemcpy(&refined, c->ks.n_refined, 8, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemcpy(&inexact, c->ks.n_inexact, 8, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(c, e, "lkv_get_decode_state");
+  out->t = st.t;
+  out->win_start = st.win_start;
+  out->open_start = st.open_start;
+  out->n_clusters = st.n_clusters;
+  out->n_units = st.n_units;
+  out->n_closed = st.n_closed;
+  out->n_evicted = st.n_evicted;
+  out->n_forced = st.n_forced;
+  out->n_refined = refined;
+  out->n_inexact = inexact;
+  return LKV_OK;
+}
+
+const char *lkv_last_error(const lkv_ctx *c) {
+  if (!c) return g_create_error.c_str();
+  return c->err.c_str();
+}
+
+}  // extern "C"

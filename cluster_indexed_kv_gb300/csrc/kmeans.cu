@@ -1,0 +1,700 @@
+// kmeans.cu -- prefill index build: K-means over each (sequence, KV head)'s
+// keys, then the cluster-grouped K/V pool and the unit table
+// [LouisKV notes, 关键设计 2: cluster the input keys with K-means; centroid =
+// mean of the cluster's keys; it is the retrieval index of the cluster].
+//
+// Lloyd round = assign (argmin squared distance to the scoring operand of the
+// current centroids) + update (member mean).
+//
+// Assignment is decided on the double-precision squared distance
+//   D(k, c) = sum_j (k_j - c_j)^2   (index order, separate sub/mul/add),
+// ties to the lowest cluster id. A fast single-precision distance e_j =
+// |c_j|^2 - 2 k.c_j (equal to D - |k|^2 up to rounding) filters: with a proven
+// bound beta on |e_j - (D_j - |k|^2)|, a key whose two smallest e differ by
+// more than 2 beta has a certain argmin; otherwise the key goes on a list and
+// is settled by evaluating D in double precision for the two candidates (or
+// for every cluster when a third one is also within 2 beta).
+//
+// Update: members are grouped by a stable counting sort (token order within a
+// cluster); the member sum of bf16 keys is formed exactly in 2^-40 fixed
+// point (double-precision token-order sum when a value is out of that range,
+// and always for fp32 keys); centroid = float(sum / count) in double.
+#include "lkv_internal.cuh"
+
+namespace lkv {
+
+// ---------------------------------------------------------------- init
+
+template <int DT>
+__global__ void k_init_cent(const void *keys, int64_t n, int32_t c,
+                            const int64_t *idx, float *cent32, int64_t gs0,
+                            int32_t u_cap) {
+  const int s = blockIdx.y, j = blockIdx.x, t = threadIdx.x;  // 128 threads
+  const int64_t row = idx[(int64_t)s * c + j];
+  const float v = load_elem<DT>(keys, ((int64_t)s * n + row) * kHeadDim + t);
+  cent32[((gs0 + s) * u_cap + j) * kHeadDim + t] = v;
+}
+
+template <int DT>
+__global__ void k_key_norms(const void *keys, int64_t n, int64_t n_cap, float *knorm) {
+  const int s = blockIdx.y;
+  const int lane = threadIdx.x & 31;
+  const int64_t i = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  if (i >= n) return;
+  float acc = 0.f;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    float x = load_elem<DT>(keys, ((int64_t)s * n + i) * kHeadDim + lane * 4 + e);
+    acc = fmaf(x, x, acc);
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (lane == 0) knorm[(int64_t)s * n_cap + i] = sqrtf(acc);
+}
+
+// Scoring/assignment operand of the current centroids (bf16-rounded for bf16
+// keys), its squared norm in fp32, and per-slice maxima of |c| and |c|^2.
+template <int DT>
+__global__ void k_prepare_operand(const float *cent32, void *cent_op, int32_t c,
+                                  int32_t c_cap, int32_t u_cap, int64_t gs0,
+                                  float *c2, float *cstat) {
+  const int s = blockIdx.y;
+  const int lane = threadIdx.x & 31;
+  const int j = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  if (j >= c) return;
+  const int64_t base = ((gs0 + s) * u_cap + j) * kHeadDim;
+  float acc = 0.f;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int k = lane * 4 + e;
+    float x = cent32[base + k];
+    if constexpr (DT == 1) {
+      uint16_t b = f32_to_bf16_bits(x);
+      ((uint16_t *)cent_op)[base + k] = b;
+      x = bf16_bits_to_f32(b);
+    } else {
+      ((float *)cent_op)[base + k] = x;
+    }
+    acc = fmaf(x, x, acc);
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (lane == 0) {
+    c2[(int64_t)s * c_cap + j] = acc;
+    // non-negative floats order like their bit patterns
+    atomicMax((unsigned *)&cstat[2 * s], __float_as_uint(sqrtf(acc)));
+    atomicMax((unsigned *)&cstat[2 * s + 1], __float_as_uint(acc));
+  }
+}
+
+// ---------------------------------------------------------------- assignment
+
+// Running three smallest (value, index) pairs, lexicographic order; only the
+// value of the third is kept.
+struct Top3 {
+  float v1, v2, v3;
+  int32_t j1, j2;
+};
+
+__device__ __forceinline__ bool lex_less(float a, int32_t ia, float b, int32_t ib) {
+  return a < b || (a == b && ia < ib);
+}
+
+__device__ __forceinline__ void top3_push(Top3 &t, float v, int32_t j) {
+  // callers push indices in increasing order, so a strict value compare
+  // keeps the lowest index among equal values
+  if (v < t.v3) {
+    if (v < t.v2) {
+      t.v3 = t.v2;
+      if (v < t.v1) {
+        t.v2 = t.v1; t.j2 = t.j1;
+        t.v1 = v; t.j1 = j;
+      } else {
+        t.v2 = v; t.j2 = j;
+      }
+    } else {
+      t.v3 = v;
+    }
+  }
+}
+
+__device__ __forceinline__ Top3 top3_merge(const Top3 &a, const Top3 &b) {
+  // merge two lexicographically sorted top-3 lists
+  float v[6] = {a.v1, a.v2, a.v3, b.v1, b.v2, b.v3};
+  int32_t j[6] = {a.j1, a.j2, 0x7fffffff, b.j1, b.j2, 0x7fffffff};
+  int ia = 0, ib = 3;
+  float ov[3];
+  int32_t oj[3];
+#pragma unroll
+  for (int k = 0; k < 3; ++k) {
+    bool take_a = (ib >= 6) || (ia < 3 && lex_less(v[ia], j[ia], v[ib], j[ib]));
+    if (take_a) { ov[k] = v[ia]; oj[k] = j[ia]; ++ia; }
+    else { ov[k] = v[ib]; oj[k] = j[ib]; ++ib; }
+  }
+  Top3 r;
+  r.v1 = ov[0]; r.j1 = oj[0]; r.v2 = ov[1]; r.j2 = oj[1]; r.v3 = ov[2];
+  return r;
+}
+
+__device__ __forceinline__ Top3 top3_shfl(const Top3 &t, int lanemask) {
+  Top3 o;
+  o.v1 = __shfl_xor_sync(0xffffffffu, t.v1, lanemask);
+  o.v2 = __shfl_xor_sync(0xffffffffu, t.v2, lanemask);
+  o.v3 = __shfl_xor_sync(0xffffffffu, t.v3, lanemask);
+  o.j1 = __shfl_xor_sync(0xffffffffu, t.j1, lanemask);
+  o.j2 = __shfl_xor_sync(0xffffffffu, t.j2, lanemask);
+  return o;
+}
+
+// Decision for one key from its filtered top-3: write the certain argmin, or
+// queue the key for the exact double-precision comparison.
+__device__ __forceinline__ void assign_decide(const Top3 &t, int32_t c, float kn,
+                                              float cmax, float c2max, float eps,
+                                              int32_t s, int64_t row, int32_t *assign_row,
+                                              int4 *amb, int32_t *amb_count,
+                                              int32_t amb_cap, int32_t *err) {
+  const float beta2 = 2.f * eps * (kn * cmax + c2max);
+  *assign_row = t.j1;
+  if (c == 1 || t.v2 - t.v1 > beta2) return;
+  const int crowded = (c > 2) && !(t.v3 - t.v1 > beta2);
+  const int slot = atomicAdd(amb_count, 1);
+  if (slot < amb_cap)
+    amb[slot] = make_int4(s, (int)row, t.j1, (int)((unsigned)t.j2 | ((unsigned)crowded << 31)));
+  else
+    set_err(err, kErrCapacity);
+}
+
+// SIMT fp32 filter: CTA = 64 keys x all centroids, 64-centroid tiles.
+// Thread (ty, tx) owns keys 4ty..4ty+3 x centroids 4tx..4tx+3 of a tile.
+constexpr int kAsTile = 64;
+constexpr int kAsThreads = 256;
+constexpr int kEsPitch = kAsTile + 1;
+constexpr size_t kAsSmem = sizeof(float) * (2 * kHeadDim * kAsTile + kAsTile * kEsPitch + kAsTile + kAsTile);
+
+template <int DT>
+__global__ void __launch_bounds__(kAsThreads)
+k_assign_simt(const void *keys, int64_t n, int32_t c, const void *cent_op,
+              int32_t u_cap, const float *c2, int32_t c_cap, const float *knorm,
+              int64_t n_cap, const float *cstat, float eps, int32_t *assign,
+              int64_t gs0, int4 *amb, int32_t *amb_count, int32_t amb_cap,
+              int32_t *err) {
+  extern __shared__ float sm[];
+  float *Ks = sm;                               // [128][64] key tile, transposed
+  float *Cs = Ks + kHeadDim * kAsTile;          // [128][64] centroid tile, transposed
+  float *Es = Cs + kHeadDim * kAsTile;          // [64][65] filtered distances
+  float *c2s = Es + kAsTile * kEsPitch;         // [64]
+  float *kns = c2s + kAsTile;                   // [64]
+  const int s = blockIdx.y;
+  const int tid = threadIdx.x;
+  const int ty = tid / 16, tx = tid % 16;
+  const int64_t row0 = (int64_t)blockIdx.x * kAsTile;
+  const int64_t gs = gs0 + s;
+  const int eb = elem_bytes<DT>();
+  // key tile: chunk (col = id % 64, part = id / 64) of 16 bytes
+  {
+    const int per_row = kHeadDim * eb / 16;  // 16 (bf16) or 32 (fp32) chunks
+    for (int id = tid; id < kAsTile * per_row; id += kAsThreads) {
+      const int r = id % kAsTile, part = id / kAsTile;
+      const int64_t i = row0 + r;
+      float vals[8];
+      const int ne = 16 / eb;
+      if (i < n) {
+        const char *src = (const char *)keys + (((int64_t)s * n + i) * kHeadDim) * eb + part * 16;
+        uint4 raw = *(const uint4 *)src;
+        if constexpr (DT == 1) {
+          const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            vals[2 * e] = __uint_as_float(w[e] << 16);
+            vals[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+          }
+        } else {
+          vals[0] = __uint_as_float(raw.x); vals[1] = __uint_as_float(raw.y);
+          vals[2] = __uint_as_float(raw.z); vals[3] = __uint_as_float(raw.w);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) vals[e] = 0.f;
+      }
+      for (int e = 0; e < ne; ++e) Ks[(part * ne + e) * kAsTile + r] = vals[e];
+    }
+    if (tid < kAsTile) {
+      const int64_t i = row0 + tid;
+      kns[tid] = (i < n) ? knorm[(int64_t)s * n_cap + i] : 0.f;
+    }
+  }
+  Top3 top;
+  top.v1 = top.v2 = top.v3 = INFINITY;
+  top.j1 = top.j2 = 0x7fffffff;
+  const int my_r = tid / 4, my_p = tid % 4;  // scan role: key my_r, 16 columns
+  const void *cbase = (const char *)cent_op + (gs * u_cap) * (int64_t)kHeadDim * eb;
+  for (int j0 = 0; j0 < c; j0 += kAsTile) {
+    __syncthreads();
+    const int per_row = kHeadDim * eb / 16;
+    for (int id = tid; id < kAsTile * per_row; id += kAsThreads) {
+      const int r = id % kAsTile, part = id / kAsTile;
+      const int j = j0 + r;
+      float vals[8];
+      const int ne = 16 / eb;
+      if (j < c) {
+        const char *src = (const char *)cbase + ((int64_t)j * kHeadDim) * eb + part * 16;
+        uint4 raw = *(const uint4 *)src;
+        if constexpr (DT == 1) {
+          const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            vals[2 * e] = __uint_as_float(w[e] << 16);
+            vals[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+          }
+        } else {
+          vals[0] = __uint_as_float(raw.x); vals[1] = __uint_as_float(raw.y);
+          vals[2] = __uint_as_float(raw.z); vals[3] = __uint_as_float(raw.w);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) vals[e] = 0.f;
+      }
+      for (int e = 0; e < ne; ++e) Cs[(part * ne + e) * kAsTile + r] = vals[e];
+    }
+    if (tid < kAsTile) c2s[tid] = (j0 + tid < c) ? c2[(int64_t)s * c_cap + j0 + tid] : 0.f;
+    __syncthreads();
+    float acc[4][4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
+#pragma unroll 8
+    for (int k = 0; k < kHeadDim; ++k) {
+      const float4 ka = *(const float4 *)&Ks[k * kAsTile + 4 * ty];
+      const float4 cb = *(const float4 *)&Cs[k * kAsTile + 4 * tx];
+      const float av[4] = {ka.x, ka.y, ka.z, ka.w};
+      const float bv[4] = {cb.x, cb.y, cb.z, cb.w};
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(av[a], bv[b], acc[a][b]);
+    }
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int b = 0; b < 4; ++b)
+        Es[(4 * ty + a) * kEsPitch + 4 * tx + b] = fmaf(-2.f, acc[a][b], c2s[4 * tx + b]);
+    __syncthreads();
+#pragma unroll 4
+    for (int q = 0; q < 16; ++q) {
+      const int col = my_p * 16 + q;
+      const int j = j0 + col;
+      if (j < c) top3_push(top, Es[my_r * kEsPitch + col], j);
+    }
+  }
+  // merge the four column slices of each key (lanes 4r..4r+3 of one warp)
+  top = top3_merge(top, top3_shfl(top, 1));
+  top = top3_merge(top, top3_shfl(top, 2));
+  const int64_t i = row0 + my_r;
+  if (my_p == 0 && i < n) {
+    assign_decide(top, c, kns[my_r], cstat[2 * s], cstat[2 * s + 1], eps, s, i,
+                  &assign[gs * n_cap + i], amb, amb_count, amb_cap, err);
+  }
+}
+
+// Exact settlement of the queued keys: warp per entry.
+template <int DT>
+__device__ __forceinline__ double sqdist64(const void *key_row, const void *cent_row) {
+  double acc = 0.0;
+  for (int j = 0; j < kHeadDim; ++j) {
+    const double diff = __dsub_rn((double)load_elem<DT>(key_row, j),
+                                  (double)load_elem<DT>(cent_row, j));
+    acc = __dadd_rn(acc, __dmul_rn(diff, diff));
+  }
+  return acc;
+}
+
+template <int DT>
+__global__ void k_assign_refine(const void *keys, int64_t n, int32_t c,
+                                const void *cent_op, int32_t u_cap, int32_t *assign,
+                                int64_t n_cap, int64_t gs0, const int4 *amb,
+                                const int32_t *amb_count, int32_t amb_cap,
+                                int64_t *n_refined) {
+  const int lane = threadIdx.x & 31;
+  const int warps = gridDim.x * (blockDim.x / 32);
+  const int w0 = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  const int total = min(*amb_count, amb_cap);
+  if (blockIdx.x == 0 && threadIdx.x == 0) atomicAdd((unsigned long long *)n_refined, (unsigned long long)total);
+  const int eb = elem_bytes<DT>();
+  for (int w = w0; w < total; w += warps) {
+    const int4 e = amb[w];
+    const int s = e.x;
+    const int64_t row = e.y;
+    const int32_t j1 = e.z, j2 = e.w & 0x7fffffff;
+    const bool crowded = (unsigned)e.w >> 31;
+    const int64_t gs = gs0 + s;
+    const char *key_row = (const char *)keys + ((int64_t)s * n + row) * kHeadDim * eb;
+    const char *cb = (const char *)cent_op + gs * u_cap * (int64_t)kHeadDim * eb;
+    double best = INFINITY;
+    int32_t bj = 0x7fffffff;
+    if (!crowded) {
+      if (lane < 2) {
+        bj = lane == 0 ? j1 : j2;
+        best = sqdist64<DT>(key_row, cb + (int64_t)bj * kHeadDim * eb);
+      }
+    } else {
+      for (int j = lane; j < c; j += 32) {
+        const double dj = sqdist64<DT>(key_row, cb + (int64_t)j * kHeadDim * eb);
+        if (dj < best) { best = dj; bj = j; }  // ascending j: keeps lowest on ties
+      }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      const double ob = __shfl_xor_sync(0xffffffffu, best, o);
+      const int32_t oj = __shfl_xor_sync(0xffffffffu, bj, o);
+      if (ob < best || (ob == best && oj < bj)) { best = ob; bj = oj; }
+    }
+    if (lane == 0) assign[gs * n_cap + row] = bj;
+  }
+}
+
+// ---------------------------------------------------------------- stable counting sort
+
+__global__ void k_count_parts(const int32_t *assign, int64_t n, int64_t n_cap,
+                              int32_t c, int32_t c_cap, int parts, int64_t gs0,
+                              int32_t *cnt_part) {
+  extern __shared__ int32_t hist[];
+  const int s = blockIdx.y, p = blockIdx.x;
+  for (int j = threadIdx.x; j < c; j += blockDim.x) hist[j] = 0;
+  __syncthreads();
+  const int64_t lo = n * p / parts, hi = n * (p + 1) / parts;
+  const int32_t *a = assign + (gs0 + s) * n_cap;
+  for (int64_t i = lo + threadIdx.x; i < hi; i += blockDim.x) atomicAdd(&hist[a[i]], 1);
+  __syncthreads();
+  int32_t *out = cnt_part + ((int64_t)s * kMaxParts + p) * c_cap;
+  for (int j = threadIdx.x; j < c; j += blockDim.x) out[j] = hist[j];
+}
+
+// Block-wide exclusive scan of one int per thread (blockDim <= 1024).
+__device__ __forceinline__ int32_t block_excl_scan(int32_t x, int32_t *warp_tot, int32_t *total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int32_t inc = x;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int32_t y = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += y;
+  }
+  if (lane == 31) warp_tot[wid] = inc;
+  __syncthreads();
+  if (wid == 0) {
+    int32_t w = lane < nw ? warp_tot[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    if (lane < nw) warp_tot[lane] = w;  // inclusive warp prefix
+    if (lane == nw - 1 && total) *total = w;
+  }
+  __syncthreads();
+  const int32_t r = inc - x + (wid ? warp_tot[wid - 1] : 0);
+  __syncthreads();
+  return r;
+}
+
+__global__ void __launch_bounds__(1024)
+k_scan_parts(int32_t c, int32_t c_cap, int parts, int32_t *cnt_part,
+             int32_t *count, int32_t *offs) {
+  __shared__ int32_t warp_tot[32];
+  const int s = blockIdx.x;
+  int32_t *cp = cnt_part + (int64_t)s * kMaxParts * c_cap;
+  const int per = (c + blockDim.x - 1) / blockDim.x;
+  const int j0 = threadIdx.x * per;
+  int32_t local = 0;
+  for (int k = 0; k < per; ++k) {
+    const int j = j0 + k;
+    if (j < c) {
+      int32_t tot = 0;
+      for (int p = 0; p < parts; ++p) tot += cp[(int64_t)p * c_cap + j];
+      count[(int64_t)s * c_cap + j] = tot;
+      local += tot;
+    }
+  }
+  int32_t run = block_excl_scan(local, warp_tot, nullptr);
+  for (int k = 0; k < per; ++k) {
+    const int j = j0 + k;
+    if (j < c) {
+      offs[(int64_t)s * c_cap + j] = run;
+      int32_t r2 = run;
+      for (int p = 0; p < parts; ++p) {
+        const int32_t x = cp[(int64_t)p * c_cap + j];
+        cp[(int64_t)p * c_cap + j] = r2;
+        r2 += x;
+      }
+      run = r2;
+    }
+  }
+}
+
+// Each part's tokens are placed by one warp, 32 at a time, in token order:
+// equal clusters within a group of 32 are ranked by lane; the part's running
+// per-cluster offsets live in shared memory.
+__global__ void k_scatter(const int32_t *assign, int64_t n, int64_t n_cap, int32_t c,
+                          int32_t c_cap, int parts, int64_t gs0, const int32_t *cnt_part,
+                          int32_t *perm) {
+  extern __shared__ int32_t off[];
+  const int s = blockIdx.y, p = blockIdx.x;
+  const int32_t *src = cnt_part + ((int64_t)s * kMaxParts + p) * c_cap;
+  for (int j = threadIdx.x; j < c; j += blockDim.x) off[j] = src[j];
+  __syncthreads();
+  if (threadIdx.x >= 32) return;
+  const int lane = threadIdx.x;
+  const int64_t lo = n * p / parts, hi = n * (p + 1) / parts;
+  const int32_t *a = assign + (gs0 + s) * n_cap;
+  int32_t *pm = perm + (gs0 + s) * n_cap;
+  const unsigned lt = (1u << lane) - 1u;
+  for (int64_t base = lo; base < hi; base += 32) {
+    const int64_t i = base + lane;
+    const bool valid = i < hi;
+    const int32_t key = valid ? a[i] : -1 - lane;
+    const unsigned peers = __match_any_sync(0xffffffffu, key);
+    const int leader = __ffs(peers) - 1;
+    const int rank = __popc(peers & lt);
+    int32_t pb = (valid && lane == leader) ? off[key] : 0;
+    pb = __shfl_sync(0xffffffffu, pb, leader);
+    if (valid) pm[pb + rank] = (int32_t)i;
+    __syncwarp();
+    if (valid && lane == leader) off[key] = pb + __popc(peers);
+    __syncwarp();
+  }
+}
+
+// ---------------------------------------------------------------- update
+
+// Warp per cluster, lane per 4 dimensions, members in token order.
+template <int DT>
+__global__ void k_update(const void *keys, int64_t n, int64_t n_cap, int32_t c,
+                         int32_t c_cap, int32_t u_cap, int64_t gs0, const int32_t *perm,
+                         const int32_t *count, const int32_t *offs, float *cent32,
+                         int64_t *n_inexact) {
+  const int s = blockIdx.y;
+  const int lane = threadIdx.x & 31;
+  const int j = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  if (j >= c) return;
+  const int32_t cnt = count[(int64_t)s * c_cap + j];
+  if (cnt == 0) return;  // empty cluster keeps its centroid
+  const int32_t base = offs[(int64_t)s * c_cap + j];
+  const int64_t gs = gs0 + s;
+  const int32_t *pm = perm + gs * n_cap + base;
+  double sum[4];
+  bool slow = (DT == 0);
+  if constexpr (DT == 1) {
+    int64_t acc[4] = {0, 0, 0, 0};
+    int oor = 0;
+    for (int32_t m = 0; m < cnt; ++m) {
+      const int64_t i = pm[m];
+      const uint2 raw = *(const uint2 *)((const uint16_t *)keys + ((int64_t)s * n + i) * kHeadDim + lane * 4);
+      acc[0] += bf16_fixed40((uint16_t)(raw.x & 0xffffu), &oor);
+      acc[1] += bf16_fixed40((uint16_t)(raw.x >> 16), &oor);
+      acc[2] += bf16_fixed40((uint16_t)(raw.y & 0xffffu), &oor);
+      acc[3] += bf16_fixed40((uint16_t)(raw.y >> 16), &oor);
+    }
+    slow = __any_sync(0xffffffffu, oor) != 0;
+    if (!slow) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sum[e] = fixed40_to_double(acc[e]);
+    } else if (lane == 0) {
+      atomicAdd((unsigned long long *)n_inexact, 1ull);
+    }
+  }
+  if (slow) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) sum[e] = 0.0;
+    for (int32_t m = 0; m < cnt; ++m) {
+      const int64_t i = pm[m];
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        sum[e] = __dadd_rn(sum[e], (double)load_elem<DT>(keys, ((int64_t)s * n + i) * kHeadDim + lane * 4 + e));
+    }
+  }
+  float *dst = cent32 + (gs * u_cap + j) * kHeadDim + lane * 4;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) dst[e] = __double2float_rn(__ddiv_rn(sum[e], (double)cnt));
+}
+
+// ---------------------------------------------------------------- pool
+
+// Warp per pool row: row pos of slice s receives token perm[pos].
+template <int DT>
+__global__ void k_pool_build(const void *keys, const void *values, int64_t n, int64_t n_cap,
+                             int64_t gs0, const int32_t *perm, void *pool_k, void *pool_v,
+                             int64_t pool_rows) {
+  const int s = blockIdx.y;
+  const int lane = threadIdx.x & 31;
+  const int64_t pos = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  if (pos >= n) return;
+  const int64_t gs = gs0 + s;
+  const int64_t i = perm[gs * n_cap + pos];
+  constexpr int row_bytes = kHeadDim * elem_bytes<DT>();
+  constexpr int chunks = row_bytes / 16;
+  if (lane < chunks) {
+    const uint4 *ks = (const uint4 *)((const char *)keys + ((int64_t)s * n + i) * row_bytes) + lane;
+    const uint4 *vs = (const uint4 *)((const char *)values + ((int64_t)s * n + i) * row_bytes) + lane;
+    uint4 *kd = (uint4 *)((char *)pool_k + (gs * pool_rows + pos) * row_bytes) + lane;
+    uint4 *vd = (uint4 *)((char *)pool_v + (gs * pool_rows + pos) * row_bytes) + lane;
+    *kd = *ks;
+    *vd = *vs;
+  }
+}
+
+__global__ void k_unit_table(int32_t c, int32_t c_cap, int32_t u_cap, int64_t gs0,
+                             const int32_t *count, const int32_t *offs, int32_t *unit_row,
+                             int32_t *unit_len) {
+  const int s = blockIdx.y;
+  const int j = blockIdx.x * blockDim.x + threadIdx.x;
+  if (j >= c) return;
+  unit_row[(gs0 + s) * u_cap + j] = offs[(int64_t)s * c_cap + j];
+  unit_len[(gs0 + s) * u_cap + j] = count[(int64_t)s * c_cap + j];
+}
+
+// Reset of one layer's decode state after a (re)build.
+__global__ void k_reset_layer(CtxView v, int layer, int32_t c) {
+  const int b = blockIdx.x;
+  const int64_t lb = (int64_t)layer * v.B + b;
+  if (threadIdx.x == 0) {
+    DecState st = {};
+    st.n_clusters = c;
+    st.n_units = c;
+    v.st[lb] = st;
+  }
+  for (int h = 0; h < v.Hkv; ++h) {
+    const int64_t gs = lb * v.Hkv + h;
+    for (int k = threadIdx.x; k < kHeadDim; k += blockDim.x) v.segsum[gs * kHeadDim + k] = 0;
+    if (threadIdx.x == 0) {
+      v.n_sel[gs] = 0;
+      v.n_tok[gs] = 0;
+      v.rng_cum[gs * (int64_t)(v.u_cap + 1)] = 0;
+      v.attn_count[gs] = 0;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- host driver
+
+static int parts_for(int64_t n) {
+  int64_t p = (n + 2047) / 2048;
+  return (int)(p < 1 ? 1 : (p > kMaxParts ? kMaxParts : p));
+}
+
+template <int DT>
+static cudaError_t group_and_pool(const CtxView &v, int layer, const KmeansScratch &ks,
+                                  int64_t n, int32_t c, int64_t gs0, int S,
+                                  cudaStream_t st) {
+  const int parts = parts_for(n);
+  const int c_cap = v.u_cap - v.t_cap;
+  k_count_parts<<<dim3(parts, S), 256, c * sizeof(int32_t), st>>>(
+      v.assign, n, v.n_cap, c, c_cap, parts, gs0, ks.cnt_part);
+  k_scan_parts<<<S, 1024, 0, st>>>(c, c_cap, parts, ks.cnt_part, ks.count, ks.offs);
+  k_scatter<<<dim3(parts, S), 128, c * sizeof(int32_t), st>>>(
+      v.assign, n, v.n_cap, c, c_cap, parts, gs0, ks.cnt_part, v.perm);
+  return cudaGetLastError();
+}
+
+template <int DT>
+static cudaError_t finish_pool(const CtxView &v, int layer, const KmeansScratch &ks,
+                               const void *keys, const void *values, int64_t n, int32_t c,
+                               int64_t gs0, int S, cudaStream_t st) {
+  const int c_cap = v.u_cap - v.t_cap;
+  k_pool_build<DT><<<dim3((unsigned)((n + 7) / 8), S), 256, 0, st>>>(
+      keys, values, n, v.n_cap, gs0, v.perm, v.pool_k, v.pool_v, v.pool_rows);
+  k_unit_table<<<dim3((c + 255) / 256, S), 256, 0, st>>>(c, c_cap, v.u_cap, gs0, ks.count,
+                                                         ks.offs, v.unit_row, v.unit_len);
+  k_reset_layer<<<v.B, 128, 0, st>>>(v, layer, c);
+  return cudaGetLastError();
+}
+
+template <int DT>
+static cudaError_t kmeans_build_t(const CtxView &v, int layer, const KmeansScratch &ks,
+                                  const void *keys, const void *values, int64_t n,
+                                  int32_t c, int32_t iters, cudaStream_t st) {
+  const int S = v.B * v.Hkv;
+  const int64_t gs0 = (int64_t)layer * S;
+  const int c_cap = v.u_cap - v.t_cap;
+  const int64_t amb_cap = (int64_t)S * v.n_cap;
+  static bool attr_done[2] = {false, false};
+  if (!attr_done[DT]) {
+    cudaFuncSetAttribute(k_assign_simt<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAsSmem);
+    attr_done[DT] = true;
+  }
+  k_init_cent<DT><<<dim3(c, S), kHeadDim, 0, st>>>(keys, n, c, ks.init_idx, v.cent32, gs0, v.u_cap);
+  k_key_norms<DT><<<dim3((unsigned)((n + 7) / 8), S), 256, 0, st>>>(keys, n, v.n_cap, ks.knorm);
+  const float eps = 0x1p-15f;  // fp32 FMA dot of 128 terms: 2*gamma_128 < 2^-16
+  for (int it = 0; it < iters; ++it) {
+    cudaMemsetAsync(ks.cstat, 0, sizeof(float) * 2 * S, st);
+    k_prepare_operand<DT><<<dim3((c + 7) / 8, S), 256, 0, st>>>(v.cent32, v.cent_op, c, c_cap,
+                                                               v.u_cap, gs0, ks.c2, ks.cstat);
+    cudaMemsetAsync(ks.amb_count, 0, sizeof(int32_t), st);
+    k_assign_simt<DT><<<dim3((unsigned)((n + kAsTile - 1) / kAsTile), S), kAsThreads, kAsSmem, st>>>(
+        keys, n, c, v.cent_op, v.u_cap, ks.c2, c_cap, ks.knorm, v.n_cap, ks.cstat, eps,
+        v.assign, gs0, ks.amb, ks.amb_count, (int32_t)amb_cap, v.err);
+    k_assign_refine<DT><<<304, 256, 0, st>>>(keys, n, c, v.cent_op, v.u_cap, v.assign, v.n_cap,
+                                             gs0, ks.amb, ks.amb_count, (int32_t)amb_cap,
+                                             ks.n_refined);
+    cudaError_t e = group_and_pool<DT>(v, layer, ks, n, c, gs0, S, st);
+    if (e != cudaSuccess) return e;
+    k_update<DT><<<dim3((c + 7) / 8, S), 256, 0, st>>>(keys, n, v.n_cap, c, c_cap, v.u_cap, gs0,
+                                                       v.perm, ks.count, ks.offs, v.cent32,
+                                                       ks.n_inexact);
+  }
+  cudaMemsetAsync(ks.cstat, 0, sizeof(float) * 2 * S, st);
+  k_prepare_operand<DT><<<dim3((c + 7) / 8, S), 256, 0, st>>>(v.cent32, v.cent_op, c, c_cap,
+                                                             v.u_cap, gs0, ks.c2, ks.cstat);
+  return finish_pool<DT>(v, layer, ks, keys, values, n, c, gs0, S, st);
+}
+
+cudaError_t launch_kmeans_build(const CtxView &v, int layer, const KmeansScratch &ks,
+                                const void *keys, const void *values, int64_t n, int32_t c,
+                                int32_t iters, bool use_tc, cudaStream_t stream) {
+  (void)use_tc;
+  if (v.dtype == 1) return kmeans_build_t<1>(v, layer, ks, keys, values, n, c, iters, stream);
+  return kmeans_build_t<0>(v, layer, ks, keys, values, n, c, iters, stream);
+}
+
+// Teacher-forced index: centroids and assignment given.
+template <int DT>
+__global__ void k_copy_given(const int32_t *assign_in, const float *cent_in, int64_t n,
+                             int32_t c, int64_t n_cap, int32_t u_cap, int64_t gs0,
+                             int32_t *assign, float *cent32, int32_t *err) {
+  const int s = blockIdx.y;
+  const int64_t gs = gs0 + s;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    int32_t a = assign_in[(int64_t)s * n + i];
+    if (a < 0 || a >= c) { set_err(err, kErrInternal); a = 0; }
+    assign[gs * n_cap + i] = a;
+  }
+  for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < (int64_t)c * kHeadDim;
+       k += (int64_t)gridDim.x * blockDim.x)
+    cent32[gs * u_cap * kHeadDim + k] = cent_in[(int64_t)s * c * kHeadDim + k];
+}
+
+template <int DT>
+static cudaError_t load_index_t(const CtxView &v, int layer, const KmeansScratch &ks,
+                                const void *keys, const void *values, int64_t n, int32_t c,
+                                const int32_t *assign, const float *cent, cudaStream_t st) {
+  const int S = v.B * v.Hkv;
+  const int64_t gs0 = (int64_t)layer * S;
+  const int c_cap = v.u_cap - v.t_cap;
+  k_copy_given<DT><<<dim3(64, S), 256, 0, st>>>(assign, cent, n, c, v.n_cap, v.u_cap, gs0,
+                                                v.assign, v.cent32, v.err);
+  cudaMemsetAsync(ks.cstat, 0, sizeof(float) * 2 * S, st);
+  k_prepare_operand<DT><<<dim3((c + 7) / 8, S), 256, 0, st>>>(v.cent32, v.cent_op, c, c_cap,
+                                                             v.u_cap, gs0, ks.c2, ks.cstat);
+  cudaError_t e = group_and_pool<DT>(v, layer, ks, n, c, gs0, S, st);
+  if (e != cudaSuccess) return e;
+  return finish_pool<DT>(v, layer, ks, keys, values, n, c, gs0, S, st);
+}
+
+cudaError_t launch_load_index(const CtxView &v, int layer, const KmeansScratch &ks,
+                              const void *keys, const void *values, int64_t n, int32_t c,
+                              const int32_t *assign, const float *cent, cudaStream_t stream) {
+  if (v.dtype == 1) return load_index_t<1>(v, layer, ks, keys, values, n, c, assign, cent, stream);
+  return load_index_t<0>(v, layer, ks, keys, values, n, c, assign, cent, stream);
+}
+
+}  // namespace lkv

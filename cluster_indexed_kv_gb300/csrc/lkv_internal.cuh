@@ -1,0 +1,179 @@
+// lkv_internal.cuh -- device-side layout and helpers shared by the liblkv
+// translation units (K-means build, decode step, C ABI).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace lkv {
+
+constexpr int kHeadDim = 128;
+constexpr int kMaxGroup = 8;
+constexpr int kMaxParts = 64;      // token parts of the stable counting sort
+constexpr int kAttnChunk = 64;     // tokens per attention work item
+constexpr int kScoreCtasPerHead = 8;
+
+// Error bits recorded on the device and reported by lkv_sync.
+enum : int32_t {
+  kErrCapacity = 1,  // a unit / selection / list capacity would overflow
+  kErrTimeout = 2,   // a bounded device-side wait gave up
+  kErrInternal = 4,  // an invariant check failed
+};
+
+// Decode state of one (layer, sequence).
+struct DecState {
+  int32_t t;           // decode tokens appended so far
+  int32_t win_start;   // first decode position in the local buffer
+  int32_t open_start;  // first decode position of the open segment
+  int32_t n_clusters;  // C
+  int32_t n_units;     // C + n_evicted
+  int32_t n_closed;    // segments closed so far; segment e is unit C + e
+  int32_t n_evicted;   // closed segments that left the buffer
+  int32_t n_forced;
+  int32_t flag;        // this step retrieves
+  float r;             // this step's r_t
+  int32_t seg_slow;    // open segment holds a value outside the exact-sum range
+  int32_t pad;
+};
+
+// Everything a kernel needs to find the context's data. Per-slice arrays are
+// indexed by the global slice gs = (layer * B + b) * Hkv + h; per-sequence
+// arrays by lb = layer * B + b. Strides are in elements.
+struct CtxView {
+  int dtype;          // 0 fp32, 1 bf16
+  int B, Hkv, G, d;
+  int L;              // local buffer tokens
+  int64_t n_cap;      // max prefill rows per slice
+  int32_t t_cap;      // max decode steps
+  int32_t u_cap;      // max units per slice (C_cap + T_cap)
+  int32_t bud_cap;    // max token budget
+  int offload;
+  // pool: prefill rows [0, n_cap) and evicted-segment rows [n_cap, n_cap+t_cap)
+  void *pool_k, *pool_v;      // slice stride pool_rows * d (HBM or pinned host)
+  int64_t pool_rows;
+  // decode region (local buffer rows), decode position t at row t
+  void *dec_k, *dec_v;        // slice stride dec_rows * d
+  int64_t dec_rows;
+  void *stage_k, *stage_v;    // offload only: [slice][bud_cap][d]
+  void *cent_op;              // [slice][u_cap][d] scoring operand (dtype)
+  float *cent32;              // [slice][u_cap][d]
+  int32_t *unit_row;          // [slice][u_cap]
+  int32_t *unit_len;          // [slice][u_cap]
+  int32_t *assign;            // [slice][n_cap]
+  int32_t *perm;              // [slice][n_cap]
+  DecState *st;               // [lb]
+  void *q_prev;               // [lb][H][d] (dtype)
+  int64_t *segsum;            // [slice][d] exact fixed-point sums (bf16) or
+                              // doubles reinterpreted (fp32)
+  float *scores;              // [slice][u_cap]
+  int32_t *sel;               // [slice][u_cap] selected unit ids, ascending
+  int32_t *n_sel;             // [slice]
+  int32_t *n_tok;             // [slice]
+  int32_t *rng_row;           // [slice][u_cap] first row of each selected unit
+  int32_t *rng_cum;           // [slice][u_cap + 1] exclusive token prefix
+  float *part_acc;            // [slice][max_chunks][G][d]
+  float *part_ml;             // [slice][max_chunks][G][2]
+  int32_t *attn_count;        // [slice]
+  int32_t max_chunks;
+  int32_t *err;               // device error bits (shared by all layers)
+};
+
+// ---------------------------------------------------------------- helpers
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) {
+  return __uint_as_float(((uint32_t)b) << 16);
+}
+
+__device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+template <int DT>
+__device__ __forceinline__ float load_elem(const void *p, int64_t i) {
+  if constexpr (DT == 1) return bf16_bits_to_f32(((const uint16_t *)p)[i]);
+  else return ((const float *)p)[i];
+}
+
+template <int DT>
+__device__ __forceinline__ void store_elem(void *p, int64_t i, float v) {
+  if constexpr (DT == 1) ((uint16_t *)p)[i] = f32_to_bf16_bits(v);
+  else ((float *)p)[i] = v;
+}
+
+template <int DT>
+constexpr int elem_bytes() { return DT == 1 ? 2 : 4; }
+
+// Monotone map of a float (with -0 folded onto +0) to uint32 such that a
+// larger score gives a SMALLER key: ascending key order = descending score.
+__device__ __forceinline__ uint32_t desc_key(float s) {
+  uint32_t b = __float_as_uint(s == 0.0f ? 0.0f : s);
+  uint32_t asc = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  return ~asc;
+}
+
+// Exact fixed-point accumulation of bf16 values: v * 2^40 as int64 is exact
+// for 2^-33 <= |v| < 32 (biased exponent 94..131) and the sum of up to 2^18
+// such terms cannot overflow. Values outside that range (other than zero)
+// set *slow so the caller can fall back to double-precision token-order sums.
+__device__ __forceinline__ int64_t bf16_fixed40(uint16_t bits, int *slow) {
+  uint32_t e = (bits >> 7) & 0xffu;
+  uint32_t m = bits & 0x7fu;
+  if (e == 0 && m == 0) return 0;
+  if (e < 94u || e > 131u) { *slow = 1; return 0; }
+  int64_t mag = (int64_t)(128u + m) << (e - 94u);
+  return (bits & 0x8000u) ? -mag : mag;
+}
+
+__device__ __forceinline__ double fixed40_to_double(int64_t v) {
+  // one correctly rounded conversion, then an exact power-of-two scale
+  return __ll2double_rn(v) * 0x1p-40;
+}
+
+__device__ __forceinline__ void set_err(int32_t *err, int32_t bits) {
+  atomicOr(err, bits);
+}
+
+// ---------------------------------------------------------------- launchers
+
+struct KmeansScratch {
+  float *knorm;        // [S][n_cap]
+  float *c2;           // [S][c_cap]
+  float *cstat;        // [S][2]: max |c|, max |c|^2
+  int32_t *cnt_part;   // [S][kMaxParts][c_cap] counts, then running offsets
+  int32_t *count;      // [S][c_cap]
+  int32_t *offs;       // [S][c_cap]
+  int4 *amb;           // [S * n_cap] ambiguous assignments
+  int32_t *amb_count;  // [1]
+  int64_t *n_refined;  // [1] running total
+  int64_t *n_inexact;  // [1] running total
+  int64_t *init_idx;   // [S][c_cap]
+};
+
+// K-means build of one layer (all slices). keys/values: [S][n][d] device.
+cudaError_t launch_kmeans_build(const CtxView &v, int layer, const KmeansScratch &ks,
+                                const void *keys, const void *values, int64_t n,
+                                int32_t c, int32_t iters, bool use_tc,
+                                cudaStream_t stream);
+// Pool and unit table from a given assignment and fp32 centroids.
+cudaError_t launch_load_index(const CtxView &v, int layer, const KmeansScratch &ks,
+                              const void *keys, const void *values, int64_t n,
+                              int32_t c, const int32_t *assign,
+                              const float *cent, cudaStream_t stream);
+
+struct StepArgs {
+  const void *q, *k_new, *v_new;   // [B][nl][H][d], [B][nl][Hkv][d]
+  float tau;
+  int32_t budget;
+  float *out;                      // [B][nl][H][d]
+  int32_t *selected_units;         // [B][nl][Hkv][u_cap] or null
+  int32_t *n_selected;             // [B][nl][Hkv] or null
+  uint8_t *boundary;               // [B][nl] or null
+  float *r_out;                    // [B][nl] or null
+  int32_t l0;                      // first layer of this call
+  int32_t nl;                      // layers in this call
+};
+
+cudaError_t launch_decode_step(const CtxView &v, const StepArgs &a, cudaStream_t stream);
+
+}  // namespace lkv

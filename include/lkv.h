@@ -1,0 +1,203 @@
+/*
+ * lkv.h -- C ABI of liblkv, a single-GPU (GB300, sm_103a) implementation of
+ * the data-parallel hot path of LouisKV-style KV-cache retrieval.
+ *
+ * Sources, cited by page title and section:
+ *   [LouisKV notes]  "LouisKV: Efficient KV Cache Retrieval for Long
+ *                    Input-Output Sequences" (papernotes.org summary):
+ *                    方法详解/整体框架 (flowchart), 关键设计 1-3.
+ *   [LouisKV blog]   "LouisKV: A New Approach to Efficient KV Cache Management
+ *                    for Long Language Model Sequences": "Semantic-Aware
+ *                    Adaptive Retrieval", "Decoupled Fine-Grained Management".
+ *   [ParisKV]        "ParisKV" technical summary (gist.science): 系统级创新 1
+ *                    (UVA offload: kernels fetch the chosen KV rows from host
+ *                    memory directly).
+ *
+ * Conventions shared by every call:
+ *   - d (head_dim) is 128. Query head h belongs to KV head h / group.
+ *   - dtype LKV_DTYPE_BF16: keys, values and queries are bfloat16 (2 bytes,
+ *     the upper half of an IEEE binary32); LKV_DTYPE_FP32: binary32.
+ *     Accumulation is fp32 (attention, scores) or exact (centroid sums).
+ *   - Pointers named "device" must be CUDA device (or managed) memory,
+ *     readable by the current device; "host" pointers are ordinary host
+ *     memory. The caller keeps ownership of everything it passes; the library
+ *     copies what it needs to keep (keys and values into its own pool).
+ *   - Calls that take device pointers are stream-ordered on the context's
+ *     stream and return before the GPU work finishes; only lkv_sync,
+ *     lkv_get_index and lkv_get_decode_state block.
+ *   - Errors: every call returns an lkv_status; nothing is thrown across the
+ *     ABI. lkv_last_error gives a one-line description. A device-side
+ *     anomaly (capacity exceeded, a bounded wait that ran out) is recorded in
+ *     the context and reported by the next lkv_sync as LKV_ECUDA /
+ *     LKV_ECAPACITY / LKV_ETIMEOUT; a CUDA launch or runtime error is
+ *     LKV_ECUDA and leaves the context unusable (LKV_ESTATE afterwards).
+ */
+#ifndef LKV_H
+#define LKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  LKV_OK = 0,
+  LKV_EINVAL = 1,     /* bad argument, null pointer, shape outside the context */
+  LKV_ENOMEM = 2,     /* device or pinned host allocation failed */
+  LKV_ECUDA = 3,      /* CUDA runtime / launch error */
+  LKV_ECAPACITY = 4,  /* more decode steps / units than the context was sized for */
+  LKV_ESTATE = 5,     /* call out of order (decode before index) or broken context */
+  LKV_ETIMEOUT = 6    /* a device-side bounded wait gave up */
+} lkv_status;
+
+typedef enum { LKV_DTYPE_FP32 = 0, LKV_DTYPE_BF16 = 1 } lkv_dtype;
+
+typedef struct lkv_config {
+  int32_t batch;        /* B sequences decoded together */
+  int32_t n_layers;     /* attention layers with their own index and state */
+  int32_t n_kv_heads;   /* H_kv */
+  int32_t group;        /* G query heads per KV head (GQA), 1..8 */
+  int32_t head_dim;     /* d; must be 128 */
+  int32_t dtype;        /* lkv_dtype */
+  int32_t local_buf;    /* L: tokens of the GPU local buffer of recent output
+                           segments [LouisKV notes, 关键设计 2] */
+  int32_t max_clusters; /* largest C a build may ask for */
+  int64_t max_prefill;  /* largest N (prefill tokens per sequence), <= 2^18 */
+  int32_t max_steps;    /* decode steps each layer may take */
+  int32_t max_budget;   /* largest token budget a decode call may pass */
+  int32_t offload;      /* 0: K/V pool in HBM. 1: prefill rows and evicted
+                           segments in pinned host memory, read by the GPU
+                           through unified virtual addressing [ParisKV, UVA
+                           offload]; centroids and the local buffer stay in HBM */
+  void *stream;         /* cudaStream_t for all work; NULL = legacy stream */
+} lkv_config;
+
+typedef struct lkv_ctx lkv_ctx;
+
+/* Allocate a context sized by *cfg (device memory for the pool, index,
+ * decode state and scratch; pinned host memory for the offloaded pool).
+ * Ownership: the caller owns *cfg; the context owns everything it allocates
+ * and frees it in lkv_destroy. Errors: LKV_EINVAL (shape), LKV_ENOMEM,
+ * LKV_ECUDA. */
+lkv_status lkv_create(const lkv_config *cfg, lkv_ctx **out);
+void lkv_destroy(lkv_ctx *ctx);
+
+/* Prefill index build for one layer [LouisKV notes, 关键设计 2; LouisKV blog,
+ * Prefill Stage]: for every (sequence, KV head), K-means over its n_tokens
+ * keys with n_clusters clusters and exactly `iters` Lloyd rounds (no early
+ * stop); each cluster's centroid is the mean of its member keys and becomes
+ * the retrieval index of a unit made of those tokens. The K/V rows are then
+ * copied into the pool, grouped by cluster. Resets the layer's decode state.
+ *
+ * keys, values: device, [B][H_kv][n_tokens][d] in the context dtype.
+ * Initialisation: slice s = b*H_kv + h takes as initial centroids the keys at
+ * the first n_clusters indices of a partial Fisher-Yates shuffle of
+ * [0, n_tokens) driven by the splitmix64 sequence seeded with seed + s.
+ * Assignment: argmin of the squared Euclidean distance, evaluated exactly
+ * (double precision, index order) wherever the fast tensor-core distance
+ * cannot separate the two best centroids; ties go to the lowest cluster id.
+ * Centroid arithmetic: member sum exact (or double, token order), divided in
+ * double, rounded once to fp32; an empty cluster keeps its centroid. For
+ * bf16, the scoring operand is the centroid rounded to bf16.
+ * Errors: LKV_EINVAL (layer, sizes above the context capacities,
+ * n_clusters > n_tokens, iters < 1), LKV_ECUDA. */
+lkv_status lkv_build_index(lkv_ctx *ctx, int32_t layer, const void *keys,
+                           const void *values, int64_t n_tokens,
+                           int32_t n_clusters, int32_t iters, uint64_t seed);
+
+/* Teacher-forced index: same as lkv_build_index but with the assignment and
+ * fp32 centroids given instead of computed (for parity runs from an external
+ * index). assign: device int32 [B][H_kv][n_tokens], values in [0, n_clusters);
+ * centroids: device fp32 [B][H_kv][n_clusters][d]. */
+lkv_status lkv_load_index(lkv_ctx *ctx, int32_t layer, const void *keys,
+                          const void *values, int64_t n_tokens,
+                          int32_t n_clusters, const int32_t *assign,
+                          const float *centroids);
+
+/* One decode step for layers [layer, layer + n_layers), every sequence
+ * [LouisKV notes, flowchart and 关键设计 1-3]. Per (sequence, layer):
+ *  1. r_t = (1/H) sum_h cos(q_{t-1}^h, q_t^h); retrieval triggers at t = 0
+ *     or when r_t < tau. r_t is evaluated in fp32: per head dot and squared
+ *     norms by fused multiply-add in index order, cos = dot / (sqrt(|a|^2) *
+ *     sqrt(|b|^2)) (0 when that is 0), head cosines added in head order.
+ *  2. On a trigger the open output segment closes; token t opens the next.
+ *  3. While the local buffer cannot take token t (it holds L tokens), its
+ *     oldest closed segment is evicted into the pool as a new unit whose
+ *     index is the mean of its keys (per KV head); with no closed segment
+ *     left the open segment is cut and evicted.
+ *  4. k_new/v_new of token t enter the local buffer.
+ *  5. On a trigger, per KV head (group-consistent selection), every unit is
+ *     scored with s_u = qbar . c_u, qbar = sum of the group's query heads
+ *     (fp32 adds in head order), the dot by fp32 fused multiply-add in index
+ *     order; units are taken in (score desc, id asc) order while their token
+ *     total stays <= budget, stopping at the first that does not fit.
+ *     Without a trigger the previous selection is reused unchanged.
+ *  6. out = softmax(q K^T / sqrt(d)) V over the selected units' tokens and
+ *     the local buffer (fp32 accumulate).
+ * q: device [B][n_layers][H][d]; k_new, v_new: device [B][n_layers][H_kv][d]
+ * (context dtype); tau: threshold; budget: tokens per (sequence, layer, KV
+ * head), 0..max_budget; local_buf must equal the context's L.
+ * Outputs (device; any may be NULL except out):
+ *   out            fp32 [B][n_layers][H][d]
+ *   selected_units int32 [B][n_layers][H_kv][max_clusters + max_steps]:
+ *                  the active selection, ascending unit id (clusters are
+ *                  units 0..C-1, evicted segments C, C+1, ... in eviction
+ *                  order); entries past n_selected are left untouched
+ *   n_selected     int32 [B][n_layers][H_kv]
+ *   boundary       uint8 [B][n_layers]: 1 where this step retrieved
+ *   r_out          fp32  [B][n_layers]: r_t (0 at t = 0)
+ * Errors: LKV_EINVAL, LKV_ESTATE (layer has no index), LKV_ECAPACITY (layer
+ * already took max_steps steps), LKV_ECUDA. */
+lkv_status lkv_decode_step(lkv_ctx *ctx, int32_t layer, int32_t n_layers,
+                           const void *q, const void *k_new, const void *v_new,
+                           float tau, int32_t budget, int32_t local_buf,
+                           float *out, int32_t *selected_units,
+                           int32_t *n_selected, uint8_t *boundary,
+                           float *r_out);
+
+/* Copy one (layer, sequence, KV head) index to host memory (blocks until the
+ * context's stream is idle). Any output pointer may be NULL.
+ *   centroids host fp32 [capacity][d]: units 0..n_units-1 (clusters, then
+ *             evicted segments); unit_len, unit_row host int32 [capacity]:
+ *             token count and first pool row of each unit (cluster rows are
+ *             contiguous in the pool; segment rows start at max_prefill + the
+ *             segment's first decode position); assign host int32 [n_tokens]
+ *             (cluster of each prefill token); perm host int32 [n_tokens]:
+ *             prefill token stored at pool row i.
+ * *n_units receives the number of units; LKV_ECAPACITY if it exceeds
+ * capacity (nothing copied). */
+lkv_status lkv_get_index(lkv_ctx *ctx, int32_t layer, int32_t seq,
+                         int32_t kv_head, int32_t capacity, float *centroids,
+                         int32_t *unit_len, int32_t *unit_row, int32_t *assign,
+                         int32_t *perm, int32_t *n_units);
+
+typedef struct lkv_decode_state {
+  int32_t t;            /* decode tokens appended so far */
+  int32_t win_start;    /* first decode position held in the local buffer */
+  int32_t open_start;   /* first decode position of the open segment */
+  int32_t n_clusters;   /* C */
+  int32_t n_units;      /* C + evicted segments (selectable units) */
+  int32_t n_closed;     /* segments closed so far (evicted or not) */
+  int32_t n_evicted;
+  int32_t n_forced;     /* segments cut because the buffer filled */
+  int64_t n_refined;    /* K-means assignments settled in double precision */
+  int64_t n_inexact;    /* centroid sums that needed the double fallback */
+} lkv_decode_state;
+
+/* Blocking read of one (layer, sequence) decode state. */
+lkv_status lkv_get_decode_state(lkv_ctx *ctx, int32_t layer, int32_t seq,
+                                lkv_decode_state *out);
+
+/* Wait for the context's stream; report device-side anomalies. */
+lkv_status lkv_sync(lkv_ctx *ctx);
+
+/* Text of the last error on this context ("" if none); valid until the next
+ * call on the context. NULL ctx: the last lkv_create failure. */
+const char *lkv_last_error(const lkv_ctx *ctx);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

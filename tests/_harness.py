@@ -1,0 +1,122 @@
+"""Shared helpers of the GPU parity tests: drive liblkv through its C ABI on
+seeded synthetic inputs and run the oracle on the very same tensors."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import synth
+
+ATOL, RTOL = 2e-3, 1e-2   # attention outputs: bf16 in, fp32 accumulate
+
+
+def make_ctx(w: synth.Workload, max_steps=None, max_budget=None):
+    import cluster_indexed_kv_gb300 as lkv
+    return lkv.Context(batch=w.batch, n_layers=w.n_layers, n_kv_heads=w.n_kv_heads,
+                       group=w.group, dtype=w.torch_dtype, local_buf=w.local_buf,
+                       max_clusters=w.n_clusters, max_prefill=w.n_prefill,
+                       max_steps=max_steps or w.n_steps, max_budget=max_budget or w.budget,
+                       offload=w.offload)
+
+
+def gpu_index(ctx, layer, b, h, n):
+    return ctx.get_index(layer, b, h, n)
+
+
+def run_decode(ctx, w, q, kn, vn, *, tau=None, budget=None, keep_sel=True, layers=None):
+    """Drive T decode steps (all sequences, the given layers in one call each
+    step). Returns host arrays: out [T,B,nl,H,d], boundary [T,B,nl], r [T,B,nl],
+    n_sel [T,B,nl,Hkv] and, with keep_sel, sel: dict (t, b, li, h) -> sorted ids
+    for boundary steps and t = 0."""
+    tau = w.tau if tau is None else tau
+    budget = w.budget if budget is None else budget
+    T, B, nl = q.shape[0], q.shape[1], q.shape[2]
+    l0 = 0 if layers is None else layers[0]
+    dev = q.device
+    H, Hkv = w.n_heads, w.n_kv_heads
+    out = torch.empty(T, B, nl, H, 128, dtype=torch.float32, device=dev)
+    bnd = torch.zeros(T, B, nl, dtype=torch.uint8, device=dev)
+    r = torch.zeros(T, B, nl, dtype=torch.float32, device=dev)
+    nsel = torch.zeros(T, B, nl, Hkv, dtype=torch.int32, device=dev)
+    K = 32
+    ring = torch.full((K, B, nl, Hkv, ctx.u_cap), -1, dtype=torch.int32, device=dev)
+    sel = {}
+
+    def drain(t0, t1):
+        b_h = bnd[t0:t1].cpu().numpy()
+        n_h = nsel[t0:t1].cpu().numpy()
+        rg = ring.cpu().numpy()
+        for t in range(t0, t1):
+            for b in range(B):
+                for li in range(nl):
+                    if b_h[t - t0, b, li]:
+                        for h in range(Hkv):
+                            k = n_h[t - t0, b, li, h]
+                            sel[(t, b, li, h)] = np.sort(rg[t % K, b, li, h, :k])
+
+    for t in range(T):
+        ctx.decode_step(l0, q[t], kn[t], vn[t], tau, budget, out[t], n_layers=nl,
+                        selected_units=ring[t % K] if keep_sel else None,
+                        n_selected=nsel[t], boundary=bnd[t], r_out=r[t])
+        if keep_sel and (t % K == K - 1 or t == T - 1):
+            drain(t - (t % K), t + 1)
+    ctx.sync()
+    return dict(out=out.cpu().numpy(), boundary=bnd.cpu().numpy(), r=r.cpu().numpy(),
+                n_sel=nsel.cpu().numpy(), sel=sel)
+
+
+def oracle_decode(w, K, V, idx, q, kn, vn, b, li, *, layer=None, tau=None, budget=None,
+                  attn_mask=None):
+    """Oracle run of sequence b, call-layer li, teacher-forced from idx: a list
+    over kv heads of dicts with 'assign' and 'centroids' (fp32, clusters first)."""
+    tau = w.tau if tau is None else tau
+    budget = w.budget if budget is None else budget
+    C = w.n_clusters
+    assign = np.stack([idx[h]["assign"] for h in range(w.n_kv_heads)])
+    cent = np.stack([idx[h]["centroids"][:C] for h in range(w.n_kv_heads)])
+    return oracle.decode(synth.to_oracle(K[b]), synth.to_oracle(V[b]), assign, cent,
+                         synth.to_oracle(q[:, b, li]), synth.to_oracle(kn[:, b, li]),
+                         synth.to_oracle(vn[:, b, li]), n_clusters=C, local_buf=w.local_buf,
+                         tau=tau, budget=budget, attn_mask=attn_mask, want_seg_cent=True)
+
+
+def compare_decode(g, o, w, b, li, *, attn_mask=None, check_sel=True):
+    """Bit-exact decisions, tolerance on attention. Returns a short report."""
+    T = o["flag"].shape[0]
+    Hkv = w.n_kv_heads
+    bnd = g["boundary"][:, b, li]
+    assert np.array_equal(bnd, o["flag"]), f"boundary flags differ at {np.flatnonzero(bnd != o['flag'])[:10]}"
+    rg = g["r"][:, b, li]
+    assert np.array_equal(rg.view(np.uint32), o["r32"].view(np.uint32)), "r_t differs"
+    assert np.array_equal(g["n_sel"][:, b, li], o["n_sel"]), "n_selected differs"
+    if check_sel:
+        for t in np.flatnonzero(o["flag"]):
+            for h in range(Hkv):
+                k = o["n_sel"][t, h]
+                want = np.sort(o["sel"][t, h, :k])
+                assert np.array_equal(g["sel"][(t, b, li, h)], want), f"selection differs t={t} h={h}"
+    steps = np.arange(T) if attn_mask is None else np.flatnonzero(attn_mask)
+    got = g["out"][steps, b, li].astype(np.float64)
+    want = o["out"][steps]
+    err = np.abs(got - want)
+    ok = err <= ATOL + RTOL * np.abs(want)
+    assert ok.all(), f"attention mismatch: max abs err {err.max():.3e}"
+    return dict(max_abs_err=float(err.max()), n_boundary=int(o["flag"].sum()),
+                n_evicted=o["n_evicted"], n_forced=o["n_forced"])
+
+
+def compare_segments(ctx, w, o, b, li, layer):
+    """Evicted segments: same order, start, length and index vector."""
+    st = ctx.decode_state(layer, b)
+    assert st["n_evicted"] == o["n_evicted"], (st["n_evicted"], o["n_evicted"])
+    assert st["n_forced"] == o["n_forced"]
+    C = w.n_clusters
+    for h in range(w.n_kv_heads):
+        ix = ctx.get_index(layer, b, h, w.n_prefill)
+        assert ix["n_units"] == C + o["n_evicted"]
+        seg_row = ix["unit_row"][C:] - w.n_prefill
+        assert np.array_equal(seg_row, o["seg_start"])
+        assert np.array_equal(ix["unit_len"][C:], o["seg_len"])
+        assert np.array_equal(ix["centroids"][C:].view(np.uint32),
+                              o["seg_cent"][:, h].view(np.uint32))
