@@ -1,0 +1,390 @@
+"""Benchmark: LouisKV-style retrieval decode at 32K input, batch 8, on one GB300.
+
+One bench step = one pass of the whole hot path over one batch: the prefill
+index build (K-means, 20 Lloyd rounds, C = 2048, N = 32768 keys per
+(sequence, KV head), 8 sequences x 8 KV heads) followed by T = 8192 decode
+steps (boundary test, segment/eviction bookkeeping, group scoring and budget
+selection on triggers, sparse attention every step) of all 8 sequences.
+
+Printed (one JSON line, rank 0): value = decode steps/s (one decode step =
+all 8 sequences advance one token), k-means Mkeys/s, the attention kernel's
+HBM roofline fraction, the oracle timed on the host cores, an end-to-end
+number through the C ABI with host buffers, and the SM clocks seen.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--decode-steps T] [--iters I]
+Under torchrun (N > 1) every rank runs an independent replica (weak scaling,
+no collective on the data path); rank 0 prints the aggregate.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode steps/s (retrieval+sparse attn) @32K, B=8; k-means Mkeys/s; % HBM roofline"
+UNIT = "decode steps/s"
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=3)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--decode-steps", type=int, default=None)
+    p.add_argument("--iters", type=int, default=None)
+    p.add_argument("--profile-steps", type=int, default=512)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args(argv)
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def workload(args):
+    import synth
+    w = synth.WORKLOADS["b8_32k"]
+    if args.decode_steps:
+        w = w.replace(n_steps=args.decode_steps)
+    if args.iters:
+        w = w.replace(iters=args.iters)
+    return w
+
+
+def config_of(w, world):
+    return {"workload": f"{w.name}: B={w.batch}, N={w.n_prefill}, C={w.n_clusters}, "
+                        f"iters={w.iters}, T={w.n_steps}, tau={w.tau}, budget={w.budget}, "
+                        f"L={w.local_buf}, H_kv={w.n_kv_heads}x{w.group}, d={w.head_dim}, "
+                        f"jump_p={w.jump_p}",
+            "batch_per_gpu": w.batch, "prefill_tokens": w.n_prefill, "decode_steps": w.n_steps,
+            "parallelism": f"replicas x{world}",
+            "l2": "inputs larger than L2 between timed steps (1.07 GB prefill K/V, "
+                  f"{w.n_steps * w.batch * (w.n_heads + 2 * w.n_kv_heads) * 256 / 1e9:.2f} GB decode "
+                  "inputs); the roofline pass writes 256 MB before every decode step"}
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index=0):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = None
+
+    def start(self):
+        try:
+            self.out = open(os.path.join("/tmp", f"lkv_clocks_{os.getpid()}.csv"), "w+")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.seek(0)
+        rows = [r.split(",") for r in self.out.read().strip().splitlines() if r.strip()]
+        self.out.close()
+        try:
+            os.unlink(self.out.name)
+        except OSError:
+            pass
+        if not rows:
+            return None
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [v for v in (num(r[1]) for r in rows if len(r) > 1) if v is not None]
+        mx = [v for v in (num(r[2]) for r in rows if len(r) > 2) if v is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4)
+                          if len(r) > 5 + i and r[5 + i].strip() == "Active"})
+        load = [s for s in sm if s > 0.5 * max(sm)] if sm else []
+        return {"sm_mhz": statistics.median(load) if load else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- oracle samples
+
+def oracle_decode_sample(K0, V0, idx, q, kn, vn, w, n_steps, head=0):
+    """Seconds per (sequence, KV head) decode step of the oracle, timed on one
+    KV head of sequence 0 over n_steps steps (K0, V0: [H_kv, N, d])."""
+    import numpy as np
+    import oracle
+    import synth
+    h = head
+    g0, g1 = h * w.group, (h + 1) * w.group
+    keys = synth.to_oracle(K0[h:h + 1])
+    vals = synth.to_oracle(V0[h:h + 1])
+    qq = synth.to_oracle(q[:n_steps, 0, 0, g0:g1])
+    kk = synth.to_oracle(kn[:n_steps, 0, 0, h:h + 1])
+    vv = synth.to_oracle(vn[:n_steps, 0, 0, h:h + 1])
+    assign = np.ascontiguousarray(idx["assign"][None])
+    cent = np.ascontiguousarray(idx["centroids"][None, :w.n_clusters])
+    t0 = time.perf_counter()
+    oracle.decode(keys, vals, assign, cent, qq, kk, vv, n_clusters=w.n_clusters,
+                  local_buf=w.local_buf, tau=w.tau, budget=w.budget)
+    return (time.perf_counter() - t0) / n_steps
+
+
+def oracle_kmeans_sample(keys_bits, c, n_keys):
+    """Seconds for one Lloyd round of the oracle on n_keys keys, c clusters."""
+    import numpy as np
+    import oracle
+    keys = np.ascontiguousarray(keys_bits[:n_keys])
+    cent = oracle.bf16_bits_to_f32(keys_bits[:c]).astype(np.float32)
+    t0 = time.perf_counter()
+    a = oracle.assign(keys, oracle.operand(cent, oracle.BF16))
+    oracle.update(keys, a, cent)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(K, V, idx0, q, kn, vn, w, n_steps=48, kmeans_keys=1024):
+    import synth
+    per = oracle_decode_sample(K[0].cpu(), V[0].cpu(), idx0, q, kn, vn, w, n_steps)
+    steps_per_s = 1.0 / (per * w.batch * w.n_kv_heads)
+    km = oracle_kmeans_sample(synth.to_oracle(K[0, 0]), w.n_clusters, kmeans_keys)
+    return {"value": steps_per_s, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"single-threaded C oracle: 1 (sequence, KV head) x {n_steps} decode steps "
+                      f"of the full-size workload (teacher-forced from the GPU index), scaled by "
+                      f"B x H_kv = {w.batch * w.n_kv_heads}; k-means: one Lloyd round of "
+                      f"{kmeans_keys} keys x {w.n_clusters} clusters",
+            "kmeans_mkeys_per_s": kmeans_keys / km / 1e6}
+
+
+# ---------------------------------------------------------------- our arm
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def run_ours(args, rank, world, local):
+    import torch
+    import synth
+    import cluster_indexed_kv_gb300 as lkv
+
+    torch.cuda.set_device(local)
+    lkv.build()
+    w = workload(args)
+    T = w.n_steps
+    dev = "cuda"
+    K, V = synth.prefill(w, 0, dev)
+    q, kn, vn, _ = synth.decode_inputs(w, dev, n_steps=T)
+    prof_T = min(args.profile_steps, T)
+    ctx = lkv.Context(batch=w.batch, n_layers=1, n_kv_heads=w.n_kv_heads, group=w.group,
+                      dtype=w.torch_dtype, local_buf=w.local_buf, max_clusters=w.n_clusters,
+                      max_prefill=w.n_prefill, max_steps=T, max_budget=w.budget)
+    stream = ctx.stream
+    out = torch.empty(T, w.batch, 1, w.n_heads, 128, device=dev)
+    bnd = torch.zeros(T, w.batch, 1, dtype=torch.uint8, device=dev)
+    ev = {}
+
+    def one_step():
+        ctx.build_index(0, K, V, w.n_clusters, w.iters, 1)
+        ev["mid"].record(stream)
+        ctx.decode_steps(0, q, kn, vn, w.tau, w.budget, out, boundary=bnd)
+
+    ev["mid"] = torch.cuda.Event(enable_timing=True)
+    for _ in range(args.warmup):
+        one_step()
+    ctx.sync()
+    ctx.profile(reset=True)
+    dist = world > 1 and torch.distributed.is_initialized()
+    if dist:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    build_ms = dec_ms = 0.0
+    t_wall = time.perf_counter()
+    for _ in range(args.steps):
+        e0 = torch.cuda.Event(enable_timing=True)
+        ev["mid"] = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        one_step()
+        e1.record(stream)
+        e1.synchronize()
+        build_ms += e0.elapsed_time(ev["mid"])
+        dec_ms += ev["mid"].elapsed_time(e1)
+    torch.cuda.synchronize()
+    if dist:
+        torch.distributed.barrier()
+    wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    kern, _ = ctx.profile(reset=True)
+    launches = int(sum(v[0] for v in kern.values()))
+    trig = float(bnd.float().mean().item())
+    st = ctx.decode_state(0, 0)
+    times = torch.tensor([build_ms, dec_ms, wall * 1e3], dtype=torch.float64, device=dev)
+    if dist:
+        torch.distributed.all_reduce(times, op=torch.distributed.ReduceOp.MAX)
+    build_ms, dec_ms, wall_ms = times.tolist()
+    K_steps = args.steps
+    value = world * T * K_steps / (dec_ms / 1e3)
+    mkeys = world * w.batch * w.n_kv_heads * w.n_prefill * w.iters * K_steps / (build_ms / 1e3) / 1e6
+
+    # ---- roofline pass: single-step launches, L2 overwritten before every
+    # step, CUDA events around every kernel on the context stream
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    ctx.build_index(0, K, V, w.n_clusters, w.iters, 1)
+    ctx.set_profiling(True)
+    ctx.profile(reset=True)
+    for t in range(prof_T):
+        flush.fill_(float(t))
+        ctx.decode_step(0, q[t], kn[t], vn[t], w.tau, w.budget, out[t], boundary=bnd[t])
+    kern_p, ctr = ctx.profile(reset=True)
+    ctx.set_profiling(False)
+    hbm_peak, peak_kind = peaks()
+    n_attn, ms_attn = kern_p["lkv_attn"]
+    slices = ctr["attn_slices"]
+    eb = 2 if w.dtype == "bf16" else 4
+    alg_bytes = (ctr["attn_rows"] * 2 * 128 * eb + slices * w.group * 128 * (eb + 4)) / max(n_attn, 1)
+    attn_s = ms_attn / max(n_attn, 1) / 1e3
+    achieved = alg_bytes / attn_s / 1e9
+    breakdown = {k: {"launches": int(v[0]), "avg_us": round(v[1] / v[0] * 1e3, 2)}
+                 for k, v in kern_p.items() if v[0]}
+
+    result = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K_steps,
+        "warmup": args.warmup, "ms_per_step": wall_ms / K_steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": config_of(w, world),
+        "tokens_per_s": value * w.batch,
+        "kmeans_mkeys_per_s": mkeys,
+        "decode_ms_per_bench_step": dec_ms / K_steps, "build_ms_per_bench_step": build_ms / K_steps,
+        "trigger_rate": trig, "kmeans_refined_keys_total": st["n_refined"],
+        "roofline": {"kernel": "lkv_attn", "bound": "hbm", "achieved": achieved, "peak": hbm_peak,
+                     "unit": "GB/s", "frac": achieved / hbm_peak, "traffic": None,
+                     "peak_source": f"{peak_kind} hbm_gbs (burst copy)",
+                     "alg_bytes_per_launch": alg_bytes, "avg_launch_us": attn_s * 1e6,
+                     "launches": int(n_attn), "l2": "256 MB written before every step"},
+        "kernel_breakdown_us": breakdown,
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+
+    # ---- end to end through the C ABI with host buffers: every decode step's
+    # inputs come from pinned host memory and its outputs go back to it
+    if not args.no_e2e:
+        qh, knh, vnh = (x.cpu().pin_memory() for x in (q, kn, vn))
+        outh = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        h2d = (q[0].numel() + kn[0].numel() + vn[0].numel()) * eb
+        d2h = out[0].numel() * 4
+        chunk = 256
+        ctx.build_index(0, K, V, w.n_clusters, w.iters, 1)
+        ctx.sync()
+        ea, eb_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ea.record(stream)
+        for c0 in range(0, T, chunk):
+            n = min(chunk, T - c0)
+            q[c0:c0 + n].copy_(qh[c0:c0 + n], non_blocking=True)
+            kn[c0:c0 + n].copy_(knh[c0:c0 + n], non_blocking=True)
+            vn[c0:c0 + n].copy_(vnh[c0:c0 + n], non_blocking=True)
+            ctx.decode_steps(0, q[c0:c0 + n], kn[c0:c0 + n], vn[c0:c0 + n], w.tau, w.budget,
+                             out[c0:c0 + n])
+            outh[c0:c0 + n].copy_(out[c0:c0 + n], non_blocking=True)
+        eb_.record(stream)
+        eb_.synchronize()
+        result["e2e"] = {"value": world * T / (ea.elapsed_time(eb_) / 1e3), "unit": UNIT,
+                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        idx0 = ctx.get_index(0, 0, 0, w.n_prefill)
+        result["cpu_baseline"] = cpu_baseline(K, V, idx0, q, kn, vn, w)
+    ctx.close()
+    return result
+
+
+# ---------------------------------------------------------------- reference arm
+
+def run_reference(args, rank, world):
+    """The oracle timed as it stands on the host cores, same metric and
+    workload; each step is a bounded sample (one (sequence, KV head))."""
+    import numpy as np
+    import torch
+    import oracle
+    import synth
+    w = workload(args)
+    if rank != 0:
+        return None
+    n_steps = 32
+    K, V = synth.prefill(w, 0, "cpu", seqs=[0], heads=[0])
+    q, kn, vn, _ = synth.decode_inputs(w, "cpu", n_steps=n_steps, seqs=[0])
+    # the sampled head's index, built by the oracle itself (one Lloyd round)
+    km = oracle.kmeans(synth.to_oracle(K[0, 0]), w.n_clusters, 1, 1)
+    idx = {"assign": km["assign"], "centroids": km["cent"]}
+    Kf = torch.zeros(1, w.n_kv_heads, w.n_prefill, 128, dtype=K.dtype)
+    Vf = torch.zeros_like(Kf)
+    Kf[0, 0], Vf[0, 0] = K[0, 0], V[0, 0]
+    for _ in range(args.warmup):
+        oracle_decode_sample(Kf[0], Vf[0], idx, q, kn, vn, w, 4)
+    per = [oracle_decode_sample(Kf[0], Vf[0], idx, q, kn, vn, w, n_steps) for _ in range(args.steps)]
+    value = 1.0 / (float(np.mean(per)) * w.batch * w.n_kv_heads)
+    sample = (f"single-threaded C oracle: 1 (sequence, KV head) x {n_steps} decode steps per step "
+              f"of the full-size workload, index from one oracle Lloyd round; scaled by "
+              f"B x H_kv = {w.batch * w.n_kv_heads}")
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": float(np.mean(per)) * w.batch * w.n_kv_heads * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_of(w, world),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch
+        import torch.distributed as td
+        backend = "nccl" if (args.impl == "ours" and torch.cuda.is_available()) else "gloo"
+        td.init_process_group(backend=backend)
+    try:
+        if args.impl == "reference":
+            res = run_reference(args, rank, world)
+        else:
+            res = run_ours(args, rank, world, local)
+        if rank == 0 and res is not None:
+            print(json.dumps(res), flush=True)
+    finally:
+        if world > 1:
+            import torch.distributed as td
+            td.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -107,6 +107,28 @@ class Context:
                              _opt_ptr(boundary, "boundary", torch.uint8),
                              _opt_ptr(r_out, "r_out", torch.float32))
 
+    def decode_steps(self, layer: int, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                     tau: float, budget: int, out: torch.Tensor, *, n_layers: int = 1,
+                     selected_units: torch.Tensor | None = None,
+                     n_selected: torch.Tensor | None = None,
+                     boundary: torch.Tensor | None = None,
+                     r_out: torch.Tensor | None = None) -> None:
+        """q.shape[0] consecutive decode steps (see lkv_decode_steps)."""
+        _lib.lkv_decode_steps(self._ctx, layer, n_layers, q.shape[0], _dev_ptr(q, "q", self.dtype),
+                              _dev_ptr(k_new, "k_new", self.dtype),
+                              _dev_ptr(v_new, "v_new", self.dtype), float(tau), budget,
+                              self.local_buf, _dev_ptr(out, "out", torch.float32),
+                              _opt_ptr(selected_units, "selected_units", torch.int32),
+                              _opt_ptr(n_selected, "n_selected", torch.int32),
+                              _opt_ptr(boundary, "boundary", torch.uint8),
+                              _opt_ptr(r_out, "r_out", torch.float32))
+
+    def set_profiling(self, enable: bool) -> None:
+        _lib.lkv_set_profiling(self._ctx, enable)
+
+    def profile(self, reset: bool = False):
+        return _lib.lkv_get_profile(self._ctx, reset)
+
     def get_index(self, layer: int, seq: int, kv_head: int, n_tokens: int) -> dict:
         cap = self.u_cap
         cent = np.zeros((cap, 128), np.float32)

@@ -18,8 +18,8 @@ STATUS_NAMES = {0: "LKV_OK", 1: "LKV_EINVAL", 2: "LKV_ENOMEM", 3: "LKV_ECUDA",
 LKV_DTYPE_FP32, LKV_DTYPE_BF16 = 0, 1
 
 EXPORTED = ("lkv_create", "lkv_destroy", "lkv_build_index", "lkv_load_index",
-            "lkv_decode_step", "lkv_get_index", "lkv_get_decode_state", "lkv_sync",
-            "lkv_last_error")
+            "lkv_decode_step", "lkv_decode_steps", "lkv_get_index", "lkv_get_decode_state",
+            "lkv_sync", "lkv_last_error", "lkv_set_profiling", "lkv_get_profile")
 
 
 class lkv_config(C.Structure):
@@ -39,6 +39,10 @@ class lkv_decode_state(C.Structure):
         ("n_evicted", C.c_int32), ("n_forced", C.c_int32), ("n_refined", C.c_int64),
         ("n_inexact", C.c_int64),
     ]
+
+
+class lkv_kernel_stat(C.Structure):
+    _fields_ = [("name", C.c_char * 24), ("launches", C.c_int64), ("total_ms", C.c_double)]
 
 
 class LKVError(RuntimeError):
@@ -74,6 +78,13 @@ def load(path: str = LIB_PATH):
         L.lkv_load_index.restype = st
         L.lkv_decode_step.argtypes = [vp, i32, i32, vp, vp, vp, f32, i32, i32, vp, vp, vp, vp, vp]
         L.lkv_decode_step.restype = st
+        L.lkv_decode_steps.argtypes = [vp, i32, i32, i32, vp, vp, vp, f32, i32, i32, vp, vp, vp,
+                                       vp, vp]
+        L.lkv_decode_steps.restype = st
+        L.lkv_set_profiling.argtypes = [vp, i32]
+        L.lkv_set_profiling.restype = st
+        L.lkv_get_profile.argtypes = [vp, vp, i32, C.POINTER(i32), vp, i32]
+        L.lkv_get_profile.restype = st
         L.lkv_get_index.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, C.POINTER(i32)]
         L.lkv_get_index.restype = st
         L.lkv_get_decode_state.argtypes = [vp, i32, i32, C.POINTER(lkv_decode_state)]
@@ -116,6 +127,28 @@ def lkv_decode_step(ctx, layer, n_layers, q_ptr, k_ptr, v_ptr, tau, budget, loca
                     out_ptr, sel_ptr, nsel_ptr, boundary_ptr, r_ptr):
     _check(load().lkv_decode_step(ctx, layer, n_layers, q_ptr, k_ptr, v_ptr, tau, budget,
                                   local_buf, out_ptr, sel_ptr, nsel_ptr, boundary_ptr, r_ptr), ctx)
+
+
+def lkv_decode_steps(ctx, layer, n_layers, n_steps, q_ptr, k_ptr, v_ptr, tau, budget, local_buf,
+                     out_ptr, sel_ptr, nsel_ptr, boundary_ptr, r_ptr):
+    _check(load().lkv_decode_steps(ctx, layer, n_layers, n_steps, q_ptr, k_ptr, v_ptr, tau,
+                                   budget, local_buf, out_ptr, sel_ptr, nsel_ptr, boundary_ptr,
+                                   r_ptr), ctx)
+
+
+def lkv_set_profiling(ctx, enable: bool) -> None:
+    _check(load().lkv_set_profiling(ctx, 1 if enable else 0), ctx)
+
+
+def lkv_get_profile(ctx, reset: bool = False):
+    """(dict kernel -> (launches, total_ms), dict of work counters)."""
+    stats = (lkv_kernel_stat * 32)()
+    n = C.c_int32(0)
+    ctr = (C.c_int64 * 4)()
+    _check(load().lkv_get_profile(ctx, stats, 32, C.byref(n), ctr, 1 if reset else 0), ctx)
+    kern = {stats[i].name.decode(): (stats[i].launches, stats[i].total_ms) for i in range(n.value)}
+    names = ("attn_rows", "attn_slices", "score_units", "gather_rows")
+    return kern, {k: ctr[i] for i, k in enumerate(names)}
 
 
 def lkv_get_index(ctx, layer, seq, kv_head, capacity, cent_ptr, len_ptr, row_ptr, assign_ptr,

@@ -13,11 +13,20 @@ using lkv::CtxView;
 using lkv::DecState;
 using lkv::KmeansScratch;
 
+struct GraphEntry {
+  lkv::StepArgs args{};
+  int steps = 0;
+  cudaGraphExec_t exec = nullptr;
+};
+
 struct lkv_ctx {
   lkv_config cfg{};
   CtxView v{};
   KmeansScratch ks{};
   cudaStream_t stream = nullptr;
+  cudaStream_t capture = nullptr;   // private stream for CUDA-graph capture
+  lkv::Prof prof;
+  std::vector<GraphEntry> graphs;
   std::vector<void *> dev;
   std::vector<void *> host;
   std::vector<int32_t> steps;     // decode steps taken per layer
@@ -76,6 +85,12 @@ static void *halloc(lkv_ctx *c, size_t bytes, lkv_status *st) {
 }
 
 static void free_all(lkv_ctx *c) {
+  for (GraphEntry &g : c->graphs)
+    if (g.exec) cudaGraphExecDestroy(g.exec);
+  c->graphs.clear();
+  c->prof.release();
+  if (c->capture) cudaStreamDestroy(c->capture);
+  c->capture = nullptr;
   for (void *p : c->dev) cudaFree(p);
   for (void *p : c->host) cudaFreeHost(p);
   c->dev.clear();
@@ -180,7 +195,11 @@ lkv_status lkv_create(const lkv_config *cfg, lkv_ctx **out) {
   v.part_acc = (float *)dalloc(c, S_all * max_chunks * G * d * 4, &st);
   v.part_ml = (float *)dalloc(c, S_all * max_chunks * G * 2 * 4, &st);
   v.attn_count = (int32_t *)dalloc(c, S_all * 4, &st);
+  v.max_pieces = u_cap + max_chunks;
+  v.pieces = (int4 *)dalloc(c, S_all * (int64_t)v.max_pieces * sizeof(int4), &st);
+  v.chunk_piece = (int32_t *)dalloc(c, S_all * (int64_t)(max_chunks + 1) * 4, &st);
   v.err = (int32_t *)dalloc(c, 4, &st);
+  v.counters = (int64_t *)dalloc(c, lkv::kCounters * 8, &st);
 
   KmeansScratch &ks = c->ks;
   ks.knorm = (float *)dalloc(c, S * n_cap * 4, &st);
@@ -206,6 +225,9 @@ lkv_status lkv_create(const lkv_config *cfg, lkv_ctx **out) {
   if (e == cudaSuccess) e = cudaMemsetAsync(v.err, 0, 4, c->stream);
   if (e == cudaSuccess) e = cudaMemsetAsync(ks.n_refined, 0, 8, c->stream);
   if (e == cudaSuccess) e = cudaMemsetAsync(ks.n_inexact, 0, 8, c->stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(v.counters, 0, lkv::kCounters * 8, c->stream);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&c->capture, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = lkv::prepare_kernels(k.dtype, k.group);
   if (e == cudaSuccess) e = cudaStreamSynchronize(c->stream);
   if (e != cudaSuccess) {
     g_create_error = std::string("initialisation: ") + cudaGetErrorString(e);
@@ -248,7 +270,7 @@ lkv_status lkv_build_index(lkv_ctx *c, int32_t layer, const void *keys, const vo
   std::vector<int64_t> idx((size_t)S * nc), perm;
   for (int sl = 0; sl < S; ++sl) init_indices(n, nc, seed + (uint64_t)sl, idx.data() + (size_t)sl * nc, perm);
   cudaError_t e = cudaMemcpyAsync(c->ks.init_idx, idx.data(), idx.size() * 8, cudaMemcpyHostToDevice, c->stream);
-  if (e == cudaSuccess) e = lkv::launch_kmeans_build(c->v, layer, c->ks, keys, values, n, nc, iters, false, c->stream);
+  if (e == cudaSuccess) e = lkv::launch_kmeans_build(c->v, layer, c->ks, keys, values, n, nc, iters, false, c->stream, c->prof);
   if (e != cudaSuccess) return cuda_fail(c, e, "lkv_build_index");
   c->built[layer] = 1;
   c->steps[layer] = 0;
@@ -265,7 +287,7 @@ lkv_status lkv_load_index(lkv_ctx *c, int32_t layer, const void *keys, const voi
   if (!keys || !values || !assign || !cent) return fail(c, LKV_EINVAL, "null argument");
   if (n < 1 || n > c->cfg.max_prefill) return fail(c, LKV_EINVAL, "n_tokens outside 1..max_prefill");
   if (nc < 1 || nc > c->cfg.max_clusters) return fail(c, LKV_EINVAL, "n_clusters outside 1..max_clusters");
-  cudaError_t e = lkv::launch_load_index(c->v, layer, c->ks, keys, values, n, nc, assign, cent, c->stream);
+  cudaError_t e = lkv::launch_load_index(c->v, layer, c->ks, keys, values, n, nc, assign, cent, c->stream, c->prof);
   if (e != cudaSuccess) return cuda_fail(c, e, "lkv_load_index");
   c->built[layer] = 1;
   c->steps[layer] = 0;
@@ -274,30 +296,188 @@ lkv_status lkv_load_index(lkv_ctx *c, int32_t layer, const void *keys, const voi
   return LKV_OK;
 }
 
+static lkv_status check_step_args(lkv_ctx *c, int32_t layer, int32_t nl, int32_t n_steps,
+                                  const void *q, const void *k_new, const void *v_new, float tau,
+                                  int32_t budget, int32_t local_buf, const float *out) {
+  if (nl < 1 || layer < 0 || layer + nl > c->cfg.n_layers) return fail(c, LKV_EINVAL, "layer range out of bounds");
+  if (!q || !k_new || !v_new || !out) return fail(c, LKV_EINVAL, "null input or output");
+  if (n_steps < 0) return fail(c, LKV_EINVAL, "n_steps must be >= 0");
+  if (budget < 0 || budget > c->cfg.max_budget) return fail(c, LKV_EINVAL, "budget outside 0..max_budget");
+  if (local_buf != c->cfg.local_buf) return fail(c, LKV_EINVAL, "local_buf differs from the context's");
+  if (tau != tau) return fail(c, LKV_EINVAL, "tau is NaN");
+  for (int l = layer; l < layer + nl; ++l) {
+    if (!c->built[l]) return fail(c, LKV_ESTATE, "layer " + std::to_string(l) + " has no index");
+    if (c->steps[l] != c->steps[layer])
+      return fail(c, LKV_EINVAL, "layers decoded in one call must have taken the same number of steps");
+    if ((int64_t)c->steps[l] + n_steps > c->cfg.max_steps) return fail(c, LKV_ECAPACITY, "max_steps reached");
+  }
+  return LKV_OK;
+}
+
+static lkv::StepArgs step_args(lkv_ctx *c, int32_t layer, int32_t nl, bool multi, const void *q,
+                               const void *k_new, const void *v_new, float tau, int32_t budget,
+                               float *out, int32_t *sel, int32_t *nsel, uint8_t *bnd, float *r) {
+  lkv::StepArgs a{};
+  a.q = q; a.k_new = k_new; a.v_new = v_new;
+  a.tau = tau; a.budget = budget;
+  a.out = out; a.selected_units = sel; a.n_selected = nsel;
+  a.boundary = bnd; a.r_out = r;
+  a.l0 = layer; a.nl = nl;
+  a.base_t = 0;
+  if (multi) {
+    const int64_t B = c->cfg.batch, Hkv = c->cfg.n_kv_heads, H = Hkv * c->cfg.group;
+    const size_t es = c->cfg.dtype == LKV_DTYPE_BF16 ? 2 : 4;
+    a.stride_q = B * nl * H * 128;
+    a.stride_kv = B * nl * Hkv * 128;
+    a.stride_out = B * nl * H * 128;
+    a.stride_sel = B * nl * Hkv * (int64_t)c->v.u_cap;
+    a.stride_nsel = B * nl * Hkv;
+    a.stride_b = B * nl;
+    // kernels address step t (the absolute decode position) at base + t *
+    // stride; shifting every base back by the call's first position makes
+    // the arguments, and so a cached graph, identical for every call that
+    // walks the same full-length buffers chunk by chunk
+    const uint64_t t0 = (uint64_t)c->steps[layer];
+    auto shift = [t0](const void *p, int64_t stride, size_t eb) -> uintptr_t {
+      return p ? (uintptr_t)p - (uintptr_t)(t0 * (uint64_t)stride * eb) : 0;
+    };
+    a.q = (const void *)shift(q, a.stride_q, es);
+    a.k_new = (const void *)shift(k_new, a.stride_kv, es);
+    a.v_new = (const void *)shift(v_new, a.stride_kv, es);
+    a.out = (float *)shift(out, a.stride_out, 4);
+    a.selected_units = (int32_t *)shift(sel, a.stride_sel, 4);
+    a.n_selected = (int32_t *)shift(nsel, a.stride_nsel, 4);
+    a.boundary = (uint8_t *)shift(bnd, a.stride_b, 1);
+    a.r_out = (float *)shift(r, a.stride_b, 4);
+  }
+  return a;
+}
+
+static int kernels_per_step(const lkv_ctx *c) { return c->v.offload ? 5 : 4; }
+
 lkv_status lkv_decode_step(lkv_ctx *c, int32_t layer, int32_t nl, const void *q,
                            const void *k_new, const void *v_new, float tau, int32_t budget,
                            int32_t local_buf, float *out, int32_t *selected_units,
                            int32_t *n_selected, uint8_t *boundary, float *r_out) {
   lkv_status s = check_usable(c);
   if (s != LKV_OK) return s;
-  if (nl < 1 || layer < 0 || layer + nl > c->cfg.n_layers) return fail(c, LKV_EINVAL, "layer range out of bounds");
-  if (!q || !k_new || !v_new || !out) return fail(c, LKV_EINVAL, "null input or output");
-  if (budget < 0 || budget > c->cfg.max_budget) return fail(c, LKV_EINVAL, "budget outside 0..max_budget");
-  if (local_buf != c->cfg.local_buf) return fail(c, LKV_EINVAL, "local_buf differs from the context's");
-  if (tau != tau) return fail(c, LKV_EINVAL, "tau is NaN");
-  for (int l = layer; l < layer + nl; ++l) {
-    if (!c->built[l]) return fail(c, LKV_ESTATE, "layer " + std::to_string(l) + " has no index");
-    if (c->steps[l] >= c->cfg.max_steps) return fail(c, LKV_ECAPACITY, "max_steps reached");
-  }
-  lkv::StepArgs a{};
-  a.q = q; a.k_new = k_new; a.v_new = v_new;
-  a.tau = tau; a.budget = budget;
-  a.out = out; a.selected_units = selected_units; a.n_selected = n_selected;
-  a.boundary = boundary; a.r_out = r_out;
-  a.l0 = layer; a.nl = nl;
-  cudaError_t e = lkv::launch_decode_step(c->v, a, c->stream);
+  s = check_step_args(c, layer, nl, 1, q, k_new, v_new, tau, budget, local_buf, out);
+  if (s != LKV_OK) return s;
+  lkv::StepArgs a = step_args(c, layer, nl, false, q, k_new, v_new, tau, budget, out,
+                              selected_units, n_selected, boundary, r_out);
+  cudaError_t e = lkv::launch_decode_step(c->v, a, c->stream, c->prof);
   if (e != cudaSuccess) return cuda_fail(c, e, "lkv_decode_step");
   for (int l = layer; l < layer + nl; ++l) c->steps[l] += 1;
+  return LKV_OK;
+}
+
+// Graph of `steps` consecutive decode steps with these arguments (cached).
+static cudaError_t step_graph(lkv_ctx *c, const lkv::StepArgs &a, int steps, cudaGraphExec_t *out) {
+  for (GraphEntry &g : c->graphs)
+    if (g.steps == steps && std::memcmp(&g.args, &a, sizeof a) == 0) {
+      *out = g.exec;
+      return cudaSuccess;
+    }
+  lkv::Prof quiet;
+  quiet.counting = false;
+  cudaGraph_t graph = nullptr;
+  cudaError_t e = cudaStreamBeginCapture(c->capture, cudaStreamCaptureModeThreadLocal);
+  if (e != cudaSuccess) return e;
+  for (int i = 0; i < steps && e == cudaSuccess; ++i) e = lkv::launch_decode_step(c->v, a, c->capture, quiet);
+  cudaError_t e2 = cudaStreamEndCapture(c->capture, &graph);
+  if (e == cudaSuccess) e = e2;
+  cudaGraphExec_t exec = nullptr;
+  if (e == cudaSuccess) e = cudaGraphInstantiate(&exec, graph, 0);
+  if (graph) cudaGraphDestroy(graph);
+  if (e != cudaSuccess) return e;
+  if (c->graphs.size() >= 8) {
+    cudaGraphExecDestroy(c->graphs.front().exec);
+    c->graphs.erase(c->graphs.begin());
+  }
+  GraphEntry g;
+  g.args = a;
+  g.steps = steps;
+  g.exec = exec;
+  c->graphs.push_back(g);
+  *out = exec;
+  return cudaSuccess;
+}
+
+lkv_status lkv_decode_steps(lkv_ctx *c, int32_t layer, int32_t nl, int32_t n_steps,
+                            const void *q, const void *k_new, const void *v_new, float tau,
+                            int32_t budget, int32_t local_buf, float *out,
+                            int32_t *selected_units, int32_t *n_selected, uint8_t *boundary,
+                            float *r_out) {
+  lkv_status s = check_usable(c);
+  if (s != LKV_OK) return s;
+  s = check_step_args(c, layer, nl, n_steps, q, k_new, v_new, tau, budget, local_buf, out);
+  if (s != LKV_OK) return s;
+  if (n_steps == 0) return LKV_OK;
+  lkv::StepArgs a = step_args(c, layer, nl, true, q, k_new, v_new, tau, budget, out,
+                              selected_units, n_selected, boundary, r_out);
+  cudaError_t e = cudaSuccess;
+  constexpr int kGraphSteps = 64;
+  if (c->prof.timing || n_steps < kGraphSteps) {
+    for (int i = 0; i < n_steps && e == cudaSuccess; ++i) e = lkv::launch_decode_step(c->v, a, c->stream, c->prof);
+  } else {
+    cudaGraphExec_t exec = nullptr;
+    e = step_graph(c, a, kGraphSteps, &exec);
+    const int reps = n_steps / kGraphSteps, tail = n_steps % kGraphSteps;
+    for (int r = 0; r < reps && e == cudaSuccess; ++r) e = cudaGraphLaunch(exec, c->stream);
+    if (e == cudaSuccess && c->prof.counting) {
+      const int kinds[5] = {lkv::kPBoundary, lkv::kPScore, lkv::kPSelect, lkv::kPAttn, lkv::kPGather};
+      for (int k = 0; k < kernels_per_step(c); ++k) c->prof.launches[kinds[k]] += (int64_t)reps * kGraphSteps;
+    }
+    for (int i = 0; i < tail && e == cudaSuccess; ++i) e = lkv::launch_decode_step(c->v, a, c->stream, c->prof);
+  }
+  if (e != cudaSuccess) return cuda_fail(c, e, "lkv_decode_steps");
+  for (int l = layer; l < layer + nl; ++l) c->steps[l] += n_steps;
+  return LKV_OK;
+}
+
+static const char *kKindNames[lkv::kPNum] = {
+    "lkv_boundary", "lkv_score", "lkv_select", "lkv_gather_offload", "lkv_attn",
+    "kmeans_init", "kmeans_operand", "kmeans_assign", "kmeans_refine", "kmeans_sort",
+    "kmeans_update", "kmeans_pool"};
+
+lkv_status lkv_set_profiling(lkv_ctx *c, int32_t enable) {
+  lkv_status s = check_usable(c);
+  if (s != LKV_OK) return s;
+  c->prof.timing = enable != 0;
+  return LKV_OK;
+}
+
+lkv_status lkv_get_profile(lkv_ctx *c, lkv_kernel_stat *stats, int32_t capacity, int32_t *n_stats,
+                           int64_t *counters, int32_t reset) {
+  lkv_status s = check_usable(c);
+  if (s != LKV_OK) return s;
+  s = lkv_sync(c);
+  if (s != LKV_OK) return s;
+  c->prof.resolve();
+  if (n_stats) *n_stats = lkv::kPNum;
+  for (int k = 0; k < lkv::kPNum && stats && k < capacity; ++k) {
+    std::memset(stats[k].name, 0, sizeof stats[k].name);
+    std::strncpy(stats[k].name, kKindNames[k], sizeof stats[k].name - 1);
+    stats[k].launches = c->prof.launches[k];
+    stats[k].total_ms = c->prof.ms[k];
+  }
+  if (counters) {
+    int64_t h[lkv::kCounters] = {};
+    cudaError_t e = cudaMemcpy(h, c->v.counters, sizeof h, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(c, e, "lkv_get_profile");
+    counters[0] = h[lkv::kCntAttnRows];
+    counters[1] = h[lkv::kCntAttnSlices];
+    counters[2] = h[lkv::kCntScoreUnits];
+    counters[3] = h[lkv::kCntGatherRows];
+  }
+  if (reset) {
+    for (int k = 0; k < lkv::kPNum; ++k) {
+      c->prof.launches[k] = 0;
+      c->prof.ms[k] = 0.0;
+    }
+    cudaError_t e = cudaMemset(c->v.counters, 0, lkv::kCounters * 8);
+    if (e != cudaSuccess) return cuda_fail(c, e, "lkv_get_profile");
+  }
   return LKV_OK;
 }
 

@@ -584,34 +584,38 @@ static int parts_for(int64_t n) {
 template <int DT>
 static cudaError_t group_and_pool(const CtxView &v, int layer, const KmeansScratch &ks,
                                   int64_t n, int32_t c, int64_t gs0, int S,
-                                  cudaStream_t st) {
+                                  cudaStream_t st, Prof &prof) {
   const int parts = parts_for(n);
+  prof.begin(kPKmSort, st, 3);
   const int c_cap = v.u_cap - v.t_cap;
   k_count_parts<<<dim3(parts, S), 256, c * sizeof(int32_t), st>>>(
       v.assign, n, v.n_cap, c, c_cap, parts, gs0, ks.cnt_part);
   k_scan_parts<<<S, 1024, 0, st>>>(c, c_cap, parts, ks.cnt_part, ks.count, ks.offs);
   k_scatter<<<dim3(parts, S), 128, c * sizeof(int32_t), st>>>(
       v.assign, n, v.n_cap, c, c_cap, parts, gs0, ks.cnt_part, v.perm);
+  prof.end(st);
   return cudaGetLastError();
 }
 
 template <int DT>
 static cudaError_t finish_pool(const CtxView &v, int layer, const KmeansScratch &ks,
                                const void *keys, const void *values, int64_t n, int32_t c,
-                               int64_t gs0, int S, cudaStream_t st) {
+                               int64_t gs0, int S, cudaStream_t st, Prof &prof) {
   const int c_cap = v.u_cap - v.t_cap;
+  prof.begin(kPKmPool, st, 3);
   k_pool_build<DT><<<dim3((unsigned)((n + 7) / 8), S), 256, 0, st>>>(
       keys, values, n, v.n_cap, gs0, v.perm, v.pool_k, v.pool_v, v.pool_rows);
   k_unit_table<<<dim3((c + 255) / 256, S), 256, 0, st>>>(c, c_cap, v.u_cap, gs0, ks.count,
                                                          ks.offs, v.unit_row, v.unit_len);
   k_reset_layer<<<v.B, 128, 0, st>>>(v, layer, c);
+  prof.end(st);
   return cudaGetLastError();
 }
 
 template <int DT>
 static cudaError_t kmeans_build_t(const CtxView &v, int layer, const KmeansScratch &ks,
                                   const void *keys, const void *values, int64_t n,
-                                  int32_t c, int32_t iters, cudaStream_t st) {
+                                  int32_t c, int32_t iters, cudaStream_t st, Prof &prof) {
   const int S = v.B * v.Hkv;
   const int64_t gs0 = (int64_t)layer * S;
   const int c_cap = v.u_cap - v.t_cap;
@@ -621,38 +625,50 @@ static cudaError_t kmeans_build_t(const CtxView &v, int layer, const KmeansScrat
     cudaFuncSetAttribute(k_assign_simt<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAsSmem);
     attr_done[DT] = true;
   }
+  prof.begin(kPKmInit, st, 2);
   k_init_cent<DT><<<dim3(c, S), kHeadDim, 0, st>>>(keys, n, c, ks.init_idx, v.cent32, gs0, v.u_cap);
   k_key_norms<DT><<<dim3((unsigned)((n + 7) / 8), S), 256, 0, st>>>(keys, n, v.n_cap, ks.knorm);
+  prof.end(st);
   const float eps = 0x1p-15f;  // fp32 FMA dot of 128 terms: 2*gamma_128 < 2^-16
   for (int it = 0; it < iters; ++it) {
+    prof.begin(kPKmOperand, st);
     cudaMemsetAsync(ks.cstat, 0, sizeof(float) * 2 * S, st);
     k_prepare_operand<DT><<<dim3((c + 7) / 8, S), 256, 0, st>>>(v.cent32, v.cent_op, c, c_cap,
                                                                v.u_cap, gs0, ks.c2, ks.cstat);
     cudaMemsetAsync(ks.amb_count, 0, sizeof(int32_t), st);
+    prof.end(st);
+    prof.begin(kPKmAssign, st);
     k_assign_simt<DT><<<dim3((unsigned)((n + kAsTile - 1) / kAsTile), S), kAsThreads, kAsSmem, st>>>(
         keys, n, c, v.cent_op, v.u_cap, ks.c2, c_cap, ks.knorm, v.n_cap, ks.cstat, eps,
         v.assign, gs0, ks.amb, ks.amb_count, (int32_t)amb_cap, v.err);
+    prof.end(st);
+    prof.begin(kPKmRefine, st);
     k_assign_refine<DT><<<304, 256, 0, st>>>(keys, n, c, v.cent_op, v.u_cap, v.assign, v.n_cap,
                                              gs0, ks.amb, ks.amb_count, (int32_t)amb_cap,
                                              ks.n_refined);
-    cudaError_t e = group_and_pool<DT>(v, layer, ks, n, c, gs0, S, st);
+    prof.end(st);
+    cudaError_t e = group_and_pool<DT>(v, layer, ks, n, c, gs0, S, st, prof);
     if (e != cudaSuccess) return e;
+    prof.begin(kPKmUpdate, st);
     k_update<DT><<<dim3((c + 7) / 8, S), 256, 0, st>>>(keys, n, v.n_cap, c, c_cap, v.u_cap, gs0,
                                                        v.perm, ks.count, ks.offs, v.cent32,
                                                        ks.n_inexact);
+    prof.end(st);
   }
+  prof.begin(kPKmOperand, st);
   cudaMemsetAsync(ks.cstat, 0, sizeof(float) * 2 * S, st);
   k_prepare_operand<DT><<<dim3((c + 7) / 8, S), 256, 0, st>>>(v.cent32, v.cent_op, c, c_cap,
                                                              v.u_cap, gs0, ks.c2, ks.cstat);
-  return finish_pool<DT>(v, layer, ks, keys, values, n, c, gs0, S, st);
+  prof.end(st);
+  return finish_pool<DT>(v, layer, ks, keys, values, n, c, gs0, S, st, prof);
 }
 
 cudaError_t launch_kmeans_build(const CtxView &v, int layer, const KmeansScratch &ks,
                                 const void *keys, const void *values, int64_t n, int32_t c,
-                                int32_t iters, bool use_tc, cudaStream_t stream) {
+                                int32_t iters, bool use_tc, cudaStream_t stream, Prof &prof) {
   (void)use_tc;
-  if (v.dtype == 1) return kmeans_build_t<1>(v, layer, ks, keys, values, n, c, iters, stream);
-  return kmeans_build_t<0>(v, layer, ks, keys, values, n, c, iters, stream);
+  if (v.dtype == 1) return kmeans_build_t<1>(v, layer, ks, keys, values, n, c, iters, stream, prof);
+  return kmeans_build_t<0>(v, layer, ks, keys, values, n, c, iters, stream, prof);
 }
 
 // Teacher-forced index: centroids and assignment given.
@@ -676,7 +692,8 @@ __global__ void k_copy_given(const int32_t *assign_in, const float *cent_in, int
 template <int DT>
 static cudaError_t load_index_t(const CtxView &v, int layer, const KmeansScratch &ks,
                                 const void *keys, const void *values, int64_t n, int32_t c,
-                                const int32_t *assign, const float *cent, cudaStream_t st) {
+                                const int32_t *assign, const float *cent, cudaStream_t st,
+                                Prof &prof) {
   const int S = v.B * v.Hkv;
   const int64_t gs0 = (int64_t)layer * S;
   const int c_cap = v.u_cap - v.t_cap;
@@ -685,16 +702,17 @@ static cudaError_t load_index_t(const CtxView &v, int layer, const KmeansScratch
   cudaMemsetAsync(ks.cstat, 0, sizeof(float) * 2 * S, st);
   k_prepare_operand<DT><<<dim3((c + 7) / 8, S), 256, 0, st>>>(v.cent32, v.cent_op, c, c_cap,
                                                              v.u_cap, gs0, ks.c2, ks.cstat);
-  cudaError_t e = group_and_pool<DT>(v, layer, ks, n, c, gs0, S, st);
+  cudaError_t e = group_and_pool<DT>(v, layer, ks, n, c, gs0, S, st, prof);
   if (e != cudaSuccess) return e;
-  return finish_pool<DT>(v, layer, ks, keys, values, n, c, gs0, S, st);
+  return finish_pool<DT>(v, layer, ks, keys, values, n, c, gs0, S, st, prof);
 }
 
 cudaError_t launch_load_index(const CtxView &v, int layer, const KmeansScratch &ks,
                               const void *keys, const void *values, int64_t n, int32_t c,
-                              const int32_t *assign, const float *cent, cudaStream_t stream) {
-  if (v.dtype == 1) return load_index_t<1>(v, layer, ks, keys, values, n, c, assign, cent, stream);
-  return load_index_t<0>(v, layer, ks, keys, values, n, c, assign, cent, stream);
+                              const int32_t *assign, const float *cent, cudaStream_t stream,
+                              Prof &prof) {
+  if (v.dtype == 1) return load_index_t<1>(v, layer, ks, keys, values, n, c, assign, cent, stream, prof);
+  return load_index_t<0>(v, layer, ks, keys, values, n, c, assign, cent, stream, prof);
 }
 
 }  // namespace lkv

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <vector>
+
 namespace lkv {
 
 constexpr int kHeadDim = 128;
@@ -72,11 +74,82 @@ struct CtxView {
   int32_t *n_tok;             // [slice]
   int32_t *rng_row;           // [slice][u_cap] first row of each selected unit
   int32_t *rng_cum;           // [slice][u_cap + 1] exclusive token prefix
+  int4 *pieces;               // [slice][max_pieces] (src row, first token, length, 0)
+  int32_t *chunk_piece;       // [slice][max_chunks + 1] first piece of each chunk
+  int32_t max_pieces;
   float *part_acc;            // [slice][max_chunks][G][d]
   float *part_ml;             // [slice][max_chunks][G][2]
   int32_t *attn_count;        // [slice]
   int32_t max_chunks;
   int32_t *err;               // device error bits (shared by all layers)
+  int64_t *counters;          // [kCounters] work counters (see CounterId)
+};
+
+// Work counters accumulated on the device (read by lkv_get_profile).
+enum CounterId : int { kCntAttnRows = 0, kCntScoreUnits = 1, kCntGatherRows = 2,
+                       kCntAttnSlices = 3, kCounters = 8 };
+
+// Kernel kinds for launch counting and event timing.
+enum ProfKind : int {
+  kPBoundary = 0, kPScore, kPSelect, kPGather, kPAttn,
+  kPKmInit, kPKmOperand, kPKmAssign, kPKmRefine, kPKmSort, kPKmUpdate, kPKmPool,
+  kPNum
+};
+
+// Host-side launch counter and (when enabled) CUDA-event timer: begin/end
+// bracket the launches of one kernel kind on the context stream.
+struct Prof {
+  bool timing = false;
+  bool counting = true;
+  int64_t launches[kPNum] = {};
+  double ms[kPNum] = {};
+  struct Rec { int kind; cudaEvent_t a, b; };
+  std::vector<Rec> recs;
+  std::vector<cudaEvent_t> pool;
+  int open_kind = -1;
+  cudaEvent_t open_a = nullptr;
+
+  cudaEvent_t take() {
+    if (pool.empty()) {
+      cudaEvent_t e = nullptr;
+      cudaEventCreate(&e);
+      return e;
+    }
+    cudaEvent_t e = pool.back();
+    pool.pop_back();
+    return e;
+  }
+  void begin(int kind, cudaStream_t s, int n = 1) {
+    if (counting) launches[kind] += n;
+    if (!timing) return;
+    open_kind = kind;
+    open_a = take();
+    cudaEventRecord(open_a, s);
+  }
+  void end(cudaStream_t s) {
+    if (!timing || open_kind < 0) return;
+    cudaEvent_t b = take();
+    cudaEventRecord(b, s);
+    recs.push_back({open_kind, open_a, b});
+    open_kind = -1;
+    if (recs.size() >= 8192) resolve();
+  }
+  void resolve() {
+    if (recs.empty()) return;
+    cudaEventSynchronize(recs.back().b);
+    for (const Rec &r : recs) {
+      float t = 0.f;
+      if (cudaEventElapsedTime(&t, r.a, r.b) == cudaSuccess) ms[r.kind] += t;
+      pool.push_back(r.a);
+      pool.push_back(r.b);
+    }
+    recs.clear();
+  }
+  void release() {
+    resolve();
+    for (cudaEvent_t e : pool) cudaEventDestroy(e);
+    pool.clear();
+  }
 };
 
 // ---------------------------------------------------------------- helpers
@@ -154,15 +227,23 @@ struct KmeansScratch {
 cudaError_t launch_kmeans_build(const CtxView &v, int layer, const KmeansScratch &ks,
                                 const void *keys, const void *values, int64_t n,
                                 int32_t c, int32_t iters, bool use_tc,
-                                cudaStream_t stream);
+                                cudaStream_t stream, Prof &prof);
 // Pool and unit table from a given assignment and fp32 centroids.
 cudaError_t launch_load_index(const CtxView &v, int layer, const KmeansScratch &ks,
                               const void *keys, const void *values, int64_t n,
                               int32_t c, const int32_t *assign,
-                              const float *cent, cudaStream_t stream);
+                              const float *cent, cudaStream_t stream, Prof &prof);
 
+// Inputs and outputs of one decode step are found at base + k * stride where
+// k = (tokens the sequence's layer had appended before this step) - base_t:
+// a single-step call passes strides 0; a multi-step call passes per-step
+// strides (and bases shifted so that base_t = 0), so that one captured step
+// replays unchanged from a CUDA graph.
 struct StepArgs {
   const void *q, *k_new, *v_new;   // [B][nl][H][d], [B][nl][Hkv][d]
+  int32_t base_t;                  // decode position of the call's first step
+  int64_t stride_q, stride_kv;     // elements between consecutive steps' inputs
+  int64_t stride_out, stride_sel, stride_nsel, stride_b;  // outputs, per step
   float tau;
   int32_t budget;
   float *out;                      // [B][nl][H][d]
@@ -174,6 +255,9 @@ struct StepArgs {
   int32_t nl;                      // layers in this call
 };
 
-cudaError_t launch_decode_step(const CtxView &v, const StepArgs &a, cudaStream_t stream);
+cudaError_t launch_decode_step(const CtxView &v, const StepArgs &a, cudaStream_t stream,
+                               Prof &prof);
+// One-time kernel attributes (dynamic shared memory limits), before any capture.
+cudaError_t prepare_kernels(int dtype, int group);
 
 }  // namespace lkv

@@ -157,6 +157,43 @@ lkv_status lkv_decode_step(lkv_ctx *ctx, int32_t layer, int32_t n_layers,
                            int32_t *n_selected, uint8_t *boundary,
                            float *r_out);
 
+/* n_steps consecutive decode steps of layers [layer, layer + n_layers): the
+ * same computation as n_steps calls of lkv_decode_step, with step i's
+ * tensors at i * (one step's size) from each base pointer:
+ *   q [n_steps][B][n_layers][H][d], k_new/v_new [n_steps][B][n_layers][H_kv][d],
+ *   out [n_steps][B][n_layers][H][d], selected_units
+ *   [n_steps][B][n_layers][H_kv][max_clusters + max_steps], n_selected
+ *   [n_steps][B][n_layers][H_kv], boundary and r_out [n_steps][B][n_layers].
+ * The steps run from a captured CUDA graph of 64 steps (cached per argument
+ * set), so the host issues one launch per 64 steps; with profiling enabled
+ * (lkv_set_profiling) they are launched one kernel at a time instead. All
+ * layers of the call must have taken the same number of steps (LKV_EINVAL).
+ * Errors as lkv_decode_step. */
+lkv_status lkv_decode_steps(lkv_ctx *ctx, int32_t layer, int32_t n_layers,
+                            int32_t n_steps, const void *q, const void *k_new,
+                            const void *v_new, float tau, int32_t budget,
+                            int32_t local_buf, float *out, int32_t *selected_units,
+                            int32_t *n_selected, uint8_t *boundary, float *r_out);
+
+/* Per-kernel launch counts (always kept) and CUDA-event durations (kept while
+ * profiling is enabled: each launch is bracketed by events on the context
+ * stream). */
+typedef struct lkv_kernel_stat {
+  char name[24];
+  int64_t launches;
+  double total_ms;
+} lkv_kernel_stat;
+
+lkv_status lkv_set_profiling(lkv_ctx *ctx, int32_t enable);
+
+/* Blocking. stats: host array of capacity entries (one per kernel kind; the
+ * number of kinds goes to *n_stats). counters (optional, host int64[4]):
+ * rows attended (K and V rows read by the attention), attention slices
+ * processed, units scored, rows gathered from host memory. reset != 0 zeroes
+ * everything afterwards. */
+lkv_status lkv_get_profile(lkv_ctx *ctx, lkv_kernel_stat *stats, int32_t capacity,
+                           int32_t *n_stats, int64_t *counters, int32_t reset);
+
 /* Copy one (layer, sequence, KV head) index to host memory (blocks until the
  * context's stream is idle). Any output pointer may be NULL.
  *   centroids host fp32 [capacity][d]: units 0..n_units-1 (clusters, then

@@ -203,3 +203,58 @@ def test_errors_are_status_codes():
     assert e.value.status == 4
     ctx.sync()
     ctx.close()
+
+
+def test_decode_steps_graph_matches_single_steps():
+    """lkv_decode_steps (64-step CUDA graphs + tail, chunked over one set of
+    full-length buffers) gives bit-identical results to single steps."""
+    w = synth.WORKLOADS["long_out"].replace(batch=2, n_kv_heads=2, n_prefill=600, n_components=20,
+                                            n_clusters=20, iters=3, local_buf=16, budget=120,
+                                            jump_p=0.1)
+    T = 150
+    K, V = synth.prefill(w, 0, "cuda")
+    q, kn, vn, _ = synth.decode_inputs(w, "cuda", n_steps=T)
+    outs = []
+    for mode in ("single", "chunks"):
+        ctx = H.make_ctx(w, max_steps=T)
+        ctx.build_index(0, K, V, w.n_clusters, w.iters, 9)
+        out = torch.zeros(T, w.batch, 1, w.n_heads, 128, device="cuda")
+        bnd = torch.zeros(T, w.batch, 1, dtype=torch.uint8, device="cuda")
+        nsel = torch.zeros(T, w.batch, 1, w.n_kv_heads, dtype=torch.int32, device="cuda")
+        sel = torch.full((T, w.batch, 1, w.n_kv_heads, ctx.u_cap), -1, dtype=torch.int32,
+                         device="cuda")
+        if mode == "single":
+            for t in range(T):
+                ctx.decode_step(0, q[t], kn[t], vn[t], 0.9, w.budget, out[t], boundary=bnd[t],
+                                n_selected=nsel[t], selected_units=sel[t])
+        else:
+            for c0, c1 in ((0, 70), (70, 140), (140, 150)):
+                ctx.decode_steps(0, q[c0:c1], kn[c0:c1], vn[c0:c1], 0.9, w.budget, out[c0:c1],
+                                 boundary=bnd[c0:c1], n_selected=nsel[c0:c1],
+                                 selected_units=sel[c0:c1])
+        ctx.sync()
+        outs.append((out.cpu(), bnd.cpu(), nsel.cpu(), sel.cpu()))
+        ctx.close()
+    for a, b in zip(outs[0], outs[1]):
+        assert torch.equal(a, b)
+    assert outs[0][1].sum() > 3
+
+
+def test_profile_counters_and_launch_counts():
+    w = synth.WORKLOADS["long_in"].replace(batch=2, n_kv_heads=2, n_prefill=500, n_components=20,
+                                           n_clusters=20, iters=2, local_buf=8, budget=100)
+    T = 70
+    K, V = synth.prefill(w, 0, "cuda")
+    q, kn, vn, _ = synth.decode_inputs(w, "cuda", n_steps=T)
+    ctx = H.make_ctx(w, max_steps=T)
+    ctx.build_index(0, K, V, w.n_clusters, w.iters, 1)
+    ctx.set_profiling(True)
+    ctx.profile(reset=True)
+    out = torch.zeros(T, w.batch, 1, w.n_heads, 128, device="cuda")
+    ctx.decode_steps(0, q, kn, vn, 0.9, w.budget, out)
+    kern, ctr = ctx.profile(reset=True)
+    assert kern["lkv_attn"][0] == T and kern["lkv_attn"][1] > 0
+    assert ctr["attn_slices"] == T * w.batch * w.n_kv_heads
+    # every attended row is a selected token (<= budget) or a buffer token (<= L)
+    assert ctr["attn_rows"] <= ctr["attn_slices"] * (w.budget + w.local_buf)
+    ctx.close()
