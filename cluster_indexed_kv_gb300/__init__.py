@@ -18,7 +18,7 @@ __all__ = ["Context", "LKVError", "build"]
 
 
 def build(force: bool = False) -> str:
-    from .build import build as _build
+    from .builder import build as _build
     return _build(force=force)
 
 

@@ -2,7 +2,7 @@
 
 Each CUDA translation unit compiles in parallel into ``_build/``; the shared
 library lands in ``cluster_indexed_kv_gb300/_build/liblkv.so``. Run
-``python -m cluster_indexed_kv_gb300.build``.
+``python -m cluster_indexed_kv_gb300.builder``.
 """
 from __future__ import annotations
 
