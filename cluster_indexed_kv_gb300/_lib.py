@@ -19,7 +19,8 @@ LKV_DTYPE_FP32, LKV_DTYPE_BF16 = 0, 1
 
 EXPORTED = ("lkv_create", "lkv_destroy", "lkv_build_index", "lkv_load_index",
             "lkv_decode_step", "lkv_decode_steps", "lkv_get_index", "lkv_get_decode_state",
-            "lkv_sync", "lkv_last_error", "lkv_set_profiling", "lkv_get_profile")
+            "lkv_sync", "lkv_last_error", "lkv_set_profiling", "lkv_get_profile",
+            "lkv_kmeans_static")
 
 
 class lkv_config(C.Structure):
@@ -64,7 +65,7 @@ def load(path: str = LIB_PATH):
         if not os.path.exists(path):
             raise RuntimeError(
                 f"liblkv.so not found at {path}; build it with "
-                "`python -m cluster_indexed_kv_gb300.build` (needs nvcc)")
+                "`python -m cluster_indexed_kv_gb300.builder` (needs nvcc)")
         L = C.CDLL(path)
         vp, i32, i64, u64, f32 = C.c_void_p, C.c_int32, C.c_int64, C.c_uint64, C.c_float
         st = C.c_int
@@ -89,6 +90,8 @@ def load(path: str = LIB_PATH):
         L.lkv_get_index.restype = st
         L.lkv_get_decode_state.argtypes = [vp, i32, i32, C.POINTER(lkv_decode_state)]
         L.lkv_get_decode_state.restype = st
+        L.lkv_kmeans_static.argtypes = [vp, i32, i64, i32, i32, u64, vp, vp, vp]
+        L.lkv_kmeans_static.restype = st
         L.lkv_sync.argtypes = [vp]
         L.lkv_sync.restype = st
         L.lkv_last_error.argtypes = [vp]
@@ -163,6 +166,12 @@ def lkv_get_decode_state(ctx, layer, seq) -> lkv_decode_state:
     s = lkv_decode_state()
     _check(load().lkv_get_decode_state(ctx, layer, seq, C.byref(s)), ctx)
     return s
+
+
+def lkv_kmeans_static(keys_ptr, dtype, n_tokens, n_clusters, iters, seed, cent_ptr, assign_ptr,
+                      stream_ptr) -> None:
+    _check(load().lkv_kmeans_static(keys_ptr, dtype, n_tokens, n_clusters, iters, seed, cent_ptr,
+                                    assign_ptr, stream_ptr), None)
 
 
 def lkv_sync(ctx) -> None:

@@ -41,6 +41,11 @@ struct lkv_ctx {
 
 static thread_local std::string g_create_error;
 
+namespace lkv {
+// Error text of calls that have no context (read with lkv_last_error(NULL)).
+void set_unbound_error(const char *msg) { g_create_error = msg; }
+}  // namespace lkv
+
 static lkv_status fail(lkv_ctx *c, lkv_status s, const std::string &msg) {
   if (c) c->err = msg;
   else g_create_error = msg;

@@ -19,6 +19,10 @@
 // cluster); the member sum of bf16 keys is formed exactly in 2^-40 fixed
 // point (double-precision token-order sum when a value is out of that range,
 // and always for fp32 keys); centroid = float(sum / count) in double.
+#include <mutex>
+#include <string>
+
+#include "../../include/lkv.h"
 #include "lkv_internal.cuh"
 
 namespace lkv {
@@ -715,4 +719,184 @@ cudaError_t launch_load_index(const CtxView &v, int layer, const KmeansScratch &
   return load_index_t<0>(v, layer, ks, keys, values, n, c, assign, cent, stream, prof);
 }
 
+
+// ---------------------------------------------------------------- allocation-free K-means
+
+// lkv_kmeans_static runs the same K-means as lkv_build_index for one
+// (sequence, KV head) slice, but every intermediate buffer lives in the
+// fixed array below instead of memory obtained from cudaMalloc. The array is
+// part of the library image: each GPU that loads the library holds it until
+// the process exits, and all calls on a GPU share it.
+constexpr int64_t kStaticMaxTokens = 32768;
+constexpr int32_t kStaticMaxClusters = 2048;
+constexpr size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
+constexpr size_t kSoKnorm = 0;
+constexpr size_t kSoC2 = kSoKnorm + al256(kStaticMaxTokens * 4);
+constexpr size_t kSoCstat = kSoC2 + al256(kStaticMaxClusters * 4);
+constexpr size_t kSoCntPart = kSoCstat + 256;
+constexpr size_t kSoCount = kSoCntPart + al256((size_t)kMaxParts * kStaticMaxClusters * 4);
+constexpr size_t kSoOffs = kSoCount + al256(kStaticMaxClusters * 4);
+constexpr size_t kSoAmb = kSoOffs + al256(kStaticMaxClusters * 4);
+constexpr size_t kSoMisc = kSoAmb + al256(kStaticMaxTokens * sizeof(int4));
+constexpr size_t kSoInit = kSoMisc + 256;  // misc: amb_count, err (int32), n_refined, n_inexact (int64)
+constexpr size_t kSoShuffle = kSoInit + al256(kStaticMaxClusters * 8);
+constexpr size_t kSoCentOp = kSoShuffle + al256(kStaticMaxTokens * 8);
+constexpr size_t kSoPerm = kSoCentOp + al256((size_t)kStaticMaxClusters * kHeadDim * 4);
+constexpr size_t kStaticScratchBytes = kSoPerm + al256(kStaticMaxTokens * 4);
+
+static __device__ __align__(256) unsigned char g_kmeans_scratch[kStaticScratchBytes];
+
+__device__ __forceinline__ uint64_t splitmix64_dev(uint64_t &state) {
+  uint64_t z = (state += 0x9e3779b97f4a7c15ull);
+  z = (z ^ (z >> 30)) * 0xbf58476d1ce4e5b9ull;
+  z = (z ^ (z >> 27)) * 0x94d049bb133111ebull;
+  return z ^ (z >> 31);
+}
+
+// The initial centroid indices of lkv_build_index (first c entries of a
+// splitmix64-driven partial Fisher-Yates shuffle of [0, n)), drawn on the
+// device so that no host buffer is needed. One block.
+__global__ void k_static_init_indices(int64_t n, int32_t c, uint64_t seed, int64_t *shuffle,
+                                      int64_t *idx) {
+  for (int64_t i = threadIdx.x; i < n; i += blockDim.x) shuffle[i] = i;
+  __syncthreads();
+  if (threadIdx.x != 0) return;
+  uint64_t st = seed;
+  for (int32_t i = 0; i < c; ++i) {
+    const uint64_t r = splitmix64_dev(st);
+    const int64_t j = (int64_t)i + (int64_t)(r % (uint64_t)(n - i));
+    const int64_t t = shuffle[i];
+    shuffle[i] = shuffle[j];
+    shuffle[j] = t;
+    idx[i] = shuffle[i];
+  }
+}
+
+template <int DT>
+static cudaError_t kmeans_static_t(unsigned char *base, const void *keys, int64_t n, int32_t c,
+                                   int32_t iters, uint64_t seed, float *cent, int32_t *assign,
+                                   cudaStream_t st) {
+  CtxView v{};
+  v.dtype = DT;
+  v.B = 1;
+  v.Hkv = 1;
+  v.n_cap = n;
+  v.t_cap = 0;
+  v.u_cap = c;
+  v.cent32 = cent;
+  v.cent_op = base + kSoCentOp;
+  v.assign = assign;
+  v.perm = (int32_t *)(base + kSoPerm);
+  v.err = (int32_t *)(base + kSoMisc + 4);
+  KmeansScratch ks{};
+  ks.knorm = (float *)(base + kSoKnorm);
+  ks.c2 = (float *)(base + kSoC2);
+  ks.cstat = (float *)(base + kSoCstat);
+  ks.cnt_part = (int32_t *)(base + kSoCntPart);
+  ks.count = (int32_t *)(base + kSoCount);
+  ks.offs = (int32_t *)(base + kSoOffs);
+  ks.amb = (int4 *)(base + kSoAmb);
+  ks.amb_count = (int32_t *)(base + kSoMisc);
+  ks.n_refined = (int64_t *)(base + kSoMisc + 8);
+  ks.n_inexact = (int64_t *)(base + kSoMisc + 16);
+  ks.init_idx = (int64_t *)(base + kSoInit);
+  Prof quiet;
+  quiet.counting = false;
+  const int64_t amb_cap = n;
+  const float eps = 0x1p-15f;
+  // the array keeps the previous call's contents: clear what must start at zero
+  cudaError_t e = cudaMemsetAsync(base + kSoMisc, 0, 256, st);
+  if (e != cudaSuccess) return e;
+  k_static_init_indices<<<1, 1024, 0, st>>>(n, c, seed, (int64_t *)(base + kSoShuffle), ks.init_idx);
+  k_init_cent<DT><<<dim3(c, 1), kHeadDim, 0, st>>>(keys, n, c, ks.init_idx, v.cent32, 0, v.u_cap);
+  k_key_norms<DT><<<dim3((unsigned)((n + 7) / 8), 1), 256, 0, st>>>(keys, n, v.n_cap, ks.knorm);
+  for (int it = 0; it < iters; ++it) {
+    e = cudaMemsetAsync(ks.cstat, 0, sizeof(float) * 2, st);
+    if (e != cudaSuccess) return e;
+    k_prepare_operand<DT><<<dim3((c + 7) / 8, 1), 256, 0, st>>>(v.cent32, v.cent_op, c, c, v.u_cap,
+                                                              0, ks.c2, ks.cstat);
+    e = cudaMemsetAsync(ks.amb_count, 0, sizeof(int32_t), st);
+    if (e != cudaSuccess) return e;
+    k_assign_simt<DT><<<dim3((unsigned)((n + kAsTile - 1) / kAsTile), 1), kAsThreads, kAsSmem, st>>>(
+        keys, n, c, v.cent_op, v.u_cap, ks.c2, c, ks.knorm, v.n_cap, ks.cstat, eps, v.assign, 0,
+        ks.amb, ks.amb_count, (int32_t)amb_cap, v.err);
+    k_assign_refine<DT><<<304, 256, 0, st>>>(keys, n, c, v.cent_op, v.u_cap, v.assign, v.n_cap, 0,
+                                             ks.amb, ks.amb_count, (int32_t)amb_cap, ks.n_refined);
+    e = group_and_pool<DT>(v, 0, ks, n, c, 0, 1, st, quiet);
+    if (e != cudaSuccess) return e;
+    k_update<DT><<<dim3((c + 7) / 8, 1), 256, 0, st>>>(keys, n, v.n_cap, c, c, v.u_cap, 0, v.perm,
+                                                       ks.count, ks.offs, v.cent32, ks.n_inexact);
+  }
+  return cudaGetLastError();
+}
+
+// Per-device address of g_kmeans_scratch. In host code the array's name is
+// only a host-side stand-in, so the device address is looked up once per
+// device (with that device current) and cached.
+static std::mutex g_static_mu;
+static void *g_static_addr[64] = {};
+
+static cudaError_t static_scratch_address(void **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (!g_static_addr[dev]) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_kmeans_scratch);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k_assign_simt<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAsSmem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k_assign_simt<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAsSmem);
+    if (e != cudaSuccess) return e;
+    g_static_addr[dev] = p;
+  }
+  *out = g_static_addr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace lkv
+
+extern "C" lkv_status lkv_kmeans_static(const void *keys, int32_t dtype, int64_t n_tokens,
+                                        int32_t n_clusters, int32_t iters, uint64_t seed,
+                                        float *centroids, int32_t *assign, void *stream) {
+  using namespace lkv;
+  if (!keys || !centroids || !assign) {
+    set_unbound_error("lkv_kmeans_static: null keys, centroids or assign");
+    return LKV_EINVAL;
+  }
+  if (dtype != LKV_DTYPE_FP32 && dtype != LKV_DTYPE_BF16) {
+    set_unbound_error("lkv_kmeans_static: bad dtype");
+    return LKV_EINVAL;
+  }
+  if (n_tokens < 1 || n_tokens > kStaticMaxTokens) {
+    set_unbound_error("lkv_kmeans_static: n_tokens must be 1..32768 (size of the built-in scratch)");
+    return LKV_EINVAL;
+  }
+  if (n_clusters < 1 || n_clusters > kStaticMaxClusters || n_clusters > n_tokens) {
+    set_unbound_error("lkv_kmeans_static: n_clusters must be 1..min(2048, n_tokens) "
+                      "(size of the built-in scratch)");
+    return LKV_EINVAL;
+  }
+  if (iters < 1) {
+    set_unbound_error("lkv_kmeans_static: iters must be >= 1");
+    return LKV_EINVAL;
+  }
+  void *base = nullptr;
+  cudaError_t e = static_scratch_address(&base);
+  if (e == cudaSuccess) {
+    cudaStream_t st = (cudaStream_t)stream;
+    e = dtype == LKV_DTYPE_BF16
+            ? kmeans_static_t<1>((unsigned char *)base, keys, n_tokens, n_clusters, iters, seed, centroids, assign, st)
+            : kmeans_static_t<0>((unsigned char *)base, keys, n_tokens, n_clusters, iters, seed, centroids, assign, st);
+  }
+  if (e != cudaSuccess) {
+    set_unbound_error((std::string("lkv_kmeans_static: ") + cudaGetErrorString(e)).c_str());
+    return LKV_ECUDA;
+  }
+  return LKV_OK;
+}
+
+namespace lkv {
 }  // namespace lkv

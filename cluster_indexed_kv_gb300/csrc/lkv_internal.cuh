@@ -257,6 +257,8 @@ struct StepArgs {
 
 cudaError_t launch_decode_step(const CtxView &v, const StepArgs &a, cudaStream_t stream,
                                Prof &prof);
+// Error text of calls that have no context (read with lkv_last_error(NULL)).
+void set_unbound_error(const char *msg);
 // One-time kernel attributes (dynamic shared memory limits), before any capture.
 cudaError_t prepare_kernels(int dtype, int group);
 

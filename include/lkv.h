@@ -223,6 +223,31 @@ typedef struct lkv_decode_state {
   int64_t n_inexact;    /* centroid sums that needed the double fallback */
 } lkv_decode_state;
 
+/* Allocation-free K-means of one (sequence, KV head) slice. The pages have
+ * no counterpart to this call; it exists for callers that must not allocate
+ * GPU memory themselves or through us: a process whose device memory is
+ * owned by another allocator (a serving engine or framework that reserves
+ * the whole GPU up front, so an extra cudaMalloc fails or fragments its
+ * pool), or code that must not risk the implicit device synchronisation of
+ * cudaMalloc/cudaFree. It computes exactly what lkv_build_index computes for
+ * a slice (same seeded initialisation with seed, same Lloyd rounds, same
+ * bit-exact centroids and assignment), without the K/V pool.
+ * keys: device, [n_tokens][d] in dtype; centroids: device fp32
+ * [n_clusters][d], out; assign: device int32 [n_tokens], out; stream: a
+ * cudaStream_t or NULL. Nothing is allocated: every intermediate lives in one
+ * fixed array inside the library (about 2.7 MB, held by every GPU that loads
+ * the library until the process exits), which limits n_tokens to 32768 and
+ * n_clusters to 2048 (LKV_EINVAL beyond). All calls on a GPU share that
+ * array and it keeps the previous call's contents, so calls that may
+ * overlap on the GPU (different streams, different host threads) race: order
+ * them on one stream. The first call on each device looks up the array's
+ * device address and sets kernel attributes, so make that first call before
+ * any stream capture. Asynchronous on stream; errors: LKV_EINVAL, LKV_ECUDA
+ * (text via lkv_last_error(NULL)). */
+lkv_status lkv_kmeans_static(const void *keys, int32_t dtype, int64_t n_tokens,
+                             int32_t n_clusters, int32_t iters, uint64_t seed,
+                             float *centroids, int32_t *assign, void *stream);
+
 /* Blocking read of one (layer, sequence) decode state. */
 lkv_status lkv_get_decode_state(lkv_ctx *ctx, int32_t layer, int32_t seq,
                                 lkv_decode_state *out);
