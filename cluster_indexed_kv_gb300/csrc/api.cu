@@ -200,6 +200,7 @@ lkv_status lkv_create(const lkv_config *cfg, lkv_ctx **out) {
   v.part_acc = (float *)dalloc(c, S_all * max_chunks * G * d * 4, &st);
   v.part_ml = (float *)dalloc(c, S_all * max_chunks * G * 2 * 4, &st);
   v.attn_count = (int32_t *)dalloc(c, S_all * 4, &st);
+  v.score_count = (int32_t *)dalloc(c, S_all * 4, &st);
   v.max_pieces = u_cap + max_chunks;
   v.pieces = (int4 *)dalloc(c, S_all * (int64_t)v.max_pieces * sizeof(int4), &st);
   v.chunk_piece = (int32_t *)dalloc(c, S_all * (int64_t)(max_chunks + 1) * 4, &st);
@@ -227,6 +228,7 @@ lkv_status lkv_create(const lkv_config *cfg, lkv_ctx **out) {
   cudaError_t e = cudaSuccess;
   if (e == cudaSuccess) e = cudaMemsetAsync(v.st, 0, LB * sizeof(DecState), c->stream);
   if (e == cudaSuccess) e = cudaMemsetAsync(v.attn_count, 0, S_all * 4, c->stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(v.score_count, 0, S_all * 4, c->stream);
   if (e == cudaSuccess) e = cudaMemsetAsync(v.err, 0, 4, c->stream);
   if (e == cudaSuccess) e = cudaMemsetAsync(ks.n_refined, 0, 8, c->stream);
   if (e == cudaSuccess) e = cudaMemsetAsync(ks.n_inexact, 0, 8, c->stream);
@@ -358,7 +360,7 @@ static lkv::StepArgs step_args(lkv_ctx *c, int32_t layer, int32_t nl, bool multi
   return a;
 }
 
-static int kernels_per_step(const lkv_ctx *c) { return c->v.offload ? 5 : 4; }
+static int kernels_per_step(const lkv_ctx *c) { return c->v.offload ? 4 : 3; }
 
 lkv_status lkv_decode_step(lkv_ctx *c, int32_t layer, int32_t nl, const void *q,
                            const void *k_new, const void *v_new, float tau, int32_t budget,
@@ -430,7 +432,7 @@ lkv_status lkv_decode_steps(lkv_ctx *c, int32_t layer, int32_t nl, int32_t n_ste
     const int reps = n_steps / kGraphSteps, tail = n_steps % kGraphSteps;
     for (int r = 0; r < reps && e == cudaSuccess; ++r) e = cudaGraphLaunch(exec, c->stream);
     if (e == cudaSuccess && c->prof.counting) {
-      const int kinds[5] = {lkv::kPBoundary, lkv::kPScore, lkv::kPSelect, lkv::kPAttn, lkv::kPGather};
+      const int kinds[4] = {lkv::kPBoundary, lkv::kPScore, lkv::kPAttn, lkv::kPGather};
       for (int k = 0; k < kernels_per_step(c); ++k) c->prof.launches[kinds[k]] += (int64_t)reps * kGraphSteps;
     }
     for (int i = 0; i < tail && e == cudaSuccess; ++i) e = lkv::launch_decode_step(c->v, a, c->stream, c->prof);
@@ -441,7 +443,7 @@ lkv_status lkv_decode_steps(lkv_ctx *c, int32_t layer, int32_t nl, int32_t n_ste
 }
 
 static const char *kKindNames[lkv::kPNum] = {
-    "lkv_boundary", "lkv_score", "lkv_select", "lkv_gather_offload", "lkv_attn",
+    "lkv_boundary", "lkv_score_select", "lkv_gather_offload", "lkv_attn",
     "kmeans_init", "kmeans_operand", "kmeans_assign", "kmeans_refine", "kmeans_sort",
     "kmeans_update", "kmeans_pool"};
 

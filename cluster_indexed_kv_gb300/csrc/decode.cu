@@ -3,13 +3,15 @@
 //
 //   k_step_boundary  r_t, trigger flag, segment close, local-buffer eviction,
 //                    append of token t                      (1 CTA / (seq, layer))
-//   k_score          s_u = qbar . c_u for every unit         (trigger steps only)
-//   k_select         (score desc, id asc) budget prefix, plus the copy plan of
-//                    the selected rows in 64-token chunks    (trigger steps only)
+//   k_score_select   s_u = qbar . c_u for every unit; the last score CTA of a
+//                    (seq, layer, kv head) then takes the (score desc, id asc)
+//                    budget prefix and writes the copy plan of the selected
+//                    rows in 64-token chunks                 (trigger steps only)
 //   k_gather_offload selected rows host -> HBM staging (UVA; offload only)
-//   k_attn           split-K softmax attention: each CTA stages one 64-token
-//                    chunk of (selected rows ++ local buffer) with bulk copies,
-//                    the last CTA of each (seq, layer, kv head) combines
+//   k_attn           split-K softmax attention: each CTA streams a run of
+//                    64-token chunks of (selected rows ++ local buffer) through
+//                    a 3-stage bulk-copy ring; the last CTA of each
+//                    (seq, layer, kv head) combines the partials
 //
 // Inputs/outputs of step k of a call live at base + k * stride (StepArgs).
 #include "lkv_internal.cuh"
@@ -278,48 +280,7 @@ __global__ void __launch_bounds__(1024) k_step_boundary(CtxView v, StepArgs a) {
   }
 }
 
-// ---------------------------------------------------------------- scoring
-
-template <int DT>
-__global__ void __launch_bounds__(256) k_score(CtxView v, StepArgs a) {
-  const int per_l = v.B * v.Hkv;
-  const int li = blockIdx.x / per_l, rem = blockIdx.x % per_l;
-  const int b = rem / v.Hkv, h = rem % v.Hkv;
-  const int l = a.l0 + li;
-  const int64_t lb = (int64_t)l * v.B + b;
-  const int64_t gs = lb * v.Hkv + h;
-  const DecState *stp = v.st + lb;
-  if (!stp->flag) return;
-  const int U = stp->n_units;
-  const int64_t k = (stp->t - 1) - a.base_t;
-  const void *q = (const char *)a.q + k * a.stride_q * elem_bytes<DT>();
-  __shared__ float qbar[kHeadDim];
-  const int H = v.Hkv * v.G;
-  const int64_t qoff = (((int64_t)b * a.nl + li) * H + (int64_t)h * v.G) * kHeadDim;
-  if (threadIdx.x < kHeadDim) {
-    float acc = load_elem<DT>(q, qoff + threadIdx.x);
-    for (int g = 1; g < v.G; ++g) acc = __fadd_rn(acc, load_elem<DT>(q, qoff + (int64_t)g * kHeadDim + threadIdx.x));
-    qbar[threadIdx.x] = acc;
-  }
-  __syncthreads();
-  constexpr int per16 = 16 / elem_bytes<DT>();
-  for (int u = blockIdx.y * blockDim.x + threadIdx.x; u < U; u += gridDim.y * blockDim.x) {
-    const int64_t base = (gs * v.u_cap + u) * kHeadDim;
-    float s = 0.f;
-#pragma unroll 4
-    for (int j0 = 0; j0 < kHeadDim; j0 += per16) {
-      float c[8];
-      load16<DT>(v.cent_op, base + j0, c);
-#pragma unroll
-      for (int e = 0; e < per16; ++e) s = __fmaf_rn(qbar[j0 + e], c[e], s);
-    }
-    v.scores[gs * v.u_cap + u] = s;
-  }
-  if (blockIdx.y == 0 && threadIdx.x == 0)
-    atomicAdd((unsigned long long *)&v.counters[kCntScoreUnits], (unsigned long long)U);
-}
-
-// ---------------------------------------------------------------- selection
+// ---------------------------------------------------------------- scoring + selection
 
 __device__ __forceinline__ int32_t block_scan_excl(int32_t x, int32_t *wt, int32_t *total) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
@@ -347,27 +308,21 @@ __device__ __forceinline__ int32_t block_scan_excl(int32_t x, int32_t *wt, int32
   return r;
 }
 
-// Weighted radix select of the cut: the smallest key value K* (desc_key of a
-// score) with sum_{key <= K*} len > budget. Units with key < K* all precede
-// the first unit that does not fit; units with key == K* are taken in id
-// order while they fit. Output: ascending unit ids, their first rows, the
-// exclusive token prefix, and the copy plan: the selected rows cut into
-// pieces that never cross a 64-token chunk boundary.
-__global__ void __launch_bounds__(1024) k_select(CtxView v, StepArgs a) {
-  const int per_l = v.B * v.Hkv;
-  const int li = blockIdx.x / per_l, rem = blockIdx.x % per_l;
-  const int b = rem / v.Hkv, h = rem % v.Hkv;
-  const int l = a.l0 + li;
-  const int64_t lb = (int64_t)l * v.B + b;
-  const int64_t gs = lb * v.Hkv + h;
-  const DecState *stp = v.st + lb;
-  if (!stp->flag) return;
-  const int U = stp->n_units;
-  const int budget = a.budget;
+constexpr int kScoreThreads = 256;
+constexpr int kScoreWarps = kScoreThreads / 32;
+
+// Budget selection of one (seq, layer, kv head) by the whole block: a
+// length-weighted radix select of the cut K* (the smallest desc_key value
+// with sum_{key <= K*} len > budget). Units with key < K* all precede the
+// first unit that does not fit; units with key == K* are taken in id order
+// while they fit. Output: ascending unit ids, their first rows, the exclusive
+// token prefix, and the copy plan (selected rows cut at 64-token chunk
+// boundaries).
+__device__ void select_units(const CtxView &v, int64_t gs, int U, int budget) {
   const float *sc = v.scores + gs * v.u_cap;
   const int32_t *ln = v.unit_len + gs * v.u_cap;
   const int tid = threadIdx.x, nth = blockDim.x, wid = tid >> 5;
-  __shared__ int32_t whist[32][256];
+  __shared__ int32_t whist[kScoreWarps][256];
   __shared__ int32_t wt[32];
   __shared__ int32_t s_total, s_below, s_all, s_nsel, s_ntok, s_npieces;
   __shared__ uint32_t s_prefix, s_mask;
@@ -385,23 +340,23 @@ __global__ void __launch_bounds__(1024) k_select(CtxView v, StepArgs a) {
   if (!s_all) {
     for (int pass = 0; pass < 4; ++pass) {
       const int shift = 24 - 8 * pass;
-      for (int x = tid; x < 32 * 256; x += nth) (&whist[0][0])[x] = 0;
+      for (int x = tid; x < kScoreWarps * 256; x += nth) (&whist[0][0])[x] = 0;
       __syncthreads();
       const uint32_t prefix = s_prefix, mask = s_mask;
       for (int u = tid; u < U; u += nth) {
-        const uint32_t key = desc_key(sc[u]);
+        const uint32_t key = desc_key(__ldcg(sc + u));
         if ((key & mask) == prefix) atomicAdd(&whist[wid][(key >> shift) & 255u], ln[u]);
       }
       __syncthreads();
-      if (tid < 256) {
+      for (int bin = tid; bin < 256; bin += nth) {
         int32_t tot = 0;
-        for (int w = 0; w < 32; ++w) tot += whist[w][tid];
-        whist[0][tid] = tot;
+        for (int w = 0; w < kScoreWarps; ++w) tot += whist[w][bin];
+        whist[0][bin] = tot;
       }
       __syncthreads();
       if (tid < 32) {
-        // warp scan over the 256 bins (8 per lane) for the bin where the
-        // running weight first exceeds the budget
+        // warp scan over the 256 bins (8 per lane): the bin where the running
+        // weight first exceeds the budget
         int32_t loc[8], sum = 0;
 #pragma unroll
         for (int e = 0; e < 8; ++e) { loc[e] = whist[0][tid * 8 + e]; sum += loc[e]; }
@@ -411,9 +366,8 @@ __global__ void __launch_bounds__(1024) k_select(CtxView v, StepArgs a) {
           const int32_t y = __shfl_up_sync(kFull, inc, o);
           if (tid >= o) inc += y;
         }
-        const int32_t base = s_below + inc - sum;
         int found = -1;
-        int32_t run = base;
+        int32_t run = s_below + inc - sum;
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           if (found < 0 && run + loc[e] > budget) found = e;
@@ -437,24 +391,27 @@ __global__ void __launch_bounds__(1024) k_select(CtxView v, StepArgs a) {
   const int32_t below = s_below;
   const int per = (U + nth - 1) / nth;
   const int u0 = tid * per, u1 = min(U, u0 + per);
+  auto is_sel = [&](int u, int32_t &run) -> bool {
+    if (all) return true;
+    const uint32_t key = desc_key(__ldcg(sc + u));
+    if (key < kstar) return true;
+    if (key == kstar) {
+      run += ln[u];
+      return below + run <= budget;
+    }
+    return false;
+  };
   // exclusive id-order prefix of the tied units' lengths
   int32_t tl = 0;
   if (!all)
     for (int u = u0; u < u1; ++u)
-      if (desc_key(sc[u]) == kstar) tl += ln[u];
+      if (desc_key(__ldcg(sc + u)) == kstar) tl += ln[u];
   const int32_t tie_ex = block_scan_excl(tl, wt, nullptr);
   int32_t cnt = 0, toks = 0;
   {
     int32_t run = tie_ex;
-    for (int u = u0; u < u1; ++u) {
-      bool sel = all;
-      if (!all) {
-        const uint32_t key = desc_key(sc[u]);
-        if (key < kstar) sel = true;
-        else if (key == kstar) { run += ln[u]; sel = below + run <= budget; }
-      }
-      if (sel) { ++cnt; toks += ln[u]; }
-    }
+    for (int u = u0; u < u1; ++u)
+      if (is_sel(u, run)) { ++cnt; toks += ln[u]; }
   }
   const int32_t cnt_ex = block_scan_excl(cnt, wt, &s_nsel);
   const int32_t tok_ex = block_scan_excl(toks, wt, &s_ntok);
@@ -466,21 +423,14 @@ __global__ void __launch_bounds__(1024) k_select(CtxView v, StepArgs a) {
     int32_t *cum_out = v.rng_cum + gs * (int64_t)(v.u_cap + 1);
     const int32_t *rows = v.unit_row + gs * v.u_cap;
     for (int u = u0; u < u1; ++u) {
-      bool sel = all;
-      if (!all) {
-        const uint32_t key = desc_key(sc[u]);
-        if (key < kstar) sel = true;
-        else if (key == kstar) { run += ln[u]; sel = below + run <= budget; }
-      }
-      if (sel) {
-        const int32_t len = ln[u];
-        sel_out[kk] = u;
-        row_out[kk] = rows[u];
-        cum_out[kk] = cum;
-        if (len > 0) npc += (cum + len - 1) / kAttnChunk - cum / kAttnChunk + 1;
-        cum += len;
-        ++kk;
-      }
+      if (!is_sel(u, run)) continue;
+      const int32_t len = ln[u];
+      sel_out[kk] = u;
+      row_out[kk] = rows[u];
+      cum_out[kk] = cum;
+      if (len > 0) npc += (cum + len - 1) / kAttnChunk - cum / kAttnChunk + 1;
+      cum += len;
+      ++kk;
     }
   }
   const int32_t pc_ex = block_scan_excl(npc, wt, &s_npieces);
@@ -490,13 +440,7 @@ __global__ void __launch_bounds__(1024) k_select(CtxView v, StepArgs a) {
     int32_t *cp = v.chunk_piece + gs * (int64_t)(v.max_chunks + 1);
     const int32_t *rows = v.unit_row + gs * v.u_cap;
     for (int u = u0; u < u1 && p - pc_ex < npc; ++u) {
-      bool sel = all;
-      if (!all) {
-        const uint32_t key = desc_key(sc[u]);
-        if (key < kstar) sel = true;
-        else if (key == kstar) { run += ln[u]; sel = below + run <= budget; }
-      }
-      if (!sel) continue;
+      if (!is_sel(u, run)) continue;
       int32_t len = ln[u], src = rows[u], f = cum;
       cum += len;
       while (len > 0) {
@@ -519,6 +463,57 @@ __global__ void __launch_bounds__(1024) k_select(CtxView v, StepArgs a) {
     const int nsc = (s_ntok + kAttnChunk - 1) / kAttnChunk;
     if (nsc <= v.max_chunks) v.chunk_piece[gs * (int64_t)(v.max_chunks + 1) + nsc] = s_npieces;
     if (s_ntok > budget || s_npieces > v.max_pieces) set_err(v.err, kErrInternal);
+  }
+}
+
+// Scores of every unit (one thread per unit, fp32 FMA in index order), then
+// the last CTA of the (seq, layer, kv head) to finish runs the selection.
+template <int DT>
+__global__ void __launch_bounds__(kScoreThreads) k_score_select(CtxView v, StepArgs a) {
+  const int per_l = v.B * v.Hkv;
+  const int li = blockIdx.x / per_l, rem = blockIdx.x % per_l;
+  const int b = rem / v.Hkv, h = rem % v.Hkv;
+  const int l = a.l0 + li;
+  const int64_t lb = (int64_t)l * v.B + b;
+  const int64_t gs = lb * v.Hkv + h;
+  const DecState *stp = v.st + lb;
+  if (!stp->flag) return;
+  const int U = stp->n_units;
+  const int64_t k = (stp->t - 1) - a.base_t;
+  const void *q = (const char *)a.q + k * a.stride_q * elem_bytes<DT>();
+  __shared__ float qbar[kHeadDim];
+  __shared__ int s_last;
+  const int H = v.Hkv * v.G;
+  const int64_t qoff = (((int64_t)b * a.nl + li) * H + (int64_t)h * v.G) * kHeadDim;
+  if (threadIdx.x < kHeadDim) {
+    float acc = load_elem<DT>(q, qoff + threadIdx.x);
+    for (int g = 1; g < v.G; ++g) acc = __fadd_rn(acc, load_elem<DT>(q, qoff + (int64_t)g * kHeadDim + threadIdx.x));
+    qbar[threadIdx.x] = acc;
+  }
+  __syncthreads();
+  constexpr int per16 = 16 / elem_bytes<DT>();
+  for (int u = blockIdx.y * blockDim.x + threadIdx.x; u < U; u += gridDim.y * blockDim.x) {
+    const int64_t base = (gs * v.u_cap + u) * kHeadDim;
+    float s = 0.f;
+#pragma unroll 4
+    for (int j0 = 0; j0 < kHeadDim; j0 += per16) {
+      float c[8];
+      load16<DT>(v.cent_op, base + j0, c);
+#pragma unroll
+      for (int e = 0; e < per16; ++e) s = __fmaf_rn(qbar[j0 + e], c[e], s);
+    }
+    v.scores[gs * v.u_cap + u] = s;
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = (atomicAdd(&v.score_count[gs], 1) == (int)gridDim.y - 1);
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  select_units(v, gs, U, a.budget);
+  if (threadIdx.x == 0) {
+    v.score_count[gs] = 0;
+    atomicAdd((unsigned long long *)&v.counters[kCntScoreUnits], (unsigned long long)U);
   }
 }
 
@@ -566,64 +561,119 @@ __global__ void __launch_bounds__(256) k_gather_offload(CtxView v, StepArgs a) {
 // ---------------------------------------------------------------- attention
 
 constexpr int kAttnWarps = 4;
+constexpr int kAttnThreads = kAttnWarps * 32;
 constexpr int kTokPerWarp = kAttnChunk / kAttnWarps;  // 16
+constexpr int kStages = 3;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;      // 2 s
 
-// Butterfly reduce-scatter of 32 per-lane partials (P == 32) or of 16
-// partials replicated over both half-warps (P == 16): on return lane L holds
-// the full sum of partial index L % P.
-template <int P>
-__device__ __forceinline__ float reduce_scatter(float (&x)[32], int lane) {
-  if constexpr (P == 32) {
-    const bool up = lane & 16;
+union F2U {
+  float2 f;
+  unsigned long long u;
+};
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  F2U x{a}, y{b}, z{c}, r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r.u) : "l"(x.u), "l"(y.u), "l"(z.u));
+  return r.f;
+}
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+  F2U x{a}, y{b}, r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r.u) : "l"(x.u), "l"(y.u));
+  return r.f;
+}
+
+// 16 elements of a row owned by lane k of an 8-lane group: dims
+// [8k, 8k + 8) and [64 + 8k, 64 + 8k + 8), as 8 float pairs. For bf16 rows
+// the group's lanes read each 128-byte half of the row contiguously.
+template <int DT>
+__device__ __forceinline__ void row16(const unsigned char *row, int k, float2 (&o)[8]) {
+  if constexpr (DT == 1) {
+    const uint4 a = *(const uint4 *)(row + 16 * k);
+    const uint4 b = *(const uint4 *)(row + 128 + 16 * k);
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const float send = up ? x[j] : x[j + 16];
-      const float keep = up ? x[j + 16] : x[j];
-      x[j] = keep + __shfl_xor_sync(kFull, send, 16);
-    }
+    for (int p = 0; p < 8; ++p) o[p] = make_float2(__uint_as_float(w[p] << 16), __uint_as_float(w[p] & 0xffff0000u));
   } else {
-#pragma unroll
-    for (int j = 0; j < 16; ++j) x[j] += __shfl_xor_sync(kFull, x[j], 16);
+    const float4 a = *(const float4 *)(row + 32 * k);
+    const float4 b = *(const float4 *)(row + 32 * k + 16);
+    const float4 c = *(const float4 *)(row + 256 + 32 * k);
+    const float4 d = *(const float4 *)(row + 256 + 32 * k + 16);
+    o[0] = make_float2(a.x, a.y); o[1] = make_float2(a.z, a.w);
+    o[2] = make_float2(b.x, b.y); o[3] = make_float2(b.z, b.w);
+    o[4] = make_float2(c.x, c.y); o[5] = make_float2(c.z, c.w);
+    o[6] = make_float2(d.x, d.y); o[7] = make_float2(d.z, d.w);
   }
+}
+
+// Element index (within the head) of pair p, element e, owned by lane k.
+__device__ __forceinline__ int dim_of(int k, int p, int e) {
+  return (p < 4 ? 8 * k + 2 * p : 64 + 8 * k + 2 * (p - 4)) + e;
+}
+
+// Reduce the per-lane partial dot products of the G heads of one token over
+// its 8-lane group; on return lane k holds the full score of head
+// head_of_lane<G>(k).
+template <int G>
+__device__ __forceinline__ float reduce_heads(float (&x)[G], int lane) {
+  const bool b2 = lane & 4, b1 = lane & 2, b0 = lane & 1;
+  if constexpr (G == 8) {
 #pragma unroll
-  for (int m = 8; m >= 1; m >>= 1) {
-    const bool up = lane & m;
-#pragma unroll
-    for (int j = 0; j < m; ++j) {
-      const float send = up ? x[j] : x[j + m];
-      const float keep = up ? x[j + m] : x[j];
-      x[j] = keep + __shfl_xor_sync(kFull, send, m);
+    for (int j = 0; j < 4; ++j) {
+      const float send = b2 ? x[j] : x[j + 4], keep = b2 ? x[j + 4] : x[j];
+      x[j] = keep + __shfl_xor_sync(kFull, send, 4);
     }
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const float send = b1 ? x[j] : x[j + 2], keep = b1 ? x[j + 2] : x[j];
+      x[j] = keep + __shfl_xor_sync(kFull, send, 2);
+    }
+    const float send = b0 ? x[0] : x[1], keep = b0 ? x[1] : x[0];
+    return keep + __shfl_xor_sync(kFull, send, 1);
+  } else if constexpr (G == 4) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const float send = b2 ? x[j] : x[j + 2], keep = b2 ? x[j + 2] : x[j];
+      x[j] = keep + __shfl_xor_sync(kFull, send, 4);
+    }
+    const float send = b1 ? x[0] : x[1], keep = b1 ? x[1] : x[0];
+    float r = keep + __shfl_xor_sync(kFull, send, 2);
+    return r + __shfl_xor_sync(kFull, r, 1);
+  } else if constexpr (G == 2) {
+    const float send = b2 ? x[0] : x[1], keep = b2 ? x[1] : x[0];
+    float r = keep + __shfl_xor_sync(kFull, send, 4);
+    r += __shfl_xor_sync(kFull, r, 2);
+    return r + __shfl_xor_sync(kFull, r, 1);
+  } else {
+    float r = x[0];
+    r += __shfl_xor_sync(kFull, r, 4);
+    r += __shfl_xor_sync(kFull, r, 2);
+    return r + __shfl_xor_sync(kFull, r, 1);
   }
-  return x[0];
+}
+
+template <int G>
+__device__ __forceinline__ int head_of_lane(int k) {
+  if constexpr (G == 8) return ((k >> 2) & 1) * 4 + ((k >> 1) & 1) * 2 + (k & 1);
+  else if constexpr (G == 4) return ((k >> 2) & 1) * 2 + ((k >> 1) & 1);
+  else if constexpr (G == 2) return (k >> 2) & 1;
+  else return 0;
 }
 
 template <int DT>
-__device__ __forceinline__ void row4(const unsigned char *row, int lane, float (&o)[4]) {
-  if constexpr (DT == 1) {
-    const uint2 r = *(const uint2 *)(row + lane * 8);
-    o[0] = __uint_as_float(r.x << 16); o[1] = __uint_as_float(r.x & 0xffff0000u);
-    o[2] = __uint_as_float(r.y << 16); o[3] = __uint_as_float(r.y & 0xffff0000u);
-  } else {
-    const float4 r = *(const float4 *)(row + lane * 16);
-    o[0] = r.x; o[1] = r.y; o[2] = r.z; o[3] = r.w;
-  }
-}
+constexpr int stage_bytes() { return 2 * kAttnChunk * kHeadDim * elem_bytes<DT>(); }
 
+// Split-K attention. CTA (slice, split) streams chunks [split * cpc, ...) of
+// the slice's token list (selected rows, then the local buffer) through a
+// 3-stage ring of shared-memory buffers filled by bulk copies. Per chunk,
+// each warp owns 16 rows: pass 1 scores them (8 lanes per row, 4 rows per
+// instruction), pass 2 adds p * V into per-lane accumulators.
 template <int DT, int G>
-__global__ void __launch_bounds__(kAttnWarps * 32) k_attn(CtxView v, StepArgs a) {
+__global__ void __launch_bounds__(kAttnThreads, 2) k_attn(CtxView v, StepArgs a, int cpc) {
   constexpr int RB = kHeadDim * elem_bytes<DT>();
-  constexpr int TB = (32 / G) < kTokPerWarp ? (32 / G) : kTokPerWarp;  // tokens per batch
-  constexpr int P = TB * G;                                           // partials per lane
-  constexpr int NB = kTokPerWarp / TB;
+  constexpr int SB = stage_bytes<DT>();
   extern __shared__ __align__(128) unsigned char smem[];
-  unsigned char *Ks = smem;                      // [64][RB]
-  unsigned char *Vs = smem + kAttnChunk * RB;    // [64][RB]
-  __shared__ __align__(8) uint64_t bar;
+  __shared__ __align__(8) uint64_t bar[kStages];
   __shared__ float qs[G][kHeadDim];
-  __shared__ float ps[kAttnWarps][32];
-  __shared__ float cs[kAttnWarps][G];
+  __shared__ __align__(16) float S[kAttnChunk][G];
   __shared__ float wm[kAttnWarps][G], wl[kAttnWarps][G];
   __shared__ float wacc[kAttnWarps][G][kHeadDim];
   __shared__ int s_last, s_ok;
@@ -635,174 +685,220 @@ __global__ void __launch_bounds__(kAttnWarps * 32) k_attn(CtxView v, StepArgs a)
   const int64_t lb = (int64_t)l * v.B + b;
   const int64_t gs = lb * v.Hkv + h;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int grp = lane >> 3, kk = lane & 7;
   const DecState st = v.st[lb];
   const int t_cur = st.t - 1, ws = st.win_start;
   const int64_t k = t_cur - a.base_t;
   const int nt = v.n_tok[gs];
   const int total = nt + (t_cur - ws + 1);
   const int H = v.Hkv * G;
-  const int nchunks = gridDim.y;
-  const int chunk = blockIdx.y;
-  const int f0 = chunk * kAttnChunk;
-  const int nrow = max(0, min(kAttnChunk, total - f0));
+  const int nsplit = gridDim.y, split = blockIdx.y;
+  const int nch = (total + kAttnChunk - 1) / kAttnChunk;
+  const int c_begin = split * cpc;
+  const int n_my = max(0, min(cpc, nch - c_begin));
 
-  // --- stage the chunk's rows: warp 0 issues one bulk copy per piece
   if (tid == 0) {
-    mbar_init(&bar, 1);
+    for (int i = 0; i < kStages; ++i) mbar_init(&bar[i], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
-  if (wid == 0) {
-    int p0 = 0, p1 = 0;
-    const unsigned char *selk, *selv;
-    if (!v.offload) {
-      selk = (const unsigned char *)v.pool_k + gs * v.pool_rows * RB;
-      selv = (const unsigned char *)v.pool_v + gs * v.pool_rows * RB;
-      if (f0 < nt) {
+
+  const unsigned char *selk, *selv;
+  if (!v.offload) {
+    selk = (const unsigned char *)v.pool_k + gs * v.pool_rows * RB;
+    selv = (const unsigned char *)v.pool_v + gs * v.pool_rows * RB;
+  } else {
+    selk = (const unsigned char *)v.stage_k + gs * (int64_t)v.bud_cap * RB;
+    selv = (const unsigned char *)v.stage_v + gs * (int64_t)v.bud_cap * RB;
+  }
+  // warp 0 fills stage (i % kStages) with chunk c_begin + i
+  auto issue = [&](int i) {
+    unsigned char *Ks = smem + (i % kStages) * SB;
+    unsigned char *Vs = Ks + SB / 2;
+    uint64_t *br = &bar[i % kStages];
+    const int c = c_begin + i, f0 = c * kAttnChunk;
+    const int nrow = min(kAttnChunk, total - f0);
+    int p0 = 0, p1 = 0, sel_direct = 0;
+    if (f0 < nt) {
+      if (!v.offload) {
         const int32_t *cp = v.chunk_piece + gs * (int64_t)(v.max_chunks + 1);
         const int nsc = (nt + kAttnChunk - 1) / kAttnChunk;
-        p0 = cp[chunk];
-        p1 = (chunk + 1 < nsc) ? cp[chunk + 1] : cp[nsc];
+        p0 = cp[c];
+        p1 = (c + 1 < nsc) ? cp[c + 1] : cp[nsc];
+      } else {
+        sel_direct = min(f0 + kAttnChunk, nt) - f0;
       }
-    } else {
-      selk = (const unsigned char *)v.stage_k + gs * (int64_t)v.bud_cap * RB;
-      selv = (const unsigned char *)v.stage_v + gs * (int64_t)v.bud_cap * RB;
     }
-    uint32_t bytes = 0;
     const int4 *pieces = v.pieces + gs * (int64_t)v.max_pieces;
+    uint32_t bytes = 0;
     for (int p = p0 + lane; p < p1; p += 32) bytes += 2u * (uint32_t)pieces[p].z * RB;
-    const int win0 = max(f0, nt), win1 = f0 + nrow;  // local-buffer part of the chunk
-    int sel_direct = 0;                              // offload: staged rows, one piece
-    if (v.offload && f0 < nt) sel_direct = min(f0 + kAttnChunk, nt) - f0;
-    if (lane == 0) {
-      if (win1 > win0) bytes += 2u * (uint32_t)(win1 - win0) * RB;
-      bytes += 2u * (uint32_t)sel_direct * RB;
-    }
+    const int win0 = max(f0, nt), win1 = f0 + nrow;
+    if (lane == 0) bytes += 2u * (uint32_t)(max(win1 - win0, 0) + sel_direct) * RB;
 #pragma unroll
     for (int o = 16; o; o >>= 1) bytes += __shfl_xor_sync(kFull, bytes, o);
-    if (lane == 0) mbar_arrive_expect_tx(&bar, bytes);
+    if (lane == 0) mbar_arrive_expect_tx(br, bytes);
     __syncwarp();
     for (int p = p0 + lane; p < p1; p += 32) {
       const int4 pc = pieces[p];
       const int dr = pc.y - f0;
-      bulk_g2s(Ks + dr * RB, selk + (int64_t)pc.x * RB, (uint32_t)pc.z * RB, &bar);
-      bulk_g2s(Vs + dr * RB, selv + (int64_t)pc.x * RB, (uint32_t)pc.z * RB, &bar);
+      bulk_g2s(Ks + dr * RB, selk + (int64_t)pc.x * RB, (uint32_t)pc.z * RB, br);
+      bulk_g2s(Vs + dr * RB, selv + (int64_t)pc.x * RB, (uint32_t)pc.z * RB, br);
     }
     if (lane == 0) {
       if (sel_direct > 0) {
-        bulk_g2s(Ks, selk + (int64_t)f0 * RB, (uint32_t)sel_direct * RB, &bar);
-        bulk_g2s(Vs, selv + (int64_t)f0 * RB, (uint32_t)sel_direct * RB, &bar);
+        bulk_g2s(Ks, selk + (int64_t)f0 * RB, (uint32_t)sel_direct * RB, br);
+        bulk_g2s(Vs, selv + (int64_t)f0 * RB, (uint32_t)sel_direct * RB, br);
       }
       if (win1 > win0) {
         const int64_t r0 = gs * v.dec_rows + ws + (win0 - nt);
         bulk_g2s(Ks + (win0 - f0) * RB, (const unsigned char *)v.dec_k + r0 * RB,
-                 (uint32_t)(win1 - win0) * RB, &bar);
+                 (uint32_t)(win1 - win0) * RB, br);
         bulk_g2s(Vs + (win0 - f0) * RB, (const unsigned char *)v.dec_v + r0 * RB,
-                 (uint32_t)(win1 - win0) * RB, &bar);
+                 (uint32_t)(win1 - win0) * RB, br);
       }
     }
-  }
+  };
+  if (wid == 0)
+    for (int i = 0; i < min(n_my, kStages); ++i) issue(i);
+
   // query rows of the group, pre-scaled by log2(e)/sqrt(d) (scores in base 2)
   const float qscale = 1.4426950408889634f * rsqrtf((float)kHeadDim);
   const void *q = (const char *)a.q + k * a.stride_q * elem_bytes<DT>();
   const int64_t qoff = (((int64_t)b * a.nl + li) * H + (int64_t)h * G) * kHeadDim;
-  for (int x = tid; x < G * kHeadDim; x += blockDim.x)
+  for (int x = tid; x < G * kHeadDim; x += kAttnThreads)
     qs[x / kHeadDim][x % kHeadDim] = load_elem<DT>(q, qoff + x) * qscale;
-  if (tid == 0) s_ok = mbar_wait_bounded(&bar, 0, kWaitLimitNs) ? 1 : 0;
+  if (tid == 0) s_ok = 1;
   __syncthreads();
-  if (!s_ok) {
-    // the copies did not land in time: record it and wait (bounded) once more
-    // so that no copy is still writing this block's shared memory at exit
-    if (tid == 0) {
-      set_err(v.err, kErrTimeout);
-      mbar_wait_bounded(&bar, 0, kWaitLimitNs);
-    }
-    __syncthreads();
-  } else {
-    mbar_wait_bounded(&bar, 0, kWaitLimitNs);  // completes at once; orders the reads below
-  }
-
-  float qr[G][4];
+  float2 q2[G][8];
 #pragma unroll
   for (int g = 0; g < G; ++g)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) qr[g][e] = qs[g][lane * 4 + e];
+    for (int p = 0; p < 8; ++p) q2[g][p] = make_float2(qs[g][dim_of(kk, p, 0)], qs[g][dim_of(kk, p, 1)]);
 
-  const int own = lane % P;  // partial index (token own / G, head own % G) this lane owns
-  float m_own = -INFINITY, l_own = 0.f;
-  float acc[G][4];
+  const int hl = head_of_lane<G>(kk);          // head whose score this lane ends with
+  const int own_g = lane % G;                   // head of this lane's softmax bookkeeping
+  float m_run[G];
+#pragma unroll
+  for (int g = 0; g < G; ++g) m_run[g] = -INFINITY;
+  float m_own = -INFINITY, l_own = 0.f;  // running max and sum of head own_g
+  float2 acc[G][8];
 #pragma unroll
   for (int g = 0; g < G; ++g)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) acc[g][e] = 0.f;
+    for (int p = 0; p < 8; ++p) acc[g][p] = make_float2(0.f, 0.f);
 
+  const int r0 = wid * kTokPerWarp;
+  for (int i = 0; i < n_my; ++i) {
+    const unsigned char *Ks = smem + (i % kStages) * SB;
+    const unsigned char *Vs = Ks + SB / 2;
+    if (!mbar_wait_bounded(&bar[i % kStages], (i / kStages) & 1, kWaitLimitNs)) s_ok = 0;
+    const int nrow = min(kAttnChunk, total - (c_begin + i) * kAttnChunk);
+    // pass 1: scores of this warp's 16 rows, 4 rows per instruction
 #pragma unroll
-  for (int bt = 0; bt < NB; ++bt) {
-    const int r0 = wid * kTokPerWarp + bt * TB;
-    float part[32];
-#pragma unroll
-    for (int i = 0; i < TB; ++i) {
-      float kk[4];
-      row4<DT>(Ks + (r0 + i) * RB, lane, kk);
+    for (int it = 0; it < kTokPerWarp / 4; ++it) {
+      const int r = r0 + it * 4 + grp;
+      float2 kv[8];
+      row16<DT>(Ks + r * RB, kk, kv);
+      float part[G];
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        float s = qr[g][0] * kk[0];
-        s = fmaf(qr[g][1], kk[1], s);
-        s = fmaf(qr[g][2], kk[2], s);
-        s = fmaf(qr[g][3], kk[3], s);
-        part[i * G + g] = s;
+        float2 s2 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int p = 0; p < 8; ++p) s2 = ffma2(q2[g][p], kv[p], s2);
+        part[g] = s2.x + s2.y;
       }
+      float s = reduce_heads<G>(part, lane);
+      if (r >= nrow) s = -INFINITY;
+      if ((kk & (8 / G - 1)) == 0) S[r][hl] = s;
     }
-#pragma unroll
-    for (int j = P; j < 32; ++j) part[j] = 0.f;
-    float s = reduce_scatter<P>(part, lane);
-    if (r0 + own / G >= nrow) s = -INFINITY;
-    float mx = s;
-#pragma unroll
-    for (int msk = G; msk < P; msk <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, msk));
-    const float m_new = fmaxf(m_own, mx);
-    const float corr = (m_own == -INFINITY) ? 0.f : exp2f(m_own - m_new);
-    const float p = (s == -INFINITY) ? 0.f : exp2f(s - m_new);
-    l_own = l_own * corr + p;
-    m_own = m_new;
-    if (lane < P) ps[wid][lane] = p;
-    if (lane < G) cs[wid][lane] = corr;
     __syncwarp();
+    // chunk maximum per head over the warp's rows, softmax weights in place
+    float mx = -INFINITY;
+    for (int x = lane; x < kTokPerWarp * G; x += 32) mx = fmaxf(mx, S[r0 + x / G][x % G]);
+#pragma unroll
+    for (int msk = G; msk < 32; msk <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, msk));
+    float corr[G];
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-      const float c = cs[wid][g];
+      const float mc = __shfl_sync(kFull, mx, g);
+      const float mn = fmaxf(m_run[g], mc);
+      corr[g] = (m_run[g] == -INFINITY) ? 0.f : exp2f(m_run[g] - mn);
+      m_run[g] = mn;
+    }
+    // mx already holds the chunk maximum of head own_g in this lane
+    const float m_own_new = fmaxf(m_own, mx);
+    const float corr_own = (m_own == -INFINITY) ? 0.f : exp2f(m_own - m_own_new);
+    m_own = m_own_new;
+    float psum = 0.f;
+    for (int x = lane; x < kTokPerWarp * G; x += 32) {
+      const float sv = S[r0 + x / G][x % G];
+      const float p = (sv == -INFINITY) ? 0.f : exp2f(sv - m_own_new);
+      S[r0 + x / G][x % G] = p;
+      psum += p;
+    }
+    l_own = l_own * corr_own + psum;
+    __syncwarp();
+    // pass 2: acc = corr * acc + sum_r p_r v_r
 #pragma unroll
-      for (int e = 0; e < 4; ++e) acc[g][e] *= c;
+    for (int g = 0; g < G; ++g) {
+      const float2 c2 = make_float2(corr[g], corr[g]);
+#pragma unroll
+      for (int p = 0; p < 8; ++p) acc[g][p] = fmul2(acc[g][p], c2);
     }
 #pragma unroll
-    for (int i = 0; i < TB; ++i) {
-      float vv[4];
-      row4<DT>(Vs + (r0 + i) * RB, lane, vv);
-      if (r0 + i >= nrow) vv[0] = vv[1] = vv[2] = vv[3] = 0.f;  // unwritten shared memory
+    for (int it = 0; it < kTokPerWarp / 4; ++it) {
+      const int r = r0 + it * 4 + grp;
+      float2 vv[8];
+      row16<DT>(Vs + r * RB, kk, vv);
+      if (r >= nrow) {
+#pragma unroll
+        for (int p = 0; p < 8; ++p) vv[p] = make_float2(0.f, 0.f);  // unwritten shared memory
+      }
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        const float pg = ps[wid][i * G + g];
+        const float pg = S[r][g];
+        const float2 p2 = make_float2(pg, pg);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) acc[g][e] = fmaf(pg, vv[e], acc[g][e]);
+        for (int p = 0; p < 8; ++p) acc[g][p] = ffma2(p2, vv[p], acc[g][p]);
       }
     }
-    __syncwarp();
+    __syncthreads();  // every warp is done with this stage and with S
+    if (wid == 0 && i + kStages < n_my) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      issue(i + kStages);
+    }
   }
-  // per-head totals of this warp
+  if (!s_ok && tid == 0) set_err(v.err, kErrTimeout);
+
+  // sum the four row groups of each warp; per-head totals of l
 #pragma unroll
-  for (int msk = G; msk < P; msk <<= 1) l_own += __shfl_xor_sync(kFull, l_own, msk);
-  if (lane < G) {
+  for (int g = 0; g < G; ++g)
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+      acc[g][p].x += __shfl_xor_sync(kFull, acc[g][p].x, 8);
+      acc[g][p].y += __shfl_xor_sync(kFull, acc[g][p].y, 8);
+      acc[g][p].x += __shfl_xor_sync(kFull, acc[g][p].x, 16);
+      acc[g][p].y += __shfl_xor_sync(kFull, acc[g][p].y, 16);
+    }
+#pragma unroll
+  for (int msk = G; msk < 32; msk <<= 1) l_own += __shfl_xor_sync(kFull, l_own, msk);
+  if (lane < G) {  // lane g < G keeps the books of head g
     wm[wid][lane] = m_own;
     wl[wid][lane] = l_own;
   }
+  if (grp == 0) {
 #pragma unroll
-  for (int g = 0; g < G; ++g)
+    for (int g = 0; g < G; ++g)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) wacc[wid][g][lane * 4 + e] = acc[g][e];
+      for (int p = 0; p < 8; ++p) {
+        wacc[wid][g][dim_of(kk, p, 0)] = acc[g][p].x;
+        wacc[wid][g][dim_of(kk, p, 1)] = acc[g][p].y;
+      }
+  }
   __syncthreads();
-  // merge the warps into the chunk partial
-  const int64_t pbase = (gs * v.max_chunks + chunk) * G;
-  for (int x = tid; x < G * kHeadDim; x += blockDim.x) {
+  // merge the warps into this CTA's partial
+  const int64_t pbase = (gs * v.max_chunks + split) * G;
+  for (int x = tid; x < G * kHeadDim; x += kAttnThreads) {
     const int g = x / kHeadDim, dim = x % kHeadDim;
     float mm = -INFINITY;
 #pragma unroll
@@ -822,24 +918,25 @@ __global__ void __launch_bounds__(kAttnWarps * 32) k_attn(CtxView v, StepArgs a)
   }
   __threadfence();
   __syncthreads();
-  if (tid == 0) s_last = (atomicAdd(&v.attn_count[gs], 1) == nchunks - 1);
+  if (tid == 0) s_last = (atomicAdd(&v.attn_count[gs], 1) == nsplit - 1);
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  // last CTA: combine the chunk partials, publish the outputs
+  // last CTA: combine the partials, publish the outputs
   float *out = a.out + k * a.stride_out;
   const int64_t obase = (((int64_t)b * a.nl + li) * H + (int64_t)h * G) * kHeadDim;
-  for (int x = tid; x < G * kHeadDim; x += blockDim.x) {
+  for (int x = tid; x < G * kHeadDim; x += kAttnThreads) {
     const int g = x / kHeadDim, dim = x % kHeadDim;
     float mm = -INFINITY;
-    for (int c = 0; c < nchunks; ++c)
+#pragma unroll 8
+    for (int c = 0; c < nsplit; ++c)
       mm = fmaxf(mm, __ldcg(&v.part_ml[((gs * v.max_chunks + c) * G + g) * 2]));
     float o = 0.f, z = 0.f;
-    for (int c = 0; c < nchunks; ++c) {
+#pragma unroll 8
+    for (int c = 0; c < nsplit; ++c) {
       const int64_t pi = (gs * v.max_chunks + c) * G + g;
       const float mc = __ldcg(&v.part_ml[pi * 2]);
-      if (mc == -INFINITY) continue;
-      const float sw = exp2f(mc - mm);
+      const float sw = (mc == -INFINITY) ? 0.f : exp2f(mc - mm);
       o = fmaf(sw, __ldcg(&v.part_acc[pi * kHeadDim + dim]), o);
       z = fmaf(sw, __ldcg(&v.part_ml[pi * 2 + 1]), z);
     }
@@ -850,7 +947,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32) k_attn(CtxView v, StepArgs a)
   if (a.selected_units) {
     const int32_t *sel = v.sel + gs * v.u_cap;
     int32_t *dst = a.selected_units + k * a.stride_sel + so * v.u_cap;
-    for (int x = tid; x < ns; x += blockDim.x) dst[x] = sel[x];
+    for (int x = tid; x < ns; x += kAttnThreads) dst[x] = sel[x];
   }
   if (tid == 0) {
     if (a.n_selected) a.n_selected[k * a.stride_nsel + so] = ns;
@@ -863,12 +960,22 @@ __global__ void __launch_bounds__(kAttnWarps * 32) k_attn(CtxView v, StepArgs a)
 // ---------------------------------------------------------------- host
 
 template <int DT, int G>
-constexpr size_t attn_smem() { return 2 * kAttnChunk * kHeadDim * elem_bytes<DT>(); }
+constexpr size_t attn_smem() { return (size_t)kStages * stage_bytes<DT>(); }
+
+// Split of a slice's chunks over CTAs: about two CTAs per SM in total.
+static void attn_split(int slices, int nch, int *nsplit, int *cpc) {
+  int want = (2 * 152 + slices - 1) / slices;
+  if (want < 1) want = 1;
+  if (want > nch) want = nch;
+  *cpc = (nch + want - 1) / want;
+  *nsplit = (nch + *cpc - 1) / *cpc;
+}
 
 template <int DT, int G>
-static void launch_attn(const CtxView &v, const StepArgs &a, int slices, int nchunks,
-                        cudaStream_t st) {
-  k_attn<DT, G><<<dim3(slices, nchunks), kAttnWarps * 32, attn_smem<DT, G>(), st>>>(v, a);
+static void launch_attn(const CtxView &v, const StepArgs &a, int slices, int nch, cudaStream_t st) {
+  int nsplit = 1, cpc = 1;
+  attn_split(slices, nch, &nsplit, &cpc);
+  k_attn<DT, G><<<dim3(slices, nsplit), kAttnThreads, attn_smem<DT, G>(), st>>>(v, a, cpc);
 }
 
 template <int DT, int G>
@@ -899,23 +1006,20 @@ static cudaError_t decode_t(const CtxView &v, const StepArgs &a, cudaStream_t st
   k_step_boundary<DT><<<a.nl * v.B, 1024, 0, st>>>(v, a);
   prof.end(st);
   prof.begin(kPScore, st);
-  k_score<DT><<<dim3(slices, kScoreCtasPerHead), 256, 0, st>>>(v, a);
-  prof.end(st);
-  prof.begin(kPSelect, st);
-  k_select<<<slices, 1024, 0, st>>>(v, a);
+  k_score_select<DT><<<dim3(slices, kScoreCtasPerHead), kScoreThreads, 0, st>>>(v, a);
   prof.end(st);
   if (v.offload) {
     prof.begin(kPGather, st);
     k_gather_offload<DT><<<dim3(slices, 16), 256, 0, st>>>(v, a);
     prof.end(st);
   }
-  const int nchunks = (a.budget + v.L + kAttnChunk - 1) / kAttnChunk;
+  const int nch = (a.budget + v.L + kAttnChunk - 1) / kAttnChunk;
   prof.begin(kPAttn, st);
   switch (v.G) {
-    case 1: launch_attn<DT, 1>(v, a, slices, nchunks, st); break;
-    case 2: launch_attn<DT, 2>(v, a, slices, nchunks, st); break;
-    case 4: launch_attn<DT, 4>(v, a, slices, nchunks, st); break;
-    case 8: launch_attn<DT, 8>(v, a, slices, nchunks, st); break;
+    case 1: launch_attn<DT, 1>(v, a, slices, nch, st); break;
+    case 2: launch_attn<DT, 2>(v, a, slices, nch, st); break;
+    case 4: launch_attn<DT, 4>(v, a, slices, nch, st); break;
+    case 8: launch_attn<DT, 8>(v, a, slices, nch, st); break;
     default: return cudaErrorInvalidValue;
   }
   prof.end(st);

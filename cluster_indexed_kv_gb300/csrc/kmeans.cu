@@ -574,6 +574,7 @@ __global__ void k_reset_layer(CtxView v, int layer, int32_t c) {
       v.n_tok[gs] = 0;
       v.rng_cum[gs * (int64_t)(v.u_cap + 1)] = 0;
       v.attn_count[gs] = 0;
+      v.score_count[gs] = 0;
     }
   }
 }

@@ -80,6 +80,7 @@ struct CtxView {
   float *part_acc;            // [slice][max_chunks][G][d]
   float *part_ml;             // [slice][max_chunks][G][2]
   int32_t *attn_count;        // [slice]
+  int32_t *score_count;       // [slice] score CTAs done this step (last one selects)
   int32_t max_chunks;
   int32_t *err;               // device error bits (shared by all layers)
   int64_t *counters;          // [kCounters] work counters (see CounterId)
@@ -91,7 +92,7 @@ enum CounterId : int { kCntAttnRows = 0, kCntScoreUnits = 1, kCntGatherRows = 2,
 
 // Kernel kinds for launch counting and event timing.
 enum ProfKind : int {
-  kPBoundary = 0, kPScore, kPSelect, kPGather, kPAttn,
+  kPBoundary = 0, kPScore, kPGather, kPAttn,
   kPKmInit, kPKmOperand, kPKmAssign, kPKmRefine, kPKmSort, kPKmUpdate, kPKmPool,
   kPNum
 };
