@@ -131,8 +131,19 @@ __device__ bool close_segment(const CtxView &v, DecState &st, int64_t lb, int s0
   return true;
 }
 
+// Programmatic dependent launch: a kernel waits here for the previous kernel
+// in the stream to complete (and its writes to be visible) before it touches
+// any state; the next kernel may be scheduled as soon as this one signals.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+constexpr int kBoundaryThreads = 1024;
+constexpr int kQPitch = kHeadDim + 8;  // padded query rows in shared memory (floats)
+
 template <int DT>
-__global__ void __launch_bounds__(1024) k_step_boundary(CtxView v, StepArgs a) {
+__global__ void __launch_bounds__(kBoundaryThreads) k_step_boundary(CtxView v, StepArgs a) {
   const int li = blockIdx.x / v.B, b = blockIdx.x % v.B;
   const int l = a.l0 + li;
   const int64_t lb = (int64_t)l * v.B + b;
@@ -141,12 +152,16 @@ __global__ void __launch_bounds__(1024) k_step_boundary(CtxView v, StepArgs a) {
   __shared__ DecState st;
   __shared__ float cosv[kMaxHeads];
   __shared__ int slow_any;
+  extern __shared__ float qsm[];  // [2][H][kQPitch]: previous and current queries
+  pdl_wait();
+  pdl_trigger();
   if (tid == 0) {
     st = v.st[lb];
     slow_any = 0;
   }
   __syncthreads();
   const int t = st.t;
+  const int n_closed0 = st.n_closed;
   const int64_t k = t - a.base_t;
   const void *q = (const char *)a.q + k * a.stride_q * elem_bytes<DT>();
   const void *k_new = (const char *)a.k_new + k * a.stride_kv * elem_bytes<DT>();
@@ -154,21 +169,55 @@ __global__ void __launch_bounds__(1024) k_step_boundary(CtxView v, StepArgs a) {
   const int64_t qoff = ((int64_t)b * a.nl + li) * H * kHeadDim;
   const int64_t kvoff = ((int64_t)b * a.nl + li) * v.Hkv * kHeadDim;
 
+  // all loads of the step at once: both query sets (16-byte vectors into
+  // padded shared rows) and this thread's key/value elements and running sums
+  constexpr int per16 = 16 / elem_bytes<DT>();
+  const int nvec = H * kHeadDim / per16;
+  for (int x = tid; x < 2 * nvec; x += nth) {
+    const int which = x / nvec, y = x % nvec;
+    const int head = y / (kHeadDim / per16), j0 = (y % (kHeadDim / per16)) * per16;
+    float e[8];
+    if (which == 0) load16<DT>(v.q_prev, (lb * H + head) * kHeadDim + j0, e);
+    else load16<DT>(q, qoff + (int64_t)head * kHeadDim + j0, e);
+    float *dst = qsm + ((int64_t)which * H + head) * kQPitch + j0;
+#pragma unroll
+    for (int i = 0; i < per16; ++i) dst[i] = e[i];
+  }
+  constexpr int kMaxPer = 2;  // Hkv * d <= 2048
+  uint32_t kbits[kMaxPer], vbits[kMaxPer];
+  int64_t ssum[kMaxPer];
+#pragma unroll
+  for (int r = 0; r < kMaxPer; ++r) {
+    const int x = tid + r * nth;
+    if (x < v.Hkv * kHeadDim) {
+      const int64_t gs = lb * v.Hkv + x / kHeadDim;
+      if constexpr (DT == 1) {
+        kbits[r] = ((const uint16_t *)k_new)[kvoff + x];
+        vbits[r] = ((const uint16_t *)v_new)[kvoff + x];
+      } else {
+        kbits[r] = __float_as_uint(((const float *)k_new)[kvoff + x]);
+        vbits[r] = __float_as_uint(((const float *)v_new)[kvoff + x]);
+      }
+      ssum[r] = v.segsum[gs * kHeadDim + x % kHeadDim];
+    }
+  }
+  __syncthreads();
+
   // 1. r_t = (1/H) sum_h cos(q_{t-1}^h, q_t^h) in fp32, fixed operation order
   if (t > 0) {
     if (tid < H) {
+      const float *x = qsm + tid * kQPitch;
+      const float *y = qsm + (H + tid) * kQPitch;
       float dot = 0.f, na = 0.f, nb = 0.f;
-      constexpr int per16 = 16 / elem_bytes<DT>();
-#pragma unroll 2
-      for (int j0 = 0; j0 < kHeadDim; j0 += per16) {
-        float x[8], y[8];
-        load16<DT>(v.q_prev, (lb * H + tid) * kHeadDim + j0, x);
-        load16<DT>(q, qoff + (int64_t)tid * kHeadDim + j0, y);
+#pragma unroll 8
+      for (int j = 0; j < kHeadDim; j += 4) {
+        const float4 xa = *(const float4 *)(x + j), ya = *(const float4 *)(y + j);
+        const float xv[4] = {xa.x, xa.y, xa.z, xa.w}, yv[4] = {ya.x, ya.y, ya.z, ya.w};
 #pragma unroll
-        for (int e = 0; e < per16; ++e) {
-          dot = __fmaf_rn(x[e], y[e], dot);
-          na = __fmaf_rn(x[e], x[e], na);
-          nb = __fmaf_rn(y[e], y[e], nb);
+        for (int e = 0; e < 4; ++e) {
+          dot = __fmaf_rn(xv[e], yv[e], dot);
+          na = __fmaf_rn(xv[e], xv[e], na);
+          nb = __fmaf_rn(yv[e], yv[e], nb);
         }
       }
       const float den = __fmul_rn(__fsqrt_rn(na), __fsqrt_rn(nb));
@@ -244,30 +293,45 @@ __global__ void __launch_bounds__(1024) k_step_boundary(CtxView v, StepArgs a) {
   __syncthreads();
 
   // 4. token t enters the local buffer; its key joins the open segment's sum
+  //    (a segment closed during this step restarted the sum at zero)
+  const bool restarted = st.n_closed != n_closed0;
   int slow = 0;
-  for (int x = tid; x < v.Hkv * kHeadDim; x += nth) {
+#pragma unroll
+  for (int r = 0; r < kMaxPer; ++r) {
+    const int x = tid + r * nth;
+    if (x >= v.Hkv * kHeadDim) continue;
     const int h = x / kHeadDim, dim = x % kHeadDim;
     const int64_t gs = lb * v.Hkv + h;
     const int64_t di = (gs * v.dec_rows + t) * kHeadDim + dim;
+    const int64_t prev = restarted ? 0 : ssum[r];
     if constexpr (DT == 1) {
-      const uint16_t kb = ((const uint16_t *)k_new)[kvoff + x];
-      ((uint16_t *)v.dec_k)[di] = kb;
-      ((uint16_t *)v.dec_v)[di] = ((const uint16_t *)v_new)[kvoff + x];
-      v.segsum[gs * kHeadDim + dim] += bf16_fixed40(kb, &slow);
+      ((uint16_t *)v.dec_k)[di] = (uint16_t)kbits[r];
+      ((uint16_t *)v.dec_v)[di] = (uint16_t)vbits[r];
+      v.segsum[gs * kHeadDim + dim] = prev + bf16_fixed40((uint16_t)kbits[r], &slow);
     } else {
-      const float kf = ((const float *)k_new)[kvoff + x];
-      ((float *)v.dec_k)[di] = kf;
-      ((float *)v.dec_v)[di] = ((const float *)v_new)[kvoff + x];
-      const double s = __longlong_as_double(v.segsum[gs * kHeadDim + dim]);
-      v.segsum[gs * kHeadDim + dim] = __double_as_longlong(__dadd_rn(s, (double)kf));
+      ((float *)v.dec_k)[di] = __uint_as_float(kbits[r]);
+      ((float *)v.dec_v)[di] = __uint_as_float(vbits[r]);
+      v.segsum[gs * kHeadDim + dim] =
+          __double_as_longlong(__dadd_rn(__longlong_as_double(prev), (double)__uint_as_float(kbits[r])));
     }
   }
   if (slow) atomicOr(&slow_any, 1);
-  for (int x = tid; x < H * kHeadDim; x += nth) {
-    if constexpr (DT == 1)
-      ((uint16_t *)v.q_prev)[lb * H * kHeadDim + x] = ((const uint16_t *)q)[qoff + x];
-    else
-      ((float *)v.q_prev)[lb * H * kHeadDim + x] = ((const float *)q)[qoff + x];
+  // the current queries become the previous ones
+  for (int y = tid; y < nvec; y += nth) {
+    const int head = y / (kHeadDim / per16), j0 = (y % (kHeadDim / per16)) * per16;
+    const float *src = qsm + ((int64_t)H + head) * kQPitch + j0;
+    if constexpr (DT == 1) {
+      uint4 o;
+      uint32_t w[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        w[i] = (__float_as_uint(src[2 * i]) >> 16) | (__float_as_uint(src[2 * i + 1]) & 0xffff0000u);
+      o.x = w[0]; o.y = w[1]; o.z = w[2]; o.w = w[3];
+      *(uint4 *)((uint16_t *)v.q_prev + (lb * H + head) * kHeadDim + j0) = o;
+    } else {
+      *(float4 *)((float *)v.q_prev + (lb * H + head) * kHeadDim + j0) =
+          make_float4(src[0], src[1], src[2], src[3]);
+    }
   }
   __syncthreads();
   if (tid == 0) {
@@ -476,6 +540,8 @@ __global__ void __launch_bounds__(kScoreThreads) k_score_select(CtxView v, StepA
   const int l = a.l0 + li;
   const int64_t lb = (int64_t)l * v.B + b;
   const int64_t gs = lb * v.Hkv + h;
+  pdl_wait();
+  pdl_trigger();
   const DecState *stp = v.st + lb;
   if (!stp->flag) return;
   const int U = stp->n_units;
@@ -536,6 +602,8 @@ __global__ void __launch_bounds__(256) k_gather_offload(CtxView v, StepArgs a) {
   const int b = rem / v.Hkv, h = rem % v.Hkv;
   const int64_t lb = (int64_t)(a.l0 + li) * v.B + b;
   const int64_t gs = lb * v.Hkv + h;
+  pdl_wait();
+  pdl_trigger();
   if (!v.st[lb].flag) return;
   const int ns = v.n_sel[gs], nt = v.n_tok[gs];
   const int32_t *cum = v.rng_cum + gs * (int64_t)(v.u_cap + 1);
@@ -686,6 +754,8 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn(CtxView v, StepArgs a,
   const int64_t gs = lb * v.Hkv + h;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int grp = lane >> 3, kk = lane & 7;
+  pdl_wait();
+  pdl_trigger();
   const DecState st = v.st[lb];
   const int t_cur = st.t - 1, ws = st.win_start;
   const int64_t k = t_cur - a.base_t;
@@ -776,11 +846,10 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn(CtxView v, StepArgs a,
     for (int p = 0; p < 8; ++p) q2[g][p] = make_float2(qs[g][dim_of(kk, p, 0)], qs[g][dim_of(kk, p, 1)]);
 
   const int hl = head_of_lane<G>(kk);          // head whose score this lane ends with
-  const int own_g = lane % G;                   // head of this lane's softmax bookkeeping
   float m_run[G];
 #pragma unroll
   for (int g = 0; g < G; ++g) m_run[g] = -INFINITY;
-  float m_own = -INFINITY, l_own = 0.f;  // running max and sum of head own_g
+  float m_own = -INFINITY, l_own = 0.f;  // running max and sum of head lane % G
   float2 acc[G][8];
 #pragma unroll
   for (int g = 0; g < G; ++g)
@@ -825,7 +894,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn(CtxView v, StepArgs a,
       corr[g] = (m_run[g] == -INFINITY) ? 0.f : exp2f(m_run[g] - mn);
       m_run[g] = mn;
     }
-    // mx already holds the chunk maximum of head own_g in this lane
+    // mx already holds the chunk maximum of head lane % G
     const float m_own_new = fmaxf(m_own, mx);
     const float corr_own = (m_own == -INFINITY) ? 0.f : exp2f(m_own - m_own_new);
     m_own = m_own_new;
@@ -959,12 +1028,33 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn(CtxView v, StepArgs a,
 
 // ---------------------------------------------------------------- host
 
+// Launch with programmatic stream serialization: the kernel may be scheduled
+// while its predecessor drains and waits for it in pdl_wait().
+template <typename... KArgs, typename... Args>
+static void launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 template <int DT, int G>
 constexpr size_t attn_smem() { return (size_t)kStages * stage_bytes<DT>(); }
 
-// Split of a slice's chunks over CTAs: about two CTAs per SM in total.
+static int g_attn_slots = 2 * 152;  // resident attention CTAs on the device
+
+// Split of a slice's chunks over CTAs so that the whole grid is resident at
+// once (one wave).
 static void attn_split(int slices, int nch, int *nsplit, int *cpc) {
-  int want = (2 * 152 + slices - 1) / slices;
+  int want = g_attn_slots / slices;
   if (want < 1) want = 1;
   if (want > nch) want = nch;
   *cpc = (nch + want - 1) / want;
@@ -975,13 +1065,22 @@ template <int DT, int G>
 static void launch_attn(const CtxView &v, const StepArgs &a, int slices, int nch, cudaStream_t st) {
   int nsplit = 1, cpc = 1;
   attn_split(slices, nch, &nsplit, &cpc);
-  k_attn<DT, G><<<dim3(slices, nsplit), kAttnThreads, attn_smem<DT, G>(), st>>>(v, a, cpc);
+  launch_pdl(k_attn<DT, G>, dim3(slices, nsplit), dim3(kAttnThreads), attn_smem<DT, G>(), st, v, a, cpc);
 }
 
 template <int DT, int G>
 static cudaError_t prep_attn() {
-  return cudaFuncSetAttribute(k_attn<DT, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)attn_smem<DT, G>());
+  cudaError_t e = cudaFuncSetAttribute(k_attn<DT, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)attn_smem<DT, G>());
+  if (e != cudaSuccess) return e;
+  int per_sm = 0, dev = 0, sms = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_attn<DT, G>, kAttnThreads, attn_smem<DT, G>());
+  if (e == cudaSuccess) e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  if (per_sm > 0 && sms > 0) g_attn_slots = per_sm * sms;
+  return cudaFuncSetAttribute(k_step_boundary<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)(2 * kMaxHeads * kQPitch * sizeof(float)));
 }
 
 template <int DT>
@@ -1002,15 +1101,17 @@ cudaError_t prepare_kernels(int dtype, int group) {
 template <int DT>
 static cudaError_t decode_t(const CtxView &v, const StepArgs &a, cudaStream_t st, Prof &prof) {
   const int slices = a.nl * v.B * v.Hkv;
+  const int H = v.Hkv * v.G;
   prof.begin(kPBoundary, st);
-  k_step_boundary<DT><<<a.nl * v.B, 1024, 0, st>>>(v, a);
+  launch_pdl(k_step_boundary<DT>, dim3(a.nl * v.B), dim3(kBoundaryThreads),
+             (size_t)2 * H * kQPitch * sizeof(float), st, v, a);
   prof.end(st);
   prof.begin(kPScore, st);
-  k_score_select<DT><<<dim3(slices, kScoreCtasPerHead), kScoreThreads, 0, st>>>(v, a);
+  launch_pdl(k_score_select<DT>, dim3(slices, kScoreCtasPerHead), dim3(kScoreThreads), 0, st, v, a);
   prof.end(st);
   if (v.offload) {
     prof.begin(kPGather, st);
-    k_gather_offload<DT><<<dim3(slices, 16), 256, 0, st>>>(v, a);
+    launch_pdl(k_gather_offload<DT>, dim3(slices, 16), dim3(256), 0, st, v, a);
     prof.end(st);
   }
   const int nch = (a.budget + v.L + kAttnChunk - 1) / kAttnChunk;
