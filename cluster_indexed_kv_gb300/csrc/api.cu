@@ -204,6 +204,8 @@ lkv_status lkv_create(const lkv_config *cfg, lkv_ctx **out) {
   v.max_pieces = u_cap + max_chunks;
   v.pieces = (int4 *)dalloc(c, S_all * (int64_t)v.max_pieces * sizeof(int4), &st);
   v.chunk_piece = (int32_t *)dalloc(c, S_all * (int64_t)(max_chunks + 1) * 4, &st);
+  v.chunk_pieces = (int4 *)dalloc(c, S_all * (int64_t)max_chunks * lkv::kAttnChunk * sizeof(int4), &st);
+  v.chunk_count = (int32_t *)dalloc(c, S_all * (int64_t)max_chunks * 4, &st);
   v.err = (int32_t *)dalloc(c, 4, &st);
   v.counters = (int64_t *)dalloc(c, lkv::kCounters * 8, &st);
 

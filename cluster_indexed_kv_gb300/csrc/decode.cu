@@ -520,13 +520,27 @@ __device__ void select_units(const CtxView &v, int64_t gs, int U, int budget) {
     }
   }
   __syncthreads();
+  const int nsc = (s_ntok + kAttnChunk - 1) / kAttnChunk;
   if (tid == 0) {
     v.n_sel[gs] = s_nsel;
     v.n_tok[gs] = s_ntok;
     v.rng_cum[gs * (int64_t)(v.u_cap + 1) + s_nsel] = s_ntok;
-    const int nsc = (s_ntok + kAttnChunk - 1) / kAttnChunk;
     if (nsc <= v.max_chunks) v.chunk_piece[gs * (int64_t)(v.max_chunks + 1) + nsc] = s_npieces;
-    if (s_ntok > budget || s_npieces > v.max_pieces) set_err(v.err, kErrInternal);
+    if (s_ntok > budget || s_npieces > v.max_pieces || nsc > v.max_chunks) set_err(v.err, kErrInternal);
+  }
+  __syncthreads();
+  // the same pieces, grouped per chunk in fixed 64-slot blocks (a chunk of 64
+  // rows has at most 64 pieces) so that the attention reads them in one go
+  if (nsc <= v.max_chunks && s_npieces <= v.max_pieces) {
+    const int32_t *cp = v.chunk_piece + gs * (int64_t)(v.max_chunks + 1);
+    const int4 *pieces = v.pieces + gs * (int64_t)v.max_pieces;
+    for (int p = tid; p < s_npieces; p += nth) {
+      const int4 pc = pieces[p];
+      const int c = pc.y / kAttnChunk;
+      v.chunk_pieces[(gs * v.max_chunks + c) * kAttnChunk + (p - cp[c])] = pc;
+    }
+    for (int c = tid; c < nsc; c += nth)
+      v.chunk_count[gs * v.max_chunks + c] = cp[c + 1] - cp[c];
   }
 }
 
@@ -632,6 +646,7 @@ constexpr int kAttnWarps = 4;
 constexpr int kAttnThreads = kAttnWarps * 32;
 constexpr int kTokPerWarp = kAttnChunk / kAttnWarps;  // 16
 constexpr int kStages = 3;
+constexpr int kPreChunks = 8;  // chunks whose copy plan a CTA prefetches
 constexpr uint64_t kWaitLimitNs = 2000000000ull;      // 2 s
 
 union F2U {
@@ -743,7 +758,8 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn(CtxView v, StepArgs a,
   __shared__ float qs[G][kHeadDim];
   __shared__ __align__(16) float S[kAttnChunk][G];
   __shared__ float wm[kAttnWarps][G], wl[kAttnWarps][G];
-  __shared__ float wacc[kAttnWarps][G][kHeadDim];
+  __shared__ int4 pcs[kPreChunks][kAttnChunk];
+  __shared__ int pcn[kPreChunks];
   __shared__ int s_last, s_ok;
 
   const int per_l = v.B * v.Hkv;
@@ -766,7 +782,17 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn(CtxView v, StepArgs a,
   const int nch = (total + kAttnChunk - 1) / kAttnChunk;
   const int c_begin = split * cpc;
   const int n_my = max(0, min(cpc, nch - c_begin));
+  const int nsc = (nt + kAttnChunk - 1) / kAttnChunk;
 
+  // the copy plan of this CTA's first chunks, fetched at once
+  if (!v.offload)
+    for (int x = tid; x < kPreChunks * kAttnChunk; x += kAttnThreads) {
+      const int c = c_begin + x / kAttnChunk;
+      if (x / kAttnChunk < n_my && c < nsc) {
+        pcs[x / kAttnChunk][x % kAttnChunk] = v.chunk_pieces[(gs * v.max_chunks + c) * kAttnChunk + x % kAttnChunk];
+        if (x % kAttnChunk == 0) pcn[x / kAttnChunk] = v.chunk_count[gs * v.max_chunks + c];
+      }
+    }
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) mbar_init(&bar[i], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -788,27 +814,30 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn(CtxView v, StepArgs a,
     uint64_t *br = &bar[i % kStages];
     const int c = c_begin + i, f0 = c * kAttnChunk;
     const int nrow = min(kAttnChunk, total - f0);
-    int p0 = 0, p1 = 0, sel_direct = 0;
+    int np = 0, sel_direct = 0;
+    const int4 *pieces = nullptr;
     if (f0 < nt) {
       if (!v.offload) {
-        const int32_t *cp = v.chunk_piece + gs * (int64_t)(v.max_chunks + 1);
-        const int nsc = (nt + kAttnChunk - 1) / kAttnChunk;
-        p0 = cp[c];
-        p1 = (c + 1 < nsc) ? cp[c + 1] : cp[nsc];
+        if (i < kPreChunks) {
+          pieces = pcs[i];
+          np = pcn[i];
+        } else {
+          pieces = v.chunk_pieces + (gs * v.max_chunks + c) * kAttnChunk;
+          np = v.chunk_count[gs * v.max_chunks + c];
+        }
       } else {
         sel_direct = min(f0 + kAttnChunk, nt) - f0;
       }
     }
-    const int4 *pieces = v.pieces + gs * (int64_t)v.max_pieces;
     uint32_t bytes = 0;
-    for (int p = p0 + lane; p < p1; p += 32) bytes += 2u * (uint32_t)pieces[p].z * RB;
+    for (int p = lane; p < np; p += 32) bytes += 2u * (uint32_t)pieces[p].z * RB;
     const int win0 = max(f0, nt), win1 = f0 + nrow;
     if (lane == 0) bytes += 2u * (uint32_t)(max(win1 - win0, 0) + sel_direct) * RB;
 #pragma unroll
     for (int o = 16; o; o >>= 1) bytes += __shfl_xor_sync(kFull, bytes, o);
     if (lane == 0) mbar_arrive_expect_tx(br, bytes);
     __syncwarp();
-    for (int p = p0 + lane; p < p1; p += 32) {
+    for (int p = lane; p < np; p += 32) {
       const int4 pc = pieces[p];
       const int dr = pc.y - f0;
       bulk_g2s(Ks + dr * RB, selk + (int64_t)pc.x * RB, (uint32_t)pc.z * RB, br);
@@ -860,7 +889,12 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn(CtxView v, StepArgs a,
   for (int i = 0; i < n_my; ++i) {
     const unsigned char *Ks = smem + (i % kStages) * SB;
     const unsigned char *Vs = Ks + SB / 2;
-    if (!mbar_wait_bounded(&bar[i % kStages], (i / kStages) & 1, kWaitLimitNs)) s_ok = 0;
+    if (!mbar_wait_bounded(&bar[i % kStages], (i / kStages) & 1, kWaitLimitNs)) {
+      // record the timeout, then give the copies one more bounded wait so
+      // that none is still writing a buffer this block reuses
+      s_ok = 0;
+      mbar_wait_bounded(&bar[i % kStages], (i / kStages) & 1, kWaitLimitNs);
+    }
     const int nrow = min(kAttnChunk, total - (c_begin + i) * kAttnChunk);
     // pass 1: scores of this warp's 16 rows, 4 rows per instruction
 #pragma unroll
@@ -938,6 +972,9 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn(CtxView v, StepArgs a,
     }
   }
   if (!s_ok && tid == 0) set_err(v.err, kErrTimeout);
+  // the pipeline buffers are free now: reuse them for the warp accumulators
+  float(*wacc)[G][kHeadDim] = reinterpret_cast<float(*)[G][kHeadDim]>(smem);
+  static_assert(kAttnWarps * G * kHeadDim * sizeof(float) <= (size_t)kStages * stage_bytes<DT>(), "");
 
   // sum the four row groups of each warp; per-head totals of l
 #pragma unroll

@@ -76,6 +76,8 @@ struct CtxView {
   int32_t *rng_cum;           // [slice][u_cap + 1] exclusive token prefix
   int4 *pieces;               // [slice][max_pieces] (src row, first token, length, 0)
   int32_t *chunk_piece;       // [slice][max_chunks + 1] first piece of each chunk
+  int4 *chunk_pieces;         // [slice][max_chunks][64] the pieces of each chunk
+  int32_t *chunk_count;       // [slice][max_chunks] pieces in each chunk
   int32_t max_pieces;
   float *part_acc;            // [slice][max_chunks][G][d]
   float *part_ml;             // [slice][max_chunks][G][2]
