@@ -642,9 +642,9 @@ __global__ void __launch_bounds__(256) k_gather_offload(CtxView v, StepArgs a) {
 
 // ---------------------------------------------------------------- attention
 
-constexpr int kAttnWarps = 4;
+constexpr int kAttnWarps = 8;
 constexpr int kAttnThreads = kAttnWarps * 32;
-constexpr int kTokPerWarp = kAttnChunk / kAttnWarps;  // 16
+constexpr int kRowsPerWarp = kAttnChunk / kAttnWarps;  // 8 rows of each chunk
 constexpr int kStages = 3;
 constexpr int kPreChunks = 8;  // chunks whose copy plan a CTA prefetches
 constexpr uint64_t kWaitLimitNs = 2000000000ull;      // 2 s
@@ -664,69 +664,59 @@ __device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
   return r.f;
 }
 
-// 16 elements of a row owned by lane k of an 8-lane group: dims
-// [8k, 8k + 8) and [64 + 8k, 64 + 8k + 8), as 8 float pairs. For bf16 rows
-// the group's lanes read each 128-byte half of the row contiguously.
+// The 8 consecutive elements [8k, 8k + 8) of a row owned by lane k of a
+// 16-lane group, as 4 float pairs (the group reads the row contiguously).
 template <int DT>
-__device__ __forceinline__ void row16(const unsigned char *row, int k, float2 (&o)[8]) {
+__device__ __forceinline__ void row8(const unsigned char *row, int k, float2 (&o)[4]) {
   if constexpr (DT == 1) {
     const uint4 a = *(const uint4 *)(row + 16 * k);
-    const uint4 b = *(const uint4 *)(row + 128 + 16 * k);
-    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    const uint32_t w[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
-    for (int p = 0; p < 8; ++p) o[p] = make_float2(__uint_as_float(w[p] << 16), __uint_as_float(w[p] & 0xffff0000u));
+    for (int p = 0; p < 4; ++p)
+      o[p] = make_float2(__uint_as_float(w[p] << 16), __uint_as_float(w[p] & 0xffff0000u));
   } else {
     const float4 a = *(const float4 *)(row + 32 * k);
     const float4 b = *(const float4 *)(row + 32 * k + 16);
-    const float4 c = *(const float4 *)(row + 256 + 32 * k);
-    const float4 d = *(const float4 *)(row + 256 + 32 * k + 16);
     o[0] = make_float2(a.x, a.y); o[1] = make_float2(a.z, a.w);
     o[2] = make_float2(b.x, b.y); o[3] = make_float2(b.z, b.w);
-    o[4] = make_float2(c.x, c.y); o[5] = make_float2(c.z, c.w);
-    o[6] = make_float2(d.x, d.y); o[7] = make_float2(d.z, d.w);
   }
 }
 
-// Element index (within the head) of pair p, element e, owned by lane k.
-__device__ __forceinline__ int dim_of(int k, int p, int e) {
-  return (p < 4 ? 8 * k + 2 * p : 64 + 8 * k + 2 * (p - 4)) + e;
+// Keep-or-send halving step of a butterfly reduce-scatter: lanes with `up`
+// keep the upper half of x[0..2n), the others the lower half.
+template <int N>
+__device__ __forceinline__ void halve(float *x, bool up, int mask) {
+#pragma unroll
+  for (int j = 0; j < N; ++j) {
+    const float send = up ? x[j] : x[j + N], keep = up ? x[j + N] : x[j];
+    x[j] = keep + __shfl_xor_sync(kFull, send, mask);
+  }
 }
 
-// Reduce the per-lane partial dot products of the G heads of one token over
-// its 8-lane group; on return lane k holds the full score of head
+// Reduce the per-lane partial dot products of the G heads of one row over
+// its 16-lane group; on return lane k holds the full score of head
 // head_of_lane<G>(k).
 template <int G>
 __device__ __forceinline__ float reduce_heads(float (&x)[G], int lane) {
-  const bool b2 = lane & 4, b1 = lane & 2, b0 = lane & 1;
+  const bool b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
   if constexpr (G == 8) {
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float send = b2 ? x[j] : x[j + 4], keep = b2 ? x[j + 4] : x[j];
-      x[j] = keep + __shfl_xor_sync(kFull, send, 4);
-    }
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const float send = b1 ? x[j] : x[j + 2], keep = b1 ? x[j + 2] : x[j];
-      x[j] = keep + __shfl_xor_sync(kFull, send, 2);
-    }
-    const float send = b0 ? x[0] : x[1], keep = b0 ? x[1] : x[0];
-    return keep + __shfl_xor_sync(kFull, send, 1);
+    halve<4>(x, b3, 8);
+    halve<2>(x, b2, 4);
+    halve<1>(x, b1, 2);
+    return x[0] + __shfl_xor_sync(kFull, x[0], 1);
   } else if constexpr (G == 4) {
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const float send = b2 ? x[j] : x[j + 2], keep = b2 ? x[j + 2] : x[j];
-      x[j] = keep + __shfl_xor_sync(kFull, send, 4);
-    }
-    const float send = b1 ? x[0] : x[1], keep = b1 ? x[1] : x[0];
-    float r = keep + __shfl_xor_sync(kFull, send, 2);
+    halve<2>(x, b3, 8);
+    halve<1>(x, b2, 4);
+    float r = x[0] + __shfl_xor_sync(kFull, x[0], 2);
     return r + __shfl_xor_sync(kFull, r, 1);
   } else if constexpr (G == 2) {
-    const float send = b2 ? x[0] : x[1], keep = b2 ? x[1] : x[0];
-    float r = keep + __shfl_xor_sync(kFull, send, 4);
+    halve<1>(x, b3, 8);
+    float r = x[0] + __shfl_xor_sync(kFull, x[0], 4);
     r += __shfl_xor_sync(kFull, r, 2);
     return r + __shfl_xor_sync(kFull, r, 1);
   } else {
     float r = x[0];
+    r += __shfl_xor_sync(kFull, r, 8);
     r += __shfl_xor_sync(kFull, r, 4);
     r += __shfl_xor_sync(kFull, r, 2);
     return r + __shfl_xor_sync(kFull, r, 1);
@@ -735,9 +725,9 @@ __device__ __forceinline__ float reduce_heads(float (&x)[G], int lane) {
 
 template <int G>
 __device__ __forceinline__ int head_of_lane(int k) {
-  if constexpr (G == 8) return ((k >> 2) & 1) * 4 + ((k >> 1) & 1) * 2 + (k & 1);
-  else if constexpr (G == 4) return ((k >> 2) & 1) * 2 + ((k >> 1) & 1);
-  else if constexpr (G == 2) return (k >> 2) & 1;
+  if constexpr (G == 8) return ((k >> 3) & 1) * 4 + ((k >> 2) & 1) * 2 + ((k >> 1) & 1);
+  else if constexpr (G == 4) return ((k >> 3) & 1) * 2 + ((k >> 2) & 1);
+  else if constexpr (G == 2) return (k >> 3) & 1;
   else return 0;
 }
 
@@ -747,8 +737,8 @@ constexpr int stage_bytes() { return 2 * kAttnChunk * kHeadDim * elem_bytes<DT>(
 // Split-K attention. CTA (slice, split) streams chunks [split * cpc, ...) of
 // the slice's token list (selected rows, then the local buffer) through a
 // 3-stage ring of shared-memory buffers filled by bulk copies. Per chunk,
-// each warp owns 16 rows: pass 1 scores them (8 lanes per row, 4 rows per
-// instruction), pass 2 adds p * V into per-lane accumulators.
+// each of the 8 warps owns 8 rows: pass 1 scores them (16 lanes per row, 2
+// rows per instruction), pass 2 adds p * V into per-lane accumulators.
 template <int DT, int G>
 __global__ void __launch_bounds__(kAttnThreads, 2) k_attn(CtxView v, StepArgs a, int cpc) {
   constexpr int RB = kHeadDim * elem_bytes<DT>();
@@ -769,7 +759,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn(CtxView v, StepArgs a,
   const int64_t lb = (int64_t)l * v.B + b;
   const int64_t gs = lb * v.Hkv + h;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  const int grp = lane >> 3, kk = lane & 7;
+  const int grp = lane >> 4, kk = lane & 15;
   pdl_wait();
   pdl_trigger();
   const DecState st = v.st[lb];
@@ -868,24 +858,24 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn(CtxView v, StepArgs a,
     qs[x / kHeadDim][x % kHeadDim] = load_elem<DT>(q, qoff + x) * qscale;
   if (tid == 0) s_ok = 1;
   __syncthreads();
-  float2 q2[G][8];
+  float2 q2[G][4];
 #pragma unroll
   for (int g = 0; g < G; ++g)
 #pragma unroll
-    for (int p = 0; p < 8; ++p) q2[g][p] = make_float2(qs[g][dim_of(kk, p, 0)], qs[g][dim_of(kk, p, 1)]);
+    for (int p = 0; p < 4; ++p) q2[g][p] = make_float2(qs[g][8 * kk + 2 * p], qs[g][8 * kk + 2 * p + 1]);
 
-  const int hl = head_of_lane<G>(kk);          // head whose score this lane ends with
+  const int hl = head_of_lane<G>(kk);  // head whose score this lane ends with
   float m_run[G];
 #pragma unroll
   for (int g = 0; g < G; ++g) m_run[g] = -INFINITY;
   float m_own = -INFINITY, l_own = 0.f;  // running max and sum of head lane % G
-  float2 acc[G][8];
+  float2 acc[G][4];
 #pragma unroll
   for (int g = 0; g < G; ++g)
 #pragma unroll
-    for (int p = 0; p < 8; ++p) acc[g][p] = make_float2(0.f, 0.f);
+    for (int p = 0; p < 4; ++p) acc[g][p] = make_float2(0.f, 0.f);
 
-  const int r0 = wid * kTokPerWarp;
+  const int r0 = wid * kRowsPerWarp;
   for (int i = 0; i < n_my; ++i) {
     const unsigned char *Ks = smem + (i % kStages) * SB;
     const unsigned char *Vs = Ks + SB / 2;
@@ -896,28 +886,28 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn(CtxView v, StepArgs a,
       mbar_wait_bounded(&bar[i % kStages], (i / kStages) & 1, kWaitLimitNs);
     }
     const int nrow = min(kAttnChunk, total - (c_begin + i) * kAttnChunk);
-    // pass 1: scores of this warp's 16 rows, 4 rows per instruction
+    // pass 1: scores of this warp's 8 rows, 2 rows per instruction
 #pragma unroll
-    for (int it = 0; it < kTokPerWarp / 4; ++it) {
-      const int r = r0 + it * 4 + grp;
-      float2 kv[8];
-      row16<DT>(Ks + r * RB, kk, kv);
+    for (int it = 0; it < kRowsPerWarp / 2; ++it) {
+      const int r = r0 + it * 2 + grp;
+      float2 kv[4];
+      row8<DT>(Ks + r * RB, kk, kv);
       float part[G];
 #pragma unroll
       for (int g = 0; g < G; ++g) {
         float2 s2 = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int p = 0; p < 8; ++p) s2 = ffma2(q2[g][p], kv[p], s2);
+        for (int p = 0; p < 4; ++p) s2 = ffma2(q2[g][p], kv[p], s2);
         part[g] = s2.x + s2.y;
       }
       float s = reduce_heads<G>(part, lane);
       if (r >= nrow) s = -INFINITY;
-      if ((kk & (8 / G - 1)) == 0) S[r][hl] = s;
+      if ((kk & (16 / G - 1)) == 0) S[r][hl] = s;
     }
     __syncwarp();
     // chunk maximum per head over the warp's rows, softmax weights in place
     float mx = -INFINITY;
-    for (int x = lane; x < kTokPerWarp * G; x += 32) mx = fmaxf(mx, S[r0 + x / G][x % G]);
+    for (int x = lane; x < kRowsPerWarp * G; x += 32) mx = fmaxf(mx, S[r0 + x / G][x % G]);
 #pragma unroll
     for (int msk = G; msk < 32; msk <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, msk));
     float corr[G];
@@ -933,7 +923,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn(CtxView v, StepArgs a,
     const float corr_own = (m_own == -INFINITY) ? 0.f : exp2f(m_own - m_own_new);
     m_own = m_own_new;
     float psum = 0.f;
-    for (int x = lane; x < kTokPerWarp * G; x += 32) {
+    for (int x = lane; x < kRowsPerWarp * G; x += 32) {
       const float sv = S[r0 + x / G][x % G];
       const float p = (sv == -INFINITY) ? 0.f : exp2f(sv - m_own_new);
       S[r0 + x / G][x % G] = p;
@@ -946,23 +936,23 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn(CtxView v, StepArgs a,
     for (int g = 0; g < G; ++g) {
       const float2 c2 = make_float2(corr[g], corr[g]);
 #pragma unroll
-      for (int p = 0; p < 8; ++p) acc[g][p] = fmul2(acc[g][p], c2);
+      for (int p = 0; p < 4; ++p) acc[g][p] = fmul2(acc[g][p], c2);
     }
 #pragma unroll
-    for (int it = 0; it < kTokPerWarp / 4; ++it) {
-      const int r = r0 + it * 4 + grp;
-      float2 vv[8];
-      row16<DT>(Vs + r * RB, kk, vv);
+    for (int it = 0; it < kRowsPerWarp / 2; ++it) {
+      const int r = r0 + it * 2 + grp;
+      float2 vv[4];
+      row8<DT>(Vs + r * RB, kk, vv);
       if (r >= nrow) {
 #pragma unroll
-        for (int p = 0; p < 8; ++p) vv[p] = make_float2(0.f, 0.f);  // unwritten shared memory
+        for (int p = 0; p < 4; ++p) vv[p] = make_float2(0.f, 0.f);  // unwritten shared memory
       }
 #pragma unroll
       for (int g = 0; g < G; ++g) {
         const float pg = S[r][g];
         const float2 p2 = make_float2(pg, pg);
 #pragma unroll
-        for (int p = 0; p < 8; ++p) acc[g][p] = ffma2(p2, vv[p], acc[g][p]);
+        for (int p = 0; p < 4; ++p) acc[g][p] = ffma2(p2, vv[p], acc[g][p]);
       }
     }
     __syncthreads();  // every warp is done with this stage and with S
@@ -976,13 +966,11 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn(CtxView v, StepArgs a,
   float(*wacc)[G][kHeadDim] = reinterpret_cast<float(*)[G][kHeadDim]>(smem);
   static_assert(kAttnWarps * G * kHeadDim * sizeof(float) <= (size_t)kStages * stage_bytes<DT>(), "");
 
-  // sum the four row groups of each warp; per-head totals of l
+  // sum the two row groups of each warp; per-head totals of l
 #pragma unroll
   for (int g = 0; g < G; ++g)
 #pragma unroll
-    for (int p = 0; p < 8; ++p) {
-      acc[g][p].x += __shfl_xor_sync(kFull, acc[g][p].x, 8);
-      acc[g][p].y += __shfl_xor_sync(kFull, acc[g][p].y, 8);
+    for (int p = 0; p < 4; ++p) {
       acc[g][p].x += __shfl_xor_sync(kFull, acc[g][p].x, 16);
       acc[g][p].y += __shfl_xor_sync(kFull, acc[g][p].y, 16);
     }
@@ -996,9 +984,9 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn(CtxView v, StepArgs a,
 #pragma unroll
     for (int g = 0; g < G; ++g)
 #pragma unroll
-      for (int p = 0; p < 8; ++p) {
-        wacc[wid][g][dim_of(kk, p, 0)] = acc[g][p].x;
-        wacc[wid][g][dim_of(kk, p, 1)] = acc[g][p].y;
+      for (int p = 0; p < 4; ++p) {
+        wacc[wid][g][8 * kk + 2 * p] = acc[g][p].x;
+        wacc[wid][g][8 * kk + 2 * p + 1] = acc[g][p].y;
       }
   }
   __syncthreads();
