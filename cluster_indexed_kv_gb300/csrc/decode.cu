@@ -750,6 +750,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn(CtxView v, StepArgs a,
   __shared__ float wm[kAttnWarps][G], wl[kAttnWarps][G];
   __shared__ int4 pcs[kPreChunks][kAttnChunk];
   __shared__ int pcn[kPreChunks];
+  __shared__ int done_cnt[kStages];  // warps finished with the chunk in each stage
   __shared__ int s_last, s_ok;
 
   const int per_l = v.B * v.Hkv;
@@ -784,7 +785,10 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn(CtxView v, StepArgs a,
       }
     }
   if (tid == 0) {
-    for (int i = 0; i < kStages; ++i) mbar_init(&bar[i], 1);
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&bar[i], 1);
+      done_cnt[i] = 0;
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
@@ -955,12 +959,23 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn(CtxView v, StepArgs a,
         for (int p = 0; p < 4; ++p) acc[g][p] = ffma2(p2, vv[p], acc[g][p]);
       }
     }
-    __syncthreads();  // every warp is done with this stage and with S
-    if (wid == 0 && i + kStages < n_my) {
+    // this warp is done with the stage; the last warp to finish refills it
+    // with chunk i + kStages (no block-wide barrier: warps run ahead freely)
+    __syncwarp();
+    int last = 0;
+    if (lane == 0) {
+      __threadfence_block();
+      last = atomicAdd(&done_cnt[i % kStages], 1) == kAttnWarps - 1;
+      if (last) done_cnt[i % kStages] = 0;
+      __threadfence_block();
+    }
+    last = __shfl_sync(kFull, last, 0);
+    if (last && i + kStages < n_my) {
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       issue(i + kStages);
     }
   }
+  __syncthreads();
   if (!s_ok && tid == 0) set_err(v.err, kErrTimeout);
   // the pipeline buffers are free now: reuse them for the warp accumulators
   float(*wacc)[G][kHeadDim] = reinterpret_cast<float(*)[G][kHeadDim]>(smem);
