@@ -189,6 +189,7 @@ lkv_status lkv_create(const lkv_config *cfg, lkv_ctx **out) {
   v.perm = (int32_t *)dalloc(c, S_all * n_cap * 4, &st);
   v.st = (DecState *)dalloc(c, LB * sizeof(DecState), &st);
   v.q_prev = dalloc(c, LB * H * d * es, &st);
+  v.q_attn = (float *)dalloc(c, LB * H * d * 4, &st);
   v.segsum = (int64_t *)dalloc(c, S_all * d * 8, &st);
   v.scores = (float *)dalloc(c, S_all * u_cap * 4, &st);
   v.sel = (int32_t *)dalloc(c, S_all * u_cap * 4, &st);
@@ -197,8 +198,6 @@ lkv_status lkv_create(const lkv_config *cfg, lkv_ctx **out) {
   v.rng_row = (int32_t *)dalloc(c, S_all * u_cap * 4, &st);
   v.rng_cum = (int32_t *)dalloc(c, S_all * (u_cap + 1) * 4, &st);
   v.max_chunks = max_chunks;
-  v.part_acc = (float *)dalloc(c, S_all * max_chunks * G * d * 4, &st);
-  v.part_ml = (float *)dalloc(c, S_all * max_chunks * G * 2 * 4, &st);
   v.attn_count = (int32_t *)dalloc(c, S_all * 4, &st);
   v.score_count = (int32_t *)dalloc(c, S_all * 4, &st);
   v.max_pieces = u_cap + max_chunks;

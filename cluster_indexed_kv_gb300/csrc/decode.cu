@@ -316,10 +316,14 @@ __global__ void __launch_bounds__(kBoundaryThreads) k_step_boundary(CtxView v, S
     }
   }
   if (slow) atomicOr(&slow_any, 1);
-  // the current queries become the previous ones
+  // the current queries become the previous ones; the attention gets them
+  // pre-scaled by log2(e)/sqrt(d) (its scores are in base 2)
+  const float qscale = 1.4426950408889634f * rsqrtf((float)kHeadDim);
   for (int y = tid; y < nvec; y += nth) {
     const int head = y / (kHeadDim / per16), j0 = (y % (kHeadDim / per16)) * per16;
     const float *src = qsm + ((int64_t)H + head) * kQPitch + j0;
+#pragma unroll
+    for (int i = 0; i < per16; ++i) v.q_attn[(lb * H + head) * kHeadDim + j0 + i] = src[i] * qscale;
     if constexpr (DT == 1) {
       uint4 o;
       uint32_t w[4];
@@ -734,11 +738,33 @@ __device__ __forceinline__ int head_of_lane(int k) {
 template <int DT>
 constexpr int stage_bytes() { return 2 * kAttnChunk * kHeadDim * elem_bytes<DT>(); }
 
-// Split-K attention. CTA (slice, split) streams chunks [split * cpc, ...) of
-// the slice's token list (selected rows, then the local buffer) through a
-// 3-stage ring of shared-memory buffers filled by bulk copies. Per chunk,
-// each of the 8 warps owns 8 rows: pass 1 scores them (16 lanes per row, 2
-// rows per instruction), pass 2 adds p * V into per-lane accumulators.
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Load a float from the shared memory of CTA `rank` of this cluster, at the
+// address that p has in this CTA.
+__device__ __forceinline__ float ld_dsmem(const float *p, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(p)), "r"(rank));
+  float x;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(x) : "r"(remote) : "memory");
+  return x;
+}
+
+constexpr int kMaxSplit = 8;  // CTAs per slice = thread-block cluster size (portable maximum)
+
+// Split-K attention. The nsplit CTAs of a (seq, layer, kv head) form one
+// thread-block cluster; CTA split streams chunks [split * cpc, ...) of the
+// slice's token list (selected rows, then the local buffer) through a 3-stage
+// ring of shared-memory buffers filled by bulk copies. Per chunk, each of the
+// 8 warps owns 8 rows: pass 1 scores them (16 lanes per row, 2 rows per
+// instruction), pass 2 adds p * V into per-lane accumulators. The CTAs'
+// partial softmax states meet in CTA 0 through distributed shared memory.
 template <int DT, int G>
 __global__ void __launch_bounds__(kAttnThreads, 2) k_attn(CtxView v, StepArgs a, int cpc) {
   constexpr int RB = kHeadDim * elem_bytes<DT>();
@@ -751,7 +777,9 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn(CtxView v, StepArgs a,
   __shared__ int4 pcs[kPreChunks][kAttnChunk];
   __shared__ int pcn[kPreChunks];
   __shared__ int done_cnt[kStages];  // warps finished with the chunk in each stage
-  __shared__ int s_last, s_ok;
+  __shared__ float part_m[G], part_l[G], part_acc[G][kHeadDim];  // this CTA's partial
+  __shared__ DecState s_st;
+  __shared__ int s_nt, s_ns, s_ok;
 
   const int per_l = v.B * v.Hkv;
   const int li = blockIdx.x / per_l, rem = blockIdx.x % per_l;
@@ -761,37 +789,42 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn(CtxView v, StepArgs a,
   const int64_t gs = lb * v.Hkv + h;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int grp = lane >> 4, kk = lane & 15;
-  pdl_wait();
-  pdl_trigger();
-  const DecState st = v.st[lb];
-  const int t_cur = st.t - 1, ws = st.win_start;
-  const int64_t k = t_cur - a.base_t;
-  const int nt = v.n_tok[gs];
-  const int total = nt + (t_cur - ws + 1);
   const int H = v.Hkv * G;
   const int nsplit = gridDim.y, split = blockIdx.y;
-  const int nch = (total + kAttnChunk - 1) / kAttnChunk;
   const int c_begin = split * cpc;
-  const int n_my = max(0, min(cpc, nch - c_begin));
-  const int nsc = (nt + kAttnChunk - 1) / kAttnChunk;
+  pdl_wait();
+  pdl_trigger();
 
-  // the copy plan of this CTA's first chunks, fetched at once
-  if (!v.offload)
-    for (int x = tid; x < kPreChunks * kAttnChunk; x += kAttnThreads) {
-      const int c = c_begin + x / kAttnChunk;
-      if (x / kAttnChunk < n_my && c < nsc) {
-        pcs[x / kAttnChunk][x % kAttnChunk] = v.chunk_pieces[(gs * v.max_chunks + c) * kAttnChunk + x % kAttnChunk];
-        if (x % kAttnChunk == 0) pcn[x / kAttnChunk] = v.chunk_count[gs * v.max_chunks + c];
-      }
-    }
+  // one round of loads: decode state, queries, and (speculatively) the copy
+  // plan of this CTA's first chunks
   if (tid == 0) {
+    s_st = v.st[lb];
+    s_nt = v.n_tok[gs];
+    s_ns = v.n_sel[gs];
+    s_ok = 1;
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&bar[i], 1);
       done_cnt[i] = 0;
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  for (int x = tid; x < G * kHeadDim; x += kAttnThreads)
+    qs[x / kHeadDim][x % kHeadDim] = v.q_attn[(lb * H + (int64_t)h * G) * kHeadDim + x];
+  if (!v.offload)
+    for (int x = tid; x < kPreChunks * kAttnChunk; x += kAttnThreads) {
+      const int i = x / kAttnChunk, c = c_begin + i;
+      if (i < cpc && c < v.max_chunks) {
+        pcs[i][x % kAttnChunk] = v.chunk_pieces[(gs * v.max_chunks + c) * kAttnChunk + x % kAttnChunk];
+        if (x % kAttnChunk == 0) pcn[i] = v.chunk_count[gs * v.max_chunks + c];
+      }
+    }
   __syncthreads();
+  const int t_cur = s_st.t - 1, ws = s_st.win_start;
+  const int64_t k = t_cur - a.base_t;
+  const int nt = s_nt;
+  const int total = nt + (t_cur - ws + 1);
+  const int nch = (total + kAttnChunk - 1) / kAttnChunk;
+  const int n_my = max(0, min(cpc, nch - c_begin));
 
   const unsigned char *selk, *selv;
   if (!v.offload) {
@@ -801,7 +834,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn(CtxView v, StepArgs a,
     selk = (const unsigned char *)v.stage_k + gs * (int64_t)v.bud_cap * RB;
     selv = (const unsigned char *)v.stage_v + gs * (int64_t)v.bud_cap * RB;
   }
-  // warp 0 fills stage (i % kStages) with chunk c_begin + i
+  // one warp fills stage (i % kStages) with chunk c_begin + i
   auto issue = [&](int i) {
     unsigned char *Ks = smem + (i % kStages) * SB;
     unsigned char *Vs = Ks + SB / 2;
@@ -854,14 +887,6 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn(CtxView v, StepArgs a,
   if (wid == 0)
     for (int i = 0; i < min(n_my, kStages); ++i) issue(i);
 
-  // query rows of the group, pre-scaled by log2(e)/sqrt(d) (scores in base 2)
-  const float qscale = 1.4426950408889634f * rsqrtf((float)kHeadDim);
-  const void *q = (const char *)a.q + k * a.stride_q * elem_bytes<DT>();
-  const int64_t qoff = (((int64_t)b * a.nl + li) * H + (int64_t)h * G) * kHeadDim;
-  for (int x = tid; x < G * kHeadDim; x += kAttnThreads)
-    qs[x / kHeadDim][x % kHeadDim] = load_elem<DT>(q, qoff + x) * qscale;
-  if (tid == 0) s_ok = 1;
-  __syncthreads();
   float2 q2[G][4];
 #pragma unroll
   for (int g = 0; g < G; ++g)
@@ -1006,7 +1031,6 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn(CtxView v, StepArgs a,
   }
   __syncthreads();
   // merge the warps into this CTA's partial
-  const int64_t pbase = (gs * v.max_chunks + split) * G;
   for (int x = tid; x < G * kHeadDim; x += kAttnThreads) {
     const int g = x / kHeadDim, dim = x % kHeadDim;
     float mm = -INFINITY;
@@ -1019,51 +1043,52 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn(CtxView v, StepArgs a,
       o = fmaf(sw, wacc[w][g][dim], o);
       z = fmaf(sw, wl[w][g], z);
     }
-    v.part_acc[(pbase + g) * kHeadDim + dim] = o;
+    part_acc[g][dim] = o;
     if (dim == 0) {
-      v.part_ml[(pbase + g) * 2] = mm;
-      v.part_ml[(pbase + g) * 2 + 1] = z;
+      part_m[g] = mm;
+      part_l[g] = z;
     }
   }
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) s_last = (atomicAdd(&v.attn_count[gs], 1) == nsplit - 1);
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  // last CTA: combine the partials, publish the outputs
-  float *out = a.out + k * a.stride_out;
-  const int64_t obase = (((int64_t)b * a.nl + li) * H + (int64_t)h * G) * kHeadDim;
-  for (int x = tid; x < G * kHeadDim; x += kAttnThreads) {
-    const int g = x / kHeadDim, dim = x % kHeadDim;
-    float mm = -INFINITY;
-#pragma unroll 8
-    for (int c = 0; c < nsplit; ++c)
-      mm = fmaxf(mm, __ldcg(&v.part_ml[((gs * v.max_chunks + c) * G + g) * 2]));
-    float o = 0.f, z = 0.f;
-#pragma unroll 8
-    for (int c = 0; c < nsplit; ++c) {
-      const int64_t pi = (gs * v.max_chunks + c) * G + g;
-      const float mc = __ldcg(&v.part_ml[pi * 2]);
-      const float sw = (mc == -INFINITY) ? 0.f : exp2f(mc - mm);
-      o = fmaf(sw, __ldcg(&v.part_acc[pi * kHeadDim + dim]), o);
-      z = fmaf(sw, __ldcg(&v.part_ml[pi * 2 + 1]), z);
+  // CTA 0 of the cluster combines every CTA's partial (read through
+  // distributed shared memory); the second cluster barrier keeps the other
+  // CTAs' shared memory alive until it is done
+  cluster_sync();
+  if (cluster_rank() == 0) {
+    float *out = a.out + k * a.stride_out;
+    const int64_t obase = (((int64_t)b * a.nl + li) * H + (int64_t)h * G) * kHeadDim;
+    for (int x = tid; x < G * kHeadDim; x += kAttnThreads) {
+      const int g = x / kHeadDim, dim = x % kHeadDim;
+      float mc[kMaxSplit];
+      float mm = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < kMaxSplit; ++c) {
+        mc[c] = (c < nsplit) ? ld_dsmem(&part_m[g], c) : -INFINITY;
+        mm = fmaxf(mm, mc[c]);
+      }
+      float o = 0.f, z = 0.f;
+#pragma unroll
+      for (int c = 0; c < kMaxSplit; ++c) {
+        if (c >= nsplit || mc[c] == -INFINITY) continue;
+        const float sw = exp2f(mc[c] - mm);
+        o = fmaf(sw, ld_dsmem(&part_acc[g][dim], c), o);
+        z = fmaf(sw, ld_dsmem(&part_l[g], c), z);
+      }
+      out[obase + x] = o / z;
     }
-    out[obase + x] = o / z;
+    const int64_t so = ((int64_t)b * a.nl + li) * v.Hkv + h;
+    const int ns = s_ns;
+    if (a.selected_units) {
+      const int32_t *sel = v.sel + gs * v.u_cap;
+      int32_t *dst = a.selected_units + k * a.stride_sel + so * v.u_cap;
+      for (int x = tid; x < ns; x += kAttnThreads) dst[x] = sel[x];
+    }
+    if (tid == 0) {
+      if (a.n_selected) a.n_selected[k * a.stride_nsel + so] = ns;
+      atomicAdd((unsigned long long *)&v.counters[kCntAttnRows], (unsigned long long)total);
+      atomicAdd((unsigned long long *)&v.counters[kCntAttnSlices], 1ull);
+    }
   }
-  const int64_t so = ((int64_t)b * a.nl + li) * v.Hkv + h;
-  const int ns = v.n_sel[gs];
-  if (a.selected_units) {
-    const int32_t *sel = v.sel + gs * v.u_cap;
-    int32_t *dst = a.selected_units + k * a.stride_sel + so * v.u_cap;
-    for (int x = tid; x < ns; x += kAttnThreads) dst[x] = sel[x];
-  }
-  if (tid == 0) {
-    if (a.n_selected) a.n_selected[k * a.stride_nsel + so] = ns;
-    v.attn_count[gs] = 0;
-    atomicAdd((unsigned long long *)&v.counters[kCntAttnRows], (unsigned long long)total);
-    atomicAdd((unsigned long long *)&v.counters[kCntAttnSlices], 1ull);
-  }
+  cluster_sync();
 }
 
 // ---------------------------------------------------------------- host
@@ -1091,11 +1116,12 @@ constexpr size_t attn_smem() { return (size_t)kStages * stage_bytes<DT>(); }
 
 static int g_attn_slots = 2 * 152;  // resident attention CTAs on the device
 
-// Split of a slice's chunks over CTAs so that the whole grid is resident at
-// once (one wave).
+// Split of a slice's chunks over the CTAs of one cluster (at most kMaxSplit),
+// so that the whole grid is resident at once where possible.
 static void attn_split(int slices, int nch, int *nsplit, int *cpc) {
   int want = g_attn_slots / slices;
   if (want < 1) want = 1;
+  if (want > kMaxSplit) want = kMaxSplit;
   if (want > nch) want = nch;
   *cpc = (nch + want - 1) / want;
   *nsplit = (nch + *cpc - 1) / *cpc;
@@ -1105,7 +1131,21 @@ template <int DT, int G>
 static void launch_attn(const CtxView &v, const StepArgs &a, int slices, int nch, cudaStream_t st) {
   int nsplit = 1, cpc = 1;
   attn_split(slices, nch, &nsplit, &cpc);
-  launch_pdl(k_attn<DT, G>, dim3(slices, nsplit), dim3(kAttnThreads), attn_smem<DT, G>(), st, v, a, cpc);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(slices, nsplit);
+  cfg.blockDim = dim3(kAttnThreads);
+  cfg.dynamicSmemBytes = attn_smem<DT, G>();
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 1;
+  attr[1].val.clusterDim.y = nsplit;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  cudaLaunchKernelEx(&cfg, k_attn<DT, G>, v, a, cpc);
 }
 
 template <int DT, int G>

@@ -66,6 +66,7 @@ struct CtxView {
   int32_t *perm;              // [slice][n_cap]
   DecState *st;               // [lb]
   void *q_prev;               // [lb][H][d] (dtype)
+  float *q_attn;              // [lb][H][d] this step's queries * log2(e)/sqrt(d), fp32
   int64_t *segsum;            // [slice][d] exact fixed-point sums (bf16) or
                               // doubles reinterpreted (fp32)
   float *scores;              // [slice][u_cap]
@@ -79,8 +80,6 @@ struct CtxView {
   int4 *chunk_pieces;         // [slice][max_chunks][64] the pieces of each chunk
   int32_t *chunk_count;       // [slice][max_chunks] pieces in each chunk
   int32_t max_pieces;
-  float *part_acc;            // [slice][max_chunks][G][d]
-  float *part_ml;             // [slice][max_chunks][G][2]
   int32_t *attn_count;        // [slice]
   int32_t *score_count;       // [slice] score CTAs done this step (last one selects)
   int32_t max_chunks;
