@@ -386,17 +386,32 @@ constexpr int kScoreWarps = kScoreThreads / 32;
 // while they fit. Output: ascending unit ids, their first rows, the exclusive
 // token prefix, and the copy plan (selected rows cut at 64-token chunk
 // boundaries).
+constexpr int kSelSmemUnits = 4096;  // units whose keys and lengths fit in shared memory
+
 __device__ void select_units(const CtxView &v, int64_t gs, int U, int budget) {
-  const float *sc = v.scores + gs * v.u_cap;
-  const int32_t *ln = v.unit_len + gs * v.u_cap;
   const int tid = threadIdx.x, nth = blockDim.x, wid = tid >> 5;
+  // keys and lengths once into shared memory (fall back to global memory for
+  // very large unit tables)
+  __shared__ uint32_t key_s[kSelSmemUnits];
+  __shared__ int32_t len_s[kSelSmemUnits];
+  const float *scg = v.scores + gs * v.u_cap;
+  const int32_t *lng = v.unit_len + gs * v.u_cap;
+  const bool in_smem = U <= kSelSmemUnits;
+  if (in_smem)
+    for (int u = tid; u < U; u += nth) {
+      key_s[u] = desc_key(__ldcg(scg + u));
+      len_s[u] = lng[u];
+    }
+  __syncthreads();
+  auto keyof = [&](int u) -> uint32_t { return in_smem ? key_s[u] : desc_key(__ldcg(scg + u)); };
+  auto lenof = [&](int u) -> int32_t { return in_smem ? len_s[u] : lng[u]; };
   __shared__ int32_t whist[kScoreWarps][256];
   __shared__ int32_t wt[32];
   __shared__ int32_t s_total, s_below, s_all, s_nsel, s_ntok, s_npieces;
   __shared__ uint32_t s_prefix, s_mask;
 
   int32_t part = 0;
-  for (int u = tid; u < U; u += nth) part += ln[u];
+  for (int u = tid; u < U; u += nth) part += lenof(u);
   block_scan_excl(part, wt, &s_total);
   if (tid == 0) {
     s_all = s_total <= budget;
@@ -412,8 +427,8 @@ __device__ void select_units(const CtxView &v, int64_t gs, int U, int budget) {
       __syncthreads();
       const uint32_t prefix = s_prefix, mask = s_mask;
       for (int u = tid; u < U; u += nth) {
-        const uint32_t key = desc_key(__ldcg(sc + u));
-        if ((key & mask) == prefix) atomicAdd(&whist[wid][(key >> shift) & 255u], ln[u]);
+        const uint32_t key = keyof(u);
+        if ((key & mask) == prefix) atomicAdd(&whist[wid][(key >> shift) & 255u], lenof(u));
       }
       __syncthreads();
       for (int bin = tid; bin < 256; bin += nth) {
@@ -461,10 +476,10 @@ __device__ void select_units(const CtxView &v, int64_t gs, int U, int budget) {
   const int u0 = tid * per, u1 = min(U, u0 + per);
   auto is_sel = [&](int u, int32_t &run) -> bool {
     if (all) return true;
-    const uint32_t key = desc_key(__ldcg(sc + u));
+    const uint32_t key = keyof(u);
     if (key < kstar) return true;
     if (key == kstar) {
-      run += ln[u];
+      run += lenof(u);
       return below + run <= budget;
     }
     return false;
@@ -473,13 +488,13 @@ __device__ void select_units(const CtxView &v, int64_t gs, int U, int budget) {
   int32_t tl = 0;
   if (!all)
     for (int u = u0; u < u1; ++u)
-      if (desc_key(__ldcg(sc + u)) == kstar) tl += ln[u];
+      if (keyof(u) == kstar) tl += lenof(u);
   const int32_t tie_ex = block_scan_excl(tl, wt, nullptr);
   int32_t cnt = 0, toks = 0;
   {
     int32_t run = tie_ex;
     for (int u = u0; u < u1; ++u)
-      if (is_sel(u, run)) { ++cnt; toks += ln[u]; }
+      if (is_sel(u, run)) { ++cnt; toks += lenof(u); }
   }
   const int32_t cnt_ex = block_scan_excl(cnt, wt, &s_nsel);
   const int32_t tok_ex = block_scan_excl(toks, wt, &s_ntok);
@@ -492,7 +507,7 @@ __device__ void select_units(const CtxView &v, int64_t gs, int U, int budget) {
     const int32_t *rows = v.unit_row + gs * v.u_cap;
     for (int u = u0; u < u1; ++u) {
       if (!is_sel(u, run)) continue;
-      const int32_t len = ln[u];
+      const int32_t len = lenof(u);
       sel_out[kk] = u;
       row_out[kk] = rows[u];
       cum_out[kk] = cum;
@@ -509,7 +524,7 @@ __device__ void select_units(const CtxView &v, int64_t gs, int U, int budget) {
     const int32_t *rows = v.unit_row + gs * v.u_cap;
     for (int u = u0; u < u1 && p - pc_ex < npc; ++u) {
       if (!is_sel(u, run)) continue;
-      int32_t len = ln[u], src = rows[u], f = cum;
+      int32_t len = lenof(u), src = rows[u], f = cum;
       cum += len;
       while (len > 0) {
         const int32_t room = kAttnChunk - f % kAttnChunk;
@@ -575,16 +590,26 @@ __global__ void __launch_bounds__(kScoreThreads) k_score_select(CtxView v, StepA
     qbar[threadIdx.x] = acc;
   }
   __syncthreads();
-  constexpr int per16 = 16 / elem_bytes<DT>();
+  constexpr int nvec = kHeadDim * elem_bytes<DT>() / 16;  // 16-byte vectors per centroid row
   for (int u = blockIdx.y * blockDim.x + threadIdx.x; u < U; u += gridDim.y * blockDim.x) {
-    const int64_t base = (gs * v.u_cap + u) * kHeadDim;
-    float s = 0.f;
-#pragma unroll 4
-    for (int j0 = 0; j0 < kHeadDim; j0 += per16) {
-      float c[8];
-      load16<DT>(v.cent_op, base + j0, c);
+    const uint4 *row = (const uint4 *)((const char *)v.cent_op + (gs * v.u_cap + u) * kHeadDim * elem_bytes<DT>());
+    uint4 raw[nvec];
 #pragma unroll
-      for (int e = 0; e < per16; ++e) s = __fmaf_rn(qbar[j0 + e], c[e], s);
+    for (int j = 0; j < nvec; ++j) raw[j] = __ldg(row + j);  // the whole row in one round trip
+    float s = 0.f;
+#pragma unroll
+    for (int j = 0; j < nvec; ++j) {
+      const uint32_t w[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
+      if constexpr (DT == 1) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          s = __fmaf_rn(qbar[j * 8 + 2 * e], __uint_as_float(w[e] << 16), s);
+          s = __fmaf_rn(qbar[j * 8 + 2 * e + 1], __uint_as_float(w[e] & 0xffff0000u), s);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) s = __fmaf_rn(qbar[j * 4 + e], __uint_as_float(w[e]), s);
+      }
     }
     v.scores[gs * v.u_cap + u] = s;
   }
