@@ -126,6 +126,12 @@ class Context:
     def set_profiling(self, enable: bool) -> None:
         _lib.lkv_set_profiling(self._ctx, enable)
 
+    def set_kmeans_filter(self, tensor_cores: bool) -> None:
+        """Tensor-core (default) or SIMT distance filter for the K-means
+        assignment; the result is the same either way."""
+        _lib.lkv_set_kmeans_filter(self._ctx, _lib.LKV_FILTER_TENSOR if tensor_cores
+                                   else _lib.LKV_FILTER_SIMT)
+
     def profile(self, reset: bool = False):
         return _lib.lkv_get_profile(self._ctx, reset)
 

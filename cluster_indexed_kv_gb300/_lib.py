@@ -20,7 +20,8 @@ LKV_DTYPE_FP32, LKV_DTYPE_BF16 = 0, 1
 EXPORTED = ("lkv_create", "lkv_destroy", "lkv_build_index", "lkv_load_index",
             "lkv_decode_step", "lkv_decode_steps", "lkv_get_index", "lkv_get_decode_state",
             "lkv_sync", "lkv_last_error", "lkv_set_profiling", "lkv_get_profile",
-            "lkv_kmeans_static")
+            "lkv_kmeans_static", "lkv_set_kmeans_filter")
+LKV_FILTER_TENSOR, LKV_FILTER_SIMT = 0, 1
 
 
 class lkv_config(C.Structure):
@@ -84,6 +85,8 @@ def load(path: str = LIB_PATH):
         L.lkv_decode_steps.restype = st
         L.lkv_set_profiling.argtypes = [vp, i32]
         L.lkv_set_profiling.restype = st
+        L.lkv_set_kmeans_filter.argtypes = [vp, i32]
+        L.lkv_set_kmeans_filter.restype = st
         L.lkv_get_profile.argtypes = [vp, vp, i32, C.POINTER(i32), vp, i32]
         L.lkv_get_profile.restype = st
         L.lkv_get_index.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, C.POINTER(i32)]
@@ -141,6 +144,10 @@ def lkv_decode_steps(ctx, layer, n_layers, n_steps, q_ptr, k_ptr, v_ptr, tau, bu
 
 def lkv_set_profiling(ctx, enable: bool) -> None:
     _check(load().lkv_set_profiling(ctx, 1 if enable else 0), ctx)
+
+
+def lkv_set_kmeans_filter(ctx, filter_: int) -> None:
+    _check(load().lkv_set_kmeans_filter(ctx, filter_), ctx)
 
 
 def lkv_get_profile(ctx, reset: bool = False):

@@ -35,6 +35,7 @@ struct lkv_ctx {
   std::vector<int32_t> n_clusters;
   std::string err;
   bool broken = false;
+  bool use_tc = true;             // tensor-core distance filter for bf16 keys
   int alloc_index = 0;
   int fail_at = -1;               // host-side allocation-failure injection
 };
@@ -278,7 +279,7 @@ lkv_status lkv_build_index(lkv_ctx *c, int32_t layer, const void *keys, const vo
   std::vector<int64_t> idx((size_t)S * nc), perm;
   for (int sl = 0; sl < S; ++sl) init_indices(n, nc, seed + (uint64_t)sl, idx.data() + (size_t)sl * nc, perm);
   cudaError_t e = cudaMemcpyAsync(c->ks.init_idx, idx.data(), idx.size() * 8, cudaMemcpyHostToDevice, c->stream);
-  if (e == cudaSuccess) e = lkv::launch_kmeans_build(c->v, layer, c->ks, keys, values, n, nc, iters, false, c->stream, c->prof);
+  if (e == cudaSuccess) e = lkv::launch_kmeans_build(c->v, layer, c->ks, keys, values, n, nc, iters, c->use_tc, c->stream, c->prof);
   if (e != cudaSuccess) return cuda_fail(c, e, "lkv_build_index");
   c->built[layer] = 1;
   c->steps[layer] = 0;
@@ -446,7 +447,15 @@ lkv_status lkv_decode_steps(lkv_ctx *c, int32_t layer, int32_t nl, int32_t n_ste
 static const char *kKindNames[lkv::kPNum] = {
     "lkv_boundary", "lkv_score_select", "lkv_gather_offload", "lkv_attn",
     "kmeans_init", "kmeans_operand", "kmeans_assign", "kmeans_refine", "kmeans_sort",
-    "kmeans_update", "kmeans_pool"};
+    "kmeans_update", "kmeans_pool", "kmeans_assign_tc"};
+
+lkv_status lkv_set_kmeans_filter(lkv_ctx *ctx, int32_t filter) {
+  if (!ctx) return fail(nullptr, LKV_EINVAL, "null context");
+  if (filter != LKV_FILTER_TENSOR && filter != LKV_FILTER_SIMT)
+    return fail(ctx, LKV_EINVAL, "unknown K-means filter");
+  ctx->use_tc = filter == LKV_FILTER_TENSOR;
+  return LKV_OK;
+}
 
 lkv_status lkv_set_profiling(lkv_ctx *c, int32_t enable) {
   lkv_status s = check_usable(c);

@@ -19,6 +19,9 @@
 // cluster); the member sum of bf16 keys is formed exactly in 2^-40 fixed
 // point (double-precision token-order sum when a value is out of that range,
 // and always for fp32 keys); centroid = float(sum / count) in double.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <mutex>
 #include <string>
 
@@ -158,9 +161,12 @@ __device__ __forceinline__ void assign_decide(const Top3 &t, int32_t c, float kn
                                               int4 *amb, int32_t *amb_count,
                                               int32_t amb_cap, int32_t *err) {
   const float beta2 = 2.f * eps * (kn * cmax + c2max);
-  *assign_row = t.j1;
-  if (c == 1 || t.v2 - t.v1 > beta2) return;
-  const int crowded = (c > 2) && !(t.v3 - t.v1 > beta2);
+  // (non-finite keys or centroids leave the filter without a candidate: the
+  // id written stays in range and the key goes to the full exact scan)
+  const bool valid = t.j1 < c && (c == 1 || t.j2 < c);
+  *assign_row = t.j1 < c ? t.j1 : 0;
+  if (c == 1 || (valid && t.v2 - t.v1 > beta2)) return;
+  const int crowded = !valid || ((c > 2) && !(t.v3 - t.v1 > beta2));
   const int slot = atomicAdd(amb_count, 1);
   if (slot < amb_cap)
     amb[slot] = make_int4(s, (int)row, t.j1, (int)((unsigned)t.j2 | ((unsigned)crowded << 31)));
@@ -301,6 +307,302 @@ k_assign_simt(const void *keys, int64_t n, int32_t c, const void *cent_op,
   }
 }
 
+// ---------------------------------------------------------------- tcgen05 distance filter
+
+// Tensor-core filter for bf16 keys: a persistent CTA takes 128-key tiles; per
+// tile it streams the centroid operand in 256-row chunks and computes
+// k . c~ for all 128 x 256 pairs with tcgen05.mma (bf16 x bf16 -> fp32 in
+// TMEM, two accumulators so MMAs of chunk n+1 overlap the epilogue of chunk
+// n). Warp 0 issues the TMA loads (128B-swizzled K-major tiles), warp 1 the
+// MMAs and owns the tensor memory, warps 2..9 read the accumulators (two warps
+// per TMEM lane quadrant, one per half of the columns), form
+// e_j = |c~_j|^2 - 2 k.c~_j and keep the three smallest per key; the same
+// certified decision as the SIMT filter follows (eps covers the tensor-core
+// fp32 accumulation error with a wide margin).
+constexpr int kTcM = 128;
+constexpr int kTcN = 256;
+constexpr int kTcWarps = 10;
+constexpr int kTcThreads = kTcWarps * 32;
+constexpr uint32_t kTcABytes = kTcM * kHeadDim * 2;  // 32 KB: two 64-column halves of 16 KB
+constexpr uint32_t kTcBBytes = kTcN * kHeadDim * 2;  // 64 KB: two halves of 32 KB
+constexpr size_t kTcSmem = 2 * kTcABytes + 2 * kTcBBytes + 1024;
+constexpr uint32_t kTcIdesc = (1u << 4)            // fp32 accumulator
+                              | (1u << 7)          // A bf16
+                              | (1u << 10)         // B bf16
+                              | ((uint32_t)(kTcN >> 3) << 17) | ((uint32_t)(kTcM >> 4) << 24);
+constexpr uint64_t kTcWaitNs = 2000000000ull;
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ uint64_t gtimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void tc_mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void tc_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void tc_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ bool tc_try_wait(uint64_t *bar, uint32_t phase) {
+  uint32_t ok;
+  asm volatile("{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+               : "=r"(ok) : "r"(smem_addr(bar)), "r"(phase) : "memory");
+  return ok != 0;
+}
+// Bounded wait; on timeout it raises the block's abort flag and returns false.
+__device__ __forceinline__ bool tc_wait(uint64_t *bar, uint32_t phase, volatile int *abort) {
+  if (tc_try_wait(bar, phase)) return true;
+  const uint64_t t0 = gtimer();
+  while (!tc_try_wait(bar, phase)) {
+    if (*abort || gtimer() - t0 > kTcWaitNs) {
+      *abort = 1;
+      return false;
+    }
+  }
+  return true;
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(dst), "l"((uint64_t)map), "r"(x), "r"(y), "r"(smem_addr(bar)) : "memory");
+}
+// Shared-memory matrix descriptor of a K-major bf16 tile written by TMA with
+// 128-byte swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;            // leading byte offset (unused for this layout)
+  d |= (uint64_t)(1024 >> 4) << 32;  // stride byte offset: 8 rows x 128 bytes
+  d |= (uint64_t)1 << 46;            // descriptor version
+  d |= (uint64_t)2 << 61;            // 128-byte swizzle
+  return d;
+}
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t accumulate) {
+  asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+               " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}"
+               ::"r"(d_tmem), "l"(a), "l"(b), "r"(kTcIdesc), "r"(accumulate));
+}
+__device__ __forceinline__ void tc_commit(uint64_t *bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+               ::"r"(smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+k_assign_tc(const __grid_constant__ CUtensorMap keys_map, const __grid_constant__ CUtensorMap cent_map,
+            int64_t n, int32_t c, int32_t u_cap, const float *c2, int32_t c_cap, const float *knorm,
+            int64_t n_cap, const float *cstat, float eps, int32_t *assign, int64_t gs0, int n_slices,
+            int4 *amb, int32_t *amb_count, int32_t amb_cap, int32_t *err) {
+  extern __shared__ unsigned char tc_smem_raw[];
+  __shared__ __align__(8) uint64_t a_full[2], a_empty[2], b_full[2], b_empty[2], acc_full[2], acc_empty[2];
+  __shared__ __align__(8) uint64_t mma_done;
+  __shared__ uint32_t tmem_base_s;
+  __shared__ volatile int abort_s;
+  __shared__ float xv[kTcM][3];
+  __shared__ int32_t xj[kTcM][2];
+  const uint32_t base = (smem_addr(tc_smem_raw) + 1023u) & ~1023u;
+  const uint32_t A0 = base, B0 = base + 2 * kTcABytes;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tiles = (int)((n + kTcM - 1) / kTcM);
+  const int n_items = n_slices * tiles;
+  const int nch = (c + kTcN - 1) / kTcN;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      tc_mbar_init(&a_full[i], 1);
+      tc_mbar_init(&a_empty[i], 1);
+      tc_mbar_init(&b_full[i], 1);
+      tc_mbar_init(&b_empty[i], 1);
+      tc_mbar_init(&acc_full[i], 1);
+      tc_mbar_init(&acc_empty[i], 8);
+    }
+    tc_mbar_init(&mma_done, 1);
+    abort_s = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {  // tensor memory: two 128 x 256 fp32 accumulators
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 ::"r"(smem_addr(&tmem_base_s)), "r"(2 * kTcN) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_s;
+
+  if (warp == 0) {
+    if (lane == 0) {  // TMA producer
+      int it = 0, gc = 0;
+      int a_last[2] = {-1, -1}, b_last[2] = {-1, -1};  // last fill count issued per stage
+      for (int item = blockIdx.x; item < n_items && !abort_s; item += gridDim.x, ++it) {
+        const int sl = item / tiles;
+        const int64_t m0 = (int64_t)(item % tiles) * kTcM;
+        const int ai = it & 1;
+        if (!tc_wait(&a_empty[ai], ((it >> 1) & 1) ^ 1, &abort_s)) break;
+        tc_expect_tx(&a_full[ai], kTcABytes);
+        const int ya = (int)(sl * n + m0);
+        tma_load_2d(A0 + ai * kTcABytes, &keys_map, 0, ya, &a_full[ai]);
+        tma_load_2d(A0 + ai * kTcABytes + kTcABytes / 2, &keys_map, 64, ya, &a_full[ai]);
+        a_last[ai] = it;
+        for (int ch = 0; ch < nch; ++ch, ++gc) {
+          const int bi = gc & 1;
+          if (!tc_wait(&b_empty[bi], ((gc >> 1) & 1) ^ 1, &abort_s)) break;
+          tc_expect_tx(&b_full[bi], kTcBBytes);
+          const int yb = (int)((gs0 + sl) * u_cap + (int64_t)ch * kTcN);
+          tma_load_2d(B0 + bi * kTcBBytes, &cent_map, 0, yb, &b_full[bi]);
+          tma_load_2d(B0 + bi * kTcBBytes + kTcBBytes / 2, &cent_map, 64, yb, &b_full[bi]);
+          b_last[bi] = gc;
+        }
+      }
+      if (abort_s) {  // let the copies still in flight land before the block exits
+        const uint64_t t0 = gtimer();
+        for (int i = 0; i < 2; ++i) {
+          while (a_last[i] >= 0 && !tc_try_wait(&a_full[i], (a_last[i] >> 1) & 1) && gtimer() - t0 < kTcWaitNs) {}
+          while (b_last[i] >= 0 && !tc_try_wait(&b_full[i], (b_last[i] >> 1) & 1) && gtimer() - t0 < kTcWaitNs) {}
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {  // MMA issuer
+      int it = 0, gc = 0;
+      for (int item = blockIdx.x; item < n_items && !abort_s; item += gridDim.x, ++it) {
+        const int ai = it & 1;
+        if (!tc_wait(&a_full[ai], (it >> 1) & 1, &abort_s)) break;
+        tc_fence_after();
+        for (int ch = 0; ch < nch; ++ch, ++gc) {
+          const int bi = gc & 1, ti = gc & 1;
+          if (!tc_wait(&b_full[bi], (gc >> 1) & 1, &abort_s)) break;
+          if (!tc_wait(&acc_empty[ti], ((gc >> 1) & 1) ^ 1, &abort_s)) break;
+          tc_fence_after();
+          const uint32_t d = tmem + ti * kTcN;
+#pragma unroll
+          for (int k = 0; k < kHeadDim / 16; ++k) {
+            const uint32_t ao = A0 + ai * kTcABytes + (k >> 2) * (kTcABytes / 2) + (k & 3) * 32;
+            const uint32_t bo = B0 + bi * kTcBBytes + (k >> 2) * (kTcBBytes / 2) + (k & 3) * 32;
+            tc_mma(d, sw128_desc(ao), sw128_desc(bo), k > 0 ? 1u : 0u);
+          }
+          tc_commit(&b_empty[bi]);
+          tc_commit(&acc_full[ti]);
+        }
+        tc_commit(&a_empty[ai]);
+      }
+      // every MMA of this block has completed before the tensor memory is freed
+      tc_commit(&mma_done);
+      const uint64_t t0 = gtimer();
+      while (!tc_try_wait(&mma_done, 0) && gtimer() - t0 < kTcWaitNs) {}
+    }
+  } else {  // epilogue: warps 2..9
+    const int quad = warp & 3, half = warp >= 6 ? 1 : 0;
+    const int row = quad * 32 + lane;
+    int gc = 0;
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+      const int sl = item / tiles;
+      const int64_t i = (int64_t)(item % tiles) * kTcM + row;
+      const float kn = (i < n) ? knorm[(int64_t)sl * n_cap + i] : 0.f;
+      Top3 top;
+      top.v1 = top.v2 = top.v3 = INFINITY;
+      top.j1 = top.j2 = 0x7fffffff;
+      const float *c2s = c2 + (int64_t)sl * c_cap;
+      for (int ch = 0; ch < nch; ++ch, ++gc) {
+        const int ti = gc & 1;
+        if (!abort_s) tc_wait(&acc_full[ti], (gc >> 1) & 1, &abort_s);
+        __syncwarp();
+        tc_fence_after();
+#pragma unroll 1
+        for (int g = 0; g < 4; ++g) {
+          const int col = half * 128 + g * 32;
+          const int j0 = ch * kTcN + col;
+          uint32_t r[32];
+          tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + ti * kTcN + col, r);
+          if (j0 + 32 <= c) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              top3_push(top, fmaf(-2.f, __uint_as_float(r[e]), __ldg(c2s + j0 + e)), j0 + e);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const int j = j0 + e;
+              if (j < c) top3_push(top, fmaf(-2.f, __uint_as_float(r[e]), __ldg(c2s + j)), j);
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) tc_arrive(&acc_empty[ti]);
+      }
+      // merge the two column halves of each key, then decide
+      if (half == 1) {
+        xv[row][0] = top.v1; xv[row][1] = top.v2; xv[row][2] = top.v3;
+        xj[row][0] = top.j1; xj[row][1] = top.j2;
+      }
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      if (half == 0 && i < n) {
+        Top3 o;
+        o.v1 = xv[row][0]; o.v2 = xv[row][1]; o.v3 = xv[row][2];
+        o.j1 = xj[row][0]; o.j2 = xj[row][1];
+        const Top3 m = top3_merge(top, o);
+        assign_decide(m, c, kn, cstat[2 * sl], cstat[2 * sl + 1], eps, sl, i,
+                      &assign[(gs0 + sl) * n_cap + i], amb, amb_count, amb_cap, err);
+      }
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * kTcN) : "memory");
+  }
+  if (threadIdx.x == 0 && abort_s) set_err(err, kErrTimeout);
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// against libcuda).
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (PFN_cuTensorMapEncodeTiled_v12000)p;
+  });
+  return fn;
+}
+
+// 2-D bf16 tensor map over `rows` rows of 128 elements, boxes of 64 x box_rows
+// with 128-byte swizzle (out-of-range rows read as zeros).
+static bool make_map(CUtensorMap *map, const void *base, uint64_t rows, uint32_t box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)kHeadDim * 2};
+  const cuuint32_t box[2] = {64, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Exact settlement of the queued keys: warp per entry.
 template <int DT>
 __device__ __forceinline__ double sqdist64(const void *key_row, const void *cent_row) {
@@ -353,7 +655,7 @@ __global__ void k_assign_refine(const void *keys, int64_t n, int32_t c,
       const int32_t oj = __shfl_xor_sync(0xffffffffu, bj, o);
       if (ob < best || (ob == best && oj < bj)) { best = ob; bj = oj; }
     }
-    if (lane == 0) assign[gs * n_cap + row] = bj;
+    if (lane == 0) assign[gs * n_cap + row] = bj < c ? bj : 0;
   }
 }
 
@@ -620,7 +922,8 @@ static cudaError_t finish_pool(const CtxView &v, int layer, const KmeansScratch 
 template <int DT>
 static cudaError_t kmeans_build_t(const CtxView &v, int layer, const KmeansScratch &ks,
                                   const void *keys, const void *values, int64_t n,
-                                  int32_t c, int32_t iters, cudaStream_t st, Prof &prof) {
+                                  int32_t c, int32_t iters, bool use_tc, cudaStream_t st,
+                                  Prof &prof) {
   const int S = v.B * v.Hkv;
   const int64_t gs0 = (int64_t)layer * S;
   const int c_cap = v.u_cap - v.t_cap;
@@ -628,7 +931,27 @@ static cudaError_t kmeans_build_t(const CtxView &v, int layer, const KmeansScrat
   static bool attr_done[2] = {false, false};
   if (!attr_done[DT]) {
     cudaFuncSetAttribute(k_assign_simt<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAsSmem);
+    cudaFuncSetAttribute(k_assign_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmem);
     attr_done[DT] = true;
+  }
+  // tensor-core filter (bf16 keys): TMA descriptors of the keys and of the
+  // whole centroid-operand table, one persistent CTA per SM
+  CUtensorMap keys_map, cent_map;
+  int tc_grid = 0;
+  if (DT == 1 && use_tc) {
+    const uint64_t op_rows = (uint64_t)v.u_cap * (uint64_t)(gs0 + S);
+    if (!make_map(&keys_map, keys, (uint64_t)S * (uint64_t)n, kTcM) ||
+        !make_map(&cent_map, v.cent_op, op_rows, kTcN)) {
+      use_tc = false;
+    } else {
+      int dev = 0, sms = 0;
+      cudaGetDevice(&dev);
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      const int64_t items = (int64_t)S * ((n + kTcM - 1) / kTcM);
+      tc_grid = (int)(items < sms ? items : sms);
+    }
+  } else {
+    use_tc = false;
   }
   prof.begin(kPKmInit, st, 2);
   k_init_cent<DT><<<dim3(c, S), kHeadDim, 0, st>>>(keys, n, c, ks.init_idx, v.cent32, gs0, v.u_cap);
@@ -642,10 +965,17 @@ static cudaError_t kmeans_build_t(const CtxView &v, int layer, const KmeansScrat
                                                                v.u_cap, gs0, ks.c2, ks.cstat);
     cudaMemsetAsync(ks.amb_count, 0, sizeof(int32_t), st);
     prof.end(st);
-    prof.begin(kPKmAssign, st);
-    k_assign_simt<DT><<<dim3((unsigned)((n + kAsTile - 1) / kAsTile), S), kAsThreads, kAsSmem, st>>>(
-        keys, n, c, v.cent_op, v.u_cap, ks.c2, c_cap, ks.knorm, v.n_cap, ks.cstat, eps,
-        v.assign, gs0, ks.amb, ks.amb_count, (int32_t)amb_cap, v.err);
+    prof.begin(use_tc ? kPKmAssignTc : kPKmAssign, st);
+    if (use_tc) {
+      k_assign_tc<<<tc_grid, kTcThreads, kTcSmem, st>>>(keys_map, cent_map, n, c, v.u_cap, ks.c2, c_cap,
+                                                        ks.knorm, v.n_cap, ks.cstat, 0x1p-13f, v.assign,
+                                                        gs0, S, ks.amb, ks.amb_count, (int32_t)amb_cap,
+                                                        v.err);
+    } else {
+      k_assign_simt<DT><<<dim3((unsigned)((n + kAsTile - 1) / kAsTile), S), kAsThreads, kAsSmem, st>>>(
+          keys, n, c, v.cent_op, v.u_cap, ks.c2, c_cap, ks.knorm, v.n_cap, ks.cstat, eps,
+          v.assign, gs0, ks.amb, ks.amb_count, (int32_t)amb_cap, v.err);
+    }
     prof.end(st);
     prof.begin(kPKmRefine, st);
     k_assign_refine<DT><<<304, 256, 0, st>>>(keys, n, c, v.cent_op, v.u_cap, v.assign, v.n_cap,
@@ -671,9 +1001,8 @@ static cudaError_t kmeans_build_t(const CtxView &v, int layer, const KmeansScrat
 cudaError_t launch_kmeans_build(const CtxView &v, int layer, const KmeansScratch &ks,
                                 const void *keys, const void *values, int64_t n, int32_t c,
                                 int32_t iters, bool use_tc, cudaStream_t stream, Prof &prof) {
-  (void)use_tc;
-  if (v.dtype == 1) return kmeans_build_t<1>(v, layer, ks, keys, values, n, c, iters, stream, prof);
-  return kmeans_build_t<0>(v, layer, ks, keys, values, n, c, iters, stream, prof);
+  if (v.dtype == 1) return kmeans_build_t<1>(v, layer, ks, keys, values, n, c, iters, use_tc, stream, prof);
+  return kmeans_build_t<0>(v, layer, ks, keys, values, n, c, iters, false, stream, prof);
 }
 
 // Teacher-forced index: centroids and assignment given.

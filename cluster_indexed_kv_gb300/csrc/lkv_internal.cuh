@@ -94,7 +94,7 @@ enum CounterId : int { kCntAttnRows = 0, kCntScoreUnits = 1, kCntGatherRows = 2,
 // Kernel kinds for launch counting and event timing.
 enum ProfKind : int {
   kPBoundary = 0, kPScore, kPGather, kPAttn,
-  kPKmInit, kPKmOperand, kPKmAssign, kPKmRefine, kPKmSort, kPKmUpdate, kPKmPool,
+  kPKmInit, kPKmOperand, kPKmAssign, kPKmRefine, kPKmSort, kPKmUpdate, kPKmPool, kPKmAssignTc,
   kPNum
 };
 

@@ -175,6 +175,17 @@ lkv_status lkv_decode_steps(lkv_ctx *ctx, int32_t layer, int32_t n_layers,
                             int32_t local_buf, float *out, int32_t *selected_units,
                             int32_t *n_selected, uint8_t *boundary, float *r_out);
 
+/* Which kernel screens the K-means distances before the exact settlement.
+ * LKV_FILTER_TENSOR (the default): tcgen05 tensor-core tiles, used for bf16
+ * keys; fp32 keys always take the SIMT filter. LKV_FILTER_SIMT: the fp32
+ * FMA filter for every dtype. Both certify their decisions against the exact
+ * double-precision distance ("LouisKV ... Long Input-Output Sequences",
+ * 关键设计 2: keys go to their nearest centroid), so the assignment and the
+ * centroids do not depend on the choice; only the speed does.
+ * Errors: LKV_EINVAL (null context or unknown value). */
+enum { LKV_FILTER_TENSOR = 0, LKV_FILTER_SIMT = 1 };
+lkv_status lkv_set_kmeans_filter(lkv_ctx *ctx, int32_t filter);
+
 /* Per-kernel launch counts (always kept) and CUDA-event durations (kept while
  * profiling is enabled: each launch is bracketed by events on the context
  * stream). */

@@ -62,6 +62,7 @@ def test_null_arguments_are_rejected(libpath):
     assert L.lkv_build_index(None, 0, None, None, 1, 1, 1, 0) == _lib.LKV_EINVAL
     assert L.lkv_decode_step(None, 0, 1, None, None, None, 0.7, 1, 1, None, None, None, None,
                              None) == _lib.LKV_EINVAL
+    assert L.lkv_set_kmeans_filter(None, _lib.LKV_FILTER_SIMT) == _lib.LKV_EINVAL
 
 
 def test_binding_fails_loudly_without_library(tmp_path):
