@@ -211,13 +211,14 @@ lkv_status lkv_create(const lkv_config *cfg, lkv_ctx **out) {
 
   KmeansScratch &ks = c->ks;
   ks.knorm = (float *)dalloc(c, S * n_cap * 4, &st);
-  ks.c2 = (float *)dalloc(c, S * c_cap * 4, &st);
+  ks.c2_pitch = (c_cap + 255) / 256 * 256;
+  ks.c2 = (float *)dalloc(c, S * ks.c2_pitch * 4, &st);
   ks.cstat = (float *)dalloc(c, S * 2 * 4, &st);
   ks.cnt_part = (int32_t *)dalloc(c, S * lkv::kMaxParts * c_cap * 4, &st);
   ks.count = (int32_t *)dalloc(c, S * c_cap * 4, &st);
   ks.offs = (int32_t *)dalloc(c, S * c_cap * 4, &st);
   ks.amb = (int4 *)dalloc(c, S * n_cap * sizeof(int4), &st);
-  ks.amb_count = (int32_t *)dalloc(c, 4, &st);
+  ks.amb_count = (int32_t *)dalloc(c, 8, &st);  // front and back ends of the queue
   ks.n_refined = (int64_t *)dalloc(c, 8, &st);
   ks.n_inexact = (int64_t *)dalloc(c, 8, &st);
   ks.init_idx = (int64_t *)dalloc(c, S * c_cap * 8, &st);

@@ -63,12 +63,15 @@ __global__ void k_key_norms(const void *keys, int64_t n, int64_t n_cap, float *k
 // keys), its squared norm in fp32, and per-slice maxima of |c| and |c|^2.
 template <int DT>
 __global__ void k_prepare_operand(const float *cent32, void *cent_op, int32_t c,
-                                  int32_t c_cap, int32_t u_cap, int64_t gs0,
+                                  int32_t c_pad, int32_t c2_pitch, int32_t u_cap, int64_t gs0,
                                   float *c2, float *cstat) {
   const int s = blockIdx.y;
   const int lane = threadIdx.x & 31;
   const int j = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
-  if (j >= c) return;
+  if (j >= c) {  // padding of the |c|^2 table up to c_pad: +inf never wins
+    if (j < c_pad && lane == 0) c2[(int64_t)s * c2_pitch + j] = INFINITY;
+    return;
+  }
   const int64_t base = ((gs0 + s) * u_cap + j) * kHeadDim;
   float acc = 0.f;
 #pragma unroll
@@ -87,7 +90,7 @@ __global__ void k_prepare_operand(const float *cent32, void *cent_op, int32_t c,
 #pragma unroll
   for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
   if (lane == 0) {
-    c2[(int64_t)s * c_cap + j] = acc;
+    c2[(int64_t)s * c2_pitch + j] = acc;
     // non-negative floats order like their bit patterns
     atomicMax((unsigned *)&cstat[2 * s], __float_as_uint(sqrtf(acc)));
     atomicMax((unsigned *)&cstat[2 * s + 1], __float_as_uint(acc));
@@ -154,22 +157,26 @@ __device__ __forceinline__ Top3 top3_shfl(const Top3 &t, int lanemask) {
 }
 
 // Decision for one key from its filtered top-3: write the certain argmin, or
-// queue the key for the exact double-precision comparison.
+// queue the key for the exact double-precision comparison. Keys with two
+// candidates fill the queue from the front (amb_count), keys with three or
+// more from the back (amb_crowd); each key queues at most once and the queue
+// holds one entry per key, so the two ends never meet.
 __device__ __forceinline__ void assign_decide(const Top3 &t, int32_t c, float kn,
                                               float cmax, float c2max, float eps,
                                               int32_t s, int64_t row, int32_t *assign_row,
                                               int4 *amb, int32_t *amb_count,
-                                              int32_t amb_cap, int32_t *err) {
+                                              int32_t *amb_crowd, int32_t amb_cap,
+                                              int32_t *err) {
   const float beta2 = 2.f * eps * (kn * cmax + c2max);
   // (non-finite keys or centroids leave the filter without a candidate: the
   // id written stays in range and the key goes to the full exact scan)
   const bool valid = t.j1 < c && (c == 1 || t.j2 < c);
   *assign_row = t.j1 < c ? t.j1 : 0;
   if (c == 1 || (valid && t.v2 - t.v1 > beta2)) return;
-  const int crowded = !valid || ((c > 2) && !(t.v3 - t.v1 > beta2));
-  const int slot = atomicAdd(amb_count, 1);
+  const bool crowded = !valid || ((c > 2) && !(t.v3 - t.v1 > beta2));
+  const int slot = atomicAdd(crowded ? amb_crowd : amb_count, 1);
   if (slot < amb_cap)
-    amb[slot] = make_int4(s, (int)row, t.j1, (int)((unsigned)t.j2 | ((unsigned)crowded << 31)));
+    amb[crowded ? amb_cap - 1 - slot : slot] = make_int4(s, (int)row, t.j1, t.j2);
   else
     set_err(err, kErrCapacity);
 }
@@ -186,7 +193,7 @@ __global__ void __launch_bounds__(kAsThreads)
 k_assign_simt(const void *keys, int64_t n, int32_t c, const void *cent_op,
               int32_t u_cap, const float *c2, int32_t c_cap, const float *knorm,
               int64_t n_cap, const float *cstat, float eps, int32_t *assign,
-              int64_t gs0, int4 *amb, int32_t *amb_count, int32_t amb_cap,
+              int64_t gs0, int4 *amb, int32_t *amb_count, int32_t *amb_crowd, int32_t amb_cap,
               int32_t *err) {
   extern __shared__ float sm[];
   float *Ks = sm;                               // [128][64] key tile, transposed
@@ -303,7 +310,7 @@ k_assign_simt(const void *keys, int64_t n, int32_t c, const void *cent_op,
   const int64_t i = row0 + my_r;
   if (my_p == 0 && i < n) {
     assign_decide(top, c, kns[my_r], cstat[2 * s], cstat[2 * s + 1], eps, s, i,
-                  &assign[gs * n_cap + i], amb, amb_count, amb_cap, err);
+                  &assign[gs * n_cap + i], amb, amb_count, amb_crowd, amb_cap, err);
   }
 }
 
@@ -314,14 +321,15 @@ k_assign_simt(const void *keys, int64_t n, int32_t c, const void *cent_op,
 // k . c~ for all 128 x 256 pairs with tcgen05.mma (bf16 x bf16 -> fp32 in
 // TMEM, two accumulators so MMAs of chunk n+1 overlap the epilogue of chunk
 // n). Warp 0 issues the TMA loads (128B-swizzled K-major tiles), warp 1 the
-// MMAs and owns the tensor memory, warps 2..9 read the accumulators (two warps
-// per TMEM lane quadrant, one per half of the columns), form
+// MMAs and owns the tensor memory, warps 2..17 read the accumulators (four
+// warps per TMEM lane quadrant, one per 64-column quarter of a chunk), form
 // e_j = |c~_j|^2 - 2 k.c~_j and keep the three smallest per key; the same
 // certified decision as the SIMT filter follows (eps covers the tensor-core
 // fp32 accumulation error with a wide margin).
 constexpr int kTcM = 128;
 constexpr int kTcN = 256;
-constexpr int kTcWarps = 10;
+constexpr int kTcEpiWarps = 16;
+constexpr int kTcWarps = 2 + kTcEpiWarps;
 constexpr int kTcThreads = kTcWarps * 32;
 constexpr uint32_t kTcABytes = kTcM * kHeadDim * 2;  // 32 KB: two 64-column halves of 16 KB
 constexpr uint32_t kTcBBytes = kTcN * kHeadDim * 2;  // 64 KB: two halves of 32 KB
@@ -393,6 +401,15 @@ __device__ __forceinline__ void tc_commit(uint64_t *bar) {
 }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+// Two IEEE single-precision fused multiply-adds in one instruction.
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+      " mov.b64 rc, {%6, %7};\n fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}"
+      : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
@@ -407,16 +424,16 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 
 __global__ void __launch_bounds__(kTcThreads, 1)
 k_assign_tc(const __grid_constant__ CUtensorMap keys_map, const __grid_constant__ CUtensorMap cent_map,
-            int64_t n, int32_t c, int32_t u_cap, const float *c2, int32_t c_cap, const float *knorm,
+            int64_t n, int32_t c, int32_t u_cap, const float *c2, int32_t c2_pitch, const float *knorm,
             int64_t n_cap, const float *cstat, float eps, int32_t *assign, int64_t gs0, int n_slices,
-            int4 *amb, int32_t *amb_count, int32_t amb_cap, int32_t *err) {
+            int4 *amb, int32_t *amb_count, int32_t *amb_crowd, int32_t amb_cap, int32_t *err) {
   extern __shared__ unsigned char tc_smem_raw[];
   __shared__ __align__(8) uint64_t a_full[2], a_empty[2], b_full[2], b_empty[2], acc_full[2], acc_empty[2];
   __shared__ __align__(8) uint64_t mma_done;
   __shared__ uint32_t tmem_base_s;
   __shared__ volatile int abort_s;
-  __shared__ float xv[kTcM][3];
-  __shared__ int32_t xj[kTcM][2];
+  __shared__ float xv[3][kTcM][3];
+  __shared__ int32_t xj[3][kTcM][2];
   const uint32_t base = (smem_addr(tc_smem_raw) + 1023u) & ~1023u;
   const uint32_t A0 = base, B0 = base + 2 * kTcABytes;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -431,7 +448,7 @@ k_assign_tc(const __grid_constant__ CUtensorMap keys_map, const __grid_constant_
       tc_mbar_init(&b_full[i], 1);
       tc_mbar_init(&b_empty[i], 1);
       tc_mbar_init(&acc_full[i], 1);
-      tc_mbar_init(&acc_empty[i], 8);
+      tc_mbar_init(&acc_empty[i], kTcEpiWarps);
     }
     tc_mbar_init(&mma_done, 1);
     abort_s = 0;
@@ -508,9 +525,10 @@ k_assign_tc(const __grid_constant__ CUtensorMap keys_map, const __grid_constant_
       const uint64_t t0 = gtimer();
       while (!tc_try_wait(&mma_done, 0) && gtimer() - t0 < kTcWaitNs) {}
     }
-  } else {  // epilogue: warps 2..9
-    const int quad = warp & 3, half = warp >= 6 ? 1 : 0;
+  } else {  // epilogue: warps 2..17
+    const int quad = warp & 3, qtr = (warp - 2) >> 2;
     const int row = quad * 32 + lane;
+    const uint32_t tbase = tmem + ((uint32_t)(quad * 32) << 16) + qtr * 64;
     int gc = 0;
     for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
       const int sl = item / tiles;
@@ -519,49 +537,61 @@ k_assign_tc(const __grid_constant__ CUtensorMap keys_map, const __grid_constant_
       Top3 top;
       top.v1 = top.v2 = top.v3 = INFINITY;
       top.j1 = top.j2 = 0x7fffffff;
-      const float *c2s = c2 + (int64_t)sl * c_cap;
+      const float4 *c2s = (const float4 *)(c2 + (int64_t)sl * c2_pitch + qtr * 64);
       for (int ch = 0; ch < nch; ++ch, ++gc) {
         const int ti = gc & 1;
-        if (!abort_s) tc_wait(&acc_full[ti], (gc >> 1) & 1, &abort_s);
-        __syncwarp();
-        tc_fence_after();
 #pragma unroll 1
-        for (int g = 0; g < 4; ++g) {
-          const int col = half * 128 + g * 32;
-          const int j0 = ch * kTcN + col;
+        for (int g = 0; g < 2; ++g) {
+          // |c|^2 of the 32 columns (padded with +inf past the last cluster),
+          // requested before the accumulator wait so the two latencies overlap
+          float4 cc[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) cc[e] = __ldg(c2s + ch * (kTcN / 4) + g * 8 + e);
+          if (g == 0) {
+            if (!abort_s) tc_wait(&acc_full[ti], (gc >> 1) & 1, &abort_s);
+            __syncwarp();
+            tc_fence_after();
+          }
           uint32_t r[32];
-          tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + ti * kTcN + col, r);
-          if (j0 + 32 <= c) {
+          tmem_ld32(tbase + ti * kTcN + g * 32, r);
+          const int j0 = ch * kTcN + qtr * 64 + g * 32;
 #pragma unroll
-            for (int e = 0; e < 32; ++e)
-              top3_push(top, fmaf(-2.f, __uint_as_float(r[e]), __ldg(c2s + j0 + e)), j0 + e);
-          } else {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              const int j = j0 + e;
-              if (j < c) top3_push(top, fmaf(-2.f, __uint_as_float(r[e]), __ldg(c2s + j)), j);
-            }
+          for (int e = 0; e < 8; ++e) {
+            const float2 lo = fma2(make_float2(-2.f, -2.f),
+                                   make_float2(__uint_as_float(r[4 * e]), __uint_as_float(r[4 * e + 1])),
+                                   make_float2(cc[e].x, cc[e].y));
+            const float2 hi = fma2(make_float2(-2.f, -2.f),
+                                   make_float2(__uint_as_float(r[4 * e + 2]), __uint_as_float(r[4 * e + 3])),
+                                   make_float2(cc[e].z, cc[e].w));
+            top3_push(top, lo.x, j0 + 4 * e);
+            top3_push(top, lo.y, j0 + 4 * e + 1);
+            top3_push(top, hi.x, j0 + 4 * e + 2);
+            top3_push(top, hi.y, j0 + 4 * e + 3);
           }
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) tc_arrive(&acc_empty[ti]);
       }
-      // merge the two column halves of each key, then decide
-      if (half == 1) {
-        xv[row][0] = top.v1; xv[row][1] = top.v2; xv[row][2] = top.v3;
-        xj[row][0] = top.j1; xj[row][1] = top.j2;
+      // merge the four column quarters of each key, then decide
+      if (qtr > 0) {
+        xv[qtr - 1][row][0] = top.v1; xv[qtr - 1][row][1] = top.v2; xv[qtr - 1][row][2] = top.v3;
+        xj[qtr - 1][row][0] = top.j1; xj[qtr - 1][row][1] = top.j2;
       }
-      asm volatile("bar.sync 1, 256;" ::: "memory");
-      if (half == 0 && i < n) {
-        Top3 o;
-        o.v1 = xv[row][0]; o.v2 = xv[row][1]; o.v3 = xv[row][2];
-        o.j1 = xj[row][0]; o.j2 = xj[row][1];
-        const Top3 m = top3_merge(top, o);
+      asm volatile("bar.sync 1, %0;" ::"n"(kTcEpiWarps * 32) : "memory");
+      if (qtr == 0 && i < n) {
+        Top3 m = top;
+#pragma unroll
+        for (int q = 0; q < 3; ++q) {
+          Top3 o;
+          o.v1 = xv[q][row][0]; o.v2 = xv[q][row][1]; o.v3 = xv[q][row][2];
+          o.j1 = xj[q][row][0]; o.j2 = xj[q][row][1];
+          m = top3_merge(m, o);
+        }
         assign_decide(m, c, kn, cstat[2 * sl], cstat[2 * sl + 1], eps, sl, i,
-                      &assign[(gs0 + sl) * n_cap + i], amb, amb_count, amb_cap, err);
+                      &assign[(gs0 + sl) * n_cap + i], amb, amb_count, amb_crowd, amb_cap, err);
       }
-      asm volatile("bar.sync 1, 256;" ::: "memory");
+      asm volatile("bar.sync 1, %0;" ::"n"(kTcEpiWarps * 32) : "memory");
     }
   }
   tc_fence_before();
@@ -615,12 +645,60 @@ __device__ __forceinline__ double sqdist64(const void *key_row, const void *cent
   return acc;
 }
 
+// Single-precision squared distances of one key to centroids j0..j0+31 by a
+// warp: lane l holds key dimensions 4l..4l+3, forms its partial sums for all
+// 32 centroids, and a butterfly transpose-reduction leaves centroid j0 + l's
+// total in lane l (+inf past the last centroid).
 template <int DT>
-__global__ void k_assign_refine(const void *keys, int64_t n, int32_t c,
-                                const void *cent_op, int32_t u_cap, int32_t *assign,
-                                int64_t n_cap, int64_t gs0, const int4 *amb,
-                                const int32_t *amb_count, int32_t amb_cap,
-                                int64_t *n_refined) {
+__device__ __forceinline__ float scan32(const float (&k4)[4], const char *cb, int j0, int c,
+                                        int lane) {
+  constexpr int eb = DT == 1 ? 2 : 4;
+  float v[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const int j = j0 + i;
+    if (j < c) {
+      const char *row = cb + ((int64_t)j * kHeadDim + lane * 4) * eb;
+      float cv[4];
+      if constexpr (DT == 1) {
+        const uint2 u = __ldg((const uint2 *)row);
+        cv[0] = __uint_as_float(u.x << 16); cv[1] = __uint_as_float(u.x & 0xffff0000u);
+        cv[2] = __uint_as_float(u.y << 16); cv[3] = __uint_as_float(u.y & 0xffff0000u);
+      } else {
+        const float4 f = __ldg((const float4 *)row);
+        cv[0] = f.x; cv[1] = f.y; cv[2] = f.z; cv[3] = f.w;
+      }
+      float acc = 0.f;
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const float d = k4[t] - cv[t];
+        acc = fmaf(d, d, acc);
+      }
+      v[i] = acc;
+    } else {
+      v[i] = INFINITY;
+    }
+  }
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    const bool upper = lane & off;
+#pragma unroll
+    for (int i = 0; i < off; ++i) {
+      const float send = upper ? v[i] : v[i + off];
+      const float keep = upper ? v[i + off] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+    }
+  }
+  return v[0];
+}
+
+// Keys with two candidates: a warp per queue entry, the two exact distances
+// computed by lanes 0 and 1 (each sequentially over the dimensions, the
+// oracle's order), the smaller wins, the lower id on a tie.
+template <int DT>
+__global__ void k_refine_pairs(const void *keys, int64_t n, const void *cent_op, int32_t u_cap,
+                               int32_t *assign, int64_t n_cap, int64_t gs0, const int4 *amb,
+                               const int32_t *amb_count, int32_t amb_cap, int64_t *n_refined) {
   const int lane = threadIdx.x & 31;
   const int warps = gridDim.x * (blockDim.x / 32);
   const int w0 = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
@@ -629,24 +707,75 @@ __global__ void k_assign_refine(const void *keys, int64_t n, int32_t c,
   const int eb = elem_bytes<DT>();
   for (int w = w0; w < total; w += warps) {
     const int4 e = amb[w];
-    const int s = e.x;
+    const int64_t gs = gs0 + e.x;
     const int64_t row = e.y;
-    const int32_t j1 = e.z, j2 = e.w & 0x7fffffff;
-    const bool crowded = (unsigned)e.w >> 31;
-    const int64_t gs = gs0 + s;
-    const char *key_row = (const char *)keys + ((int64_t)s * n + row) * kHeadDim * eb;
-    const char *cb = (const char *)cent_op + gs * u_cap * (int64_t)kHeadDim * eb;
     double best = INFINITY;
     int32_t bj = 0x7fffffff;
-    if (!crowded) {
-      if (lane < 2) {
-        bj = lane == 0 ? j1 : j2;
-        best = sqdist64<DT>(key_row, cb + (int64_t)bj * kHeadDim * eb);
-      }
-    } else {
-      for (int j = lane; j < c; j += 32) {
-        const double dj = sqdist64<DT>(key_row, cb + (int64_t)j * kHeadDim * eb);
-        if (dj < best) { best = dj; bj = j; }  // ascending j: keeps lowest on ties
+    if (lane < 2) {
+      const char *key_row = (const char *)keys + ((int64_t)e.x * n + row) * kHeadDim * eb;
+      const char *cb = (const char *)cent_op + gs * u_cap * (int64_t)kHeadDim * eb;
+      bj = lane == 0 ? e.z : e.w;
+      best = sqdist64<DT>(key_row, cb + (int64_t)bj * kHeadDim * eb);
+    }
+    const double ob = __shfl_xor_sync(0xffffffffu, best, 1);
+    const int32_t oj = __shfl_xor_sync(0xffffffffu, bj, 1);
+    if (ob < best || (ob == best && oj < bj)) bj = oj;
+    if (lane == 0) assign[gs * n_cap + row] = bj;
+  }
+}
+
+// Keys with three or more candidates within the filter's margin: a CTA per
+// queue entry. A single-precision pass over all centroids (each warp a
+// stripe of 32-centroid blocks) bounds every squared distance D_j: each term
+// (k_i - c_i)^2 takes one rounding of the difference and one FMA, and a sum
+// of 128 non-negative terms in any order lies within 2^-16 * D_j of the true
+// value. The true argmin is therefore among the centroids whose
+// single-precision distance is within a factor 1 + 2^-13 of the smallest one
+// (plus 2^-100 for underflowing terms); only those get the exact distance.
+constexpr int kCrowdThreads = 256;
+
+template <int DT>
+__global__ void __launch_bounds__(kCrowdThreads)
+k_refine_crowded(const void *keys, int64_t n, int32_t c, const void *cent_op, int32_t u_cap,
+                 int32_t *assign, int64_t n_cap, int64_t gs0, const int4 *amb,
+                 const int32_t *amb_crowd, int32_t amb_cap, int64_t *n_refined) {
+  extern __shared__ float d32[];  // [c]
+  __shared__ float wmin[kCrowdThreads / 32];
+  __shared__ double wbest[kCrowdThreads / 32];
+  __shared__ int32_t wj[kCrowdThreads / 32];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  constexpr int nw = kCrowdThreads / 32;
+  const int total = min(*amb_crowd, amb_cap);
+  if (blockIdx.x == 0 && threadIdx.x == 0) atomicAdd((unsigned long long *)n_refined, (unsigned long long)total);
+  const int eb = elem_bytes<DT>();
+  for (int q = blockIdx.x; q < total; q += gridDim.x) {
+    const int4 e = amb[amb_cap - 1 - q];
+    const int64_t gs = gs0 + e.x;
+    const int64_t row = e.y;
+    const char *key_row = (const char *)keys + ((int64_t)e.x * n + row) * kHeadDim * eb;
+    const char *cb = (const char *)cent_op + gs * u_cap * (int64_t)kHeadDim * eb;
+    float k4[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) k4[t] = load_elem<DT>(key_row, lane * 4 + t);
+    float m = INFINITY;
+    for (int j0 = wid * 32; j0 < c; j0 += nw * 32) {
+      const float dj = scan32<DT>(k4, cb, j0, c, lane);
+      if (j0 + lane < c) d32[j0 + lane] = dj;
+      m = fminf(m, dj);
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) m = fminf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0) wmin[wid] = m;
+    __syncthreads();
+#pragma unroll
+    for (int w = 0; w < nw; ++w) m = fminf(m, wmin[w]);
+    const float thr = fmaf(m, 0x1p-13f, m) + 0x1p-100f;
+    double best = INFINITY;
+    int32_t bj = 0x7fffffff;
+    for (int j = threadIdx.x; j < c; j += kCrowdThreads) {
+      if (d32[j] <= thr) {
+        const double d64 = sqdist64<DT>(key_row, cb + (int64_t)j * kHeadDim * eb);
+        if (d64 < best) { best = d64; bj = j; }  // ascending j: keeps lowest on ties
       }
     }
 #pragma unroll
@@ -655,8 +784,27 @@ __global__ void k_assign_refine(const void *keys, int64_t n, int32_t c,
       const int32_t oj = __shfl_xor_sync(0xffffffffu, bj, o);
       if (ob < best || (ob == best && oj < bj)) { best = ob; bj = oj; }
     }
-    if (lane == 0) assign[gs * n_cap + row] = bj < c ? bj : 0;
+    if (lane == 0) { wbest[wid] = best; wj[wid] = bj; }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      for (int w = 1; w < nw; ++w)
+        if (wbest[w] < best || (wbest[w] == best && wj[w] < bj)) { best = wbest[w]; bj = wj[w]; }
+      assign[gs * n_cap + row] = bj < c ? bj : 0;  // (no finite distance: stays in range)
+    }
+    __syncthreads();
   }
+}
+
+// Both settlement kernels for one filter pass.
+template <int DT>
+static void launch_refine(const void *keys, int64_t n, int32_t c, const void *cent_op,
+                          int32_t u_cap, int32_t *assign, int64_t n_cap, int64_t gs0,
+                          const int4 *amb, const int32_t *amb_count, const int32_t *amb_crowd,
+                          int32_t amb_cap, int64_t *n_refined, cudaStream_t st) {
+  k_refine_pairs<DT><<<304, 256, 0, st>>>(keys, n, cent_op, u_cap, assign, n_cap, gs0, amb,
+                                          amb_count, amb_cap, n_refined);
+  k_refine_crowded<DT><<<608, kCrowdThreads, (size_t)c * sizeof(float), st>>>(
+      keys, n, c, cent_op, u_cap, assign, n_cap, gs0, amb, amb_crowd, amb_cap, n_refined);
 }
 
 // ---------------------------------------------------------------- stable counting sort
@@ -927,11 +1075,13 @@ static cudaError_t kmeans_build_t(const CtxView &v, int layer, const KmeansScrat
   const int S = v.B * v.Hkv;
   const int64_t gs0 = (int64_t)layer * S;
   const int c_cap = v.u_cap - v.t_cap;
+  const int c_pad = (c + kTcN - 1) / kTcN * kTcN;  // |c|^2 table padded with +inf
   const int64_t amb_cap = (int64_t)S * v.n_cap;
   static bool attr_done[2] = {false, false};
   if (!attr_done[DT]) {
     cudaFuncSetAttribute(k_assign_simt<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAsSmem);
     cudaFuncSetAttribute(k_assign_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmem);
+    cudaFuncSetAttribute(k_refine_crowded<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
     attr_done[DT] = true;
   }
   // tensor-core filter (bf16 keys): TMA descriptors of the keys and of the
@@ -961,26 +1111,25 @@ static cudaError_t kmeans_build_t(const CtxView &v, int layer, const KmeansScrat
   for (int it = 0; it < iters; ++it) {
     prof.begin(kPKmOperand, st);
     cudaMemsetAsync(ks.cstat, 0, sizeof(float) * 2 * S, st);
-    k_prepare_operand<DT><<<dim3((c + 7) / 8, S), 256, 0, st>>>(v.cent32, v.cent_op, c, c_cap,
+    k_prepare_operand<DT><<<dim3((c_pad + 7) / 8, S), 256, 0, st>>>(v.cent32, v.cent_op, c, c_pad, ks.c2_pitch,
                                                                v.u_cap, gs0, ks.c2, ks.cstat);
-    cudaMemsetAsync(ks.amb_count, 0, sizeof(int32_t), st);
+    cudaMemsetAsync(ks.amb_count, 0, 2 * sizeof(int32_t), st);  // both ends of the queue
     prof.end(st);
     prof.begin(use_tc ? kPKmAssignTc : kPKmAssign, st);
     if (use_tc) {
-      k_assign_tc<<<tc_grid, kTcThreads, kTcSmem, st>>>(keys_map, cent_map, n, c, v.u_cap, ks.c2, c_cap,
+      k_assign_tc<<<tc_grid, kTcThreads, kTcSmem, st>>>(keys_map, cent_map, n, c, v.u_cap, ks.c2, ks.c2_pitch,
                                                         ks.knorm, v.n_cap, ks.cstat, 0x1p-13f, v.assign,
-                                                        gs0, S, ks.amb, ks.amb_count, (int32_t)amb_cap,
-                                                        v.err);
+                                                        gs0, S, ks.amb, ks.amb_count, ks.amb_count + 1,
+                                                        (int32_t)amb_cap, v.err);
     } else {
       k_assign_simt<DT><<<dim3((unsigned)((n + kAsTile - 1) / kAsTile), S), kAsThreads, kAsSmem, st>>>(
-          keys, n, c, v.cent_op, v.u_cap, ks.c2, c_cap, ks.knorm, v.n_cap, ks.cstat, eps,
-          v.assign, gs0, ks.amb, ks.amb_count, (int32_t)amb_cap, v.err);
+          keys, n, c, v.cent_op, v.u_cap, ks.c2, ks.c2_pitch, ks.knorm, v.n_cap, ks.cstat, eps,
+          v.assign, gs0, ks.amb, ks.amb_count, ks.amb_count + 1, (int32_t)amb_cap, v.err);
     }
     prof.end(st);
     prof.begin(kPKmRefine, st);
-    k_assign_refine<DT><<<304, 256, 0, st>>>(keys, n, c, v.cent_op, v.u_cap, v.assign, v.n_cap,
-                                             gs0, ks.amb, ks.amb_count, (int32_t)amb_cap,
-                                             ks.n_refined);
+    launch_refine<DT>(keys, n, c, v.cent_op, v.u_cap, v.assign, v.n_cap, gs0, ks.amb, ks.amb_count,
+                      ks.amb_count + 1, (int32_t)amb_cap, ks.n_refined, st);
     prof.end(st);
     cudaError_t e = group_and_pool<DT>(v, layer, ks, n, c, gs0, S, st, prof);
     if (e != cudaSuccess) return e;
@@ -992,7 +1141,7 @@ static cudaError_t kmeans_build_t(const CtxView &v, int layer, const KmeansScrat
   }
   prof.begin(kPKmOperand, st);
   cudaMemsetAsync(ks.cstat, 0, sizeof(float) * 2 * S, st);
-  k_prepare_operand<DT><<<dim3((c + 7) / 8, S), 256, 0, st>>>(v.cent32, v.cent_op, c, c_cap,
+  k_prepare_operand<DT><<<dim3((c_pad + 7) / 8, S), 256, 0, st>>>(v.cent32, v.cent_op, c, c_pad, ks.c2_pitch,
                                                              v.u_cap, gs0, ks.c2, ks.cstat);
   prof.end(st);
   return finish_pool<DT>(v, layer, ks, keys, values, n, c, gs0, S, st, prof);
@@ -1030,11 +1179,11 @@ static cudaError_t load_index_t(const CtxView &v, int layer, const KmeansScratch
                                 Prof &prof) {
   const int S = v.B * v.Hkv;
   const int64_t gs0 = (int64_t)layer * S;
-  const int c_cap = v.u_cap - v.t_cap;
+  const int c_pad = (c + kTcN - 1) / kTcN * kTcN;
   k_copy_given<DT><<<dim3(64, S), 256, 0, st>>>(assign, cent, n, c, v.n_cap, v.u_cap, gs0,
                                                 v.assign, v.cent32, v.err);
   cudaMemsetAsync(ks.cstat, 0, sizeof(float) * 2 * S, st);
-  k_prepare_operand<DT><<<dim3((c + 7) / 8, S), 256, 0, st>>>(v.cent32, v.cent_op, c, c_cap,
+  k_prepare_operand<DT><<<dim3((c_pad + 7) / 8, S), 256, 0, st>>>(v.cent32, v.cent_op, c, c_pad, ks.c2_pitch,
                                                              v.u_cap, gs0, ks.c2, ks.cstat);
   cudaError_t e = group_and_pool<DT>(v, layer, ks, n, c, gs0, S, st, prof);
   if (e != cudaSuccess) return e;
@@ -1068,7 +1217,7 @@ constexpr size_t kSoCount = kSoCntPart + al256((size_t)kMaxParts * kStaticMaxClu
 constexpr size_t kSoOffs = kSoCount + al256(kStaticMaxClusters * 4);
 constexpr size_t kSoAmb = kSoOffs + al256(kStaticMaxClusters * 4);
 constexpr size_t kSoMisc = kSoAmb + al256(kStaticMaxTokens * sizeof(int4));
-constexpr size_t kSoInit = kSoMisc + 256;  // misc: amb_count, err (int32), n_refined, n_inexact (int64)
+constexpr size_t kSoInit = kSoMisc + 256;  // misc: amb_count, err (int32), n_refined, n_inexact (int64), amb_crowd (int32)
 constexpr size_t kSoShuffle = kSoInit + al256(kStaticMaxClusters * 8);
 constexpr size_t kSoCentOp = kSoShuffle + al256(kStaticMaxTokens * 8);
 constexpr size_t kSoPerm = kSoCentOp + al256((size_t)kStaticMaxClusters * kHeadDim * 4);
@@ -1121,12 +1270,14 @@ static cudaError_t kmeans_static_t(unsigned char *base, const void *keys, int64_
   KmeansScratch ks{};
   ks.knorm = (float *)(base + kSoKnorm);
   ks.c2 = (float *)(base + kSoC2);
+  ks.c2_pitch = c;
   ks.cstat = (float *)(base + kSoCstat);
   ks.cnt_part = (int32_t *)(base + kSoCntPart);
   ks.count = (int32_t *)(base + kSoCount);
   ks.offs = (int32_t *)(base + kSoOffs);
   ks.amb = (int4 *)(base + kSoAmb);
   ks.amb_count = (int32_t *)(base + kSoMisc);
+  int32_t *amb_crowd = (int32_t *)(base + kSoMisc + 24);
   ks.n_refined = (int64_t *)(base + kSoMisc + 8);
   ks.n_inexact = (int64_t *)(base + kSoMisc + 16);
   ks.init_idx = (int64_t *)(base + kSoInit);
@@ -1143,15 +1294,16 @@ static cudaError_t kmeans_static_t(unsigned char *base, const void *keys, int64_
   for (int it = 0; it < iters; ++it) {
     e = cudaMemsetAsync(ks.cstat, 0, sizeof(float) * 2, st);
     if (e != cudaSuccess) return e;
-    k_prepare_operand<DT><<<dim3((c + 7) / 8, 1), 256, 0, st>>>(v.cent32, v.cent_op, c, c, v.u_cap,
+    k_prepare_operand<DT><<<dim3((c + 7) / 8, 1), 256, 0, st>>>(v.cent32, v.cent_op, c, c, c, v.u_cap,
                                                               0, ks.c2, ks.cstat);
     e = cudaMemsetAsync(ks.amb_count, 0, sizeof(int32_t), st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(amb_crowd, 0, sizeof(int32_t), st);
     if (e != cudaSuccess) return e;
     k_assign_simt<DT><<<dim3((unsigned)((n + kAsTile - 1) / kAsTile), 1), kAsThreads, kAsSmem, st>>>(
         keys, n, c, v.cent_op, v.u_cap, ks.c2, c, ks.knorm, v.n_cap, ks.cstat, eps, v.assign, 0,
-        ks.amb, ks.amb_count, (int32_t)amb_cap, v.err);
-    k_assign_refine<DT><<<304, 256, 0, st>>>(keys, n, c, v.cent_op, v.u_cap, v.assign, v.n_cap, 0,
-                                             ks.amb, ks.amb_count, (int32_t)amb_cap, ks.n_refined);
+        ks.amb, ks.amb_count, amb_crowd, (int32_t)amb_cap, v.err);
+    launch_refine<DT>(keys, n, c, v.cent_op, v.u_cap, v.assign, v.n_cap, 0, ks.amb, ks.amb_count,
+                      amb_crowd, (int32_t)amb_cap, ks.n_refined, st);
     e = group_and_pool<DT>(v, 0, ks, n, c, 0, 1, st, quiet);
     if (e != cudaSuccess) return e;
     k_update<DT><<<dim3((c + 7) / 8, 1), 256, 0, st>>>(keys, n, v.n_cap, c, c, v.u_cap, 0, v.perm,

@@ -213,13 +213,14 @@ __device__ __forceinline__ void set_err(int32_t *err, int32_t bits) {
 
 struct KmeansScratch {
   float *knorm;        // [S][n_cap]
-  float *c2;           // [S][c_cap]
+  float *c2;           // [S][c2_pitch]: |c|^2 of the operand centroids
+  int32_t c2_pitch;    // c_cap rounded up to a multiple of 256
   float *cstat;        // [S][2]: max |c|, max |c|^2
   int32_t *cnt_part;   // [S][kMaxParts][c_cap] counts, then running offsets
   int32_t *count;      // [S][c_cap]
   int32_t *offs;       // [S][c_cap]
   int4 *amb;           // [S * n_cap] ambiguous assignments
-  int32_t *amb_count;  // [1]
+  int32_t *amb_count;  // [2]: two-candidate entries (front), crowded entries (back)
   int64_t *n_refined;  // [1] running total
   int64_t *n_inexact;  // [1] running total
   int64_t *init_idx;   // [S][c_cap]
