@@ -22,6 +22,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <cfloat>
 #include <mutex>
 #include <string>
 
@@ -68,8 +69,18 @@ __global__ void k_prepare_operand(const float *cent32, void *cent_op, int32_t c,
   const int s = blockIdx.y;
   const int lane = threadIdx.x & 31;
   const int j = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
-  if (j >= c) {  // padding of the |c|^2 table up to c_pad: +inf never wins
-    if (j < c_pad && lane == 0) c2[(int64_t)s * c2_pitch + j] = INFINITY;
+  if (j >= c) {
+    // padding up to c_pad for the tensor-core filter: |c|^2 = FLT_MAX (a
+    // finite value no distance reaches) and zero operand rows, so the padded
+    // columns of a chunk stay finite and never win
+    if (j < c_pad) {
+      if (lane == 0) c2[(int64_t)s * c2_pitch + j] = FLT_MAX;
+      if (j < u_cap) {
+        const int64_t base = ((gs0 + s) * u_cap + j) * kHeadDim;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) store_elem<DT>(cent_op, base + lane * 4 + e, 0.f);
+      }
+    }
     return;
   }
   const int64_t base = ((gs0 + s) * u_cap + j) * kHeadDim;
@@ -339,6 +350,10 @@ constexpr uint32_t kTcIdesc = (1u << 4)            // fp32 accumulator
                               | (1u << 10)         // B bf16
                               | ((uint32_t)(kTcN >> 3) << 17) | ((uint32_t)(kTcM >> 4) << 24);
 constexpr uint64_t kTcWaitNs = 2000000000ull;
+// Filter margin: 2^-13 bounds the tensor-core fp32 accumulation error of a
+// 128-term bf16 dot product with a wide safety factor; 2^-16 covers the
+// column id carried in the low mantissa bits of each value.
+constexpr float kTcEps = 0x1p-13f + 0x1p-16f;
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -380,6 +395,12 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
       ::"r"(dst), "l"((uint64_t)map), "r"(x), "r"(y), "r"(smem_addr(bar)) : "memory");
 }
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int x, int y, int z,
+                                            uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+      ::"r"(dst), "l"((uint64_t)map), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar)) : "memory");
+}
 // Shared-memory matrix descriptor of a K-major bf16 tile written by TMA with
 // 128-byte swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart.
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
@@ -408,6 +429,46 @@ __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
       " mov.b64 rc, {%6, %7};\n fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}"
       : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
   return d;
+}
+
+// Branch-free candidate tracking for the tensor-core filter. A value carries
+// its column's position among the thread's 64 columns of a chunk in the low
+// six mantissa bits (a relative change below 2^-17, covered by the filter's
+// margin), so the three smallest values keep their columns without separate
+// index bookkeeping.
+__device__ __forceinline__ float pack6(float e, uint32_t local) {
+  return __uint_as_float((__float_as_uint(e) & 0xFFFFFFC0u) | local);
+}
+__device__ __forceinline__ float min3f(float a, float b, float c) {
+  float d;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+// Sorted (c1 <= c2 <= c3) absorbs the pair {q, r}. Merging the sorted pairs
+// (c1, c2) and (m, M) = (min, max)(q, r) is Batcher's 2 x 2 merge: the
+// smallest is min(c1, m) and the middle two are u = max(c1, m) and
+// v = min(c2, M) in either order; c3 caps the third.
+__device__ __forceinline__ void top3_pair(float &c1, float &c2, float &c3, float q, float r) {
+  const float m = fminf(q, r), M = fmaxf(q, r);
+  const float u = fmaxf(c1, m), v = fminf(c2, M);
+  c1 = fminf(c1, m);
+  c2 = fminf(u, v);
+  c3 = fminf(c3, fmaxf(u, v));
+}
+// Merge of two candidate lists with explicit column ids.
+__device__ __forceinline__ Top3 top3_union(const Top3 &a, const Top3 &b) {
+  Top3 r;
+  const bool bw = b.v1 < a.v1;
+  r.v1 = bw ? b.v1 : a.v1;
+  r.j1 = bw ? b.j1 : a.j1;
+  float x = bw ? a.v1 : b.v1;
+  int32_t jx = bw ? a.j1 : b.j1;
+  if (a.v2 < x) { x = a.v2; jx = a.j2; }
+  if (b.v2 < x) { x = b.v2; jx = b.j2; }
+  r.v2 = x;
+  r.j2 = jx;
+  r.v3 = min3f(a.v3, b.v3, fminf(fmaxf(a.v1, b.v2), fmaxf(a.v2, b.v1)));
+  return r;
 }
 
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
@@ -482,9 +543,10 @@ k_assign_tc(const __grid_constant__ CUtensorMap keys_map, const __grid_constant_
           const int bi = gc & 1;
           if (!tc_wait(&b_empty[bi], ((gc >> 1) & 1) ^ 1, &abort_s)) break;
           tc_expect_tx(&b_full[bi], kTcBBytes);
-          const int yb = (int)((gs0 + sl) * u_cap + (int64_t)ch * kTcN);
-          tma_load_2d(B0 + bi * kTcBBytes, &cent_map, 0, yb, &b_full[bi]);
-          tma_load_2d(B0 + bi * kTcBBytes + kTcBBytes / 2, &cent_map, 64, yb, &b_full[bi]);
+          // rows past the slice's table read as zeros
+          const int zb = (int)(gs0 + sl);
+          tma_load_3d(B0 + bi * kTcBBytes, &cent_map, 0, ch * kTcN, zb, &b_full[bi]);
+          tma_load_3d(B0 + bi * kTcBBytes + kTcBBytes / 2, &cent_map, 64, ch * kTcN, zb, &b_full[bi]);
           b_last[bi] = gc;
         }
       }
@@ -540,10 +602,11 @@ k_assign_tc(const __grid_constant__ CUtensorMap keys_map, const __grid_constant_
       const float4 *c2s = (const float4 *)(c2 + (int64_t)sl * c2_pitch + qtr * 64);
       for (int ch = 0; ch < nch; ++ch, ++gc) {
         const int ti = gc & 1;
-#pragma unroll 1
+        float p1 = INFINITY, p2 = INFINITY, p3 = INFINITY;  // this chunk's 64 columns
+#pragma unroll
         for (int g = 0; g < 2; ++g) {
-          // |c|^2 of the 32 columns (padded with +inf past the last cluster),
-          // requested before the accumulator wait so the two latencies overlap
+          // |c|^2 of the 32 columns (FLT_MAX past the last cluster), requested
+          // before the accumulator wait so the two latencies overlap
           float4 cc[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) cc[e] = __ldg(c2s + ch * (kTcN / 4) + g * 8 + e);
@@ -554,7 +617,6 @@ k_assign_tc(const __grid_constant__ CUtensorMap keys_map, const __grid_constant_
           }
           uint32_t r[32];
           tmem_ld32(tbase + ti * kTcN + g * 32, r);
-          const int j0 = ch * kTcN + qtr * 64 + g * 32;
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const float2 lo = fma2(make_float2(-2.f, -2.f),
@@ -563,15 +625,21 @@ k_assign_tc(const __grid_constant__ CUtensorMap keys_map, const __grid_constant_
             const float2 hi = fma2(make_float2(-2.f, -2.f),
                                    make_float2(__uint_as_float(r[4 * e + 2]), __uint_as_float(r[4 * e + 3])),
                                    make_float2(cc[e].z, cc[e].w));
-            top3_push(top, lo.x, j0 + 4 * e);
-            top3_push(top, lo.y, j0 + 4 * e + 1);
-            top3_push(top, hi.x, j0 + 4 * e + 2);
-            top3_push(top, hi.y, j0 + 4 * e + 3);
+            const uint32_t l0 = g * 32 + 4 * e;
+            top3_pair(p1, p2, p3, pack6(lo.x, l0), pack6(lo.y, l0 + 1));
+            top3_pair(p1, p2, p3, pack6(hi.x, l0 + 2), pack6(hi.y, l0 + 3));
           }
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) tc_arrive(&acc_empty[ti]);
+        // fold the chunk's three into the running list with column ids
+        const int jb = ch * kTcN + qtr * 64;
+        Top3 cur;
+        cur.v1 = p1; cur.v2 = p2; cur.v3 = p3;
+        cur.j1 = p1 < INFINITY ? jb + (int)(__float_as_uint(p1) & 63u) : 0x7fffffff;
+        cur.j2 = p2 < INFINITY ? jb + (int)(__float_as_uint(p2) & 63u) : 0x7fffffff;
+        top = top3_union(top, cur);
       }
       // merge the four column quarters of each key, then decide
       if (qtr > 0) {
@@ -586,7 +654,7 @@ k_assign_tc(const __grid_constant__ CUtensorMap keys_map, const __grid_constant_
           Top3 o;
           o.v1 = xv[q][row][0]; o.v2 = xv[q][row][1]; o.v3 = xv[q][row][2];
           o.j1 = xj[q][row][0]; o.j2 = xj[q][row][1];
-          m = top3_merge(m, o);
+          m = top3_union(m, o);
         }
         assign_decide(m, c, kn, cstat[2 * sl], cstat[2 * sl + 1], eps, sl, i,
                       &assign[(gs0 + sl) * n_cap + i], amb, amb_count, amb_crowd, amb_cap, err);
@@ -619,18 +687,20 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// 2-D bf16 tensor map over `rows` rows of 128 elements, boxes of 64 x box_rows
-// with 128-byte swizzle (out-of-range rows read as zeros).
-static bool make_map(CUtensorMap *map, const void *base, uint64_t rows, uint32_t box_rows) {
+// bf16 tensor map over `slices` tables of `rows` rows of 128 elements
+// (slices == 0: one 2-D table), boxes of 64 x box_rows with 128-byte swizzle;
+// rows outside a table read as zeros.
+static bool make_map(CUtensorMap *map, const void *base, uint64_t rows, uint32_t box_rows,
+                     uint64_t slices = 0) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (!enc) return false;
-  const cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)kHeadDim * 2};
-  const cuuint32_t box[2] = {64, box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  const cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)rows, (cuuint64_t)slices};
+  const cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)kHeadDim * 2 * rows};
+  const cuuint32_t box[3] = {64, box_rows, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, slices ? 3 : 2, const_cast<void *>(base), dims,
+             strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Exact settlement of the queued keys: warp per entry.
@@ -1089,9 +1159,8 @@ static cudaError_t kmeans_build_t(const CtxView &v, int layer, const KmeansScrat
   CUtensorMap keys_map, cent_map;
   int tc_grid = 0;
   if (DT == 1 && use_tc) {
-    const uint64_t op_rows = (uint64_t)v.u_cap * (uint64_t)(gs0 + S);
     if (!make_map(&keys_map, keys, (uint64_t)S * (uint64_t)n, kTcM) ||
-        !make_map(&cent_map, v.cent_op, op_rows, kTcN)) {
+        !make_map(&cent_map, v.cent_op, (uint64_t)v.u_cap, kTcN, (uint64_t)(gs0 + S))) {
       use_tc = false;
     } else {
       int dev = 0, sms = 0;
@@ -1118,7 +1187,7 @@ static cudaError_t kmeans_build_t(const CtxView &v, int layer, const KmeansScrat
     prof.begin(use_tc ? kPKmAssignTc : kPKmAssign, st);
     if (use_tc) {
       k_assign_tc<<<tc_grid, kTcThreads, kTcSmem, st>>>(keys_map, cent_map, n, c, v.u_cap, ks.c2, ks.c2_pitch,
-                                                        ks.knorm, v.n_cap, ks.cstat, 0x1p-13f, v.assign,
+                                                        ks.knorm, v.n_cap, ks.cstat, kTcEps, v.assign,
                                                         gs0, S, ks.amb, ks.amb_count, ks.amb_count + 1,
                                                         (int32_t)amb_cap, v.err);
     } else {
