@@ -182,12 +182,30 @@ def cpu_baseline(K, V, idx0, q, kn, vn, w, n_steps=48, kmeans_keys=1024):
 # ---------------------------------------------------------------- our arm
 
 def peaks():
+    """(HBM GB/s, bf16 TFLOP/s burst, bf16 TFLOP/s sustained, source)."""
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             p = json.load(f)
-        return float(p["hbm_gbs"]), "measured"
+        return (float(p["hbm_gbs"]), float(p["bf16_tflops"]),
+                float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), "measured")
     except Exception:
-        return 6800.0, "fallback"
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def ncu_traffic(kernel, units):
+    """DRAM bytes per launch from the committed ncu summary, scaled to
+    `units` (the launch's work units) when the capture ran a smaller case;
+    None when the kernel's source changed after the capture."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "ncu_traffic.txt")) as f:
+            rec = json.load(f)[kernel]
+        with open(os.path.join(ROOT, rec["source"]), "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != rec["source_sha256"]:
+                return None
+        return rec["dram_bytes_per_launch"] * units / rec["units_per_launch"]
+    except Exception:
+        return None
 
 
 def run_ours(args, rank, world, local):
@@ -267,7 +285,7 @@ def run_ours(args, rank, world, local):
         ctx.decode_step(0, q[t], kn[t], vn[t], w.tau, w.budget, out[t], boundary=bnd[t])
     kern_p, ctr = ctx.profile(reset=True)
     ctx.set_profiling(False)
-    hbm_peak, peak_kind = peaks()
+    hbm_peak, tc_peak, tc_peak_sus, peak_kind = peaks()
     n_attn, ms_attn = kern_p["lkv_attn"]
     slices = ctr["attn_slices"]
     eb = 2 if w.dtype == "bf16" else 4
@@ -276,6 +294,24 @@ def run_ours(args, rank, world, local):
     achieved = alg_bytes / attn_s / 1e9
     breakdown = {k: {"launches": int(v[0]), "avg_us": round(v[1] / v[0] * 1e3, 2)}
                  for k, v in kern_p.items() if v[0]}
+
+    # ---- K-means distance contraction on the tensor cores: one build with
+    # CUDA events around every kernel (L2 overwritten first; the keys, 537 MB,
+    # exceed L2 anyway)
+    flush.fill_(-1.0)
+    ctx.set_profiling(True)
+    ctx.profile(reset=True)
+    ctx.build_index(0, K, V, w.n_clusters, w.iters, 1)
+    kern_b, _ = ctx.profile(reset=True)
+    ctx.set_profiling(False)
+    S = w.batch * w.n_kv_heads
+    km_kernel = "kmeans_assign_tc" if kern_b.get("kmeans_assign_tc", (0, 0))[0] else "kmeans_assign"
+    n_km, ms_km = kern_b[km_kernel]
+    km_flops = 2.0 * S * w.n_prefill * w.n_clusters * 128
+    km_s = ms_km / max(n_km, 1) / 1e3
+    km_tf = km_flops / km_s / 1e12
+    build_breakdown = {k: {"launches": int(v[0]), "avg_us": round(v[1] / v[0] * 1e3, 2)}
+                       for k, v in kern_b.items() if v[0]}
 
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K_steps,
@@ -287,11 +323,20 @@ def run_ours(args, rank, world, local):
         "decode_ms_per_bench_step": dec_ms / K_steps, "build_ms_per_bench_step": build_ms / K_steps,
         "trigger_rate": trig, "kmeans_refined_keys_total": st["n_refined"],
         "roofline": {"kernel": "lkv_attn", "bound": "hbm", "achieved": achieved, "peak": hbm_peak,
-                     "unit": "GB/s", "frac": achieved / hbm_peak, "traffic": None,
+                     "unit": "GB/s", "frac": achieved / hbm_peak,
+                     "traffic": ncu_traffic("lkv_attn", ctr["attn_rows"] / max(n_attn, 1)),
                      "peak_source": f"{peak_kind} hbm_gbs (burst copy)",
                      "alg_bytes_per_launch": alg_bytes, "avg_launch_us": attn_s * 1e6,
                      "launches": int(n_attn), "l2": "256 MB written before every step"},
+        "roofline_kmeans_assign": {
+            "kernel": "k_assign_tc" if km_kernel == "kmeans_assign_tc" else "k_assign_simt",
+            "bound": "tensor", "achieved": km_tf, "peak": tc_peak, "unit": "TFLOP/s",
+            "frac": km_tf / tc_peak, "frac_of_sustained": km_tf / tc_peak_sus,
+            "traffic": ncu_traffic("k_assign_tc", S) if km_kernel == "kmeans_assign_tc" else None,
+            "peak_source": f"{peak_kind} bf16_tflops (cuBLAS burst)",
+            "flops_per_launch": km_flops, "avg_launch_us": km_s * 1e6, "launches": int(n_km)},
         "kernel_breakdown_us": breakdown,
+        "build_breakdown_us": build_breakdown,
         "gpu_launches": launches,
         "clocks": clk,
     }

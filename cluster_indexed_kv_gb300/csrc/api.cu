@@ -25,6 +25,7 @@ struct lkv_ctx {
   KmeansScratch ks{};
   cudaStream_t stream = nullptr;
   cudaStream_t capture = nullptr;   // private stream for CUDA-graph capture
+  lkv::Pipe pipe{};                 // side streams and events of a pipelined capture
   lkv::Prof prof;
   std::vector<GraphEntry> graphs;
   std::vector<void *> dev;
@@ -97,6 +98,14 @@ static void free_all(lkv_ctx *c) {
   c->prof.release();
   if (c->capture) cudaStreamDestroy(c->capture);
   c->capture = nullptr;
+  for (int i = 0; i < 2; ++i) {
+    if (c->pipe.attn[i]) cudaStreamDestroy(c->pipe.attn[i]);
+    if (c->pipe.attn_done[i]) cudaEventDestroy(c->pipe.attn_done[i]);
+    c->pipe.attn[i] = nullptr;
+    c->pipe.attn_done[i] = nullptr;
+  }
+  if (c->pipe.sel_done) cudaEventDestroy(c->pipe.sel_done);
+  c->pipe.sel_done = nullptr;
   for (void *p : c->dev) cudaFree(p);
   for (void *p : c->host) cudaFreeHost(p);
   c->dev.clear();
@@ -164,6 +173,8 @@ lkv_status lkv_create(const lkv_config *cfg, lkv_ctx **out) {
   v.B = B; v.Hkv = Hkv; v.G = G; v.d = d; v.L = k.local_buf;
   v.n_cap = n_cap; v.t_cap = t_cap; v.u_cap = u_cap; v.bud_cap = k.max_budget;
   v.offload = k.offload ? 1 : 0;
+  v.S_all = S_all;
+  v.n_lb = (int32_t)LB;
   v.pool_rows = pool_rows;
   if (!k.offload) {
     v.pool_k = dalloc(c, S_all * pool_rows * d * es, &st);
@@ -179,8 +190,8 @@ lkv_status lkv_create(const lkv_config *cfg, lkv_ctx **out) {
     v.dec_k = dalloc(c, S_all * t_cap * d * es, &st);
     v.dec_v = dalloc(c, S_all * t_cap * d * es, &st);
     v.dec_rows = t_cap;
-    v.stage_k = dalloc(c, S_all * (int64_t)k.max_budget * d * es, &st);
-    v.stage_v = dalloc(c, S_all * (int64_t)k.max_budget * d * es, &st);
+    v.stage_k = dalloc(c, 2 * S_all * (int64_t)k.max_budget * d * es, &st);  // per plan slot
+    v.stage_v = dalloc(c, 2 * S_all * (int64_t)k.max_budget * d * es, &st);
   }
   v.cent_op = dalloc(c, S_all * u_cap * d * es, &st);
   v.cent32 = (float *)dalloc(c, S_all * u_cap * d * 4, &st);
@@ -190,22 +201,24 @@ lkv_status lkv_create(const lkv_config *cfg, lkv_ctx **out) {
   v.perm = (int32_t *)dalloc(c, S_all * n_cap * 4, &st);
   v.st = (DecState *)dalloc(c, LB * sizeof(DecState), &st);
   v.q_prev = dalloc(c, LB * H * d * es, &st);
-  v.q_attn = (float *)dalloc(c, LB * H * d * 4, &st);
+  v.q_attn = (float *)dalloc(c, 2 * LB * H * d * 4, &st);  // per step slot
+  v.aview = (int4 *)dalloc(c, 2 * LB * sizeof(int4), &st);
   v.segsum = (int64_t *)dalloc(c, S_all * d * 8, &st);
   v.scores = (float *)dalloc(c, S_all * u_cap * 4, &st);
-  v.sel = (int32_t *)dalloc(c, S_all * u_cap * 4, &st);
-  v.n_sel = (int32_t *)dalloc(c, S_all * 4, &st);
-  v.n_tok = (int32_t *)dalloc(c, S_all * 4, &st);
-  v.rng_row = (int32_t *)dalloc(c, S_all * u_cap * 4, &st);
-  v.rng_cum = (int32_t *)dalloc(c, S_all * (u_cap + 1) * 4, &st);
+  // the selection plan, one copy per plan slot
+  v.sel = (int32_t *)dalloc(c, 2 * S_all * u_cap * 4, &st);
+  v.n_sel = (int32_t *)dalloc(c, 2 * S_all * 4, &st);
+  v.n_tok = (int32_t *)dalloc(c, 2 * S_all * 4, &st);
+  v.rng_row = (int32_t *)dalloc(c, 2 * S_all * u_cap * 4, &st);
+  v.rng_cum = (int32_t *)dalloc(c, 2 * S_all * (u_cap + 1) * 4, &st);
   v.max_chunks = max_chunks;
   v.attn_count = (int32_t *)dalloc(c, S_all * 4, &st);
   v.score_count = (int32_t *)dalloc(c, S_all * 4, &st);
   v.max_pieces = u_cap + max_chunks;
   v.pieces = (int4 *)dalloc(c, S_all * (int64_t)v.max_pieces * sizeof(int4), &st);
   v.chunk_piece = (int32_t *)dalloc(c, S_all * (int64_t)(max_chunks + 1) * 4, &st);
-  v.chunk_pieces = (int4 *)dalloc(c, S_all * (int64_t)max_chunks * lkv::kAttnChunk * sizeof(int4), &st);
-  v.chunk_count = (int32_t *)dalloc(c, S_all * (int64_t)max_chunks * 4, &st);
+  v.chunk_pieces = (int4 *)dalloc(c, 2 * S_all * (int64_t)max_chunks * lkv::kAttnChunk * sizeof(int4), &st);
+  v.chunk_count = (int32_t *)dalloc(c, 2 * S_all * (int64_t)max_chunks * 4, &st);
   v.err = (int32_t *)dalloc(c, 4, &st);
   v.counters = (int64_t *)dalloc(c, lkv::kCounters * 8, &st);
 
@@ -237,6 +250,11 @@ lkv_status lkv_create(const lkv_config *cfg, lkv_ctx **out) {
   if (e == cudaSuccess) e = cudaMemsetAsync(ks.n_inexact, 0, 8, c->stream);
   if (e == cudaSuccess) e = cudaMemsetAsync(v.counters, 0, lkv::kCounters * 8, c->stream);
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&c->capture, cudaStreamNonBlocking);
+  for (int i = 0; i < 2; ++i) {
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&c->pipe.attn[i], cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->pipe.attn_done[i], cudaEventDisableTiming);
+  }
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->pipe.sel_done, cudaEventDisableTiming);
   if (e == cudaSuccess) e = lkv::prepare_kernels(k.dtype, k.group);
   if (e == cudaSuccess) e = cudaStreamSynchronize(c->stream);
   if (e != cudaSuccess) {
@@ -393,7 +411,17 @@ static cudaError_t step_graph(lkv_ctx *c, const lkv::StepArgs &a, int steps, cud
   cudaGraph_t graph = nullptr;
   cudaError_t e = cudaStreamBeginCapture(c->capture, cudaStreamCaptureModeThreadLocal);
   if (e != cudaSuccess) return e;
-  for (int i = 0; i < steps && e == cudaSuccess; ++i) e = lkv::launch_decode_step(c->v, a, c->capture, quiet);
+  // step i's attention overlaps step i + 1's boundary test and selection
+  // (step and plan slots keep their inputs apart)
+  lkv::Pipe pipe = c->pipe;
+  for (int i = 0; i < steps && e == cudaSuccess; ++i) {
+    lkv::StepArgs ai = a;
+    ai.slot = i & 1;
+    pipe.step = i;
+    e = lkv::launch_decode_step(c->v, ai, c->capture, quiet, &pipe);
+  }
+  for (int i = 0; i < 2 && i < steps && e == cudaSuccess; ++i)
+    e = cudaStreamWaitEvent(c->capture, c->pipe.attn_done[(steps - 1 - i) & 1], 0);
   cudaError_t e2 = cudaStreamEndCapture(c->capture, &graph);
   if (e == cudaSuccess) e = e2;
   cudaGraphExec_t exec = nullptr;

@@ -230,10 +230,12 @@ __global__ void __launch_bounds__(kBoundaryThreads) k_step_boundary(CtxView v, S
       r = __fdiv_rn(r, (float)H);
       st.r = r;
       st.flag = r < a.tau ? 1 : 0;
+      st.plan ^= st.flag;  // a retrieval writes its plan into the other slot
     }
   } else if (tid == 0) {
     st.r = 0.f;
     st.flag = 1;
+    st.plan ^= 1;
   }
   __syncthreads();
 
@@ -323,7 +325,8 @@ __global__ void __launch_bounds__(kBoundaryThreads) k_step_boundary(CtxView v, S
     const int head = y / (kHeadDim / per16), j0 = (y % (kHeadDim / per16)) * per16;
     const float *src = qsm + ((int64_t)H + head) * kQPitch + j0;
 #pragma unroll
-    for (int i = 0; i < per16; ++i) v.q_attn[(lb * H + head) * kHeadDim + j0 + i] = src[i] * qscale;
+    for (int i = 0; i < per16; ++i)
+      v.q_attn[(((int64_t)a.slot * v.n_lb + lb) * H + head) * kHeadDim + j0 + i] = src[i] * qscale;
     if constexpr (DT == 1) {
       uint4 o;
       uint32_t w[4];
@@ -342,6 +345,8 @@ __global__ void __launch_bounds__(kBoundaryThreads) k_step_boundary(CtxView v, S
     if (slow_any) st.seg_slow = 1;
     st.t = t + 1;
     v.st[lb] = st;
+    // what this step's attention needs, in the step's slot
+    v.aview[(int64_t)a.slot * v.n_lb + lb] = make_int4(t, st.win_start, st.plan, 0);
     const int64_t o = (int64_t)b * a.nl + li;
     if (a.boundary) a.boundary[k * a.stride_b + o] = (uint8_t)st.flag;
     if (a.r_out) a.r_out[k * a.stride_b + o] = st.r;
@@ -388,7 +393,7 @@ constexpr int kScoreWarps = kScoreThreads / 32;
 // boundaries).
 constexpr int kSelSmemUnits = 4096;  // units whose keys and lengths fit in shared memory
 
-__device__ void select_units(const CtxView &v, int64_t gs, int U, int budget) {
+__device__ void select_units(const CtxView &v, int64_t gs, int U, int budget, int ps) {
   const int tid = threadIdx.x, nth = blockDim.x, wid = tid >> 5;
   // keys and lengths once into shared memory (fall back to global memory for
   // very large unit tables)
@@ -501,9 +506,9 @@ __device__ void select_units(const CtxView &v, int64_t gs, int U, int budget) {
   int32_t npc = 0;  // copy pieces of this thread's selected units
   {
     int32_t run = tie_ex, kk = cnt_ex, cum = tok_ex;
-    int32_t *sel_out = v.sel + gs * v.u_cap;
-    int32_t *row_out = v.rng_row + gs * v.u_cap;
-    int32_t *cum_out = v.rng_cum + gs * (int64_t)(v.u_cap + 1);
+    int32_t *sel_out = plan_sel(v, ps, gs);
+    int32_t *row_out = plan_rng_row(v, ps, gs);
+    int32_t *cum_out = plan_rng_cum(v, ps, gs);
     const int32_t *rows = v.unit_row + gs * v.u_cap;
     for (int u = u0; u < u1; ++u) {
       if (!is_sel(u, run)) continue;
@@ -541,9 +546,9 @@ __device__ void select_units(const CtxView &v, int64_t gs, int U, int budget) {
   __syncthreads();
   const int nsc = (s_ntok + kAttnChunk - 1) / kAttnChunk;
   if (tid == 0) {
-    v.n_sel[gs] = s_nsel;
-    v.n_tok[gs] = s_ntok;
-    v.rng_cum[gs * (int64_t)(v.u_cap + 1) + s_nsel] = s_ntok;
+    *plan_nsel(v, ps, gs) = s_nsel;
+    *plan_ntok(v, ps, gs) = s_ntok;
+    plan_rng_cum(v, ps, gs)[s_nsel] = s_ntok;
     if (nsc <= v.max_chunks) v.chunk_piece[gs * (int64_t)(v.max_chunks + 1) + nsc] = s_npieces;
     if (s_ntok > budget || s_npieces > v.max_pieces || nsc > v.max_chunks) set_err(v.err, kErrInternal);
   }
@@ -556,10 +561,10 @@ __device__ void select_units(const CtxView &v, int64_t gs, int U, int budget) {
     for (int p = tid; p < s_npieces; p += nth) {
       const int4 pc = pieces[p];
       const int c = pc.y / kAttnChunk;
-      v.chunk_pieces[(gs * v.max_chunks + c) * kAttnChunk + (p - cp[c])] = pc;
+      plan_chunk_pieces(v, ps, gs)[c * kAttnChunk + (p - cp[c])] = pc;
     }
     for (int c = tid; c < nsc; c += nth)
-      v.chunk_count[gs * v.max_chunks + c] = cp[c + 1] - cp[c];
+      plan_chunk_count(v, ps, gs)[c] = cp[c + 1] - cp[c];
   }
 }
 
@@ -619,7 +624,7 @@ __global__ void __launch_bounds__(kScoreThreads) k_score_select(CtxView v, StepA
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  select_units(v, gs, U, a.budget);
+  select_units(v, gs, U, a.budget, stp->plan);
   if (threadIdx.x == 0) {
     v.score_count[gs] = 0;
     atomicAdd((unsigned long long *)&v.counters[kCntScoreUnits], (unsigned long long)U);
@@ -648,9 +653,10 @@ __global__ void __launch_bounds__(256) k_gather_offload(CtxView v, StepArgs a) {
   pdl_wait();
   pdl_trigger();
   if (!v.st[lb].flag) return;
-  const int ns = v.n_sel[gs], nt = v.n_tok[gs];
-  const int32_t *cum = v.rng_cum + gs * (int64_t)(v.u_cap + 1);
-  const int32_t *rows = v.rng_row + gs * v.u_cap;
+  const int ps = v.st[lb].plan;
+  const int ns = *plan_nsel(v, ps, gs), nt = *plan_ntok(v, ps, gs);
+  const int32_t *cum = plan_rng_cum(v, ps, gs);
+  const int32_t *rows = plan_rng_row(v, ps, gs);
   constexpr int rb = kHeadDim * elem_bytes<DT>();
   constexpr int per_row = rb / 16;
   const int lane = threadIdx.x & 31;
@@ -660,7 +666,7 @@ __global__ void __launch_bounds__(256) k_gather_offload(CtxView v, StepArgs a) {
     const int64_t row = rows[r] + (f - cum[r]);
     if (lane < per_row) {
       const int64_t src = (gs * v.pool_rows + row) * rb + lane * 16;
-      const int64_t dst = (gs * (int64_t)v.bud_cap + f) * rb + lane * 16;
+      const int64_t dst = (((int64_t)ps * v.S_all + gs) * v.bud_cap + f) * rb + lane * 16;
       *(uint4 *)((char *)v.stage_k + dst) = __ldcg((const uint4 *)((const char *)v.pool_k + src));
       *(uint4 *)((char *)v.stage_v + dst) = __ldcg((const uint4 *)((const char *)v.pool_v + src));
     }
@@ -803,7 +809,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn(CtxView v, StepArgs a,
   __shared__ int pcn[kPreChunks];
   __shared__ int done_cnt[kStages];  // warps finished with the chunk in each stage
   __shared__ float part_m[G], part_l[G], part_acc[G][kHeadDim];  // this CTA's partial
-  __shared__ DecState s_st;
+  __shared__ int4 s_view;  // (t, win_start, plan slot, 0) of this step
   __shared__ int s_nt, s_ns, s_ok;
 
   const int per_l = v.B * v.Hkv;
@@ -820,12 +826,10 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn(CtxView v, StepArgs a,
   pdl_wait();
   pdl_trigger();
 
-  // one round of loads: decode state, queries, and (speculatively) the copy
-  // plan of this CTA's first chunks
+  // the step's view (window and plan slot) with the queries, then the plan:
+  // its counts and the copy plan of this CTA's first chunks
   if (tid == 0) {
-    s_st = v.st[lb];
-    s_nt = v.n_tok[gs];
-    s_ns = v.n_sel[gs];
+    s_view = v.aview[(int64_t)a.slot * v.n_lb + lb];
     s_ok = 1;
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&bar[i], 1);
@@ -834,17 +838,26 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn(CtxView v, StepArgs a,
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   for (int x = tid; x < G * kHeadDim; x += kAttnThreads)
-    qs[x / kHeadDim][x % kHeadDim] = v.q_attn[(lb * H + (int64_t)h * G) * kHeadDim + x];
+    qs[x / kHeadDim][x % kHeadDim] =
+        v.q_attn[(((int64_t)a.slot * v.n_lb + lb) * H + (int64_t)h * G) * kHeadDim + x];
+  __syncthreads();
+  const int ps = s_view.z;
+  const int4 *plan_pcs = plan_chunk_pieces(v, ps, gs);
+  const int32_t *plan_pcn = plan_chunk_count(v, ps, gs);
+  if (tid == 0) {
+    s_nt = *plan_ntok(v, ps, gs);
+    s_ns = *plan_nsel(v, ps, gs);
+  }
   if (!v.offload)
     for (int x = tid; x < kPreChunks * kAttnChunk; x += kAttnThreads) {
       const int i = x / kAttnChunk, c = c_begin + i;
       if (i < cpc && c < v.max_chunks) {
-        pcs[i][x % kAttnChunk] = v.chunk_pieces[(gs * v.max_chunks + c) * kAttnChunk + x % kAttnChunk];
-        if (x % kAttnChunk == 0) pcn[i] = v.chunk_count[gs * v.max_chunks + c];
+        pcs[i][x % kAttnChunk] = plan_pcs[c * kAttnChunk + x % kAttnChunk];
+        if (x % kAttnChunk == 0) pcn[i] = plan_pcn[c];
       }
     }
   __syncthreads();
-  const int t_cur = s_st.t - 1, ws = s_st.win_start;
+  const int t_cur = s_view.x, ws = s_view.y;
   const int64_t k = t_cur - a.base_t;
   const int nt = s_nt;
   const int total = nt + (t_cur - ws + 1);
@@ -856,8 +869,8 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn(CtxView v, StepArgs a,
     selk = (const unsigned char *)v.pool_k + gs * v.pool_rows * RB;
     selv = (const unsigned char *)v.pool_v + gs * v.pool_rows * RB;
   } else {
-    selk = (const unsigned char *)v.stage_k + gs * (int64_t)v.bud_cap * RB;
-    selv = (const unsigned char *)v.stage_v + gs * (int64_t)v.bud_cap * RB;
+    selk = (const unsigned char *)v.stage_k + ((int64_t)ps * v.S_all + gs) * v.bud_cap * RB;
+    selv = (const unsigned char *)v.stage_v + ((int64_t)ps * v.S_all + gs) * v.bud_cap * RB;
   }
   // one warp fills stage (i % kStages) with chunk c_begin + i
   auto issue = [&](int i) {
@@ -874,8 +887,8 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn(CtxView v, StepArgs a,
           pieces = pcs[i];
           np = pcn[i];
         } else {
-          pieces = v.chunk_pieces + (gs * v.max_chunks + c) * kAttnChunk;
-          np = v.chunk_count[gs * v.max_chunks + c];
+          pieces = plan_pcs + c * kAttnChunk;
+          np = plan_pcn[c];
         }
       } else {
         sel_direct = min(f0 + kAttnChunk, nt) - f0;
@@ -1103,7 +1116,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn(CtxView v, StepArgs a,
     const int64_t so = ((int64_t)b * a.nl + li) * v.Hkv + h;
     const int ns = s_ns;
     if (a.selected_units) {
-      const int32_t *sel = v.sel + gs * v.u_cap;
+      const int32_t *sel = plan_sel(v, ps, gs);
       int32_t *dst = a.selected_units + k * a.stride_sel + so * v.u_cap;
       for (int x = tid; x < ns; x += kAttnThreads) dst[x] = sel[x];
     }
@@ -1204,9 +1217,13 @@ cudaError_t prepare_kernels(int dtype, int group) {
 }
 
 template <int DT>
-static cudaError_t decode_t(const CtxView &v, const StepArgs &a, cudaStream_t st, Prof &prof) {
+static cudaError_t decode_t(const CtxView &v, const StepArgs &a, cudaStream_t st, Prof &prof,
+                            const Pipe *pipe) {
   const int slices = a.nl * v.B * v.Hkv;
   const int H = v.Hkv * v.G;
+  cudaError_t e = cudaSuccess;
+  if (pipe && pipe->step >= 2) e = cudaStreamWaitEvent(st, pipe->attn_done[pipe->step & 1], 0);
+  if (e != cudaSuccess) return e;
   prof.begin(kPBoundary, st);
   launch_pdl(k_step_boundary<DT>, dim3(a.nl * v.B), dim3(kBoundaryThreads),
              (size_t)2 * H * kQPitch * sizeof(float), st, v, a);
@@ -1220,22 +1237,33 @@ static cudaError_t decode_t(const CtxView &v, const StepArgs &a, cudaStream_t st
     prof.end(st);
   }
   const int nch = (a.budget + v.L + kAttnChunk - 1) / kAttnChunk;
-  prof.begin(kPAttn, st);
+  cudaStream_t as = st;
+  if (pipe) {
+    as = pipe->attn[pipe->step & 1];
+    e = cudaEventRecord(pipe->sel_done, st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(as, pipe->sel_done, 0);
+    if (e != cudaSuccess) return e;
+  }
+  prof.begin(kPAttn, as);
   switch (v.G) {
-    case 1: launch_attn<DT, 1>(v, a, slices, nch, st); break;
-    case 2: launch_attn<DT, 2>(v, a, slices, nch, st); break;
-    case 4: launch_attn<DT, 4>(v, a, slices, nch, st); break;
-    case 8: launch_attn<DT, 8>(v, a, slices, nch, st); break;
+    case 1: launch_attn<DT, 1>(v, a, slices, nch, as); break;
+    case 2: launch_attn<DT, 2>(v, a, slices, nch, as); break;
+    case 4: launch_attn<DT, 4>(v, a, slices, nch, as); break;
+    case 8: launch_attn<DT, 8>(v, a, slices, nch, as); break;
     default: return cudaErrorInvalidValue;
   }
-  prof.end(st);
+  prof.end(as);
+  if (pipe) {
+    e = cudaEventRecord(pipe->attn_done[pipe->step & 1], as);
+    if (e != cudaSuccess) return e;
+  }
   return cudaGetLastError();
 }
 
 cudaError_t launch_decode_step(const CtxView &v, const StepArgs &a, cudaStream_t stream,
-                               Prof &prof) {
-  if (v.dtype == 1) return decode_t<1>(v, a, stream, prof);
-  return decode_t<0>(v, a, stream, prof);
+                               Prof &prof, const Pipe *pipe) {
+  if (v.dtype == 1) return decode_t<1>(v, a, stream, prof, pipe);
+  return decode_t<0>(v, a, stream, prof, pipe);
 }
 
 }  // namespace lkv

@@ -62,50 +62,71 @@ __global__ void k_key_norms(const void *keys, int64_t n, int64_t n_cap, float *k
 
 // Scoring/assignment operand of the current centroids (bf16-rounded for bf16
 // keys), its squared norm in fp32, and per-slice maxima of |c| and |c|^2.
+// A CTA covers 64 centroids (a warp per centroid, lane per 4 dimensions) and
+// folds its maxima into the slice's two words with one atomic each.
+constexpr int kPrepPerCta = 64;
+
 template <int DT>
-__global__ void k_prepare_operand(const float *cent32, void *cent_op, int32_t c,
-                                  int32_t c_pad, int32_t c2_pitch, int32_t u_cap, int64_t gs0,
-                                  float *c2, float *cstat) {
+__global__ void __launch_bounds__(256)
+k_prepare_operand(const float *cent32, void *cent_op, int32_t c, int32_t c_pad, int32_t c2_pitch,
+                  int32_t u_cap, int64_t gs0, float *c2, float *cstat) {
+  __shared__ float wmax[8][2];
   const int s = blockIdx.y;
-  const int lane = threadIdx.x & 31;
-  const int j = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
-  if (j >= c) {
-    // padding up to c_pad for the tensor-core filter: |c|^2 = FLT_MAX (a
-    // finite value no distance reaches) and zero operand rows, so the padded
-    // columns of a chunk stay finite and never win
-    if (j < c_pad) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  float cmax = 0.f, c2max = 0.f;
+  for (int t = 0; t < kPrepPerCta / 8; ++t) {
+    const int j = blockIdx.x * kPrepPerCta + t * 8 + wid;
+    if (j >= c_pad) break;
+    const int64_t base = ((gs0 + s) * u_cap + j) * kHeadDim + lane * 4;
+    if (j >= c) {
+      // padding up to c_pad for the tensor-core filter: |c|^2 = FLT_MAX (a
+      // finite value no distance reaches) and zero operand rows, so the
+      // padded columns of a chunk stay finite and never win
       if (lane == 0) c2[(int64_t)s * c2_pitch + j] = FLT_MAX;
       if (j < u_cap) {
-        const int64_t base = ((gs0 + s) * u_cap + j) * kHeadDim;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) store_elem<DT>(cent_op, base + lane * 4 + e, 0.f);
+        if constexpr (DT == 1) *(uint2 *)((uint16_t *)cent_op + base) = make_uint2(0u, 0u);
+        else *(float4 *)((float *)cent_op + base) = make_float4(0.f, 0.f, 0.f, 0.f);
       }
+      continue;
     }
-    return;
-  }
-  const int64_t base = ((gs0 + s) * u_cap + j) * kHeadDim;
-  float acc = 0.f;
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const int k = lane * 4 + e;
-    float x = cent32[base + k];
+    const float4 x4 = *(const float4 *)(cent32 + base);
+    float x[4] = {x4.x, x4.y, x4.z, x4.w};
     if constexpr (DT == 1) {
-      uint16_t b = f32_to_bf16_bits(x);
-      ((uint16_t *)cent_op)[base + k] = b;
-      x = bf16_bits_to_f32(b);
-    } else {
-      ((float *)cent_op)[base + k] = x;
-    }
-    acc = fmaf(x, x, acc);
-  }
+      uint16_t b[4];
 #pragma unroll
-  for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-  if (lane == 0) {
-    c2[(int64_t)s * c2_pitch + j] = acc;
-    // non-negative floats order like their bit patterns
-    atomicMax((unsigned *)&cstat[2 * s], __float_as_uint(sqrtf(acc)));
-    atomicMax((unsigned *)&cstat[2 * s + 1], __float_as_uint(acc));
+      for (int e = 0; e < 4; ++e) {
+        b[e] = f32_to_bf16_bits(x[e]);
+        x[e] = bf16_bits_to_f32(b[e]);
+      }
+      *(uint2 *)((uint16_t *)cent_op + base) =
+          make_uint2((uint32_t)b[0] | ((uint32_t)b[1] << 16), (uint32_t)b[2] | ((uint32_t)b[3] << 16));
+    } else {
+      *(float4 *)((float *)cent_op + base) = x4;
+    }
+    float acc = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc = fmaf(x[e], x[e], acc);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) c2[(int64_t)s * c2_pitch + j] = acc;
+    cmax = fmaxf(cmax, sqrtf(acc));
+    c2max = fmaxf(c2max, acc);
   }
+  if (lane == 0) { wmax[wid][0] = cmax; wmax[wid][1] = c2max; }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < 8; ++w) { cmax = fmaxf(cmax, wmax[w][0]); c2max = fmaxf(c2max, wmax[w][1]); }
+    // non-negative floats order like their bit patterns
+    atomicMax((unsigned *)&cstat[2 * s], __float_as_uint(cmax));
+    atomicMax((unsigned *)&cstat[2 * s + 1], __float_as_uint(c2max));
+  }
+}
+
+template <int DT>
+static void launch_prepare(const CtxView &v, int32_t c, int32_t c_pad, int32_t c2_pitch, int64_t gs0,
+                           int S, float *c2, float *cstat, cudaStream_t st) {
+  k_prepare_operand<DT><<<dim3((c_pad + kPrepPerCta - 1) / kPrepPerCta, S), 256, 0, st>>>(
+      v.cent32, v.cent_op, c, c_pad, c2_pitch, v.u_cap, gs0, c2, cstat);
 }
 
 // ---------------------------------------------------------------- assignment
@@ -990,9 +1011,26 @@ __global__ void k_scatter(const int32_t *assign, int64_t n, int64_t n_cap, int32
 
 // ---------------------------------------------------------------- update
 
-// Warp per cluster, lane per 4 dimensions, members in token order.
+// Warp per cluster, lane per 4 dimensions, members in token order. Members
+// are fetched sixteen at a time (indices first, then the sixteen key rows) so
+// the loads overlap; the sums still take the members in token order. Blocks
+// of two warps keep a long cluster from holding up the others.
+constexpr int kUpdBatch = 16;
+constexpr int kUpdThreads = 64;
+
 template <int DT>
-__global__ void k_update(const void *keys, int64_t n, int64_t n_cap, int32_t c,
+__device__ __forceinline__ void load4(const void *keys, int64_t row, int lane, float (&x)[4],
+                                      uint2 &raw) {
+  if constexpr (DT == 1) {
+    raw = __ldg((const uint2 *)((const uint16_t *)keys + row * kHeadDim + lane * 4));
+  } else {
+    const float4 f = __ldg((const float4 *)((const float *)keys + row * kHeadDim + lane * 4));
+    x[0] = f.x; x[1] = f.y; x[2] = f.z; x[3] = f.w;
+  }
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kUpdThreads) k_update(const void *keys, int64_t n, int64_t n_cap, int32_t c,
                          int32_t c_cap, int32_t u_cap, int64_t gs0, const int32_t *perm,
                          const int32_t *count, const int32_t *offs, float *cent32,
                          int64_t *n_inexact) {
@@ -1005,18 +1043,31 @@ __global__ void k_update(const void *keys, int64_t n, int64_t n_cap, int32_t c,
   const int32_t base = offs[(int64_t)s * c_cap + j];
   const int64_t gs = gs0 + s;
   const int32_t *pm = perm + gs * n_cap + base;
-  double sum[4];
+  const int64_t row0 = (int64_t)s * n;
+  double sum[4] = {0.0, 0.0, 0.0, 0.0};
   bool slow = (DT == 0);
   if constexpr (DT == 1) {
     int64_t acc[4] = {0, 0, 0, 0};
     int oor = 0;
-    for (int32_t m = 0; m < cnt; ++m) {
-      const int64_t i = pm[m];
-      const uint2 raw = *(const uint2 *)((const uint16_t *)keys + ((int64_t)s * n + i) * kHeadDim + lane * 4);
-      acc[0] += bf16_fixed40((uint16_t)(raw.x & 0xffffu), &oor);
-      acc[1] += bf16_fixed40((uint16_t)(raw.x >> 16), &oor);
-      acc[2] += bf16_fixed40((uint16_t)(raw.y & 0xffffu), &oor);
-      acc[3] += bf16_fixed40((uint16_t)(raw.y >> 16), &oor);
+    for (int32_t m0 = 0; m0 < cnt; m0 += kUpdBatch) {
+      const int nb = min(kUpdBatch, cnt - m0);
+      const int32_t mine = lane < nb ? __ldg(pm + m0 + lane) : 0;
+      uint2 raw[kUpdBatch];
+      float unused[4];
+#pragma unroll
+      for (int b = 0; b < kUpdBatch; ++b) {
+        const int32_t i = __shfl_sync(0xffffffffu, mine, b);
+        if (b < nb) load4<DT>(keys, row0 + i, lane, unused, raw[b]);
+      }
+#pragma unroll
+      for (int b = 0; b < kUpdBatch; ++b) {
+        if (b < nb) {
+          acc[0] += bf16_fixed40((uint16_t)(raw[b].x & 0xffffu), &oor);
+          acc[1] += bf16_fixed40((uint16_t)(raw[b].x >> 16), &oor);
+          acc[2] += bf16_fixed40((uint16_t)(raw[b].y & 0xffffu), &oor);
+          acc[3] += bf16_fixed40((uint16_t)(raw[b].y >> 16), &oor);
+        }
+      }
     }
     slow = __any_sync(0xffffffffu, oor) != 0;
     if (!slow) {
@@ -1026,14 +1077,44 @@ __global__ void k_update(const void *keys, int64_t n, int64_t n_cap, int32_t c,
       atomicAdd((unsigned long long *)n_inexact, 1ull);
     }
   }
-  if (slow) {
+  if (slow) {  // double-precision sums in token order
+    for (int32_t m0 = 0; m0 < cnt; m0 += kUpdBatch) {
+      const int nb = min(kUpdBatch, cnt - m0);
+      const int32_t mine = lane < nb ? __ldg(pm + m0 + lane) : 0;
+      if constexpr (DT == 1) {
+        uint2 raw[kUpdBatch];
+        float unused[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) sum[e] = 0.0;
-    for (int32_t m = 0; m < cnt; ++m) {
-      const int64_t i = pm[m];
+        for (int b = 0; b < kUpdBatch; ++b) {
+          const int32_t i = __shfl_sync(0xffffffffu, mine, b);
+          if (b < nb) load4<DT>(keys, row0 + i, lane, unused, raw[b]);
+        }
 #pragma unroll
-      for (int e = 0; e < 4; ++e)
-        sum[e] = __dadd_rn(sum[e], (double)load_elem<DT>(keys, ((int64_t)s * n + i) * kHeadDim + lane * 4 + e));
+        for (int b = 0; b < kUpdBatch; ++b) {
+          if (b < nb) {
+            sum[0] = __dadd_rn(sum[0], (double)__uint_as_float(raw[b].x << 16));
+            sum[1] = __dadd_rn(sum[1], (double)__uint_as_float(raw[b].x & 0xffff0000u));
+            sum[2] = __dadd_rn(sum[2], (double)__uint_as_float(raw[b].y << 16));
+            sum[3] = __dadd_rn(sum[3], (double)__uint_as_float(raw[b].y & 0xffff0000u));
+          }
+        }
+      } else {
+        float4 x[kUpdBatch];
+#pragma unroll
+        for (int b = 0; b < kUpdBatch; ++b) {
+          const int32_t i = __shfl_sync(0xffffffffu, mine, b);
+          if (b < nb) x[b] = __ldg((const float4 *)((const float *)keys + (row0 + i) * kHeadDim + lane * 4));
+        }
+#pragma unroll
+        for (int b = 0; b < kUpdBatch; ++b) {
+          if (b < nb) {
+            sum[0] = __dadd_rn(sum[0], (double)x[b].x);
+            sum[1] = __dadd_rn(sum[1], (double)x[b].y);
+            sum[2] = __dadd_rn(sum[2], (double)x[b].z);
+            sum[3] = __dadd_rn(sum[3], (double)x[b].w);
+          }
+        }
+      }
     }
   }
   float *dst = cent32 + (gs * u_cap + j) * kHeadDim + lane * 4;
@@ -1090,9 +1171,11 @@ __global__ void k_reset_layer(CtxView v, int layer, int32_t c) {
     const int64_t gs = lb * v.Hkv + h;
     for (int k = threadIdx.x; k < kHeadDim; k += blockDim.x) v.segsum[gs * kHeadDim + k] = 0;
     if (threadIdx.x == 0) {
-      v.n_sel[gs] = 0;
-      v.n_tok[gs] = 0;
-      v.rng_cum[gs * (int64_t)(v.u_cap + 1)] = 0;
+      for (int p = 0; p < 2; ++p) {  // both plan slots start empty
+        *plan_nsel(v, p, gs) = 0;
+        *plan_ntok(v, p, gs) = 0;
+        plan_rng_cum(v, p, gs)[0] = 0;
+      }
       v.attn_count[gs] = 0;
       v.score_count[gs] = 0;
     }
@@ -1180,8 +1263,7 @@ static cudaError_t kmeans_build_t(const CtxView &v, int layer, const KmeansScrat
   for (int it = 0; it < iters; ++it) {
     prof.begin(kPKmOperand, st);
     cudaMemsetAsync(ks.cstat, 0, sizeof(float) * 2 * S, st);
-    k_prepare_operand<DT><<<dim3((c_pad + 7) / 8, S), 256, 0, st>>>(v.cent32, v.cent_op, c, c_pad, ks.c2_pitch,
-                                                               v.u_cap, gs0, ks.c2, ks.cstat);
+    launch_prepare<DT>(v, c, c_pad, ks.c2_pitch, gs0, S, ks.c2, ks.cstat, st);
     cudaMemsetAsync(ks.amb_count, 0, 2 * sizeof(int32_t), st);  // both ends of the queue
     prof.end(st);
     prof.begin(use_tc ? kPKmAssignTc : kPKmAssign, st);
@@ -1203,15 +1285,14 @@ static cudaError_t kmeans_build_t(const CtxView &v, int layer, const KmeansScrat
     cudaError_t e = group_and_pool<DT>(v, layer, ks, n, c, gs0, S, st, prof);
     if (e != cudaSuccess) return e;
     prof.begin(kPKmUpdate, st);
-    k_update<DT><<<dim3((c + 7) / 8, S), 256, 0, st>>>(keys, n, v.n_cap, c, c_cap, v.u_cap, gs0,
+    k_update<DT><<<dim3((c + 1) / 2, S), kUpdThreads, 0, st>>>(keys, n, v.n_cap, c, c_cap, v.u_cap, gs0,
                                                        v.perm, ks.count, ks.offs, v.cent32,
                                                        ks.n_inexact);
     prof.end(st);
   }
   prof.begin(kPKmOperand, st);
   cudaMemsetAsync(ks.cstat, 0, sizeof(float) * 2 * S, st);
-  k_prepare_operand<DT><<<dim3((c_pad + 7) / 8, S), 256, 0, st>>>(v.cent32, v.cent_op, c, c_pad, ks.c2_pitch,
-                                                             v.u_cap, gs0, ks.c2, ks.cstat);
+  launch_prepare<DT>(v, c, c_pad, ks.c2_pitch, gs0, S, ks.c2, ks.cstat, st);
   prof.end(st);
   return finish_pool<DT>(v, layer, ks, keys, values, n, c, gs0, S, st, prof);
 }
@@ -1252,8 +1333,7 @@ static cudaError_t load_index_t(const CtxView &v, int layer, const KmeansScratch
   k_copy_given<DT><<<dim3(64, S), 256, 0, st>>>(assign, cent, n, c, v.n_cap, v.u_cap, gs0,
                                                 v.assign, v.cent32, v.err);
   cudaMemsetAsync(ks.cstat, 0, sizeof(float) * 2 * S, st);
-  k_prepare_operand<DT><<<dim3((c_pad + 7) / 8, S), 256, 0, st>>>(v.cent32, v.cent_op, c, c_pad, ks.c2_pitch,
-                                                             v.u_cap, gs0, ks.c2, ks.cstat);
+  launch_prepare<DT>(v, c, c_pad, ks.c2_pitch, gs0, S, ks.c2, ks.cstat, st);
   cudaError_t e = group_and_pool<DT>(v, layer, ks, n, c, gs0, S, st, prof);
   if (e != cudaSuccess) return e;
   return finish_pool<DT>(v, layer, ks, keys, values, n, c, gs0, S, st, prof);
@@ -1363,8 +1443,7 @@ static cudaError_t kmeans_static_t(unsigned char *base, const void *keys, int64_
   for (int it = 0; it < iters; ++it) {
     e = cudaMemsetAsync(ks.cstat, 0, sizeof(float) * 2, st);
     if (e != cudaSuccess) return e;
-    k_prepare_operand<DT><<<dim3((c + 7) / 8, 1), 256, 0, st>>>(v.cent32, v.cent_op, c, c, c, v.u_cap,
-                                                              0, ks.c2, ks.cstat);
+    launch_prepare<DT>(v, c, c, c, 0, 1, ks.c2, ks.cstat, st);
     e = cudaMemsetAsync(ks.amb_count, 0, sizeof(int32_t), st);
     if (e == cudaSuccess) e = cudaMemsetAsync(amb_crowd, 0, sizeof(int32_t), st);
     if (e != cudaSuccess) return e;
@@ -1375,7 +1454,7 @@ static cudaError_t kmeans_static_t(unsigned char *base, const void *keys, int64_
                       amb_crowd, (int32_t)amb_cap, ks.n_refined, st);
     e = group_and_pool<DT>(v, 0, ks, n, c, 0, 1, st, quiet);
     if (e != cudaSuccess) return e;
-    k_update<DT><<<dim3((c + 7) / 8, 1), 256, 0, st>>>(keys, n, v.n_cap, c, c, v.u_cap, 0, v.perm,
+    k_update<DT><<<dim3((c + 1) / 2, 1), kUpdThreads, 0, st>>>(keys, n, v.n_cap, c, c, v.u_cap, 0, v.perm,
                                                        ks.count, ks.offs, v.cent32, ks.n_inexact);
   }
   return cudaGetLastError();

@@ -36,7 +36,7 @@ struct DecState {
   int32_t flag;        // this step retrieves
   float r;             // this step's r_t
   int32_t seg_slow;    // open segment holds a value outside the exact-sum range
-  int32_t pad;
+  int32_t plan;        // selection-plan slot (0/1) in force; a retrieval step flips it
 };
 
 // Everything a kernel needs to find the context's data. Per-slice arrays are
@@ -51,13 +51,15 @@ struct CtxView {
   int32_t u_cap;      // max units per slice (C_cap + T_cap)
   int32_t bud_cap;    // max token budget
   int offload;
+  int64_t S_all;      // slices of all layers (n_layers * B * Hkv)
+  int32_t n_lb;       // (layer, sequence) pairs (n_layers * B)
   // pool: prefill rows [0, n_cap) and evicted-segment rows [n_cap, n_cap+t_cap)
   void *pool_k, *pool_v;      // slice stride pool_rows * d (HBM or pinned host)
   int64_t pool_rows;
   // decode region (local buffer rows), decode position t at row t
   void *dec_k, *dec_v;        // slice stride dec_rows * d
   int64_t dec_rows;
-  void *stage_k, *stage_v;    // offload only: [slice][bud_cap][d]
+  void *stage_k, *stage_v;    // offload only: [plan slot][slice][bud_cap][d]
   void *cent_op;              // [slice][u_cap][d] scoring operand (dtype)
   float *cent32;              // [slice][u_cap][d]
   int32_t *unit_row;          // [slice][u_cap]
@@ -66,19 +68,21 @@ struct CtxView {
   int32_t *perm;              // [slice][n_cap]
   DecState *st;               // [lb]
   void *q_prev;               // [lb][H][d] (dtype)
-  float *q_attn;              // [lb][H][d] this step's queries * log2(e)/sqrt(d), fp32
+  float *q_attn;              // [step slot][lb][H][d] queries * log2(e)/sqrt(d), fp32
+  int4 *aview;                // [step slot][lb] (t, win_start, plan slot, 0) for the attention
   int64_t *segsum;            // [slice][d] exact fixed-point sums (bf16) or
                               // doubles reinterpreted (fp32)
   float *scores;              // [slice][u_cap]
-  int32_t *sel;               // [slice][u_cap] selected unit ids, ascending
-  int32_t *n_sel;             // [slice]
-  int32_t *n_tok;             // [slice]
-  int32_t *rng_row;           // [slice][u_cap] first row of each selected unit
-  int32_t *rng_cum;           // [slice][u_cap + 1] exclusive token prefix
+  // the selection plan, double-buffered: [plan slot][slice]...
+  int32_t *sel;               // [2][slice][u_cap] selected unit ids, ascending
+  int32_t *n_sel;             // [2][slice]
+  int32_t *n_tok;             // [2][slice]
+  int32_t *rng_row;           // [2][slice][u_cap] first row of each selected unit
+  int32_t *rng_cum;           // [2][slice][u_cap + 1] exclusive token prefix
   int4 *pieces;               // [slice][max_pieces] (src row, first token, length, 0)
   int32_t *chunk_piece;       // [slice][max_chunks + 1] first piece of each chunk
-  int4 *chunk_pieces;         // [slice][max_chunks][64] the pieces of each chunk
-  int32_t *chunk_count;       // [slice][max_chunks] pieces in each chunk
+  int4 *chunk_pieces;         // [2][slice][max_chunks][64] the pieces of each chunk
+  int32_t *chunk_count;       // [2][slice][max_chunks] pieces in each chunk
   int32_t max_pieces;
   int32_t *attn_count;        // [slice]
   int32_t *score_count;       // [slice] score CTAs done this step (last one selects)
@@ -86,6 +90,29 @@ struct CtxView {
   int32_t *err;               // device error bits (shared by all layers)
   int64_t *counters;          // [kCounters] work counters (see CounterId)
 };
+
+// Plan-slot views of the double-buffered selection plan.
+__host__ __device__ __forceinline__ int32_t *plan_sel(const CtxView &v, int p, int64_t gs) {
+  return v.sel + ((int64_t)p * v.S_all + gs) * v.u_cap;
+}
+__host__ __device__ __forceinline__ int32_t *plan_nsel(const CtxView &v, int p, int64_t gs) {
+  return v.n_sel + (int64_t)p * v.S_all + gs;
+}
+__host__ __device__ __forceinline__ int32_t *plan_ntok(const CtxView &v, int p, int64_t gs) {
+  return v.n_tok + (int64_t)p * v.S_all + gs;
+}
+__host__ __device__ __forceinline__ int32_t *plan_rng_row(const CtxView &v, int p, int64_t gs) {
+  return v.rng_row + ((int64_t)p * v.S_all + gs) * v.u_cap;
+}
+__host__ __device__ __forceinline__ int32_t *plan_rng_cum(const CtxView &v, int p, int64_t gs) {
+  return v.rng_cum + ((int64_t)p * v.S_all + gs) * (v.u_cap + 1);
+}
+__host__ __device__ __forceinline__ int4 *plan_chunk_pieces(const CtxView &v, int p, int64_t gs) {
+  return v.chunk_pieces + ((int64_t)p * v.S_all + gs) * v.max_chunks * 64;
+}
+__host__ __device__ __forceinline__ int32_t *plan_chunk_count(const CtxView &v, int p, int64_t gs) {
+  return v.chunk_count + ((int64_t)p * v.S_all + gs) * v.max_chunks;
+}
 
 // Work counters accumulated on the device (read by lkv_get_profile).
 enum CounterId : int { kCntAttnRows = 0, kCntScoreUnits = 1, kCntGatherRows = 2,
@@ -255,11 +282,26 @@ struct StepArgs {
   uint8_t *boundary;               // [B][nl] or null
   float *r_out;                    // [B][nl] or null
   int32_t l0;                      // first layer of this call
+  int32_t slot;                    // step slot (queries, attention view): the step's
+                                   // index in a pipelined capture mod 2, else 0
   int32_t nl;                      // layers in this call
 };
 
+// Streams and events of a pipelined multi-step capture: step i's attention
+// runs on attn[i % 2], after the step's selection (sel_done); step i's
+// boundary kernel waits for step i - 2's attention (attn_done[i % 2]), the
+// last user of the step slot and of the plan slot it may overwrite.
+struct Pipe {
+  cudaStream_t attn[2];
+  cudaEvent_t sel_done;
+  cudaEvent_t attn_done[2];
+  int step;  // index of the step in the capture
+};
+
+// One decode step; with `pipe` (graph capture only) the attention is forked
+// onto a side stream as described above.
 cudaError_t launch_decode_step(const CtxView &v, const StepArgs &a, cudaStream_t stream,
-                               Prof &prof);
+                               Prof &prof, const Pipe *pipe = nullptr);
 // Error text of calls that have no context (read with lkv_last_error(NULL)).
 void set_unbound_error(const char *msg);
 // One-time kernel attributes (dynamic shared memory limits), before any capture.
