@@ -324,7 +324,7 @@ def run_ours(args, rank, world, local):
         "trigger_rate": trig, "kmeans_refined_keys_total": st["n_refined"],
         "roofline": {"kernel": "lkv_attn", "bound": "hbm", "achieved": achieved, "peak": hbm_peak,
                      "unit": "GB/s", "frac": achieved / hbm_peak,
-                     "traffic": ncu_traffic("lkv_attn", ctr["attn_rows"] / max(n_attn, 1)),
+                     "traffic": ncu_traffic("lkv_attn", alg_bytes),
                      "peak_source": f"{peak_kind} hbm_gbs (burst copy)",
                      "alg_bytes_per_launch": alg_bytes, "avg_launch_us": attn_s * 1e6,
                      "launches": int(n_attn), "l2": "256 MB written before every step"},

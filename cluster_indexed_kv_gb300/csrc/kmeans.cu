@@ -1012,11 +1012,12 @@ __global__ void k_scatter(const int32_t *assign, int64_t n, int64_t n_cap, int32
 // ---------------------------------------------------------------- update
 
 // Warp per cluster, lane per 4 dimensions, members in token order. Members
-// are fetched sixteen at a time (indices first, then the sixteen key rows) so
-// the loads overlap; the sums still take the members in token order. Blocks
-// of two warps keep a long cluster from holding up the others.
-constexpr int kUpdBatch = 16;
-constexpr int kUpdThreads = 64;
+// are fetched eight at a time (indices first, then the eight key rows) so
+// the loads overlap; the sums still take the members in token order. A
+// persistent grid whose warps take clusters in turn keeps a long cluster from
+// holding up others.
+constexpr int kUpdBatch = 8;
+constexpr int kUpdThreads = 256;
 
 template <int DT>
 __device__ __forceinline__ void load4(const void *keys, int64_t row, int lane, float (&x)[4],
@@ -1030,16 +1031,17 @@ __device__ __forceinline__ void load4(const void *keys, int64_t row, int lane, f
 }
 
 template <int DT>
-__global__ void __launch_bounds__(kUpdThreads) k_update(const void *keys, int64_t n, int64_t n_cap, int32_t c,
+__global__ void __launch_bounds__(kUpdThreads, 3) k_update(const void *keys, int64_t n, int64_t n_cap, int32_t c,
                          int32_t c_cap, int32_t u_cap, int64_t gs0, const int32_t *perm,
                          const int32_t *count, const int32_t *offs, float *cent32,
-                         int64_t *n_inexact) {
-  const int s = blockIdx.y;
+                         int64_t *n_inexact, int n_slices) {
   const int lane = threadIdx.x & 31;
-  const int j = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
-  if (j >= c) return;
+  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x / 32);
+  for (int64_t w = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; w < (int64_t)n_slices * c;
+       w += nwarps) {
+  const int s = (int)(w / c), j = (int)(w % c);
   const int32_t cnt = count[(int64_t)s * c_cap + j];
-  if (cnt == 0) return;  // empty cluster keeps its centroid
+  if (cnt == 0) continue;  // empty cluster keeps its centroid
   const int32_t base = offs[(int64_t)s * c_cap + j];
   const int64_t gs = gs0 + s;
   const int32_t *pm = perm + gs * n_cap + base;
@@ -1120,6 +1122,21 @@ __global__ void __launch_bounds__(kUpdThreads) k_update(const void *keys, int64_
   float *dst = cent32 + (gs * u_cap + j) * kHeadDim + lane * 4;
 #pragma unroll
   for (int e = 0; e < 4; ++e) dst[e] = __double2float_rn(__ddiv_rn(sum[e], (double)cnt));
+  }
+}
+
+// Resident blocks of the update on this device (its persistent grid).
+template <int DT>
+static int update_grid() {
+  static int grid[2] = {0, 0};
+  if (!grid[DT]) {
+    int dev = 0, sms = 0, per = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, k_update<DT>, kUpdThreads, 0);
+    grid[DT] = (sms > 0 ? sms : 1) * (per > 0 ? per : 1);
+  }
+  return grid[DT];
 }
 
 // ---------------------------------------------------------------- pool
@@ -1285,9 +1302,9 @@ static cudaError_t kmeans_build_t(const CtxView &v, int layer, const KmeansScrat
     cudaError_t e = group_and_pool<DT>(v, layer, ks, n, c, gs0, S, st, prof);
     if (e != cudaSuccess) return e;
     prof.begin(kPKmUpdate, st);
-    k_update<DT><<<dim3((c + 1) / 2, S), kUpdThreads, 0, st>>>(keys, n, v.n_cap, c, c_cap, v.u_cap, gs0,
-                                                       v.perm, ks.count, ks.offs, v.cent32,
-                                                       ks.n_inexact);
+    k_update<DT><<<update_grid<DT>(), kUpdThreads, 0, st>>>(keys, n, v.n_cap, c, c_cap, v.u_cap, gs0,
+                                                           v.perm, ks.count, ks.offs, v.cent32,
+                                                           ks.n_inexact, S);
     prof.end(st);
   }
   prof.begin(kPKmOperand, st);
@@ -1454,8 +1471,8 @@ static cudaError_t kmeans_static_t(unsigned char *base, const void *keys, int64_
                       amb_crowd, (int32_t)amb_cap, ks.n_refined, st);
     e = group_and_pool<DT>(v, 0, ks, n, c, 0, 1, st, quiet);
     if (e != cudaSuccess) return e;
-    k_update<DT><<<dim3((c + 1) / 2, 1), kUpdThreads, 0, st>>>(keys, n, v.n_cap, c, c, v.u_cap, 0, v.perm,
-                                                       ks.count, ks.offs, v.cent32, ks.n_inexact);
+    k_update<DT><<<update_grid<DT>(), kUpdThreads, 0, st>>>(keys, n, v.n_cap, c, c, v.u_cap, 0, v.perm,
+                                                           ks.count, ks.offs, v.cent32, ks.n_inexact, 1);
   }
   return cudaGetLastError();
 }
