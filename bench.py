@@ -44,7 +44,22 @@ def parse_args(argv=None):
     p.add_argument("--profile-steps", type=int, default=512)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--workload", default="b8_32k",
+                   help="synthetic workload (default: the 32K-input, batch-8 decode workload)")
     return p.parse_args(argv)
+
+
+def max_over_ranks(values):
+    """Element-wise maximum of a list of floats over all ranks (the list
+    itself with one rank)."""
+    import torch
+    import torch.distributed as td
+    if not (td.is_available() and td.is_initialized()) or td.get_world_size() == 1:
+        return list(values)
+    dev = "cuda" if td.get_backend() == "nccl" else "cpu"
+    t = torch.tensor(list(values), dtype=torch.float64, device=dev)
+    td.all_reduce(t, op=td.ReduceOp.MAX)
+    return t.tolist()
 
 
 def dist_env():
@@ -56,7 +71,7 @@ def dist_env():
 
 def workload(args):
     import synth
-    w = synth.WORKLOADS["b8_32k"]
+    w = synth.WORKLOADS[args.workload]
     if args.decode_steps:
         w = w.replace(n_steps=args.decode_steps)
     if args.iters:
@@ -266,10 +281,7 @@ def run_ours(args, rank, world, local):
     launches = int(sum(v[0] for v in kern.values()))
     trig = float(bnd.float().mean().item())
     st = ctx.decode_state(0, 0)
-    times = torch.tensor([build_ms, dec_ms, wall * 1e3], dtype=torch.float64, device=dev)
-    if dist:
-        torch.distributed.all_reduce(times, op=torch.distributed.ReduceOp.MAX)
-    build_ms, dec_ms, wall_ms = times.tolist()
+    build_ms, dec_ms, wall_ms = max_over_ranks([build_ms, dec_ms, wall * 1e3])
     K_steps = args.steps
     value = world * T * K_steps / (dec_ms / 1e3)
     mkeys = world * w.batch * w.n_kv_heads * w.n_prefill * w.iters * K_steps / (build_ms / 1e3) / 1e6

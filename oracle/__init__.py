@@ -250,11 +250,14 @@ def attention(q_group: np.ndarray, k_rows: np.ndarray, v_rows: np.ndarray) -> np
 
 
 def decode(keys, values, assign_, cent, q, k_new, v_new, *, n_clusters, local_buf,
-           tau, budget, attn_mask=None, want_seg_cent=False):
+           tau, budget, attn_mask=None, want_seg_cent=False, want_sel=True):
     """Run one (sequence, layer) decode through the oracle.
 
     keys/values [H_kv, N, d]; assign_ [H_kv, N]; cent [H_kv, C, d] fp32;
     q [T, H, d]; k_new/v_new [T, H_kv, d]. Returns a dict of numpy arrays.
+    want_sel=False skips the per-step selection lists (n_sel and n_tok are
+    still recorded); with lists, each holds at most budget + C ids (a unit
+    that fits adds at least one token, except empty clusters).
     """
     keys, values = np.ascontiguousarray(keys), np.ascontiguousarray(values)
     q, k_new, v_new = (np.ascontiguousarray(x) for x in (q, k_new, v_new))
@@ -266,6 +269,7 @@ def decode(keys, values, assign_, cent, q, k_new, v_new, *, n_clusters, local_bu
     dt = dtype_of(q)
     c = n_clusters
     ucap = c + T
+    max_sel = min(ucap, budget + c)
     mask = None if attn_mask is None else _arr(attn_mask, np.uint8)
     args = DecodeArgs(dt, hkv, g, d, n, c, local_buf, T, tau, budget, _p(keys), _p(values),
                       _p(assign_), _p(cent), _p(q), _p(k_new), _p(v_new), _p(mask))
@@ -273,11 +277,12 @@ def decode(keys, values, assign_, cent, q, k_new, v_new, *, n_clusters, local_bu
         out=np.zeros((T, h_all, d), np.float64), flag=np.zeros(T, np.uint8),
         r32=np.zeros(T, np.float32), r64=np.zeros(T, np.float64),
         n_sel=np.zeros((T, hkv), np.int32), n_tok=np.zeros((T, hkv), np.int32),
-        sel=np.full((T, hkv, ucap), -1, np.int32), win_start=np.zeros(T, np.int32),
+        sel=np.full((T, hkv, max_sel), -1, np.int32) if want_sel else None,
+        win_start=np.zeros(T, np.int32),
         n_units=np.zeros(T, np.int32), seg_start=np.zeros(max(T, 1), np.int32),
         seg_len=np.zeros(max(T, 1), np.int32),
         seg_cent=np.zeros((max(T, 1), hkv, d), np.float32) if want_seg_cent else None)
-    r = DecodeResult(ucap, max(T, 1), *(_p(res[k]) for k in (
+    r = DecodeResult(max_sel, max(T, 1), *(_p(res[k]) for k in (
         "out", "flag", "r32", "r64", "n_sel", "n_tok", "sel", "win_start", "n_units",
         "seg_start", "seg_len", "seg_cent")), 0, 0)
     if lib().lkvo_decode(C.byref(args), C.byref(r)) != 0:
