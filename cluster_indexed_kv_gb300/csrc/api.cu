@@ -98,7 +98,7 @@ static void free_all(lkv_ctx *c) {
   c->prof.release();
   if (c->capture) cudaStreamDestroy(c->capture);
   c->capture = nullptr;
-  for (int i = 0; i < 2; ++i) {
+  for (int i = 0; i < lkv::kRing; ++i) {
     if (c->pipe.attn[i]) cudaStreamDestroy(c->pipe.attn[i]);
     if (c->pipe.attn_done[i]) cudaEventDestroy(c->pipe.attn_done[i]);
     c->pipe.attn[i] = nullptr;
@@ -190,8 +190,8 @@ lkv_status lkv_create(const lkv_config *cfg, lkv_ctx **out) {
     v.dec_k = dalloc(c, S_all * t_cap * d * es, &st);
     v.dec_v = dalloc(c, S_all * t_cap * d * es, &st);
     v.dec_rows = t_cap;
-    v.stage_k = dalloc(c, 2 * S_all * (int64_t)k.max_budget * d * es, &st);  // per plan slot
-    v.stage_v = dalloc(c, 2 * S_all * (int64_t)k.max_budget * d * es, &st);
+    v.stage_k = dalloc(c, lkv::kRing * S_all * (int64_t)k.max_budget * d * es, &st);  // per plan slot
+    v.stage_v = dalloc(c, lkv::kRing * S_all * (int64_t)k.max_budget * d * es, &st);
   }
   v.cent_op = dalloc(c, S_all * u_cap * d * es, &st);
   v.cent32 = (float *)dalloc(c, S_all * u_cap * d * 4, &st);
@@ -201,24 +201,24 @@ lkv_status lkv_create(const lkv_config *cfg, lkv_ctx **out) {
   v.perm = (int32_t *)dalloc(c, S_all * n_cap * 4, &st);
   v.st = (DecState *)dalloc(c, LB * sizeof(DecState), &st);
   v.q_prev = dalloc(c, LB * H * d * es, &st);
-  v.q_attn = (float *)dalloc(c, 2 * LB * H * d * 4, &st);  // per step slot
-  v.aview = (int4 *)dalloc(c, 2 * LB * sizeof(int4), &st);
+  v.q_attn = (float *)dalloc(c, lkv::kRing * LB * H * d * 4, &st);  // per step slot
+  v.aview = (int4 *)dalloc(c, lkv::kRing * LB * sizeof(int4), &st);
   v.segsum = (int64_t *)dalloc(c, S_all * d * 8, &st);
   v.scores = (float *)dalloc(c, S_all * u_cap * 4, &st);
   // the selection plan, one copy per plan slot
-  v.sel = (int32_t *)dalloc(c, 2 * S_all * u_cap * 4, &st);
-  v.n_sel = (int32_t *)dalloc(c, 2 * S_all * 4, &st);
-  v.n_tok = (int32_t *)dalloc(c, 2 * S_all * 4, &st);
-  v.rng_row = (int32_t *)dalloc(c, 2 * S_all * u_cap * 4, &st);
-  v.rng_cum = (int32_t *)dalloc(c, 2 * S_all * (u_cap + 1) * 4, &st);
+  v.sel = (int32_t *)dalloc(c, lkv::kRing * S_all * u_cap * 4, &st);
+  v.n_sel = (int32_t *)dalloc(c, lkv::kRing * S_all * 4, &st);
+  v.n_tok = (int32_t *)dalloc(c, lkv::kRing * S_all * 4, &st);
+  v.rng_row = (int32_t *)dalloc(c, lkv::kRing * S_all * u_cap * 4, &st);
+  v.rng_cum = (int32_t *)dalloc(c, lkv::kRing * S_all * (u_cap + 1) * 4, &st);
   v.max_chunks = max_chunks;
   v.attn_count = (int32_t *)dalloc(c, S_all * 4, &st);
   v.score_count = (int32_t *)dalloc(c, S_all * 4, &st);
   v.max_pieces = u_cap + max_chunks;
   v.pieces = (int4 *)dalloc(c, S_all * (int64_t)v.max_pieces * sizeof(int4), &st);
   v.chunk_piece = (int32_t *)dalloc(c, S_all * (int64_t)(max_chunks + 1) * 4, &st);
-  v.chunk_pieces = (int4 *)dalloc(c, 2 * S_all * (int64_t)max_chunks * lkv::kAttnChunk * sizeof(int4), &st);
-  v.chunk_count = (int32_t *)dalloc(c, 2 * S_all * (int64_t)max_chunks * 4, &st);
+  v.chunk_pieces = (int4 *)dalloc(c, lkv::kRing * S_all * (int64_t)max_chunks * lkv::kAttnChunk * sizeof(int4), &st);
+  v.chunk_count = (int32_t *)dalloc(c, lkv::kRing * S_all * (int64_t)max_chunks * 4, &st);
   v.err = (int32_t *)dalloc(c, 4, &st);
   v.counters = (int64_t *)dalloc(c, lkv::kCounters * 8, &st);
 
@@ -250,7 +250,7 @@ lkv_status lkv_create(const lkv_config *cfg, lkv_ctx **out) {
   if (e == cudaSuccess) e = cudaMemsetAsync(ks.n_inexact, 0, 8, c->stream);
   if (e == cudaSuccess) e = cudaMemsetAsync(v.counters, 0, lkv::kCounters * 8, c->stream);
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&c->capture, cudaStreamNonBlocking);
-  for (int i = 0; i < 2; ++i) {
+  for (int i = 0; i < lkv::kRing; ++i) {
     if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&c->pipe.attn[i], cudaStreamNonBlocking);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->pipe.attn_done[i], cudaEventDisableTiming);
   }
@@ -416,12 +416,12 @@ static cudaError_t step_graph(lkv_ctx *c, const lkv::StepArgs &a, int steps, cud
   lkv::Pipe pipe = c->pipe;
   for (int i = 0; i < steps && e == cudaSuccess; ++i) {
     lkv::StepArgs ai = a;
-    ai.slot = i & 1;
+    ai.slot = i % lkv::kRing;
     pipe.step = i;
     e = lkv::launch_decode_step(c->v, ai, c->capture, quiet, &pipe);
   }
-  for (int i = 0; i < 2 && i < steps && e == cudaSuccess; ++i)
-    e = cudaStreamWaitEvent(c->capture, c->pipe.attn_done[(steps - 1 - i) & 1], 0);
+  for (int i = 0; i < lkv::kRing && i < steps && e == cudaSuccess; ++i)
+    e = cudaStreamWaitEvent(c->capture, c->pipe.attn_done[(steps - 1 - i) % lkv::kRing], 0);
   cudaError_t e2 = cudaStreamEndCapture(c->capture, &graph);
   if (e == cudaSuccess) e = e2;
   cudaGraphExec_t exec = nullptr;

@@ -14,6 +14,8 @@
 //                    (seq, layer, kv head) combines the partials
 //
 // Inputs/outputs of step k of a call live at base + k * stride (StepArgs).
+#include <cstdlib>
+
 #include "lkv_internal.cuh"
 
 namespace lkv {
@@ -139,11 +141,12 @@ __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-constexpr int kBoundaryThreads = 1024;
+// 512 threads (62 registers each) fit beside an attention CTA on one SM.
+constexpr int kBoundaryThreads = 512;
 constexpr int kQPitch = kHeadDim + 8;  // padded query rows in shared memory (floats)
 
 template <int DT>
-__global__ void __launch_bounds__(kBoundaryThreads) k_step_boundary(CtxView v, StepArgs a) {
+__global__ void __launch_bounds__(kBoundaryThreads, 2) k_step_boundary(CtxView v, StepArgs a) {
   const int li = blockIdx.x / v.B, b = blockIdx.x % v.B;
   const int l = a.l0 + li;
   const int64_t lb = (int64_t)l * v.B + b;
@@ -183,7 +186,7 @@ __global__ void __launch_bounds__(kBoundaryThreads) k_step_boundary(CtxView v, S
 #pragma unroll
     for (int i = 0; i < per16; ++i) dst[i] = e[i];
   }
-  constexpr int kMaxPer = 2;  // Hkv * d <= 2048
+  constexpr int kMaxPer = 16 * kHeadDim / kBoundaryThreads;  // Hkv * d <= 2048
   uint32_t kbits[kMaxPer], vbits[kMaxPer];
   int64_t ssum[kMaxPer];
 #pragma unroll
@@ -230,12 +233,12 @@ __global__ void __launch_bounds__(kBoundaryThreads) k_step_boundary(CtxView v, S
       r = __fdiv_rn(r, (float)H);
       st.r = r;
       st.flag = r < a.tau ? 1 : 0;
-      st.plan ^= st.flag;  // a retrieval writes its plan into the other slot
+      if (st.flag) st.plan = (st.plan + 1) % kRing;  // a retrieval writes the next plan slot
     }
   } else if (tid == 0) {
     st.r = 0.f;
     st.flag = 1;
-    st.plan ^= 1;
+    st.plan = (st.plan + 1) % kRing;
   }
   __syncthreads();
 
@@ -1133,6 +1136,11 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn(CtxView v, StepArgs a,
 
 // Launch with programmatic stream serialization: the kernel may be scheduled
 // while its predecessor drains and waits for it in pdl_wait().
+// Scheduling priorities: the serial boundary/selection chain of the decode
+// steps goes first, so that a pending attention grid does not hold back the
+// next step's chain when SM resources free up.
+static int g_prio_chain = 0, g_prio_attn = 0;
+
 template <typename... KArgs, typename... Args>
 static void launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
                        cudaStream_t st, Args... args) {
@@ -1141,11 +1149,13 @@ static void launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributePriority;
+  attr[1].val.priority = g_prio_chain;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
@@ -1153,11 +1163,14 @@ template <int DT, int G>
 constexpr size_t attn_smem() { return (size_t)kStages * stage_bytes<DT>(); }
 
 static int g_attn_slots = 2 * 152;  // resident attention CTAs on the device
+static int g_attn_split = 0;        // CTAs per slice forced by LKV_ATTN_CTAS_PER_SLICE (0: auto)
+constexpr int kAttnConcurrent = 2;  // attention grids sized to run this many at once
 
 // Split of a slice's chunks over the CTAs of one cluster (at most kMaxSplit),
-// so that the whole grid is resident at once where possible.
+// so that kAttnConcurrent grids (consecutive steps of a pipelined graph) are
+// resident at once where possible.
 static void attn_split(int slices, int nch, int *nsplit, int *cpc) {
-  int want = g_attn_slots / slices;
+  int want = g_attn_split > 0 ? g_attn_split : g_attn_slots / (slices * kAttnConcurrent);
   if (want < 1) want = 1;
   if (want > kMaxSplit) want = kMaxSplit;
   if (want > nch) want = nch;
@@ -1174,15 +1187,17 @@ static void launch_attn(const CtxView &v, const StepArgs &a, int slices, int nch
   cfg.blockDim = dim3(kAttnThreads);
   cfg.dynamicSmemBytes = attn_smem<DT, G>();
   cfg.stream = st;
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[3];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   attr[1].id = cudaLaunchAttributeClusterDimension;
   attr[1].val.clusterDim.x = 1;
   attr[1].val.clusterDim.y = nsplit;
   attr[1].val.clusterDim.z = 1;
+  attr[2].id = cudaLaunchAttributePriority;
+  attr[2].val.priority = g_prio_attn;
   cfg.attrs = attr;
-  cfg.numAttrs = 2;
+  cfg.numAttrs = 3;
   cudaLaunchKernelEx(&cfg, k_attn<DT, G>, v, a, cpc);
 }
 
@@ -1197,6 +1212,15 @@ static cudaError_t prep_attn() {
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   if (per_sm > 0 && sms > 0) g_attn_slots = per_sm * sms;
+  int least = 0, greatest = 0;  // numerically: least >= greatest; greatest is the highest priority
+  if (cudaDeviceGetStreamPriorityRange(&least, &greatest) == cudaSuccess) {
+    g_prio_chain = greatest;
+    g_prio_attn = least;
+  }
+  if (const char *env = getenv("LKV_ATTN_CTAS_PER_SLICE")) {
+    const int x = atoi(env);
+    g_attn_split = (x >= 1 && x <= kMaxSplit) ? x : 0;
+  }
   return cudaFuncSetAttribute(k_step_boundary<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)(2 * kMaxHeads * kQPitch * sizeof(float)));
 }
@@ -1222,7 +1246,7 @@ static cudaError_t decode_t(const CtxView &v, const StepArgs &a, cudaStream_t st
   const int slices = a.nl * v.B * v.Hkv;
   const int H = v.Hkv * v.G;
   cudaError_t e = cudaSuccess;
-  if (pipe && pipe->step >= 2) e = cudaStreamWaitEvent(st, pipe->attn_done[pipe->step & 1], 0);
+  if (pipe && pipe->step >= kRing) e = cudaStreamWaitEvent(st, pipe->attn_done[pipe->step % kRing], 0);
   if (e != cudaSuccess) return e;
   prof.begin(kPBoundary, st);
   launch_pdl(k_step_boundary<DT>, dim3(a.nl * v.B), dim3(kBoundaryThreads),
@@ -1239,7 +1263,7 @@ static cudaError_t decode_t(const CtxView &v, const StepArgs &a, cudaStream_t st
   const int nch = (a.budget + v.L + kAttnChunk - 1) / kAttnChunk;
   cudaStream_t as = st;
   if (pipe) {
-    as = pipe->attn[pipe->step & 1];
+    as = pipe->attn[pipe->step % kRing];
     e = cudaEventRecord(pipe->sel_done, st);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(as, pipe->sel_done, 0);
     if (e != cudaSuccess) return e;
@@ -1254,7 +1278,7 @@ static cudaError_t decode_t(const CtxView &v, const StepArgs &a, cudaStream_t st
   }
   prof.end(as);
   if (pipe) {
-    e = cudaEventRecord(pipe->attn_done[pipe->step & 1], as);
+    e = cudaEventRecord(pipe->attn_done[pipe->step % kRing], as);
     if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();

@@ -1188,7 +1188,7 @@ __global__ void k_reset_layer(CtxView v, int layer, int32_t c) {
     const int64_t gs = lb * v.Hkv + h;
     for (int k = threadIdx.x; k < kHeadDim; k += blockDim.x) v.segsum[gs * kHeadDim + k] = 0;
     if (threadIdx.x == 0) {
-      for (int p = 0; p < 2; ++p) {  // both plan slots start empty
+      for (int p = 0; p < kRing; ++p) {  // every plan slot starts empty
         *plan_nsel(v, p, gs) = 0;
         *plan_ntok(v, p, gs) = 0;
         plan_rng_cum(v, p, gs)[0] = 0;

@@ -14,6 +14,7 @@ constexpr int kHeadDim = 128;
 constexpr int kMaxGroup = 8;
 constexpr int kMaxParts = 64;      // token parts of the stable counting sort
 constexpr int kAttnChunk = 64;     // tokens per attention work item
+constexpr int kRing = 4;           // steps whose attention may be in flight at once
 constexpr int kScoreCtasPerHead = 8;
 
 // Error bits recorded on the device and reported by lkv_sync.
@@ -36,7 +37,7 @@ struct DecState {
   int32_t flag;        // this step retrieves
   float r;             // this step's r_t
   int32_t seg_slow;    // open segment holds a value outside the exact-sum range
-  int32_t plan;        // selection-plan slot (0/1) in force; a retrieval step flips it
+  int32_t plan;        // selection-plan slot (0..kRing-1) in force; a retrieval step advances it
 };
 
 // Everything a kernel needs to find the context's data. Per-slice arrays are
@@ -68,21 +69,21 @@ struct CtxView {
   int32_t *perm;              // [slice][n_cap]
   DecState *st;               // [lb]
   void *q_prev;               // [lb][H][d] (dtype)
-  float *q_attn;              // [step slot][lb][H][d] queries * log2(e)/sqrt(d), fp32
+  float *q_attn;              // [kRing step slots][lb][H][d] queries * log2(e)/sqrt(d), fp32
   int4 *aview;                // [step slot][lb] (t, win_start, plan slot, 0) for the attention
   int64_t *segsum;            // [slice][d] exact fixed-point sums (bf16) or
                               // doubles reinterpreted (fp32)
   float *scores;              // [slice][u_cap]
-  // the selection plan, double-buffered: [plan slot][slice]...
-  int32_t *sel;               // [2][slice][u_cap] selected unit ids, ascending
-  int32_t *n_sel;             // [2][slice]
-  int32_t *n_tok;             // [2][slice]
-  int32_t *rng_row;           // [2][slice][u_cap] first row of each selected unit
-  int32_t *rng_cum;           // [2][slice][u_cap + 1] exclusive token prefix
+  // the selection plan, one copy per plan slot: [kRing][slice]...
+  int32_t *sel;               // [kRing][slice][u_cap] selected unit ids, ascending
+  int32_t *n_sel;             // [kRing][slice]
+  int32_t *n_tok;             // [kRing][slice]
+  int32_t *rng_row;           // [kRing][slice][u_cap] first row of each selected unit
+  int32_t *rng_cum;           // [kRing][slice][u_cap + 1] exclusive token prefix
   int4 *pieces;               // [slice][max_pieces] (src row, first token, length, 0)
   int32_t *chunk_piece;       // [slice][max_chunks + 1] first piece of each chunk
-  int4 *chunk_pieces;         // [2][slice][max_chunks][64] the pieces of each chunk
-  int32_t *chunk_count;       // [2][slice][max_chunks] pieces in each chunk
+  int4 *chunk_pieces;         // [kRing][slice][max_chunks][64] the pieces of each chunk
+  int32_t *chunk_count;       // [kRing][slice][max_chunks] pieces in each chunk
   int32_t max_pieces;
   int32_t *attn_count;        // [slice]
   int32_t *score_count;       // [slice] score CTAs done this step (last one selects)
@@ -283,18 +284,21 @@ struct StepArgs {
   float *r_out;                    // [B][nl] or null
   int32_t l0;                      // first layer of this call
   int32_t slot;                    // step slot (queries, attention view): the step's
-                                   // index in a pipelined capture mod 2, else 0
+                                   // index in a pipelined capture mod kRing, else 0
   int32_t nl;                      // layers in this call
 };
 
 // Streams and events of a pipelined multi-step capture: step i's attention
-// runs on attn[i % 2], after the step's selection (sel_done); step i's
-// boundary kernel waits for step i - 2's attention (attn_done[i % 2]), the
-// last user of the step slot and of the plan slot it may overwrite.
+// runs on attn[i % kRing], after the step's selection (sel_done); step i's
+// boundary kernel waits for step i - kRing's attention (attn_done[i % kRing]),
+// the last reader of the step slot it rewrites. A retrieval writes plan slot
+// (retrievals so far) mod kRing; the attentions that may still run then are
+// those of the kRing - 1 previous steps, whose plans are the kRing - 1
+// previous retrievals' at most, so none reads the slot being written.
 struct Pipe {
-  cudaStream_t attn[2];
+  cudaStream_t attn[kRing];
   cudaEvent_t sel_done;
-  cudaEvent_t attn_done[2];
+  cudaEvent_t attn_done[kRing];
   int step;  // index of the step in the capture
 };
 
