@@ -105,7 +105,10 @@ static void free_all(lkv_ctx *c) {
     c->pipe.attn_done[i] = nullptr;
   }
   if (c->pipe.sel_done) cudaEventDestroy(c->pipe.sel_done);
-  c->pipe.sel_done = nullptr;
+  if (c->pipe.b_done) cudaEventDestroy(c->pipe.b_done);
+  if (c->pipe.sel) cudaStreamDestroy(c->pipe.sel);
+  c->pipe.sel_done = c->pipe.b_done = nullptr;
+  c->pipe.sel = nullptr;
   for (void *p : c->dev) cudaFree(p);
   for (void *p : c->host) cudaFreeHost(p);
   c->dev.clear();
@@ -255,6 +258,8 @@ lkv_status lkv_create(const lkv_config *cfg, lkv_ctx **out) {
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->pipe.attn_done[i], cudaEventDisableTiming);
   }
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->pipe.sel_done, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->pipe.b_done, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&c->pipe.sel, cudaStreamNonBlocking);
   if (e == cudaSuccess) e = lkv::prepare_kernels(k.dtype, k.group);
   if (e == cudaSuccess) e = cudaStreamSynchronize(c->stream);
   if (e != cudaSuccess) {
@@ -420,8 +425,11 @@ static cudaError_t step_graph(lkv_ctx *c, const lkv::StepArgs &a, int steps, cud
     pipe.step = i;
     e = lkv::launch_decode_step(c->v, ai, c->capture, quiet, &pipe);
   }
+  // join every lane back into the capture stream
   for (int i = 0; i < lkv::kRing && i < steps && e == cudaSuccess; ++i)
     e = cudaStreamWaitEvent(c->capture, c->pipe.attn_done[(steps - 1 - i) % lkv::kRing], 0);
+  if (e == cudaSuccess && steps > 0) e = cudaEventRecord(c->pipe.sel_done, c->pipe.sel);
+  if (e == cudaSuccess && steps > 0) e = cudaStreamWaitEvent(c->capture, c->pipe.sel_done, 0);
   cudaError_t e2 = cudaStreamEndCapture(c->capture, &graph);
   if (e == cudaSuccess) e = e2;
   cudaGraphExec_t exec = nullptr;

@@ -349,7 +349,7 @@ __global__ void __launch_bounds__(kBoundaryThreads, 2) k_step_boundary(CtxView v
     st.t = t + 1;
     v.st[lb] = st;
     // what this step's attention needs, in the step's slot
-    v.aview[(int64_t)a.slot * v.n_lb + lb] = make_int4(t, st.win_start, st.plan, 0);
+    v.aview[(int64_t)a.slot * v.n_lb + lb] = make_int4(t, st.win_start, st.plan, st.n_units * 2 + st.flag);
     const int64_t o = (int64_t)b * a.nl + li;
     if (a.boundary) a.boundary[k * a.stride_b + o] = (uint8_t)st.flag;
     if (a.r_out) a.r_out[k * a.stride_b + o] = st.r;
@@ -571,10 +571,11 @@ __device__ void select_units(const CtxView &v, int64_t gs, int U, int budget, in
   }
 }
 
-// Scores of every unit (one thread per unit, fp32 FMA in index order), then
-// the last CTA of the (seq, layer, kv head) to finish runs the selection.
+// One CTA per (seq, layer, kv head), on retrieval steps only: the score of
+// every unit (a thread per unit at a time, fp32 FMA in index order, the
+// centroid row in one round trip), then the selection by the same block.
 template <int DT>
-__global__ void __launch_bounds__(kScoreThreads) k_score_select(CtxView v, StepArgs a) {
+__global__ void __launch_bounds__(kScoreThreads, 2) k_score_select(CtxView v, StepArgs a) {
   const int per_l = v.B * v.Hkv;
   const int li = blockIdx.x / per_l, rem = blockIdx.x % per_l;
   const int b = rem / v.Hkv, h = rem % v.Hkv;
@@ -583,13 +584,14 @@ __global__ void __launch_bounds__(kScoreThreads) k_score_select(CtxView v, StepA
   const int64_t gs = lb * v.Hkv + h;
   pdl_wait();
   pdl_trigger();
-  const DecState *stp = v.st + lb;
-  if (!stp->flag) return;
-  const int U = stp->n_units;
-  const int64_t k = (stp->t - 1) - a.base_t;
+  // the step's view, not the live state: the next step's boundary kernel may
+  // already be updating that
+  const int4 view = v.aview[(int64_t)a.slot * v.n_lb + lb];
+  if (!(view.w & 1)) return;
+  const int U = view.w >> 1;
+  const int64_t k = view.x - a.base_t;
   const void *q = (const char *)a.q + k * a.stride_q * elem_bytes<DT>();
   __shared__ float qbar[kHeadDim];
-  __shared__ int s_last;
   const int H = v.Hkv * v.G;
   const int64_t qoff = (((int64_t)b * a.nl + li) * H + (int64_t)h * v.G) * kHeadDim;
   if (threadIdx.x < kHeadDim) {
@@ -599,7 +601,7 @@ __global__ void __launch_bounds__(kScoreThreads) k_score_select(CtxView v, StepA
   }
   __syncthreads();
   constexpr int nvec = kHeadDim * elem_bytes<DT>() / 16;  // 16-byte vectors per centroid row
-  for (int u = blockIdx.y * blockDim.x + threadIdx.x; u < U; u += gridDim.y * blockDim.x) {
+  for (int u = threadIdx.x; u < U; u += blockDim.x) {
     const uint4 *row = (const uint4 *)((const char *)v.cent_op + (gs * v.u_cap + u) * kHeadDim * elem_bytes<DT>());
     uint4 raw[nvec];
 #pragma unroll
@@ -621,17 +623,10 @@ __global__ void __launch_bounds__(kScoreThreads) k_score_select(CtxView v, StepA
     }
     v.scores[gs * v.u_cap + u] = s;
   }
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) s_last = (atomicAdd(&v.score_count[gs], 1) == (int)gridDim.y - 1);
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  select_units(v, gs, U, a.budget, stp->plan);
-  if (threadIdx.x == 0) {
-    v.score_count[gs] = 0;
+  __syncthreads();  // the block's score writes are visible to the block
+  select_units(v, gs, U, a.budget, view.z);
+  if (threadIdx.x == 0)
     atomicAdd((unsigned long long *)&v.counters[kCntScoreUnits], (unsigned long long)U);
-  }
 }
 
 // ---------------------------------------------------------------- offload gather
@@ -655,8 +650,9 @@ __global__ void __launch_bounds__(256) k_gather_offload(CtxView v, StepArgs a) {
   const int64_t gs = lb * v.Hkv + h;
   pdl_wait();
   pdl_trigger();
-  if (!v.st[lb].flag) return;
-  const int ps = v.st[lb].plan;
+  const int4 view = v.aview[(int64_t)a.slot * v.n_lb + lb];
+  if (!(view.w & 1)) return;
+  const int ps = view.z;
   const int ns = *plan_nsel(v, ps, gs), nt = *plan_ntok(v, ps, gs);
   const int32_t *cum = plan_rng_cum(v, ps, gs);
   const int32_t *rows = plan_rng_row(v, ps, gs);
@@ -1252,19 +1248,28 @@ static cudaError_t decode_t(const CtxView &v, const StepArgs &a, cudaStream_t st
   launch_pdl(k_step_boundary<DT>, dim3(a.nl * v.B), dim3(kBoundaryThreads),
              (size_t)2 * H * kQPitch * sizeof(float), st, v, a);
   prof.end(st);
-  prof.begin(kPScore, st);
-  launch_pdl(k_score_select<DT>, dim3(slices, kScoreCtasPerHead), dim3(kScoreThreads), 0, st, v, a);
-  prof.end(st);
+  // pipelined: the selection lane follows the boundary lane, the step's
+  // attention follows its selection
+  cudaStream_t ss = st;
+  if (pipe) {
+    ss = pipe->sel;
+    e = cudaEventRecord(pipe->b_done, st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(ss, pipe->b_done, 0);
+    if (e != cudaSuccess) return e;
+  }
+  prof.begin(kPScore, ss);
+  launch_pdl(k_score_select<DT>, dim3(slices), dim3(kScoreThreads), 0, ss, v, a);
+  prof.end(ss);
   if (v.offload) {
-    prof.begin(kPGather, st);
-    launch_pdl(k_gather_offload<DT>, dim3(slices, 16), dim3(256), 0, st, v, a);
-    prof.end(st);
+    prof.begin(kPGather, ss);
+    launch_pdl(k_gather_offload<DT>, dim3(slices, 16), dim3(256), 0, ss, v, a);
+    prof.end(ss);
   }
   const int nch = (a.budget + v.L + kAttnChunk - 1) / kAttnChunk;
   cudaStream_t as = st;
   if (pipe) {
     as = pipe->attn[pipe->step % kRing];
-    e = cudaEventRecord(pipe->sel_done, st);
+    e = cudaEventRecord(pipe->sel_done, ss);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(as, pipe->sel_done, 0);
     if (e != cudaSuccess) return e;
   }

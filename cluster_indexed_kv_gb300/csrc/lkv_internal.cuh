@@ -15,7 +15,6 @@ constexpr int kMaxGroup = 8;
 constexpr int kMaxParts = 64;      // token parts of the stable counting sort
 constexpr int kAttnChunk = 64;     // tokens per attention work item
 constexpr int kRing = 4;           // steps whose attention may be in flight at once
-constexpr int kScoreCtasPerHead = 8;
 
 // Error bits recorded on the device and reported by lkv_sync.
 enum : int32_t {
@@ -288,16 +287,23 @@ struct StepArgs {
   int32_t nl;                      // layers in this call
 };
 
-// Streams and events of a pipelined multi-step capture: step i's attention
-// runs on attn[i % kRing], after the step's selection (sel_done); step i's
-// boundary kernel waits for step i - kRing's attention (attn_done[i % kRing]),
-// the last reader of the step slot it rewrites. A retrieval writes plan slot
-// (retrievals so far) mod kRing; the attentions that may still run then are
-// those of the kRing - 1 previous steps, whose plans are the kRing - 1
-// previous retrievals' at most, so none reads the slot being written.
+// Streams and events of a pipelined multi-step capture, three lanes:
+//  - boundary kernels on the capture stream, one after the other (the decode
+//    state chain); step i's waits for step i - kRing's attention
+//    (attn_done[i % kRing]), the last reader of the step slot it rewrites;
+//  - scoring/selection (and the offload gather) on `sel`, each after its
+//    step's boundary kernel (b_done) and the previous selection. They read
+//    the step's view, never the live state, and a boundary kernel only
+//    writes units that the selections still running cannot reach;
+//  - step i's attention on attn[i % kRing], after its selection (sel_done).
+// A retrieval writes plan slot (retrievals so far) mod kRing; the attentions
+// that may still run then are those of the kRing - 1 previous steps, whose
+// plans are the kRing - 1 previous retrievals' at most, so none reads the
+// slot being written.
 struct Pipe {
+  cudaStream_t sel;
   cudaStream_t attn[kRing];
-  cudaEvent_t sel_done;
+  cudaEvent_t b_done, sel_done;
   cudaEvent_t attn_done[kRing];
   int step;  // index of the step in the capture
 };
