@@ -998,11 +998,16 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn(CtxView v, StepArgs a,
     l_own = l_own * corr_own + psum;
     __syncwarp();
     // pass 2: acc = corr * acc + sum_r p_r v_r
+    bool rescale = false;  // (warp-uniform: the chunk maxima come from shuffles)
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const float2 c2 = make_float2(corr[g], corr[g]);
+    for (int g = 0; g < G; ++g) rescale |= corr[g] != 1.f;
+    if (rescale) {
 #pragma unroll
-      for (int p = 0; p < 4; ++p) acc[g][p] = fmul2(acc[g][p], c2);
+      for (int g = 0; g < G; ++g) {
+        const float2 c2 = make_float2(corr[g], corr[g]);
+#pragma unroll
+        for (int p = 0; p < 4; ++p) acc[g][p] = fmul2(acc[g][p], c2);
+      }
     }
 #pragma unroll
     for (int it = 0; it < kRowsPerWarp / 2; ++it) {
@@ -1086,14 +1091,17 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn(CtxView v, StepArgs a,
       part_l[g] = z;
     }
   }
-  // CTA 0 of the cluster combines every CTA's partial (read through
-  // distributed shared memory); the second cluster barrier keeps the other
-  // CTAs' shared memory alive until it is done
+  // every CTA of the cluster combines its share of the outputs from all
+  // CTAs' partials (read through distributed shared memory); the second
+  // cluster barrier keeps each CTA's shared memory alive until all are done
   cluster_sync();
-  if (cluster_rank() == 0) {
+  {
+    const int rank = (int)cluster_rank();
     float *out = a.out + k * a.stride_out;
     const int64_t obase = (((int64_t)b * a.nl + li) * H + (int64_t)h * G) * kHeadDim;
-    for (int x = tid; x < G * kHeadDim; x += kAttnThreads) {
+    const int per = (G * kHeadDim + nsplit - 1) / nsplit;
+    const int x1 = min(G * kHeadDim, (rank + 1) * per);
+    for (int x = rank * per + tid; x < x1; x += kAttnThreads) {
       const int g = x / kHeadDim, dim = x % kHeadDim;
       float mc[kMaxSplit];
       float mm = -INFINITY;
@@ -1117,9 +1125,9 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn(CtxView v, StepArgs a,
     if (a.selected_units) {
       const int32_t *sel = plan_sel(v, ps, gs);
       int32_t *dst = a.selected_units + k * a.stride_sel + so * v.u_cap;
-      for (int x = tid; x < ns; x += kAttnThreads) dst[x] = sel[x];
+      for (int x = rank * kAttnThreads + tid; x < ns; x += nsplit * kAttnThreads) dst[x] = sel[x];
     }
-    if (tid == 0) {
+    if (rank == 0 && tid == 0) {
       if (a.n_selected) a.n_selected[k * a.stride_nsel + so] = ns;
       atomicAdd((unsigned long long *)&v.counters[kCntAttnRows], (unsigned long long)total);
       atomicAdd((unsigned long long *)&v.counters[kCntAttnSlices], 1ull);
