@@ -207,17 +207,26 @@ def peaks():
         return 6800.0, 1900.0, 1700.0, "fallback"
 
 
+def kernel_source_sha256(source, region):
+    """SHA-256 of the part of `source` from the line `region[0]` up to the
+    line `region[1]` (the kernel and its device helpers)."""
+    import hashlib
+    with open(os.path.join(ROOT, source)) as f:
+        text = f.read()
+    i = text.index(region[0])
+    j = text.index(region[1], i)
+    return hashlib.sha256(text[i:j].encode()).hexdigest()
+
+
 def ncu_traffic(kernel, units):
     """DRAM bytes per launch from the committed ncu summary, scaled to
     `units` (the launch's work units) when the capture ran a smaller case;
     None when the kernel's source changed after the capture."""
-    import hashlib
     try:
         with open(os.path.join(ROOT, "profiles", "ncu_traffic.txt")) as f:
             rec = json.load(f)[kernel]
-        with open(os.path.join(ROOT, rec["source"]), "rb") as f:
-            if hashlib.sha256(f.read()).hexdigest() != rec["source_sha256"]:
-                return None
+        if kernel_source_sha256(rec["source"], rec["region"]) != rec["region_sha256"]:
+            return None
         return rec["dram_bytes_per_launch"] * units / rec["units_per_launch"]
     except Exception:
         return None

@@ -1168,13 +1168,13 @@ constexpr size_t attn_smem() { return (size_t)kStages * stage_bytes<DT>(); }
 
 static int g_attn_slots = 2 * 152;  // resident attention CTAs on the device
 static int g_attn_split = 0;        // CTAs per slice forced by LKV_ATTN_CTAS_PER_SLICE (0: auto)
-constexpr int kAttnConcurrent = 2;  // attention grids sized to run this many at once
+constexpr int kAttnConcurrent = 2;  // pipelined attention grids sized to run this many at once
 
-// Split of a slice's chunks over the CTAs of one cluster (at most kMaxSplit),
-// so that kAttnConcurrent grids (consecutive steps of a pipelined graph) are
+// Split of a slice's chunks over the CTAs of one cluster (at most kMaxSplit):
+// `concurrent` grids (consecutive steps of a pipelined graph, else 1) are
 // resident at once where possible.
-static void attn_split(int slices, int nch, int *nsplit, int *cpc) {
-  int want = g_attn_split > 0 ? g_attn_split : g_attn_slots / (slices * kAttnConcurrent);
+static void attn_split(int slices, int nch, int concurrent, int *nsplit, int *cpc) {
+  int want = g_attn_split > 0 ? g_attn_split : g_attn_slots / (slices * concurrent);
   if (want < 1) want = 1;
   if (want > kMaxSplit) want = kMaxSplit;
   if (want > nch) want = nch;
@@ -1183,9 +1183,10 @@ static void attn_split(int slices, int nch, int *nsplit, int *cpc) {
 }
 
 template <int DT, int G>
-static void launch_attn(const CtxView &v, const StepArgs &a, int slices, int nch, cudaStream_t st) {
+static void launch_attn(const CtxView &v, const StepArgs &a, int slices, int nch, int concurrent,
+                        cudaStream_t st) {
   int nsplit = 1, cpc = 1;
-  attn_split(slices, nch, &nsplit, &cpc);
+  attn_split(slices, nch, concurrent, &nsplit, &cpc);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(slices, nsplit);
   cfg.blockDim = dim3(kAttnThreads);
@@ -1281,12 +1282,13 @@ static cudaError_t decode_t(const CtxView &v, const StepArgs &a, cudaStream_t st
     if (e == cudaSuccess) e = cudaStreamWaitEvent(as, pipe->sel_done, 0);
     if (e != cudaSuccess) return e;
   }
+  const int conc = pipe ? kAttnConcurrent : 1;
   prof.begin(kPAttn, as);
   switch (v.G) {
-    case 1: launch_attn<DT, 1>(v, a, slices, nch, as); break;
-    case 2: launch_attn<DT, 2>(v, a, slices, nch, as); break;
-    case 4: launch_attn<DT, 4>(v, a, slices, nch, as); break;
-    case 8: launch_attn<DT, 8>(v, a, slices, nch, as); break;
+    case 1: launch_attn<DT, 1>(v, a, slices, nch, conc, as); break;
+    case 2: launch_attn<DT, 2>(v, a, slices, nch, conc, as); break;
+    case 4: launch_attn<DT, 4>(v, a, slices, nch, conc, as); break;
+    case 8: launch_attn<DT, 8>(v, a, slices, nch, conc, as); break;
     default: return cudaErrorInvalidValue;
   }
   prof.end(as);
