@@ -184,12 +184,13 @@ def oracle_kmeans_sample(keys_bits, c, n_keys):
 def cpu_baseline(K, V, idx0, q, kn, vn, w, n_steps=48, kmeans_keys=1024):
     import synth
     per = oracle_decode_sample(K[0].cpu(), V[0].cpu(), idx0, q, kn, vn, w, n_steps)
-    steps_per_s = 1.0 / (per * w.batch * w.n_kv_heads)
+    units = w.batch * w.n_kv_heads * w.n_layers
+    steps_per_s = 1.0 / (per * units)
     km = oracle_kmeans_sample(synth.to_oracle(K[0, 0]), w.n_clusters, kmeans_keys)
     return {"value": steps_per_s, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"single-threaded C oracle: 1 (sequence, KV head) x {n_steps} decode steps "
-                      f"of the full-size workload (teacher-forced from the GPU index), scaled by "
-                      f"B x H_kv = {w.batch * w.n_kv_heads}; k-means: one Lloyd round of "
+            "sample": f"single-threaded C oracle: 1 (sequence, layer, KV head) x {n_steps} decode "
+                      f"steps of the full-size workload (teacher-forced from the GPU index), scaled "
+                      f"by B x layers x H_kv = {units}; k-means: one Lloyd round of "
                       f"{kmeans_keys} keys x {w.n_clusters} clusters",
             "kmeans_mkeys_per_s": kmeans_keys / km / 1e6}
 
@@ -240,23 +241,28 @@ def run_ours(args, rank, world, local):
     torch.cuda.set_device(local)
     lkv.build()
     w = workload(args)
-    T = w.n_steps
+    T, NL = w.n_steps, w.n_layers
     dev = "cuda"
-    K, V = synth.prefill(w, 0, dev)
+    KV = [synth.prefill(w, layer, dev) for layer in range(NL)]
+    K, V = KV[0]
     q, kn, vn, _ = synth.decode_inputs(w, dev, n_steps=T)
     prof_T = min(args.profile_steps, T)
-    ctx = lkv.Context(batch=w.batch, n_layers=1, n_kv_heads=w.n_kv_heads, group=w.group,
+    ctx = lkv.Context(batch=w.batch, n_layers=NL, n_kv_heads=w.n_kv_heads, group=w.group,
                       dtype=w.torch_dtype, local_buf=w.local_buf, max_clusters=w.n_clusters,
-                      max_prefill=w.n_prefill, max_steps=T, max_budget=w.budget)
+                      max_prefill=w.n_prefill, max_steps=T, max_budget=w.budget, offload=w.offload)
     stream = ctx.stream
-    out = torch.empty(T, w.batch, 1, w.n_heads, 128, device=dev)
-    bnd = torch.zeros(T, w.batch, 1, dtype=torch.uint8, device=dev)
+    out = torch.empty(T, w.batch, NL, w.n_heads, 128, device=dev)
+    bnd = torch.zeros(T, w.batch, NL, dtype=torch.uint8, device=dev)
     ev = {}
 
+    def build_all():
+        for layer, (Kl, Vl) in enumerate(KV):
+            ctx.build_index(layer, Kl, Vl, w.n_clusters, w.iters, 1)
+
     def one_step():
-        ctx.build_index(0, K, V, w.n_clusters, w.iters, 1)
+        build_all()
         ev["mid"].record(stream)
-        ctx.decode_steps(0, q, kn, vn, w.tau, w.budget, out, boundary=bnd)
+        ctx.decode_steps(0, q, kn, vn, w.tau, w.budget, out, n_layers=NL, boundary=bnd)
 
     ev["mid"] = torch.cuda.Event(enable_timing=True)
     for _ in range(args.warmup):
@@ -293,17 +299,18 @@ def run_ours(args, rank, world, local):
     build_ms, dec_ms, wall_ms = max_over_ranks([build_ms, dec_ms, wall * 1e3])
     K_steps = args.steps
     value = world * T * K_steps / (dec_ms / 1e3)
-    mkeys = world * w.batch * w.n_kv_heads * w.n_prefill * w.iters * K_steps / (build_ms / 1e3) / 1e6
+    mkeys = world * NL * w.batch * w.n_kv_heads * w.n_prefill * w.iters * K_steps / (build_ms / 1e3) / 1e6
 
     # ---- roofline pass: single-step launches, L2 overwritten before every
     # step, CUDA events around every kernel on the context stream
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
-    ctx.build_index(0, K, V, w.n_clusters, w.iters, 1)
+    build_all()
     ctx.set_profiling(True)
     ctx.profile(reset=True)
     for t in range(prof_T):
         flush.fill_(float(t))
-        ctx.decode_step(0, q[t], kn[t], vn[t], w.tau, w.budget, out[t], boundary=bnd[t])
+        ctx.decode_step(0, q[t], kn[t], vn[t], w.tau, w.budget, out[t], n_layers=NL,
+                        boundary=bnd[t])
     kern_p, ctr = ctx.profile(reset=True)
     ctx.set_profiling(False)
     hbm_peak, tc_peak, tc_peak_sus, peak_kind = peaks()
@@ -315,6 +322,14 @@ def run_ours(args, rank, world, local):
     achieved = alg_bytes / attn_s / 1e9
     breakdown = {k: {"launches": int(v[0]), "avg_us": round(v[1] / v[0] * 1e3, 2)}
                  for k, v in kern_p.items() if v[0]}
+    uva = None
+    if w.offload:  # rows read from pinned host memory over the host link
+        n_g, ms_g = kern_p["lkv_gather_offload"]
+        g_bytes = ctr["gather_rows"] * 2 * 128 * eb
+        uva = {"kernel": "k_gather_offload", "bytes": g_bytes, "kernel_ms": ms_g, "launches": int(n_g),
+               "achieved_GBps": g_bytes / (ms_g / 1e3) / 1e9 if ms_g > 0 else None,
+               "note": "bytes read over UVA / total event time of every gather launch "
+                       "(launches on steps without retrieval exit at once)"}
 
     # ---- K-means distance contraction on the tensor cores: one build with
     # CUDA events around every kernel (L2 overwritten first; the keys, 537 MB,
@@ -357,6 +372,7 @@ def run_ours(args, rank, world, local):
             "peak_source": f"{peak_kind} bf16_tflops (cuBLAS burst)",
             "flops_per_launch": km_flops, "avg_launch_us": km_s * 1e6, "launches": int(n_km)},
         "kernel_breakdown_us": breakdown,
+        "uva_gather": uva,
         "build_breakdown_us": build_breakdown,
         "gpu_launches": launches,
         "clocks": clk,
@@ -370,7 +386,7 @@ def run_ours(args, rank, world, local):
         h2d = (q[0].numel() + kn[0].numel() + vn[0].numel()) * eb
         d2h = out[0].numel() * 4
         chunk = 256
-        ctx.build_index(0, K, V, w.n_clusters, w.iters, 1)
+        build_all()
         ctx.sync()
         ea, eb_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         ea.record(stream)
@@ -380,7 +396,7 @@ def run_ours(args, rank, world, local):
             kn[c0:c0 + n].copy_(knh[c0:c0 + n], non_blocking=True)
             vn[c0:c0 + n].copy_(vnh[c0:c0 + n], non_blocking=True)
             ctx.decode_steps(0, q[c0:c0 + n], kn[c0:c0 + n], vn[c0:c0 + n], w.tau, w.budget,
-                             out[c0:c0 + n])
+                             out[c0:c0 + n], n_layers=NL)
             outh[c0:c0 + n].copy_(out[c0:c0 + n], non_blocking=True)
         eb_.record(stream)
         eb_.synchronize()

@@ -631,15 +631,12 @@ __global__ void __launch_bounds__(kScoreThreads, 2) k_score_select(CtxView v, St
 
 // ---------------------------------------------------------------- offload gather
 
-// Largest r with cum[r] <= f (cum ascending, cum[0] = 0, f < cum[n]).
-__device__ __forceinline__ int find_range(const int32_t *cum, int n, int32_t f) {
-  int lo = 0, hi = n - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (__ldg(cum + mid) <= f) lo = mid; else hi = mid - 1;
-  }
-  return lo;
-}
+// On a retrieval step, the selected rows go from the pinned host pool to this
+// plan slot's HBM staging rows over UVA. A warp takes one copy piece of the
+// selection (a contiguous run of <= 64 pool rows, from the selection's piece
+// list) and moves its K and V rows in 16-byte vectors, eight loads in flight
+// per lane, so the host link sees long contiguous reads.
+constexpr int kGatherVec = 8;
 
 template <int DT>
 __global__ void __launch_bounds__(256) k_gather_offload(CtxView v, StepArgs a) {
@@ -653,21 +650,42 @@ __global__ void __launch_bounds__(256) k_gather_offload(CtxView v, StepArgs a) {
   const int4 view = v.aview[(int64_t)a.slot * v.n_lb + lb];
   if (!(view.w & 1)) return;
   const int ps = view.z;
-  const int ns = *plan_nsel(v, ps, gs), nt = *plan_ntok(v, ps, gs);
-  const int32_t *cum = plan_rng_cum(v, ps, gs);
-  const int32_t *rows = plan_rng_row(v, ps, gs);
+  const int nt = *plan_ntok(v, ps, gs);
+  const int nsc = (nt + kAttnChunk - 1) / kAttnChunk;
+  if (nt == 0 || nsc > v.max_chunks) return;
+  const int npieces = v.chunk_piece[gs * (int64_t)(v.max_chunks + 1) + nsc];
+  const int4 *pieces = v.pieces + gs * (int64_t)v.max_pieces;
   constexpr int rb = kHeadDim * elem_bytes<DT>();
   constexpr int per_row = rb / 16;
   const int lane = threadIdx.x & 31;
   const int warps = gridDim.y * (blockDim.x / 32);
-  for (int f = blockIdx.y * (blockDim.x / 32) + threadIdx.x / 32; f < nt; f += warps) {
-    const int r = find_range(cum, ns, f);
-    const int64_t row = rows[r] + (f - cum[r]);
-    if (lane < per_row) {
-      const int64_t src = (gs * v.pool_rows + row) * rb + lane * 16;
-      const int64_t dst = (((int64_t)ps * v.S_all + gs) * v.bud_cap + f) * rb + lane * 16;
-      *(uint4 *)((char *)v.stage_k + dst) = __ldcg((const uint4 *)((const char *)v.pool_k + src));
-      *(uint4 *)((char *)v.stage_v + dst) = __ldcg((const uint4 *)((const char *)v.pool_v + src));
+  const uint4 *src_k = (const uint4 *)((const char *)v.pool_k + gs * v.pool_rows * rb);
+  const uint4 *src_v = (const uint4 *)((const char *)v.pool_v + gs * v.pool_rows * rb);
+  uint4 *dst_k = (uint4 *)((char *)v.stage_k + ((int64_t)ps * v.S_all + gs) * v.bud_cap * rb);
+  uint4 *dst_v = (uint4 *)((char *)v.stage_v + ((int64_t)ps * v.S_all + gs) * v.bud_cap * rb);
+  for (int p = blockIdx.y * (blockDim.x / 32) + threadIdx.x / 32; p < npieces; p += warps) {
+    const int4 pc = pieces[p];  // (first pool row, first selected token, rows)
+    const int nvec = pc.z * per_row;
+    const uint4 *sk = src_k + (int64_t)pc.x * per_row, *sv = src_v + (int64_t)pc.x * per_row;
+    uint4 *dk = dst_k + (int64_t)pc.y * per_row, *dv = dst_v + (int64_t)pc.y * per_row;
+    for (int x0 = 0; x0 < nvec; x0 += 32 * kGatherVec) {
+      uint4 rk[kGatherVec], rv[kGatherVec];
+#pragma unroll
+      for (int e = 0; e < kGatherVec; ++e) {
+        const int x = x0 + e * 32 + lane;
+        if (x < nvec) {
+          rk[e] = __ldcg(sk + x);
+          rv[e] = __ldcg(sv + x);
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < kGatherVec; ++e) {
+        const int x = x0 + e * 32 + lane;
+        if (x < nvec) {
+          dk[x] = rk[e];
+          dv[x] = rv[e];
+        }
+      }
     }
   }
   if (blockIdx.y == 0 && threadIdx.x == 0)
