@@ -1289,7 +1289,7 @@ static cudaError_t decode_t(const CtxView &v, const StepArgs &a, cudaStream_t st
   prof.end(ss);
   if (v.offload) {
     prof.begin(kPGather, ss);
-    launch_pdl(k_gather_offload<DT>, dim3(slices, 16), dim3(256), 0, ss, v, a);
+    launch_pdl(k_gather_offload<DT>, dim3(slices, 64), dim3(256), 0, ss, v, a);
     prof.end(ss);
   }
   const int nch = (a.budget + v.L + kAttnChunk - 1) / kAttnChunk;
