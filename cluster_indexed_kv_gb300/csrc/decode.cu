@@ -15,6 +15,7 @@
 //
 // Inputs/outputs of step k of a call live at base + k * stride (StepArgs).
 #include <cstdlib>
+#include <type_traits>
 
 #include "lkv_internal.cuh"
 
@@ -775,6 +776,30 @@ __device__ __forceinline__ float reduce_heads(float (&x)[G], int lane) {
   }
 }
 
+// The same reduction when lane k holds its partials in the permuted head
+// order x[j] = head (head_of_lane(k) ^ j): the half a lane keeps is then
+// always x[0..N) and the half it sends x[N..2N), so no selects are needed.
+template <int G>
+__device__ __forceinline__ float reduce_heads_perm(float (&x)[G]) {
+  if constexpr (G >= 8) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) x[j] += __shfl_xor_sync(kFull, x[j + 4], 8);
+  }
+  if constexpr (G >= 4) {
+    constexpr int m = G >= 8 ? 4 : 8;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) x[j] += __shfl_xor_sync(kFull, x[j + 2], m);
+  }
+  if constexpr (G >= 2) {
+    constexpr int m = G >= 8 ? 2 : (G >= 4 ? 4 : 8);
+    x[0] += __shfl_xor_sync(kFull, x[1], m);
+  }
+  float r = x[0];
+#pragma unroll
+  for (int m = 16 / (2 * G); m >= 1; m >>= 1) r += __shfl_xor_sync(kFull, r, m);
+  return r;
+}
+
 template <int G>
 __device__ __forceinline__ int head_of_lane(int k) {
   if constexpr (G == 8) return ((k >> 3) & 1) * 4 + ((k >> 2) & 1) * 2 + ((k >> 1) & 1);
@@ -786,33 +811,15 @@ __device__ __forceinline__ int head_of_lane(int k) {
 template <int DT>
 constexpr int stage_bytes() { return 2 * kAttnChunk * kHeadDim * elem_bytes<DT>(); }
 
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// Load a float from the shared memory of CTA `rank` of this cluster, at the
-// address that p has in this CTA.
-__device__ __forceinline__ float ld_dsmem(const float *p, uint32_t rank) {
-  uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(p)), "r"(rank));
-  float x;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(x) : "r"(remote) : "memory");
-  return x;
-}
 
-constexpr int kMaxSplit = 8;  // CTAs per slice = thread-block cluster size (portable maximum)
-
-// Split-K attention. The nsplit CTAs of a (seq, layer, kv head) form one
-// thread-block cluster; CTA split streams chunks [split * cpc, ...) of the
-// slice's token list (selected rows, then the local buffer) through a 3-stage
-// ring of shared-memory buffers filled by bulk copies. Per chunk, each of the
-// 8 warps owns 8 rows: pass 1 scores them (16 lanes per row, 2 rows per
-// instruction), pass 2 adds p * V into per-lane accumulators. The CTAs'
-// partial softmax states meet in CTA 0 through distributed shared memory.
+// Split-K attention. CTA split of the nsplit CTAs of a (seq, layer, kv head)
+// streams chunks [split * cpc, ...) of the slice's token list (selected rows,
+// then the local buffer) through a 3-stage ring of shared-memory buffers
+// filled by bulk copies. Per chunk, each of the 8 warps owns 8 rows: pass 1
+// scores them (16 lanes per row, 2 rows per instruction), pass 2 adds p * V
+// into per-lane accumulators. The CTAs' partial softmax states go to a
+// per-step-slot scratch and the last CTA to finish combines them, so no CTA
+// waits for another.
 template <int DT, int G>
 __global__ void __launch_bounds__(kAttnThreads, 2) k_attn(CtxView v, StepArgs a, int cpc) {
   constexpr int RB = kHeadDim * elem_bytes<DT>();
@@ -825,9 +832,10 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn(CtxView v, StepArgs a,
   __shared__ int4 pcs[kPreChunks][kAttnChunk];
   __shared__ int pcn[kPreChunks];
   __shared__ int done_cnt[kStages];  // warps finished with the chunk in each stage
-  __shared__ float part_m[G], part_l[G], part_acc[G][kHeadDim];  // this CTA's partial
+  // this CTA's partial: acc [G][d], then the maxima [G] and sums [G]
+  __shared__ float part[G * kHeadDim + 2 * G];
   __shared__ int4 s_view;  // (t, win_start, plan slot, 0) of this step
-  __shared__ int s_nt, s_ns, s_ok;
+  __shared__ int s_nt, s_ns, s_ok, s_last;
 
   const int per_l = v.B * v.Hkv;
   const int li = blockIdx.x / per_l, rem = blockIdx.x % per_l;
@@ -942,13 +950,15 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn(CtxView v, StepArgs a,
   if (wid == 0)
     for (int i = 0; i < min(n_my, kStages); ++i) issue(i);
 
+  const int hl = head_of_lane<G>(kk);  // head whose score this lane ends with
+  // this lane's query slices in the permuted head order hl ^ j (see
+  // reduce_heads_perm)
   float2 q2[G][4];
 #pragma unroll
-  for (int g = 0; g < G; ++g)
+  for (int j = 0; j < G; ++j)
 #pragma unroll
-    for (int p = 0; p < 4; ++p) q2[g][p] = make_float2(qs[g][8 * kk + 2 * p], qs[g][8 * kk + 2 * p + 1]);
-
-  const int hl = head_of_lane<G>(kk);  // head whose score this lane ends with
+    for (int p = 0; p < 4; ++p)
+      q2[j][p] = make_float2(qs[hl ^ j][8 * kk + 2 * p], qs[hl ^ j][8 * kk + 2 * p + 1]);
   float m_run[G];
 #pragma unroll
   for (int g = 0; g < G; ++g) m_run[g] = -INFINITY;
@@ -970,24 +980,30 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn(CtxView v, StepArgs a,
       mbar_wait_bounded(&bar[i % kStages], (i / kStages) & 1, kWaitLimitNs);
     }
     const int nrow = min(kAttnChunk, total - (c_begin + i) * kAttnChunk);
-    // pass 1: scores of this warp's 8 rows, 2 rows per instruction
+    // pass 1: scores of this warp's 8 rows, 2 rows per instruction (rows past
+    // the chunk's end, in a slice's last chunk only, score -inf)
+    const bool full = r0 + kRowsPerWarp <= nrow;  // (warp-uniform)
+    auto pass1 = [&](auto check) {
 #pragma unroll
-    for (int it = 0; it < kRowsPerWarp / 2; ++it) {
-      const int r = r0 + it * 2 + grp;
-      float2 kv[4];
-      row8<DT>(Ks + r * RB, kk, kv);
-      float part[G];
+      for (int it = 0; it < kRowsPerWarp / 2; ++it) {
+        const int r = r0 + it * 2 + grp;
+        float2 kv[4];
+        row8<DT>(Ks + r * RB, kk, kv);
+        float part[G];
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        float2 s2 = make_float2(0.f, 0.f);
+        for (int j = 0; j < G; ++j) {
+          float2 s2 = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int p = 0; p < 4; ++p) s2 = ffma2(q2[g][p], kv[p], s2);
-        part[g] = s2.x + s2.y;
+          for (int p = 0; p < 4; ++p) s2 = ffma2(q2[j][p], kv[p], s2);
+          part[j] = s2.x + s2.y;
+        }
+        float s = reduce_heads_perm<G>(part);
+        if (decltype(check)::value && r >= nrow) s = -INFINITY;
+        if ((kk & (16 / G - 1)) == 0) S[r][hl] = s;
       }
-      float s = reduce_heads<G>(part, lane);
-      if (r >= nrow) s = -INFINITY;
-      if ((kk & (16 / G - 1)) == 0) S[r][hl] = s;
-    }
+    };
+    if (full) pass1(std::false_type{});
+    else pass1(std::true_type{});
     __syncwarp();
     // chunk maximum per head over the warp's rows, softmax weights in place
     float mx = -INFINITY;
@@ -1027,23 +1043,27 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn(CtxView v, StepArgs a,
         for (int p = 0; p < 4; ++p) acc[g][p] = fmul2(acc[g][p], c2);
       }
     }
+    auto pass2 = [&](auto check) {
 #pragma unroll
-    for (int it = 0; it < kRowsPerWarp / 2; ++it) {
-      const int r = r0 + it * 2 + grp;
-      float2 vv[4];
-      row8<DT>(Vs + r * RB, kk, vv);
-      if (r >= nrow) {
+      for (int it = 0; it < kRowsPerWarp / 2; ++it) {
+        const int r = r0 + it * 2 + grp;
+        float2 vv[4];
+        row8<DT>(Vs + r * RB, kk, vv);
+        if (decltype(check)::value && r >= nrow) {
 #pragma unroll
-        for (int p = 0; p < 4; ++p) vv[p] = make_float2(0.f, 0.f);  // unwritten shared memory
+          for (int p = 0; p < 4; ++p) vv[p] = make_float2(0.f, 0.f);  // unwritten shared memory
+        }
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float pg = S[r][g];
+          const float2 p2 = make_float2(pg, pg);
+#pragma unroll
+          for (int p = 0; p < 4; ++p) acc[g][p] = ffma2(p2, vv[p], acc[g][p]);
+        }
       }
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const float pg = S[r][g];
-        const float2 p2 = make_float2(pg, pg);
-#pragma unroll
-        for (int p = 0; p < 4; ++p) acc[g][p] = ffma2(p2, vv[p], acc[g][p]);
-      }
-    }
+    };
+    if (full) pass2(std::false_type{});
+    else pass2(std::true_type{});
     // this warp is done with the stage; the last warp to finish refills it
     // with chunk i + kStages (no block-wide barrier: warps run ahead freely)
     __syncwarp();
@@ -1103,55 +1123,66 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn(CtxView v, StepArgs a,
       o = fmaf(sw, wacc[w][g][dim], o);
       z = fmaf(sw, wl[w][g], z);
     }
-    part_acc[g][dim] = o;
+    part[g * kHeadDim + dim] = o;
     if (dim == 0) {
-      part_m[g] = mm;
-      part_l[g] = z;
+      part[G * kHeadDim + g] = mm;
+      part[G * kHeadDim + G + g] = z;
     }
   }
-  // every CTA of the cluster combines its share of the outputs from all
-  // CTAs' partials (read through distributed shared memory); the second
-  // cluster barrier keeps each CTA's shared memory alive until all are done
-  cluster_sync();
+  // the last CTA of the slice to finish combines every CTA's partial (through
+  // a per-step-slot scratch in global memory); the others leave at once
+  const int64_t so = ((int64_t)b * a.nl + li) * v.Hkv + h;
+  constexpr int kPart = G * kHeadDim + 2 * G;
+  __syncthreads();  // the partial is complete
+  const float *parts = part;
+  bool combine = true;
+  if (nsplit > 1) {
+    float *gp = v.attn_part + (((int64_t)a.slot * v.S_all + gs) * kAttnMaxSplit + split) * kPart;
+    for (int x = tid; x < kPart; x += kAttnThreads) gp[x] = part[x];
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_last = atomicAdd(&v.attn_count[(int64_t)a.slot * v.S_all + gs], 1) == nsplit - 1;
+    __syncthreads();
+    combine = s_last;
+    if (combine) __threadfence();
+    parts = v.attn_part + ((int64_t)a.slot * v.S_all + gs) * kAttnMaxSplit * kPart;
+  }
+  if (!combine) return;
   {
-    const int rank = (int)cluster_rank();
     float *out = a.out + k * a.stride_out;
     const int64_t obase = (((int64_t)b * a.nl + li) * H + (int64_t)h * G) * kHeadDim;
-    const int per = (G * kHeadDim + nsplit - 1) / nsplit;
-    const int x1 = min(G * kHeadDim, (rank + 1) * per);
-    for (int x = rank * per + tid; x < x1; x += kAttnThreads) {
-      const int g = x / kHeadDim, dim = x % kHeadDim;
-      float mc[kMaxSplit];
+    for (int x = tid; x < G * kHeadDim; x += kAttnThreads) {
+      const int g = x / kHeadDim;
+      float mc[kAttnMaxSplit];
       float mm = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < kMaxSplit; ++c) {
-        mc[c] = (c < nsplit) ? ld_dsmem(&part_m[g], c) : -INFINITY;
+      for (int c = 0; c < kAttnMaxSplit; ++c) {
+        mc[c] = (c < nsplit) ? parts[c * kPart + G * kHeadDim + g] : -INFINITY;
         mm = fmaxf(mm, mc[c]);
       }
       float o = 0.f, z = 0.f;
 #pragma unroll
-      for (int c = 0; c < kMaxSplit; ++c) {
+      for (int c = 0; c < kAttnMaxSplit; ++c) {
         if (c >= nsplit || mc[c] == -INFINITY) continue;
         const float sw = exp2f(mc[c] - mm);
-        o = fmaf(sw, ld_dsmem(&part_acc[g][dim], c), o);
-        z = fmaf(sw, ld_dsmem(&part_l[g], c), z);
+        o = fmaf(sw, parts[c * kPart + x], o);
+        z = fmaf(sw, parts[c * kPart + G * kHeadDim + G + g], z);
       }
       out[obase + x] = o / z;
     }
-    const int64_t so = ((int64_t)b * a.nl + li) * v.Hkv + h;
     const int ns = s_ns;
     if (a.selected_units) {
       const int32_t *sel = plan_sel(v, ps, gs);
       int32_t *dst = a.selected_units + k * a.stride_sel + so * v.u_cap;
-      for (int x = rank * kAttnThreads + tid; x < ns; x += nsplit * kAttnThreads) dst[x] = sel[x];
+      for (int x = tid; x < ns; x += kAttnThreads) dst[x] = sel[x];
     }
-    if (rank == 0 && tid == 0) {
+    if (tid == 0) {
+      if (nsplit > 1) v.attn_count[(int64_t)a.slot * v.S_all + gs] = 0;
       if (a.n_selected) a.n_selected[k * a.stride_nsel + so] = ns;
       atomicAdd((unsigned long long *)&v.counters[kCntAttnRows], (unsigned long long)total);
       atomicAdd((unsigned long long *)&v.counters[kCntAttnSlices], 1ull);
     }
   }
-  cluster_sync();
 }
 
 // ---------------------------------------------------------------- host
@@ -1188,13 +1219,13 @@ static int g_attn_slots = 2 * 152;  // resident attention CTAs on the device
 static int g_attn_split = 0;        // CTAs per slice forced by LKV_ATTN_CTAS_PER_SLICE (0: auto)
 constexpr int kAttnConcurrent = 2;  // pipelined attention grids sized to run this many at once
 
-// Split of a slice's chunks over the CTAs of one cluster (at most kMaxSplit):
+// Split of a slice's chunks over at most kAttnMaxSplit CTAs:
 // `concurrent` grids (consecutive steps of a pipelined graph, else 1) are
 // resident at once where possible.
 static void attn_split(int slices, int nch, int concurrent, int *nsplit, int *cpc) {
   int want = g_attn_split > 0 ? g_attn_split : g_attn_slots / (slices * concurrent);
   if (want < 1) want = 1;
-  if (want > kMaxSplit) want = kMaxSplit;
+  if (want > kAttnMaxSplit) want = kAttnMaxSplit;
   if (want > nch) want = nch;
   *cpc = (nch + want - 1) / want;
   *nsplit = (nch + *cpc - 1) / *cpc;
@@ -1210,17 +1241,13 @@ static void launch_attn(const CtxView &v, const StepArgs &a, int slices, int nch
   cfg.blockDim = dim3(kAttnThreads);
   cfg.dynamicSmemBytes = attn_smem<DT, G>();
   cfg.stream = st;
-  cudaLaunchAttribute attr[3];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
-  attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = 1;
-  attr[1].val.clusterDim.y = nsplit;
-  attr[1].val.clusterDim.z = 1;
-  attr[2].id = cudaLaunchAttributePriority;
-  attr[2].val.priority = g_prio_attn;
+  attr[1].id = cudaLaunchAttributePriority;
+  attr[1].val.priority = g_prio_attn;
   cfg.attrs = attr;
-  cfg.numAttrs = 3;
+  cfg.numAttrs = 2;
   cudaLaunchKernelEx(&cfg, k_attn<DT, G>, v, a, cpc);
 }
 
@@ -1242,7 +1269,7 @@ static cudaError_t prep_attn() {
   }
   if (const char *env = getenv("LKV_ATTN_CTAS_PER_SLICE")) {
     const int x = atoi(env);
-    g_attn_split = (x >= 1 && x <= kMaxSplit) ? x : 0;
+    g_attn_split = (x >= 1 && x <= kAttnMaxSplit) ? x : 0;
   }
   return cudaFuncSetAttribute(k_step_boundary<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)(2 * kMaxHeads * kQPitch * sizeof(float)));

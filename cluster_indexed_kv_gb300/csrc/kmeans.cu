@@ -1193,7 +1193,7 @@ __global__ void k_reset_layer(CtxView v, int layer, int32_t c) {
         *plan_ntok(v, p, gs) = 0;
         plan_rng_cum(v, p, gs)[0] = 0;
       }
-      v.attn_count[gs] = 0;
+      for (int p = 0; p < kRing; ++p) v.attn_count[p * v.S_all + gs] = 0;
       v.score_count[gs] = 0;
     }
   }

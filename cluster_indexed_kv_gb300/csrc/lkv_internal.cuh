@@ -15,6 +15,7 @@ constexpr int kMaxGroup = 8;
 constexpr int kMaxParts = 64;      // token parts of the stable counting sort
 constexpr int kAttnChunk = 64;     // tokens per attention work item
 constexpr int kRing = 4;           // steps whose attention may be in flight at once
+constexpr int kAttnMaxSplit = 8;   // CTAs per slice in one attention launch, at most
 
 // Error bits recorded on the device and reported by lkv_sync.
 enum : int32_t {
@@ -84,7 +85,8 @@ struct CtxView {
   int4 *chunk_pieces;         // [kRing][slice][max_chunks][64] the pieces of each chunk
   int32_t *chunk_count;       // [kRing][slice][max_chunks] pieces in each chunk
   int32_t max_pieces;
-  int32_t *attn_count;        // [slice]
+  int32_t *attn_count;        // [kRing step slots][slice] attention CTAs done (last one combines)
+  float *attn_part;           // [kRing][slice][kAttnMaxSplit][G * d + 2 * G] CTA partials
   int32_t *score_count;       // [slice] score CTAs done this step (last one selects)
   int32_t max_chunks;
   int32_t *err;               // device error bits (shared by all layers)
