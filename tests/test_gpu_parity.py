@@ -240,6 +240,44 @@ def test_decode_steps_graph_matches_single_steps():
     assert outs[0][1].sum() > 3
 
 
+def test_graph_with_every_step_retrieving():
+    """tau > 1: every step retrieves, so the pipelined graph advances the
+    selection-plan slot at every step and the ring of in-flight attentions
+    is always full of distinct plans; the result must still equal the
+    oracle step for step."""
+    w = synth.WORKLOADS["long_out"].replace(batch=2, n_kv_heads=2, n_prefill=900, n_components=30,
+                                            n_clusters=30, iters=3, local_buf=24, budget=160,
+                                            jump_p=0.05)
+    T = 150
+    K, V = synth.prefill(w, 0, "cuda")
+    q, kn, vn, _ = synth.decode_inputs(w, "cuda", n_steps=T)
+    ctx = H.make_ctx(w, max_steps=T)
+    ctx.build_index(0, K, V, w.n_clusters, w.iters, 4)
+    idx = {b: [ctx.get_index(0, b, h, w.n_prefill) for h in range(w.n_kv_heads)] for b in range(w.batch)}
+    out = torch.zeros(T, w.batch, 1, w.n_heads, 128, device="cuda")
+    bnd = torch.zeros(T, w.batch, 1, dtype=torch.uint8, device="cuda")
+    nsel = torch.zeros(T, w.batch, 1, w.n_kv_heads, dtype=torch.int32, device="cuda")
+    sel = torch.full((T, w.batch, 1, w.n_kv_heads, ctx.u_cap), -1, dtype=torch.int32, device="cuda")
+    ctx.decode_steps(0, q, kn, vn, 2.0, w.budget, out, boundary=bnd, n_selected=nsel,
+                     selected_units=sel)
+    ctx.sync()
+    g = dict(out=out.cpu().numpy(), boundary=bnd.cpu().numpy(), r=np.zeros((T, w.batch, 1), np.float32),
+             n_sel=nsel.cpu().numpy(), sel={})
+    sel_h = sel.cpu().numpy()
+    assert g["boundary"].all()
+    for b in range(w.batch):
+        o = H.oracle_decode(w, K, V, idx[b], q, kn, vn, b, 0, tau=2.0)
+        assert np.array_equal(g["boundary"][:, b, 0], o["flag"])
+        assert np.array_equal(g["n_sel"][:, b, 0], o["n_sel"])
+        for t in range(T):
+            for h in range(w.n_kv_heads):
+                k = o["n_sel"][t, h]
+                assert np.array_equal(np.sort(sel_h[t, b, 0, h, :k]), np.sort(o["sel"][t, h, :k]))
+        err = np.abs(g["out"][:, b, 0].astype(np.float64) - o["out"])
+        assert (err <= H.ATOL + H.RTOL * np.abs(o["out"])).all(), err.max()
+    ctx.close()
+
+
 def test_profile_counters_and_launch_counts():
     w = synth.WORKLOADS["long_in"].replace(batch=2, n_kv_heads=2, n_prefill=500, n_components=20,
                                            n_clusters=20, iters=2, local_buf=8, budget=100)
