@@ -565,7 +565,9 @@ __device__ void select_units(const CtxView &v, int64_t gs, int U, int budget, in
     for (int p = tid; p < s_npieces; p += nth) {
       const int4 pc = pieces[p];
       const int c = pc.y / kAttnChunk;
-      plan_chunk_pieces(v, ps, gs)[c * kAttnChunk + (p - cp[c])] = pc;
+      int4 q = pc;
+      if (p == cp[c]) q.w = cp[c + 1] - cp[c];  // the chunk's piece count rides on its first piece
+      plan_chunk_pieces(v, ps, gs)[c * kAttnChunk + (p - cp[c])] = q;
     }
     for (int c = tid; c < nsc; c += nth)
       plan_chunk_count(v, ps, gs)[c] = cp[c + 1] - cp[c];
@@ -829,8 +831,9 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn(CtxView v, StepArgs a,
   __shared__ float qs[G][kHeadDim];
   __shared__ __align__(16) float S[kAttnChunk][G];
   __shared__ float wm[kAttnWarps][G], wl[kAttnWarps][G];
-  __shared__ int4 pcs[kPreChunks][kAttnChunk];
+  __shared__ __align__(16) int4 pcs[kPreChunks][kAttnChunk];  // copy plans, a ring of slots
   __shared__ int pcn[kPreChunks];
+  __shared__ __align__(8) uint64_t pbar[kPreChunks];  // a plan slot's bulk load landed
   __shared__ int done_cnt[kStages];  // warps finished with the chunk in each stage
   // this CTA's partial: acc [G][d], then the maxima [G] and sums [G]
   __shared__ float part[G * kHeadDim + 2 * G];
@@ -860,6 +863,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn(CtxView v, StepArgs a,
       mbar_init(&bar[i], 1);
       done_cnt[i] = 0;
     }
+    for (int i = 0; i < kPreChunks; ++i) mbar_init(&pbar[i], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   for (int x = tid; x < G * kHeadDim; x += kAttnThreads)
@@ -906,15 +910,15 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn(CtxView v, StepArgs a,
     const int nrow = min(kAttnChunk, total - f0);
     int np = 0, sel_direct = 0;
     const int4 *pieces = nullptr;
+    const int slot = i % kPreChunks;
     if (f0 < nt) {
       if (!v.offload) {
-        if (i < kPreChunks) {
-          pieces = pcs[i];
-          np = pcn[i];
-        } else {
-          pieces = plan_pcs + c * kAttnChunk;
-          np = plan_pcn[c];
-        }
+        // chunks past the first kPreChunks: their plan was bulk-loaded into
+        // this slot when the chunk kPreChunks earlier was issued
+        if (i >= kPreChunks && !mbar_wait_bounded(&pbar[slot], ((i / kPreChunks) - 1) & 1, kWaitLimitNs))
+          s_ok = 0;
+        pieces = pcs[slot];
+        np = i < kPreChunks ? pcn[slot] : pcs[slot][0].w;
       } else {
         sel_direct = min(f0 + kAttnChunk, nt) - f0;
       }
@@ -946,9 +950,19 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn(CtxView v, StepArgs a,
                  (uint32_t)(win1 - win0) * RB, br);
       }
     }
+    // the slot's plan is consumed: bring in the plan of chunk i + kPreChunks
+    // (1 KB, its piece count in the first piece) for that chunk's refill
+    const int i2 = i + kPreChunks, c2 = c_begin + i2;
+    if (!v.offload && i2 < n_my && c2 * kAttnChunk < nt && c2 < v.max_chunks) {
+      __syncwarp();
+      if (lane == 0) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_arrive_expect_tx(&pbar[slot], kAttnChunk * sizeof(int4));
+        bulk_g2s(pcs[slot], plan_pcs + (int64_t)c2 * kAttnChunk, kAttnChunk * sizeof(int4), &pbar[slot]);
+      }
+    }
   };
-  if (wid == 0)
-    for (int i = 0; i < min(n_my, kStages); ++i) issue(i);
+  if (wid < min(n_my, kStages)) issue(wid);  // the first stages, one warp each
 
   const int hl = head_of_lane<G>(kk);  // head whose score this lane ends with
   // this lane's query slices in the permuted head order hl ^ j (see
@@ -1065,14 +1079,15 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn(CtxView v, StepArgs a,
     if (full) pass2(std::false_type{});
     else pass2(std::true_type{});
     // this warp is done with the stage; the last warp to finish refills it
-    // with chunk i + kStages (no block-wide barrier: warps run ahead freely)
+    // with chunk i + kStages (no block-wide barrier: warps run ahead freely).
+    // The warp's reads of the stage have returned (their values fed the
+    // arithmetic above), and the refill orders itself after them with the
+    // proxy fence below, so the count needs no memory fence.
     __syncwarp();
     int last = 0;
     if (lane == 0) {
-      __threadfence_block();
       last = atomicAdd(&done_cnt[i % kStages], 1) == kAttnWarps - 1;
       if (last) done_cnt[i % kStages] = 0;
-      __threadfence_block();
     }
     last = __shfl_sync(kFull, last, 0);
     if (last && i + kStages < n_my) {
