@@ -379,7 +379,10 @@ def run_ours(args, rank, world, local):
     }
 
     # ---- end to end through the C ABI with host buffers: every decode step's
-    # inputs come from pinned host memory and its outputs go back to it
+    # inputs come from pinned host memory and its outputs go back to it. The
+    # steps go in chunks of 256; a chunk's host-to-device copy (its own
+    # stream) overlaps the previous chunk's decode, and its device-to-host
+    # copy (a third stream) overlaps the next one.
     if not args.no_e2e:
         qh, knh, vnh = (x.cpu().pin_memory() for x in (q, kn, vn))
         outh = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
@@ -388,17 +391,28 @@ def run_ours(args, rank, world, local):
         chunk = 256
         build_all()
         ctx.sync()
+        torch.cuda.synchronize()
+        s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
         ea, eb_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        ea.record(stream)
-        for c0 in range(0, T, chunk):
+        ea.record(s_in)
+        starts = list(range(0, T, chunk))
+        for c0 in starts:
             n = min(chunk, T - c0)
-            q[c0:c0 + n].copy_(qh[c0:c0 + n], non_blocking=True)
-            kn[c0:c0 + n].copy_(knh[c0:c0 + n], non_blocking=True)
-            vn[c0:c0 + n].copy_(vnh[c0:c0 + n], non_blocking=True)
+            with torch.cuda.stream(s_in):
+                q[c0:c0 + n].copy_(qh[c0:c0 + n], non_blocking=True)
+                kn[c0:c0 + n].copy_(knh[c0:c0 + n], non_blocking=True)
+                vn[c0:c0 + n].copy_(vnh[c0:c0 + n], non_blocking=True)
+                inputs_in = torch.cuda.Event()
+                inputs_in.record(s_in)
+            stream.wait_event(inputs_in)
             ctx.decode_steps(0, q[c0:c0 + n], kn[c0:c0 + n], vn[c0:c0 + n], w.tau, w.budget,
                              out[c0:c0 + n], n_layers=NL)
-            outh[c0:c0 + n].copy_(out[c0:c0 + n], non_blocking=True)
-        eb_.record(stream)
+            decoded = torch.cuda.Event()
+            decoded.record(stream)
+            s_out.wait_event(decoded)
+            with torch.cuda.stream(s_out):
+                outh[c0:c0 + n].copy_(out[c0:c0 + n], non_blocking=True)
+        eb_.record(s_out)
         eb_.synchronize()
         result["e2e"] = {"value": world * T / (ea.elapsed_time(eb_) / 1e3), "unit": UNIT,
                          "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
