@@ -460,6 +460,12 @@ __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
 __device__ __forceinline__ float pack6(float e, uint32_t local) {
   return __uint_as_float((__float_as_uint(e) & 0xFFFFFFC0u) | local);
 }
+// The same bits computed with integer multiplies, (e >> 6) * 64 + local, with
+// the multipliers 2^26 and 64 passed in at run time: the epilogue's min/max
+// network saturates the ALU pipe, and multiplies issue on the FMA pipe.
+__device__ __forceinline__ float pack6_mul(float e, uint32_t local, uint32_t m26, uint32_t m64) {
+  return __uint_as_float(__umulhi(__float_as_uint(e), m26) * m64 + local);
+}
 __device__ __forceinline__ float min3f(float a, float b, float c) {
   float d;
   asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
@@ -508,7 +514,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 k_assign_tc(const __grid_constant__ CUtensorMap keys_map, const __grid_constant__ CUtensorMap cent_map,
             int64_t n, int32_t c, int32_t u_cap, const float *c2, int32_t c2_pitch, const float *knorm,
             int64_t n_cap, const float *cstat, float eps, int32_t *assign, int64_t gs0, int n_slices,
-            int4 *amb, int32_t *amb_count, int32_t *amb_crowd, int32_t amb_cap, int32_t *err) {
+            int4 *amb, int32_t *amb_count, int32_t *amb_crowd, int32_t amb_cap, int32_t *err,
+            uint32_t m26, uint32_t m64) {
   extern __shared__ unsigned char tc_smem_raw[];
   __shared__ __align__(8) uint64_t a_full[2], a_empty[2], b_full[2], b_empty[2], acc_full[2], acc_empty[2];
   __shared__ __align__(8) uint64_t mma_done;
@@ -647,8 +654,8 @@ k_assign_tc(const __grid_constant__ CUtensorMap keys_map, const __grid_constant_
                                    make_float2(__uint_as_float(r[4 * e + 2]), __uint_as_float(r[4 * e + 3])),
                                    make_float2(cc[e].z, cc[e].w));
             const uint32_t l0 = g * 32 + 4 * e;
-            top3_pair(p1, p2, p3, pack6(lo.x, l0), pack6(lo.y, l0 + 1));
-            top3_pair(p1, p2, p3, pack6(hi.x, l0 + 2), pack6(hi.y, l0 + 3));
+            top3_pair(p1, p2, p3, pack6_mul(lo.x, l0, m26, m64), pack6_mul(lo.y, l0 + 1, m26, m64));
+            top3_pair(p1, p2, p3, pack6_mul(hi.x, l0 + 2, m26, m64), pack6_mul(hi.y, l0 + 3, m26, m64));
           }
         }
         tc_fence_before();
@@ -1288,7 +1295,7 @@ static cudaError_t kmeans_build_t(const CtxView &v, int layer, const KmeansScrat
       k_assign_tc<<<tc_grid, kTcThreads, kTcSmem, st>>>(keys_map, cent_map, n, c, v.u_cap, ks.c2, ks.c2_pitch,
                                                         ks.knorm, v.n_cap, ks.cstat, kTcEps, v.assign,
                                                         gs0, S, ks.amb, ks.amb_count, ks.amb_count + 1,
-                                                        (int32_t)amb_cap, v.err);
+                                                        (int32_t)amb_cap, v.err, 1u << 26, 64u);
     } else {
       k_assign_simt<DT><<<dim3((unsigned)((n + kAsTile - 1) / kAsTile), S), kAsThreads, kAsSmem, st>>>(
           keys, n, c, v.cent_op, v.u_cap, ks.c2, ks.c2_pitch, ks.knorm, v.n_cap, ks.cstat, eps,
