@@ -165,10 +165,15 @@ lkv_status lkv_decode_step(lkv_ctx *ctx, int32_t layer, int32_t n_layers,
  *   [n_steps][B][n_layers][H_kv][max_clusters + max_steps], n_selected
  *   [n_steps][B][n_layers][H_kv], boundary and r_out [n_steps][B][n_layers].
  * The steps run from a captured CUDA graph of 64 steps (cached per argument
- * set), so the host issues one launch per 64 steps; with profiling enabled
- * (lkv_set_profiling) they are launched one kernel at a time instead. All
- * layers of the call must have taken the same number of steps (LKV_EINVAL).
- * Errors as lkv_decode_step. */
+ * set), so the host issues one launch per 64 steps. Inside the graph the
+ * attention of a step runs concurrently with the boundary tests and
+ * selections of up to four following steps (they never read what it writes);
+ * the boundary flags, r_t and selections are those of lkv_decode_step, and
+ * the attention outputs agree with it within fp32 rounding (the grid over
+ * which a slice's partial softmax sums are split can differ). With profiling
+ * enabled (lkv_set_profiling) the steps are launched one kernel at a time
+ * instead. All layers of the call must have taken the same number of steps
+ * (LKV_EINVAL). Errors as lkv_decode_step. */
 lkv_status lkv_decode_steps(lkv_ctx *ctx, int32_t layer, int32_t n_layers,
                             int32_t n_steps, const void *q, const void *k_new,
                             const void *v_new, float tau, int32_t budget,
