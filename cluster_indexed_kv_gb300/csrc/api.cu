@@ -1,5 +1,6 @@
 // api.cu -- the C ABI of liblkv (declared in include/lkv.h): context
 // allocation, argument checks, stream-ordered launches, blocking queries.
+#include <algorithm>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -176,6 +177,9 @@ lkv_status lkv_create(const lkv_config *cfg, lkv_ctx **out) {
   v.B = B; v.Hkv = Hkv; v.G = G; v.d = d; v.L = k.local_buf;
   v.n_cap = n_cap; v.t_cap = t_cap; v.u_cap = u_cap; v.bud_cap = k.max_budget;
   v.offload = k.offload ? 1 : 0;
+  // the tensor-core attention (bf16, 4 or 8 query heads per KV head) reads
+  // the per-token rows; the pieces serve the host gather and the scalar attention
+  v.need_pieces = (v.offload || !(k.dtype == 1 && (G == 4 || G == 8))) ? 1 : 0;
   v.S_all = S_all;
   v.n_lb = (int32_t)LB;
   v.pool_rows = pool_rows;
@@ -214,6 +218,8 @@ lkv_status lkv_create(const lkv_config *cfg, lkv_ctx **out) {
   v.n_tok = (int32_t *)dalloc(c, lkv::kRing * S_all * 4, &st);
   v.rng_row = (int32_t *)dalloc(c, lkv::kRing * S_all * u_cap * 4, &st);
   v.rng_cum = (int32_t *)dalloc(c, lkv::kRing * S_all * (u_cap + 1) * 4, &st);
+  v.sel_cap = (int32_t)std::min<int64_t>(k.max_budget, (int64_t)n_cap + t_cap);
+  if (!k.offload) v.sel_rows = (int32_t *)dalloc(c, lkv::kRing * S_all * (int64_t)v.sel_cap * 4, &st);
   v.max_chunks = max_chunks;
   v.attn_count = (int32_t *)dalloc(c, lkv::kRing * S_all * 4, &st);
   v.attn_part = (float *)dalloc(c, lkv::kRing * S_all * lkv::kAttnMaxSplit *
@@ -388,7 +394,7 @@ static lkv::StepArgs step_args(lkv_ctx *c, int32_t layer, int32_t nl, bool multi
   return a;
 }
 
-static int kernels_per_step(const lkv_ctx *c) { return c->v.offload ? 4 : 3; }
+static int kernels_per_step(const lkv_ctx *c) { return c->v.offload ? 5 : 4; }
 
 lkv_status lkv_decode_step(lkv_ctx *c, int32_t layer, int32_t nl, const void *q,
                            const void *k_new, const void *v_new, float tau, int32_t budget,
@@ -473,7 +479,7 @@ lkv_status lkv_decode_steps(lkv_ctx *c, int32_t layer, int32_t nl, int32_t n_ste
     const int reps = n_steps / kGraphSteps, tail = n_steps % kGraphSteps;
     for (int r = 0; r < reps && e == cudaSuccess; ++r) e = cudaGraphLaunch(exec, c->stream);
     if (e == cudaSuccess && c->prof.counting) {
-      const int kinds[4] = {lkv::kPBoundary, lkv::kPScore, lkv::kPAttn, lkv::kPGather};
+      const int kinds[5] = {lkv::kPBoundary, lkv::kPScore, lkv::kPSelect, lkv::kPAttn, lkv::kPGather};
       for (int k = 0; k < kernels_per_step(c); ++k) c->prof.launches[kinds[k]] += (int64_t)reps * kGraphSteps;
     }
     for (int i = 0; i < tail && e == cudaSuccess; ++i) e = lkv::launch_decode_step(c->v, a, c->stream, c->prof);
@@ -484,9 +490,9 @@ lkv_status lkv_decode_steps(lkv_ctx *c, int32_t layer, int32_t nl, int32_t n_ste
 }
 
 static const char *kKindNames[lkv::kPNum] = {
-    "lkv_boundary", "lkv_score_select", "lkv_gather_offload", "lkv_attn",
+    "lkv_boundary", "lkv_score", "lkv_gather_offload", "lkv_attn",
     "kmeans_init", "kmeans_operand", "kmeans_assign", "kmeans_refine", "kmeans_sort",
-    "kmeans_update", "kmeans_pool", "kmeans_assign_tc"};
+    "kmeans_update", "kmeans_pool", "kmeans_assign_tc", "lkv_select"};
 
 lkv_status lkv_set_kmeans_filter(lkv_ctx *ctx, int32_t filter) {
   if (!ctx) return fail(nullptr, LKV_EINVAL, "null context");

@@ -3,15 +3,15 @@
 //
 //   k_step_boundary  r_t, trigger flag, segment close, local-buffer eviction,
 //                    append of token t                      (1 CTA / (seq, layer))
-//   k_score_select   s_u = qbar . c_u for every unit; the last score CTA of a
-//                    (seq, layer, kv head) then takes the (score desc, id asc)
-//                    budget prefix and writes the copy plan of the selected
-//                    rows in 64-token chunks                 (trigger steps only)
+//   k_score          s_u = qbar . c_u for every unit   (8 CTAs / slice, trigger steps only)
+//   k_select         the (score desc, id asc) budget prefix, the pool row of
+//                    every selected token and the copy pieces of the selected
+//                    rows in 64-token chunks          (1 CTA / slice, trigger steps only)
 //   k_gather_offload selected rows host -> HBM staging (UVA; offload only)
-//   k_attn           split-K softmax attention: each CTA streams a run of
-//                    64-token chunks of (selected rows ++ local buffer) through
-//                    a 3-stage bulk-copy ring; the last CTA of each
-//                    (seq, layer, kv head) combines the partials
+//   k_attn           split-K softmax attention: each CTA takes a run of
+//                    64-token chunks of (selected rows ++ local buffer); the
+//                    last CTA of each (seq, layer, kv head) combines the
+//                    partials
 //
 // Inputs/outputs of step k of a call live at base + k * stride (StepArgs).
 #include <cstdlib>
@@ -385,6 +385,34 @@ __device__ __forceinline__ int32_t block_scan_excl(int32_t x, int32_t *wt, int32
   return r;
 }
 
+// The same for two values at once (one pass of barriers).
+__device__ __forceinline__ int2 block_scan_excl2(int32_t x, int32_t y, int32_t *wt, int32_t *tx,
+                                                 int32_t *ty) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int32_t ix = x, iy = y;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int32_t a = __shfl_up_sync(kFull, ix, o), b = __shfl_up_sync(kFull, iy, o);
+    if (lane >= o) { ix += a; iy += b; }
+  }
+  if (lane == 31) { wt[wid] = ix; wt[32 + wid] = iy; }
+  __syncthreads();
+  if (wid == 0) {
+    int32_t a = lane < nw ? wt[lane] : 0, b = lane < nw ? wt[32 + lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t pa = __shfl_up_sync(kFull, a, o), pb = __shfl_up_sync(kFull, b, o);
+      if (lane >= o) { a += pa; b += pb; }
+    }
+    if (lane < nw) { wt[lane] = a; wt[32 + lane] = b; }
+    if (lane == nw - 1) { *tx = a; *ty = b; }
+  }
+  __syncthreads();
+  const int2 r = make_int2(ix - x + (wid ? wt[wid - 1] : 0), iy - y + (wid ? wt[32 + wid - 1] : 0));
+  __syncthreads();
+  return r;
+}
+
 constexpr int kScoreThreads = 256;
 constexpr int kScoreWarps = kScoreThreads / 32;
 
@@ -395,27 +423,33 @@ constexpr int kScoreWarps = kScoreThreads / 32;
 // while they fit. Output: ascending unit ids, their first rows, the exclusive
 // token prefix, and the copy plan (selected rows cut at 64-token chunk
 // boundaries).
-constexpr int kSelSmemUnits = 4096;  // units whose keys and lengths fit in shared memory
+constexpr int kSelSmemUnits = 4096;  // units whose keys, lengths and rows fit in shared memory
+constexpr size_t kSelSmemBytes = (size_t)kSelSmemUnits * 12;
 
 __device__ void select_units(const CtxView &v, int64_t gs, int U, int budget, int ps) {
   const int tid = threadIdx.x, nth = blockDim.x, wid = tid >> 5;
-  // keys and lengths once into shared memory (fall back to global memory for
-  // very large unit tables)
-  __shared__ uint32_t key_s[kSelSmemUnits];
-  __shared__ int32_t len_s[kSelSmemUnits];
+  // keys, lengths and first pool rows once into shared memory, with all the
+  // loads in flight together (very large unit tables stay in global memory)
+  extern __shared__ __align__(16) uint32_t sel_smem[];
+  uint32_t *key_s = sel_smem;
+  int32_t *len_s = (int32_t *)(sel_smem + kSelSmemUnits);
+  int32_t *row_s = (int32_t *)(sel_smem + 2 * kSelSmemUnits);
   const float *scg = v.scores + gs * v.u_cap;
   const int32_t *lng = v.unit_len + gs * v.u_cap;
+  const int32_t *rwg = v.unit_row + gs * v.u_cap;
   const bool in_smem = U <= kSelSmemUnits;
   if (in_smem)
     for (int u = tid; u < U; u += nth) {
       key_s[u] = desc_key(__ldcg(scg + u));
       len_s[u] = lng[u];
+      row_s[u] = rwg[u];
     }
   __syncthreads();
   auto keyof = [&](int u) -> uint32_t { return in_smem ? key_s[u] : desc_key(__ldcg(scg + u)); };
   auto lenof = [&](int u) -> int32_t { return in_smem ? len_s[u] : lng[u]; };
+  auto rowof = [&](int u) -> int32_t { return in_smem ? row_s[u] : rwg[u]; };
   __shared__ int32_t whist[kScoreWarps][256];
-  __shared__ int32_t wt[32];
+  __shared__ int32_t wt[64];
   __shared__ int32_t s_total, s_below, s_all, s_nsel, s_ntok, s_npieces;
   __shared__ uint32_t s_prefix, s_mask;
 
@@ -505,35 +539,37 @@ __device__ void select_units(const CtxView &v, int64_t gs, int U, int budget, in
     for (int u = u0; u < u1; ++u)
       if (is_sel(u, run)) { ++cnt; toks += lenof(u); }
   }
-  const int32_t cnt_ex = block_scan_excl(cnt, wt, &s_nsel);
-  const int32_t tok_ex = block_scan_excl(toks, wt, &s_ntok);
-  int32_t npc = 0;  // copy pieces of this thread's selected units
+  const int2 ex = block_scan_excl2(cnt, toks, wt, &s_nsel, &s_ntok);
+  const int32_t cnt_ex = ex.x, tok_ex = ex.y;
+  int32_t npc = 0;  // copy pieces of this thread's selected units (when a reader needs them)
   {
     int32_t run = tie_ex, kk = cnt_ex, cum = tok_ex;
     int32_t *sel_out = plan_sel(v, ps, gs);
     int32_t *row_out = plan_rng_row(v, ps, gs);
     int32_t *cum_out = plan_rng_cum(v, ps, gs);
-    const int32_t *rows = v.unit_row + gs * v.u_cap;
+    int32_t *tok_rows = v.offload ? nullptr : plan_sel_rows(v, ps, gs);
     for (int u = u0; u < u1; ++u) {
       if (!is_sel(u, run)) continue;
-      const int32_t len = lenof(u);
+      const int32_t len = lenof(u), row = rowof(u);
       sel_out[kk] = u;
-      row_out[kk] = rows[u];
+      row_out[kk] = row;
       cum_out[kk] = cum;
-      if (len > 0) npc += (cum + len - 1) / kAttnChunk - cum / kAttnChunk + 1;
+      if (tok_rows)  // the pool row of every selected token, in token order
+        for (int32_t j = 0; j < len && cum + j < v.sel_cap; ++j) tok_rows[cum + j] = row + j;
+      if (v.need_pieces && len > 0) npc += (cum + len - 1) / kAttnChunk - cum / kAttnChunk + 1;
       cum += len;
       ++kk;
     }
   }
-  const int32_t pc_ex = block_scan_excl(npc, wt, &s_npieces);
-  {
+  if (tid == 0) s_npieces = 0;
+  const int32_t pc_ex = v.need_pieces ? block_scan_excl(npc, wt, &s_npieces) : 0;
+  if (v.need_pieces) {
     int32_t run = tie_ex, cum = tok_ex, p = pc_ex;
     int4 *pieces = v.pieces + gs * (int64_t)v.max_pieces;
     int32_t *cp = v.chunk_piece + gs * (int64_t)(v.max_chunks + 1);
-    const int32_t *rows = v.unit_row + gs * v.u_cap;
     for (int u = u0; u < u1 && p - pc_ex < npc; ++u) {
       if (!is_sel(u, run)) continue;
-      int32_t len = lenof(u), src = rows[u], f = cum;
+      int32_t len = lenof(u), src = rowof(u), f = cum;
       cum += len;
       while (len > 0) {
         const int32_t room = kAttnChunk - f % kAttnChunk;
@@ -554,12 +590,13 @@ __device__ void select_units(const CtxView &v, int64_t gs, int U, int budget, in
     *plan_ntok(v, ps, gs) = s_ntok;
     plan_rng_cum(v, ps, gs)[s_nsel] = s_ntok;
     if (nsc <= v.max_chunks) v.chunk_piece[gs * (int64_t)(v.max_chunks + 1) + nsc] = s_npieces;
-    if (s_ntok > budget || s_npieces > v.max_pieces || nsc > v.max_chunks) set_err(v.err, kErrInternal);
+    if (s_ntok > budget || s_ntok > v.sel_cap || s_npieces > v.max_pieces || nsc > v.max_chunks)
+      set_err(v.err, kErrInternal);
   }
   __syncthreads();
   // the same pieces, grouped per chunk in fixed 64-slot blocks (a chunk of 64
   // rows has at most 64 pieces) so that the attention reads them in one go
-  if (nsc <= v.max_chunks && s_npieces <= v.max_pieces) {
+  if (v.need_pieces && nsc <= v.max_chunks && s_npieces <= v.max_pieces) {
     const int32_t *cp = v.chunk_piece + gs * (int64_t)(v.max_chunks + 1);
     const int4 *pieces = v.pieces + gs * (int64_t)v.max_pieces;
     for (int p = tid; p < s_npieces; p += nth) {
@@ -574,11 +611,17 @@ __device__ void select_units(const CtxView &v, int64_t gs, int U, int budget, in
   }
 }
 
-// One CTA per (seq, layer, kv head), on retrieval steps only: the score of
-// every unit (a thread per unit at a time, fp32 FMA in index order, the
-// centroid row in one round trip), then the selection by the same block.
+// kScoreSplit CTAs per (seq, layer, kv head), on retrieval steps only: the
+// score of every unit, a thread per unit (fp32 FMA in index order, the
+// centroid row in one round trip), so that the rows of all units are in
+// flight at once. The selection follows in k_select.
+constexpr int kScoreSplit = 16;
+constexpr int kScoreCtaThreads = 128;
+
+// (128 threads with 80 registers each: a CTA fits beside two attention CTAs
+// and a thread keeps its unit's whole centroid row in flight)
 template <int DT>
-__global__ void __launch_bounds__(kScoreThreads, 2) k_score_select(CtxView v, StepArgs a) {
+__global__ void __launch_bounds__(kScoreCtaThreads, 6) k_score(CtxView v, StepArgs a) {
   const int per_l = v.B * v.Hkv;
   const int li = blockIdx.x / per_l, rem = blockIdx.x % per_l;
   const int b = rem / v.Hkv, h = rem % v.Hkv;
@@ -604,11 +647,11 @@ __global__ void __launch_bounds__(kScoreThreads, 2) k_score_select(CtxView v, St
   }
   __syncthreads();
   constexpr int nvec = kHeadDim * elem_bytes<DT>() / 16;  // 16-byte vectors per centroid row
-  for (int u = threadIdx.x; u < U; u += blockDim.x) {
+  for (int u = blockIdx.y * blockDim.x + threadIdx.x; u < U; u += gridDim.y * blockDim.x) {
     const uint4 *row = (const uint4 *)((const char *)v.cent_op + (gs * v.u_cap + u) * kHeadDim * elem_bytes<DT>());
     uint4 raw[nvec];
 #pragma unroll
-    for (int j = 0; j < nvec; ++j) raw[j] = __ldg(row + j);  // the whole row in one round trip
+    for (int j = 0; j < nvec; ++j) raw[j] = __ldg(row + j);
     float s = 0.f;
 #pragma unroll
     for (int j = 0; j < nvec; ++j) {
@@ -626,10 +669,29 @@ __global__ void __launch_bounds__(kScoreThreads, 2) k_score_select(CtxView v, St
     }
     v.scores[gs * v.u_cap + u] = s;
   }
-  __syncthreads();  // the block's score writes are visible to the block
-  select_units(v, gs, U, a.budget, view.z);
-  if (threadIdx.x == 0)
+  if (blockIdx.y == 0 && threadIdx.x == 0)
     atomicAdd((unsigned long long *)&v.counters[kCntScoreUnits], (unsigned long long)U);
+}
+
+// One CTA per (seq, layer, kv head), on retrieval steps only, launched
+// behind the scoring grid (programmatic dependent launch): the budget
+// selection and the copy plan.
+__global__ void __launch_bounds__(kScoreThreads) k_select(CtxView v, StepArgs a) {
+  const int per_l = v.B * v.Hkv;
+  const int li = blockIdx.x / per_l, rem = blockIdx.x % per_l;
+  const int b = rem / v.Hkv, h = rem % v.Hkv;
+  const int64_t lb = (int64_t)(a.l0 + li) * v.B + b;
+  const int64_t gs = lb * v.Hkv + h;
+  // the step view was written before the scoring grid started (stream
+  // order), so a slice without retrieval leaves before the wait
+  const int4 view = v.aview[(int64_t)a.slot * v.n_lb + lb];
+  if (!(view.w & 1)) {
+    pdl_trigger();
+    return;
+  }
+  pdl_wait();  // the scores are complete and visible
+  pdl_trigger();
+  select_units(v, gs, view.w >> 1, a.budget, view.z);
 }
 
 // ---------------------------------------------------------------- offload gather
@@ -697,9 +759,16 @@ __global__ void __launch_bounds__(256) k_gather_offload(CtxView v, StepArgs a) {
 
 // ---------------------------------------------------------------- attention
 
-constexpr int kAttnWarps = 8;
-constexpr int kAttnThreads = kAttnWarps * 32;
-constexpr int kRowsPerWarp = kAttnChunk / kAttnWarps;  // 8 rows of each chunk
+// Two variants of the per-chunk arithmetic. The tensor-core one (bf16 rows,
+// 4 or 8 query heads per KV head) runs 4 warps of 16 rows each; the scalar
+// one (fp32 rows, or 1-2 query heads) 8 warps of 8 rows.
+template <int DT, int G>
+constexpr bool attn_tc() { return DT == 1 && (G == 4 || G == 8); }
+template <int DT, int G>
+constexpr int attn_warps() { return attn_tc<DT, G>() ? 4 : 8; }
+template <int DT, int G>
+constexpr int attn_threads() { return 32 * attn_warps<DT, G>(); }
+constexpr int kRowsPerWarp = 8;  // scalar variant: rows of each chunk per warp
 constexpr int kStages = 3;
 constexpr int kPreChunks = 8;  // chunks whose copy plan a CTA prefetches
 constexpr uint64_t kWaitLimitNs = 2000000000ull;      // 2 s
@@ -717,6 +786,48 @@ __device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
   F2U x{a}, y{b}, r;
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r.u) : "l"(x.u), "l"(y.u));
   return r.f;
+}
+
+// d += A (16 x 16, row-major) * B (16 x 8, column-major), bf16 operands, fp32
+// accumulation. Lane (g = lane / 4, t = lane % 4) holds A rows g and g + 8,
+// columns 2t, 2t + 1, 2t + 8, 2t + 9 (a0: row g, a1: row g + 8, a2/a3 the
+// same rows at columns + 8), B rows 2t, 2t + 1 (b0) and 2t + 8, 2t + 9 (b1)
+// of column g, and D rows g (d0, d1) and g + 8 (d2, d3) at columns 2t, 2t + 1.
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// The bf16 part of x (lo = false) or of its residual x - bf16(x) (lo = true):
+// the two parts sum to x within 2^-17 relative.
+__device__ __forceinline__ uint32_t bf16_part(float x, bool lo) {
+  const __nv_bfloat16 h = __float2bfloat16_rn(x);
+  return lo ? (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x - __bfloat162float(h)))
+            : (uint32_t)__bfloat16_as_ushort(h);
+}
+__device__ __forceinline__ uint32_t bf16_pair(float x0, float x1, bool lo) {
+  return bf16_part(x0, lo) | (bf16_part(x1, lo) << 16);
+}
+__device__ __forceinline__ uint32_t prmt(uint32_t x, uint32_t y, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(x), "r"(y), "r"(sel));
+  return r;
+}
+// 16-byte asynchronous global -> shared copy; n < 16 source bytes are
+// read and the rest zero-filled (n = 0: nothing is read).
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, uint32_t n) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(n)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ uint32_t word(const uint4 &x, int j) {
+  return j == 0 ? x.x : j == 1 ? x.y : j == 2 ? x.z : x.w;
 }
 
 // The 8 consecutive elements [8k, 8k + 8) of a row owned by lane k of a
@@ -817,20 +928,28 @@ constexpr int stage_bytes() { return 2 * kAttnChunk * kHeadDim * elem_bytes<DT>(
 // Split-K attention. CTA split of the nsplit CTAs of a (seq, layer, kv head)
 // streams chunks [split * cpc, ...) of the slice's token list (selected rows,
 // then the local buffer) through a 3-stage ring of shared-memory buffers
-// filled by bulk copies. Per chunk, each of the 8 warps owns 8 rows: pass 1
-// scores them (16 lanes per row, 2 rows per instruction), pass 2 adds p * V
-// into per-lane accumulators. The CTAs' partial softmax states go to a
-// per-step-slot scratch and the last CTA to finish combines them, so no CTA
-// waits for another.
+// filled by bulk copies. Per chunk each warp owns a block of rows: it scores
+// them, updates its online softmax and adds p * V into its accumulators.
+//  - tensor-core variant (bf16 rows, G = 4 or 8): 4 warps of 16 rows. Scores
+//    and p * V are 16x8x16 bf16 products with fp32 accumulation; the queries
+//    and the softmax weights enter as a bf16 high part plus a bf16 residual
+//    (two columns per head), so both keep fp32 accuracy.
+//  - scalar variant: 8 warps of 8 rows; pass 1 scores them (16 lanes per row,
+//    2 rows per instruction), pass 2 adds p * V with packed fp32 FMAs.
+// The CTAs' partial softmax states go to a per-step-slot scratch and the last
+// CTA to finish combines them, so no CTA waits for another.
 template <int DT, int G>
-__global__ void __launch_bounds__(kAttnThreads, 2) k_attn(CtxView v, StepArgs a, int cpc) {
+__global__ void __launch_bounds__(attn_threads<DT, G>(), 2) k_attn(CtxView v, StepArgs a, int cpc) {
+  constexpr bool TC = attn_tc<DT, G>();
+  constexpr int NW = attn_warps<DT, G>();
+  constexpr int NTH = 32 * NW;
   constexpr int RB = kHeadDim * elem_bytes<DT>();
   constexpr int SB = stage_bytes<DT>();
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ __align__(8) uint64_t bar[kStages];
   __shared__ float qs[G][kHeadDim];
   __shared__ __align__(16) float S[kAttnChunk][G];
-  __shared__ float wm[kAttnWarps][G], wl[kAttnWarps][G];
+  __shared__ float wm[NW][G], wl[NW][G];
   __shared__ __align__(16) int4 pcs[kPreChunks][kAttnChunk];  // copy plans, a ring of slots
   __shared__ int pcn[kPreChunks];
   __shared__ __align__(8) uint64_t pbar[kPreChunks];  // a plan slot's bulk load landed
@@ -866,7 +985,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn(CtxView v, StepArgs a,
     for (int i = 0; i < kPreChunks; ++i) mbar_init(&pbar[i], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  for (int x = tid; x < G * kHeadDim; x += kAttnThreads)
+  for (int x = tid; x < G * kHeadDim; x += NTH)
     qs[x / kHeadDim][x % kHeadDim] =
         v.q_attn[(((int64_t)a.slot * v.n_lb + lb) * H + (int64_t)h * G) * kHeadDim + x];
   __syncthreads();
@@ -877,8 +996,8 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn(CtxView v, StepArgs a,
     s_nt = *plan_ntok(v, ps, gs);
     s_ns = *plan_nsel(v, ps, gs);
   }
-  if (!v.offload)
-    for (int x = tid; x < kPreChunks * kAttnChunk; x += kAttnThreads) {
+  if (!TC && !v.offload)  // (the tensor-core variant reads the plan's token rows instead)
+    for (int x = tid; x < kPreChunks * kAttnChunk; x += NTH) {
       const int i = x / kAttnChunk, c = c_begin + i;
       if (i < cpc && c < v.max_chunks) {
         pcs[i][x % kAttnChunk] = plan_pcs[c * kAttnChunk + x % kAttnChunk];
@@ -962,131 +1081,26 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn(CtxView v, StepArgs a,
       }
     }
   };
-  if (wid < min(n_my, kStages)) issue(wid);  // the first stages, one warp each
+  if (!TC && wid < min(n_my, kStages)) issue(wid);  // the first stages, one warp each
 
-  const int hl = head_of_lane<G>(kk);  // head whose score this lane ends with
-  // this lane's query slices in the permuted head order hl ^ j (see
-  // reduce_heads_perm)
-  float2 q2[G][4];
-#pragma unroll
-  for (int j = 0; j < G; ++j)
-#pragma unroll
-    for (int p = 0; p < 4; ++p)
-      q2[j][p] = make_float2(qs[hl ^ j][8 * kk + 2 * p], qs[hl ^ j][8 * kk + 2 * p + 1]);
-  float m_run[G];
-#pragma unroll
-  for (int g = 0; g < G; ++g) m_run[g] = -INFINITY;
-  float m_own = -INFINITY, l_own = 0.f;  // running max and sum of head lane % G
-  float2 acc[G][4];
-#pragma unroll
-  for (int g = 0; g < G; ++g)
-#pragma unroll
-    for (int p = 0; p < 4; ++p) acc[g][p] = make_float2(0.f, 0.f);
-
-  const int r0 = wid * kRowsPerWarp;
-  for (int i = 0; i < n_my; ++i) {
-    const unsigned char *Ks = smem + (i % kStages) * SB;
-    const unsigned char *Vs = Ks + SB / 2;
+  auto wait_stage = [&](int i) {
     if (!mbar_wait_bounded(&bar[i % kStages], (i / kStages) & 1, kWaitLimitNs)) {
       // record the timeout, then give the copies one more bounded wait so
       // that none is still writing a buffer this block reuses
       s_ok = 0;
       mbar_wait_bounded(&bar[i % kStages], (i / kStages) & 1, kWaitLimitNs);
     }
-    const int nrow = min(kAttnChunk, total - (c_begin + i) * kAttnChunk);
-    // pass 1: scores of this warp's 8 rows, 2 rows per instruction (rows past
-    // the chunk's end, in a slice's last chunk only, score -inf)
-    const bool full = r0 + kRowsPerWarp <= nrow;  // (warp-uniform)
-    auto pass1 = [&](auto check) {
-#pragma unroll
-      for (int it = 0; it < kRowsPerWarp / 2; ++it) {
-        const int r = r0 + it * 2 + grp;
-        float2 kv[4];
-        row8<DT>(Ks + r * RB, kk, kv);
-        float part[G];
-#pragma unroll
-        for (int j = 0; j < G; ++j) {
-          float2 s2 = make_float2(0.f, 0.f);
-#pragma unroll
-          for (int p = 0; p < 4; ++p) s2 = ffma2(q2[j][p], kv[p], s2);
-          part[j] = s2.x + s2.y;
-        }
-        float s = reduce_heads_perm<G>(part);
-        if (decltype(check)::value && r >= nrow) s = -INFINITY;
-        if ((kk & (16 / G - 1)) == 0) S[r][hl] = s;
-      }
-    };
-    if (full) pass1(std::false_type{});
-    else pass1(std::true_type{});
-    __syncwarp();
-    // chunk maximum per head over the warp's rows, softmax weights in place
-    float mx = -INFINITY;
-    for (int x = lane; x < kRowsPerWarp * G; x += 32) mx = fmaxf(mx, S[r0 + x / G][x % G]);
-#pragma unroll
-    for (int msk = G; msk < 32; msk <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, msk));
-    float corr[G];
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const float mc = __shfl_sync(kFull, mx, g);
-      const float mn = fmaxf(m_run[g], mc);
-      corr[g] = (m_run[g] == -INFINITY) ? 0.f : exp2f(m_run[g] - mn);
-      m_run[g] = mn;
-    }
-    // mx already holds the chunk maximum of head lane % G
-    const float m_own_new = fmaxf(m_own, mx);
-    const float corr_own = (m_own == -INFINITY) ? 0.f : exp2f(m_own - m_own_new);
-    m_own = m_own_new;
-    float psum = 0.f;
-    for (int x = lane; x < kRowsPerWarp * G; x += 32) {
-      const float sv = S[r0 + x / G][x % G];
-      const float p = (sv == -INFINITY) ? 0.f : exp2f(sv - m_own_new);
-      S[r0 + x / G][x % G] = p;
-      psum += p;
-    }
-    l_own = l_own * corr_own + psum;
-    __syncwarp();
-    // pass 2: acc = corr * acc + sum_r p_r v_r
-    bool rescale = false;  // (warp-uniform: the chunk maxima come from shuffles)
-#pragma unroll
-    for (int g = 0; g < G; ++g) rescale |= corr[g] != 1.f;
-    if (rescale) {
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const float2 c2 = make_float2(corr[g], corr[g]);
-#pragma unroll
-        for (int p = 0; p < 4; ++p) acc[g][p] = fmul2(acc[g][p], c2);
-      }
-    }
-    auto pass2 = [&](auto check) {
-#pragma unroll
-      for (int it = 0; it < kRowsPerWarp / 2; ++it) {
-        const int r = r0 + it * 2 + grp;
-        float2 vv[4];
-        row8<DT>(Vs + r * RB, kk, vv);
-        if (decltype(check)::value && r >= nrow) {
-#pragma unroll
-          for (int p = 0; p < 4; ++p) vv[p] = make_float2(0.f, 0.f);  // unwritten shared memory
-        }
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const float pg = S[r][g];
-          const float2 p2 = make_float2(pg, pg);
-#pragma unroll
-          for (int p = 0; p < 4; ++p) acc[g][p] = ffma2(p2, vv[p], acc[g][p]);
-        }
-      }
-    };
-    if (full) pass2(std::false_type{});
-    else pass2(std::true_type{});
-    // this warp is done with the stage; the last warp to finish refills it
-    // with chunk i + kStages (no block-wide barrier: warps run ahead freely).
-    // The warp's reads of the stage have returned (their values fed the
-    // arithmetic above), and the refill orders itself after them with the
-    // proxy fence below, so the count needs no memory fence.
+  };
+  // this warp is done with stage i; the last warp to finish refills it with
+  // chunk i + kStages (no block-wide barrier: warps run ahead freely). The
+  // warp's reads of the stage have returned (their values fed the arithmetic
+  // before), and the refill orders itself after them with the proxy fence
+  // below, so the count needs no memory fence.
+  auto release_stage = [&](int i) {
     __syncwarp();
     int last = 0;
     if (lane == 0) {
-      last = atomicAdd(&done_cnt[i % kStages], 1) == kAttnWarps - 1;
+      last = atomicAdd(&done_cnt[i % kStages], 1) == NW - 1;
       if (last) done_cnt[i % kStages] = 0;
     }
     last = __shfl_sync(kFull, last, 0);
@@ -1094,46 +1108,380 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn(CtxView v, StepArgs a,
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       issue(i + kStages);
     }
-  }
-  __syncthreads();
-  if (!s_ok && tid == 0) set_err(v.err, kErrTimeout);
-  // the pipeline buffers are free now: reuse them for the warp accumulators
+  };
+  // after the loop the pipeline buffers are free: the warp accumulators go there
   float(*wacc)[G][kHeadDim] = reinterpret_cast<float(*)[G][kHeadDim]>(smem);
-  static_assert(kAttnWarps * G * kHeadDim * sizeof(float) <= (size_t)kStages * stage_bytes<DT>(), "");
+  static_assert(NW * G * kHeadDim * sizeof(float) <= (size_t)kStages * stage_bytes<DT>(), "");
 
-  // sum the two row groups of each warp; per-head totals of l
+  if constexpr (TC) {
+    // Column n of product nt_ (NT = G / 4 products per 16-row block) carries
+    // head (G == 8 ? n : n % 4): its bf16 high part for nt_ == 0 (G == 8) or
+    // n < 4 (G == 4), else the bf16 residual. Lane (g, t) ends with D columns
+    // 2t, 2t + 1, i.e. heads hb and hb + 1.
+    constexpr int NT = G / 4;
+    const int gq = lane >> 2, tq = lane & 3;
+    const int hb = G == 8 ? 2 * tq : 2 * (tq & 1);
+    auto col_head = [](int n) { return G == 8 ? n : (n & 3); };
+    auto col_lo = [](int nt, int n) { return G == 8 ? nt == 1 : n >= 4; };
+    // B operand of the scores: k-steps 2P and 2P + 1 take dims
+    // [32P + 8t, 32P + 8t + 8) (the same order as the K rows' A operand)
+    uint32_t qb[4][NT][4];
 #pragma unroll
-  for (int g = 0; g < G; ++g)
+    for (int P = 0; P < 4; ++P)
 #pragma unroll
-    for (int p = 0; p < 4; ++p) {
-      acc[g][p].x += __shfl_xor_sync(kFull, acc[g][p].x, 16);
-      acc[g][p].y += __shfl_xor_sync(kFull, acc[g][p].y, 16);
+      for (int nt_ = 0; nt_ < NT; ++nt_) {
+        const float *qh = qs[col_head(gq)] + 32 * P + 8 * tq;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) qb[P][nt_][w] = bf16_pair(qh[2 * w], qh[2 * w + 1], col_lo(nt_, gq));
+      }
+    float mr[2] = {-INFINITY, -INFINITY}, lr[2] = {0.f, 0.f};  // heads hb, hb + 1
+    float o[NT][8][4];
+#pragma unroll
+    for (int nt_ = 0; nt_ < NT; ++nt_)
+#pragma unroll
+      for (int m = 0; m < 8; ++m)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[nt_][m][e] = 0.f;
+
+    const int r0 = 16 * wid;  // this warp's 16 rows of every chunk
+    // This warp's ring: kStages stages of its 16 rows (K rows, then V rows),
+    // filled by 16-byte asynchronous copies that the warp issues itself, so
+    // no warp waits for another. Lane (rh = lane / 16, seg = lane % 16)
+    // copies bytes [16 seg, 16 seg + 16) of rows rh, rh + 2, ..., rh + 14.
+    constexpr int WB = 16 * RB;
+    unsigned char *ring = smem + wid * kStages * 2 * WB;
+    const int rh = lane >> 4, seg = lane & 15;
+    const int32_t *tok_rows = v.offload ? nullptr : plan_sel_rows(v, ps, gs);
+    const unsigned char *deck = (const unsigned char *)v.dec_k + gs * v.dec_rows * RB;
+    const unsigned char *decv = (const unsigned char *)v.dec_v + gs * v.dec_rows * RB;
+    // the pool rows of this lane's rows of chunk i (loaded a chunk ahead of
+    // their copies; entries past the selected tokens are not used)
+    auto fetch_rows = [&](int i, int32_t (&x)[8]) {
+      const int f0 = (c_begin + i) * kAttnChunk + r0 + rh;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int f = f0 + 2 * k;
+        x[k] = (tok_rows && i < n_my && f < nt && f < v.sel_cap) ? tok_rows[f] : 0;
+      }
+    };
+    auto copy_rows = [&](int i, const int32_t (&x)[8]) {
+      unsigned char *Kd = ring + (i % kStages) * 2 * WB;
+      if (i < n_my) {
+        const int f0 = (c_begin + i) * kAttnChunk + r0 + rh;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int f = f0 + 2 * k;
+          const unsigned char *ks = selk, *vs = selv;
+          uint32_t n = 16;
+          if (f < nt) {  // a selected row: pool row, or staging row f
+            const int64_t row = tok_rows ? x[k] : f;
+            ks += row * RB;
+            vs += row * RB;
+          } else if (f < total) {  // a local-buffer row
+            ks = deck + (int64_t)(ws + f - nt) * RB;
+            vs = decv + (int64_t)(ws + f - nt) * RB;
+          } else {
+            n = 0;  // past the slice's last token: zero fill
+          }
+          const int r = rh + 2 * k;
+          cp_async16(Kd + r * RB + 16 * seg, ks + 16 * seg, n);
+          cp_async16(Kd + WB + r * RB + 16 * seg, vs + 16 * seg, n);
+        }
+      }
+      cp_async_commit();  // (an empty group past this CTA's chunks)
+    };
+    {
+      int32_t x0[kStages][8];
+#pragma unroll
+      for (int i = 0; i < kStages; ++i) fetch_rows(i, x0[i]);
+#pragma unroll
+      for (int i = 0; i < kStages; ++i) copy_rows(i, x0[i]);
     }
+    int32_t xn[8];
+    fetch_rows(kStages, xn);
+    for (int i = 0; i < n_my; ++i) {
+      const unsigned char *Kw = ring + (i % kStages) * 2 * WB;
+      const unsigned char *Vw = Kw + WB;
+      cp_async_wait<kStages - 1>();  // this lane's copies of chunk i have landed
+      __syncwarp();                  // and so have the other lanes'
+      const int nrow = min(kAttnChunk, total - (c_begin + i) * kAttnChunk);
+      const bool full = r0 + 16 <= nrow;  // (warp-uniform)
+      // scores of rows g and g + 8, two accumulation chains
+      float sc[NT][2][4];
 #pragma unroll
-  for (int msk = G; msk < 32; msk <<= 1) l_own += __shfl_xor_sync(kFull, l_own, msk);
-  if (lane < G) {  // lane g < G keeps the books of head g
-    wm[wid][lane] = m_own;
-    wl[wid][lane] = l_own;
-  }
-  if (grp == 0) {
+      for (int nt_ = 0; nt_ < NT; ++nt_)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sc[nt_][0][e] = sc[nt_][1][e] = 0.f;
+      const unsigned char *kr = Kw + gq * RB + 16 * tq;
+#pragma unroll
+      for (int P = 0; P < 4; ++P) {
+        const uint4 x = *(const uint4 *)(kr + 64 * P);
+        const uint4 y = *(const uint4 *)(kr + 8 * RB + 64 * P);
+#pragma unroll
+        for (int nt_ = 0; nt_ < NT; ++nt_) {
+          mma_bf16(sc[nt_][0], x.x, y.x, x.y, y.y, qb[P][nt_][0], qb[P][nt_][1]);
+          mma_bf16(sc[nt_][1], x.z, y.z, x.w, y.w, qb[P][nt_][2], qb[P][nt_][3]);
+        }
+      }
+      // s[0], s[1]: row g, heads hb, hb + 1; s[2], s[3]: row g + 8
+      float s[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        s[e] = sc[0][0][e] + sc[0][1][e];
+        if constexpr (NT == 2) s[e] += sc[1][0][e] + sc[1][1][e];
+        else s[e] += __shfl_xor_sync(kFull, s[e], 2);  // high part + residual
+      }
+      if (!full) {  // rows past the chunk's end (a slice's last chunk) score -inf
+        if (r0 + gq >= nrow) s[0] = s[1] = -INFINITY;
+        if (r0 + gq + 8 >= nrow) s[2] = s[3] = -INFINITY;
+      }
+      // online softmax over the warp's rows; rescale only when a maximum moves
+      float c[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        float mx = fmaxf(s[e], s[e + 2]);
+#pragma unroll
+        for (int msk = 4; msk < 32; msk <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, msk));
+        const float mn = fmaxf(mr[e], mx);
+        c[e] = (mr[e] == -INFINITY) ? 0.f : exp2f(mr[e] - mn);
+        mr[e] = mn;
+      }
+      float p[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) p[e] = (s[e] == -INFINITY) ? 0.f : exp2f(s[e] - mr[e & 1]);
+#pragma unroll
+      for (int e = 0; e < 2; ++e) lr[e] = lr[e] * c[e] + p[e] + p[e + 2];
+      if (__any_sync(kFull, c[0] != 1.f || c[1] != 1.f)) {
+#pragma unroll
+        for (int nt_ = 0; nt_ < NT; ++nt_)
+#pragma unroll
+          for (int m = 0; m < 8; ++m)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) o[nt_][m][e] *= c[e & 1];
+      }
+      // p^T as the B operand of p * V (rows = tokens, columns as above),
+      // through the warp's rows of S
+      if (G == 8 || tq < 2) {
+        *(float2 *)&S[r0 + gq][hb] = make_float2(p[0], p[1]);
+        *(float2 *)&S[r0 + gq + 8][hb] = make_float2(p[2], p[3]);
+      }
+      __syncwarp();
+      uint32_t pb[NT][2];
+#pragma unroll
+      for (int nt_ = 0; nt_ < NT; ++nt_) {
+        const int h = col_head(gq);
+        const bool lo = col_lo(nt_, gq);
+        pb[nt_][0] = bf16_pair(S[r0 + 2 * tq][h], S[r0 + 2 * tq + 1][h], lo);
+        pb[nt_][1] = bf16_pair(S[r0 + 2 * tq + 8][h], S[r0 + 2 * tq + 9][h], lo);
+      }
+      // p * V: product m = 4hf + j has output rows dim 64hf + 8g + 2j (row g)
+      // and that dim + 1 (row g + 8); lane (g, t) reads tokens 2t, 2t + 1,
+      // 2t + 8, 2t + 9 at dims [64hf + 8g, + 8) and pairs them up by token
+      // (rows past the slice's end were zero-filled)
+      const unsigned char *vr = Vw + (2 * tq) * RB + 16 * gq;
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        const uint4 v0 = *(const uint4 *)(vr + 128 * hf);
+        const uint4 v1 = *(const uint4 *)(vr + RB + 128 * hf);
+        const uint4 v2 = *(const uint4 *)(vr + 8 * RB + 128 * hf);
+        const uint4 v3 = *(const uint4 *)(vr + 9 * RB + 128 * hf);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t w0 = word(v0, j), w1 = word(v1, j), w2 = word(v2, j), w3 = word(v3, j);
+          const uint32_t a0 = prmt(w0, w1, 0x5410u), a1 = prmt(w0, w1, 0x7632u);
+          const uint32_t a2 = prmt(w2, w3, 0x5410u), a3 = prmt(w2, w3, 0x7632u);
+#pragma unroll
+          for (int nt_ = 0; nt_ < NT; ++nt_)
+            mma_bf16(o[nt_][4 * hf + j], a0, a1, a2, a3, pb[nt_][0], pb[nt_][1]);
+        }
+      }
+      // every lane's reads of this stage (and of S) are done: refill the
+      // stage with chunk i + kStages, fetch the rows of the chunk after it
+      __syncwarp();
+      copy_rows(i + kStages, xn);
+      fetch_rows(i + kStages + 1, xn);
+    }
+    cp_async_wait<0>();  // (only empty groups can remain)
+    __syncthreads();
+    // the warp's result: high part + residual, then heads hb, hb + 1 at dims
+    // 64hf + 8g + [0, 8) from the lanes that hold the high parts
+#pragma unroll
+    for (int m = 0; m < 8; ++m)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if constexpr (NT == 2) o[0][m][e] += o[NT - 1][m][e];
+        else o[0][m][e] += __shfl_xor_sync(kFull, o[0][m][e], 2);
+      }
+#pragma unroll
+    for (int e = 0; e < 2; ++e)
+#pragma unroll
+      for (int msk = 4; msk < 32; msk <<= 1) lr[e] += __shfl_xor_sync(kFull, lr[e], msk);
+    if (G == 8 || tq < 2) {
+      if (gq == 0) {
+        wm[wid][hb] = mr[0];
+        wm[wid][hb + 1] = mr[1];
+        wl[wid][hb] = lr[0];
+        wl[wid][hb + 1] = lr[1];
+      }
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          float *dst = &wacc[wid][hb + e][64 * hf + 8 * gq];
+          *(float4 *)dst = make_float4(o[0][4 * hf][e], o[0][4 * hf][e + 2], o[0][4 * hf + 1][e],
+                                       o[0][4 * hf + 1][e + 2]);
+          *(float4 *)(dst + 4) = make_float4(o[0][4 * hf + 2][e], o[0][4 * hf + 2][e + 2],
+                                             o[0][4 * hf + 3][e], o[0][4 * hf + 3][e + 2]);
+        }
+    }
+  } else {
+    const int hl = head_of_lane<G>(kk);  // head whose score this lane ends with
+    // this lane's query slices in the permuted head order hl ^ j (see
+    // reduce_heads_perm)
+    float2 q2[G][4];
+#pragma unroll
+    for (int j = 0; j < G; ++j)
+#pragma unroll
+      for (int p = 0; p < 4; ++p)
+        q2[j][p] = make_float2(qs[hl ^ j][8 * kk + 2 * p], qs[hl ^ j][8 * kk + 2 * p + 1]);
+    float m_run[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) m_run[g] = -INFINITY;
+    float m_own = -INFINITY, l_own = 0.f;  // running max and sum of head lane % G
+    float2 acc[G][4];
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+      for (int p = 0; p < 4; ++p) acc[g][p] = make_float2(0.f, 0.f);
+
+    const int r0 = wid * kRowsPerWarp;
+    for (int i = 0; i < n_my; ++i) {
+      const unsigned char *Ks = smem + (i % kStages) * SB;
+      const unsigned char *Vs = Ks + SB / 2;
+      wait_stage(i);
+      const int nrow = min(kAttnChunk, total - (c_begin + i) * kAttnChunk);
+      // pass 1: scores of this warp's 8 rows, 2 rows per instruction (rows past
+      // the chunk's end, in a slice's last chunk only, score -inf)
+      const bool full = r0 + kRowsPerWarp <= nrow;  // (warp-uniform)
+      auto pass1 = [&](auto check) {
+#pragma unroll
+        for (int it = 0; it < kRowsPerWarp / 2; ++it) {
+          const int r = r0 + it * 2 + grp;
+          float2 kv[4];
+          row8<DT>(Ks + r * RB, kk, kv);
+          float part[G];
+#pragma unroll
+          for (int j = 0; j < G; ++j) {
+            float2 s2 = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int p = 0; p < 4; ++p) s2 = ffma2(q2[j][p], kv[p], s2);
+            part[j] = s2.x + s2.y;
+          }
+          float s = reduce_heads_perm<G>(part);
+          if (decltype(check)::value && r >= nrow) s = -INFINITY;
+          if ((kk & (16 / G - 1)) == 0) S[r][hl] = s;
+        }
+      };
+      if (full) pass1(std::false_type{});
+      else pass1(std::true_type{});
+      __syncwarp();
+      // chunk maximum per head over the warp's rows, softmax weights in place
+      float mx = -INFINITY;
+      for (int x = lane; x < kRowsPerWarp * G; x += 32) mx = fmaxf(mx, S[r0 + x / G][x % G]);
+#pragma unroll
+      for (int msk = G; msk < 32; msk <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, msk));
+      float corr[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float mc = __shfl_sync(kFull, mx, g);
+        const float mn = fmaxf(m_run[g], mc);
+        corr[g] = (m_run[g] == -INFINITY) ? 0.f : exp2f(m_run[g] - mn);
+        m_run[g] = mn;
+      }
+      // mx already holds the chunk maximum of head lane % G
+      const float m_own_new = fmaxf(m_own, mx);
+      const float corr_own = (m_own == -INFINITY) ? 0.f : exp2f(m_own - m_own_new);
+      m_own = m_own_new;
+      float psum = 0.f;
+      for (int x = lane; x < kRowsPerWarp * G; x += 32) {
+        const float sv = S[r0 + x / G][x % G];
+        const float p = (sv == -INFINITY) ? 0.f : exp2f(sv - m_own_new);
+        S[r0 + x / G][x % G] = p;
+        psum += p;
+      }
+      l_own = l_own * corr_own + psum;
+      __syncwarp();
+      // pass 2: acc = corr * acc + sum_r p_r v_r
+      bool rescale = false;  // (warp-uniform: the chunk maxima come from shuffles)
+#pragma unroll
+      for (int g = 0; g < G; ++g) rescale |= corr[g] != 1.f;
+      if (rescale) {
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float2 c2 = make_float2(corr[g], corr[g]);
+#pragma unroll
+          for (int p = 0; p < 4; ++p) acc[g][p] = fmul2(acc[g][p], c2);
+        }
+      }
+      auto pass2 = [&](auto check) {
+#pragma unroll
+        for (int it = 0; it < kRowsPerWarp / 2; ++it) {
+          const int r = r0 + it * 2 + grp;
+          float2 vv[4];
+          row8<DT>(Vs + r * RB, kk, vv);
+          if (decltype(check)::value && r >= nrow) {
+#pragma unroll
+            for (int p = 0; p < 4; ++p) vv[p] = make_float2(0.f, 0.f);  // unwritten shared memory
+          }
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            const float pg = S[r][g];
+            const float2 p2 = make_float2(pg, pg);
+#pragma unroll
+            for (int p = 0; p < 4; ++p) acc[g][p] = ffma2(p2, vv[p], acc[g][p]);
+          }
+        }
+      };
+      if (full) pass2(std::false_type{});
+      else pass2(std::true_type{});
+      release_stage(i);
+    }
+    __syncthreads();
+    // sum the two row groups of each warp; per-head totals of l
 #pragma unroll
     for (int g = 0; g < G; ++g)
 #pragma unroll
       for (int p = 0; p < 4; ++p) {
-        wacc[wid][g][8 * kk + 2 * p] = acc[g][p].x;
-        wacc[wid][g][8 * kk + 2 * p + 1] = acc[g][p].y;
+        acc[g][p].x += __shfl_xor_sync(kFull, acc[g][p].x, 16);
+        acc[g][p].y += __shfl_xor_sync(kFull, acc[g][p].y, 16);
       }
+#pragma unroll
+    for (int msk = G; msk < 32; msk <<= 1) l_own += __shfl_xor_sync(kFull, l_own, msk);
+    if (lane < G) {  // lane g < G keeps the books of head g
+      wm[wid][lane] = m_own;
+      wl[wid][lane] = l_own;
+    }
+    if (grp == 0) {
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+          wacc[wid][g][8 * kk + 2 * p] = acc[g][p].x;
+          wacc[wid][g][8 * kk + 2 * p + 1] = acc[g][p].y;
+        }
+    }
   }
   __syncthreads();
+  if (!s_ok && tid == 0) set_err(v.err, kErrTimeout);
   // merge the warps into this CTA's partial
-  for (int x = tid; x < G * kHeadDim; x += kAttnThreads) {
+  for (int x = tid; x < G * kHeadDim; x += NTH) {
     const int g = x / kHeadDim, dim = x % kHeadDim;
     float mm = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kAttnWarps; ++w) mm = fmaxf(mm, wm[w][g]);
+    for (int w = 0; w < NW; ++w) mm = fmaxf(mm, wm[w][g]);
     float o = 0.f, z = 0.f;
 #pragma unroll
-    for (int w = 0; w < kAttnWarps; ++w) {
+    for (int w = 0; w < NW; ++w) {
       const float sw = (wm[w][g] == -INFINITY) ? 0.f : exp2f(wm[w][g] - mm);
       o = fmaf(sw, wacc[w][g][dim], o);
       z = fmaf(sw, wl[w][g], z);
@@ -1153,7 +1501,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn(CtxView v, StepArgs a,
   bool combine = true;
   if (nsplit > 1) {
     float *gp = v.attn_part + (((int64_t)a.slot * v.S_all + gs) * kAttnMaxSplit + split) * kPart;
-    for (int x = tid; x < kPart; x += kAttnThreads) gp[x] = part[x];
+    for (int x = tid; x < kPart; x += NTH) gp[x] = part[x];
     __threadfence();
     __syncthreads();
     if (tid == 0) s_last = atomicAdd(&v.attn_count[(int64_t)a.slot * v.S_all + gs], 1) == nsplit - 1;
@@ -1166,7 +1514,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn(CtxView v, StepArgs a,
   {
     float *out = a.out + k * a.stride_out;
     const int64_t obase = (((int64_t)b * a.nl + li) * H + (int64_t)h * G) * kHeadDim;
-    for (int x = tid; x < G * kHeadDim; x += kAttnThreads) {
+    for (int x = tid; x < G * kHeadDim; x += NTH) {
       const int g = x / kHeadDim;
       float mc[kAttnMaxSplit];
       float mm = -INFINITY;
@@ -1189,7 +1537,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn(CtxView v, StepArgs a,
     if (a.selected_units) {
       const int32_t *sel = plan_sel(v, ps, gs);
       int32_t *dst = a.selected_units + k * a.stride_sel + so * v.u_cap;
-      for (int x = tid; x < ns; x += kAttnThreads) dst[x] = sel[x];
+      for (int x = tid; x < ns; x += NTH) dst[x] = sel[x];
     }
     if (tid == 0) {
       if (nsplit > 1) v.attn_count[(int64_t)a.slot * v.S_all + gs] = 0;
@@ -1199,6 +1547,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn(CtxView v, StepArgs a,
     }
   }
 }
+
 
 // ---------------------------------------------------------------- host
 
@@ -1253,7 +1602,7 @@ static void launch_attn(const CtxView &v, const StepArgs &a, int slices, int nch
   attn_split(slices, nch, concurrent, &nsplit, &cpc);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(slices, nsplit);
-  cfg.blockDim = dim3(kAttnThreads);
+  cfg.blockDim = dim3(attn_threads<DT, G>());
   cfg.dynamicSmemBytes = attn_smem<DT, G>();
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
@@ -1272,7 +1621,8 @@ static cudaError_t prep_attn() {
                                        (int)attn_smem<DT, G>());
   if (e != cudaSuccess) return e;
   int per_sm = 0, dev = 0, sms = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_attn<DT, G>, kAttnThreads, attn_smem<DT, G>());
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_attn<DT, G>, attn_threads<DT, G>(),
+                                                    attn_smem<DT, G>());
   if (e == cudaSuccess) e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
@@ -1286,6 +1636,8 @@ static cudaError_t prep_attn() {
     const int x = atoi(env);
     g_attn_split = (x >= 1 && x <= kAttnMaxSplit) ? x : 0;
   }
+  e = cudaFuncSetAttribute(k_select, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSelSmemBytes);
+  if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(k_step_boundary<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)(2 * kMaxHeads * kQPitch * sizeof(float)));
 }
@@ -1327,7 +1679,10 @@ static cudaError_t decode_t(const CtxView &v, const StepArgs &a, cudaStream_t st
     if (e != cudaSuccess) return e;
   }
   prof.begin(kPScore, ss);
-  launch_pdl(k_score_select<DT>, dim3(slices), dim3(kScoreThreads), 0, ss, v, a);
+  launch_pdl(k_score<DT>, dim3(slices, kScoreSplit), dim3(kScoreCtaThreads), 0, ss, v, a);
+  prof.end(ss);
+  prof.begin(kPSelect, ss);
+  launch_pdl(k_select, dim3(slices), dim3(kScoreThreads), kSelSmemBytes, ss, v, a);
   prof.end(ss);
   if (v.offload) {
     prof.begin(kPGather, ss);

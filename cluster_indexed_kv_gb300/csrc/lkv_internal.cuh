@@ -51,6 +51,8 @@ struct CtxView {
   int32_t t_cap;      // max decode steps
   int32_t u_cap;      // max units per slice (C_cap + T_cap)
   int32_t bud_cap;    // max token budget
+  int32_t sel_cap;    // selected tokens a plan can hold: min(bud_cap, n_cap + t_cap)
+  int32_t need_pieces;  // a reader of the copy pieces exists (host offload gather or the scalar attention)
   int offload;
   int64_t S_all;      // slices of all layers (n_layers * B * Hkv)
   int32_t n_lb;       // (layer, sequence) pairs (n_layers * B)
@@ -79,6 +81,7 @@ struct CtxView {
   int32_t *n_sel;             // [kRing][slice]
   int32_t *n_tok;             // [kRing][slice]
   int32_t *rng_row;           // [kRing][slice][u_cap] first row of each selected unit
+  int32_t *sel_rows;          // [kRing][slice][sel_cap] pool row of each selected token (HBM pool only)
   int32_t *rng_cum;           // [kRing][slice][u_cap + 1] exclusive token prefix
   int4 *pieces;               // [slice][max_pieces] (src row, first token, length, 0)
   int32_t *chunk_piece;       // [slice][max_chunks + 1] first piece of each chunk
@@ -109,6 +112,9 @@ __host__ __device__ __forceinline__ int32_t *plan_rng_row(const CtxView &v, int 
 __host__ __device__ __forceinline__ int32_t *plan_rng_cum(const CtxView &v, int p, int64_t gs) {
   return v.rng_cum + ((int64_t)p * v.S_all + gs) * (v.u_cap + 1);
 }
+__host__ __device__ __forceinline__ int32_t *plan_sel_rows(const CtxView &v, int p, int64_t gs) {
+  return v.sel_rows + ((int64_t)p * v.S_all + gs) * v.sel_cap;
+}
 __host__ __device__ __forceinline__ int4 *plan_chunk_pieces(const CtxView &v, int p, int64_t gs) {
   return v.chunk_pieces + ((int64_t)p * v.S_all + gs) * v.max_chunks * 64;
 }
@@ -124,6 +130,7 @@ enum CounterId : int { kCntAttnRows = 0, kCntScoreUnits = 1, kCntGatherRows = 2,
 enum ProfKind : int {
   kPBoundary = 0, kPScore, kPGather, kPAttn,
   kPKmInit, kPKmOperand, kPKmAssign, kPKmRefine, kPKmSort, kPKmUpdate, kPKmPool, kPKmAssignTc,
+  kPSelect,
   kPNum
 };
 

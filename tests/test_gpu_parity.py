@@ -113,6 +113,18 @@ def test_decode_bf16_evictions_and_forced_cuts():
     assert all(r["n_evicted"] > 5 for r in rep)
 
 
+@pytest.mark.parametrize("group", [1, 2, 8])
+def test_decode_query_group_sizes(group):
+    """GQA groups other than 4 query heads per KV head: 8 takes the
+    tensor-core attention with two products per row block, 1 and 2 the scalar
+    one; decisions bit-exact, outputs within tolerance, ragged last chunks."""
+    w = synth.WORKLOADS["long_out"].replace(batch=2, n_kv_heads=2, group=group, n_prefill=700,
+                                            n_components=30, n_clusters=30, iters=4, local_buf=40,
+                                            budget=150, jump_p=0.08)
+    rep = _decode_check(w, tau=0.9, T=120)
+    assert sum(r["n_boundary"] for r in rep) >= 2
+
+
 def test_decode_never_triggering_forces_cuts():
     w = synth.WORKLOADS["long_in"].replace(batch=1, n_kv_heads=2, n_prefill=500, n_components=20,
                                            n_clusters=20, iters=3, local_buf=8, budget=64)
