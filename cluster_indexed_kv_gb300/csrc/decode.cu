@@ -769,7 +769,10 @@ constexpr int attn_warps() { return attn_tc<DT, G>() ? 4 : 8; }
 template <int DT, int G>
 constexpr int attn_threads() { return 32 * attn_warps<DT, G>(); }
 constexpr int kRowsPerWarp = 8;  // scalar variant: rows of each chunk per warp
-constexpr int kStages = 3;
+constexpr int kStages = 3;       // scalar variant: chunk stages per CTA
+constexpr int kTcStages = 2;     // tensor-core variant: stages of each warp's ring
+template <int DT, int G>
+constexpr int attn_min_blocks() { return attn_tc<DT, G>() ? 3 : 2; }
 constexpr int kPreChunks = 8;  // chunks whose copy plan a CTA prefetches
 constexpr uint64_t kWaitLimitNs = 2000000000ull;      // 2 s
 
@@ -923,6 +926,13 @@ __device__ __forceinline__ int head_of_lane(int k) {
 
 template <int DT>
 constexpr int stage_bytes() { return 2 * kAttnChunk * kHeadDim * elem_bytes<DT>(); }
+// dynamic shared memory: the scalar variant's chunk ring, or the tensor-core
+// variant's per-warp rings (each stage 16 rows of K and V)
+template <int DT, int G>
+constexpr size_t attn_smem() {
+  return attn_tc<DT, G>() ? (size_t)attn_warps<DT, G>() * kTcStages * 2 * 16 * kHeadDim * elem_bytes<DT>()
+                          : (size_t)kStages * stage_bytes<DT>();
+}
 
 
 // Split-K attention. CTA split of the nsplit CTAs of a (seq, layer, kv head)
@@ -939,7 +949,8 @@ constexpr int stage_bytes() { return 2 * kAttnChunk * kHeadDim * elem_bytes<DT>(
 // The CTAs' partial softmax states go to a per-step-slot scratch and the last
 // CTA to finish combines them, so no CTA waits for another.
 template <int DT, int G>
-__global__ void __launch_bounds__(attn_threads<DT, G>(), 2) k_attn(CtxView v, StepArgs a, int cpc) {
+__global__ void __launch_bounds__(attn_threads<DT, G>(), attn_min_blocks<DT, G>())
+    k_attn(CtxView v, StepArgs a, int cpc) {
   constexpr bool TC = attn_tc<DT, G>();
   constexpr int NW = attn_warps<DT, G>();
   constexpr int NTH = 32 * NW;
@@ -1111,7 +1122,7 @@ __global__ void __launch_bounds__(attn_threads<DT, G>(), 2) k_attn(CtxView v, St
   };
   // after the loop the pipeline buffers are free: the warp accumulators go there
   float(*wacc)[G][kHeadDim] = reinterpret_cast<float(*)[G][kHeadDim]>(smem);
-  static_assert(NW * G * kHeadDim * sizeof(float) <= (size_t)kStages * stage_bytes<DT>(), "");
+  static_assert(NW * G * kHeadDim * sizeof(float) <= attn_smem<DT, G>(), "");
 
   if constexpr (TC) {
     // Column n of product nt_ (NT = G / 4 products per 16-row block) carries
@@ -1144,12 +1155,12 @@ __global__ void __launch_bounds__(attn_threads<DT, G>(), 2) k_attn(CtxView v, St
         for (int e = 0; e < 4; ++e) o[nt_][m][e] = 0.f;
 
     const int r0 = 16 * wid;  // this warp's 16 rows of every chunk
-    // This warp's ring: kStages stages of its 16 rows (K rows, then V rows),
+    // This warp's ring: kTcStages stages of its 16 rows (K rows, then V rows),
     // filled by 16-byte asynchronous copies that the warp issues itself, so
     // no warp waits for another. Lane (rh = lane / 16, seg = lane % 16)
     // copies bytes [16 seg, 16 seg + 16) of rows rh, rh + 2, ..., rh + 14.
     constexpr int WB = 16 * RB;
-    unsigned char *ring = smem + wid * kStages * 2 * WB;
+    unsigned char *ring = smem + wid * kTcStages * 2 * WB;
     const int rh = lane >> 4, seg = lane & 15;
     const int32_t *tok_rows = v.offload ? nullptr : plan_sel_rows(v, ps, gs);
     const unsigned char *deck = (const unsigned char *)v.dec_k + gs * v.dec_rows * RB;
@@ -1165,7 +1176,7 @@ __global__ void __launch_bounds__(attn_threads<DT, G>(), 2) k_attn(CtxView v, St
       }
     };
     auto copy_rows = [&](int i, const int32_t (&x)[8]) {
-      unsigned char *Kd = ring + (i % kStages) * 2 * WB;
+      unsigned char *Kd = ring + (i % kTcStages) * 2 * WB;
       if (i < n_my) {
         const int f0 = (c_begin + i) * kAttnChunk + r0 + rh;
 #pragma unroll
@@ -1191,18 +1202,18 @@ __global__ void __launch_bounds__(attn_threads<DT, G>(), 2) k_attn(CtxView v, St
       cp_async_commit();  // (an empty group past this CTA's chunks)
     };
     {
-      int32_t x0[kStages][8];
+      int32_t x0[kTcStages][8];
 #pragma unroll
-      for (int i = 0; i < kStages; ++i) fetch_rows(i, x0[i]);
+      for (int i = 0; i < kTcStages; ++i) fetch_rows(i, x0[i]);
 #pragma unroll
-      for (int i = 0; i < kStages; ++i) copy_rows(i, x0[i]);
+      for (int i = 0; i < kTcStages; ++i) copy_rows(i, x0[i]);
     }
     int32_t xn[8];
-    fetch_rows(kStages, xn);
+    fetch_rows(kTcStages, xn);
     for (int i = 0; i < n_my; ++i) {
-      const unsigned char *Kw = ring + (i % kStages) * 2 * WB;
+      const unsigned char *Kw = ring + (i % kTcStages) * 2 * WB;
       const unsigned char *Vw = Kw + WB;
-      cp_async_wait<kStages - 1>();  // this lane's copies of chunk i have landed
+      cp_async_wait<kTcStages - 1>();  // this lane's copies of chunk i have landed
       __syncwarp();                  // and so have the other lanes'
       const int nrow = min(kAttnChunk, total - (c_begin + i) * kAttnChunk);
       const bool full = r0 + 16 <= nrow;  // (warp-uniform)
@@ -1296,10 +1307,10 @@ __global__ void __launch_bounds__(attn_threads<DT, G>(), 2) k_attn(CtxView v, St
         }
       }
       // every lane's reads of this stage (and of S) are done: refill the
-      // stage with chunk i + kStages, fetch the rows of the chunk after it
+      // stage with chunk i + kTcStages, fetch the rows of the chunk after it
       __syncwarp();
-      copy_rows(i + kStages, xn);
-      fetch_rows(i + kStages + 1, xn);
+      copy_rows(i + kTcStages, xn);
+      fetch_rows(i + kTcStages + 1, xn);
     }
     cp_async_wait<0>();  // (only empty groups can remain)
     __syncthreads();
@@ -1473,7 +1484,12 @@ __global__ void __launch_bounds__(attn_threads<DT, G>(), 2) k_attn(CtxView v, St
   }
   __syncthreads();
   if (!s_ok && tid == 0) set_err(v.err, kErrTimeout);
-  // merge the warps into this CTA's partial
+  // merge the warps into this CTA's partial: straight to the per-step-slot
+  // scratch when the slice is split over several CTAs, else to shared memory
+  const int64_t so = ((int64_t)b * a.nl + li) * v.Hkv + h;
+  constexpr int kPart = G * kHeadDim + 2 * G;  // acc [G][d], maxima [G], sums [G]
+  const int64_t slot_part = ((int64_t)a.slot * v.S_all + gs) * kAttnMaxSplit * kPart;
+  float *mine = nsplit > 1 ? v.attn_part + slot_part + (int64_t)split * kPart : part;
   for (int x = tid; x < G * kHeadDim; x += NTH) {
     const int g = x / kHeadDim, dim = x % kHeadDim;
     float mm = -INFINITY;
@@ -1486,31 +1502,35 @@ __global__ void __launch_bounds__(attn_threads<DT, G>(), 2) k_attn(CtxView v, St
       o = fmaf(sw, wacc[w][g][dim], o);
       z = fmaf(sw, wl[w][g], z);
     }
-    part[g * kHeadDim + dim] = o;
+    mine[g * kHeadDim + dim] = o;
     if (dim == 0) {
-      part[G * kHeadDim + g] = mm;
-      part[G * kHeadDim + G + g] = z;
+      mine[G * kHeadDim + g] = mm;
+      mine[G * kHeadDim + G + g] = z;
     }
   }
-  // the last CTA of the slice to finish combines every CTA's partial (through
-  // a per-step-slot scratch in global memory); the others leave at once
-  const int64_t so = ((int64_t)b * a.nl + li) * v.Hkv + h;
-  constexpr int kPart = G * kHeadDim + 2 * G;
-  __syncthreads();  // the partial is complete
+  // the last CTA of the slice to finish combines every CTA's partial; the
+  // others leave at once
   const float *parts = part;
-  bool combine = true;
   if (nsplit > 1) {
-    float *gp = v.attn_part + (((int64_t)a.slot * v.S_all + gs) * kAttnMaxSplit + split) * kPart;
-    for (int x = tid; x < kPart; x += NTH) gp[x] = part[x];
     __threadfence();
     __syncthreads();
     if (tid == 0) s_last = atomicAdd(&v.attn_count[(int64_t)a.slot * v.S_all + gs], 1) == nsplit - 1;
     __syncthreads();
-    combine = s_last;
-    if (combine) __threadfence();
-    parts = v.attn_part + ((int64_t)a.slot * v.S_all + gs) * kAttnMaxSplit * kPart;
+    if (!s_last) return;
+    __threadfence();
+    // all partials into shared memory (the ring is free) in one round of
+    // coalesced loads
+    float *staged = reinterpret_cast<float *>(smem);
+    static_assert((size_t)kAttnMaxSplit * kPart * sizeof(float) <= attn_smem<DT, G>(), "");
+    if constexpr (kPart % 4 == 0) {
+      const float4 *src = reinterpret_cast<const float4 *>(v.attn_part + slot_part);
+      for (int x = tid; x < nsplit * kPart / 4; x += NTH) reinterpret_cast<float4 *>(staged)[x] = __ldcg(src + x);
+    } else {
+      for (int x = tid; x < nsplit * kPart; x += NTH) staged[x] = __ldcg(v.attn_part + slot_part + x);
+    }
+    parts = staged;
   }
-  if (!combine) return;
+  __syncthreads();
   {
     float *out = a.out + k * a.stride_out;
     const int64_t obase = (((int64_t)b * a.nl + li) * H + (int64_t)h * G) * kHeadDim;
@@ -1576,8 +1596,7 @@ static void launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
   cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
-template <int DT, int G>
-constexpr size_t attn_smem() { return (size_t)kStages * stage_bytes<DT>(); }
+
 
 static int g_attn_slots = 2 * 152;  // resident attention CTAs on the device
 static int g_attn_split = 0;        // CTAs per slice forced by LKV_ATTN_CTAS_PER_SLICE (0: auto)
