@@ -163,27 +163,16 @@ __global__ void __launch_bounds__(kBoundaryThreads, 2) k_step_boundary(CtxView v
     st = v.st[lb];
     slow_any = 0;
   }
-  __syncthreads();
-  const int t = st.t;
-  const int n_closed0 = st.n_closed;
-  const int64_t k = t - a.base_t;
-  const void *q = (const char *)a.q + k * a.stride_q * elem_bytes<DT>();
-  const void *k_new = (const char *)a.k_new + k * a.stride_kv * elem_bytes<DT>();
-  const void *v_new = (const char *)a.v_new + k * a.stride_kv * elem_bytes<DT>();
-  const int64_t qoff = ((int64_t)b * a.nl + li) * H * kHeadDim;
-  const int64_t kvoff = ((int64_t)b * a.nl + li) * v.Hkv * kHeadDim;
-
-  // all loads of the step at once: both query sets (16-byte vectors into
-  // padded shared rows) and this thread's key/value elements and running sums
+  // loads that do not depend on the step go out with the state's: the
+  // previous queries (16-byte vectors into padded shared rows) and this
+  // thread's running sums of the open segment
   constexpr int per16 = 16 / elem_bytes<DT>();
   const int nvec = H * kHeadDim / per16;
-  for (int x = tid; x < 2 * nvec; x += nth) {
-    const int which = x / nvec, y = x % nvec;
+  for (int y = tid; y < nvec; y += nth) {
     const int head = y / (kHeadDim / per16), j0 = (y % (kHeadDim / per16)) * per16;
     float e[8];
-    if (which == 0) load16<DT>(v.q_prev, (lb * H + head) * kHeadDim + j0, e);
-    else load16<DT>(q, qoff + (int64_t)head * kHeadDim + j0, e);
-    float *dst = qsm + ((int64_t)which * H + head) * kQPitch + j0;
+    load16<DT>(v.q_prev, (lb * H + head) * kHeadDim + j0, e);
+    float *dst = qsm + (int64_t)head * kQPitch + j0;
 #pragma unroll
     for (int i = 0; i < per16; ++i) dst[i] = e[i];
   }
@@ -193,8 +182,22 @@ __global__ void __launch_bounds__(kBoundaryThreads, 2) k_step_boundary(CtxView v
 #pragma unroll
   for (int r = 0; r < kMaxPer; ++r) {
     const int x = tid + r * nth;
+    if (x < v.Hkv * kHeadDim) ssum[r] = v.segsum[(lb * v.Hkv + x / kHeadDim) * kHeadDim + x % kHeadDim];
+  }
+  __syncthreads();
+  const int t = st.t;
+  const int n_closed0 = st.n_closed;
+  const int64_t k = t - a.base_t;
+  const void *q = (const char *)a.q + k * a.stride_q * elem_bytes<DT>();
+  const void *k_new = (const char *)a.k_new + k * a.stride_kv * elem_bytes<DT>();
+  const void *v_new = (const char *)a.v_new + k * a.stride_kv * elem_bytes<DT>();
+  const int64_t qoff = ((int64_t)b * a.nl + li) * H * kHeadDim;
+  const int64_t kvoff = ((int64_t)b * a.nl + li) * v.Hkv * kHeadDim;
+  // then the step's inputs: the new key/value elements and the current queries
+#pragma unroll
+  for (int r = 0; r < kMaxPer; ++r) {
+    const int x = tid + r * nth;
     if (x < v.Hkv * kHeadDim) {
-      const int64_t gs = lb * v.Hkv + x / kHeadDim;
       if constexpr (DT == 1) {
         kbits[r] = ((const uint16_t *)k_new)[kvoff + x];
         vbits[r] = ((const uint16_t *)v_new)[kvoff + x];
@@ -202,8 +205,15 @@ __global__ void __launch_bounds__(kBoundaryThreads, 2) k_step_boundary(CtxView v
         kbits[r] = __float_as_uint(((const float *)k_new)[kvoff + x]);
         vbits[r] = __float_as_uint(((const float *)v_new)[kvoff + x]);
       }
-      ssum[r] = v.segsum[gs * kHeadDim + x % kHeadDim];
     }
+  }
+  for (int y = tid; y < nvec; y += nth) {
+    const int head = y / (kHeadDim / per16), j0 = (y % (kHeadDim / per16)) * per16;
+    float e[8];
+    load16<DT>(q, qoff + (int64_t)head * kHeadDim + j0, e);
+    float *dst = qsm + ((int64_t)H + head) * kQPitch + j0;
+#pragma unroll
+    for (int i = 0; i < per16; ++i) dst[i] = e[i];
   }
   __syncthreads();
 
@@ -328,9 +338,11 @@ __global__ void __launch_bounds__(kBoundaryThreads, 2) k_step_boundary(CtxView v
   for (int y = tid; y < nvec; y += nth) {
     const int head = y / (kHeadDim / per16), j0 = (y % (kHeadDim / per16)) * per16;
     const float *src = qsm + ((int64_t)H + head) * kQPitch + j0;
+    float4 *qa = (float4 *)(v.q_attn + (((int64_t)a.slot * v.n_lb + lb) * H + head) * kHeadDim + j0);
 #pragma unroll
-    for (int i = 0; i < per16; ++i)
-      v.q_attn[(((int64_t)a.slot * v.n_lb + lb) * H + head) * kHeadDim + j0 + i] = src[i] * qscale;
+    for (int i = 0; i < per16 / 4; ++i)
+      qa[i] = make_float4(src[4 * i] * qscale, src[4 * i + 1] * qscale, src[4 * i + 2] * qscale,
+                          src[4 * i + 3] * qscale);
     if constexpr (DT == 1) {
       uint4 o;
       uint32_t w[4];
@@ -1001,6 +1013,19 @@ __global__ void __launch_bounds__(attn_threads<DT, G>(), attn_min_blocks<DT, G>(
         v.q_attn[(((int64_t)a.slot * v.n_lb + lb) * H + (int64_t)h * G) * kHeadDim + x];
   __syncthreads();
   const int ps = s_view.z;
+  // tensor-core variant: the token rows of this warp's first chunks go out
+  // with the plan's counts (entries past the selected tokens are not used)
+  int32_t pre_rows[kTcStages][8];
+  if constexpr (TC) {
+    const int32_t *tr = v.offload ? nullptr : plan_sel_rows(v, ps, gs);
+#pragma unroll
+    for (int i = 0; i < kTcStages; ++i)
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int f = (c_begin + i) * kAttnChunk + 16 * wid + (lane >> 4) + 2 * k;
+        pre_rows[i][k] = (tr && f < v.sel_cap) ? tr[f] : 0;
+      }
+  }
   const int4 *plan_pcs = plan_chunk_pieces(v, ps, gs);
   const int32_t *plan_pcn = plan_chunk_count(v, ps, gs);
   if (tid == 0) {
@@ -1201,13 +1226,8 @@ __global__ void __launch_bounds__(attn_threads<DT, G>(), attn_min_blocks<DT, G>(
       }
       cp_async_commit();  // (an empty group past this CTA's chunks)
     };
-    {
-      int32_t x0[kTcStages][8];
 #pragma unroll
-      for (int i = 0; i < kTcStages; ++i) fetch_rows(i, x0[i]);
-#pragma unroll
-      for (int i = 0; i < kTcStages; ++i) copy_rows(i, x0[i]);
-    }
+    for (int i = 0; i < kTcStages; ++i) copy_rows(i, pre_rows[i]);
     int32_t xn[8];
     fetch_rows(kTcStages, xn);
     for (int i = 0; i < n_my; ++i) {
