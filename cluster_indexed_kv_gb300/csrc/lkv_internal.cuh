@@ -14,7 +14,7 @@ constexpr int kHeadDim = 128;
 constexpr int kMaxGroup = 8;
 constexpr int kMaxParts = 64;      // token parts of the stable counting sort
 constexpr int kAttnChunk = 64;     // tokens per attention work item
-constexpr int kRing = 4;           // steps whose attention may be in flight at once
+constexpr int kRing = 16;          // steps whose attention may be in flight at once
 constexpr int kAttnMaxSplit = 8;   // CTAs per slice in one attention launch, at most
 
 // Error bits recorded on the device and reported by lkv_sync.

@@ -167,7 +167,7 @@ lkv_status lkv_decode_step(lkv_ctx *ctx, int32_t layer, int32_t n_layers,
  * The steps run from a captured CUDA graph of 64 steps (cached per argument
  * set), so the host issues one launch per 64 steps. Inside the graph the
  * attention of a step runs concurrently with the boundary tests and
- * selections of up to four following steps (they never read what it writes);
+ * selections of up to fifteen following steps (they never read what it writes);
  * the boundary flags, r_t and selections are those of lkv_decode_step, and
  * the attention outputs agree with it within fp32 rounding (the grid over
  * which a slice's partial softmax sums are split can differ). With profiling
