@@ -224,7 +224,6 @@ lkv_status lkv_create(const lkv_config *cfg, lkv_ctx **out) {
   v.attn_count = (int32_t *)dalloc(c, lkv::kRing * S_all * 4, &st);
   v.attn_part = (float *)dalloc(c, lkv::kRing * S_all * lkv::kAttnMaxSplit *
                                        (int64_t)(k.group * d + 2 * k.group) * 4, &st);
-  v.score_count = (int32_t *)dalloc(c, S_all * 4, &st);
   v.max_pieces = u_cap + max_chunks;
   v.pieces = (int4 *)dalloc(c, S_all * (int64_t)v.max_pieces * sizeof(int4), &st);
   v.chunk_piece = (int32_t *)dalloc(c, S_all * (int64_t)(max_chunks + 1) * 4, &st);
@@ -255,7 +254,6 @@ lkv_status lkv_create(const lkv_config *cfg, lkv_ctx **out) {
   cudaError_t e = cudaSuccess;
   if (e == cudaSuccess) e = cudaMemsetAsync(v.st, 0, LB * sizeof(DecState), c->stream);
   if (e == cudaSuccess) e = cudaMemsetAsync(v.attn_count, 0, lkv::kRing * S_all * 4, c->stream);
-  if (e == cudaSuccess) e = cudaMemsetAsync(v.score_count, 0, S_all * 4, c->stream);
   if (e == cudaSuccess) e = cudaMemsetAsync(v.err, 0, 4, c->stream);
   if (e == cudaSuccess) e = cudaMemsetAsync(ks.n_refined, 0, 8, c->stream);
   if (e == cudaSuccess) e = cudaMemsetAsync(ks.n_inexact, 0, 8, c->stream);

@@ -1201,7 +1201,6 @@ __global__ void k_reset_layer(CtxView v, int layer, int32_t c) {
         plan_rng_cum(v, p, gs)[0] = 0;
       }
       for (int p = 0; p < kRing; ++p) v.attn_count[p * v.S_all + gs] = 0;
-      v.score_count[gs] = 0;
     }
   }
 }

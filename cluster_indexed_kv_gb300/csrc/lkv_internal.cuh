@@ -90,13 +90,12 @@ struct CtxView {
   int32_t max_pieces;
   int32_t *attn_count;        // [kRing step slots][slice] attention CTAs done (last one combines)
   float *attn_part;           // [kRing][slice][kAttnMaxSplit][G * d + 2 * G] CTA partials
-  int32_t *score_count;       // [slice] score CTAs done this step (last one selects)
   int32_t max_chunks;
   int32_t *err;               // device error bits (shared by all layers)
   int64_t *counters;          // [kCounters] work counters (see CounterId)
 };
 
-// Plan-slot views of the double-buffered selection plan.
+// Plan-slot views of the selection plan (kRing slots).
 __host__ __device__ __forceinline__ int32_t *plan_sel(const CtxView &v, int p, int64_t gs) {
   return v.sel + ((int64_t)p * v.S_all + gs) * v.u_cap;
 }
