@@ -815,15 +815,15 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
-// The bf16 part of x (lo = false) or of its residual x - bf16(x) (lo = true):
-// the two parts sum to x within 2^-17 relative.
-__device__ __forceinline__ uint32_t bf16_part(float x, bool lo) {
-  const __nv_bfloat16 h = __float2bfloat16_rn(x);
-  return lo ? (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x - __bfloat162float(h)))
-            : (uint32_t)__bfloat16_as_ushort(h);
-}
+// The bf16 parts of (x0, x1) (lo = false) or of their residuals x - bf16(x)
+// (lo = true), packed low = x0: a value's two parts sum to it within 2^-17
+// relative.
 __device__ __forceinline__ uint32_t bf16_pair(float x0, float x1, bool lo) {
-  return bf16_part(x0, lo) | (bf16_part(x1, lo) << 16);
+  // packed conversions: two values per instruction
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+  const __nv_bfloat162 r = __floats2bfloat162_rn(x0 - __low2float(h), x1 - __high2float(h));
+  const __nv_bfloat162 w = lo ? r : h;
+  return *reinterpret_cast<const uint32_t *>(&w);
 }
 __device__ __forceinline__ uint32_t prmt(uint32_t x, uint32_t y, uint32_t sel) {
   uint32_t r;
@@ -1207,18 +1207,24 @@ __global__ void __launch_bounds__(attn_threads<DT, G>(), attn_min_blocks<DT, G>(
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const int f = f0 + 2 * k;
+          // the source row: on the HBM pool every row is a pool row of the
+          // slice (a selected token's from the plan, a local-buffer token's at
+          // max_prefill + its position); offloaded, selected rows are staging
+          // rows and local-buffer rows decode rows
           const unsigned char *ks = selk, *vs = selv;
+          int64_t row = 0;
           uint32_t n = 16;
-          if (f < nt) {  // a selected row: pool row, or staging row f
-            const int64_t row = tok_rows ? x[k] : f;
-            ks += row * RB;
-            vs += row * RB;
-          } else if (f < total) {  // a local-buffer row
-            ks = deck + (int64_t)(ws + f - nt) * RB;
-            vs = decv + (int64_t)(ws + f - nt) * RB;
+          if (f < nt) {
+            row = tok_rows ? x[k] : f;
+          } else if (f < total) {
+            row = ws + f - nt;
+            if (tok_rows) row += v.n_cap;
+            else { ks = deck; vs = decv; }
           } else {
             n = 0;  // past the slice's last token: zero fill
           }
+          ks += row * RB;
+          vs += row * RB;
           const int r = rh + 2 * k;
           cp_async16(Kd + r * RB + 16 * seg, ks + 16 * seg, n);
           cp_async16(Kd + WB + r * RB + 16 * seg, vs + 16 * seg, n);
