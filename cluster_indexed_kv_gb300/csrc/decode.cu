@@ -1626,7 +1626,7 @@ static void launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 
 static int g_attn_slots = 2 * 152;  // resident attention CTAs on the device
 static int g_attn_split = 0;        // CTAs per slice forced by LKV_ATTN_CTAS_PER_SLICE (0: auto)
-constexpr int kAttnConcurrent = 2;  // pipelined attention grids sized to run this many at once
+constexpr int kAttnConcurrent = 3;  // pipelined attention grids sized to run this many at once
 
 // Split of a slice's chunks over at most kAttnMaxSplit CTAs:
 // `concurrent` grids (consecutive steps of a pipelined graph, else 1) are
