@@ -44,6 +44,8 @@ def parse_args(argv=None):
     p.add_argument("--profile-steps", type=int, default=512)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-probes", action="store_true",
+                   help="skip the host-offload/UVA and 4-layer probes of the default workload")
     p.add_argument("--workload", default="b8_32k",
                    help="synthetic workload (default: the 32K-input, batch-8 decode workload)")
     return p.parse_args(argv)
@@ -181,13 +183,34 @@ def oracle_kmeans_sample(keys_bits, c, n_keys):
     return time.perf_counter() - t0
 
 
+def host_cpu():
+    """(logical CPUs, CPU model) of this host."""
+    model = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                k, _, v = line.partition(":")
+                if k.strip() in ("model name", "Model", "CPU part") and v.strip():
+                    model = v.strip()
+                    if k.strip() == "model name":
+                        break
+    except OSError:
+        pass
+    if model is None:
+        import platform
+        model = platform.processor() or platform.machine()
+    return os.cpu_count(), model
+
+
 def cpu_baseline(K, V, idx0, q, kn, vn, w, n_steps=48, kmeans_keys=1024):
     import synth
     per = oracle_decode_sample(K[0].cpu(), V[0].cpu(), idx0, q, kn, vn, w, n_steps)
     units = w.batch * w.n_kv_heads * w.n_layers
     steps_per_s = 1.0 / (per * units)
     km = oracle_kmeans_sample(synth.to_oracle(K[0, 0]), w.n_clusters, kmeans_keys)
+    nproc, model = host_cpu()
     return {"value": steps_per_s, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "host_nproc": nproc, "host_cpu": model,
             "sample": f"single-threaded C oracle: 1 (sequence, layer, KV head) x {n_steps} decode "
                       f"steps of the full-size workload (teacher-forced from the GPU index), scaled "
                       f"by B x layers x H_kv = {units}; k-means: one Lloyd round of "
@@ -231,6 +254,40 @@ def ncu_traffic(kernel, units):
         return rec["dram_bytes_per_launch"] * units / rec["units_per_launch"]
     except Exception:
         return None
+
+
+def attn_roofline(kern, ctr, w, eb):
+    """(launches, total ms, algorithmic bytes per launch, seconds per launch,
+    GB/s) of the attention from a profiled pass: every K and V row attended
+    once, plus the queries read and the fp32 outputs written."""
+    n_attn, ms_attn = kern["lkv_attn"]
+    slices = ctr["attn_slices"]
+    alg = (ctr["attn_rows"] * 2 * 128 * eb + slices * w.group * 128 * (eb + 4)) / max(n_attn, 1)
+    sec = ms_attn / max(n_attn, 1) / 1e3
+    return n_attn, ms_attn, alg, sec, alg / sec / 1e9
+
+
+def selection_rooflines(kern, ctr, w, eb, hbm_peak, peak_kind):
+    """HBM rooflines of the scoring and selection kernels from a profiled pass
+    in which every slice retrieves. Scoring reads one centroid-operand row per
+    unit (d elements) and the group's queries; selection reads a score, a
+    length and a first pool row per unit (12 bytes) and writes the selected
+    ids, first rows and token offsets (12 bytes a unit) and the pool row of
+    every selected token (4 bytes)."""
+    out = {}
+    n_sc, ms_sc = kern["lkv_score"]
+    n_se, ms_se = kern["lkv_select"]
+    slices = ctr["attn_slices"]
+    b_sc = (ctr["score_units"] * 128 * eb + slices * w.group * 128 * eb) / max(n_sc, 1)
+    b_se = (ctr["score_units"] * 12 + ctr["sel_units"] * 12 + ctr["sel_tokens"] * 4) / max(n_se, 1)
+    for name, n, ms, b in (("k_score", n_sc, ms_sc, b_sc), ("k_select", n_se, ms_se, b_se)):
+        sec = ms / max(n, 1) / 1e3
+        a = b / sec / 1e9 if sec > 0 else None
+        out[name] = {"bound": "hbm", "achieved": a, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": a / hbm_peak if a else None, "alg_bytes_per_launch": b,
+                     "avg_launch_us": sec * 1e6, "launches": int(n),
+                     "peak_source": f"{peak_kind} hbm_gbs (burst copy)"}
+    return out
 
 
 def run_ours(args, rank, world, local):
@@ -301,35 +358,45 @@ def run_ours(args, rank, world, local):
     value = world * T * K_steps / (dec_ms / 1e3)
     mkeys = world * NL * w.batch * w.n_kv_heads * w.n_prefill * w.iters * K_steps / (build_ms / 1e3) / 1e6
 
-    # ---- roofline pass: single-step launches, L2 overwritten before every
-    # step, CUDA events around every kernel on the context stream
+    # ---- roofline pass: the decode first advances through the pipelined graph
+    # until the local buffer has been full for a while, then prof_T
+    # single-step launches run with L2 overwritten before every step and CUDA
+    # events around every kernel on the context stream
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     build_all()
+    warm = max(0, min(T - prof_T, max(2 * w.local_buf, 1024)))
+    if warm:
+        ctx.decode_steps(0, q[:warm], kn[:warm], vn[:warm], w.tau, w.budget, out[:warm],
+                         n_layers=NL)
     ctx.set_profiling(True)
     ctx.profile(reset=True)
-    for t in range(prof_T):
+    for t in range(warm, warm + prof_T):
         flush.fill_(float(t))
         ctx.decode_step(0, q[t], kn[t], vn[t], w.tau, w.budget, out[t], n_layers=NL,
                         boundary=bnd[t])
     kern_p, ctr = ctx.profile(reset=True)
     ctx.set_profiling(False)
     hbm_peak, tc_peak, tc_peak_sus, peak_kind = peaks()
-    n_attn, ms_attn = kern_p["lkv_attn"]
-    slices = ctr["attn_slices"]
     eb = 2 if w.dtype == "bf16" else 4
-    alg_bytes = (ctr["attn_rows"] * 2 * 128 * eb + slices * w.group * 128 * (eb + 4)) / max(n_attn, 1)
-    attn_s = ms_attn / max(n_attn, 1) / 1e3
-    achieved = alg_bytes / attn_s / 1e9
+    n_attn, ms_attn, alg_bytes, attn_s, achieved = attn_roofline(kern_p, ctr, w, eb)
     breakdown = {k: {"launches": int(v[0]), "avg_us": round(v[1] / v[0] * 1e3, 2)}
                  for k, v in kern_p.items() if v[0]}
-    uva = None
-    if w.offload:  # rows read from pinned host memory over the host link
-        n_g, ms_g = kern_p["lkv_gather_offload"]
-        g_bytes = ctr["gather_rows"] * 2 * 128 * eb
-        uva = {"kernel": "k_gather_offload", "bytes": g_bytes, "kernel_ms": ms_g, "launches": int(n_g),
-               "achieved_GBps": g_bytes / (ms_g / 1e3) / 1e9 if ms_g > 0 else None,
-               "note": "bytes read over UVA / total event time of every gather launch "
-                       "(launches on steps without retrieval exit at once)"}
+
+    # ---- scoring and selection kernels: single-step launches in which every
+    # slice retrieves (tau above any r_t), L2 overwritten before every step
+    sel_lane = None
+    sel_T = min(128, T - warm - prof_T)
+    if sel_T >= 16:
+        t0 = warm + prof_T
+        ctx.set_profiling(True)
+        ctx.profile(reset=True)
+        for t in range(t0, t0 + sel_T):
+            flush.fill_(float(t))
+            ctx.decode_step(0, q[t], kn[t], vn[t], 2.0, w.budget, out[t], n_layers=NL)
+        kern_s, ctr_s = ctx.profile(reset=True)
+        ctx.set_profiling(False)
+        sel_lane = selection_rooflines(kern_s, ctr_s, w, eb, hbm_peak, peak_kind)
+        sel_lane["steps"] = f"decode steps {t0}..{t0 + sel_T - 1}, tau 2.0 (every slice retrieves)"
 
     # ---- K-means distance contraction on the tensor cores: one build with
     # CUDA events around every kernel (L2 overwritten first; the keys, 537 MB,
@@ -371,8 +438,8 @@ def run_ours(args, rank, world, local):
             "traffic": ncu_traffic("k_assign_tc", S) if km_kernel == "kmeans_assign_tc" else None,
             "peak_source": f"{peak_kind} bf16_tflops (cuBLAS burst)",
             "flops_per_launch": km_flops, "avg_launch_us": km_s * 1e6, "launches": int(n_km)},
+        "roofline_selection_lane": sel_lane,
         "kernel_breakdown_us": breakdown,
-        "uva_gather": uva,
         "build_breakdown_us": build_breakdown,
         "gpu_launches": launches,
         "clocks": clk,
@@ -416,11 +483,133 @@ def run_ours(args, rank, world, local):
         eb_.synchronize()
         result["e2e"] = {"value": world * T / (ea.elapsed_time(eb_) / 1e3), "unit": UNIT,
                          "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        idx0 = ctx.get_index(0, 0, 0, w.n_prefill)
-        result["cpu_baseline"] = cpu_baseline(K, V, idx0, q, kn, vn, w)
+    want_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
+    idx0 = ctx.get_index(0, 0, 0, w.n_prefill) if want_cpu else None
     ctx.close()
+    if not args.no_probes and args.workload == "b8_32k":
+        del out, flush
+        torch.cuda.empty_cache()
+        result["uva_gather"] = offload_probe(torch, hbm_peak)
+        torch.cuda.empty_cache()
+        result["multi_layer"] = multi_layer_probe(torch, w, hbm_peak, peak_kind)
+        torch.cuda.empty_cache()
+    if want_cpu:
+        result["cpu_baseline"] = cpu_baseline(K, V, idx0, q, kn, vn, w)
     return result
+
+
+def offload_probe(torch, hbm_peak):
+    """The host-offload shape on one layer (8 KV heads x 131072 keys in pinned
+    host memory, C = 8192, budget 2048, L = 512): the UVA gather's rate on
+    steps where every slice retrieves, against the ceiling of a plain UVA
+    read of 1 GiB of pinned host memory on the same link (lkv_uva_read), and
+    the decode rate of this shape through the pipelined graph at tau 0.7."""
+    import synth
+    import cluster_indexed_kv_gb300 as lkv
+    from cluster_indexed_kv_gb300 import _lib
+    w = synth.WORKLOADS["offload"].replace(n_layers=1, iters=2, n_steps=384)
+    T1, T2 = 256, 128
+    K, V = synth.prefill(w, 0, "cuda")
+    q, kn, vn, _ = synth.decode_inputs(w, "cuda")
+    ctx = lkv.Context(batch=1, n_layers=1, n_kv_heads=w.n_kv_heads, group=w.group,
+                      dtype=w.torch_dtype, local_buf=w.local_buf, max_clusters=w.n_clusters,
+                      max_prefill=w.n_prefill, max_steps=w.n_steps, max_budget=w.budget,
+                      offload=True)
+    ctx.build_index(0, K, V, w.n_clusters, w.iters, 1)
+    del K, V
+    out = torch.empty(w.n_steps, 1, 1, w.n_heads, 128, device="cuda")
+    ctx.sync()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(ctx.stream)
+    ctx.decode_steps(0, q[:T1], kn[:T1], vn[:T1], w.tau, w.budget, out[:T1])
+    e1.record(ctx.stream)
+    e1.synchronize()
+    steps_per_s = T1 / (e0.elapsed_time(e1) / 1e3)
+    ctx.set_profiling(True)
+    ctx.profile(reset=True)
+    for t in range(T1, T1 + T2):
+        ctx.decode_step(0, q[t], kn[t], vn[t], 2.0, w.budget, out[t])
+    kern, ctr = ctx.profile(reset=True)
+    ctx.close()
+    n_g, ms_g = kern["lkv_gather_offload"]
+    g_bytes = ctr["gather_rows"] * 2 * 128 * 2
+    achieved = g_bytes / (ms_g / 1e3) / 1e9
+    # the link's ceiling: plain streaming read of pinned host memory over UVA
+    nbytes = 1 << 30
+    host = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    host.fill_(1)
+    dst = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    best = float("inf")
+    for _ in range(4):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        _lib.lkv_uva_read(host.data_ptr(), dst.data_ptr(), nbytes, torch.cuda.current_stream().cuda_stream)
+        b.record()
+        b.synchronize()
+        best = min(best, a.elapsed_time(b))
+    ceiling = nbytes / (best / 1e3) / 1e9
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    dst.copy_(host, non_blocking=True)
+    b.record()
+    b.synchronize()
+    dma = nbytes / (a.elapsed_time(b) / 1e3) / 1e9
+    return {"kernel": "k_gather_offload", "bound": "host link", "achieved": achieved,
+            "peak": ceiling, "unit": "GB/s", "frac": achieved / ceiling,
+            "peak_source": "lkv_uva_read: plain 16-byte UVA reads of 1 GiB of pinned host memory "
+                           "on this box (best of 4)",
+            "dma_h2d_GBps": dma, "bytes": g_bytes, "launches": int(n_g),
+            "avg_launch_us": ms_g / max(n_g, 1) * 1e3,
+            "workload": "1 layer of the host-offload shape: 8 KV heads x 131072 keys in pinned "
+                        "host memory, C=8192, budget 2048, L=512; gather timed on 128 steps "
+                        "where every slice retrieves",
+            "offload_decode_steps_per_s": steps_per_s,
+            "offload_decode_note": f"{T1} steps at tau {w.tau} through the pipelined graph"}
+
+
+def multi_layer_probe(torch, w0, hbm_peak, peak_kind):
+    """The 32K-input, batch-8 workload with 4 attention layers decoded in one
+    call per step (4 x 64 slices, about 200 MB of selected and local-buffer
+    rows per step, more than L2 holds): decode steps/s through the pipelined
+    graph, and the attention roofline of one 4-layer launch with L2
+    overwritten before every step."""
+    import synth
+    import cluster_indexed_kv_gb300 as lkv
+    NL, T1, T2 = 4, 1024, 64
+    w = w0.replace(n_layers=NL, n_steps=T1 + T2)
+    ctx = lkv.Context(batch=w.batch, n_layers=NL, n_kv_heads=w.n_kv_heads, group=w.group,
+                      dtype=w.torch_dtype, local_buf=w.local_buf, max_clusters=w.n_clusters,
+                      max_prefill=w.n_prefill, max_steps=w.n_steps, max_budget=w.budget)
+    for layer in range(NL):
+        K, V = synth.prefill(w, layer, "cuda")
+        ctx.build_index(layer, K, V, w.n_clusters, w.iters, 1 + layer)
+        del K, V
+    q, kn, vn, _ = synth.decode_inputs(w, "cuda")
+    out = torch.empty(w.n_steps, w.batch, NL, w.n_heads, 128, device="cuda")
+    ctx.sync()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(ctx.stream)
+    ctx.decode_steps(0, q[:T1], kn[:T1], vn[:T1], w.tau, w.budget, out[:T1], n_layers=NL)
+    e1.record(ctx.stream)
+    e1.synchronize()
+    steps_per_s = T1 / (e0.elapsed_time(e1) / 1e3)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+    ctx.set_profiling(True)
+    ctx.profile(reset=True)
+    for t in range(T1, T1 + T2):
+        flush.fill_(float(t))
+        ctx.decode_step(0, q[t], kn[t], vn[t], w.tau, w.budget, out[t], n_layers=NL)
+    kern, ctr = ctx.profile(reset=True)
+    ctx.close()
+    n_attn, _, alg, sec, achieved = attn_roofline(kern, ctr, w, 2)
+    return {"workload": f"b8_32k x {NL} layers (one decode call per step for all layers)",
+            "decode_steps_per_s": steps_per_s, "tokens_per_s": steps_per_s * w.batch,
+            "decode_note": f"steps 0..{T1 - 1} through the pipelined graph",
+            "attn_roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak,
+                              "unit": "GB/s", "frac": achieved / hbm_peak,
+                              "alg_bytes_per_launch": alg, "avg_launch_us": sec * 1e6,
+                              "launches": int(n_attn), "peak_source": f"{peak_kind} hbm_gbs",
+                              "l2": "256 MB written before every step"}}
 
 
 # ---------------------------------------------------------------- reference arm
@@ -457,6 +646,7 @@ def run_reference(args, rank, world):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": config_of(w, world),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "host_nproc": host_cpu()[0], "host_cpu": host_cpu()[1],
                              "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 

@@ -154,3 +154,8 @@ class Context:
 
     def sync(self) -> None:
         _lib.lkv_sync(self._ctx)
+
+    def diag_wait_timeout(self, limit_ns: int) -> None:
+        """Failure-path check: a device wait that nothing completes runs out
+        after limit_ns; the next sync() raises LKV_ETIMEOUT."""
+        _lib.lkv_diag_wait_timeout(self._ctx, limit_ns)

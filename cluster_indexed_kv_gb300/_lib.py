@@ -20,7 +20,8 @@ LKV_DTYPE_FP32, LKV_DTYPE_BF16 = 0, 1
 EXPORTED = ("lkv_create", "lkv_destroy", "lkv_build_index", "lkv_load_index",
             "lkv_decode_step", "lkv_decode_steps", "lkv_get_index", "lkv_get_decode_state",
             "lkv_sync", "lkv_last_error", "lkv_set_profiling", "lkv_get_profile",
-            "lkv_kmeans_static", "lkv_set_kmeans_filter")
+            "lkv_kmeans_static", "lkv_kmeans_static_status", "lkv_set_kmeans_filter",
+            "lkv_diag_wait_timeout", "lkv_uva_read")
 LKV_FILTER_TENSOR, LKV_FILTER_SIMT = 0, 1
 
 
@@ -95,6 +96,12 @@ def load(path: str = LIB_PATH):
         L.lkv_get_decode_state.restype = st
         L.lkv_kmeans_static.argtypes = [vp, i32, i64, i32, i32, u64, vp, vp, vp]
         L.lkv_kmeans_static.restype = st
+        L.lkv_kmeans_static_status.argtypes = [vp]
+        L.lkv_kmeans_static_status.restype = st
+        L.lkv_uva_read.argtypes = [vp, vp, i64, vp]
+        L.lkv_uva_read.restype = st
+        L.lkv_diag_wait_timeout.argtypes = [vp, i64]
+        L.lkv_diag_wait_timeout.restype = st
         L.lkv_sync.argtypes = [vp]
         L.lkv_sync.restype = st
         L.lkv_last_error.argtypes = [vp]
@@ -154,10 +161,10 @@ def lkv_get_profile(ctx, reset: bool = False):
     """(dict kernel -> (launches, total_ms), dict of work counters)."""
     stats = (lkv_kernel_stat * 32)()
     n = C.c_int32(0)
-    ctr = (C.c_int64 * 4)()
+    ctr = (C.c_int64 * 6)()
     _check(load().lkv_get_profile(ctx, stats, 32, C.byref(n), ctr, 1 if reset else 0), ctx)
     kern = {stats[i].name.decode(): (stats[i].launches, stats[i].total_ms) for i in range(n.value)}
-    names = ("attn_rows", "attn_slices", "score_units", "gather_rows")
+    names = ("attn_rows", "attn_slices", "score_units", "gather_rows", "sel_units", "sel_tokens")
     return kern, {k: ctr[i] for i, k in enumerate(names)}
 
 
@@ -179,6 +186,18 @@ def lkv_kmeans_static(keys_ptr, dtype, n_tokens, n_clusters, iters, seed, cent_p
                       stream_ptr) -> None:
     _check(load().lkv_kmeans_static(keys_ptr, dtype, n_tokens, n_clusters, iters, seed, cent_ptr,
                                     assign_ptr, stream_ptr), None)
+
+
+def lkv_kmeans_static_status(stream_ptr) -> None:
+    _check(load().lkv_kmeans_static_status(stream_ptr), None)
+
+
+def lkv_uva_read(host_ptr, dev_ptr, nbytes: int, stream_ptr) -> None:
+    _check(load().lkv_uva_read(host_ptr, dev_ptr, nbytes, stream_ptr), None)
+
+
+def lkv_diag_wait_timeout(ctx, limit_ns: int) -> None:
+    _check(load().lkv_diag_wait_timeout(ctx, limit_ns), ctx)
 
 
 def lkv_sync(ctx) -> None:

@@ -529,6 +529,8 @@ lkv_status lkv_get_profile(lkv_ctx *c, lkv_kernel_stat *stats, int32_t capacity,
     counters[1] = h[lkv::kCntAttnSlices];
     counters[2] = h[lkv::kCntScoreUnits];
     counters[3] = h[lkv::kCntGatherRows];
+    counters[4] = h[lkv::kCntSelUnits];
+    counters[5] = h[lkv::kCntSelTokens];
   }
   if (reset) {
     for (int k = 0; k < lkv::kPNum; ++k) {
@@ -538,6 +540,37 @@ lkv_status lkv_get_profile(lkv_ctx *c, lkv_kernel_stat *stats, int32_t capacity,
     cudaError_t e = cudaMemset(c->v.counters, 0, lkv::kCounters * 8);
     if (e != cudaSuccess) return cuda_fail(c, e, "lkv_get_profile");
   }
+  return LKV_OK;
+}
+
+lkv_status lkv_uva_read(const void *host_src, void *dev_dst, int64_t bytes, void *stream) {
+  if (!host_src || !dev_dst || bytes < 0 || bytes % 16 != 0 ||
+      ((uintptr_t)host_src | (uintptr_t)dev_dst) % 16 != 0) {
+    lkv::set_unbound_error("lkv_uva_read: null pointer, or size/address not a multiple of 16");
+    return LKV_EINVAL;
+  }
+  cudaPointerAttributes attr{};
+  cudaError_t e = cudaPointerGetAttributes(&attr, host_src);
+  if (e != cudaSuccess || attr.type != cudaMemoryTypeHost) {
+    cudaGetLastError();
+    lkv::set_unbound_error("lkv_uva_read: host_src is not pinned host memory");
+    return LKV_EINVAL;
+  }
+  e = lkv::launch_uva_read(attr.devicePointer ? attr.devicePointer : host_src, dev_dst, bytes,
+                           (cudaStream_t)stream);
+  if (e != cudaSuccess) {
+    lkv::set_unbound_error((std::string("lkv_uva_read: ") + cudaGetErrorString(e)).c_str());
+    return LKV_ECUDA;
+  }
+  return LKV_OK;
+}
+
+lkv_status lkv_diag_wait_timeout(lkv_ctx *c, int64_t limit_ns) {
+  lkv_status s = check_usable(c);
+  if (s != LKV_OK) return s;
+  if (limit_ns < 0 || limit_ns > 1000000000) return fail(c, LKV_EINVAL, "limit_ns must be 0..1e9");
+  cudaError_t e = lkv::launch_diag_wait(c->v, (uint64_t)limit_ns, c->stream);
+  if (e != cudaSuccess) return cuda_fail(c, e, "lkv_diag_wait_timeout");
   return LKV_OK;
 }
 

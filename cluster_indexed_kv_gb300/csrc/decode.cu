@@ -600,6 +600,8 @@ __device__ void select_units(const CtxView &v, int64_t gs, int U, int budget, in
   if (tid == 0) {
     *plan_nsel(v, ps, gs) = s_nsel;
     *plan_ntok(v, ps, gs) = s_ntok;
+    atomicAdd((unsigned long long *)&v.counters[kCntSelUnits], (unsigned long long)s_nsel);
+    atomicAdd((unsigned long long *)&v.counters[kCntSelTokens], (unsigned long long)s_ntok);
     plan_rng_cum(v, ps, gs)[s_nsel] = s_ntok;
     if (nsc <= v.max_chunks) v.chunk_piece[gs * (int64_t)(v.max_chunks + 1) + nsc] = s_npieces;
     if (s_ntok > budget || s_ntok > v.sel_cap || s_npieces > v.max_pieces || nsc > v.max_chunks)
@@ -1594,6 +1596,57 @@ __global__ void __launch_bounds__(attn_threads<DT, G>(), attn_min_blocks<DT, G>(
   }
 }
 
+
+// ---------------------------------------------------------------- host-link ceiling
+
+// Plain streaming read of pinned, mapped host memory into device memory:
+// every thread moves 16-byte vectors, eight loads in flight, over a grid
+// that fills the GPU. It does what the offload gather does minus the
+// selection (one contiguous run), so its rate is the ceiling that gather is
+// measured against on the same link.
+__global__ void __launch_bounds__(256) k_uva_read(const uint4 *src, uint4 *dst, int64_t n16) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  for (; i + 7 * stride < n16; i += 8 * stride) {
+    uint4 r[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) r[e] = __ldcg(src + i + e * stride);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) dst[i + e * stride] = r[e];
+  }
+  for (; i < n16; i += stride) dst[i] = __ldcg(src + i);
+}
+
+cudaError_t launch_uva_read(const void *host_src, void *dev_dst, int64_t bytes, cudaStream_t st) {
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  k_uva_read<<<sms * 8, 256, 0, st>>>((const uint4 *)host_src, (uint4 *)dev_dst, bytes / 16);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- failure-path check
+
+// One CTA waits on an mbarrier that nothing completes. The wait gives up
+// after limit_ns, records the timeout bit exactly as a kernel whose bounded
+// wait ran out does, and the CTA returns.
+__global__ void k_diag_wait(CtxView v, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  const bool ok = mbar_wait_bounded(&bar, 0, limit_ns);
+  __syncthreads();
+  if (!ok && threadIdx.x == 0) set_err(v.err, kErrTimeout);
+}
+
+cudaError_t launch_diag_wait(const CtxView &v, uint64_t limit_ns, cudaStream_t st) {
+  k_diag_wait<<<1, 32, 0, st>>>(v, limit_ns);
+  return cudaGetLastError();
+}
 
 // ---------------------------------------------------------------- host
 

@@ -1243,6 +1243,29 @@ static cudaError_t finish_pool(const CtxView &v, int layer, const KmeansScratch 
   return cudaGetLastError();
 }
 
+// Dynamic shared-memory limits of the K-means kernels. A kernel attribute
+// applies to the current device only, so it is set once per (device, key
+// dtype), under a lock, and every return code is checked.
+static std::mutex g_km_attr_mu;
+static bool g_km_attr_done[64][2] = {};
+
+template <int DT>
+static cudaError_t kmeans_kernel_attributes() {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_km_attr_mu);
+  if (g_km_attr_done[dev][DT]) return cudaSuccess;
+  e = cudaFuncSetAttribute(k_assign_simt<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAsSmem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(k_assign_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(k_refine_crowded<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
+  if (e == cudaSuccess) g_km_attr_done[dev][DT] = true;
+  return e;
+}
+
 template <int DT>
 static cudaError_t kmeans_build_t(const CtxView &v, int layer, const KmeansScratch &ks,
                                   const void *keys, const void *values, int64_t n,
@@ -1253,12 +1276,9 @@ static cudaError_t kmeans_build_t(const CtxView &v, int layer, const KmeansScrat
   const int c_cap = v.u_cap - v.t_cap;
   const int c_pad = (c + kTcN - 1) / kTcN * kTcN;  // |c|^2 table padded with +inf
   const int64_t amb_cap = (int64_t)S * v.n_cap;
-  static bool attr_done[2] = {false, false};
-  if (!attr_done[DT]) {
-    cudaFuncSetAttribute(k_assign_simt<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAsSmem);
-    cudaFuncSetAttribute(k_assign_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmem);
-    cudaFuncSetAttribute(k_refine_crowded<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
-    attr_done[DT] = true;
+  {
+    cudaError_t e = kmeans_kernel_attributes<DT>();
+    if (e != cudaSuccess) return e;
   }
   // tensor-core filter (bf16 keys): TMA descriptors of the keys and of the
   // whole centroid-operand table, one persistent CTA per SM
@@ -1389,7 +1409,11 @@ constexpr size_t kSoCount = kSoCntPart + al256((size_t)kMaxParts * kStaticMaxClu
 constexpr size_t kSoOffs = kSoCount + al256(kStaticMaxClusters * 4);
 constexpr size_t kSoAmb = kSoOffs + al256(kStaticMaxClusters * 4);
 constexpr size_t kSoMisc = kSoAmb + al256(kStaticMaxTokens * sizeof(int4));
-constexpr size_t kSoInit = kSoMisc + 256;  // misc: amb_count, err (int32), n_refined, n_inexact (int64), amb_crowd (int32)
+// misc: amb_count (int32 at 0), n_refined and n_inexact (int64 at 8, 16),
+// amb_crowd (int32 at 24), all cleared by every call; the device error bits
+// (int32 at kSoErr) are sticky until lkv_kmeans_static_status reads them
+constexpr size_t kSoErr = 128;
+constexpr size_t kSoInit = kSoMisc + 256;
 constexpr size_t kSoShuffle = kSoInit + al256(kStaticMaxClusters * 8);
 constexpr size_t kSoCentOp = kSoShuffle + al256(kStaticMaxTokens * 8);
 constexpr size_t kSoPerm = kSoCentOp + al256((size_t)kStaticMaxClusters * kHeadDim * 4);
@@ -1438,7 +1462,7 @@ static cudaError_t kmeans_static_t(unsigned char *base, const void *keys, int64_
   v.cent_op = base + kSoCentOp;
   v.assign = assign;
   v.perm = (int32_t *)(base + kSoPerm);
-  v.err = (int32_t *)(base + kSoMisc + 4);
+  v.err = (int32_t *)(base + kSoMisc + kSoErr);
   KmeansScratch ks{};
   ks.knorm = (float *)(base + kSoKnorm);
   ks.c2 = (float *)(base + kSoC2);
@@ -1457,8 +1481,9 @@ static cudaError_t kmeans_static_t(unsigned char *base, const void *keys, int64_
   quiet.counting = false;
   const int64_t amb_cap = n;
   const float eps = 0x1p-15f;
-  // the array keeps the previous call's contents: clear what must start at zero
-  cudaError_t e = cudaMemsetAsync(base + kSoMisc, 0, 256, st);
+  // the array keeps the previous call's contents: clear what must start at
+  // zero (the error bits stay until lkv_kmeans_static_status collects them)
+  cudaError_t e = cudaMemsetAsync(base + kSoMisc, 0, kSoErr, st);
   if (e != cudaSuccess) return e;
   k_static_init_indices<<<1, 1024, 0, st>>>(n, c, seed, (int64_t *)(base + kSoShuffle), ks.init_idx);
   k_init_cent<DT><<<dim3(c, 1), kHeadDim, 0, st>>>(keys, n, c, ks.init_idx, v.cent32, 0, v.u_cap);
@@ -1485,7 +1510,9 @@ static cudaError_t kmeans_static_t(unsigned char *base, const void *keys, int64_
 
 // Per-device address of g_kmeans_scratch. In host code the array's name is
 // only a host-side stand-in, so the device address is looked up once per
-// device (with that device current) and cached.
+// device (with that device current) and cached for the life of the process;
+// a cudaDeviceReset reloads the module and invalidates the cached address, so
+// calls after a reset are not supported.
 static std::mutex g_static_mu;
 static void *g_static_addr[64] = {};
 
@@ -1551,5 +1578,32 @@ extern "C" lkv_status lkv_kmeans_static(const void *keys, int32_t dtype, int64_t
   return LKV_OK;
 }
 
-namespace lkv {
-}  // namespace lkv
+extern "C" lkv_status lkv_kmeans_static_status(void *stream) {
+  using namespace lkv;
+  void *base = nullptr;
+  cudaError_t e = static_scratch_address(&base);
+  int32_t bits = 0;
+  int32_t *err = (int32_t *)((unsigned char *)base + kSoMisc + kSoErr);
+  cudaStream_t st = (cudaStream_t)stream;
+  if (e == cudaSuccess) e = cudaMemcpyAsync(&bits, err, sizeof bits, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e == cudaSuccess && bits) e = cudaMemsetAsync(err, 0, sizeof bits, st);
+  if (e == cudaSuccess && bits) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) {
+    set_unbound_error((std::string("lkv_kmeans_static_status: ") + cudaGetErrorString(e)).c_str());
+    return LKV_ECUDA;
+  }
+  if (bits & kErrTimeout) {
+    set_unbound_error("lkv_kmeans_static: a device-side wait gave up");
+    return LKV_ETIMEOUT;
+  }
+  if (bits & kErrCapacity) {
+    set_unbound_error("lkv_kmeans_static: the settlement queue of the built-in scratch overflowed");
+    return LKV_ECAPACITY;
+  }
+  if (bits) {
+    set_unbound_error("lkv_kmeans_static: a device-side invariant check failed");
+    return LKV_ECUDA;
+  }
+  return LKV_OK;
+}

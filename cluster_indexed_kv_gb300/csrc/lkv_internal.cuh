@@ -123,7 +123,7 @@ __host__ __device__ __forceinline__ int32_t *plan_chunk_count(const CtxView &v, 
 
 // Work counters accumulated on the device (read by lkv_get_profile).
 enum CounterId : int { kCntAttnRows = 0, kCntScoreUnits = 1, kCntGatherRows = 2,
-                       kCntAttnSlices = 3, kCounters = 8 };
+                       kCntAttnSlices = 3, kCntSelUnits = 4, kCntSelTokens = 5, kCounters = 8 };
 
 // Kernel kinds for launch counting and event timing.
 enum ProfKind : int {
@@ -320,6 +320,12 @@ struct Pipe {
 // onto a side stream as described above.
 cudaError_t launch_decode_step(const CtxView &v, const StepArgs &a, cudaStream_t stream,
                                Prof &prof, const Pipe *pipe = nullptr);
+// Streaming read of `bytes` (a multiple of 16) of pinned host memory into
+// device memory by plain 16-byte loads over UVA (the host-link ceiling).
+cudaError_t launch_uva_read(const void *host_src, void *dev_dst, int64_t bytes, cudaStream_t stream);
+// One CTA whose bounded wait on a barrier nobody completes runs out after
+// limit_ns and records kErrTimeout (tests the failure path).
+cudaError_t launch_diag_wait(const CtxView &v, uint64_t limit_ns, cudaStream_t stream);
 // Error text of calls that have no context (read with lkv_last_error(NULL)).
 void set_unbound_error(const char *msg);
 // One-time kernel attributes (dynamic shared memory limits), before any capture.

@@ -203,10 +203,10 @@ typedef struct lkv_kernel_stat {
 lkv_status lkv_set_profiling(lkv_ctx *ctx, int32_t enable);
 
 /* Blocking. stats: host array of capacity entries (one per kernel kind; the
- * number of kinds goes to *n_stats). counters (optional, host int64[4]):
+ * number of kinds goes to *n_stats). counters (optional, host int64[6]):
  * rows attended (K and V rows read by the attention), attention slices
- * processed, units scored, rows gathered from host memory. reset != 0 zeroes
- * everything afterwards. */
+ * processed, units scored, rows gathered from host memory, units selected,
+ * tokens selected. reset != 0 zeroes everything afterwards. */
 lkv_status lkv_get_profile(lkv_ctx *ctx, lkv_kernel_stat *stats, int32_t capacity,
                            int32_t *n_stats, int64_t *counters, int32_t reset);
 
@@ -246,8 +246,10 @@ typedef struct lkv_decode_state {
  * the whole GPU up front, so an extra cudaMalloc fails or fragments its
  * pool), or code that must not risk the implicit device synchronisation of
  * cudaMalloc/cudaFree. It computes exactly what lkv_build_index computes for
- * a slice (same seeded initialisation with seed, same Lloyd rounds, same
- * bit-exact centroids and assignment), without the K/V pool.
+ * one slice (same Lloyd rounds, same bit-exact centroids and assignment),
+ * without the K/V pool. The initialisation is drawn from `seed` as given:
+ * lkv_build_index seeds slice s = b*H_kv + h with its seed + s, so to
+ * reproduce slice s of a build, pass the build's seed + s.
  * keys: device, [n_tokens][d] in dtype; centroids: device fp32
  * [n_clusters][d], out; assign: device int32 [n_tokens], out; stream: a
  * cudaStream_t or NULL. Nothing is allocated: every intermediate lives in one
@@ -258,15 +260,44 @@ typedef struct lkv_decode_state {
  * overlap on the GPU (different streams, different host threads) race: order
  * them on one stream. The first call on each device looks up the array's
  * device address and sets kernel attributes, so make that first call before
- * any stream capture. Asynchronous on stream; errors: LKV_EINVAL, LKV_ECUDA
- * (text via lkv_last_error(NULL)). */
+ * any stream capture; the address is kept for the life of the process, so
+ * calls after a cudaDeviceReset are not supported. Asynchronous on stream;
+ * errors returned at once: LKV_EINVAL, LKV_ECUDA (text via
+ * lkv_last_error(NULL)). Device-side anomalies of the call (an overflowing
+ * settlement queue, a failed invariant check) are recorded in the array and
+ * kept until lkv_kmeans_static_status collects them. */
 lkv_status lkv_kmeans_static(const void *keys, int32_t dtype, int64_t n_tokens,
                              int32_t n_clusters, int32_t iters, uint64_t seed,
                              float *centroids, int32_t *assign, void *stream);
 
+/* Blocking companion of lkv_kmeans_static (it allocates nothing either):
+ * waits for `stream`, then reports and clears the device-side anomalies that
+ * the lkv_kmeans_static calls on the current device recorded since the last
+ * status call: LKV_OK, LKV_ECAPACITY, LKV_ETIMEOUT or LKV_ECUDA (text via
+ * lkv_last_error(NULL)). */
+lkv_status lkv_kmeans_static_status(void *stream);
+
 /* Blocking read of one (layer, sequence) decode state. */
 lkv_status lkv_get_decode_state(lkv_ctx *ctx, int32_t layer, int32_t seq,
                                 lkv_decode_state *out);
+
+/* Host-link ceiling for the offload gather [ParisKV, 系统级创新 1: kernels
+ * read the chosen K/V rows from host memory over UVA]: one kernel streams
+ * `bytes` of pinned host memory (cudaHostAlloc / cudaHostRegister) into
+ * device memory with plain 16-byte loads over UVA, a contiguous read with the
+ * load pattern of the gather. host_src: pinned host, dev_dst: device, both
+ * 16-byte aligned, bytes a multiple of 16. Asynchronous on `stream`
+ * (cudaStream_t or NULL). Errors: LKV_EINVAL, LKV_ECUDA (text via
+ * lkv_last_error(NULL)). */
+lkv_status lkv_uva_read(const void *host_src, void *dev_dst, int64_t bytes, void *stream);
+
+/* Failure-path check (no counterpart in the pages): launches, on the
+ * context's stream, one CTA that waits on a barrier that nothing completes.
+ * The wait gives up after limit_ns nanoseconds (0..1e9, else LKV_EINVAL) and
+ * records the timeout in the context exactly as a decode or K-means kernel
+ * whose bounded wait ran out, so the next lkv_sync returns LKV_ETIMEOUT and
+ * clears it; the context stays usable. Asynchronous. */
+lkv_status lkv_diag_wait_timeout(lkv_ctx *ctx, int64_t limit_ns);
 
 /* Wait for the context's stream; report device-side anomalies. */
 lkv_status lkv_sync(lkv_ctx *ctx);

@@ -250,14 +250,16 @@ def attention(q_group: np.ndarray, k_rows: np.ndarray, v_rows: np.ndarray) -> np
 
 
 def decode(keys, values, assign_, cent, q, k_new, v_new, *, n_clusters, local_buf,
-           tau, budget, attn_mask=None, want_seg_cent=False, want_sel=True):
+           tau, budget, attn_mask=None, want_seg_cent=False, want_sel=True, max_sel=None):
     """Run one (sequence, layer) decode through the oracle.
 
     keys/values [H_kv, N, d]; assign_ [H_kv, N]; cent [H_kv, C, d] fp32;
     q [T, H, d]; k_new/v_new [T, H_kv, d]. Returns a dict of numpy arrays.
     want_sel=False skips the per-step selection lists (n_sel and n_tok are
     still recorded); with lists, each holds at most budget + C ids (a unit
-    that fits adds at least one token, except empty clusters).
+    that fits adds at least one token, except empty clusters). max_sel caps
+    the recorded list length for long runs (the call fails if a selection is
+    longer).
     """
     keys, values = np.ascontiguousarray(keys), np.ascontiguousarray(values)
     q, k_new, v_new = (np.ascontiguousarray(x) for x in (q, k_new, v_new))
@@ -269,7 +271,7 @@ def decode(keys, values, assign_, cent, q, k_new, v_new, *, n_clusters, local_bu
     dt = dtype_of(q)
     c = n_clusters
     ucap = c + T
-    max_sel = min(ucap, budget + c)
+    max_sel = min(ucap, budget + c) if max_sel is None else min(ucap, budget + c, max_sel)
     mask = None if attn_mask is None else _arr(attn_mask, np.uint8)
     args = DecodeArgs(dt, hkv, g, d, n, c, local_buf, T, tau, budget, _p(keys), _p(values),
                       _p(assign_), _p(cent), _p(q), _p(k_new), _p(v_new), _p(mask))

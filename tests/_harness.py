@@ -120,3 +120,94 @@ def compare_segments(ctx, w, o, b, li, layer):
         assert np.array_equal(ix["unit_len"][C:], o["seg_len"])
         assert np.array_equal(ix["centroids"][C:].view(np.uint32),
                               o["seg_cent"][:, h].view(np.uint32))
+
+
+# ---------------------------------------------------------------- graph path at full size
+
+def run_graph(ctx, w, q, kn, vn, *, seqs, tau=None, budget=None, chunk=512, keep_out=True):
+    """A whole run through lkv_decode_steps (the pipelined CUDA graph that the
+    benchmark times), in chunks of `chunk` steps. Returns host arrays:
+    boundary [T,B], r [T,B], n_sel [T,B,Hkv] for every sequence; for the
+    sequences in `seqs`, out {b: [T,H,d]} and the selections at retrieval
+    steps sel {(t, b, h): ascending ids}."""
+    tau = w.tau if tau is None else tau
+    budget = w.budget if budget is None else budget
+    T, B = q.shape[0], q.shape[1]
+    Hkv, H = w.n_kv_heads, w.n_heads
+    dev = q.device
+    out = torch.empty(T, B, 1, H, 128, dtype=torch.float32, device=dev)
+    bnd = torch.zeros(T, B, 1, dtype=torch.uint8, device=dev)
+    r = torch.zeros(T, B, 1, dtype=torch.float32, device=dev)
+    nsel = torch.zeros(T, B, 1, Hkv, dtype=torch.int32, device=dev)
+    selbuf = torch.full((chunk, B, 1, Hkv, ctx.u_cap), -1, dtype=torch.int32, device=dev)
+    sel = {}
+    sidx = torch.tensor(list(seqs), dtype=torch.long, device=dev)
+    for c0 in range(0, T, chunk):
+        c1 = min(T, c0 + chunk)
+        ctx.decode_steps(0, q[c0:c1], kn[c0:c1], vn[c0:c1], tau, budget, out[c0:c1],
+                         selected_units=selbuf[:c1 - c0], n_selected=nsel[c0:c1],
+                         boundary=bnd[c0:c1], r_out=r[c0:c1])
+        ctx.sync()
+        fl = bnd[c0:c1, :, 0].index_select(1, sidx).cpu().numpy()
+        ns = nsel[c0:c1, :, 0].index_select(1, sidx).cpu().numpy()
+        kmax = int(ns.max()) if ns.size else 0
+        steps = np.flatnonzero(fl.any(axis=1))
+        if len(steps) and kmax:
+            st = torch.as_tensor(steps, device=dev)
+            got = selbuf[:, :, 0, :, :kmax].index_select(0, st).index_select(1, sidx).cpu().numpy()
+            for i, t in enumerate(steps):
+                for j, b in enumerate(seqs):
+                    if fl[t, j]:
+                        for h in range(Hkv):
+                            sel[(c0 + int(t), b, h)] = np.sort(got[i, j, h, :ns[t, j, h]])
+    res = dict(boundary=bnd[:, :, 0].cpu().numpy(), r=r[:, :, 0].cpu().numpy(),
+               n_sel=nsel[:, :, 0].cpu().numpy(), sel=sel)
+    if keep_out:
+        res["out"] = {b: out[:, b, 0].cpu().numpy() for b in seqs}
+    return res
+
+
+def spawn_pool(workers):
+    """Process pool for oracle work (spawn: safe after the parent used the GPU)."""
+    import concurrent.futures as cf
+    import multiprocessing as mp
+    return cf.ProcessPoolExecutor(max_workers=workers, mp_context=mp.get_context("spawn"))
+
+
+def oracle_inputs(tmpdir, tag, w, K, V, idx, q, kn, vn, b, li=0):
+    """Write one sequence's oracle inputs (teacher-forced index `idx`: a list
+    over KV heads of dicts with 'assign' and 'centroids') as .npy files."""
+    import os
+    C = w.n_clusters
+    arrays = dict(keys=synth.to_oracle(K[b]), values=synth.to_oracle(V[b]),
+                  assign=np.stack([ix["assign"] for ix in idx]).astype(np.int32),
+                  cent=np.stack([ix["centroids"][:C] for ix in idx]).astype(np.float32),
+                  q=synth.to_oracle(q[:, b, li]), k_new=synth.to_oracle(kn[:, b, li]),
+                  v_new=synth.to_oracle(vn[:, b, li]))
+    paths = {}
+    for k, a in arrays.items():
+        p = os.path.join(str(tmpdir), f"{tag}_{k}.npy")
+        np.save(p, a)
+        paths[k] = p
+    return paths
+
+
+def compare_graph_run(g, o, w, b, *, label=""):
+    """Bit-exact flags, r_t, selection sizes and selections; tolerance on the
+    attention outputs at the oracle's sampled steps."""
+    bnd = g["boundary"][:, b]
+    assert np.array_equal(bnd, o["flag"]), \
+        f"{label} flags differ at {np.flatnonzero(bnd != o['flag'])[:10]}"
+    assert np.array_equal(g["r"][:, b].view(np.uint32), o["r32"].view(np.uint32)), f"{label} r_t differs"
+    assert np.array_equal(g["n_sel"][:, b], o["n_sel"]), f"{label} n_selected differs"
+    n_checked = 0
+    for (t, h), want in o["sel"].items():
+        assert np.array_equal(g["sel"][(t, b, h)], want), f"{label} selection differs t={t} h={h}"
+        n_checked += 1
+    steps = o["attn_steps"]
+    got = g["out"][b][steps].astype(np.float64)
+    err = np.abs(got - o["out"])
+    ok = err <= ATOL + RTOL * np.abs(o["out"])
+    assert ok.all(), f"{label} attention mismatch: max abs err {err.max():.3e}"
+    return dict(n_sel_checked=n_checked, n_attn_steps=len(steps), max_abs_err=float(err.max()),
+                n_boundary=int(o["flag"].sum()), n_evicted=o["n_evicted"])

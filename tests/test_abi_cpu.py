@@ -65,6 +65,19 @@ def test_null_arguments_are_rejected(libpath):
     assert L.lkv_set_kmeans_filter(None, _lib.LKV_FILTER_SIMT) == _lib.LKV_EINVAL
 
 
+def test_injected_allocation_failure_without_device(libpath, monkeypatch):
+    """LKV_FAIL_ALLOC_AFTER=0 fails the first allocation of lkv_create, before
+    any CUDA call, so the status path is checked here without a GPU."""
+    _lib.load(libpath)
+    monkeypatch.setenv("LKV_FAIL_ALLOC_AFTER", "0")
+    cfg = _lib.lkv_config(batch=1, n_layers=1, n_kv_heads=8, group=4, head_dim=128, dtype=1,
+                          local_buf=16, max_clusters=64, max_prefill=4096, max_steps=16,
+                          max_budget=128, offload=0, stream=None)
+    with pytest.raises(_lib.LKVError) as e:
+        _lib.lkv_create(cfg)
+    assert e.value.status == _lib.LKV_ENOMEM and "injected" in str(e.value)
+
+
 def test_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises(RuntimeError, match="not found"):
         _lib._lib = None

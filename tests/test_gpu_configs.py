@@ -3,9 +3,10 @@
 Each test runs one configuration at its full size on the GPU and checks it
 against the oracle on the same seeded inputs, where the oracle can follow in
 seconds: whole runs for the long-output configuration, every step for the
-long-input one, sampled layers for the 36-layer host-offload configuration and
-sampled sequences and sweep points for the batch-32 sweep. Decisions (flags,
-r_t, selections, evicted segments, cluster assignments) must be bit-exact and
+long-input one and sampled layers for the 36-layer host-offload
+configuration (the batch-32 sweep and the benchmarked workload are in
+test_gpu_fullsize.py). Decisions (flags, r_t, selections, evicted segments,
+cluster assignments) must be bit-exact and
 attention outputs within 2e-3 abs + 1e-2 rel; the indexes are teacher-forced
 into the oracle from the GPU once K-means itself has been checked."""
 import numpy as np
@@ -153,41 +154,4 @@ def test_host_offload_36_layers():
         o = _oracle_run(w, K[0], V[0], idx, q, kn, vn, 0, layer, tau=w.tau, budget=w.budget,
                         attn_mask=mask)
         H.compare_decode(g, o, w, 0, layer, attn_mask=mask)
-    ctx.close()
-
-
-@pytest.fixture(scope="module")
-def sweep_inputs():
-    w = synth.WORKLOADS["sweep"]
-    K, V = synth.prefill(w, 0, "cuda")
-    q, kn, vn, _ = synth.decode_inputs(w, "cuda")
-    return K, V, q, kn, vn
-
-
-@pytest.mark.parametrize("tau,budget", [(0.5, 512), (0.7, 1024), (0.9, 2048)])
-def test_sweep_batch32(sweep_inputs, tau, budget):
-    """B = 32, N = 32768, C = 2048: the whole 8192-step run through the
-    pipelined graph at this (tau, budget) point, sequences 0 and 31 compared
-    with the oracle over the first 256 steps (selections included) and their
-    flags over the whole run; the trigger rate is reported."""
-    K, V, q, kn, vn = sweep_inputs
-    w = synth.WORKLOADS["sweep"].replace(tau=tau, budget=budget)
-    T, T1 = w.n_steps, 256
-    ctx = H.make_ctx(w, max_budget=2048)
-    ctx.build_index(0, K, V, w.n_clusters, w.iters, 5)
-    idx = {b: _index(ctx, w, 0, b) for b in (0, 31)}
-    g1 = H.run_decode(ctx, w, q[:T1], kn[:T1], vn[:T1])
-    out = torch.empty(T - T1, w.batch, 1, w.n_heads, 128, device="cuda")
-    bnd = torch.zeros(T - T1, w.batch, 1, dtype=torch.uint8, device="cuda")
-    ctx.decode_steps(0, q[T1:], kn[T1:], vn[T1:], w.tau, w.budget, out, boundary=bnd)
-    ctx.sync()
-    flags = np.concatenate([g1["boundary"], bnd.cpu().numpy()])
-    for b in (0, 31):
-        o = _oracle_run(w, K[b], V[b], idx[b], q[:T1], kn[:T1], vn[:T1], b, 0, tau=w.tau,
-                        budget=w.budget)
-        H.compare_decode(g1, o, w, b, 0)
-        ofull = _oracle_run(w, K[b], V[b], idx[b], q, kn, vn, b, 0, tau=w.tau, budget=w.budget,
-                            attn_mask=np.zeros(T, np.uint8), want_sel=False)
-        assert np.array_equal(flags[:, b, 0], ofull["flag"])
-    print(f"sweep tau={tau} budget={budget}: trigger rate {flags.mean():.4f}")
     ctx.close()
