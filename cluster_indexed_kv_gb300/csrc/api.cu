@@ -210,6 +210,7 @@ lkv_status lkv_create(const lkv_config *cfg, lkv_ctx **out) {
   v.q_prev = dalloc(c, LB * H * d * es, &st);
   v.q_attn = (float *)dalloc(c, lkv::kRing * LB * H * d * 4, &st);  // per step slot
   v.aview = (int4 *)dalloc(c, lkv::kRing * LB * sizeof(int4), &st);
+  v.adesc = (int4 *)dalloc(c, lkv::kRing * S_all * sizeof(int4), &st);
   v.segsum = (int64_t *)dalloc(c, S_all * d * 8, &st);
   v.scores = (float *)dalloc(c, S_all * u_cap * 4, &st);
   // the selection plan, one copy per plan slot
@@ -224,6 +225,17 @@ lkv_status lkv_create(const lkv_config *cfg, lkv_ctx **out) {
   v.attn_count = (int32_t *)dalloc(c, lkv::kRing * S_all * 4, &st);
   v.attn_part = (float *)dalloc(c, lkv::kRing * S_all * lkv::kAttnMaxSplit *
                                        (int64_t)(k.group * d + 2 * k.group) * 4, &st);
+  if (st == LKV_OK) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      sms = 160;
+    }
+    v.w_cap = lkv::stream_warp_cap(sms);
+  }
+  v.attn_wpart = (float *)dalloc(c, lkv::kRing * (int64_t)v.w_cap *
+                                        (int64_t)(k.group * d + 2 * k.group) * 4, &st);
   v.max_pieces = u_cap + max_chunks;
   v.pieces = (int4 *)dalloc(c, S_all * (int64_t)v.max_pieces * sizeof(int4), &st);
   v.chunk_piece = (int32_t *)dalloc(c, S_all * (int64_t)(max_chunks + 1) * 4, &st);

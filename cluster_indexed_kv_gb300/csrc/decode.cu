@@ -142,9 +142,16 @@ __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// 512 threads (62 registers each) fit beside an attention CTA on one SM.
+// 512 threads (64 registers each), the queries staged in their own dtype.
 constexpr int kBoundaryThreads = 512;
-constexpr int kQPitch = kHeadDim + 8;  // padded query rows in shared memory (floats)
+constexpr int kQPitch = kHeadDim + 8;  // padded query rows in shared memory (elements)
+
+// One staged query element as a float.
+template <int DT>
+__device__ __forceinline__ float qs_get(const void *qs, int i) {
+  if constexpr (DT == 1) return __uint_as_float(((uint32_t)((const uint16_t *)qs)[i]) << 16);
+  else return ((const float *)qs)[i];
+}
 
 template <int DT>
 __global__ void __launch_bounds__(kBoundaryThreads, 2) k_step_boundary(CtxView v, StepArgs a) {
@@ -156,7 +163,10 @@ __global__ void __launch_bounds__(kBoundaryThreads, 2) k_step_boundary(CtxView v
   __shared__ DecState st;
   __shared__ float cosv[kMaxHeads];
   __shared__ int slow_any;
-  extern __shared__ float qsm[];  // [2][H][kQPitch]: previous and current queries
+  // [2][H][kQPitch] elements of the dtype: previous and current queries
+  extern __shared__ __align__(16) unsigned char qsm_raw[];
+  using QT = typename std::conditional<DT == 1, uint16_t, float>::type;
+  QT *qsm = reinterpret_cast<QT *>(qsm_raw);
   pdl_wait();
   pdl_trigger();
   if (tid == 0) {
@@ -170,14 +180,13 @@ __global__ void __launch_bounds__(kBoundaryThreads, 2) k_step_boundary(CtxView v
   const int nvec = H * kHeadDim / per16;
   for (int y = tid; y < nvec; y += nth) {
     const int head = y / (kHeadDim / per16), j0 = (y % (kHeadDim / per16)) * per16;
-    float e[8];
-    load16<DT>(v.q_prev, (lb * H + head) * kHeadDim + j0, e);
-    float *dst = qsm + (int64_t)head * kQPitch + j0;
-#pragma unroll
-    for (int i = 0; i < per16; ++i) dst[i] = e[i];
+    *(uint4 *)(qsm + (int64_t)head * kQPitch + j0) =
+        __ldg((const uint4 *)((const QT *)v.q_prev + (lb * H + head) * kHeadDim + j0));
   }
   constexpr int kMaxPer = 16 * kHeadDim / kBoundaryThreads;  // Hkv * d <= 2048
-  uint32_t kbits[kMaxPer], vbits[kMaxPer];
+  // the new key and value elements: one register a pair for bf16 (key in
+  // the high half), two for fp32
+  uint32_t kbits[kMaxPer], vbits[DT == 1 ? 1 : kMaxPer];
   int64_t ssum[kMaxPer];
 #pragma unroll
   for (int r = 0; r < kMaxPer; ++r) {
@@ -199,40 +208,33 @@ __global__ void __launch_bounds__(kBoundaryThreads, 2) k_step_boundary(CtxView v
     const int x = tid + r * nth;
     if (x < v.Hkv * kHeadDim) {
       if constexpr (DT == 1) {
-        kbits[r] = ((const uint16_t *)k_new)[kvoff + x];
-        vbits[r] = ((const uint16_t *)v_new)[kvoff + x];
+        kbits[r] = ((uint32_t)((const uint16_t *)k_new)[kvoff + x] << 16) |
+                   (uint32_t)((const uint16_t *)v_new)[kvoff + x];
       } else {
         kbits[r] = __float_as_uint(((const float *)k_new)[kvoff + x]);
-        vbits[r] = __float_as_uint(((const float *)v_new)[kvoff + x]);
+        vbits[DT == 1 ? 0 : r] = __float_as_uint(((const float *)v_new)[kvoff + x]);
       }
     }
   }
   for (int y = tid; y < nvec; y += nth) {
     const int head = y / (kHeadDim / per16), j0 = (y % (kHeadDim / per16)) * per16;
-    float e[8];
-    load16<DT>(q, qoff + (int64_t)head * kHeadDim + j0, e);
-    float *dst = qsm + ((int64_t)H + head) * kQPitch + j0;
-#pragma unroll
-    for (int i = 0; i < per16; ++i) dst[i] = e[i];
+    *(uint4 *)(qsm + ((int64_t)H + head) * kQPitch + j0) =
+        __ldg((const uint4 *)((const QT *)q + qoff + (int64_t)head * kHeadDim + j0));
   }
   __syncthreads();
 
   // 1. r_t = (1/H) sum_h cos(q_{t-1}^h, q_t^h) in fp32, fixed operation order
   if (t > 0) {
     if (tid < H) {
-      const float *x = qsm + tid * kQPitch;
-      const float *y = qsm + (H + tid) * kQPitch;
+      const QT *x = qsm + tid * kQPitch;
+      const QT *y = qsm + (H + tid) * kQPitch;
       float dot = 0.f, na = 0.f, nb = 0.f;
 #pragma unroll 8
-      for (int j = 0; j < kHeadDim; j += 4) {
-        const float4 xa = *(const float4 *)(x + j), ya = *(const float4 *)(y + j);
-        const float xv[4] = {xa.x, xa.y, xa.z, xa.w}, yv[4] = {ya.x, ya.y, ya.z, ya.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          dot = __fmaf_rn(xv[e], yv[e], dot);
-          na = __fmaf_rn(xv[e], xv[e], na);
-          nb = __fmaf_rn(yv[e], yv[e], nb);
-        }
+      for (int j = 0; j < kHeadDim; ++j) {
+        const float xv = qs_get<DT>(x, j), yv = qs_get<DT>(y, j);
+        dot = __fmaf_rn(xv, yv, dot);
+        na = __fmaf_rn(xv, xv, na);
+        nb = __fmaf_rn(yv, yv, nb);
       }
       const float den = __fmul_rn(__fsqrt_rn(na), __fsqrt_rn(nb));
       cosv[tid] = den > 0.f ? __fdiv_rn(dot, den) : 0.f;
@@ -321,12 +323,12 @@ __global__ void __launch_bounds__(kBoundaryThreads, 2) k_step_boundary(CtxView v
     const int64_t di = (gs * v.dec_rows + t) * kHeadDim + dim;
     const int64_t prev = restarted ? 0 : ssum[r];
     if constexpr (DT == 1) {
-      ((uint16_t *)v.dec_k)[di] = (uint16_t)kbits[r];
-      ((uint16_t *)v.dec_v)[di] = (uint16_t)vbits[r];
-      v.segsum[gs * kHeadDim + dim] = prev + bf16_fixed40((uint16_t)kbits[r], &slow);
+      ((uint16_t *)v.dec_k)[di] = (uint16_t)(kbits[r] >> 16);
+      ((uint16_t *)v.dec_v)[di] = (uint16_t)(kbits[r] & 0xffffu);
+      v.segsum[gs * kHeadDim + dim] = prev + bf16_fixed40((uint16_t)(kbits[r] >> 16), &slow);
     } else {
       ((float *)v.dec_k)[di] = __uint_as_float(kbits[r]);
-      ((float *)v.dec_v)[di] = __uint_as_float(vbits[r]);
+      ((float *)v.dec_v)[di] = __uint_as_float(vbits[DT == 1 ? 0 : r]);
       v.segsum[gs * kHeadDim + dim] =
           __double_as_longlong(__dadd_rn(__longlong_as_double(prev), (double)__uint_as_float(kbits[r])));
     }
@@ -337,24 +339,13 @@ __global__ void __launch_bounds__(kBoundaryThreads, 2) k_step_boundary(CtxView v
   const float qscale = 1.4426950408889634f * rsqrtf((float)kHeadDim);
   for (int y = tid; y < nvec; y += nth) {
     const int head = y / (kHeadDim / per16), j0 = (y % (kHeadDim / per16)) * per16;
-    const float *src = qsm + ((int64_t)H + head) * kQPitch + j0;
+    const QT *src = qsm + ((int64_t)H + head) * kQPitch + j0;
     float4 *qa = (float4 *)(v.q_attn + (((int64_t)a.slot * v.n_lb + lb) * H + head) * kHeadDim + j0);
 #pragma unroll
     for (int i = 0; i < per16 / 4; ++i)
-      qa[i] = make_float4(src[4 * i] * qscale, src[4 * i + 1] * qscale, src[4 * i + 2] * qscale,
-                          src[4 * i + 3] * qscale);
-    if constexpr (DT == 1) {
-      uint4 o;
-      uint32_t w[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        w[i] = (__float_as_uint(src[2 * i]) >> 16) | (__float_as_uint(src[2 * i + 1]) & 0xffff0000u);
-      o.x = w[0]; o.y = w[1]; o.z = w[2]; o.w = w[3];
-      *(uint4 *)((uint16_t *)v.q_prev + (lb * H + head) * kHeadDim + j0) = o;
-    } else {
-      *(float4 *)((float *)v.q_prev + (lb * H + head) * kHeadDim + j0) =
-          make_float4(src[0], src[1], src[2], src[3]);
-    }
+      qa[i] = make_float4(qs_get<DT>(src, 4 * i) * qscale, qs_get<DT>(src, 4 * i + 1) * qscale,
+                          qs_get<DT>(src, 4 * i + 2) * qscale, qs_get<DT>(src, 4 * i + 3) * qscale);
+    *(uint4 *)((QT *)v.q_prev + (lb * H + head) * kHeadDim + j0) = *(const uint4 *)src;
   }
   __syncthreads();
   if (tid == 0) {
@@ -554,23 +545,47 @@ __device__ void select_units(const CtxView &v, int64_t gs, int U, int budget, in
   const int2 ex = block_scan_excl2(cnt, toks, wt, &s_nsel, &s_ntok);
   const int32_t cnt_ex = ex.x, tok_ex = ex.y;
   int32_t npc = 0;  // copy pieces of this thread's selected units (when a reader needs them)
+  // the selected units' first rows and token offsets, also kept in shared
+  // memory (the radix histograms are free now) so that the pool row of every
+  // selected token can be written by one thread per token
+  constexpr int kSelStage = kScoreWarps * 256 / 2;
+  int32_t *cum_sh = &whist[0][0], *row_sh = cum_sh + kSelStage;
+  int32_t *tok_rows = v.offload ? nullptr : plan_sel_rows(v, ps, gs);
+  const bool staged = s_nsel <= kSelStage;
   {
     int32_t run = tie_ex, kk = cnt_ex, cum = tok_ex;
     int32_t *sel_out = plan_sel(v, ps, gs);
     int32_t *row_out = plan_rng_row(v, ps, gs);
     int32_t *cum_out = plan_rng_cum(v, ps, gs);
-    int32_t *tok_rows = v.offload ? nullptr : plan_sel_rows(v, ps, gs);
     for (int u = u0; u < u1; ++u) {
       if (!is_sel(u, run)) continue;
       const int32_t len = lenof(u), row = rowof(u);
       sel_out[kk] = u;
       row_out[kk] = row;
       cum_out[kk] = cum;
-      if (tok_rows)  // the pool row of every selected token, in token order
+      if (staged) {
+        cum_sh[kk] = cum;
+        row_sh[kk] = row;
+      } else if (tok_rows) {
         for (int32_t j = 0; j < len && cum + j < v.sel_cap; ++j) tok_rows[cum + j] = row + j;
+      }
       if (v.need_pieces && len > 0) npc += (cum + len - 1) / kAttnChunk - cum / kAttnChunk + 1;
       cum += len;
       ++kk;
+    }
+  }
+  if (staged && tok_rows) {
+    __syncthreads();
+    // token x belongs to the last selected unit whose offset is <= x
+    const int nsel = s_nsel, ntk = min(s_ntok, v.sel_cap);
+    for (int x = tid; x < ntk; x += nth) {
+      int lo = 0, hi = nsel - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (cum_sh[mid] <= x) lo = mid;
+        else hi = mid - 1;
+      }
+      tok_rows[x] = row_sh[lo] + (x - cum_sh[lo]);
     }
   }
   if (tid == 0) s_npieces = 0;
@@ -696,16 +711,19 @@ __global__ void __launch_bounds__(kScoreThreads) k_select(CtxView v, StepArgs a)
   const int b = rem / v.Hkv, h = rem % v.Hkv;
   const int64_t lb = (int64_t)(a.l0 + li) * v.B + b;
   const int64_t gs = lb * v.Hkv + h;
-  // the step view was written before the scoring grid started (stream
-  // order), so a slice without retrieval leaves before the wait
+  // the step view was written before the scoring grid started (stream order)
   const int4 view = v.aview[(int64_t)a.slot * v.n_lb + lb];
+  pdl_wait();  // the scores (and every earlier selection's plan) are complete and visible
+  pdl_trigger();
+  int4 *desc = v.adesc + (int64_t)a.slot * v.S_all + gs;
   if (!(view.w & 1)) {
-    pdl_trigger();
+    // no retrieval: the plan in force stays; the attention's descriptor
+    // carries its token count
+    if (threadIdx.x == 0) *desc = make_int4(view.x, view.y, view.z, *plan_ntok(v, view.z, gs));
     return;
   }
-  pdl_wait();  // the scores are complete and visible
-  pdl_trigger();
   select_units(v, gs, view.w >> 1, a.budget, view.z);
+  if (threadIdx.x == 0) *desc = make_int4(view.x, view.y, view.z, *plan_ntok(v, view.z, gs));
 }
 
 // ---------------------------------------------------------------- offload gather
@@ -1597,6 +1615,534 @@ __global__ void __launch_bounds__(attn_threads<DT, G>(), attn_min_blocks<DT, G>(
 }
 
 
+// ---------------------------------------------------------------- streaming attention
+
+// Tensor-core attention (bf16 rows, 4 or 8 query heads per KV head) that
+// splits the step's rows over warps in proportion to each slice's actual
+// size. Every slice of the call has total_s = (local-buffer rows) +
+// (selected tokens) rows, known only on the device; warp w of the W warps
+// of the launch serves exactly one slice:
+//   w0(s) = floor((W - S) * pre(s) / R) + s,   pre(s) = sum of the totals of
+//   slices before s, R = all rows,
+// so slice s gets w0(s + 1) - w0(s) >= 1 warps and every warp about R / W
+// rows, whatever the mix of slice sizes. A slice's rows are ordered local
+// buffer first (their pool rows follow from the window start alone), then
+// the selected tokens (pool row from the plan's per-token row table, or the
+// offload staging row). A warp streams its rows in 16-row tiles through its
+// own ring of NS stages of 16-byte cp.async copies (no warp waits for
+// another), computes scores and p * V with mma.sync bf16 products (queries
+// and softmax weights split into a bf16 high part and a bf16 residual, so
+// both keep fp32 accuracy), writes its partial softmax state, and the last
+// warp of the slice to finish combines the slice's partials.
+constexpr int kStreamMaxSlices = 1024;  // slices of one call the streaming kernel takes
+constexpr int kStreamRowsPerWarp = 64;  // fewest rows a warp is given at the largest budget
+
+template <int NS>
+constexpr size_t stream_ring_bytes(int nw) { return (size_t)nw * NS * 2 * 16 * kHeadDim * 2; }
+// dynamic shared memory: the rings, then per slice the row prefix (S + 1
+// entries), the window start, the selected-token count, t and the plan slot
+template <int NS>
+constexpr size_t stream_smem(int nw, int S) { return stream_ring_bytes<NS>(nw) + (size_t)(5 * S + 1) * 4; }
+
+int stream_warp_cap(int sms) { return sms * 16 > kStreamMaxSlices ? sms * 16 : kStreamMaxSlices; }
+
+constexpr int kStreamIdxWin = 256;  // selected-token row entries a warp keeps in shared memory
+
+__device__ __forceinline__ int32_t atom_add_acq_rel_gpu(int32_t *p, int32_t x) {
+  int32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(x) : "memory");
+  return old;
+}
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+template <int G, int NW, int NS, int MINB>
+__global__ void __launch_bounds__(32 * NW, MINB) k_attn_stream(CtxView v, StepArgs a, int S, int W) {
+  constexpr int RB = kHeadDim * 2;  // bytes of a bf16 row
+  constexpr int WB = 16 * RB;       // a stage: 16 K rows, then 16 V rows
+  constexpr int NT = G / 4;         // products per 16-row block
+  constexpr int kPart = G * kHeadDim + 2 * G;
+  static_assert(kPart * 4 <= NS * 2 * WB, "a warp's state must fit in its ring");
+  extern __shared__ __align__(128) unsigned char smem[];
+  int32_t *pre = reinterpret_cast<int32_t *>(smem + stream_ring_bytes<NS>(NW));  // [S + 1]
+  int32_t *ws_s = pre + S + 1, *nt_s = ws_s + S, *t_s = nt_s + S, *pl_s = t_s + S;
+  __shared__ int32_t wt[64];
+  __shared__ int32_t s_total;
+  __shared__ int32_t sl_w[NW];                   // slice of each warp (-1: no work)
+  __shared__ int32_t idx_w[NW][kStreamIdxWin];   // each warp's window of the token-row table
+  __shared__ __align__(16) float S_w[NW][16][G];  // each warp's softmax weights of a tile
+  __shared__ __align__(8) uint64_t full_w[NW][NS];  // a stage's copies have landed
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int w = blockIdx.x * NW + wid;
+  const int per_l = v.B * v.Hkv;
+  const int64_t gs0 = (int64_t)a.l0 * per_l;
+  if (lane < NS) {
+    mbar_init(&full_w[wid][lane], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  pdl_wait();
+  pdl_trigger();
+
+  // 1. the call's slice descriptors, their row totals and the exclusive prefix
+  {
+    const int4 *desc = v.adesc + (int64_t)a.slot * v.S_all + gs0;
+    const int per = (S + 32 * NW - 1) / (32 * NW);
+    const int s0 = tid * per, s1 = min(S, s0 + per);
+    int32_t part = 0;
+    for (int s = s0; s < s1; ++s) {
+      const int4 d = desc[s];
+      ws_s[s] = d.y;
+      nt_s[s] = d.w;
+      t_s[s] = d.x;
+      pl_s[s] = d.z;
+      part += d.w + (d.x - d.y + 1);
+    }
+    int32_t run = block_scan_excl(part, wt, &s_total);
+    for (int s = s0; s < s1; ++s) {
+      pre[s] = run;
+      run += nt_s[s] + (t_s[s] - ws_s[s] + 1);
+    }
+    if (tid == 0) pre[S] = s_total;
+    __syncthreads();
+  }
+  const int64_t R = pre[S];
+  const bool active = w < W;
+  // 2. this warp's slice (largest s with w0(s) <= w) and its shares of the
+  //    slice's local-buffer rows and selected tokens
+  auto w0 = [&](int s) -> int { return (int)((int64_t)(W - S) * pre[s] / R) + s; };
+  int sl = 0;
+  {
+    int lo = 0, hi = S - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (w0(mid) <= w) lo = mid;
+      else hi = mid - 1;
+    }
+    sl = lo;
+  }
+  const int wf = w0(sl), nw_s = w0(sl + 1) - wf;
+  if (lane == 0) sl_w[wid] = active ? sl : -1;
+  const int li = sl / per_l, rem = sl % per_l;
+  const int b = rem / v.Hkv, h = rem % v.Hkv;
+  const int64_t lb = (int64_t)(a.l0 + li) * v.B + b;
+  const int64_t gs = gs0 + sl;
+  const int win = t_s[sl] - ws_s[sl] + 1, ntok = nt_s[sl], ws = ws_s[sl], ps = pl_s[sl];
+  const int kw = w - wf;
+  const int wa = active ? (int)((int64_t)win * kw / nw_s) : 0;
+  const int wb = active ? (int)((int64_t)win * (kw + 1) / nw_s) : 0;
+  const int ja = active ? (int)((int64_t)ntok * kw / nw_s) : 0;
+  const int jb = active ? (int)((int64_t)ntok * (kw + 1) / nw_s) : 0;
+  const int n_wt = (wb - wa + 15) / 16;            // local-buffer tiles, first
+  const int n_tiles = n_wt + (jb - ja + 15) / 16;  // then selected-token tiles
+  const int64_t so = ((int64_t)b * a.nl + li) * v.Hkv + h;
+  const int64_t k_out = t_s[sl] - a.base_t;
+  // the slice's first warp reports the selection in force (it does not
+  // depend on the attention)
+  if (active && kw == 0) {
+    const int ns = *plan_nsel(v, ps, gs);
+    if (a.selected_units) {
+      const int32_t *sel = plan_sel(v, ps, gs);
+      int32_t *dst = a.selected_units + k_out * a.stride_sel + so * v.u_cap;
+      for (int x = lane; x < ns; x += 32) dst[x] = sel[x];
+    }
+    if (lane == 0 && a.n_selected) a.n_selected[k_out * a.stride_nsel + so] = ns;
+  }
+
+  // row sources: local-buffer row f and selected token j
+  const unsigned char *win_k, *win_v, *sel_k, *sel_v;
+  const int32_t *tok_rows = nullptr;
+  if (!v.offload) {
+    win_k = (const unsigned char *)v.pool_k + (gs * v.pool_rows + v.n_cap + ws) * RB;
+    win_v = (const unsigned char *)v.pool_v + (gs * v.pool_rows + v.n_cap + ws) * RB;
+    sel_k = (const unsigned char *)v.pool_k + gs * v.pool_rows * RB;
+    sel_v = (const unsigned char *)v.pool_v + gs * v.pool_rows * RB;
+    tok_rows = plan_sel_rows(v, ps, gs);
+  } else {
+    win_k = (const unsigned char *)v.dec_k + (gs * v.dec_rows + ws) * RB;
+    win_v = (const unsigned char *)v.dec_v + (gs * v.dec_rows + ws) * RB;
+    sel_k = (const unsigned char *)v.stage_k + ((int64_t)ps * v.S_all + gs) * v.bud_cap * RB;
+    sel_v = (const unsigned char *)v.stage_v + ((int64_t)ps * v.S_all + gs) * v.bud_cap * RB;
+  }
+  // a window of the selected tokens' table entries (pool rows) in shared
+  // memory, filled with one round of loads
+  int32_t *idx = idx_w[wid];
+  int jwin = ja;
+  int32_t e_idx[kStreamIdxWin / 32];  // the first window, loaded now, stored when first needed
+  auto load_idx = [&](int j0) {
+    jwin = j0;
+#pragma unroll
+    for (int r = 0; r < kStreamIdxWin / 32; ++r) {
+      const int j = j0 + lane + 32 * r;
+      e_idx[r] = j < jb ? tok_rows[j] : 0;
+    }
+  };
+  auto store_idx = [&]() {
+#pragma unroll
+    for (int r = 0; r < kStreamIdxWin / 32; ++r) idx[lane + 32 * r] = e_idx[r];
+    __syncwarp();
+  };
+  auto fill_idx = [&](int j0) {
+    load_idx(j0);
+    store_idx();
+  };
+  bool idx_ready = tok_rows == nullptr || jb == ja;
+  if (!idx_ready) load_idx(ja);
+  unsigned char *ring = smem + (size_t)wid * NS * 2 * WB;
+  // Tile i goes to stage i % NS as bulk copies of its runs of consecutive
+  // pool rows (lane r < 16 looks at row r; a run starts where the rows stop
+  // being consecutive), completing on the stage's barrier. Rows past the
+  // tile's end are zeroed so that their zero softmax weights meet finite
+  // values.
+  int n_issued = 0;
+  auto issue = [&](int i) {
+    if (i >= n_tiles) return;
+    n_issued = i + 1;
+    const bool wt_ = i < n_wt;
+    const int base = wt_ ? wa + 16 * i : ja + 16 * (i - n_wt);
+    const int nrow = wt_ ? min(16, wb - base) : min(16, jb - base);
+    if (!wt_ && !idx_ready) {
+      store_idx();
+      idx_ready = true;
+    }
+    if (!wt_ && tok_rows && base + nrow > jwin + kStreamIdxWin) fill_idx(base);
+    unsigned char *Kd = ring + (i % NS) * 2 * WB;
+    uint64_t *bar = &full_w[wid][i % NS];
+    int32_t row = 0;
+    if (lane < nrow) row = (wt_ || !tok_rows) ? base + lane : idx[base + lane - jwin];
+    const int32_t prev = __shfl_up_sync(kFull, row, 1);
+    const unsigned starts = __ballot_sync(kFull, lane < nrow && (lane == 0 || row != prev + 1));
+    if (nrow < 16) {  // zero the rows past the tile's end (generic proxy)
+      for (int x = lane; x < (16 - nrow) * RB / 16; x += 32) {
+        reinterpret_cast<uint4 *>(Kd + nrow * RB)[x] = make_uint4(0, 0, 0, 0);
+        reinterpret_cast<uint4 *>(Kd + WB + nrow * RB)[x] = make_uint4(0, 0, 0, 0);
+      }
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+    if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)nrow * 2 * RB);
+    __syncwarp();
+    if ((starts >> lane) & 1) {
+      const unsigned after = starts & ~((2u << lane) - 1);  // later run starts
+      const int end = after ? __ffs(after) - 1 : nrow;
+      const uint32_t bytes = (uint32_t)(end - lane) * RB;
+      const unsigned char *ks = (wt_ ? win_k : sel_k) + (int64_t)row * RB;
+      const unsigned char *vs = (wt_ ? win_v : sel_v) + (int64_t)row * RB;
+      bulk_g2s(Kd + lane * RB, ks, bytes, bar);
+      bulk_g2s(Kd + WB + lane * RB, vs, bytes, bar);
+    }
+  };
+  // the first stages: the local-buffer tiles (no table entries needed); the
+  // selected-token tiles follow in the loop, by when their entries are in
+  for (int i = 0; i < NS && i < (idx_ready ? n_tiles : n_wt); ++i) issue(i);
+
+  // the queries (pre-scaled by log2(e)/sqrt(d)): column n of product nt_
+  // carries head (G == 8 ? n : n % 4), its bf16 high part for nt_ == 0
+  // (G == 8) or n < 4 (G == 4), else the bf16 residual; lane (g, t) ends
+  // with D columns 2t, 2t + 1, i.e. heads hb and hb + 1
+  const int gq = lane >> 2, tq = lane & 3;
+  const int hb = G == 8 ? 2 * tq : 2 * (tq & 1);
+  auto col_head = [](int n) { return G == 8 ? n : (n & 3); };
+  auto col_lo = [](int nt, int n) { return G == 8 ? nt == 1 : n >= 4; };
+  const int H = v.Hkv * G;
+  uint32_t qb[4][NT][4];
+  if (active) {
+    const float *qh = v.q_attn + (((int64_t)a.slot * v.n_lb + lb) * H + (int64_t)h * G + col_head(gq)) * kHeadDim +
+                      8 * tq;
+    float qf[4][8];
+#pragma unroll
+    for (int P = 0; P < 4; ++P) {
+      const float4 u0 = __ldg((const float4 *)(qh + 32 * P));
+      const float4 u1 = __ldg((const float4 *)(qh + 32 * P + 4));
+      qf[P][0] = u0.x; qf[P][1] = u0.y; qf[P][2] = u0.z; qf[P][3] = u0.w;
+      qf[P][4] = u1.x; qf[P][5] = u1.y; qf[P][6] = u1.z; qf[P][7] = u1.w;
+    }
+#pragma unroll
+    for (int P = 0; P < 4; ++P)
+#pragma unroll
+      for (int nt_ = 0; nt_ < NT; ++nt_)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) qb[P][nt_][q] = bf16_pair(qf[P][2 * q], qf[P][2 * q + 1], col_lo(nt_, gq));
+  }
+  float mr[2] = {-INFINITY, -INFINITY}, lr[2] = {0.f, 0.f};  // heads hb, hb + 1
+  float o[NT][8][4];
+#pragma unroll
+  for (int nt_ = 0; nt_ < NT; ++nt_)
+#pragma unroll
+    for (int m = 0; m < 8; ++m)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[nt_][m][e] = 0.f;
+  bool ok = true;
+
+  for (int i = 0; i < n_tiles; ++i) {
+    const unsigned char *Kw = ring + (i % NS) * 2 * WB;
+    const unsigned char *Vw = Kw + WB;
+    while (n_issued <= i) issue(n_issued);  // (a warp whose first tile is a selected one)
+    if (!mbar_wait_bounded(&full_w[wid][i % NS], (i / NS) & 1, kWaitLimitNs)) {
+      ok = false;  // record it; the drain below waits once more for the copies
+      break;
+    }
+    const bool wt_ = i < n_wt;
+    const int nrow = wt_ ? min(16, wb - (wa + 16 * i)) : min(16, jb - (ja + 16 * (i - n_wt)));
+    // scores of rows g and g + 8, two accumulation chains
+    float sc[NT][2][4];
+#pragma unroll
+    for (int nt_ = 0; nt_ < NT; ++nt_)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sc[nt_][0][e] = sc[nt_][1][e] = 0.f;
+    const unsigned char *kr = Kw + gq * RB + 16 * tq;
+#pragma unroll
+    for (int P = 0; P < 4; ++P) {
+      const uint4 x = *(const uint4 *)(kr + 64 * P);
+      const uint4 y = *(const uint4 *)(kr + 8 * RB + 64 * P);
+#pragma unroll
+      for (int nt_ = 0; nt_ < NT; ++nt_) {
+        mma_bf16(sc[nt_][0], x.x, y.x, x.y, y.y, qb[P][nt_][0], qb[P][nt_][1]);
+        mma_bf16(sc[nt_][1], x.z, y.z, x.w, y.w, qb[P][nt_][2], qb[P][nt_][3]);
+      }
+    }
+    // s[0], s[1]: row g, heads hb, hb + 1; s[2], s[3]: row g + 8
+    float s[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      s[e] = sc[0][0][e] + sc[0][1][e];
+      if constexpr (NT == 2) s[e] += sc[1][0][e] + sc[1][1][e];
+      else s[e] += __shfl_xor_sync(kFull, s[e], 2);  // high part + residual
+    }
+    if (nrow < 16) {  // rows past the tile's end score -inf
+      if (gq >= nrow) s[0] = s[1] = -INFINITY;
+      if (gq + 8 >= nrow) s[2] = s[3] = -INFINITY;
+    }
+    // online softmax; rescale only when a maximum moves
+    float c[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      float mx = fmaxf(s[e], s[e + 2]);
+#pragma unroll
+      for (int msk = 4; msk < 32; msk <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, msk));
+      const float mn = fmaxf(mr[e], mx);
+      c[e] = (mr[e] == -INFINITY) ? 0.f : exp2f(mr[e] - mn);
+      mr[e] = mn;
+    }
+    float p[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) p[e] = (s[e] == -INFINITY) ? 0.f : exp2f(s[e] - mr[e & 1]);
+#pragma unroll
+    for (int e = 0; e < 2; ++e) lr[e] = lr[e] * c[e] + p[e] + p[e + 2];
+    if (__any_sync(kFull, c[0] != 1.f || c[1] != 1.f)) {
+#pragma unroll
+      for (int nt_ = 0; nt_ < NT; ++nt_)
+#pragma unroll
+        for (int m = 0; m < 8; ++m)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) o[nt_][m][e] *= c[e & 1];
+    }
+    // p^T as the B operand of p * V (rows = tokens), through shared memory
+    float(*Sw)[G] = S_w[wid];
+    if (G == 8 || tq < 2) {
+      *(float2 *)&Sw[gq][hb] = make_float2(p[0], p[1]);
+      *(float2 *)&Sw[gq + 8][hb] = make_float2(p[2], p[3]);
+    }
+    __syncwarp();
+    uint32_t pb[NT][2];
+#pragma unroll
+    for (int nt_ = 0; nt_ < NT; ++nt_) {
+      const int hh = col_head(gq);
+      const bool lo_ = col_lo(nt_, gq);
+      pb[nt_][0] = bf16_pair(Sw[2 * tq][hh], Sw[2 * tq + 1][hh], lo_);
+      pb[nt_][1] = bf16_pair(Sw[2 * tq + 8][hh], Sw[2 * tq + 9][hh], lo_);
+    }
+    // p * V: product m = 4 hf + j has output rows dim 64 hf + 8 g + 2 j (row
+    // g) and that dim + 1 (row g + 8); lane (g, t) reads tokens 2t, 2t + 1,
+    // 2t + 8, 2t + 9 at dims [64 hf + 8 g, + 8) and pairs them up by token
+    const unsigned char *vr = Vw + (2 * tq) * RB + 16 * gq;
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      const uint4 v0 = *(const uint4 *)(vr + 128 * hf);
+      const uint4 v1 = *(const uint4 *)(vr + RB + 128 * hf);
+      const uint4 v2 = *(const uint4 *)(vr + 8 * RB + 128 * hf);
+      const uint4 v3 = *(const uint4 *)(vr + 9 * RB + 128 * hf);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t w0_ = word(v0, j), w1_ = word(v1, j), w2_ = word(v2, j), w3_ = word(v3, j);
+        const uint32_t a0 = prmt(w0_, w1_, 0x5410u), a1 = prmt(w0_, w1_, 0x7632u);
+        const uint32_t a2 = prmt(w2_, w3_, 0x5410u), a3 = prmt(w2_, w3_, 0x7632u);
+#pragma unroll
+        for (int nt_ = 0; nt_ < NT; ++nt_) mma_bf16(o[nt_][4 * hf + j], a0, a1, a2, a3, pb[nt_][0], pb[nt_][1]);
+      }
+    }
+    // every lane's reads of this stage (and of the weights) are done: keep
+    // NS tiles in flight
+    __syncwarp();
+    while (n_issued < n_tiles && n_issued < i + 1 + NS) issue(n_issued);
+  }
+  if (!ok) {
+    // a copy never completed: record it, and let every copy this warp issued
+    // land (one more bounded wait per stage) before the block's memory goes
+    if (lane == 0) set_err(v.err, kErrTimeout);
+    for (int i2 = max(0, n_issued - NS); i2 < n_issued; ++i2)
+      mbar_wait_bounded(&full_w[wid][i2 % NS], (i2 / NS) & 1, kWaitLimitNs);
+  }
+  __syncwarp();
+
+  // 3. this warp's state (high part + residual, per-head maxima and sums)
+  //    into its ring, which is free now
+#pragma unroll
+  for (int m = 0; m < 8; ++m)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      if constexpr (NT == 2) o[0][m][e] += o[NT - 1][m][e];
+      else o[0][m][e] += __shfl_xor_sync(kFull, o[0][m][e], 2);
+    }
+#pragma unroll
+  for (int e = 0; e < 2; ++e)
+#pragma unroll
+    for (int msk = 4; msk < 32; msk <<= 1) lr[e] += __shfl_xor_sync(kFull, lr[e], msk);
+  float *mine = reinterpret_cast<float *>(ring);
+  if (G == 8 || tq < 2) {
+    if (gq == 0) {
+      mine[G * kHeadDim + hb] = mr[0];
+      mine[G * kHeadDim + hb + 1] = mr[1];
+      mine[G * kHeadDim + G + hb] = lr[0];
+      mine[G * kHeadDim + G + hb + 1] = lr[1];
+    }
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        float *dst = mine + (hb + e) * kHeadDim + 64 * hf + 8 * gq;
+        *(float4 *)dst = make_float4(o[0][4 * hf][e], o[0][4 * hf][e + 2], o[0][4 * hf + 1][e],
+                                     o[0][4 * hf + 1][e + 2]);
+        *(float4 *)(dst + 4) = make_float4(o[0][4 * hf + 2][e], o[0][4 * hf + 2][e + 2],
+                                           o[0][4 * hf + 3][e], o[0][4 * hf + 3][e + 2]);
+      }
+  }
+  __syncthreads();
+
+  // 4. the first warp of each slice in this CTA merges the CTA's warps of
+  //    that slice into one partial (stored at the index of that first warp);
+  //    the last partial of the slice to arrive combines them all
+  if (!active || (wid > 0 && sl_w[wid - 1] == sl)) return;
+  int n_mine = 1;
+  while (wid + n_mine < NW && sl_w[wid + n_mine] == sl) ++n_mine;
+  constexpr int kVec = G * kHeadDim / 4 / 32;  // float4s per lane (= G; float4 lane + 32 j lies in head j)
+  static_assert(kVec == G, "");
+  float4 acc[kVec];
+  float M[G], Z[G];
+  {
+    const float *st0 = reinterpret_cast<const float *>(smem + (size_t)wid * NS * 2 * WB);
+    constexpr size_t kStride = (size_t)NS * 2 * WB / 4;  // floats between consecutive warps' states
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      M[g] = -INFINITY;
+      for (int u = 0; u < n_mine; ++u) M[g] = fmaxf(M[g], st0[u * kStride + G * kHeadDim + g]);
+      Z[g] = 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < kVec; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int u = 0; u < n_mine; ++u) {
+      const float *st = st0 + u * kStride;
+#pragma unroll
+      for (int j = 0; j < kVec; ++j) {
+        const float m = st[G * kHeadDim + j];
+        const float f = (m == -INFINITY) ? 0.f : exp2f(m - M[j]);
+        const float4 x = *reinterpret_cast<const float4 *>(st + 4 * (lane + 32 * j));
+        acc[j].x = fmaf(f, x.x, acc[j].x);
+        acc[j].y = fmaf(f, x.y, acc[j].y);
+        acc[j].z = fmaf(f, x.z, acc[j].z);
+        acc[j].w = fmaf(f, x.w, acc[j].w);
+        Z[j] = fmaf(f, st[G * kHeadDim + G + j], Z[j]);
+      }
+    }
+  }
+  // partial ids of the slice: its first warp, then the first warp of every
+  // later CTA that serves it
+  const int n_parts = 1 + (w0(sl + 1) - 1) / NW - wf / NW;
+  float *pbase = v.attn_wpart + (int64_t)a.slot * v.w_cap * kPart;
+  int32_t *cnt = v.attn_count + (int64_t)a.slot * v.S_all + gs;
+  if (n_parts > 1) {
+    float *dst = pbase + (int64_t)w * kPart;
+#pragma unroll
+    for (int j = 0; j < kVec; ++j) *reinterpret_cast<float4 *>(dst + 4 * (lane + 32 * j)) = acc[j];
+    if (lane == 0)
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        dst[G * kHeadDim + g] = M[g];
+        dst[G * kHeadDim + G + g] = Z[g];
+      }
+    // publish (every lane's release fence) and count; the last partial's
+    // warp acquires the others' before reading them
+    fence_acq_rel_gpu();
+    __syncwarp();
+    int last = 0;
+    if (lane == 0) last = atom_add_acq_rel_gpu(cnt, 1) == n_parts - 1;
+    last = __shfl_sync(kFull, last, 0);
+    if (!last) return;
+    fence_acq_rel_gpu();
+    // every partial's maxima, sums and accumulators, loaded together in
+    // groups of four
+    float Mx[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) Mx[g] = -INFINITY;
+    for (int c0 = 0; c0 < n_parts; c0 += 32) {
+      const int cc = c0 + lane;
+      const int pid = cc == 0 ? wf : (wf / NW + cc) * NW;
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+        Mx[g] = fmaxf(Mx[g], cc < n_parts ? __ldcg(pbase + (int64_t)pid * kPart + G * kHeadDim + g) : -INFINITY);
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+#pragma unroll
+      for (int msk = 16; msk; msk >>= 1) Mx[g] = fmaxf(Mx[g], __shfl_xor_sync(kFull, Mx[g], msk));
+      M[g] = Mx[g];
+      Z[g] = 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < kVec; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c0 = 0; c0 < n_parts; c0 += 4) {
+      float4 x[4][kVec];
+      float mm[4][G], ll[4][G];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int cc = c0 + u;
+        const int pid = cc == 0 ? wf : (wf / NW + cc) * NW;
+        const float *src = pbase + (int64_t)(cc < n_parts ? pid : wf) * kPart;
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          mm[u][g] = __ldcg(src + G * kHeadDim + g);
+          ll[u][g] = __ldcg(src + G * kHeadDim + G + g);
+        }
+#pragma unroll
+        for (int j = 0; j < kVec; ++j) x[u][j] = __ldcg(reinterpret_cast<const float4 *>(src) + lane + 32 * j);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (c0 + u >= n_parts) break;
+#pragma unroll
+        for (int j = 0; j < kVec; ++j) {
+          const float f = (mm[u][j] == -INFINITY) ? 0.f : exp2f(mm[u][j] - M[j]);
+          Z[j] = fmaf(f, ll[u][j], Z[j]);
+          acc[j].x = fmaf(f, x[u][j].x, acc[j].x);
+          acc[j].y = fmaf(f, x[u][j].y, acc[j].y);
+          acc[j].z = fmaf(f, x[u][j].z, acc[j].z);
+          acc[j].w = fmaf(f, x[u][j].w, acc[j].w);
+        }
+      }
+    }
+  }
+  float *out = a.out + k_out * a.stride_out + (((int64_t)b * a.nl + li) * H + (int64_t)h * G) * kHeadDim;
+#pragma unroll
+  for (int j = 0; j < kVec; ++j) {
+    const float z = Z[j];
+    reinterpret_cast<float4 *>(out)[lane + 32 * j] =
+        make_float4(acc[j].x / z, acc[j].y / z, acc[j].z / z, acc[j].w / z);
+  }
+  if (lane == 0) {
+    if (n_parts > 1) *cnt = 0;
+    atomicAdd((unsigned long long *)&v.counters[kCntAttnRows], (unsigned long long)(win + ntok));
+    atomicAdd((unsigned long long *)&v.counters[kCntAttnSlices], 1ull);
+  }
+}
+
 // ---------------------------------------------------------------- host-link ceiling
 
 // Plain streaming read of pinned, mapped host memory into device memory:
@@ -1713,6 +2259,99 @@ static void launch_attn(const CtxView &v, const StepArgs &a, int slices, int nch
   cudaLaunchKernelEx(&cfg, k_attn<DT, G>, v, a, cpc);
 }
 
+// Streaming attention launch configurations: (warps per CTA, ring stages
+// per warp). A single-step launch has the GPU to itself and takes one CTA of
+// 8 warps with 3-stage rings per SM; inside a pipelined decode graph three
+// attention launches share the GPU with the boundary and selection kernels,
+// so CTAs are smaller.
+struct StreamCfg {
+  int nw, ns, minb;  // warps per CTA, ring stages per warp, CTAs per SM the registers must allow
+};
+constexpr StreamCfg kStreamCfgs[] = {{8, 3, 1}, {4, 2, 3}, {4, 3, 2}, {8, 2, 1}};
+static int g_stream_single = 0, g_stream_pipe = 1;
+static int g_stream_pipe_div = 3;  // a pipelined launch takes 1 / this of the resident warps
+static int g_stream_blocks[4] = {1, 1, 1, 1};  // resident CTAs per SM of each configuration
+static int g_sms = 152;
+
+template <int G, int C>
+static auto stream_kernel() {
+  constexpr StreamCfg cf = kStreamCfgs[C];
+  return k_attn_stream<G, cf.nw, cf.ns, cf.minb>;
+}
+
+template <int G, int C>
+static cudaError_t prep_stream() {
+  constexpr StreamCfg cf = kStreamCfgs[C];
+  const size_t smem = stream_smem<cf.ns>(cf.nw, kStreamMaxSlices);
+  cudaError_t e = cudaFuncSetAttribute(stream_kernel<G, C>(), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, stream_kernel<G, C>(), 32 * cf.nw,
+                                                    stream_ring_bytes<cf.ns>(cf.nw) + 8 * 1024);
+  if (e != cudaSuccess) return e;
+  g_stream_blocks[C] = per_sm > 0 ? per_sm : 1;
+  return cudaSuccess;
+}
+
+template <int G>
+static cudaError_t prep_stream_all() {
+  cudaError_t e = prep_stream<G, 0>();
+  if (e == cudaSuccess) e = prep_stream<G, 1>();
+  if (e == cudaSuccess) e = prep_stream<G, 2>();
+  if (e == cudaSuccess) e = prep_stream<G, 3>();
+  if (e != cudaSuccess) return e;
+  if (const char *env = getenv("LKV_ATTN_STREAM_PIPE")) {
+    const int x = atoi(env);
+    if (x >= 0 && x < 4) g_stream_pipe = x;
+  }
+  if (const char *env = getenv("LKV_ATTN_STREAM_DIV")) {
+    const int x = atoi(env);
+    if (x >= 1 && x <= 16) g_stream_pipe_div = x;
+  }
+  if (const char *env = getenv("LKV_ATTN_STREAM_SINGLE")) {
+    const int x = atoi(env);
+    if (x >= 0 && x < 4) g_stream_single = x;
+  }
+  return cudaSuccess;
+}
+
+template <int G, int C>
+static void launch_stream_c(const CtxView &v, const StepArgs &a, int slices, int concurrent,
+                            cudaStream_t st) {
+  constexpr StreamCfg cf = kStreamCfgs[C];
+  int64_t W = (int64_t)g_stream_blocks[C] * g_sms * cf.nw / (concurrent > 1 ? g_stream_pipe_div : 1);
+  const int64_t rows_cap = (int64_t)slices * ((a.budget + v.L + kStreamRowsPerWarp - 1) / kStreamRowsPerWarp);
+  if (W > rows_cap) W = rows_cap;
+  if (W < slices) W = slices;
+  if (W > v.w_cap) W = v.w_cap;
+  const int P = (int)((W + cf.nw - 1) / cf.nw);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(P);
+  cfg.blockDim = dim3(32 * cf.nw);
+  cfg.dynamicSmemBytes = stream_smem<cf.ns>(cf.nw, slices);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributePriority;
+  attr[1].val.priority = g_prio_attn;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  cudaLaunchKernelEx(&cfg, stream_kernel<G, C>(), v, a, slices, (int)W);
+}
+
+template <int G>
+static void launch_stream(const CtxView &v, const StepArgs &a, int slices, int concurrent,
+                          cudaStream_t st) {
+  switch (concurrent > 1 ? g_stream_pipe : g_stream_single) {
+    case 0: launch_stream_c<G, 0>(v, a, slices, concurrent, st); break;
+    case 1: launch_stream_c<G, 1>(v, a, slices, concurrent, st); break;
+    case 2: launch_stream_c<G, 2>(v, a, slices, concurrent, st); break;
+    default: launch_stream_c<G, 3>(v, a, slices, concurrent, st); break;
+  }
+}
+
 template <int DT, int G>
 static cudaError_t prep_attn() {
   cudaError_t e = cudaFuncSetAttribute(k_attn<DT, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1725,6 +2364,11 @@ static cudaError_t prep_attn() {
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   if (per_sm > 0 && sms > 0) g_attn_slots = per_sm * sms;
+  if (sms > 0) g_sms = sms;
+  if constexpr (DT == 1 && (G == 4 || G == 8)) {
+    e = prep_stream_all<G>();
+    if (e != cudaSuccess) return e;
+  }
   int least = 0, greatest = 0;  // numerically: least >= greatest; greatest is the highest priority
   if (cudaDeviceGetStreamPriorityRange(&least, &greatest) == cudaSuccess) {
     g_prio_chain = greatest;
@@ -1737,7 +2381,7 @@ static cudaError_t prep_attn() {
   e = cudaFuncSetAttribute(k_select, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSelSmemBytes);
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(k_step_boundary<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)(2 * kMaxHeads * kQPitch * sizeof(float)));
+                              (int)(2 * kMaxHeads * kQPitch * elem_bytes<DT>()));
 }
 
 template <int DT>
@@ -1765,7 +2409,7 @@ static cudaError_t decode_t(const CtxView &v, const StepArgs &a, cudaStream_t st
   if (e != cudaSuccess) return e;
   prof.begin(kPBoundary, st);
   launch_pdl(k_step_boundary<DT>, dim3(a.nl * v.B), dim3(kBoundaryThreads),
-             (size_t)2 * H * kQPitch * sizeof(float), st, v, a);
+             (size_t)2 * H * kQPitch * elem_bytes<DT>(), st, v, a);
   prof.end(st);
   // pipelined: the selection lane follows the boundary lane, the step's
   // attention follows its selection
@@ -1797,12 +2441,19 @@ static cudaError_t decode_t(const CtxView &v, const StepArgs &a, cudaStream_t st
   }
   const int conc = pipe ? kAttnConcurrent : 1;
   prof.begin(kPAttn, as);
-  switch (v.G) {
-    case 1: launch_attn<DT, 1>(v, a, slices, nch, conc, as); break;
-    case 2: launch_attn<DT, 2>(v, a, slices, nch, conc, as); break;
-    case 4: launch_attn<DT, 4>(v, a, slices, nch, conc, as); break;
-    case 8: launch_attn<DT, 8>(v, a, slices, nch, conc, as); break;
-    default: return cudaErrorInvalidValue;
+  const bool stream = DT == 1 && (v.G == 4 || v.G == 8) && slices <= kStreamMaxSlices;
+  if (stream && v.G == 4) {
+    launch_stream<4>(v, a, slices, conc, as);
+  } else if (stream) {
+    launch_stream<8>(v, a, slices, conc, as);
+  } else {
+    switch (v.G) {
+      case 1: launch_attn<DT, 1>(v, a, slices, nch, conc, as); break;
+      case 2: launch_attn<DT, 2>(v, a, slices, nch, conc, as); break;
+      case 4: launch_attn<DT, 4>(v, a, slices, nch, conc, as); break;
+      case 8: launch_attn<DT, 8>(v, a, slices, nch, conc, as); break;
+      default: return cudaErrorInvalidValue;
+    }
   }
   prof.end(as);
   if (pipe) {

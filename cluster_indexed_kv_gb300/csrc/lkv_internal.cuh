@@ -72,7 +72,9 @@ struct CtxView {
   DecState *st;               // [lb]
   void *q_prev;               // [lb][H][d] (dtype)
   float *q_attn;              // [kRing step slots][lb][H][d] queries * log2(e)/sqrt(d), fp32
-  int4 *aview;                // [step slot][lb] (t, win_start, plan slot, 0) for the attention
+  int4 *aview;                // [step slot][lb] (t, win_start, plan slot, 2 * units + flag)
+  int4 *adesc;                // [step slot][slice] (t, win_start, plan slot, selected tokens),
+                              // written by the selection kernel on every step
   int64_t *segsum;            // [slice][d] exact fixed-point sums (bf16) or
                               // doubles reinterpreted (fp32)
   float *scores;              // [slice][u_cap]
@@ -88,7 +90,9 @@ struct CtxView {
   int4 *chunk_pieces;         // [kRing][slice][max_chunks][64] the pieces of each chunk
   int32_t *chunk_count;       // [kRing][slice][max_chunks] pieces in each chunk
   int32_t max_pieces;
-  int32_t *attn_count;        // [kRing step slots][slice] attention CTAs done (last one combines)
+  int32_t *attn_count;        // [kRing step slots][slice] attention CTAs / warps done (last one combines)
+  float *attn_wpart;          // [kRing][w_cap][G * d + 2 * G] per-warp partials of the streaming attention
+  int32_t w_cap;              // warps the streaming attention may use in one launch
   float *attn_part;           // [kRing][slice][kAttnMaxSplit][G * d + 2 * G] CTA partials
   int32_t max_chunks;
   int32_t *err;               // device error bits (shared by all layers)
@@ -328,6 +332,9 @@ cudaError_t launch_uva_read(const void *host_src, void *dev_dst, int64_t bytes, 
 cudaError_t launch_diag_wait(const CtxView &v, uint64_t limit_ns, cudaStream_t stream);
 // Error text of calls that have no context (read with lkv_last_error(NULL)).
 void set_unbound_error(const char *msg);
+// Per-warp partial slots the streaming attention needs on a GPU with `sms`
+// multiprocessors (the most warps one launch may use).
+int stream_warp_cap(int sms);
 // One-time kernel attributes (dynamic shared memory limits), before any capture.
 cudaError_t prepare_kernels(int dtype, int group);
 

@@ -219,7 +219,10 @@ def test_errors_are_status_codes():
 
 def test_decode_steps_graph_matches_single_steps():
     """lkv_decode_steps (64-step CUDA graphs + tail, chunked over one set of
-    full-length buffers) gives bit-identical results to single steps."""
+    full-length buffers) takes bit-identical decisions (flags, selection
+    sizes and sets) to single steps; the attention outputs agree within fp32
+    rounding (the two paths split a slice's rows over different warp groups,
+    which changes the order of the partial softmax sums)."""
     w = synth.WORKLOADS["long_out"].replace(batch=2, n_kv_heads=2, n_prefill=600, n_components=20,
                                             n_clusters=20, iters=3, local_buf=16, budget=120,
                                             jump_p=0.1)
@@ -247,8 +250,10 @@ def test_decode_steps_graph_matches_single_steps():
         ctx.sync()
         outs.append((out.cpu(), bnd.cpu(), nsel.cpu(), sel.cpu()))
         ctx.close()
-    for a, b in zip(outs[0], outs[1]):
+    for a, b in zip(outs[0][1:], outs[1][1:]):
         assert torch.equal(a, b)
+    o1, o2 = outs[0][0], outs[1][0]
+    assert torch.allclose(o1, o2, rtol=1e-5, atol=1e-6), (o1 - o2).abs().max()
     assert outs[0][1].sum() > 3
 
 
