@@ -455,14 +455,11 @@ __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
 // Branch-free candidate tracking for the tensor-core filter. A value carries
 // its column's position among the thread's 64 columns of a chunk in the low
 // six mantissa bits (a relative change below 2^-17, covered by the filter's
-// margin), so the three smallest values keep their columns without separate
-// index bookkeeping.
-__device__ __forceinline__ float pack6(float e, uint32_t local) {
-  return __uint_as_float((__float_as_uint(e) & 0xFFFFFFC0u) | local);
-}
-// The same bits computed with integer multiplies, (e >> 6) * 64 + local, with
-// the multipliers 2^26 and 64 passed in at run time: the epilogue's min/max
-// network saturates the ALU pipe, and multiplies issue on the FMA pipe.
+// margin), so the two smallest values keep their columns without separate
+// index bookkeeping. The bits are formed with integer multiplies,
+// (e >> 6) * 64 + local, with the multipliers 2^26 and 64 passed in at run
+// time: the min/max network already loads the ALU pipe, and multiplies issue
+// on the FMA pipe (measured faster than a single logic operation on the ALU).
 __device__ __forceinline__ float pack6_mul(float e, uint32_t local, uint32_t m26, uint32_t m64) {
   return __uint_as_float(__umulhi(__float_as_uint(e), m26) * m64 + local);
 }
@@ -471,18 +468,20 @@ __device__ __forceinline__ float min3f(float a, float b, float c) {
   asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
 }
-// Sorted (c1 <= c2 <= c3) absorbs the pair {q, r}. Merging the sorted pairs
-// (c1, c2) and (m, M) = (min, max)(q, r) is Batcher's 2 x 2 merge: the
-// smallest is min(c1, m) and the middle two are u = max(c1, m) and
-// v = min(c2, M) in either order; c3 caps the third.
-__device__ __forceinline__ void top3_pair(float &c1, float &c2, float &c3, float q, float r) {
+// The two smallest values of a block (c1 <= c2) absorb the pair {q, r}. With
+// (m, M) = (min, max)(q, r), the k-th smallest of the union of two sorted
+// lists is the minimum over i + j = k of max(a_i, b_j): the smallest is
+// min(c1, m) and the second min(c2, max(c1, m), M). Five min/max operations
+// per two values.
+__device__ __forceinline__ void top2_pair(float &c1, float &c2, float q, float r) {
   const float m = fminf(q, r), M = fmaxf(q, r);
-  const float u = fmaxf(c1, m), v = fminf(c2, M);
+  c2 = min3f(c2, fmaxf(c1, m), M);
   c1 = fminf(c1, m);
-  c2 = fminf(u, v);
-  c3 = fminf(c3, fmaxf(u, v));
 }
-// Merge of two candidate lists with explicit column ids.
+// Merge of two candidate lists with explicit column ids. The first two
+// entries of each list are exact; the third may be a lower bound of the
+// list's third smallest value, and the merged third is then a lower bound
+// too (it is a non-decreasing function of the inputs).
 __device__ __forceinline__ Top3 top3_union(const Top3 &a, const Top3 &b) {
   Top3 r;
   const bool bw = b.v1 < a.v1;
@@ -630,7 +629,7 @@ k_assign_tc(const __grid_constant__ CUtensorMap keys_map, const __grid_constant_
       const float4 *c2s = (const float4 *)(c2 + (int64_t)sl * c2_pitch + qtr * 64);
       for (int ch = 0; ch < nch; ++ch, ++gc) {
         const int ti = gc & 1;
-        float p1 = INFINITY, p2 = INFINITY, p3 = INFINITY;  // this chunk's 64 columns
+        float p1 = INFINITY, p2 = INFINITY;  // the two smallest of this chunk's 64 columns
 #pragma unroll
         for (int g = 0; g < 2; ++g) {
           // |c|^2 of the 32 columns (FLT_MAX past the last cluster), requested
@@ -654,17 +653,20 @@ k_assign_tc(const __grid_constant__ CUtensorMap keys_map, const __grid_constant_
                                    make_float2(__uint_as_float(r[4 * e + 2]), __uint_as_float(r[4 * e + 3])),
                                    make_float2(cc[e].z, cc[e].w));
             const uint32_t l0 = g * 32 + 4 * e;
-            top3_pair(p1, p2, p3, pack6_mul(lo.x, l0, m26, m64), pack6_mul(lo.y, l0 + 1, m26, m64));
-            top3_pair(p1, p2, p3, pack6_mul(hi.x, l0 + 2, m26, m64), pack6_mul(hi.y, l0 + 3, m26, m64));
+            top2_pair(p1, p2, pack6_mul(lo.x, l0, m26, m64), pack6_mul(lo.y, l0 + 1, m26, m64));
+            top2_pair(p1, p2, pack6_mul(hi.x, l0 + 2, m26, m64), pack6_mul(hi.y, l0 + 3, m26, m64));
           }
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) tc_arrive(&acc_empty[ti]);
-        // fold the chunk's three into the running list with column ids
+        // fold the chunk's two into the running list with column ids; the
+        // chunk's third smallest is at least p2, so p2 stands in as a lower
+        // bound for it (a key is certified to have at most two candidates
+        // only when that bound clears the margin)
         const int jb = ch * kTcN + qtr * 64;
         Top3 cur;
-        cur.v1 = p1; cur.v2 = p2; cur.v3 = p3;
+        cur.v1 = p1; cur.v2 = p2; cur.v3 = p2;
         cur.j1 = p1 < INFINITY ? jb + (int)(__float_as_uint(p1) & 63u) : 0x7fffffff;
         cur.j2 = p2 < INFINITY ? jb + (int)(__float_as_uint(p2) & 63u) : 0x7fffffff;
         top = top3_union(top, cur);
