@@ -268,26 +268,23 @@ def attn_roofline(kern, ctr, w, eb):
 
 
 def selection_rooflines(kern, ctr, w, eb, hbm_peak, peak_kind):
-    """HBM rooflines of the scoring and selection kernels from a profiled pass
-    in which every slice retrieves. Scoring reads one centroid-operand row per
-    unit (d elements) and the group's queries; selection reads a score, a
-    length and a first pool row per unit (12 bytes) and writes the selected
-    ids, first rows and token offsets (12 bytes a unit) and the pool row of
-    every selected token (4 bytes)."""
-    out = {}
-    n_sc, ms_sc = kern["lkv_score"]
-    n_se, ms_se = kern["lkv_select"]
+    """HBM roofline of the scoring + selection kernel from a profiled pass in
+    which every slice retrieves. Per slice it reads one centroid-operand row
+    per unit (d elements), the group's queries, and a length and a first
+    pool row per unit (8 bytes), and writes the selected ids, first rows and
+    token offsets (12 bytes a selected unit) and the pool row of every
+    selected token (4 bytes)."""
+    n, ms = kern["lkv_select"]
     slices = ctr["attn_slices"]
-    b_sc = (ctr["score_units"] * 128 * eb + slices * w.group * 128 * eb) / max(n_sc, 1)
-    b_se = (ctr["score_units"] * 12 + ctr["sel_units"] * 12 + ctr["sel_tokens"] * 4) / max(n_se, 1)
-    for name, n, ms, b in (("k_score", n_sc, ms_sc, b_sc), ("k_select", n_se, ms_se, b_se)):
-        sec = ms / max(n, 1) / 1e3
-        a = b / sec / 1e9 if sec > 0 else None
-        out[name] = {"bound": "hbm", "achieved": a, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": a / hbm_peak if a else None, "alg_bytes_per_launch": b,
-                     "avg_launch_us": sec * 1e6, "launches": int(n),
-                     "peak_source": f"{peak_kind} hbm_gbs (burst copy)"}
-    return out
+    b = (ctr["score_units"] * (128 * eb + 8) + slices * w.group * 128 * eb
+         + ctr["sel_units"] * 12 + ctr["sel_tokens"] * 4) / max(n, 1)
+    sec = ms / max(n, 1) / 1e3
+    a = b / sec / 1e9 if sec > 0 else None
+    return {"k_select": {"bound": "hbm", "achieved": a, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": a / hbm_peak if a else None, "alg_bytes_per_launch": b,
+                         "avg_launch_us": sec * 1e6, "launches": int(n),
+                         "peak_source": f"{peak_kind} hbm_gbs (burst copy)",
+                         "note": "scoring and budget selection in one kernel"}}
 
 
 def run_ours(args, rank, world, local):

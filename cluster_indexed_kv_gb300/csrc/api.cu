@@ -99,7 +99,7 @@ static void free_all(lkv_ctx *c) {
   c->prof.release();
   if (c->capture) cudaStreamDestroy(c->capture);
   c->capture = nullptr;
-  for (int i = 0; i < lkv::kRing; ++i) {
+  for (int i = 0; i < lkv::kAttnStreams; ++i) {
     if (c->pipe.attn[i]) cudaStreamDestroy(c->pipe.attn[i]);
     if (c->pipe.attn_done[i]) cudaEventDestroy(c->pipe.attn_done[i]);
     c->pipe.attn[i] = nullptr;
@@ -180,6 +180,11 @@ lkv_status lkv_create(const lkv_config *cfg, lkv_ctx **out) {
   // the tensor-core attention (bf16, 4 or 8 query heads per KV head) reads
   // the per-token rows; the pieces serve the host gather and the scalar attention
   v.need_pieces = (v.offload || !(k.dtype == 1 && (G == 4 || G == 8))) ? 1 : 0;
+  // the streaming attention over an HBM pool takes its selections from one
+  // launch per chunk of steps, with a plan ring for two chunks
+  v.chunk_sel = (!v.offload && !v.need_pieces && S_all <= lkv::kStreamMaxSlices) ? 1 : 0;
+  v.plan_ring = v.chunk_sel ? 2 * lkv::kChunk + 1 : lkv::kRing;
+  const int64_t R = v.plan_ring;
   v.S_all = S_all;
   v.n_lb = (int32_t)LB;
   v.pool_rows = pool_rows;
@@ -197,8 +202,8 @@ lkv_status lkv_create(const lkv_config *cfg, lkv_ctx **out) {
     v.dec_k = dalloc(c, S_all * t_cap * d * es, &st);
     v.dec_v = dalloc(c, S_all * t_cap * d * es, &st);
     v.dec_rows = t_cap;
-    v.stage_k = dalloc(c, lkv::kRing * S_all * (int64_t)k.max_budget * d * es, &st);  // per plan slot
-    v.stage_v = dalloc(c, lkv::kRing * S_all * (int64_t)k.max_budget * d * es, &st);
+    v.stage_k = dalloc(c, R * S_all * (int64_t)k.max_budget * d * es, &st);  // per plan slot
+    v.stage_v = dalloc(c, R * S_all * (int64_t)k.max_budget * d * es, &st);
   }
   v.cent_op = dalloc(c, S_all * u_cap * d * es, &st);
   v.cent32 = (float *)dalloc(c, S_all * u_cap * d * 4, &st);
@@ -208,21 +213,20 @@ lkv_status lkv_create(const lkv_config *cfg, lkv_ctx **out) {
   v.perm = (int32_t *)dalloc(c, S_all * n_cap * 4, &st);
   v.st = (DecState *)dalloc(c, LB * sizeof(DecState), &st);
   v.q_prev = dalloc(c, LB * H * d * es, &st);
-  v.q_attn = (float *)dalloc(c, lkv::kRing * LB * H * d * 4, &st);  // per step slot
-  v.aview = (int4 *)dalloc(c, lkv::kRing * LB * sizeof(int4), &st);
-  v.adesc = (int4 *)dalloc(c, lkv::kRing * S_all * sizeof(int4), &st);
+  v.q_attn = (float *)dalloc(c, lkv::kSlots * LB * H * d * 4, &st);  // per step slot
+  v.aview = (int4 *)dalloc(c, lkv::kSlots * LB * sizeof(int4), &st);
+  v.adesc = (int4 *)dalloc(c, lkv::kSlots * S_all * sizeof(int4), &st);
   v.segsum = (int64_t *)dalloc(c, S_all * d * 8, &st);
-  v.scores = (float *)dalloc(c, S_all * u_cap * 4, &st);
+  v.scores = (float *)dalloc(c, (v.chunk_sel ? lkv::kSlots : 1) * S_all * u_cap * 4, &st);
   // the selection plan, one copy per plan slot
-  v.sel = (int32_t *)dalloc(c, lkv::kRing * S_all * u_cap * 4, &st);
-  v.n_sel = (int32_t *)dalloc(c, lkv::kRing * S_all * 4, &st);
-  v.n_tok = (int32_t *)dalloc(c, lkv::kRing * S_all * 4, &st);
-  v.rng_row = (int32_t *)dalloc(c, lkv::kRing * S_all * u_cap * 4, &st);
-  v.rng_cum = (int32_t *)dalloc(c, lkv::kRing * S_all * (u_cap + 1) * 4, &st);
+  v.sel = (int32_t *)dalloc(c, R * S_all * u_cap * 4, &st);
+  v.n_sel = (int32_t *)dalloc(c, R * S_all * 4, &st);
+  v.n_tok = (int32_t *)dalloc(c, R * S_all * 4, &st);
   v.sel_cap = (int32_t)std::min<int64_t>(k.max_budget, (int64_t)n_cap + t_cap);
-  if (!k.offload) v.sel_rows = (int32_t *)dalloc(c, lkv::kRing * S_all * (int64_t)v.sel_cap * 4, &st);
+  if (!k.offload) v.sel_rows = (int32_t *)dalloc(c, R * S_all * (int64_t)v.sel_cap * 4, &st);
   v.max_chunks = max_chunks;
   v.attn_count = (int32_t *)dalloc(c, lkv::kRing * S_all * 4, &st);
+  v.sel_count = (int32_t *)dalloc(c, lkv::kRing * S_all * 4, &st);
   v.attn_part = (float *)dalloc(c, lkv::kRing * S_all * lkv::kAttnMaxSplit *
                                        (int64_t)(k.group * d + 2 * k.group) * 4, &st);
   if (st == LKV_OK) {
@@ -237,10 +241,11 @@ lkv_status lkv_create(const lkv_config *cfg, lkv_ctx **out) {
   v.attn_wpart = (float *)dalloc(c, lkv::kRing * (int64_t)v.w_cap *
                                         (int64_t)(k.group * d + 2 * k.group) * 4, &st);
   v.max_pieces = u_cap + max_chunks;
-  v.pieces = (int4 *)dalloc(c, S_all * (int64_t)v.max_pieces * sizeof(int4), &st);
-  v.chunk_piece = (int32_t *)dalloc(c, S_all * (int64_t)(max_chunks + 1) * 4, &st);
-  v.chunk_pieces = (int4 *)dalloc(c, lkv::kRing * S_all * (int64_t)max_chunks * lkv::kAttnChunk * sizeof(int4), &st);
-  v.chunk_count = (int32_t *)dalloc(c, lkv::kRing * S_all * (int64_t)max_chunks * 4, &st);
+  const int64_t pc = v.need_pieces ? 1 : 0;  // the copy pieces exist only where a reader needs them
+  v.pieces = (int4 *)dalloc(c, pc * S_all * (int64_t)v.max_pieces * sizeof(int4), &st);
+  v.chunk_piece = (int32_t *)dalloc(c, pc * S_all * (int64_t)(max_chunks + 1) * 4, &st);
+  v.chunk_pieces = (int4 *)dalloc(c, pc * R * S_all * (int64_t)max_chunks * lkv::kAttnChunk * sizeof(int4), &st);
+  v.chunk_count = (int32_t *)dalloc(c, pc * R * S_all * (int64_t)max_chunks * 4, &st);
   v.err = (int32_t *)dalloc(c, 4, &st);
   v.counters = (int64_t *)dalloc(c, lkv::kCounters * 8, &st);
 
@@ -266,12 +271,13 @@ lkv_status lkv_create(const lkv_config *cfg, lkv_ctx **out) {
   cudaError_t e = cudaSuccess;
   if (e == cudaSuccess) e = cudaMemsetAsync(v.st, 0, LB * sizeof(DecState), c->stream);
   if (e == cudaSuccess) e = cudaMemsetAsync(v.attn_count, 0, lkv::kRing * S_all * 4, c->stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(v.sel_count, 0, lkv::kRing * S_all * 4, c->stream);
   if (e == cudaSuccess) e = cudaMemsetAsync(v.err, 0, 4, c->stream);
   if (e == cudaSuccess) e = cudaMemsetAsync(ks.n_refined, 0, 8, c->stream);
   if (e == cudaSuccess) e = cudaMemsetAsync(ks.n_inexact, 0, 8, c->stream);
   if (e == cudaSuccess) e = cudaMemsetAsync(v.counters, 0, lkv::kCounters * 8, c->stream);
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&c->capture, cudaStreamNonBlocking);
-  for (int i = 0; i < lkv::kRing; ++i) {
+  for (int i = 0; i < lkv::kAttnStreams; ++i) {
     if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&c->pipe.attn[i], cudaStreamNonBlocking);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->pipe.attn_done[i], cudaEventDisableTiming);
   }
@@ -404,8 +410,6 @@ static lkv::StepArgs step_args(lkv_ctx *c, int32_t layer, int32_t nl, bool multi
   return a;
 }
 
-static int kernels_per_step(const lkv_ctx *c) { return c->v.offload ? 5 : 4; }
-
 lkv_status lkv_decode_step(lkv_ctx *c, int32_t layer, int32_t nl, const void *q,
                            const void *k_new, const void *v_new, float tau, int32_t budget,
                            int32_t local_buf, float *out, int32_t *selected_units,
@@ -416,7 +420,7 @@ lkv_status lkv_decode_step(lkv_ctx *c, int32_t layer, int32_t nl, const void *q,
   if (s != LKV_OK) return s;
   lkv::StepArgs a = step_args(c, layer, nl, false, q, k_new, v_new, tau, budget, out,
                               selected_units, n_selected, boundary, r_out);
-  cudaError_t e = lkv::launch_decode_step(c->v, a, c->stream, c->prof);
+  cudaError_t e = lkv::launch_decode_steps(c->v, a, 1, c->stream, c->prof);
   if (e != cudaSuccess) return cuda_fail(c, e, "lkv_decode_step");
   for (int l = layer; l < layer + nl; ++l) c->steps[l] += 1;
   return LKV_OK;
@@ -437,15 +441,15 @@ static cudaError_t step_graph(lkv_ctx *c, const lkv::StepArgs &a, int steps, cud
   // step i's attention overlaps step i + 1's boundary test and selection
   // (step and plan slots keep their inputs apart)
   lkv::Pipe pipe = c->pipe;
-  for (int i = 0; i < steps && e == cudaSuccess; ++i) {
+  for (int i = 0; i < steps && e == cudaSuccess; i += lkv::kChunk) {
     lkv::StepArgs ai = a;
-    ai.slot = i % lkv::kRing;
+    ai.slot = i;
     pipe.step = i;
-    e = lkv::launch_decode_step(c->v, ai, c->capture, quiet, &pipe);
+    e = lkv::launch_decode_steps(c->v, ai, std::min(lkv::kChunk, steps - i), c->capture, quiet, &pipe);
   }
   // join every lane back into the capture stream
-  for (int i = 0; i < lkv::kRing && i < steps && e == cudaSuccess; ++i)
-    e = cudaStreamWaitEvent(c->capture, c->pipe.attn_done[(steps - 1 - i) % lkv::kRing], 0);
+  for (int i = 0; i < lkv::kAttnStreams && i < steps && e == cudaSuccess; ++i)
+    e = cudaStreamWaitEvent(c->capture, c->pipe.attn_done[(steps - 1 - i) % lkv::kAttnStreams], 0);
   if (e == cudaSuccess && steps > 0) e = cudaEventRecord(c->pipe.sel_done, c->pipe.sel);
   if (e == cudaSuccess && steps > 0) e = cudaStreamWaitEvent(c->capture, c->pipe.sel_done, 0);
   cudaError_t e2 = cudaStreamEndCapture(c->capture, &graph);
@@ -480,19 +484,23 @@ lkv_status lkv_decode_steps(lkv_ctx *c, int32_t layer, int32_t nl, int32_t n_ste
   lkv::StepArgs a = step_args(c, layer, nl, true, q, k_new, v_new, tau, budget, out,
                               selected_units, n_selected, boundary, r_out);
   cudaError_t e = cudaSuccess;
-  constexpr int kGraphSteps = 64;
+  constexpr int kGraphSteps = lkv::kSlots;  // one captured graph: two boundary chunks
   if (c->prof.timing || n_steps < kGraphSteps) {
-    for (int i = 0; i < n_steps && e == cudaSuccess; ++i) e = lkv::launch_decode_step(c->v, a, c->stream, c->prof);
+    for (int i = 0; i < n_steps && e == cudaSuccess; ++i) e = lkv::launch_decode_steps(c->v, a, 1, c->stream, c->prof);
   } else {
     cudaGraphExec_t exec = nullptr;
     e = step_graph(c, a, kGraphSteps, &exec);
     const int reps = n_steps / kGraphSteps, tail = n_steps % kGraphSteps;
     for (int r = 0; r < reps && e == cudaSuccess; ++r) e = cudaGraphLaunch(exec, c->stream);
     if (e == cudaSuccess && c->prof.counting) {
-      const int kinds[5] = {lkv::kPBoundary, lkv::kPScore, lkv::kPSelect, lkv::kPAttn, lkv::kPGather};
-      for (int k = 0; k < kernels_per_step(c); ++k) c->prof.launches[kinds[k]] += (int64_t)reps * kGraphSteps;
+      // per graph: a boundary launch per chunk; selection, attention (and the
+      // offload gather) per step
+      c->prof.launches[lkv::kPBoundary] += (int64_t)reps * (kGraphSteps / lkv::kChunk);
+      c->prof.launches[lkv::kPSelect] += (int64_t)reps * (c->v.chunk_sel ? kGraphSteps / lkv::kChunk : kGraphSteps);
+      c->prof.launches[lkv::kPAttn] += (int64_t)reps * kGraphSteps;
+      if (c->v.offload) c->prof.launches[lkv::kPGather] += (int64_t)reps * kGraphSteps;
     }
-    for (int i = 0; i < tail && e == cudaSuccess; ++i) e = lkv::launch_decode_step(c->v, a, c->stream, c->prof);
+    for (int i = 0; i < tail && e == cudaSuccess; ++i) e = lkv::launch_decode_steps(c->v, a, 1, c->stream, c->prof);
   }
   if (e != cudaSuccess) return cuda_fail(c, e, "lkv_decode_steps");
   for (int l = layer; l < layer + nl; ++l) c->steps[l] += n_steps;

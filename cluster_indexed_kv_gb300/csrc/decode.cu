@@ -1,17 +1,17 @@
-// decode.cu -- one decode step of LouisKV-style retrieval for a range of
-// layers and all sequences [LouisKV notes, 方法详解 flowchart; 关键设计 1-3]:
+// decode.cu -- decode steps of LouisKV-style retrieval for a range of layers
+// and all sequences [LouisKV notes, 方法详解 flowchart; 关键设计 1-3]:
 //
 //   k_step_boundary  r_t, trigger flag, segment close, local-buffer eviction,
-//                    append of token t                      (1 CTA / (seq, layer))
-//   k_score          s_u = qbar . c_u for every unit   (8 CTAs / slice, trigger steps only)
-//   k_select         the (score desc, id asc) budget prefix, the pool row of
-//                    every selected token and the copy pieces of the selected
-//                    rows in 64-token chunks          (1 CTA / slice, trigger steps only)
+//                    append of token t, for a chunk of steps    (1 CTA / (seq, layer))
+//   k_select         on retrieval steps: s_u = qbar . c_u for every unit, the
+//                    (score desc, id asc) budget prefix, the pool row of every
+//                    selected token; on every step the attention's descriptor
+//                                                              (1 CTA / slice / step)
 //   k_gather_offload selected rows host -> HBM staging (UVA; offload only)
-//   k_attn           split-K softmax attention: each CTA takes a run of
-//                    64-token chunks of (selected rows ++ local buffer); the
-//                    last CTA of each (seq, layer, kv head) combines the
-//                    partials
+//   k_attn_stream    tensor-core attention over (local buffer ++ selected rows)
+//                    of every slice, rows split over warps by each slice's size;
+//                    the last partial of a slice combines (k_attn: the scalar
+//                    variant for fp32 rows or 1-2 query heads)
 //
 // Inputs/outputs of step k of a call live at base + k * stride (StepArgs).
 #include <cstdlib>
@@ -153,8 +153,14 @@ __device__ __forceinline__ float qs_get(const void *qs, int i) {
   else return ((const float *)qs)[i];
 }
 
+// n_steps consecutive decode steps of one (sequence, layer) per CTA, step i
+// in step slot a.slot + i. The state machine (segments, local buffer,
+// evictions, plan slot) is sequential, but it depends only on the step
+// inputs, never on a selection or an attention, so one launch runs a whole
+// chunk of steps ahead of the selections and attentions that read its
+// per-step views.
 template <int DT>
-__global__ void __launch_bounds__(kBoundaryThreads, 2) k_step_boundary(CtxView v, StepArgs a) {
+__global__ void __launch_bounds__(kBoundaryThreads, 2) k_step_boundary(CtxView v, StepArgs a, int n_steps) {
   const int li = blockIdx.x / v.B, b = blockIdx.x % v.B;
   const int l = a.l0 + li;
   const int64_t lb = (int64_t)l * v.B + b;
@@ -169,10 +175,7 @@ __global__ void __launch_bounds__(kBoundaryThreads, 2) k_step_boundary(CtxView v
   QT *qsm = reinterpret_cast<QT *>(qsm_raw);
   pdl_wait();
   pdl_trigger();
-  if (tid == 0) {
-    st = v.st[lb];
-    slow_any = 0;
-  }
+  if (tid == 0) st = v.st[lb];
   // loads that do not depend on the step go out with the state's: the
   // previous queries (16-byte vectors into padded shared rows) and this
   // thread's running sums of the open segment
@@ -194,6 +197,11 @@ __global__ void __launch_bounds__(kBoundaryThreads, 2) k_step_boundary(CtxView v
     if (x < v.Hkv * kHeadDim) ssum[r] = v.segsum[(lb * v.Hkv + x / kHeadDim) * kHeadDim + x % kHeadDim];
   }
   __syncthreads();
+  for (int i_step = 0; i_step < n_steps; ++i_step) {
+  // queries of step t - 1 in buffer pb, of step t in cb
+  const int pb = i_step & 1, cb = pb ^ 1;
+  const int slot = a.slot + i_step;
+  if (tid == 0) slow_any = 0;
   const int t = st.t;
   const int n_closed0 = st.n_closed;
   const int64_t k = t - a.base_t;
@@ -218,7 +226,7 @@ __global__ void __launch_bounds__(kBoundaryThreads, 2) k_step_boundary(CtxView v
   }
   for (int y = tid; y < nvec; y += nth) {
     const int head = y / (kHeadDim / per16), j0 = (y % (kHeadDim / per16)) * per16;
-    *(uint4 *)(qsm + ((int64_t)H + head) * kQPitch + j0) =
+    *(uint4 *)(qsm + ((int64_t)cb * H + head) * kQPitch + j0) =
         __ldg((const uint4 *)((const QT *)q + qoff + (int64_t)head * kHeadDim + j0));
   }
   __syncthreads();
@@ -226,8 +234,8 @@ __global__ void __launch_bounds__(kBoundaryThreads, 2) k_step_boundary(CtxView v
   // 1. r_t = (1/H) sum_h cos(q_{t-1}^h, q_t^h) in fp32, fixed operation order
   if (t > 0) {
     if (tid < H) {
-      const QT *x = qsm + tid * kQPitch;
-      const QT *y = qsm + (H + tid) * kQPitch;
+      const QT *x = qsm + ((int64_t)pb * H + tid) * kQPitch;
+      const QT *y = qsm + ((int64_t)cb * H + tid) * kQPitch;
       float dot = 0.f, na = 0.f, nb = 0.f;
 #pragma unroll 8
       for (int j = 0; j < kHeadDim; ++j) {
@@ -246,12 +254,12 @@ __global__ void __launch_bounds__(kBoundaryThreads, 2) k_step_boundary(CtxView v
       r = __fdiv_rn(r, (float)H);
       st.r = r;
       st.flag = r < a.tau ? 1 : 0;
-      if (st.flag) st.plan = (st.plan + 1) % kRing;  // a retrieval writes the next plan slot
+      if (st.flag) st.plan = (st.plan + 1) % v.plan_ring;  // a retrieval writes the next plan slot
     }
   } else if (tid == 0) {
     st.r = 0.f;
     st.flag = 1;
-    st.plan = (st.plan + 1) % kRing;
+    st.plan = (st.plan + 1) % v.plan_ring;
   }
   __syncthreads();
 
@@ -325,39 +333,42 @@ __global__ void __launch_bounds__(kBoundaryThreads, 2) k_step_boundary(CtxView v
     if constexpr (DT == 1) {
       ((uint16_t *)v.dec_k)[di] = (uint16_t)(kbits[r] >> 16);
       ((uint16_t *)v.dec_v)[di] = (uint16_t)(kbits[r] & 0xffffu);
-      v.segsum[gs * kHeadDim + dim] = prev + bf16_fixed40((uint16_t)(kbits[r] >> 16), &slow);
+      ssum[r] = prev + bf16_fixed40((uint16_t)(kbits[r] >> 16), &slow);
     } else {
       ((float *)v.dec_k)[di] = __uint_as_float(kbits[r]);
       ((float *)v.dec_v)[di] = __uint_as_float(vbits[DT == 1 ? 0 : r]);
-      v.segsum[gs * kHeadDim + dim] =
-          __double_as_longlong(__dadd_rn(__longlong_as_double(prev), (double)__uint_as_float(kbits[r])));
+      ssum[r] = __double_as_longlong(__dadd_rn(__longlong_as_double(prev), (double)__uint_as_float(kbits[r])));
     }
+    v.segsum[gs * kHeadDim + dim] = ssum[r];
   }
   if (slow) atomicOr(&slow_any, 1);
-  // the current queries become the previous ones; the attention gets them
-  // pre-scaled by log2(e)/sqrt(d) (its scores are in base 2)
+  // the attention gets this step's queries pre-scaled by log2(e)/sqrt(d)
+  // (its scores are in base 2)
   const float qscale = 1.4426950408889634f * rsqrtf((float)kHeadDim);
   for (int y = tid; y < nvec; y += nth) {
     const int head = y / (kHeadDim / per16), j0 = (y % (kHeadDim / per16)) * per16;
-    const QT *src = qsm + ((int64_t)H + head) * kQPitch + j0;
-    float4 *qa = (float4 *)(v.q_attn + (((int64_t)a.slot * v.n_lb + lb) * H + head) * kHeadDim + j0);
+    const QT *src = qsm + ((int64_t)cb * H + head) * kQPitch + j0;
+    float4 *qa = (float4 *)(v.q_attn + (((int64_t)slot * v.n_lb + lb) * H + head) * kHeadDim + j0);
 #pragma unroll
     for (int i = 0; i < per16 / 4; ++i)
       qa[i] = make_float4(qs_get<DT>(src, 4 * i) * qscale, qs_get<DT>(src, 4 * i + 1) * qscale,
                           qs_get<DT>(src, 4 * i + 2) * qscale, qs_get<DT>(src, 4 * i + 3) * qscale);
-    *(uint4 *)((QT *)v.q_prev + (lb * H + head) * kHeadDim + j0) = *(const uint4 *)src;
+    if (i_step == n_steps - 1)  // the last step's queries become the previous ones
+      *(uint4 *)((QT *)v.q_prev + (lb * H + head) * kHeadDim + j0) = *(const uint4 *)src;
   }
   __syncthreads();
   if (tid == 0) {
     if (slow_any) st.seg_slow = 1;
     st.t = t + 1;
-    v.st[lb] = st;
-    // what this step's attention needs, in the step's slot
-    v.aview[(int64_t)a.slot * v.n_lb + lb] = make_int4(t, st.win_start, st.plan, st.n_units * 2 + st.flag);
+    // what this step's scoring, selection and attention need, in its slot
+    v.aview[(int64_t)slot * v.n_lb + lb] = make_int4(t, st.win_start, st.plan, st.n_units * 2 + st.flag);
     const int64_t o = (int64_t)b * a.nl + li;
     if (a.boundary) a.boundary[k * a.stride_b + o] = (uint8_t)st.flag;
     if (a.r_out) a.r_out[k * a.stride_b + o] = st.r;
+    if (i_step == n_steps - 1) v.st[lb] = st;
   }
+  __syncthreads();
+  }  // steps
 }
 
 // ---------------------------------------------------------------- scoring + selection
@@ -416,6 +427,8 @@ __device__ __forceinline__ int2 block_scan_excl2(int32_t x, int32_t y, int32_t *
   return r;
 }
 
+// threads of the scoring + selection kernel: with at most 85 registers each a
+// CTA fits on an SM beside two attention CTAs
 constexpr int kScoreThreads = 256;
 constexpr int kScoreWarps = kScoreThreads / 32;
 
@@ -429,21 +442,22 @@ constexpr int kScoreWarps = kScoreThreads / 32;
 constexpr int kSelSmemUnits = 4096;  // units whose keys, lengths and rows fit in shared memory
 constexpr size_t kSelSmemBytes = (size_t)kSelSmemUnits * 12;
 
-__device__ void select_units(const CtxView &v, int64_t gs, int U, int budget, int ps) {
+// Keys, lengths and first pool rows of the units go into shared memory in one
+// round of loads (very large unit tables stay in global memory), unless the
+// caller already put the keys there (keys_in_smem); scg: the step's scores.
+__device__ void select_units(const CtxView &v, int64_t gs, int U, int budget, int ps, const float *scg,
+                             bool keys_in_smem) {
   const int tid = threadIdx.x, nth = blockDim.x, wid = tid >> 5;
-  // keys, lengths and first pool rows once into shared memory, with all the
-  // loads in flight together (very large unit tables stay in global memory)
   extern __shared__ __align__(16) uint32_t sel_smem[];
   uint32_t *key_s = sel_smem;
   int32_t *len_s = (int32_t *)(sel_smem + kSelSmemUnits);
   int32_t *row_s = (int32_t *)(sel_smem + 2 * kSelSmemUnits);
-  const float *scg = v.scores + gs * v.u_cap;
   const int32_t *lng = v.unit_len + gs * v.u_cap;
   const int32_t *rwg = v.unit_row + gs * v.u_cap;
   const bool in_smem = U <= kSelSmemUnits;
   if (in_smem)
     for (int u = tid; u < U; u += nth) {
-      key_s[u] = desc_key(__ldcg(scg + u));
+      if (!keys_in_smem) key_s[u] = desc_key(__ldcg(scg + u));
       len_s[u] = lng[u];
       row_s[u] = rwg[u];
     }
@@ -555,14 +569,10 @@ __device__ void select_units(const CtxView &v, int64_t gs, int U, int budget, in
   {
     int32_t run = tie_ex, kk = cnt_ex, cum = tok_ex;
     int32_t *sel_out = plan_sel(v, ps, gs);
-    int32_t *row_out = plan_rng_row(v, ps, gs);
-    int32_t *cum_out = plan_rng_cum(v, ps, gs);
     for (int u = u0; u < u1; ++u) {
       if (!is_sel(u, run)) continue;
       const int32_t len = lenof(u), row = rowof(u);
       sel_out[kk] = u;
-      row_out[kk] = row;
-      cum_out[kk] = cum;
       if (staged) {
         cum_sh[kk] = cum;
         row_sh[kk] = row;
@@ -617,8 +627,7 @@ __device__ void select_units(const CtxView &v, int64_t gs, int U, int budget, in
     *plan_ntok(v, ps, gs) = s_ntok;
     atomicAdd((unsigned long long *)&v.counters[kCntSelUnits], (unsigned long long)s_nsel);
     atomicAdd((unsigned long long *)&v.counters[kCntSelTokens], (unsigned long long)s_ntok);
-    plan_rng_cum(v, ps, gs)[s_nsel] = s_ntok;
-    if (nsc <= v.max_chunks) v.chunk_piece[gs * (int64_t)(v.max_chunks + 1) + nsc] = s_npieces;
+    if (v.need_pieces && nsc <= v.max_chunks) v.chunk_piece[gs * (int64_t)(v.max_chunks + 1) + nsc] = s_npieces;
     if (s_ntok > budget || s_ntok > v.sel_cap || s_npieces > v.max_pieces || nsc > v.max_chunks)
       set_err(v.err, kErrInternal);
   }
@@ -640,28 +649,103 @@ __device__ void select_units(const CtxView &v, int64_t gs, int U, int budget, in
   }
 }
 
-// kScoreSplit CTAs per (seq, layer, kv head), on retrieval steps only: the
-// score of every unit, a thread per unit (fp32 FMA in index order, the
-// centroid row in one round trip), so that the rows of all units are in
-// flight at once. The selection follows in k_select.
-constexpr int kScoreSplit = 16;
-constexpr int kScoreCtaThreads = 128;
+// kScoreSplit CTAs of kScoreThreads per (seq, layer, kv head) and step. On a
+// step without retrieval the first only records the step's descriptor for
+// the attention (the plan in force and its token count). On a retrieval step
+// every CTA scores its share of the units, s_u = qbar . c_u (qbar the fp32
+// sum of the group's queries in head order; the dot a sequential fp32 FMA
+// chain in index order, a thread per unit), and the last CTA of the slice to
+// finish takes the budget selection and writes the plan.
+constexpr int kScoreSplit = 8;
 
-// (128 threads with 80 registers each: a CTA fits beside two attention CTAs
-// and a thread keeps its unit's whole centroid row in flight)
 template <int DT>
-__global__ void __launch_bounds__(kScoreCtaThreads, 6) k_score(CtxView v, StepArgs a) {
+__global__ void __launch_bounds__(kScoreThreads, 3) k_select(CtxView v, StepArgs a) {
   const int per_l = v.B * v.Hkv;
   const int li = blockIdx.x / per_l, rem = blockIdx.x % per_l;
   const int b = rem / v.Hkv, h = rem % v.Hkv;
-  const int l = a.l0 + li;
-  const int64_t lb = (int64_t)l * v.B + b;
+  const int64_t lb = (int64_t)(a.l0 + li) * v.B + b;
   const int64_t gs = lb * v.Hkv + h;
-  pdl_wait();
+  const int tid = threadIdx.x, nth = blockDim.x;
+  pdl_wait();  // the step's view and every earlier selection's plan are complete and visible
   pdl_trigger();
-  // the step's view, not the live state: the next step's boundary kernel may
-  // already be updating that
   const int4 view = v.aview[(int64_t)a.slot * v.n_lb + lb];
+  int4 *desc = v.adesc + (int64_t)a.slot * v.S_all + gs;
+  if (!(view.w & 1)) {
+    // no retrieval: the plan in force stays; the attention's descriptor
+    // carries its token count
+    if (blockIdx.y == 0 && tid == 0) *desc = make_int4(view.x, view.y, view.z, *plan_ntok(v, view.z, gs));
+    return;
+  }
+  const int U = view.w >> 1;
+  const int64_t k = view.x - a.base_t;
+  const void *q = (const char *)a.q + k * a.stride_q * elem_bytes<DT>();
+  __shared__ float qbar[kHeadDim];
+  __shared__ int s_last;
+  const int H = v.Hkv * v.G;
+  const int64_t qoff = (((int64_t)b * a.nl + li) * H + (int64_t)h * v.G) * kHeadDim;
+  if (tid < kHeadDim) {
+    float acc = load_elem<DT>(q, qoff + tid);
+    for (int g = 1; g < v.G; ++g) acc = __fadd_rn(acc, load_elem<DT>(q, qoff + (int64_t)g * kHeadDim + tid));
+    qbar[tid] = acc;
+  }
+  __syncthreads();
+  constexpr int nvec = kHeadDim * elem_bytes<DT>() / 16;  // 16-byte vectors per centroid row
+  const uint4 *rows = (const uint4 *)((const char *)v.cent_op + gs * v.u_cap * kHeadDim * elem_bytes<DT>());
+  for (int u = blockIdx.y * nth + tid; u < U; u += gridDim.y * nth) {
+    uint4 cur[nvec];
+#pragma unroll
+    for (int j = 0; j < nvec; ++j) cur[j] = __ldg(rows + (int64_t)u * nvec + j);
+    float sc = 0.f;
+#pragma unroll
+    for (int j = 0; j < nvec; ++j) {
+      const uint32_t w[4] = {cur[j].x, cur[j].y, cur[j].z, cur[j].w};
+      if constexpr (DT == 1) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          sc = __fmaf_rn(qbar[j * 8 + 2 * e], __uint_as_float(w[e] << 16), sc);
+          sc = __fmaf_rn(qbar[j * 8 + 2 * e + 1], __uint_as_float(w[e] & 0xffff0000u), sc);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sc = __fmaf_rn(qbar[j * 4 + e], __uint_as_float(w[e]), sc);
+      }
+    }
+    v.scores[gs * v.u_cap + u] = sc;
+  }
+  // the last CTA of the slice to finish selects
+  __threadfence();
+  __syncthreads();
+  int32_t *cnt = v.sel_count + (int64_t)(a.slot & (kRing - 1)) * v.S_all + gs;
+  if (tid == 0) s_last = atomicAdd(cnt, 1) == (int)gridDim.y - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  if (tid == 0) {
+    *cnt = 0;
+    atomicAdd((unsigned long long *)&v.counters[kCntScoreUnits], (unsigned long long)U);
+  }
+  select_units(v, gs, U, a.budget, view.z, v.scores + gs * v.u_cap, false);
+  if (tid == 0) *desc = make_int4(view.x, view.y, view.z, *plan_ntok(v, view.z, gs));
+}
+
+// The selections of a whole chunk of steps in one launch (chunk selection):
+// a CTA per (slice, step of the chunk). Given the boundary kernel's views,
+// the retrievals of different steps are independent problems (each scores
+// the units present at its step and writes its own plan slot), so they run
+// side by side; a CTA of a step without retrieval leaves at once. Scores and
+// selection as in k_select, the scores of a step in its own slot.
+template <int DT>
+__global__ void __launch_bounds__(kScoreThreads, 3) k_select_chunk(CtxView v, StepArgs a) {
+  const int per_l = v.B * v.Hkv;
+  const int li = blockIdx.x / per_l, rem = blockIdx.x % per_l;
+  const int b = rem / v.Hkv, h = rem % v.Hkv;
+  const int64_t lb = (int64_t)(a.l0 + li) * v.B + b;
+  const int64_t gs = lb * v.Hkv + h;
+  const int tid = threadIdx.x, nth = blockDim.x;
+  const int slot = a.slot + blockIdx.y;
+  pdl_wait();  // the chunk's views are complete and visible
+  pdl_trigger();
+  const int4 view = v.aview[(int64_t)slot * v.n_lb + lb];
   if (!(view.w & 1)) return;
   const int U = view.w >> 1;
   const int64_t k = view.x - a.base_t;
@@ -669,61 +753,42 @@ __global__ void __launch_bounds__(kScoreCtaThreads, 6) k_score(CtxView v, StepAr
   __shared__ float qbar[kHeadDim];
   const int H = v.Hkv * v.G;
   const int64_t qoff = (((int64_t)b * a.nl + li) * H + (int64_t)h * v.G) * kHeadDim;
-  if (threadIdx.x < kHeadDim) {
-    float acc = load_elem<DT>(q, qoff + threadIdx.x);
-    for (int g = 1; g < v.G; ++g) acc = __fadd_rn(acc, load_elem<DT>(q, qoff + (int64_t)g * kHeadDim + threadIdx.x));
-    qbar[threadIdx.x] = acc;
+  if (tid < kHeadDim) {
+    float acc = load_elem<DT>(q, qoff + tid);
+    for (int g = 1; g < v.G; ++g) acc = __fadd_rn(acc, load_elem<DT>(q, qoff + (int64_t)g * kHeadDim + tid));
+    qbar[tid] = acc;
   }
   __syncthreads();
-  constexpr int nvec = kHeadDim * elem_bytes<DT>() / 16;  // 16-byte vectors per centroid row
-  for (int u = blockIdx.y * blockDim.x + threadIdx.x; u < U; u += gridDim.y * blockDim.x) {
-    const uint4 *row = (const uint4 *)((const char *)v.cent_op + (gs * v.u_cap + u) * kHeadDim * elem_bytes<DT>());
-    uint4 raw[nvec];
+  extern __shared__ __align__(16) uint32_t sel_smem[];
+  const bool in_smem = U <= kSelSmemUnits;
+  float *scg = v.scores + ((int64_t)slot * v.S_all + gs) * v.u_cap;
+  constexpr int nvec = kHeadDim * elem_bytes<DT>() / 16;
+  const uint4 *rows = (const uint4 *)((const char *)v.cent_op + gs * v.u_cap * kHeadDim * elem_bytes<DT>());
+  for (int u = tid; u < U; u += nth) {
+    uint4 cur[nvec];
 #pragma unroll
-    for (int j = 0; j < nvec; ++j) raw[j] = __ldg(row + j);
-    float s = 0.f;
+    for (int j = 0; j < nvec; ++j) cur[j] = __ldg(rows + (int64_t)u * nvec + j);
+    float sc = 0.f;
 #pragma unroll
     for (int j = 0; j < nvec; ++j) {
-      const uint32_t w[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
+      const uint32_t w[4] = {cur[j].x, cur[j].y, cur[j].z, cur[j].w};
       if constexpr (DT == 1) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          s = __fmaf_rn(qbar[j * 8 + 2 * e], __uint_as_float(w[e] << 16), s);
-          s = __fmaf_rn(qbar[j * 8 + 2 * e + 1], __uint_as_float(w[e] & 0xffff0000u), s);
+          sc = __fmaf_rn(qbar[j * 8 + 2 * e], __uint_as_float(w[e] << 16), sc);
+          sc = __fmaf_rn(qbar[j * 8 + 2 * e + 1], __uint_as_float(w[e] & 0xffff0000u), sc);
         }
       } else {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) s = __fmaf_rn(qbar[j * 4 + e], __uint_as_float(w[e]), s);
+        for (int e = 0; e < 4; ++e) sc = __fmaf_rn(qbar[j * 4 + e], __uint_as_float(w[e]), sc);
       }
     }
-    v.scores[gs * v.u_cap + u] = s;
+    if (in_smem) sel_smem[u] = desc_key(sc);
+    else scg[u] = sc;
   }
-  if (blockIdx.y == 0 && threadIdx.x == 0)
-    atomicAdd((unsigned long long *)&v.counters[kCntScoreUnits], (unsigned long long)U);
-}
-
-// One CTA per (seq, layer, kv head), on retrieval steps only, launched
-// behind the scoring grid (programmatic dependent launch): the budget
-// selection and the copy plan.
-__global__ void __launch_bounds__(kScoreThreads) k_select(CtxView v, StepArgs a) {
-  const int per_l = v.B * v.Hkv;
-  const int li = blockIdx.x / per_l, rem = blockIdx.x % per_l;
-  const int b = rem / v.Hkv, h = rem % v.Hkv;
-  const int64_t lb = (int64_t)(a.l0 + li) * v.B + b;
-  const int64_t gs = lb * v.Hkv + h;
-  // the step view was written before the scoring grid started (stream order)
-  const int4 view = v.aview[(int64_t)a.slot * v.n_lb + lb];
-  pdl_wait();  // the scores (and every earlier selection's plan) are complete and visible
-  pdl_trigger();
-  int4 *desc = v.adesc + (int64_t)a.slot * v.S_all + gs;
-  if (!(view.w & 1)) {
-    // no retrieval: the plan in force stays; the attention's descriptor
-    // carries its token count
-    if (threadIdx.x == 0) *desc = make_int4(view.x, view.y, view.z, *plan_ntok(v, view.z, gs));
-    return;
-  }
-  select_units(v, gs, view.w >> 1, a.budget, view.z);
-  if (threadIdx.x == 0) *desc = make_int4(view.x, view.y, view.z, *plan_ntok(v, view.z, gs));
+  if (tid == 0) atomicAdd((unsigned long long *)&v.counters[kCntScoreUnits], (unsigned long long)U);
+  __syncthreads();
+  select_units(v, gs, U, a.budget, view.z, scg, in_smem);
 }
 
 // ---------------------------------------------------------------- offload gather
@@ -1534,7 +1599,8 @@ __global__ void __launch_bounds__(attn_threads<DT, G>(), attn_min_blocks<DT, G>(
   // scratch when the slice is split over several CTAs, else to shared memory
   const int64_t so = ((int64_t)b * a.nl + li) * v.Hkv + h;
   constexpr int kPart = G * kHeadDim + 2 * G;  // acc [G][d], maxima [G], sums [G]
-  const int64_t slot_part = ((int64_t)a.slot * v.S_all + gs) * kAttnMaxSplit * kPart;
+  const int scr = a.slot & (kRing - 1);  // attention scratch slot
+  const int64_t slot_part = ((int64_t)scr * v.S_all + gs) * kAttnMaxSplit * kPart;
   float *mine = nsplit > 1 ? v.attn_part + slot_part + (int64_t)split * kPart : part;
   for (int x = tid; x < G * kHeadDim; x += NTH) {
     const int g = x / kHeadDim, dim = x % kHeadDim;
@@ -1560,7 +1626,7 @@ __global__ void __launch_bounds__(attn_threads<DT, G>(), attn_min_blocks<DT, G>(
   if (nsplit > 1) {
     __threadfence();
     __syncthreads();
-    if (tid == 0) s_last = atomicAdd(&v.attn_count[(int64_t)a.slot * v.S_all + gs], 1) == nsplit - 1;
+    if (tid == 0) s_last = atomicAdd(&v.attn_count[(int64_t)scr * v.S_all + gs], 1) == nsplit - 1;
     __syncthreads();
     if (!s_last) return;
     __threadfence();
@@ -1606,7 +1672,7 @@ __global__ void __launch_bounds__(attn_threads<DT, G>(), attn_min_blocks<DT, G>(
       for (int x = tid; x < ns; x += NTH) dst[x] = sel[x];
     }
     if (tid == 0) {
-      if (nsplit > 1) v.attn_count[(int64_t)a.slot * v.S_all + gs] = 0;
+      if (nsplit > 1) v.attn_count[(int64_t)scr * v.S_all + gs] = 0;
       if (a.n_selected) a.n_selected[k * a.stride_nsel + so] = ns;
       atomicAdd((unsigned long long *)&v.counters[kCntAttnRows], (unsigned long long)total);
       atomicAdd((unsigned long long *)&v.counters[kCntAttnSlices], 1ull);
@@ -1634,7 +1700,6 @@ __global__ void __launch_bounds__(attn_threads<DT, G>(), attn_min_blocks<DT, G>(
 // and softmax weights split into a bf16 high part and a bf16 residual, so
 // both keep fp32 accuracy), writes its partial softmax state, and the last
 // warp of the slice to finish combines the slice's partials.
-constexpr int kStreamMaxSlices = 1024;  // slices of one call the streaming kernel takes
 constexpr int kStreamRowsPerWarp = 64;  // fewest rows a warp is given at the largest budget
 
 template <int NS>
@@ -1682,14 +1747,23 @@ __global__ void __launch_bounds__(32 * NW, MINB) k_attn_stream(CtxView v, StepAr
   pdl_wait();
   pdl_trigger();
 
-  // 1. the call's slice descriptors, their row totals and the exclusive prefix
+  // 1. the call's slice descriptors (t, window start, plan slot, selected
+  //    tokens), their row totals and the exclusive prefix; with chunk
+  //    selection from the step view and the plan in force
   {
     const int4 *desc = v.adesc + (int64_t)a.slot * v.S_all + gs0;
     const int per = (S + 32 * NW - 1) / (32 * NW);
     const int s0 = tid * per, s1 = min(S, s0 + per);
     int32_t part = 0;
     for (int s = s0; s < s1; ++s) {
-      const int4 d = desc[s];
+      int4 d;
+      if (v.chunk_sel) {
+        const int64_t lb_s = (int64_t)(a.l0 + s / per_l) * v.B + (s % per_l) / v.Hkv;
+        const int4 vw = v.aview[(int64_t)a.slot * v.n_lb + lb_s];
+        d = make_int4(vw.x, vw.y, vw.z, *plan_ntok(v, vw.z, gs0 + s));
+      } else {
+        d = desc[s];
+      }
       ws_s[s] = d.y;
       nt_s[s] = d.w;
       t_s[s] = d.x;
@@ -2056,8 +2130,8 @@ __global__ void __launch_bounds__(32 * NW, MINB) k_attn_stream(CtxView v, StepAr
   // partial ids of the slice: its first warp, then the first warp of every
   // later CTA that serves it
   const int n_parts = 1 + (w0(sl + 1) - 1) / NW - wf / NW;
-  float *pbase = v.attn_wpart + (int64_t)a.slot * v.w_cap * kPart;
-  int32_t *cnt = v.attn_count + (int64_t)a.slot * v.S_all + gs;
+  float *pbase = v.attn_wpart + (int64_t)(a.slot & (kRing - 1)) * v.w_cap * kPart;
+  int32_t *cnt = v.attn_count + (int64_t)(a.slot & (kRing - 1)) * v.S_all + gs;
   if (n_parts > 1) {
     float *dst = pbase + (int64_t)w * kPart;
 #pragma unroll
@@ -2378,7 +2452,9 @@ static cudaError_t prep_attn() {
     const int x = atoi(env);
     g_attn_split = (x >= 1 && x <= kAttnMaxSplit) ? x : 0;
   }
-  e = cudaFuncSetAttribute(k_select, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSelSmemBytes);
+  e = cudaFuncSetAttribute(k_select<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSelSmemBytes);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(k_select_chunk<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSelSmemBytes);
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(k_step_boundary<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)(2 * kMaxHeads * kQPitch * elem_bytes<DT>()));
@@ -2400,19 +2476,18 @@ cudaError_t prepare_kernels(int dtype, int group) {
 }
 
 template <int DT>
-static cudaError_t decode_t(const CtxView &v, const StepArgs &a, cudaStream_t st, Prof &prof,
+static cudaError_t decode_t(const CtxView &v, const StepArgs &a, int n_steps, cudaStream_t st, Prof &prof,
                             const Pipe *pipe) {
   const int slices = a.nl * v.B * v.Hkv;
   const int H = v.Hkv * v.G;
   cudaError_t e = cudaSuccess;
-  if (pipe && pipe->step >= kRing) e = cudaStreamWaitEvent(st, pipe->attn_done[pipe->step % kRing], 0);
-  if (e != cudaSuccess) return e;
+  // the boundary tests and state of all n_steps steps, step i in slot a.slot + i
   prof.begin(kPBoundary, st);
   launch_pdl(k_step_boundary<DT>, dim3(a.nl * v.B), dim3(kBoundaryThreads),
-             (size_t)2 * H * kQPitch * elem_bytes<DT>(), st, v, a);
+             (size_t)2 * H * kQPitch * elem_bytes<DT>(), st, v, a, n_steps);
   prof.end(st);
-  // pipelined: the selection lane follows the boundary lane, the step's
-  // attention follows its selection
+  // pipelined: the selection lane follows the boundary kernel, each step's
+  // attention follows its selection on a side stream
   cudaStream_t ss = st;
   if (pipe) {
     ss = pipe->sel;
@@ -2420,53 +2495,93 @@ static cudaError_t decode_t(const CtxView &v, const StepArgs &a, cudaStream_t st
     if (e == cudaSuccess) e = cudaStreamWaitEvent(ss, pipe->b_done, 0);
     if (e != cudaSuccess) return e;
   }
-  prof.begin(kPScore, ss);
-  launch_pdl(k_score<DT>, dim3(slices, kScoreSplit), dim3(kScoreCtaThreads), 0, ss, v, a);
-  prof.end(ss);
-  prof.begin(kPSelect, ss);
-  launch_pdl(k_select, dim3(slices), dim3(kScoreThreads), kSelSmemBytes, ss, v, a);
-  prof.end(ss);
-  if (v.offload) {
-    prof.begin(kPGather, ss);
-    launch_pdl(k_gather_offload<DT>, dim3(slices, 64), dim3(256), 0, ss, v, a);
-    prof.end(ss);
-  }
   const int nch = (a.budget + v.L + kAttnChunk - 1) / kAttnChunk;
-  cudaStream_t as = st;
-  if (pipe) {
-    as = pipe->attn[pipe->step % kRing];
-    e = cudaEventRecord(pipe->sel_done, ss);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(as, pipe->sel_done, 0);
-    if (e != cudaSuccess) return e;
-  }
   const int conc = pipe ? kAttnConcurrent : 1;
-  prof.begin(kPAttn, as);
-  const bool stream = DT == 1 && (v.G == 4 || v.G == 8) && slices <= kStreamMaxSlices;
-  if (stream && v.G == 4) {
-    launch_stream<4>(v, a, slices, conc, as);
-  } else if (stream) {
-    launch_stream<8>(v, a, slices, conc, as);
-  } else {
-    switch (v.G) {
-      case 1: launch_attn<DT, 1>(v, a, slices, nch, conc, as); break;
-      case 2: launch_attn<DT, 2>(v, a, slices, nch, conc, as); break;
-      case 4: launch_attn<DT, 4>(v, a, slices, nch, conc, as); break;
-      case 8: launch_attn<DT, 8>(v, a, slices, nch, conc, as); break;
-      default: return cudaErrorInvalidValue;
+  if (v.chunk_sel) {
+    // chunk selection: every retrieval of the n_steps steps in one launch,
+    // then the steps' attentions (step i's on attn[i % kAttnStreams], so it
+    // follows step i - kAttnStreams's, whose scratch slot it may share)
+    prof.begin(kPSelect, ss);
+    launch_pdl(k_select_chunk<DT>, dim3(slices, n_steps), dim3(kScoreThreads), kSelSmemBytes, ss, v, a);
+    prof.end(ss);
+    if (pipe) {
+      e = cudaEventRecord(pipe->sel_done, ss);
+      if (e != cudaSuccess) return e;
     }
+    for (int i = 0; i < n_steps; ++i) {
+      StepArgs ai = a;
+      ai.slot = a.slot + i;
+      const int step = pipe ? pipe->step + i : 0;
+      cudaStream_t as = ss;
+      if (pipe) {
+        as = pipe->attn[step % kAttnStreams];
+        e = cudaStreamWaitEvent(as, pipe->sel_done, 0);
+        if (e != cudaSuccess) return e;
+      }
+      prof.begin(kPAttn, as);
+      if (v.G == 4) launch_stream<4>(v, ai, slices, conc, as);
+      else launch_stream<8>(v, ai, slices, conc, as);
+      prof.end(as);
+      if (pipe) {
+        e = cudaEventRecord(pipe->attn_done[step % kAttnStreams], as);
+        if (e != cudaSuccess) return e;
+      }
+    }
+    return cudaGetLastError();
   }
-  prof.end(as);
-  if (pipe) {
-    e = cudaEventRecord(pipe->attn_done[pipe->step % kRing], as);
-    if (e != cudaSuccess) return e;
+  for (int i = 0; i < n_steps; ++i) {
+    StepArgs ai = a;
+    ai.slot = a.slot + i;
+    const int step = pipe ? pipe->step + i : 0;
+    // bound the attentions in flight (see Pipe): every kSelWaitStride-th
+    // selection waits for the attention kAttnStreams steps before it
+    if (pipe && step >= kAttnStreams && step % kSelWaitStride == 0) {
+      e = cudaStreamWaitEvent(ss, pipe->attn_done[step % kAttnStreams], 0);
+      if (e != cudaSuccess) return e;
+    }
+    prof.begin(kPSelect, ss);
+    launch_pdl(k_select<DT>, dim3(slices, kScoreSplit), dim3(kScoreThreads), kSelSmemBytes, ss, v, ai);
+    prof.end(ss);
+    if (v.offload) {
+      prof.begin(kPGather, ss);
+      launch_pdl(k_gather_offload<DT>, dim3(slices, 64), dim3(256), 0, ss, v, ai);
+      prof.end(ss);
+    }
+    cudaStream_t as = ss;
+    if (pipe) {
+      as = pipe->attn[step % kAttnStreams];
+      e = cudaEventRecord(pipe->sel_done, ss);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(as, pipe->sel_done, 0);
+      if (e != cudaSuccess) return e;
+    }
+    prof.begin(kPAttn, as);
+    const bool stream = DT == 1 && (v.G == 4 || v.G == 8) && slices <= kStreamMaxSlices;
+    if (stream && v.G == 4) {
+      launch_stream<4>(v, ai, slices, conc, as);
+    } else if (stream) {
+      launch_stream<8>(v, ai, slices, conc, as);
+    } else {
+      switch (v.G) {
+        case 1: launch_attn<DT, 1>(v, ai, slices, nch, conc, as); break;
+        case 2: launch_attn<DT, 2>(v, ai, slices, nch, conc, as); break;
+        case 4: launch_attn<DT, 4>(v, ai, slices, nch, conc, as); break;
+        case 8: launch_attn<DT, 8>(v, ai, slices, nch, conc, as); break;
+        default: return cudaErrorInvalidValue;
+      }
+    }
+    prof.end(as);
+    if (pipe) {
+      e = cudaEventRecord(pipe->attn_done[step % kAttnStreams], as);
+      if (e != cudaSuccess) return e;
+    }
   }
   return cudaGetLastError();
 }
 
-cudaError_t launch_decode_step(const CtxView &v, const StepArgs &a, cudaStream_t stream,
-                               Prof &prof, const Pipe *pipe) {
-  if (v.dtype == 1) return decode_t<1>(v, a, stream, prof, pipe);
-  return decode_t<0>(v, a, stream, prof, pipe);
+cudaError_t launch_decode_steps(const CtxView &v, const StepArgs &a, int n_steps, cudaStream_t stream,
+                                Prof &prof, const Pipe *pipe) {
+  if (v.dtype == 1) return decode_t<1>(v, a, n_steps, stream, prof, pipe);
+  return decode_t<0>(v, a, n_steps, stream, prof, pipe);
 }
 
 }  // namespace lkv

@@ -1197,10 +1197,9 @@ __global__ void k_reset_layer(CtxView v, int layer, int32_t c) {
     const int64_t gs = lb * v.Hkv + h;
     for (int k = threadIdx.x; k < kHeadDim; k += blockDim.x) v.segsum[gs * kHeadDim + k] = 0;
     if (threadIdx.x == 0) {
-      for (int p = 0; p < kRing; ++p) {  // every plan slot starts empty
+      for (int p = 0; p < v.plan_ring; ++p) {  // every plan slot starts empty
         *plan_nsel(v, p, gs) = 0;
         *plan_ntok(v, p, gs) = 0;
-        plan_rng_cum(v, p, gs)[0] = 0;
       }
       for (int p = 0; p < kRing; ++p) v.attn_count[p * v.S_all + gs] = 0;
     }

@@ -14,8 +14,12 @@ constexpr int kHeadDim = 128;
 constexpr int kMaxGroup = 8;
 constexpr int kMaxParts = 64;      // token parts of the stable counting sort
 constexpr int kAttnChunk = 64;     // tokens per attention work item
-constexpr int kRing = 16;          // steps whose attention may be in flight at once
+constexpr int kRing = 32;          // plan slots and attention scratch slots (see Pipe)
+constexpr int kAttnStreams = 16;   // attention streams of a pipelined capture
+constexpr int kChunk = 64;         // decode steps whose boundary tests one launch runs
+constexpr int kSlots = 2 * kChunk; // step slots (queries, views): the steps of one captured graph
 constexpr int kAttnMaxSplit = 8;   // CTAs per slice in one attention launch, at most
+constexpr int kStreamMaxSlices = 1024;  // slices of one call the streaming attention takes
 
 // Error bits recorded on the device and reported by lkv_sync.
 enum : int32_t {
@@ -37,7 +41,7 @@ struct DecState {
   int32_t flag;        // this step retrieves
   float r;             // this step's r_t
   int32_t seg_slow;    // open segment holds a value outside the exact-sum range
-  int32_t plan;        // selection-plan slot (0..kRing-1) in force; a retrieval step advances it
+  int32_t plan;        // selection-plan slot (0..plan_ring-1) in force; a retrieval step advances it
 };
 
 // Everything a kernel needs to find the context's data. Per-slice arrays are
@@ -71,27 +75,28 @@ struct CtxView {
   int32_t *perm;              // [slice][n_cap]
   DecState *st;               // [lb]
   void *q_prev;               // [lb][H][d] (dtype)
-  float *q_attn;              // [kRing step slots][lb][H][d] queries * log2(e)/sqrt(d), fp32
-  int4 *aview;                // [step slot][lb] (t, win_start, plan slot, 2 * units + flag)
-  int4 *adesc;                // [step slot][slice] (t, win_start, plan slot, selected tokens),
+  float *q_attn;              // [kSlots step slots][lb][H][d] queries * log2(e)/sqrt(d), fp32
+  int4 *aview;                // [kSlots][lb] (t, win_start, plan slot, 2 * units + flag)
+  int4 *adesc;                // [kSlots][slice] (t, win_start, plan slot, selected tokens),
                               // written by the selection kernel on every step
   int64_t *segsum;            // [slice][d] exact fixed-point sums (bf16) or
                               // doubles reinterpreted (fp32)
-  float *scores;              // [slice][u_cap]
-  // the selection plan, one copy per plan slot: [kRing][slice]...
-  int32_t *sel;               // [kRing][slice][u_cap] selected unit ids, ascending
-  int32_t *n_sel;             // [kRing][slice]
-  int32_t *n_tok;             // [kRing][slice]
-  int32_t *rng_row;           // [kRing][slice][u_cap] first row of each selected unit
-  int32_t *sel_rows;          // [kRing][slice][sel_cap] pool row of each selected token (HBM pool only)
-  int32_t *rng_cum;           // [kRing][slice][u_cap + 1] exclusive token prefix
+  float *scores;              // chunk selection: [kSlots][slice][u_cap] per step slot, else [slice][u_cap]
+  // the selection plan, one copy per plan slot: [plan_ring][slice]...
+  int32_t plan_ring;          // plan slots: 2 * kChunk + 1 with chunk selection, else kRing
+  int32_t chunk_sel;          // one selection launch per chunk of steps (see launch_decode_steps)
+  int32_t *sel;               // [plan_ring][slice][u_cap] selected unit ids, ascending
+  int32_t *n_sel;             // [plan_ring][slice]
+  int32_t *n_tok;             // [plan_ring][slice]
+  int32_t *sel_rows;          // [plan_ring][slice][sel_cap] pool row of each selected token (HBM pool only)
   int4 *pieces;               // [slice][max_pieces] (src row, first token, length, 0)
   int32_t *chunk_piece;       // [slice][max_chunks + 1] first piece of each chunk
-  int4 *chunk_pieces;         // [kRing][slice][max_chunks][64] the pieces of each chunk
-  int32_t *chunk_count;       // [kRing][slice][max_chunks] pieces in each chunk
+  int4 *chunk_pieces;         // [plan_ring][slice][max_chunks][64] the pieces of each chunk
+  int32_t *chunk_count;       // [plan_ring][slice][max_chunks] pieces in each chunk
   int32_t max_pieces;
-  int32_t *attn_count;        // [kRing step slots][slice] attention CTAs / warps done (last one combines)
+  int32_t *attn_count;        // [kRing][slice] attention CTAs / warps done (last one combines), by step slot mod kRing
   float *attn_wpart;          // [kRing][w_cap][G * d + 2 * G] per-warp partials of the streaming attention
+  int32_t *sel_count;         // [kRing][slice] scoring CTAs done (the last one selects), by step slot mod kRing
   int32_t w_cap;              // warps the streaming attention may use in one launch
   float *attn_part;           // [kRing][slice][kAttnMaxSplit][G * d + 2 * G] CTA partials
   int32_t max_chunks;
@@ -99,7 +104,7 @@ struct CtxView {
   int64_t *counters;          // [kCounters] work counters (see CounterId)
 };
 
-// Plan-slot views of the selection plan (kRing slots).
+// Plan-slot views of the selection plan (plan_ring slots).
 __host__ __device__ __forceinline__ int32_t *plan_sel(const CtxView &v, int p, int64_t gs) {
   return v.sel + ((int64_t)p * v.S_all + gs) * v.u_cap;
 }
@@ -108,12 +113,6 @@ __host__ __device__ __forceinline__ int32_t *plan_nsel(const CtxView &v, int p, 
 }
 __host__ __device__ __forceinline__ int32_t *plan_ntok(const CtxView &v, int p, int64_t gs) {
   return v.n_tok + (int64_t)p * v.S_all + gs;
-}
-__host__ __device__ __forceinline__ int32_t *plan_rng_row(const CtxView &v, int p, int64_t gs) {
-  return v.rng_row + ((int64_t)p * v.S_all + gs) * v.u_cap;
-}
-__host__ __device__ __forceinline__ int32_t *plan_rng_cum(const CtxView &v, int p, int64_t gs) {
-  return v.rng_cum + ((int64_t)p * v.S_all + gs) * (v.u_cap + 1);
 }
 __host__ __device__ __forceinline__ int32_t *plan_sel_rows(const CtxView &v, int p, int64_t gs) {
   return v.sel_rows + ((int64_t)p * v.S_all + gs) * v.sel_cap;
@@ -294,36 +293,43 @@ struct StepArgs {
   uint8_t *boundary;               // [B][nl] or null
   float *r_out;                    // [B][nl] or null
   int32_t l0;                      // first layer of this call
-  int32_t slot;                    // step slot (queries, attention view): the step's
-                                   // index in a pipelined capture mod kRing, else 0
+  int32_t slot;                    // step slot (queries, views): the step's index in a
+                                   // captured graph (0 .. kSlots - 1), else 0; the
+                                   // attention's scratch is slot mod kRing
   int32_t nl;                      // layers in this call
 };
 
 // Streams and events of a pipelined multi-step capture, three lanes:
-//  - boundary kernels on the capture stream, one after the other (the decode
-//    state chain); step i's waits for step i - kRing's attention
-//    (attn_done[i % kRing]), the last reader of the step slot it rewrites;
-//  - scoring/selection (and the offload gather) on `sel`, each after its
-//    step's boundary kernel (b_done) and the previous selection. They read
-//    the step's view, never the live state, and a boundary kernel only
-//    writes units that the selections still running cannot reach;
-//  - step i's attention on attn[i % kRing], after its selection (sel_done).
-// A retrieval writes plan slot (retrievals so far) mod kRing; the attentions
-// that may still run then are those of the kRing - 1 previous steps, whose
-// plans are the kRing - 1 previous retrievals' at most, so none reads the
-// slot being written.
+//  - one boundary kernel per chunk of kChunk steps on the capture stream
+//    (the decode state chain), writing every step's slot (queries and view);
+//    the chunks of a graph use distinct slots;
+//  - scoring/selection (and the offload gather) on `sel`, the chunk's steps
+//    after its boundary kernel (b_done), each step after the previous one
+//    (programmatic dependent launch). Every kSelWaitStride-th step's
+//    selection i also waits for step i - kAttnStreams's attention: then at
+//    any selection j the attentions still running are within the
+//    kAttnStreams + kSelWaitStride - 1 steps before j (fewer than kRing), so
+//    a retrieval's plan slot ((retrievals so far) mod kRing) is read by no
+//    running attention, and step j's attention scratch (j mod kRing) is
+//    free. Selections read the step's view, never the live state, and a
+//    boundary kernel only writes units above the unit count a pending
+//    selection reads;
+//  - step i's attention on attn[i % kAttnStreams], after its selection (sel_done).
+constexpr int kSelWaitStride = 8;
+static_assert(kAttnStreams + kSelWaitStride - 1 < kRing, "plan ring too small for the attentions in flight");
 struct Pipe {
   cudaStream_t sel;
-  cudaStream_t attn[kRing];
+  cudaStream_t attn[kAttnStreams];
   cudaEvent_t b_done, sel_done;
-  cudaEvent_t attn_done[kRing];
-  int step;  // index of the step in the capture
+  cudaEvent_t attn_done[kAttnStreams];
+  int step;  // index of the chunk's first step in the capture
 };
 
-// One decode step; with `pipe` (graph capture only) the attention is forked
-// onto a side stream as described above.
-cudaError_t launch_decode_step(const CtxView &v, const StepArgs &a, cudaStream_t stream,
-                               Prof &prof, const Pipe *pipe = nullptr);
+// n_steps consecutive decode steps (step i in slot a.slot + i): one boundary
+// launch for all of them, then each step's scoring, selection and attention;
+// with `pipe` (graph capture only) the lanes are forked as described above.
+cudaError_t launch_decode_steps(const CtxView &v, const StepArgs &a, int n_steps, cudaStream_t stream,
+                                Prof &prof, const Pipe *pipe = nullptr);
 // Streaming read of `bytes` (a multiple of 16) of pinned host memory into
 // device memory by plain 16-byte loads over UVA (the host-link ceiling).
 cudaError_t launch_uva_read(const void *host_src, void *dev_dst, int64_t bytes, cudaStream_t stream);

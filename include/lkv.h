@@ -164,10 +164,12 @@ lkv_status lkv_decode_step(lkv_ctx *ctx, int32_t layer, int32_t n_layers,
  *   out [n_steps][B][n_layers][H][d], selected_units
  *   [n_steps][B][n_layers][H_kv][max_clusters + max_steps], n_selected
  *   [n_steps][B][n_layers][H_kv], boundary and r_out [n_steps][B][n_layers].
- * The steps run from a captured CUDA graph of 64 steps (cached per argument
- * set), so the host issues one launch per 64 steps. Inside the graph the
- * attention of a step runs concurrently with the boundary tests and
- * selections of up to fifteen following steps (they never read what it writes);
+ * The steps run from a captured CUDA graph of 128 steps (cached per argument
+ * set), so the host issues one launch per 128 steps; the steps left over run
+ * one at a time. Inside the graph one kernel runs the boundary tests and
+ * segment bookkeeping of 64 steps at a time (they depend on the inputs
+ * only), and the attention of a step runs concurrently with the selections
+ * of up to 22 following steps (they never read what it writes);
  * the boundary flags, r_t and selections are those of lkv_decode_step, and
  * the attention outputs agree with it within fp32 rounding (the grid over
  * which a slice's partial softmax sums are split can differ). With profiling

@@ -84,18 +84,34 @@ def test_load_index_rejects_out_of_range_assignment():
     ctx.close()
 
 
-@pytest.mark.parametrize("fail_at", [0, 5, 20, 38])
-def test_injected_allocation_failure(fail_at, monkeypatch):
-    """lkv_create makes 39 allocations (device and pinned host); failing the
-    first, a middle one or the last returns LKV_ENOMEM and frees the rest."""
+def _create_fails(w, fail_at, monkeypatch):
+    monkeypatch.setenv("LKV_FAIL_ALLOC_AFTER", str(fail_at))
+    try:
+        ctx = H.make_ctx(w)
+    except _lib.LKVError as e:
+        assert e.status == _lib.LKV_ENOMEM and "injected" in str(e)
+        return True
+    finally:
+        monkeypatch.delenv("LKV_FAIL_ALLOC_AFTER")
+    ctx.close()
+    return False
+
+
+def test_injected_allocation_failure(monkeypatch):
+    """Failing the first, some middle and the last of lkv_create's
+    allocations (device and pinned host) returns LKV_ENOMEM and frees the
+    rest; past the last one the injection has nothing to fail."""
     w = _small()
     torch.cuda.synchronize()
     free0 = torch.cuda.mem_get_info()[0]
-    monkeypatch.setenv("LKV_FAIL_ALLOC_AFTER", str(fail_at))
-    with pytest.raises(_lib.LKVError) as e:
-        H.make_ctx(w)
-    assert e.value.status == _lib.LKV_ENOMEM and "injected" in str(e.value)
-    monkeypatch.delenv("LKV_FAIL_ALLOC_AFTER")
+    for k in (0, 5, 20):
+        assert _create_fails(w, k, monkeypatch)
+    n = 21
+    while _create_fails(w, n, monkeypatch):
+        n += 1
+        assert n < 200
+    assert n > 25  # the context's arrays (pool, index, plans, scratch) are many
+    assert _create_fails(w, n - 1, monkeypatch)
     torch.cuda.synchronize()
     assert abs(torch.cuda.mem_get_info()[0] - free0) < (64 << 20), "allocations leaked"
     ctx = H.make_ctx(w)  # a normal create still works

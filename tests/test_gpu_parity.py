@@ -226,7 +226,7 @@ def test_decode_steps_graph_matches_single_steps():
     w = synth.WORKLOADS["long_out"].replace(batch=2, n_kv_heads=2, n_prefill=600, n_components=20,
                                             n_clusters=20, iters=3, local_buf=16, budget=120,
                                             jump_p=0.1)
-    T = 150
+    T = 300
     K, V = synth.prefill(w, 0, "cuda")
     q, kn, vn, _ = synth.decode_inputs(w, "cuda", n_steps=T)
     outs = []
@@ -243,7 +243,7 @@ def test_decode_steps_graph_matches_single_steps():
                 ctx.decode_step(0, q[t], kn[t], vn[t], 0.9, w.budget, out[t], boundary=bnd[t],
                                 n_selected=nsel[t], selected_units=sel[t])
         else:
-            for c0, c1 in ((0, 70), (70, 140), (140, 150)):
+            for c0, c1 in ((0, 140), (140, 280), (280, 300)):
                 ctx.decode_steps(0, q[c0:c1], kn[c0:c1], vn[c0:c1], 0.9, w.budget, out[c0:c1],
                                  boundary=bnd[c0:c1], n_selected=nsel[c0:c1],
                                  selected_units=sel[c0:c1])
@@ -265,7 +265,7 @@ def test_graph_with_every_step_retrieving():
     w = synth.WORKLOADS["long_out"].replace(batch=2, n_kv_heads=2, n_prefill=900, n_components=30,
                                             n_clusters=30, iters=3, local_buf=24, budget=160,
                                             jump_p=0.05)
-    T = 150
+    T = 300
     K, V = synth.prefill(w, 0, "cuda")
     q, kn, vn, _ = synth.decode_inputs(w, "cuda", n_steps=T)
     ctx = H.make_ctx(w, max_steps=T)
