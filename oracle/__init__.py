@@ -54,7 +54,13 @@ class DecodeArgs(C.Structure):
         ("keys", C.c_void_p), ("values", C.c_void_p), ("assign", C.c_void_p),
         ("cent", C.c_void_p), ("q", C.c_void_p), ("k_new", C.c_void_p),
         ("v_new", C.c_void_p), ("attn_mask", C.c_void_p),
+        ("trigger", C.c_int32), ("interval", C.c_int32), ("fill", C.c_int32),
+        ("page", C.c_int32), ("per_head", C.c_int32),
     ]
+
+
+TRIGGER_ADAPTIVE, TRIGGER_EVERY, TRIGGER_INTERVAL = 0, 1, 2
+FILL_PREFIX, FILL_SKIP = 0, 1
 
 
 class DecodeResult(C.Structure):
@@ -95,6 +101,8 @@ def lib():
             L.lkvo_group_scores.argtypes = [vp, C.c_int, i32, i32, vp, i32, vp]
             L.lkvo_select.argtypes = [vp, vp, i32, i32, vp, vp]
             L.lkvo_select.restype = i32
+            L.lkvo_select_skip.argtypes = [vp, vp, i32, i32, vp, vp]
+            L.lkvo_select_skip.restype = i32
             L.lkvo_attention.argtypes = [vp, C.c_int, i32, i32, vp, vp, i64, vp]
             L.lkvo_decode.argtypes = [C.POINTER(DecodeArgs), C.POINTER(DecodeResult)]
             L.lkvo_decode.restype = C.c_int
@@ -231,13 +239,30 @@ def group_scores(q_group: np.ndarray, cent_op: np.ndarray) -> np.ndarray:
     return s
 
 
-def select(scores: np.ndarray, lens: np.ndarray, budget: int):
+def select(scores: np.ndarray, lens: np.ndarray, budget: int, fill: int = FILL_PREFIX):
+    """(ids in selection order, tokens): lkvo_select, or lkvo_select_skip with
+    fill=FILL_SKIP."""
     s = _arr(scores, np.float32)
     ln = _arr(lens, np.int32)
     sel = np.zeros(max(1, s.size), np.int32)
     ntok = C.c_int32(0)
-    k = lib().lkvo_select(_p(s), _p(ln), s.size, budget, _p(sel), C.addressof(ntok))
+    f = lib().lkvo_select_skip if fill == FILL_SKIP else lib().lkvo_select
+    k = f(_p(s), _p(ln), s.size, budget, _p(sel), C.addressof(ntok))
     return sel[:k].copy(), ntok.value
+
+
+def page_index(keys: np.ndarray, page: int):
+    """Page-mean units of one slice [CTkvr, 1.1 (block-level indexes mean-pool
+    runs of consecutive tokens)]: unit j holds tokens [j*page, (j+1)*page)
+    (the last page may be short); its index vector is the mean of its keys,
+    by the same update as a Lloyd round. Returns (assign [n], cent [c, d])."""
+    keys = np.ascontiguousarray(keys)
+    n, d = keys.shape
+    c = -(-n // page)
+    a = (np.arange(n) // page).astype(np.int32)
+    cent, cnt, _ = update(keys, a, np.zeros((c, d), np.float32))
+    assert (cnt > 0).all()
+    return a, cent
 
 
 def attention(q_group: np.ndarray, k_rows: np.ndarray, v_rows: np.ndarray) -> np.ndarray:
@@ -250,7 +275,8 @@ def attention(q_group: np.ndarray, k_rows: np.ndarray, v_rows: np.ndarray) -> np
 
 
 def decode(keys, values, assign_, cent, q, k_new, v_new, *, n_clusters, local_buf,
-           tau, budget, attn_mask=None, want_seg_cent=False, want_sel=True, max_sel=None):
+           tau, budget, attn_mask=None, want_seg_cent=False, want_sel=True, max_sel=None,
+           trigger=TRIGGER_ADAPTIVE, interval=1, fill=FILL_PREFIX, page=0, per_head=False):
     """Run one (sequence, layer) decode through the oracle.
 
     keys/values [H_kv, N, d]; assign_ [H_kv, N]; cent [H_kv, C, d] fp32;
@@ -259,7 +285,9 @@ def decode(keys, values, assign_, cent, q, k_new, v_new, *, n_clusters, local_bu
     still recorded); with lists, each holds at most budget + C ids (a unit
     that fits adds at least one token, except empty clusters). max_sel caps
     the recorded list length for long runs (the call fails if a selection is
-    longer).
+    longer). trigger/interval/fill/page/per_head pick the retrieval policy
+    (see lkvo_decode_args); with per_head the selection records are per
+    query head ([T, H]) instead of per KV head.
     """
     keys, values = np.ascontiguousarray(keys), np.ascontiguousarray(values)
     q, k_new, v_new = (np.ascontiguousarray(x) for x in (q, k_new, v_new))
@@ -274,12 +302,14 @@ def decode(keys, values, assign_, cent, q, k_new, v_new, *, n_clusters, local_bu
     max_sel = min(ucap, budget + c) if max_sel is None else min(ucap, budget + c, max_sel)
     mask = None if attn_mask is None else _arr(attn_mask, np.uint8)
     args = DecodeArgs(dt, hkv, g, d, n, c, local_buf, T, tau, budget, _p(keys), _p(values),
-                      _p(assign_), _p(cent), _p(q), _p(k_new), _p(v_new), _p(mask))
+                      _p(assign_), _p(cent), _p(q), _p(k_new), _p(v_new), _p(mask),
+                      trigger, interval, fill, page, 1 if per_head else 0)
+    hs = h_all if per_head else hkv
     res = dict(
         out=np.zeros((T, h_all, d), np.float64), flag=np.zeros(T, np.uint8),
         r32=np.zeros(T, np.float32), r64=np.zeros(T, np.float64),
-        n_sel=np.zeros((T, hkv), np.int32), n_tok=np.zeros((T, hkv), np.int32),
-        sel=np.full((T, hkv, max_sel), -1, np.int32) if want_sel else None,
+        n_sel=np.zeros((T, hs), np.int32), n_tok=np.zeros((T, hs), np.int32),
+        sel=np.full((T, hs, max_sel), -1, np.int32) if want_sel else None,
         win_start=np.zeros(T, np.int32),
         n_units=np.zeros(T, np.int32), seg_start=np.zeros(max(T, 1), np.int32),
         seg_len=np.zeros(max(T, 1), np.int32),

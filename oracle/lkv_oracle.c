@@ -289,6 +289,29 @@ int32_t lkvo_select(const float *scores, const int32_t *len, int32_t u,
   return n_sel;
 }
 
+int32_t lkvo_select_skip(const float *scores, const int32_t *len, int32_t u,
+                         int32_t budget, int32_t *sel_out, int32_t *n_tok_out) {
+  int32_t *order = (int32_t *)malloc((size_t)(u > 0 ? u : 1) * sizeof *order);
+  for (int32_t i = 0; i < u; ++i) {
+    int32_t x = i, p = i;
+    while (p > 0 && precedes(scores, x, order[p - 1])) {
+      order[p] = order[p - 1];
+      --p;
+    }
+    order[p] = x;
+  }
+  int32_t n_sel = 0, tok = 0;
+  for (int32_t i = 0; i < u; ++i) {
+    int32_t id = order[i];
+    if (tok + len[id] > budget) continue; /* does not fit: skip it */
+    tok += len[id];
+    sel_out[n_sel++] = id;
+  }
+  free(order);
+  *n_tok_out = tok;
+  return n_sel;
+}
+
 /* ------------------------------------------------------------------------ */
 /* attention over the retrieved + local tokens [LouisKV notes, flowchart:     */
 /* Attention over retrieved or reused critical KV]                           */
@@ -335,6 +358,11 @@ int lkvo_decode(const lkvo_decode_args *a, lkvo_decode_result *r) {
   const size_t es = elem_size(dt);
   if (hkv < 1 || g < 1 || d < 1 || c < 1 || L < 1 || T < 0 || n < 0) return -1;
   const int32_t ucap = c + T; /* every eviction removes at least one token */
+  if (a->trigger < 0 || a->trigger > 2 || (a->trigger == 2 && a->interval < 1) ||
+      a->fill < 0 || a->fill > 1 || a->page < 0 || a->per_head < 0 || a->per_head > 1)
+    return -1;
+  /* selections: one per KV head, or one per query head */
+  const int32_t hs = a->per_head ? h_all : hkv, gs = a->per_head ? 1 : g;
 
   int rc = -1;
   /* cluster membership in token order, per kv head */
@@ -345,9 +373,9 @@ int lkvo_decode(const lkvo_decode_args *a, lkvo_decode_result *r) {
   float *op = (float *)malloc((size_t)hkv * ucap * d * sizeof *op);
   int32_t *ulen = (int32_t *)malloc((size_t)hkv * ucap * sizeof *ulen);
   /* active selection per kv head */
-  int32_t *act = (int32_t *)malloc((size_t)hkv * ucap * sizeof *act);
-  int32_t *act_n = (int32_t *)calloc((size_t)hkv, sizeof *act_n);
-  int32_t *act_tok = (int32_t *)calloc((size_t)hkv, sizeof *act_tok);
+  int32_t *act = (int32_t *)malloc((size_t)hs * ucap * sizeof *act);
+  int32_t *act_n = (int32_t *)calloc((size_t)hs, sizeof *act_n);
+  int32_t *act_tok = (int32_t *)calloc((size_t)hs, sizeof *act_tok);
   /* closed, not yet evicted segments: FIFO of [start, end) */
   int32_t *cl_s = (int32_t *)malloc((size_t)(T + 1) * sizeof *cl_s);
   int32_t *cl_e = (int32_t *)malloc((size_t)(T + 1) * sizeof *cl_e);
@@ -387,7 +415,7 @@ int lkvo_decode(const lkvo_decode_args *a, lkvo_decode_result *r) {
 
   for (int32_t t = 0; t < T; ++t) {
     const void *qt = row_ptr(a->q, dt, (int64_t)t * h_all, d);
-    /* 1. boundary test */
+    /* 1. boundary test (r_t is computed and recorded under every policy) */
     int flag = 1;
     float r32 = 0.0f;
     double r64 = 0.0;
@@ -395,10 +423,13 @@ int lkvo_decode(const lkvo_decode_args *a, lkvo_decode_result *r) {
       const void *qp = row_ptr(a->q, dt, (int64_t)(t - 1) * h_all, d);
       r32 = lkvo_boundary_r32(qp, qt, dt, h_all, d);
       r64 = lkvo_boundary_r64(qp, qt, dt, h_all, d);
-      flag = r32 < a->tau;
+      if (a->trigger == LKVO_TRIGGER_ADAPTIVE) flag = r32 < a->tau;
+      else if (a->trigger == LKVO_TRIGGER_INTERVAL) flag = t % a->interval == 0;
     }
-    /* 2. a boundary closes the open segment; token t starts the next one */
-    if (flag && t > 0 && open_start < t) {
+    /* 2. a boundary (or, with pages, a full page) closes the open segment;
+     *    token t starts the next one */
+    const int cut = a->page > 0 ? (t - open_start >= a->page) : flag;
+    if (cut && t > 0 && open_start < t) {
       cl_s[cl_tail] = open_start;
       cl_e[cl_tail] = t;
       ++cl_tail;
@@ -443,19 +474,27 @@ int lkvo_decode(const lkvo_decode_args *a, lkvo_decode_result *r) {
     /* 4. token t enters the local buffer [win_start, t] */
     /* 5. retrieval on a boundary step, against the pool after evictions */
     if (flag) {
-      for (int32_t kh = 0; kh < hkv; ++kh) {
-        const void *qg = row_ptr(a->q, dt, (int64_t)t * h_all + (int64_t)kh * g, d);
-        lkvo_group_scores(qg, dt, g, d, op + (size_t)kh * ucap * d, n_units, scores);
-        act_n[kh] = lkvo_select(scores, ulen + (size_t)kh * ucap, n_units,
-                                a->budget, act + (size_t)kh * ucap, &act_tok[kh]);
+      /* selection j scores with the sum of query heads j*gs .. j*gs+gs-1
+       * (its group, or the one head) against its KV head's units */
+      for (int32_t j = 0; j < hs; ++j) {
+        const int32_t kh = j * gs / g;
+        const void *qg = row_ptr(a->q, dt, (int64_t)t * h_all + (int64_t)j * gs, d);
+        lkvo_group_scores(qg, dt, gs, d, op + (size_t)kh * ucap * d, n_units, scores);
+        if (a->fill == LKVO_FILL_SKIP)
+          act_n[j] = lkvo_select_skip(scores, ulen + (size_t)kh * ucap, n_units,
+                                      a->budget, act + (size_t)j * ucap, &act_tok[j]);
+        else
+          act_n[j] = lkvo_select(scores, ulen + (size_t)kh * ucap, n_units,
+                                 a->budget, act + (size_t)j * ucap, &act_tok[j]);
       }
     }
-    /* 6. attention of each query head over its group's selection + buffer */
+    /* 6. attention of each query head over its selection + buffer */
     if (!a->attn_mask || a->attn_mask[t]) {
-      for (int32_t kh = 0; kh < hkv; ++kh) {
+      for (int32_t j = 0; j < hs; ++j) {
+        const int32_t kh = j * gs / g;
         int64_t m = 0;
-        for (int32_t s = 0; s < act_n[kh]; ++s) {
-          int32_t u = act[(size_t)kh * ucap + s];
+        for (int32_t s = 0; s < act_n[j]; ++s) {
+          int32_t u = act[(size_t)j * ucap + s];
           if (u < c) {
             const int32_t *fs = first + (size_t)kh * (c + 1);
             for (int32_t p = fs[u]; p < fs[u + 1]; ++p) {
@@ -478,9 +517,9 @@ int lkvo_decode(const lkvo_decode_args *a, lkvo_decode_result *r) {
           memcpy(vg + m * d * es, row_ptr(a->v_new, dt, (int64_t)tt * hkv + kh, d), d * es);
           ++m;
         }
-        const void *qg = row_ptr(a->q, dt, (int64_t)t * h_all + (int64_t)kh * g, d);
-        lkvo_attention(qg, dt, g, d, kg, vg, m,
-                       r->out + ((size_t)t * h_all + (size_t)kh * g) * d);
+        const void *qg = row_ptr(a->q, dt, (int64_t)t * h_all + (int64_t)j * gs, d);
+        lkvo_attention(qg, dt, gs, d, kg, vg, m,
+                       r->out + ((size_t)t * h_all + (size_t)j * gs) * d);
       }
     }
     /* per-step record */
@@ -489,13 +528,13 @@ int lkvo_decode(const lkvo_decode_args *a, lkvo_decode_result *r) {
     if (r->r64) r->r64[t] = r64;
     if (r->win_start) r->win_start[t] = win_start;
     if (r->n_units) r->n_units[t] = n_units;
-    for (int32_t kh = 0; kh < hkv; ++kh) {
-      if (r->n_sel) r->n_sel[(size_t)t * hkv + kh] = act_n[kh];
-      if (r->n_tok) r->n_tok[(size_t)t * hkv + kh] = act_tok[kh];
+    for (int32_t j = 0; j < hs; ++j) {
+      if (r->n_sel) r->n_sel[(size_t)t * hs + j] = act_n[j];
+      if (r->n_tok) r->n_tok[(size_t)t * hs + j] = act_tok[j];
       if (r->sel) {
-        if (act_n[kh] > r->max_sel) goto done;
-        memcpy(r->sel + ((size_t)t * hkv + kh) * r->max_sel, act + (size_t)kh * ucap,
-               (size_t)act_n[kh] * sizeof(int32_t));
+        if (act_n[j] > r->max_sel) goto done;
+        memcpy(r->sel + ((size_t)t * hs + j) * r->max_sel, act + (size_t)j * ucap,
+               (size_t)act_n[j] * sizeof(int32_t));
       }
     }
   }

@@ -118,6 +118,13 @@ void lkvo_group_scores(const void *q, int dtype, int32_t g, int32_t d,
 int32_t lkvo_select(const float *scores, const int32_t *len, int32_t u,
                     int32_t budget, int32_t *sel_out, int32_t *n_tok_out);
 
+/* Skip-and-continue budget fill (a selection variant; the pages fix only the
+ * stop-at-first-misfit rule above): walk the same (score descending, id
+ * ascending) order and add every unit whose length still fits in what is left
+ * of the budget, skipping the ones that do not. Same outputs as lkvo_select. */
+int32_t lkvo_select_skip(const float *scores, const int32_t *len, int32_t u,
+                         int32_t budget, int32_t *sel_out, int32_t *n_tok_out);
+
 /* Softmax attention of g query heads over n rows, in double precision:
  * out_h = sum_i softmax_i(q_h . k_i / sqrt(d)) v_i. k_rows, v_rows: [n][d]. */
 void lkvo_attention(const void *q, int dtype, int32_t g, int32_t d,
@@ -145,7 +152,26 @@ typedef struct {
   const void *k_new;    /* [T][H_kv][d] */
   const void *v_new;    /* [T][H_kv][d] */
   const uint8_t *attn_mask; /* [T] compute attention only where nonzero; NULL = all */
+  /* Retrieval policy; all zero is the method itself. The variants are the
+   * baselines the pages compare it with [LouisKV notes, 研究背景与动机 (a
+   * retrieval at every decode token, page-granular units) and 消融实验
+   * (adaptive vs fixed step, fine-grained vs page units, group-consistent
+   * selection)]. */
+  int32_t trigger;      /* LKVO_TRIGGER_ADAPTIVE: t = 0 or r_t < tau;
+                           LKVO_TRIGGER_EVERY: every step;
+                           LKVO_TRIGGER_INTERVAL: t % interval == 0 */
+  int32_t interval;     /* >= 1 with LKVO_TRIGGER_INTERVAL */
+  int32_t fill;         /* LKVO_FILL_PREFIX (lkvo_select) or LKVO_FILL_SKIP (lkvo_select_skip) */
+  int32_t page;         /* 0: the open decode segment closes at a retrieval step;
+                           P >= 1: it closes once it holds P tokens (page units),
+                           whatever the step does */
+  int32_t per_head;     /* 0: one selection per KV head from the group's summed
+                           query; 1: one per query head from its own query, and
+                           each head attends its own selection */
 } lkvo_decode_args;
+
+enum { LKVO_TRIGGER_ADAPTIVE = 0, LKVO_TRIGGER_EVERY = 1, LKVO_TRIGGER_INTERVAL = 2 };
+enum { LKVO_FILL_PREFIX = 0, LKVO_FILL_SKIP = 1 };
 
 typedef struct {
   int32_t max_sel;      /* capacity of sel per (step, kv head) */
@@ -154,9 +180,10 @@ typedef struct {
   uint8_t *flag;        /* [T] 1 = retrieval step */
   float *r32;           /* [T] decision value (0 at t = 0) */
   double *r64;          /* [T] double-precision r_t (0 at t = 0) */
-  int32_t *n_sel;       /* [T][H_kv] units in the active selection */
-  int32_t *n_tok;       /* [T][H_kv] tokens in the active selection */
-  int32_t *sel;         /* [T][H_kv][max_sel] active selection, selection order */
+  /* selection records: one per KV head, or per query head with per_head (Hs = H) */
+  int32_t *n_sel;       /* [T][Hs] units in the active selection */
+  int32_t *n_tok;       /* [T][Hs] tokens in the active selection */
+  int32_t *sel;         /* [T][Hs][max_sel] active selection, selection order */
   int32_t *win_start;   /* [T] first decode token in the local buffer after the step */
   int32_t *n_units;     /* [T] units in the pool after the step's evictions */
   int32_t *seg_start;   /* [max_segs] first decode token of evicted segment e */

@@ -444,3 +444,134 @@ def test_decode_selection_is_group_scored_budget_prefix():
         ln = np.bincount(assign[kh], minlength=c).astype(np.int32)
         k = res["n_sel"][step, kh]
         _selection_properties(s, ln, budget, res["sel"][step, kh, :k], res["n_tok"][step, kh])
+
+
+# ------------------------------------------------------------------ policy variants
+
+def test_select_skip_is_lexicographic_max_feasible_subset():
+    """Skip-and-continue fill: among all subsets whose length fits the budget,
+    the one whose membership vector, read in (score desc, id asc) order, is
+    lexicographically largest (take the best unit whenever it still fits).
+    Brute force over every subset of <= 8 units."""
+    for trial in range(300):
+        u = int(rng.integers(1, 9))
+        s = rng.integers(-3, 4, u).astype(np.float32)
+        ln = rng.integers(0, 7, u).astype(np.int32)
+        budget = int(rng.integers(0, 20))
+        sel, ntok = oracle.select(s, ln, budget, oracle.FILL_SKIP)
+        order = sorted(range(u), key=lambda x: (-float(s[x]), x))
+        best = None
+        for bits in itertools.product((1, 0), repeat=u):   # lexicographically descending
+            if sum(int(ln[order[i]]) for i in range(u) if bits[i]) <= budget:
+                best = [order[i] for i in range(u) if bits[i]]
+                break
+        assert list(sel) == best
+        assert ntok == sum(int(ln[x]) for x in sel) <= budget
+        pre, _ = oracle.select(s, ln, budget)
+        assert list(sel[: len(pre)]) == list(pre)           # extends the stop-at-misfit prefix
+
+
+def test_select_skip_special_cases():
+    s = rng.standard_normal(40).astype(np.float32)
+    ones = np.ones(40, np.int32)
+    sel, ntok = oracle.select(s, ones, 13, oracle.FILL_SKIP)   # unit lengths: the 13 best
+    assert list(sel) == list(np.argsort(-s, kind="stable")[:13]) and ntok == 13
+    ln = rng.integers(1, 9, 40).astype(np.int32)
+    sel, ntok = oracle.select(s, ln, int(ln.sum()), oracle.FILL_SKIP)
+    assert sorted(sel.tolist()) == list(range(40)) and ntok == ln.sum()
+    big = ln.copy(); big[int(np.argmax(s))] = 10 ** 6           # best never fits: the rest still do
+    sel, ntok = oracle.select(s, big, int(ln.sum()), oracle.FILL_SKIP)
+    assert int(np.argmax(s)) not in sel.tolist() and len(sel) == 39
+
+
+def _dec(keys, values, assign, cent, q, kn, vn, c, L, **kw):
+    return oracle.decode(keys, values, assign, cent, q, kn, vn, n_clusters=c, local_buf=L, **kw)
+
+
+def test_decode_trigger_policies():
+    hkv, g, n, c, T, L = 2, 4, 300, 10, 90, 12
+    args = _decode_inputs("bf16", hkv, g, n=n, c=c, T=T, jump=0.1, seed=7)
+    every = _dec(*args, c, L, tau=-5.0, budget=60, trigger=oracle.TRIGGER_EVERY)
+    forced = _dec(*args, c, L, tau=1.5, budget=60)                 # r_t < 1.5 at every step
+    assert every["flag"].all()
+    for k in ("flag", "n_sel", "n_tok", "sel", "seg_start", "seg_len"):
+        assert np.array_equal(every[k], forced[k]), k
+    assert np.array_equal(every["out"], forced["out"])
+    assert np.array_equal(every["r32"], forced["r32"])             # r_t still recorded
+    for k_int in (1, 7, 16):
+        fx = _dec(*args, c, L, tau=0.0, budget=60, trigger=oracle.TRIGGER_INTERVAL, interval=k_int)
+        assert np.array_equal(np.nonzero(fx["flag"])[0], np.arange(0, T, k_int))
+        # segments close exactly at the retrieval steps (or are cut by a full buffer)
+        ends = (fx["seg_start"] + fx["seg_len"]).tolist()
+        assert all(e % k_int == 0 for e in ends) or fx["n_forced"] > 0
+    one = _dec(*args, c, L, tau=0.0, budget=60, trigger=oracle.TRIGGER_INTERVAL, interval=1)
+    assert np.array_equal(one["sel"], every["sel"]) and np.array_equal(one["out"], every["out"])
+
+
+def test_decode_page_segments():
+    hkv, g, n, c, T, L, P = 2, 4, 300, 10, 120, 32, 8
+    args = _decode_inputs("fp32", hkv, g, n=n, c=c, T=T, jump=0.2, seed=3)
+    res = _dec(*args, c, L, tau=0.9, budget=60, page=P, want_seg_cent=True)
+    assert res["n_forced"] == 0
+    ne = res["n_evicted"]
+    assert ne >= (T - L) // P
+    assert np.array_equal(res["seg_start"], np.arange(ne) * P)     # fixed pages from token 0
+    assert (res["seg_len"] == P).all()
+    KN = _f(args[5])
+    for e in range(ne):
+        for kh in range(hkv):
+            assert np.allclose(res["seg_cent"][e, kh], KN[e * P:(e + 1) * P, kh].mean(0), atol=1e-6)
+    # pages do not depend on the retrieval steps
+    other = _dec(*args, c, L, tau=-1.0, budget=60, page=P)
+    assert np.array_equal(other["seg_start"], res["seg_start"])
+
+
+def test_page_index_closed_forms():
+    keys = rng.standard_normal((50, 128)).astype(np.float32)
+    a, cent = oracle.page_index(keys, 1)
+    assert np.array_equal(a, np.arange(50)) and np.array_equal(cent, keys)
+    a, cent = oracle.page_index(keys, 50)
+    want = np.array([math.fsum(keys[:, j].astype(np.float64)) / 50 for j in range(128)])
+    assert np.array_equal(cent[0], want.astype(np.float32))
+    a, cent = oracle.page_index(keys, 16)                          # 16, 16, 16, 2
+    assert np.array_equal(np.bincount(a), [16, 16, 16, 2])
+    assert np.allclose(cent[3], keys[48:].astype(np.float64).mean(0), atol=1e-7)
+
+
+def test_decode_per_head_reduces_to_group_cases():
+    """Per-query-head selection with g = 1 is the group selection; with the g
+    heads of every group carrying the same query, the group sum scales every
+    score by g (a power of two: exact) and each head selects what the group
+    does."""
+    hkv, n, c, T, L = 2, 300, 10, 40, 8
+    a1 = _decode_inputs("bf16", hkv, 1, n=n, c=c, T=T, seed=5)
+    r_grp = _dec(*a1, c, L, tau=0.95, budget=70)
+    r_ph = _dec(*a1, c, L, tau=0.95, budget=70, per_head=True)
+    for k in ("flag", "n_sel", "n_tok", "sel", "out"):
+        assert np.array_equal(r_grp[k], r_ph[k]), k
+    g = 4
+    keys, values, assign, cent, q, kn, vn = _decode_inputs("bf16", hkv, g, n=n, c=c, T=T, seed=5)
+    q = np.repeat(q[:, ::g], g, axis=1)                            # heads of a group share the query
+    r_grp = _dec(keys, values, assign, cent, q, kn, vn, c, L, tau=0.95, budget=70)
+    r_ph = _dec(keys, values, assign, cent, q, kn, vn, c, L, tau=0.95, budget=70, per_head=True)
+    assert r_ph["n_sel"].shape == (T, hkv * g)
+    for h in range(hkv * g):
+        assert np.array_equal(r_ph["sel"][:, h], r_grp["sel"][:, h // g])
+        assert np.array_equal(r_ph["n_tok"][:, h], r_grp["n_tok"][:, h // g])
+    assert np.allclose(r_ph["out"], r_grp["out"], atol=1e-12)
+
+
+def test_decode_per_head_selection_uses_own_query():
+    hkv, g, n, c, T, L, budget = 2, 4, 300, 10, 20, 8, 70
+    keys, values, assign, cent, q, kn, vn = _decode_inputs("bf16", hkv, g, n=n, c=c, T=T, seed=9)
+    res = _dec(keys, values, assign, cent, q, kn, vn, c, L, tau=0.95, budget=budget, per_head=True)
+    for h in range(hkv * g):
+        kh = h // g
+        op = oracle.operand(cent[kh], oracle.BF16)
+        s = oracle.group_scores(q[0, h:h + 1], op)
+        ln = np.bincount(assign[kh], minlength=c).astype(np.int32)
+        k = res["n_sel"][0, h]
+        _selection_properties(s, ln, budget, res["sel"][0, h, :k], res["n_tok"][0, h])
+    # heads of one group disagree somewhere (otherwise the variant measures nothing)
+    assert any(res["n_tok"][0, h] != res["n_tok"][0, h + 1] or
+               not np.array_equal(res["sel"][0, h], res["sel"][0, h + 1]) for h in range(g - 1))
