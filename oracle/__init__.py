@@ -56,7 +56,12 @@ class DecodeArgs(C.Structure):
         ("v_new", C.c_void_p), ("attn_mask", C.c_void_p),
         ("trigger", C.c_int32), ("interval", C.c_int32), ("fill", C.c_int32),
         ("page", C.c_int32), ("per_head", C.c_int32),
+        ("selector", C.c_int32), ("paris_rho", C.c_int32), ("paris_n_cand", C.c_int32),
+        ("paris_seed", C.c_uint64),
     ]
+
+
+SELECT_CLUSTERS, SELECT_PARIS = 0, 1
 
 
 TRIGGER_ADAPTIVE, TRIGGER_EVERY, TRIGGER_INTERVAL = 0, 1, 2
@@ -103,6 +108,14 @@ def lib():
             L.lkvo_select.restype = i32
             L.lkvo_select_skip.argtypes = [vp, vp, i32, i32, vp, vp]
             L.lkvo_select_skip.restype = i32
+            L.lkvo_paris_signs.argtypes = [u64, i32, vp]
+            L.lkvo_paris_levels.argtypes = [i32, vp, vp]
+            L.lkvo_paris_levels.restype = C.c_int
+            L.lkvo_paris_encode.argtypes = [vp, i32, vp, i32, vp, vp, vp, vp, vp]
+            L.lkvo_paris_rotate_query.argtypes = [vp, C.c_int, i32, i32, vp, vp]
+            L.lkvo_paris_select.argtypes = [vp, i32, i32, i32, i64, i32, i64, vp, vp, vp, vp,
+                                            vp, vp, vp]
+            L.lkvo_paris_select.restype = i64
             L.lkvo_attention.argtypes = [vp, C.c_int, i32, i32, vp, vp, i64, vp]
             L.lkvo_decode.argtypes = [C.POINTER(DecodeArgs), C.POINTER(DecodeResult)]
             L.lkvo_decode.restype = C.c_int
@@ -265,6 +278,60 @@ def page_index(keys: np.ndarray, page: int):
     return a, cent
 
 
+def paris_signs(seed: int, d: int = 128) -> np.ndarray:
+    out = np.zeros(d, np.int8)
+    lib().lkvo_paris_signs(seed, d, _p(out))
+    return out
+
+
+def paris_levels(m: int = 8):
+    """(thresholds T_l = t_l^2, l = 1..7, and bin means, 8) as float32."""
+    thr = np.zeros(7, np.float32)
+    lev = np.zeros(8, np.float32)
+    if lib().lkvo_paris_levels(m, _p(thr), _p(lev)) != 0:
+        raise ValueError("m must be >= 2")
+    return thr, lev
+
+
+def paris_encode(keys: np.ndarray, seed: int, m: int = 8):
+    """Metadata of bf16 keys [n, d]: (buckets [n, d/m] u8, levels [n, d] u8,
+    scales [n, d/m] f32)."""
+    keys = _arr(keys, np.uint16)
+    n, d = keys.shape
+    sign = paris_signs(seed, d)
+    thr, lev = paris_levels(m)
+    bk = np.zeros((n, d // m), np.uint8)
+    lv = np.zeros((n, d), np.uint8)
+    w = np.zeros((n, d // m), np.float32)
+    L = lib()
+    for i in range(n):
+        L.lkvo_paris_encode(_p(keys[i]), d, _p(sign), m, _p(thr), _p(lev), _p(bk[i]), _p(lv[i]),
+                            _p(w[i]))
+    return bk, lv, w
+
+
+def paris_rotate_query(q_group: np.ndarray, seed: int) -> np.ndarray:
+    q = np.ascontiguousarray(q_group)
+    g, d = q.shape
+    out = np.zeros(d, np.float32)
+    lib().lkvo_paris_rotate_query(_p(q), dtype_of(q), g, d, _p(paris_signs(seed, d)), _p(out))
+    return out
+
+
+def paris_select(qrot, bucket, level, w, *, rho, n_cand, budget, m=8):
+    """(selected ids best first, coarse scores [n], estimates [n])."""
+    qrot = _arr(qrot, np.float32)
+    bucket, level, w = _arr(bucket, np.uint8), _arr(level, np.uint8), _arr(w, np.float32)
+    n, d = level.shape
+    _, lev = paris_levels(m)
+    sel = np.zeros(max(1, min(budget, n)), np.int64)
+    coarse = np.zeros(max(1, n), np.int32)
+    est = np.zeros(max(1, n), np.float32)
+    k = lib().lkvo_paris_select(_p(qrot), d, m, rho, n_cand, budget, n, _p(bucket), _p(level),
+                                _p(w), _p(lev), _p(sel), _p(coarse), _p(est))
+    return sel[:k].copy(), coarse[:n], est[:n]
+
+
 def attention(q_group: np.ndarray, k_rows: np.ndarray, v_rows: np.ndarray) -> np.ndarray:
     q = np.ascontiguousarray(q_group)
     k, v = np.ascontiguousarray(k_rows), np.ascontiguousarray(v_rows)
@@ -276,7 +343,8 @@ def attention(q_group: np.ndarray, k_rows: np.ndarray, v_rows: np.ndarray) -> np
 
 def decode(keys, values, assign_, cent, q, k_new, v_new, *, n_clusters, local_buf,
            tau, budget, attn_mask=None, want_seg_cent=False, want_sel=True, max_sel=None,
-           trigger=TRIGGER_ADAPTIVE, interval=1, fill=FILL_PREFIX, page=0, per_head=False):
+           trigger=TRIGGER_ADAPTIVE, interval=1, fill=FILL_PREFIX, page=0, per_head=False,
+           paris=None):
     """Run one (sequence, layer) decode through the oracle.
 
     keys/values [H_kv, N, d]; assign_ [H_kv, N]; cent [H_kv, C, d] fp32;
@@ -287,23 +355,35 @@ def decode(keys, values, assign_, cent, q, k_new, v_new, *, n_clusters, local_bu
     the recorded list length for long runs (the call fails if a selection is
     longer). trigger/interval/fill/page/per_head pick the retrieval policy
     (see lkvo_decode_args); with per_head the selection records are per
-    query head ([T, H]) instead of per KV head.
+    query head ([T, H]) instead of per KV head. paris=dict(rho, n_cand, seed)
+    selects tokens with the ParisKV-style pipeline instead (n_clusters 0;
+    assign_ and cent unused; the records hold token ids, prefill i and decode
+    t as N + t, best first).
     """
     keys, values = np.ascontiguousarray(keys), np.ascontiguousarray(values)
     q, k_new, v_new = (np.ascontiguousarray(x) for x in (q, k_new, v_new))
+    hkv, n, d = keys.shape
+    if paris is not None:
+        assign_ = np.zeros((hkv, max(1, n)), np.int32)
+        cent = np.zeros((hkv, 1, d), np.float32)
+        n_clusters = 0
     assign_ = _arr(assign_, np.int32)
     cent = _arr(cent, np.float32)
-    hkv, n, d = keys.shape
     T, h_all, _ = q.shape
     g = h_all // hkv
     dt = dtype_of(q)
     c = n_clusters
     ucap = c + T
     max_sel = min(ucap, budget + c) if max_sel is None else min(ucap, budget + c, max_sel)
+    if paris is not None:
+        max_sel = max(1, budget)
     mask = None if attn_mask is None else _arr(attn_mask, np.uint8)
+    pr = paris or {}
     args = DecodeArgs(dt, hkv, g, d, n, c, local_buf, T, tau, budget, _p(keys), _p(values),
                       _p(assign_), _p(cent), _p(q), _p(k_new), _p(v_new), _p(mask),
-                      trigger, interval, fill, page, 1 if per_head else 0)
+                      trigger, interval, fill, page, 1 if per_head else 0,
+                      SELECT_PARIS if paris is not None else SELECT_CLUSTERS,
+                      pr.get("rho", 0), pr.get("n_cand", 0), pr.get("seed", 0))
     hs = h_all if per_head else hkv
     res = dict(
         out=np.zeros((T, h_all, d), np.float64), flag=np.zeros(T, np.uint8),

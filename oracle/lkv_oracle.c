@@ -347,6 +347,199 @@ void lkvo_attention(const void *q, int dtype, int32_t g, int32_t d,
 }
 
 /* ------------------------------------------------------------------------ */
+/* ParisKV-style selector [ParisKV technical summary, 核心算法创新 1-2]        */
+
+void lkvo_paris_signs(uint64_t seed, int32_t d, int8_t *sign_out) {
+  uint64_t st = seed, word = 0;
+  for (int32_t j = 0; j < d; ++j) {
+    if (j % 64 == 0) word = splitmix64_next(&st);
+    sign_out[j] = (int8_t)(((word >> (j % 64)) & 1u) ? -1 : 1);
+  }
+}
+
+/* density of |x| up to its constant, and its integral by composite Simpson */
+static double sphere_marginal(double x, int32_t m) { return pow(1.0 - x * x, 0.5 * (m - 3)); }
+
+static double simpson(double a, double b, int32_t m, int moment) {
+  const int n = 20000; /* even */
+  const double h = (b - a) / n;
+  double acc = 0.0;
+  for (int i = 0; i <= n; ++i) {
+    const double x = a + h * i;
+    double f = sphere_marginal(x, m) * (moment ? x : 1.0);
+    acc += f * (i == 0 || i == n ? 1.0 : (i % 2 ? 4.0 : 2.0));
+  }
+  return acc * h / 3.0;
+}
+
+int lkvo_paris_levels(int32_t m, float *thr_out, float *lev_out) {
+  if (m < 2) return -1;
+  const double total = simpson(0.0, 1.0, m, 0);
+  double t[9];
+  t[0] = 0.0;
+  t[8] = 1.0;
+  for (int l = 1; l < 8; ++l) {
+    double lo = 0.0, hi = 1.0; /* P(|x| < t) = l / 8 by bisection */
+    for (int it = 0; it < 60; ++it) {
+      const double mid = 0.5 * (lo + hi);
+      if (simpson(0.0, mid, m, 0) / total < l / 8.0) lo = mid;
+      else hi = mid;
+    }
+    t[l] = 0.5 * (lo + hi);
+    thr_out[l - 1] = (float)(t[l] * t[l]);
+  }
+  for (int l = 0; l < 8; ++l)
+    lev_out[l] = (float)(simpson(t[l], t[l + 1], m, 1) / simpson(t[l], t[l + 1], m, 0));
+  return 0;
+}
+
+static int hadamard_sign(int32_t i, int32_t j) {
+  unsigned x = (unsigned)(i & j), par = 0;
+  while (x) { par ^= x & 1u; x >>= 1; }
+  return par ? -1 : 1;
+}
+
+void lkvo_paris_encode(const uint16_t *key, int32_t d, const int8_t *sign, int32_t m,
+                       const float *thr, const float *lev, uint8_t *bucket_out,
+                       uint8_t *level_out, float *w_out) {
+  int64_t *k40 = (int64_t *)malloc((size_t)d * sizeof *k40);
+  int64_t *y = (int64_t *)malloc((size_t)d * sizeof *y);
+  for (int32_t j = 0; j < d; ++j) k40[j] = (int64_t)((double)lkvo_bf16_to_f32(key[j]) * 0x1p40);
+  for (int32_t i = 0; i < d; ++i) {
+    int64_t acc = 0;
+    for (int32_t j = 0; j < d; ++j) acc += (int64_t)(hadamard_sign(i, j) * sign[j]) * k40[j];
+    y[i] = acc;
+  }
+  for (int32_t b = 0; b < d / m; ++b) {
+    const int64_t *yb = y + (size_t)b * m;
+    unsigned bits = 0;
+    double n2 = 0.0;
+    for (int32_t j = 0; j < m; ++j) {
+      if (yb[j] < 0) bits |= 1u << j;
+      n2 = n2 + (double)yb[j] * (double)yb[j];
+    }
+    bucket_out[b] = (uint8_t)bits;
+    double num = 0.0, den = 0.0;
+    for (int32_t j = 0; j < m; ++j) {
+      const double sq = (double)yb[j] * (double)yb[j];
+      int l = 0;
+      for (int k = 0; k < 7; ++k)
+        if (sq >= (double)thr[k] * n2) l = k + 1;
+      level_out[(size_t)b * m + j] = (uint8_t)l;
+      const double v = (yb[j] < 0 ? -1.0 : 1.0) * (double)lev[l];
+      num = num + (double)yb[j] * v;
+      den = den + v * v;
+    }
+    w_out[b] = (float)(num / den * 0x1p-40 / sqrt((double)d));
+  }
+  free(k40);
+  free(y);
+}
+
+void lkvo_paris_rotate_query(const void *q, int dtype, int32_t g, int32_t d,
+                             const int8_t *sign, float *qrot_out) {
+  for (int32_t j = 0; j < d; ++j) {
+    float acc = elem(q, dtype, j);
+    for (int32_t h = 1; h < g; ++h) acc = acc + elem(q, dtype, (int64_t)h * d + j);
+    qrot_out[j] = sign[j] < 0 ? -acc : acc;
+  }
+  for (int32_t h = 1; h < d; h *= 2)
+    for (int32_t i = 0; i < d; i += 2 * h)
+      for (int32_t j = i; j < i + h; ++j) {
+        const float a = qrot_out[j], b = qrot_out[j + h];
+        qrot_out[j] = a + b;
+        qrot_out[j + h] = a - b;
+      }
+}
+
+/* (value desc, id asc) for the int and float rankings */
+static int better_i(const int32_t *v, int64_t a, int64_t b) {
+  return v[a] != v[b] ? v[a] > v[b] : a < b;
+}
+static int better_f(const float *v, int64_t a, int64_t b) {
+  return v[a] != v[b] ? v[a] > v[b] : a < b;
+}
+
+int64_t lkvo_paris_select(const float *qrot, int32_t d, int32_t m, int32_t rho,
+                          int64_t n_cand, int32_t budget, int64_t n,
+                          const uint8_t *bucket, const uint8_t *level, const float *w,
+                          const float *lev, int64_t *sel_out, int32_t *coarse_out,
+                          float *est_out) {
+  const int32_t nb = d / m, np = 1 << m;
+  int32_t *vote = (int32_t *)calloc((size_t)nb * np, sizeof *vote);
+  float *sim = (float *)malloc((size_t)np * sizeof *sim);
+  int32_t *coarse = (int32_t *)calloc((size_t)(n > 0 ? n : 1), sizeof *coarse);
+  float *est = (float *)calloc((size_t)(n > 0 ? n : 1), sizeof *est);
+  int64_t *order = (int64_t *)malloc((size_t)(n > 0 ? n : 1) * sizeof *order);
+  /* the rho best sign centroids of each subspace and their votes */
+  for (int32_t b = 0; b < nb; ++b) {
+    for (int32_t p = 0; p < np; ++p) {
+      float s = 0.0f;
+      for (int32_t j = 0; j < m; ++j) {
+        const float x = qrot[(size_t)b * m + j];
+        s = s + (((p >> j) & 1) ? -x : x);
+      }
+      sim[p] = s;
+    }
+    for (int32_t r = 0; r < rho && r < np; ++r) {
+      int32_t best = -1;
+      for (int32_t p = 0; p < np; ++p) {
+        if (vote[(size_t)b * np + p]) continue;
+        if (best < 0 || sim[p] > sim[best] || (sim[p] == sim[best] && p < best)) best = p;
+      }
+      vote[(size_t)b * np + best] = rho - r;
+    }
+  }
+  for (int64_t i = 0; i < n; ++i) {
+    int32_t c = 0;
+    for (int32_t b = 0; b < nb; ++b) c += vote[(size_t)b * np + bucket[(size_t)i * nb + b]];
+    coarse[i] = c;
+  }
+  /* candidates: the n_cand best coarse scores (insertion sort of all ids) */
+  for (int64_t i = 0; i < n; ++i) {
+    int64_t p = i;
+    while (p > 0 && better_i(coarse, i, order[p - 1])) {
+      order[p] = order[p - 1];
+      --p;
+    }
+    order[p] = i;
+  }
+  const int64_t nc = n_cand < n ? n_cand : n;
+  for (int64_t c = 0; c < nc; ++c) {
+    const int64_t i = order[c];
+    float e = 0.0f;
+    for (int32_t b = 0; b < nb; ++b) {
+      float dot = 0.0f;
+      for (int32_t j = 0; j < m; ++j) {
+        const size_t x = (size_t)b * m + j;
+        const float v = ((bucket[(size_t)i * nb + b] >> j) & 1) ? -lev[level[(size_t)i * d + x]]
+                                                                 : lev[level[(size_t)i * d + x]];
+        dot = fmaf(v, qrot[x], dot);
+      }
+      e = fmaf(w[(size_t)i * nb + b], dot, e);
+    }
+    est[i] = e;
+  }
+  /* the budget best candidates by the estimate */
+  int64_t *cand = (int64_t *)malloc((size_t)(nc > 0 ? nc : 1) * sizeof *cand);
+  for (int64_t c = 0; c < nc; ++c) {
+    const int64_t i = order[c];
+    int64_t p = c;
+    while (p > 0 && better_f(est, i, cand[p - 1])) {
+      cand[p] = cand[p - 1];
+      --p;
+    }
+    cand[p] = i;
+  }
+  const int64_t k = budget < nc ? budget : nc;
+  for (int64_t c = 0; c < k; ++c) sel_out[c] = cand[c];
+  if (coarse_out) memcpy(coarse_out, coarse, (size_t)n * sizeof *coarse);
+  if (est_out) memcpy(est_out, est, (size_t)n * sizeof *est);
+  free(vote); free(sim); free(coarse); free(est); free(order); free(cand);
+  return k;
+}
+
+/* ------------------------------------------------------------------------ */
 /* decode: boundary -> segment close -> append/evict -> retrieve -> attend   */
 
 int lkvo_decode(const lkvo_decode_args *a, lkvo_decode_result *r) {
@@ -356,24 +549,39 @@ int lkvo_decode(const lkvo_decode_args *a, lkvo_decode_result *r) {
   const int32_t T = a->n_steps;
   const int64_t n = a->n_prefill;
   const size_t es = elem_size(dt);
-  if (hkv < 1 || g < 1 || d < 1 || c < 1 || L < 1 || T < 0 || n < 0) return -1;
-  const int32_t ucap = c + T; /* every eviction removes at least one token */
+  const int paris = a->selector == LKVO_SELECT_PARIS;
+  /* the ParisKV-style selector has no clusters (c = 0) */
+  if (hkv < 1 || g < 1 || d < 1 || c < (paris ? 0 : 1) || L < 1 || T < 0 || n < 0) return -1;
+  const int32_t ucap = c + T > 0 ? c + T : 1; /* every eviction removes at least one token */
   if (a->trigger < 0 || a->trigger > 2 || (a->trigger == 2 && a->interval < 1) ||
       a->fill < 0 || a->fill > 1 || a->page < 0 || a->per_head < 0 || a->per_head > 1)
     return -1;
   /* selections: one per KV head, or one per query head */
   const int32_t hs = a->per_head ? h_all : hkv, gs = a->per_head ? 1 : g;
+  if (a->selector < 0 || a->selector > 1) return -1;
+  if (paris && (dt != LKVO_BF16 || a->per_head || d % 8 || a->paris_rho < 1 ||
+                a->paris_rho > 256 || a->paris_n_cand < 1))
+    return -1;
 
   int rc = -1;
+  /* ParisKV-style metadata of every prefill and decode token, per KV head */
+  const int32_t pnb = d / 8;
+  int8_t *psign = NULL;
+  uint8_t *pbk = NULL, *plv = NULL;
+  float *pw = NULL, *pq = NULL;
+  int64_t *psel = NULL;
+  float pthr[7], plev[8];
   /* cluster membership in token order, per kv head */
-  int32_t *cnt = (int32_t *)calloc((size_t)hkv * c, sizeof *cnt);
+  int32_t *cnt = (int32_t *)calloc((size_t)hkv * (c > 0 ? c : 1), sizeof *cnt);
   int32_t *first = (int32_t *)malloc((size_t)hkv * (c + 1) * sizeof *first);
   int64_t *member = (int64_t *)malloc((size_t)(hkv * n > 0 ? hkv * n : 1) * sizeof *member);
   /* per kv head unit tables: operand centroid and length */
   float *op = (float *)malloc((size_t)hkv * ucap * d * sizeof *op);
   int32_t *ulen = (int32_t *)malloc((size_t)hkv * ucap * sizeof *ulen);
   /* active selection per kv head */
-  int32_t *act = (int32_t *)malloc((size_t)hs * ucap * sizeof *act);
+  /* with the ParisKV-style selector a selection lists tokens (up to budget) */
+  const int64_t acap = paris ? (a->budget > 0 ? a->budget : 1) : ucap;
+  int32_t *act = (int32_t *)malloc((size_t)hs * acap * sizeof *act);
   int32_t *act_n = (int32_t *)calloc((size_t)hs, sizeof *act_n);
   int32_t *act_tok = (int32_t *)calloc((size_t)hs, sizeof *act_tok);
   /* closed, not yet evicted segments: FIFO of [start, end) */
@@ -388,7 +596,27 @@ int lkvo_decode(const lkvo_decode_args *a, lkvo_decode_result *r) {
       !act_tok || !cl_s || !cl_e || !scores || !segc || !segsum || !kg || !vg)
     goto done;
 
-  for (int32_t kh = 0; kh < hkv; ++kh) {
+  if (paris) {
+    const size_t ntot = (size_t)hkv * (size_t)(n + T);
+    psign = (int8_t *)malloc((size_t)d);
+    pbk = (uint8_t *)malloc(ntot * pnb);
+    plv = (uint8_t *)malloc(ntot * d);
+    pw = (float *)malloc(ntot * pnb * sizeof *pw);
+    pq = (float *)malloc((size_t)d * sizeof *pq);
+    psel = (int64_t *)malloc((size_t)acap * sizeof *psel);
+    if (!psign || !pbk || !plv || !pw || !pq || !psel) goto done;
+    lkvo_paris_signs(a->paris_seed, d, psign);
+    lkvo_paris_levels(8, pthr, plev);
+    for (int32_t kh = 0; kh < hkv; ++kh)
+      for (int64_t i = 0; i < n + T; ++i) {
+        const uint16_t *kr = i < n ? (const uint16_t *)a->keys + ((size_t)kh * n + i) * d
+                                   : (const uint16_t *)a->k_new + ((size_t)(i - n) * hkv + kh) * d;
+        const size_t x = (size_t)kh * (n + T) + i;
+        lkvo_paris_encode(kr, d, psign, 8, pthr, plev, pbk + x * pnb, plv + x * d, pw + x * pnb);
+      }
+  }
+
+  for (int32_t kh = 0; kh < hkv && !paris; ++kh) {
     const int32_t *as = a->assign + (size_t)kh * n;
     int32_t *ct = cnt + (size_t)kh * c;
     int32_t *fs = first + (size_t)kh * (c + 1);
@@ -473,7 +701,22 @@ int lkvo_decode(const lkvo_decode_args *a, lkvo_decode_result *r) {
     }
     /* 4. token t enters the local buffer [win_start, t] */
     /* 5. retrieval on a boundary step, against the pool after evictions */
-    if (flag) {
+    if (flag && paris) {
+      /* tokens: the prefill, then the decode tokens before the buffer */
+      for (int32_t kh = 0; kh < hkv; ++kh) {
+        const int64_t nreg = n + win_start;
+        const size_t x0 = (size_t)kh * (n + T);
+        const void *qg = row_ptr(a->q, dt, (int64_t)t * h_all + (int64_t)kh * g, d);
+        lkvo_paris_rotate_query(qg, dt, g, d, psign, pq);
+        /* the region is contiguous in the metadata: prefill i at i, decode t' at n + t' */
+        const int64_t k = lkvo_paris_select(pq, d, 8, a->paris_rho, a->paris_n_cand, a->budget, nreg,
+                                            pbk + x0 * pnb, plv + x0 * d, pw + x0 * pnb, plev, psel,
+                                            NULL, NULL);
+        for (int64_t c = 0; c < k; ++c) act[(size_t)kh * acap + c] = (int32_t)psel[c];
+        act_n[kh] = (int32_t)k;
+        act_tok[kh] = (int32_t)k;
+      }
+    } else if (flag) {
       /* selection j scores with the sum of query heads j*gs .. j*gs+gs-1
        * (its group, or the one head) against its KV head's units */
       for (int32_t j = 0; j < hs; ++j) {
@@ -482,10 +725,10 @@ int lkvo_decode(const lkvo_decode_args *a, lkvo_decode_result *r) {
         lkvo_group_scores(qg, dt, gs, d, op + (size_t)kh * ucap * d, n_units, scores);
         if (a->fill == LKVO_FILL_SKIP)
           act_n[j] = lkvo_select_skip(scores, ulen + (size_t)kh * ucap, n_units,
-                                      a->budget, act + (size_t)j * ucap, &act_tok[j]);
+                                      a->budget, act + (size_t)j * acap, &act_tok[j]);
         else
           act_n[j] = lkvo_select(scores, ulen + (size_t)kh * ucap, n_units,
-                                 a->budget, act + (size_t)j * ucap, &act_tok[j]);
+                                 a->budget, act + (size_t)j * acap, &act_tok[j]);
       }
     }
     /* 6. attention of each query head over its selection + buffer */
@@ -494,8 +737,16 @@ int lkvo_decode(const lkvo_decode_args *a, lkvo_decode_result *r) {
         const int32_t kh = j * gs / g;
         int64_t m = 0;
         for (int32_t s = 0; s < act_n[j]; ++s) {
-          int32_t u = act[(size_t)j * ucap + s];
-          if (u < c) {
+          int32_t u = act[(size_t)j * acap + s];
+          if (paris) { /* a token: prefill u, or decode token u - n */
+            const void *ks = u < n ? row_ptr(a->keys, dt, (int64_t)kh * n + u, d)
+                                   : row_ptr(a->k_new, dt, (int64_t)(u - n) * hkv + kh, d);
+            const void *vs = u < n ? row_ptr(a->values, dt, (int64_t)kh * n + u, d)
+                                   : row_ptr(a->v_new, dt, (int64_t)(u - n) * hkv + kh, d);
+            memcpy(kg + m * d * es, ks, d * es);
+            memcpy(vg + m * d * es, vs, d * es);
+            ++m;
+          } else if (u < c) {
             const int32_t *fs = first + (size_t)kh * (c + 1);
             for (int32_t p = fs[u]; p < fs[u + 1]; ++p) {
               int64_t i = member[(size_t)kh * n + p];
@@ -533,7 +784,7 @@ int lkvo_decode(const lkvo_decode_args *a, lkvo_decode_result *r) {
       if (r->n_tok) r->n_tok[(size_t)t * hs + j] = act_tok[j];
       if (r->sel) {
         if (act_n[j] > r->max_sel) goto done;
-        memcpy(r->sel + ((size_t)t * hs + j) * r->max_sel, act + (size_t)j * ucap,
+        memcpy(r->sel + ((size_t)t * hs + j) * r->max_sel, act + (size_t)j * acap,
                (size_t)act_n[j] * sizeof(int32_t));
       }
     }
@@ -546,5 +797,6 @@ done:
   free(cnt); free(first); free(member); free(op); free(ulen); free(act);
   free(act_n); free(act_tok); free(cl_s); free(cl_e); free(scores);
   free(segc); free(segsum); free(kg); free(vg);
+  free(psign); free(pbk); free(plv); free(pw); free(pq); free(psel);
   return rc;
 }

@@ -168,7 +168,83 @@ typedef struct {
   int32_t per_head;     /* 0: one selection per KV head from the group's summed
                            query; 1: one per query head from its own query, and
                            each head attends its own selection */
+  /* Selector: LKVO_SELECT_CLUSTERS (the method's units) or LKVO_SELECT_PARIS
+   * (tokens ranked by the ParisKV-style coarse-to-fine pipeline below, over
+   * the prefill tokens and the decode tokens that left the local buffer;
+   * bf16 only, per_head 0). With PARIS the selection records hold token ids
+   * (prefill token i, decode token t as n_prefill + t), best first. */
+  int32_t selector;
+  int32_t paris_rho;    /* sign centroids per subspace that vote */
+  int32_t paris_n_cand; /* candidates kept for the rerank */
+  uint64_t paris_seed;  /* sign flips of the rotation */
 } lkvo_decode_args;
+
+enum { LKVO_SELECT_CLUSTERS = 0, LKVO_SELECT_PARIS = 1 };
+
+/* ------------------------------------------------------------------------ */
+/* ParisKV-style selector [ParisKV technical summary, 核心算法创新 1 (l2
+ * normalisation and a shared random orthogonal rotation by SRHT; analytic
+ * sign centroids on the unit sphere) and 2 (collision voting over B
+ * subspaces with the top-rho centroids of each, then a rerank of the
+ * candidates by the calibrated estimate ||q|| sum_b w_b <v_b, q_b> from
+ * 4-bit codes: 1 sign bit + 3 magnitude bits per coordinate from the Beta
+ * prior that the rotation induces)]. Readings: the rotation is
+ * H diag(D) / sqrt(d) with H the Sylvester-Hadamard matrix and D random
+ * signs; a key is rotated exactly (its bf16 values as integers times 2^40);
+ * the bucket of a subspace is the sign pattern of the rotated key there (the
+ * nearest analytic centroid); the 3-bit magnitude of coordinate j of the
+ * subspace direction u = y_b / |y_b| is the number of prior quantiles t_l
+ * (l = 1..7, P(|x| < t_l) = l/8 for a coordinate x of a uniform unit vector
+ * in R^m) at or below |u_j|, its value the prior's mean of |x| over that
+ * bin; w_b = <y_b, v_b> / <v_b, v_b> (the least-squares scale of the
+ * dequantised direction v_b, which holds |y_b| and the calibration); the
+ * vote of the r-th best centroid (r = 0..rho-1) is rho - r; the constant
+ * factor ||q|| of the estimate is dropped (it does not change the order). */
+
+/* D_j = -1 where bit j % 64 of the (j / 64)-th splitmix64 output of seed is
+ * set, else +1. */
+void lkvo_paris_signs(uint64_t seed, int32_t d, int8_t *sign_out);
+
+/* Quantiles and bin means of |x| for a coordinate x of a uniform unit vector
+ * in R^m (density of x proportional to (1 - x^2)^((m-3)/2)), by Simpson
+ * integration and bisection in double: thr_out[l-1] = float(t_l^2) for
+ * l = 1..7, lev_out[l] = float(E[|x| : t_l <= |x| < t_{l+1}]) for l = 0..7
+ * (t_0 = 0, t_8 = 1). Returns 0, or -1 for m < 2. */
+int lkvo_paris_levels(int32_t m, float *thr_out, float *lev_out);
+
+/* Metadata of one bf16 key (d dims, B = d / m subspaces, m = 8):
+ * y = H D round_toward_zero(k * 2^40) in exact integers; bucket_out[b] = the
+ * sign bits of y over subspace b (bit j set where y_{mb+j} < 0);
+ * level_out[i] = #{l : y_i^2 >= thr[l] * n2_b} with n2_b = sum_j y_{mb+j}^2
+ * (double products and adds in index order); w_out[b] = float of
+ * (sum_j y_j v_j) / (sum_j v_j^2) * 2^-40 / sqrt(d), v_j = +-lev[level_j]
+ * (double, index order). */
+void lkvo_paris_encode(const uint16_t *key, int32_t d, const int8_t *sign, int32_t m,
+                       const float *thr, const float *lev, uint8_t *bucket_out,
+                       uint8_t *level_out, float *w_out);
+
+/* The rotated group query in single precision: qbar = sum of the g heads
+ * (adds in head order), x_j = D_j qbar_j, then the in-place fast Hadamard
+ * butterfly over h = 1, 2, 4, ..., d/2 (pairs (j, j + h) -> (a + b, a - b)
+ * within blocks of 2h, in index order). */
+void lkvo_paris_rotate_query(const void *q, int dtype, int32_t g, int32_t d,
+                             const int8_t *sign, float *qrot_out);
+
+/* Token selection over n tokens with their metadata ([n][B] buckets, [n][d]
+ * levels, [n][B] scales): per subspace the 2^m sign patterns p score
+ * sim_p = sum_j (bit j of p ? -q_j : q_j) (single-precision adds in index
+ * order); the best rho by (sim desc, p asc) vote rho - r; a token's coarse
+ * score is the sum of its buckets' votes; the n_cand best tokens by (coarse
+ * desc, id asc) are reranked by est = sum_b w_b dot_b, dot_b = sum_j v_j q_j
+ * (fmaf chains in index order, est = fmaf(w_b, dot_b, est)); the budget best
+ * by (est desc, id asc) are selected. sel_out receives their ids, best
+ * first; coarse_out [n] and est_out [n] (optional) the scores (est only for
+ * candidates, else 0). Returns the number selected. */
+int64_t lkvo_paris_select(const float *qrot, int32_t d, int32_t m, int32_t rho,
+                          int64_t n_cand, int32_t budget, int64_t n,
+                          const uint8_t *bucket, const uint8_t *level, const float *w,
+                          const float *lev, int64_t *sel_out, int32_t *coarse_out,
+                          float *est_out);
 
 enum { LKVO_TRIGGER_ADAPTIVE = 0, LKVO_TRIGGER_EVERY = 1, LKVO_TRIGGER_INTERVAL = 2 };
 enum { LKVO_FILL_PREFIX = 0, LKVO_FILL_SKIP = 1 };

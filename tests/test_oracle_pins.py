@@ -575,3 +575,147 @@ def test_decode_per_head_selection_uses_own_query():
     # heads of one group disagree somewhere (otherwise the variant measures nothing)
     assert any(res["n_tok"][0, h] != res["n_tok"][0, h + 1] or
                not np.array_equal(res["sel"][0, h], res["sel"][0, h + 1]) for h in range(g - 1))
+
+
+# ------------------------------------------------------------------ ParisKV-style selector
+
+def test_paris_levels_are_beta_prior_quantiles_and_bin_means():
+    """The rotation makes each coordinate x of a subspace direction in R^8
+    behave like one of a uniform unit vector: x^2 ~ Beta(1/2, 7/2). The
+    thresholds are its quantiles at l/8, the levels the bin means of |x|."""
+    stats = pytest.importorskip("scipy.stats")
+    integrate = pytest.importorskip("scipy.integrate")
+    thr, lev = oracle.paris_levels(8)
+    want = stats.beta.ppf(np.arange(1, 8) / 8, 0.5, 3.5)
+    assert np.allclose(thr, want, rtol=2e-7, atol=0)
+    t = np.concatenate([[0.0], np.sqrt(want), [1.0]])
+    dens = lambda x: (1 - x * x) ** 2.5
+    for l in range(8):
+        num = integrate.quad(lambda x: x * dens(x), t[l], t[l + 1], epsabs=1e-14)[0]
+        den = integrate.quad(dens, t[l], t[l + 1], epsabs=1e-14)[0]
+        assert abs(lev[l] - num / den) <= 2e-7 * num / den
+    assert np.all(np.diff(lev) > 0) and lev[0] > 0 and lev[-1] < 1
+
+
+def test_paris_signs_follow_splitmix64_bits():
+    s = oracle.paris_signs(77, 128)
+    words = oracle.splitmix64(77, 2)
+    for j in range(128):
+        bit = (int(words[j // 64]) >> (j % 64)) & 1
+        assert s[j] == (-1 if bit else 1)
+
+
+def _paris_keys(n=64, seed=3):
+    r = np.random.default_rng(seed)
+    return bf16(r.standard_normal((n, 128)).astype(np.float32))
+
+
+def test_paris_encode_against_hadamard_and_nearest_sign_centroid():
+    linalg = pytest.importorskip("scipy.linalg")
+    seed = 11
+    keys = _paris_keys()
+    bk, lv, w = oracle.paris_encode(keys, seed)
+    Hm = linalg.hadamard(128).astype(np.float64)
+    D = oracle.paris_signs(seed).astype(np.float64)
+    thr, lev = oracle.paris_levels(8)
+    for i in range(len(keys)):
+        k = unbf16(keys[i]).astype(np.float64)
+        y = Hm @ (D * k)                                  # exact: bf16 values, +-1 weights
+        yb = y.reshape(16, 8)
+        # the bucket is the nearest of the 256 analytic centroids s / sqrt(8)
+        pats = np.array([[-1.0 if (p >> j) & 1 else 1.0 for j in range(8)] for p in range(256)])
+        for b in range(16):
+            u = yb[b] / np.linalg.norm(yb[b])
+            assert int(np.argmax(pats @ u)) == bk[i, b]
+            mag = (u * u)[:, None] >= thr[None, :].astype(np.float64)
+            assert np.array_equal(lv[i, 8 * b:8 * b + 8], mag.sum(1))
+            v = np.where(pats[bk[i, b]] < 0, -1.0, 1.0) * lev[lv[i, 8 * b:8 * b + 8]]
+            ws = (yb[b] @ v) / (v @ v) / math.sqrt(128)
+            assert abs(w[i, b] - ws) <= 1e-6 * abs(ws)
+
+
+def test_paris_query_rotation_is_hadamard_of_signed_group_sum():
+    linalg = pytest.importorskip("scipy.linalg")
+    r = np.random.default_rng(5)
+    q = bf16(r.standard_normal((4, 128)).astype(np.float32))
+    got = oracle.paris_rotate_query(q, 9)
+    qbar = unbf16(q).astype(np.float64).sum(0)
+    want = linalg.hadamard(128) @ (oracle.paris_signs(9).astype(np.float64) * qbar)
+    assert np.allclose(got, want, rtol=1e-5, atol=1e-4)
+
+
+def test_paris_estimate_tracks_the_inner_product():
+    """est_i ~ sqrt(d) <k_i, qbar> (the rotation scale): strong correlation
+    and the right scale, from 3-bit magnitudes."""
+    seed = 4
+    keys = _paris_keys(400, seed=8)
+    r = np.random.default_rng(6)
+    q = bf16(r.standard_normal((4, 128)).astype(np.float32))
+    bk, lv, w = oracle.paris_encode(keys, seed)
+    qr = oracle.paris_rotate_query(q, seed)
+    _, coarse, est = oracle.paris_select(qr, bk, lv, w, rho=4, n_cand=400, budget=10)
+    true = unbf16(keys).astype(np.float64) @ unbf16(q).astype(np.float64).sum(0)
+    assert np.corrcoef(est, true)[0, 1] > 0.97
+    slope = (est @ true) / (true @ true)
+    assert abs(slope / math.sqrt(128) - 1) < 0.05
+    assert coarse.max() <= 16 * 4 and coarse.min() >= 0
+
+
+def test_paris_select_definition_on_small_sets():
+    """Brute force: candidates are the n_cand best (coarse desc, id asc), the
+    selection the budget best of those by (estimate desc, id asc); a key with
+    the query's own direction collects every subspace's top vote."""
+    seed = 2
+    for trial in range(20):
+        r = np.random.default_rng(100 + trial)
+        n = int(r.integers(5, 60))
+        keys = _paris_keys(n, seed=200 + trial)
+        q = bf16(r.standard_normal((2, 128)).astype(np.float32))
+        bk, lv, w = oracle.paris_encode(keys, seed)
+        qr = oracle.paris_rotate_query(q, seed)
+        rho, n_cand, budget = int(r.integers(1, 9)), int(r.integers(1, n + 3)), int(r.integers(0, n + 3))
+        sel, coarse, est = oracle.paris_select(qr, bk, lv, w, rho=rho, n_cand=n_cand, budget=budget)
+        cand = sorted(range(n), key=lambda i: (-int(coarse[i]), i))[:n_cand]
+        want = sorted(cand, key=lambda i: (-float(est[i]), i))[:budget]
+        assert list(sel) == want
+    # the query's own direction: its sign pattern is the top centroid everywhere
+    k = bf16(np.random.default_rng(1).standard_normal((1, 128)).astype(np.float32))
+    bk, lv, w = oracle.paris_encode(np.concatenate([k, _paris_keys(30)]), seed)
+    qr = oracle.paris_rotate_query(k, seed)
+    _, coarse, _ = oracle.paris_select(qr, bk, lv, w, rho=3, n_cand=31, budget=1)
+    assert coarse[0] == 16 * 3
+
+
+def test_decode_paris_fullcache_special_case():
+    """Budget and candidate count above every token: the ParisKV-style
+    selection takes every prefill and evicted token, so the output is full
+    attention over all tokens so far."""
+    hkv, g, n, T, L = 2, 4, 120, 40, 8
+    keys, values, _, _, q, kn, vn = _decode_inputs("bf16", hkv, g, n=n, c=4, T=T)
+    res = oracle.decode(keys, values, None, None, q, kn, vn, n_clusters=0, local_buf=L, tau=1.5,
+                        budget=n + T, paris=dict(rho=4, n_cand=n + T, seed=3))
+    K, Vv, Q, KN, VN = (_f(x) for x in (keys, values, q, kn, vn))
+    for t in range(T):
+        assert res["n_sel"][t, 0] == n + res["win_start"][t]
+        for kh in range(hkv):
+            kk = np.concatenate([K[kh], KN[: t + 1, kh]])
+            vv = np.concatenate([Vv[kh], VN[: t + 1, kh]])
+            want = _softmax_attn(Q[t, kh * g:(kh + 1) * g], kk, vv)
+            assert np.allclose(res["out"][t, kh * g:(kh + 1) * g], want, atol=1e-10)
+
+
+def test_decode_paris_selection_matches_select_over_region():
+    hkv, g, n, T, L, budget = 1, 4, 200, 60, 8, 40
+    keys, values, _, _, q, kn, vn = _decode_inputs("bf16", hkv, g, n=n, c=4, T=T, jump=0.2, seed=12)
+    pr = dict(rho=4, n_cand=80, seed=5)
+    res = oracle.decode(keys, values, None, None, q, kn, vn, n_clusters=0, local_buf=L, tau=0.9,
+                        budget=budget, paris=pr)
+    allk = np.concatenate([keys[0], kn[:, 0]])
+    bk, lv, w = oracle.paris_encode(allk, pr["seed"])
+    for t in np.flatnonzero(res["flag"]):
+        reg = n + res["win_start"][t]
+        qr = oracle.paris_rotate_query(q[t, 0:g], pr["seed"])
+        sel, _, _ = oracle.paris_select(qr, bk[:reg], lv[:reg], w[:reg], rho=4, n_cand=80, budget=budget)
+        k = res["n_sel"][t, 0]
+        assert k == len(sel) == min(budget, 80, reg)
+        assert np.array_equal(res["sel"][t, 0, :k], sel)
