@@ -490,6 +490,12 @@ def run_ours(args, rank, world, local):
         torch.cuda.empty_cache()
         result["multi_layer"] = multi_layer_probe(torch, w, hbm_peak, peak_kind)
         torch.cuda.empty_cache()
+        result["policy_baselines"] = policy_probe(torch, w)
+        torch.cuda.empty_cache()
+        result["async_build"] = async_build_probe(torch)
+        torch.cuda.empty_cache()
+        result["paris_selector"] = paris_probe(torch, w)
+        torch.cuda.empty_cache()
     if want_cpu:
         result["cpu_baseline"] = cpu_baseline(K, V, idx0, q, kn, vn, w)
     return result
@@ -607,6 +613,198 @@ def multi_layer_probe(torch, w0, hbm_peak, peak_kind):
                               "alg_bytes_per_launch": alg, "avg_launch_us": sec * 1e6,
                               "launches": int(n_attn), "peak_source": f"{peak_kind} hbm_gbs",
                               "l2": "256 MB written before every step"}}
+
+
+def policy_probe(torch, w0):
+    """The retrieval policies on the 32K-input, batch-8 workload, each over
+    the same inputs: the method (retrieval when r_t < tau, K-means clusters
+    and boundary segments), retrieval at every step, at every 32nd step, and
+    the page-granular every-step baseline (16-token pages of the input, as
+    many units as clusters, and 16-token output pages). Per policy: decode
+    steps/s through the pipelined graph (steps 0..1535), then 256 single-step
+    launches with CUDA events around every kernel (L2 overwritten before
+    every step) for the share of the step that goes to scoring + selection
+    (the retrieval; the K/V rows are read where they lie by the attention)."""
+    import synth
+    import cluster_indexed_kv_gb300 as lkv
+    T1, T2 = 1536, 256
+    w = w0.replace(n_steps=T1 + T2, iters=4)
+    K, V = synth.prefill(w, 0, "cuda")
+    q, kn, vn, _ = synth.decode_inputs(w, "cuda")
+    out = torch.empty(w.n_steps, w.batch, 1, w.n_heads, 128, device="cuda")
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+    rows = {}
+    policies = [("method: adaptive r_t < tau, clusters + segments", dict(), 0),
+                ("every-step retrieval, clusters + segments", dict(trigger="every"), 0),
+                ("every 32nd step, clusters + segments", dict(trigger="interval", interval=32), 0),
+                ("every-step retrieval, 16-token pages in and out", dict(trigger="every", page=16), 16),
+                ("method with a selection per query head (not group-consistent)", dict(per_head=True), 0)]
+    for name, pol, pages in policies:
+        ctx = lkv.Context(batch=w.batch, n_layers=1, n_kv_heads=w.n_kv_heads, group=w.group,
+                          dtype=w.torch_dtype, local_buf=w.local_buf, max_clusters=w.n_clusters,
+                          max_prefill=w.n_prefill, max_steps=w.n_steps, max_budget=w.budget)
+        if pages:
+            ctx.build_pages(0, K, V, pages)
+        else:
+            ctx.build_index(0, K, V, w.n_clusters, w.iters, 1)
+        ctx.set_policy(**pol)
+        bnd = torch.zeros(w.n_steps, w.batch, 1, dtype=torch.uint8, device="cuda")
+        ctx.sync()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(ctx.stream)
+        ctx.decode_steps(0, q[:T1], kn[:T1], vn[:T1], w.tau, w.budget, out[:T1], boundary=bnd[:T1])
+        e1.record(ctx.stream)
+        e1.synchronize()
+        sps = T1 / (e0.elapsed_time(e1) / 1e3)
+        ctx.set_profiling(True)
+        ctx.profile(reset=True)
+        for t in range(T1, T1 + T2):
+            flush.fill_(float(t))
+            ctx.decode_step(0, q[t], kn[t], vn[t], w.tau, w.budget, out[t], boundary=bnd[t])
+        kern, ctr = ctx.profile(reset=True)
+        ctx.close()
+        ms = {k: v[1] for k, v in kern.items() if v[0]}
+        total = sum(ms.values())
+        retr = ms.get("lkv_select", 0.0) + ms.get("lkv_score", 0.0) + ms.get("lkv_gather_offload", 0.0)
+        rows[name] = {"decode_steps_per_s": sps, "retrieval_rate": float(bnd.float().mean().item()),
+                      "retrieval_share_of_step": retr / total if total else None,
+                      "single_step_us": {k: round(v / T2 * 1e3, 2) for k, v in ms.items()},
+                      "attended_rows_per_step": ctr["attn_rows"] / T2,
+                      "attended_bytes_per_step": ctr["attn_rows"] * 2 * 128 * 2 / T2,
+                      "selected_tokens_per_retrieval": ctr["sel_tokens"] / max(
+                          1, int(bnd[T1:].sum().item()) * w.n_kv_heads)}
+    return {"workload": "b8_32k (4 Lloyd rounds for the clustered rows)", "policies": rows,
+            "note": "share = scoring+selection kernel time / all decode kernel time of the "
+                    "single-step launches (the pages' breakdown also counts the host transfer "
+                    "of an offloaded cache; here the rows stay in HBM). selected tokens per "
+                    "retrieval count every query head's own selection in the per-head row (what "
+                    "separate per-head gathers would move); its attended rows are the union "
+                    "the kernel reads once per group"}
+
+
+def paris_probe(torch, w0):
+    """The ParisKV-style token selector on the 32K-input, batch-8 workload
+    (same inputs, budget 1024 tokens, rho 4, 2560 candidates = 7.8% of the
+    prefill): decode steps/s through the pipelined graph with the method's
+    adaptive trigger and with retrieval at every step, then 128 single-step
+    launches at every step (L2 overwritten before each) for the selection
+    kernel's time and its HBM roofline (bucket bytes of every region token,
+    codes and scales of every candidate, 16 + 128 bytes)."""
+    import synth
+    import cluster_indexed_kv_gb300 as lkv
+    T1, T2 = 1536, 128
+    w = w0.replace(n_steps=2 * T1 + T2)
+    K, V = synth.prefill(w, 0, "cuda")
+    q, kn, vn, _ = synth.decode_inputs(w, "cuda")
+    out = torch.empty(w.n_steps, w.batch, 1, w.n_heads, 128, device="cuda")
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+    res = {"workload": "b8_32k, ParisKV-style selector (rho 4, 2560 candidates, budget 1024 tokens)"}
+    for name, pol, t0 in (("adaptive", dict(), 0), ("every_step", dict(trigger="every"), T1)):
+        ctx = lkv.Context(batch=w.batch, n_layers=1, n_kv_heads=w.n_kv_heads, group=w.group,
+                          dtype=w.torch_dtype, local_buf=w.local_buf, max_clusters=w.n_clusters,
+                          max_prefill=w.n_prefill, max_steps=w.n_steps, max_budget=w.budget)
+        ctx.build_paris(0, K, V, rho=4, n_cand=2560, seed=1)
+        ctx.set_policy(**pol)
+        ctx.sync()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(ctx.stream)
+        ctx.decode_steps(0, q[:T1], kn[:T1], vn[:T1], w.tau, w.budget, out[:T1])
+        e1.record(ctx.stream)
+        e1.synchronize()
+        res[f"decode_steps_per_s_{name}"] = T1 / (e0.elapsed_time(e1) / 1e3)
+        if name == "every_step":
+            ctx.set_profiling(True)
+            ctx.profile(reset=True)
+            for t in range(T1, T1 + T2):
+                flush.fill_(float(t))
+                ctx.decode_step(0, q[t], kn[t], vn[t], w.tau, w.budget, out[t])
+            kern, ctr = ctx.profile(reset=True)
+            n_sel, ms_sel = kern["lkv_select"]
+            sec = ms_sel / n_sel / 1e3
+            region = ctr["score_units"] / n_sel           # region tokens per launch
+            cand = min(2560, region / (w.batch * w.n_kv_heads)) * w.batch * w.n_kv_heads
+            alg = region * 16 + cand * 128
+            res["select_us"] = sec * 1e6
+            res["select_roofline"] = {"bound": "hbm", "achieved": alg / sec / 1e9, "unit": "GB/s",
+                                      "alg_bytes_per_launch": alg,
+                                      "note": "bucket bytes of every region token + codes and scales "
+                                              "of every candidate"}
+            res["single_step_us"] = {k: round(v[1] / v[0] * 1e3, 2) for k, v in kern.items() if v[0]}
+        ctx.close()
+    return res
+
+
+def async_build_probe(torch):
+    """Index build pipelined behind a prefill stand-in: 4 layers of the
+    32K-input shape (8 KV heads x 32768 keys, C = 2048, 20 Lloyd rounds).
+    The stand-in for a layer's prefill forward is a chain of cuBLAS bf16
+    GEMMs [32768 x 4096] x [4096 x 4096] with the FLOPs of one Qwen3-8B-shaped
+    layer at 32K tokens (projections and MLP 2*N*193M, causal attention
+    2*N^2*d*H: 21.4 TFLOP, 19 GEMMs). Timed alone, the builds alone, then the
+    prefill with layer l's build (lkv_build_index_async on the context's own
+    stream) waiting for layer l's event: hidden fraction = 1 - (overlapped -
+    prefill) / builds."""
+    import synth
+    import cluster_indexed_kv_gb300 as lkv
+    NL = 4
+    w = synth.WORKLOADS["long_in"].replace(n_layers=NL)
+    KV = [synth.prefill(w, l, "cuda") for l in range(NL)]
+    side = torch.cuda.Stream()
+    ctx = lkv.Context(batch=1, n_layers=NL, n_kv_heads=w.n_kv_heads, group=w.group,
+                      dtype=w.torch_dtype, local_buf=w.local_buf, max_clusters=w.n_clusters,
+                      max_prefill=w.n_prefill, max_steps=w.n_steps, max_budget=w.budget, stream=side)
+    x0 = torch.randn(w.n_prefill, 4096, device="cuda", dtype=torch.bfloat16)
+    wm = torch.randn(4096, 4096, device="cuda", dtype=torch.bfloat16) / 64.0
+    n_gemm = 19
+    main = torch.cuda.current_stream()
+
+    def prefill_layer(x):
+        for _ in range(n_gemm):
+            x = x @ wm
+        return x
+
+    def timed(fn):
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(main)
+        fn()
+        main.wait_stream(side)
+        b.record(main)
+        b.synchronize()
+        return a.elapsed_time(b)
+
+    def pre_only():
+        x = x0
+        for _ in range(NL):
+            x = prefill_layer(x)
+
+    def build_only():
+        with torch.cuda.stream(side):
+            side.wait_stream(main)
+            for l in range(NL):
+                ctx.build_index(l, KV[l][0], KV[l][1], w.n_clusters, w.iters, 1 + l)
+
+    def overlapped():
+        x = x0
+        for l in range(NL):
+            x = prefill_layer(x)
+            ev = torch.cuda.Event()
+            ev.record(main)
+            ctx.build_index_async(l, KV[l][0], KV[l][1], w.n_clusters, w.iters, 1 + l, ready=ev)
+
+    for fn in (pre_only, build_only, overlapped):
+        timed(fn)  # warm-up
+    res = {}
+    for name, fn in (("prefill_ms", pre_only), ("build_ms", build_only), ("overlapped_ms", overlapped)):
+        res[name] = sorted(timed(fn) for _ in range(3))[1]
+    ctx.close()
+    hidden = 1.0 - (res["overlapped_ms"] - res["prefill_ms"]) / res["build_ms"]
+    return {"workload": "4 layers x (1 sequence, 8 KV heads, 32768 keys, C=2048, 20 rounds)",
+            **res, "hidden_fraction": hidden,
+            "prefill_slowdown": res["overlapped_ms"] / res["prefill_ms"] - 1.0,
+            "prefill_standin": f"{n_gemm} cuBLAS bf16 GEMMs [32768x4096]x[4096x4096] per layer",
+            "note": "median of 3; the pages report TTFT +3.5% over FullCache with their overlap "
+                    "(another model, GPU and prefill; context only)"}
 
 
 # ---------------------------------------------------------------- reference arm

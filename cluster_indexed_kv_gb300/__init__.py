@@ -34,6 +34,15 @@ def _dev_ptr(t: torch.Tensor, name: str, dtype=None) -> int:
     return t.data_ptr()
 
 
+def _event_ptr(ev):
+    """cudaEvent_t of a torch.cuda.Event (created now if it never was), or None."""
+    if ev is None:
+        return None
+    if not ev.cuda_event:
+        ev.record()  # torch creates the CUDA event at its first record
+    return ev.cuda_event
+
+
 def _opt_ptr(t, name, dtype=None):
     return None if t is None else _dev_ptr(t, name, dtype)
 
@@ -91,6 +100,46 @@ class Context:
                             _dev_ptr(values, "values", self.dtype), n, n_clusters,
                             _dev_ptr(assign, "assign", torch.int32),
                             _dev_ptr(centroids, "centroids", torch.float32))
+
+    def build_index_async(self, layer: int, keys: torch.Tensor, values: torch.Tensor,
+                          n_clusters: int, iters: int, seed: int,
+                          ready: "torch.cuda.Event | None" = None,
+                          done: "torch.cuda.Event | None" = None) -> None:
+        """build_index on the context's stream after `ready` (an event the
+        producer recorded when this layer's keys and values were complete);
+        `done` is recorded once the build has finished reading them."""
+        n = keys.shape[-2]
+        _lib.lkv_build_index_async(self._ctx, layer, _dev_ptr(keys, "keys", self.dtype),
+                                   _dev_ptr(values, "values", self.dtype), n, n_clusters, iters,
+                                   seed, _event_ptr(ready), _event_ptr(done))
+
+    def build_paris(self, layer: int, keys: torch.Tensor, values: torch.Tensor, *, rho: int = 4,
+                    n_cand: int = 2048, seed: int = 1) -> None:
+        """ParisKV-style token selector for this layer (see lkv_build_paris):
+        the pool in token order plus per-token codes; no clusters."""
+        n = keys.shape[-2]
+        _lib.lkv_build_paris(self._ctx, layer, _dev_ptr(keys, "keys", self.dtype),
+                             _dev_ptr(values, "values", self.dtype), n, rho, n_cand, seed)
+
+    def build_pages(self, layer: int, keys: torch.Tensor, values: torch.Tensor, page: int) -> None:
+        """Page-mean units (ceil(N / page) pages of consecutive tokens) instead
+        of a K-means index."""
+        n = keys.shape[-2]
+        _lib.lkv_build_pages(self._ctx, layer, _dev_ptr(keys, "keys", self.dtype),
+                             _dev_ptr(values, "values", self.dtype), n, page)
+
+    def set_policy(self, trigger: str = "adaptive", interval: int = 1, fill: str = "prefix",
+                   page: int = 0, per_head: bool = False) -> None:
+        """Retrieval policy: trigger "adaptive" (r_t < tau), "every" or
+        "interval"; fill "prefix" (stop at the first unit that does not fit)
+        or "skip"; page 0 (segments close at retrievals) or P (P-token pages);
+        per_head: a selection per query head (selection records become
+        [.., H, u_cap] and [.., H])."""
+        trig = {"adaptive": _lib.LKV_TRIGGER_ADAPTIVE, "every": _lib.LKV_TRIGGER_EVERY,
+                "interval": _lib.LKV_TRIGGER_INTERVAL}[trigger]
+        fl = {"prefix": _lib.LKV_FILL_PREFIX, "skip": _lib.LKV_FILL_SKIP}[fill]
+        _lib.lkv_set_policy(self._ctx, trig, interval, fl, page, 1 if per_head else 0)
+        self.per_head = bool(per_head)
 
     def decode_step(self, layer: int, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
                     tau: float, budget: int, out: torch.Tensor, *, n_layers: int = 1,

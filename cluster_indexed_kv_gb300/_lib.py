@@ -21,8 +21,11 @@ EXPORTED = ("lkv_create", "lkv_destroy", "lkv_build_index", "lkv_load_index",
             "lkv_decode_step", "lkv_decode_steps", "lkv_get_index", "lkv_get_decode_state",
             "lkv_sync", "lkv_last_error", "lkv_set_profiling", "lkv_get_profile",
             "lkv_kmeans_static", "lkv_kmeans_static_status", "lkv_set_kmeans_filter",
-            "lkv_diag_wait_timeout", "lkv_uva_read")
+            "lkv_diag_wait_timeout", "lkv_uva_read", "lkv_set_policy", "lkv_build_pages",
+            "lkv_build_index_async", "lkv_build_paris", "lkv_paris_levels")
 LKV_FILTER_TENSOR, LKV_FILTER_SIMT = 0, 1
+LKV_TRIGGER_ADAPTIVE, LKV_TRIGGER_EVERY, LKV_TRIGGER_INTERVAL = 0, 1, 2
+LKV_FILL_PREFIX, LKV_FILL_SKIP = 0, 1
 
 
 class lkv_config(C.Structure):
@@ -33,6 +36,15 @@ class lkv_config(C.Structure):
         ("max_steps", C.c_int32), ("max_budget", C.c_int32), ("offload", C.c_int32),
         ("stream", C.c_void_p),
     ]
+
+
+class lkv_policy(C.Structure):
+    _fields_ = [("trigger", C.c_int32), ("interval", C.c_int32), ("fill", C.c_int32),
+                ("page", C.c_int32), ("per_head", C.c_int32)]
+
+
+class lkv_paris_params(C.Structure):
+    _fields_ = [("rho", C.c_int32), ("n_cand", C.c_int32), ("seed", C.c_uint64)]
 
 
 class lkv_decode_state(C.Structure):
@@ -77,6 +89,8 @@ def load(path: str = LIB_PATH):
         L.lkv_destroy.restype = None
         L.lkv_build_index.argtypes = [vp, i32, vp, vp, i64, i32, i32, u64]
         L.lkv_build_index.restype = st
+        L.lkv_build_index_async.argtypes = [vp, i32, vp, vp, i64, i32, i32, u64, vp, vp]
+        L.lkv_build_index_async.restype = st
         L.lkv_load_index.argtypes = [vp, i32, vp, vp, i64, i32, vp, vp]
         L.lkv_load_index.restype = st
         L.lkv_decode_step.argtypes = [vp, i32, i32, vp, vp, vp, f32, i32, i32, vp, vp, vp, vp, vp]
@@ -102,6 +116,14 @@ def load(path: str = LIB_PATH):
         L.lkv_uva_read.restype = st
         L.lkv_diag_wait_timeout.argtypes = [vp, i64]
         L.lkv_diag_wait_timeout.restype = st
+        L.lkv_set_policy.argtypes = [vp, C.POINTER(lkv_policy)]
+        L.lkv_set_policy.restype = st
+        L.lkv_build_pages.argtypes = [vp, i32, vp, vp, i64, i32]
+        L.lkv_build_pages.restype = st
+        L.lkv_build_paris.argtypes = [vp, i32, vp, vp, i64, C.POINTER(lkv_paris_params)]
+        L.lkv_build_paris.restype = st
+        L.lkv_paris_levels.argtypes = [vp, vp]
+        L.lkv_paris_levels.restype = st
         L.lkv_sync.argtypes = [vp]
         L.lkv_sync.restype = st
         L.lkv_last_error.argtypes = [vp]
@@ -131,6 +153,12 @@ def lkv_build_index(ctx, layer, keys_ptr, values_ptr, n_tokens, n_clusters, iter
                                   iters, seed), ctx)
 
 
+def lkv_build_index_async(ctx, layer, keys_ptr, values_ptr, n_tokens, n_clusters, iters, seed,
+                          ready_event, done_event):
+    _check(load().lkv_build_index_async(ctx, layer, keys_ptr, values_ptr, n_tokens, n_clusters,
+                                        iters, seed, ready_event, done_event), ctx)
+
+
 def lkv_load_index(ctx, layer, keys_ptr, values_ptr, n_tokens, n_clusters, assign_ptr, cent_ptr):
     _check(load().lkv_load_index(ctx, layer, keys_ptr, values_ptr, n_tokens, n_clusters,
                                  assign_ptr, cent_ptr), ctx)
@@ -147,6 +175,27 @@ def lkv_decode_steps(ctx, layer, n_layers, n_steps, q_ptr, k_ptr, v_ptr, tau, bu
     _check(load().lkv_decode_steps(ctx, layer, n_layers, n_steps, q_ptr, k_ptr, v_ptr, tau,
                                    budget, local_buf, out_ptr, sel_ptr, nsel_ptr, boundary_ptr,
                                    r_ptr), ctx)
+
+
+def lkv_set_policy(ctx, trigger: int, interval: int, fill: int, page: int, per_head: int = 0) -> None:
+    pol = lkv_policy(trigger, interval, fill, page, per_head)
+    _check(load().lkv_set_policy(ctx, C.byref(pol)), ctx)
+
+
+def lkv_build_pages(ctx, layer, keys_ptr, values_ptr, n_tokens, page):
+    _check(load().lkv_build_pages(ctx, layer, keys_ptr, values_ptr, n_tokens, page), ctx)
+
+
+def lkv_build_paris(ctx, layer, keys_ptr, values_ptr, n_tokens, rho, n_cand, seed):
+    prm = lkv_paris_params(rho, n_cand, seed)
+    _check(load().lkv_build_paris(ctx, layer, keys_ptr, values_ptr, n_tokens, C.byref(prm)), ctx)
+
+
+def lkv_paris_levels():
+    """(thresholds [7], bin means [8]) as lists of floats (host only)."""
+    thr, lev = (C.c_float * 7)(), (C.c_float * 8)()
+    _check(load().lkv_paris_levels(thr, lev), None)
+    return list(thr), list(lev)
 
 
 def lkv_set_profiling(ctx, enable: bool) -> None:

@@ -9,6 +9,7 @@
 
 #include "../../include/lkv.h"
 #include "lkv_internal.cuh"
+#include "paris.cuh"
 
 using lkv::CtxView;
 using lkv::DecState;
@@ -32,7 +33,7 @@ struct lkv_ctx {
   std::vector<void *> dev;
   std::vector<void *> host;
   std::vector<int32_t> steps;     // decode steps taken per layer
-  std::vector<int8_t> built;      // index present per layer
+  std::vector<int8_t> built;      // index present per layer (1 clusters or pages, 2 ParisKV-style)
   std::vector<int64_t> n_tokens;  // prefill tokens per layer
   std::vector<int32_t> n_clusters;
   std::string err;
@@ -40,6 +41,7 @@ struct lkv_ctx {
   bool use_tc = true;             // tensor-core distance filter for bf16 keys
   int alloc_index = 0;
   int fail_at = -1;               // host-side allocation-failure injection
+  uint64_t paris_seed = 0;        // seed of the ParisKV-style selector's signs
 };
 
 static thread_local std::string g_create_error;
@@ -174,6 +176,7 @@ lkv_status lkv_create(const lkv_config *cfg, lkv_ctx **out) {
   lkv_status st = LKV_OK;
   CtxView &v = c->v;
   v.dtype = k.dtype;
+  v.pol_interval = 1;
   v.B = B; v.Hkv = Hkv; v.G = G; v.d = d; v.L = k.local_buf;
   v.n_cap = n_cap; v.t_cap = t_cap; v.u_cap = u_cap; v.bud_cap = k.max_budget;
   v.offload = k.offload ? 1 : 0;
@@ -317,6 +320,7 @@ lkv_status lkv_build_index(lkv_ctx *c, int32_t layer, const void *keys, const vo
                            int64_t n, int32_t nc, int32_t iters, uint64_t seed) {
   lkv_status s = check_usable(c);
   if (s != LKV_OK) return s;
+  if (c->v.paris) return fail(c, LKV_EINVAL, "the context uses the ParisKV-style selector");
   if (layer < 0 || layer >= c->cfg.n_layers) return fail(c, LKV_EINVAL, "layer out of range");
   if (!keys || !values) return fail(c, LKV_EINVAL, "null keys or values");
   if (n < 1 || n > c->cfg.max_prefill) return fail(c, LKV_EINVAL, "n_tokens outside 1..max_prefill");
@@ -336,10 +340,29 @@ lkv_status lkv_build_index(lkv_ctx *c, int32_t layer, const void *keys, const vo
   return LKV_OK;
 }
 
+lkv_status lkv_build_index_async(lkv_ctx *c, int32_t layer, const void *keys, const void *values,
+                                 int64_t n, int32_t nc, int32_t iters, uint64_t seed, void *ready_event,
+                                 void *done_event) {
+  lkv_status s = check_usable(c);
+  if (s != LKV_OK) return s;
+  if (ready_event) {
+    cudaError_t e = cudaStreamWaitEvent(c->stream, (cudaEvent_t)ready_event, 0);
+    if (e != cudaSuccess) return cuda_fail(c, e, "lkv_build_index_async: waiting for ready_event");
+  }
+  s = lkv_build_index(c, layer, keys, values, n, nc, iters, seed);
+  if (s != LKV_OK) return s;
+  if (done_event) {
+    cudaError_t e = cudaEventRecord((cudaEvent_t)done_event, c->stream);
+    if (e != cudaSuccess) return cuda_fail(c, e, "lkv_build_index_async: recording done_event");
+  }
+  return LKV_OK;
+}
+
 lkv_status lkv_load_index(lkv_ctx *c, int32_t layer, const void *keys, const void *values,
                           int64_t n, int32_t nc, const int32_t *assign, const float *cent) {
   lkv_status s = check_usable(c);
   if (s != LKV_OK) return s;
+  if (c->v.paris) return fail(c, LKV_EINVAL, "the context uses the ParisKV-style selector");
   if (layer < 0 || layer >= c->cfg.n_layers) return fail(c, LKV_EINVAL, "layer out of range");
   if (!keys || !values || !assign || !cent) return fail(c, LKV_EINVAL, "null argument");
   if (n < 1 || n > c->cfg.max_prefill) return fail(c, LKV_EINVAL, "n_tokens outside 1..max_prefill");
@@ -383,12 +406,13 @@ static lkv::StepArgs step_args(lkv_ctx *c, int32_t layer, int32_t nl, bool multi
   a.base_t = 0;
   if (multi) {
     const int64_t B = c->cfg.batch, Hkv = c->cfg.n_kv_heads, H = Hkv * c->cfg.group;
+    const int64_t Hs = c->v.pol_per_head ? H : Hkv;  // selection records per query or KV head
     const size_t es = c->cfg.dtype == LKV_DTYPE_BF16 ? 2 : 4;
     a.stride_q = B * nl * H * 128;
     a.stride_kv = B * nl * Hkv * 128;
     a.stride_out = B * nl * H * 128;
-    a.stride_sel = B * nl * Hkv * (int64_t)c->v.u_cap;
-    a.stride_nsel = B * nl * Hkv;
+    a.stride_sel = B * nl * Hs * (int64_t)c->v.u_cap;
+    a.stride_nsel = B * nl * Hs;
     a.stride_b = B * nl;
     // kernels address step t (the absolute decode position) at base + t *
     // stride; shifting every base back by the call's first position makes
@@ -504,6 +528,143 @@ lkv_status lkv_decode_steps(lkv_ctx *c, int32_t layer, int32_t nl, int32_t n_ste
   }
   if (e != cudaSuccess) return cuda_fail(c, e, "lkv_decode_steps");
   for (int l = layer; l < layer + nl; ++l) c->steps[l] += n_steps;
+  return LKV_OK;
+}
+
+lkv_status lkv_set_policy(lkv_ctx *c, const lkv_policy *p) {
+  lkv_status s = check_usable(c);
+  if (s != LKV_OK) return s;
+  if (!p) return fail(c, LKV_EINVAL, "null policy");
+  if (p->trigger < LKV_TRIGGER_ADAPTIVE || p->trigger > LKV_TRIGGER_INTERVAL)
+    return fail(c, LKV_EINVAL, "unknown trigger");
+  if (p->trigger == LKV_TRIGGER_INTERVAL && p->interval < 1) return fail(c, LKV_EINVAL, "interval must be >= 1");
+  if (p->fill != LKV_FILL_PREFIX && p->fill != LKV_FILL_SKIP) return fail(c, LKV_EINVAL, "unknown fill");
+  if (p->page < 0) return fail(c, LKV_EINVAL, "page must be >= 0");
+  if (p->per_head != 0 && p->per_head != 1) return fail(c, LKV_EINVAL, "per_head must be 0 or 1");
+  if (p->per_head && c->v.paris) return fail(c, LKV_EINVAL, "per-head selection does not apply to the ParisKV-style selector");
+  CtxView &v = c->v;
+  if (p->per_head) {
+    // the union of the heads' selections is read by the streaming attention
+    // from per-token rows in HBM, with the heads' mask in the rows' top byte
+    if (v.offload || v.need_pieces || v.S_all > lkv::kStreamMaxSlices)
+      return fail(c, LKV_EINVAL, "per-head selection needs an HBM pool, bf16, 4 or 8 query heads per KV head "
+                                 "and at most 1024 slices");
+    if (v.pool_rows >= (int64_t(1) << lkv::kRowBits))
+      return fail(c, LKV_EINVAL, "per-head selection needs max_prefill + max_steps < 2^24");
+  }
+  // the graphs captured the previous policy in their kernel arguments
+  cudaError_t e = cudaStreamSynchronize(c->stream);
+  if (e != cudaSuccess) return cuda_fail(c, e, "lkv_set_policy");
+  if (p->per_head && !v.sel_mask) {
+    // first use: the union's rows (up to G budgets), the heads' masks and counts
+    lkv_status st = LKV_OK;
+    const int64_t R = v.plan_ring;
+    const int32_t cap = (int32_t)std::min<int64_t>((int64_t)c->cfg.group * c->cfg.max_budget, v.pool_rows);
+    int32_t *rows = (int32_t *)dalloc(c, R * v.S_all * (int64_t)cap * 4, &st);
+    uint8_t *mask = (uint8_t *)dalloc(c, R * v.S_all * (int64_t)v.u_cap, &st);
+    int32_t *hn = (int32_t *)dalloc(c, R * v.S_all * lkv::kMaxGroup * 4, &st);
+    int32_t *ht = (int32_t *)dalloc(c, R * v.S_all * lkv::kMaxGroup * 4, &st);
+    if (st != LKV_OK) return st;
+    e = cudaMemsetAsync(hn, 0, R * v.S_all * lkv::kMaxGroup * 4, c->stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(ht, 0, R * v.S_all * lkv::kMaxGroup * 4, c->stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(c->stream);
+    if (e != cudaSuccess) return cuda_fail(c, e, "lkv_set_policy");
+    v.sel_rows = rows;
+    v.sel_cap = cap;
+    v.sel_mask = mask;
+    v.hsel_n = hn;
+    v.hsel_tok = ht;
+  }
+  for (GraphEntry &g : c->graphs)
+    if (g.exec) cudaGraphExecDestroy(g.exec);
+  c->graphs.clear();
+  c->v.pol_trigger = p->trigger;
+  c->v.pol_interval = p->trigger == LKV_TRIGGER_INTERVAL ? p->interval : 1;
+  c->v.pol_fill = p->fill;
+  c->v.pol_page = p->page;
+  c->v.pol_per_head = p->per_head;
+  return LKV_OK;
+}
+
+lkv_status lkv_build_pages(lkv_ctx *c, int32_t layer, const void *keys, const void *values, int64_t n,
+                           int32_t page) {
+  lkv_status s = check_usable(c);
+  if (s != LKV_OK) return s;
+  if (c->v.paris) return fail(c, LKV_EINVAL, "the context uses the ParisKV-style selector");
+  if (layer < 0 || layer >= c->cfg.n_layers) return fail(c, LKV_EINVAL, "layer out of range");
+  if (!keys || !values) return fail(c, LKV_EINVAL, "null keys or values");
+  if (n < 1 || n > c->cfg.max_prefill) return fail(c, LKV_EINVAL, "n_tokens outside 1..max_prefill");
+  if (page < 1) return fail(c, LKV_EINVAL, "page must be >= 1");
+  const int64_t nc = (n + page - 1) / page;
+  if (nc > c->cfg.max_clusters) return fail(c, LKV_EINVAL, "ceil(n_tokens / page) exceeds max_clusters");
+  cudaError_t e = lkv::launch_page_index(c->v, layer, c->ks, keys, values, n, page, c->stream, c->prof);
+  if (e != cudaSuccess) return cuda_fail(c, e, "lkv_build_pages");
+  c->built[layer] = 1;
+  c->steps[layer] = 0;
+  c->n_tokens[layer] = n;
+  c->n_clusters[layer] = (int32_t)nc;
+  return LKV_OK;
+}
+
+lkv_status lkv_paris_levels(float *thr, float *lev) {
+  if (!thr || !lev) {
+    lkv::set_unbound_error("lkv_paris_levels: null pointer");
+    return LKV_EINVAL;
+  }
+  lkv::paris_levels_host(thr, lev);
+  return LKV_OK;
+}
+
+lkv_status lkv_build_paris(lkv_ctx *c, int32_t layer, const void *keys, const void *values, int64_t n,
+                           const lkv_paris_params *p) {
+  lkv_status s = check_usable(c);
+  if (s != LKV_OK) return s;
+  CtxView &v = c->v;
+  if (layer < 0 || layer >= c->cfg.n_layers) return fail(c, LKV_EINVAL, "layer out of range");
+  if (!keys || !values || !p) return fail(c, LKV_EINVAL, "null argument");
+  if (n < 1 || n > c->cfg.max_prefill) return fail(c, LKV_EINVAL, "n_tokens outside 1..max_prefill");
+  if (p->rho < 1 || p->rho > lkv::kParisMaxRho) return fail(c, LKV_EINVAL, "rho must be 1..15");
+  if (p->n_cand < 1 || p->n_cand > lkv::kParisMaxCand) return fail(c, LKV_EINVAL, "n_cand must be 1..4096");
+  if (v.dtype != LKV_DTYPE_BF16 || v.offload || v.need_pieces || v.S_all > lkv::kStreamMaxSlices)
+    return fail(c, LKV_EINVAL, "the ParisKV-style selector needs bf16, an HBM pool, group 4 or 8 and at most "
+                               "1024 slices");
+  if ((int64_t)v.u_cap < c->cfg.max_budget)
+    return fail(c, LKV_EINVAL, "max_clusters + max_steps must be >= max_budget (selected tokens are listed)");
+  if (v.pol_per_head) return fail(c, LKV_EINVAL, "per-head selection does not apply to the ParisKV-style selector");
+  for (int l = 0; l < c->cfg.n_layers; ++l)
+    if (c->built[l] == 1) return fail(c, LKV_EINVAL, "a layer of the context was built with clusters or pages");
+  if (v.paris && (v.paris_rho != p->rho || v.paris_n_cand != p->n_cand || c->paris_seed != p->seed))
+    return fail(c, LKV_EINVAL, "rho, n_cand and seed are fixed by the context's first lkv_build_paris");
+  if (!v.paris) {
+    cudaError_t e = cudaStreamSynchronize(c->stream);
+    if (e != cudaSuccess) return cuda_fail(c, e, "lkv_build_paris");
+    lkv_status st = LKV_OK;
+    const int64_t rows = v.S_all * v.pool_rows;
+    uint8_t *bk = (uint8_t *)dalloc(c, rows * lkv::kParisSub, &st);
+    uint8_t *code = (uint8_t *)dalloc(c, rows * 64, &st);
+    float *w = (float *)dalloc(c, rows * lkv::kParisSub * 4, &st);
+    if (st != LKV_OK) return st;
+    for (GraphEntry &g : c->graphs)
+      if (g.exec) cudaGraphExecDestroy(g.exec);
+    c->graphs.clear();
+    uint64_t sm = p->seed;
+    v.paris_sign[0] = splitmix64_next(sm);
+    v.paris_sign[1] = splitmix64_next(sm);
+    lkv::paris_levels_host(v.paris_thr, v.paris_lev);
+    v.paris_rho = p->rho;
+    v.paris_n_cand = p->n_cand;
+    v.pk_bucket = bk;
+    v.pk_code = code;
+    v.pk_w = w;
+    v.paris = 1;
+    c->paris_seed = p->seed;
+  }
+  cudaError_t e = lkv::launch_paris_index(v, layer, c->ks, keys, values, n, c->stream, c->prof);
+  if (e != cudaSuccess) return cuda_fail(c, e, "lkv_build_paris");
+  c->built[layer] = 2;
+  c->steps[layer] = 0;
+  c->n_tokens[layer] = n;
+  c->n_clusters[layer] = 0;
   return LKV_OK;
 }
 

@@ -18,6 +18,7 @@
 #include <type_traits>
 
 #include "lkv_internal.cuh"
+#include "paris.cuh"
 
 namespace lkv {
 
@@ -142,6 +143,28 @@ __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// ParisKV-style selector: the metadata of the keys the chunk's steps
+// appended (a CTA per (sequence, layer) and step, a warp per KV head), after
+// the boundary kernel and before the chunk's selections.
+__global__ void __launch_bounds__(512) k_paris_append(CtxView v, StepArgs a) {
+  const int li = blockIdx.x / v.B, b = blockIdx.x % v.B;
+  const int64_t lb = (int64_t)(a.l0 + li) * v.B + b;
+  const int wid = threadIdx.x >> 5;
+  pdl_wait();
+  pdl_trigger();
+  if (wid >= v.Hkv) return;
+  const int t = v.aview[(int64_t)(a.slot + blockIdx.y) * v.n_lb + lb].x;
+  const int64_t k = t - a.base_t;
+  const uint16_t *kn = (const uint16_t *)a.k_new + k * a.stride_kv +
+                       (((int64_t)b * a.nl + li) * v.Hkv + wid) * kHeadDim;
+  const uint2 raw = __ldg(reinterpret_cast<const uint2 *>(kn) + (threadIdx.x & 31));
+  const uint16_t k4[4] = {(uint16_t)(raw.x & 0xffffu), (uint16_t)(raw.x >> 16), (uint16_t)(raw.y & 0xffffu),
+                          (uint16_t)(raw.y >> 16)};
+  const int64_t row = (lb * v.Hkv + wid) * v.pool_rows + v.n_cap + t;
+  paris_encode_warp(k4, v.paris_sign, v.paris_thr, v.paris_lev, v.pk_bucket + row * kParisSub,
+                    v.pk_code + row * 64, v.pk_w + row * kParisSub);
+}
+
 // 512 threads (64 registers each), the queries staged in their own dtype.
 constexpr int kBoundaryThreads = 512;
 constexpr int kQPitch = kHeadDim + 8;  // padded query rows in shared memory (elements)
@@ -253,7 +276,10 @@ __global__ void __launch_bounds__(kBoundaryThreads, 2) k_step_boundary(CtxView v
       for (int h = 0; h < H; ++h) r = __fadd_rn(r, cosv[h]);
       r = __fdiv_rn(r, (float)H);
       st.r = r;
-      st.flag = r < a.tau ? 1 : 0;
+      // the policy's trigger (r_t is computed and reported under every one)
+      st.flag = v.pol_trigger == kTrigEvery      ? 1
+                : v.pol_trigger == kTrigInterval ? (t % v.pol_interval == 0 ? 1 : 0)
+                                                 : (r < a.tau ? 1 : 0);
       if (st.flag) st.plan = (st.plan + 1) % v.plan_ring;  // a retrieval writes the next plan slot
     }
   } else if (tid == 0) {
@@ -263,8 +289,10 @@ __global__ void __launch_bounds__(kBoundaryThreads, 2) k_step_boundary(CtxView v
   }
   __syncthreads();
 
-  // 2. a boundary closes the open segment; token t opens the next one
-  if (st.flag && t > 0 && st.open_start < t) {
+  // 2. a boundary (with page units: a full page) closes the open segment;
+  //    token t opens the next one
+  const bool cut = v.pol_page > 0 ? t - st.open_start >= v.pol_page : st.flag != 0;
+  if (cut && t > 0 && st.open_start < t) {
     const int s0 = st.open_start;
     if (close_segment<DT>(v, st, lb, s0, t) && tid == 0) st.open_start = t;
     __syncthreads();
@@ -442,6 +470,136 @@ constexpr int kScoreWarps = kScoreThreads / 32;
 constexpr int kSelSmemUnits = 4096;  // units whose keys, lengths and rows fit in shared memory
 constexpr size_t kSelSmemBytes = (size_t)kSelSmemUnits * 12;
 
+// Length-weighted radix select of the budget cut over the units' descending
+// keys: cut->all when every unit fits; else cut->prefix = K*, the smallest
+// key with sum_{key <= K*} len > budget, and cut->below = the length of the
+// units with key < K*. Called by the whole block; whist and wt are scratch.
+struct RadixCut {
+  int32_t total, all, below;
+  uint32_t prefix, mask;
+};
+
+template <typename KeyOf, typename LenOf>
+__device__ void radix_cut(int U, int budget, KeyOf keyof, LenOf lenof, int32_t (*whist)[256], int32_t *wt,
+                          RadixCut *cut) {
+  const int tid = threadIdx.x, nth = blockDim.x, wid = tid >> 5;
+  int32_t part = 0;
+  for (int u = tid; u < U; u += nth) part += lenof(u);
+  block_scan_excl(part, wt, &cut->total);
+  if (tid == 0) {
+    cut->all = cut->total <= budget;
+    cut->prefix = 0;
+    cut->mask = 0;
+    cut->below = 0;
+  }
+  __syncthreads();
+  if (!cut->all) {
+    for (int pass = 0; pass < 4; ++pass) {
+      const int shift = 24 - 8 * pass;
+      for (int x = tid; x < kScoreWarps * 256; x += nth) (&whist[0][0])[x] = 0;
+      __syncthreads();
+      const uint32_t prefix = cut->prefix, mask = cut->mask;
+      for (int u = tid; u < U; u += nth) {
+        const uint32_t key = keyof(u);
+        if ((key & mask) == prefix) atomicAdd(&whist[wid][(key >> shift) & 255u], lenof(u));
+      }
+      __syncthreads();
+      for (int bin = tid; bin < 256; bin += nth) {
+        int32_t tot = 0;
+        for (int w = 0; w < kScoreWarps; ++w) tot += whist[w][bin];
+        whist[0][bin] = tot;
+      }
+      __syncthreads();
+      if (tid < 32) {
+        // warp scan over the 256 bins (8 per lane): the bin where the running
+        // weight first exceeds the budget
+        int32_t loc[8], sum = 0;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) { loc[e] = whist[0][tid * 8 + e]; sum += loc[e]; }
+        int32_t inc = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int32_t y = __shfl_up_sync(kFull, inc, o);
+          if (tid >= o) inc += y;
+        }
+        int found = -1;
+        int32_t run = cut->below + inc - sum;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          if (found < 0 && run + loc[e] > budget) found = e;
+          if (found < 0) run += loc[e];
+        }
+        const unsigned hit = __ballot_sync(kFull, found >= 0);
+        const int src = hit ? __ffs(hit) - 1 : 31;
+        const int digit = __shfl_sync(kFull, tid * 8 + (found >= 0 ? found : 7), src);
+        const int32_t below = __shfl_sync(kFull, run, src);
+        if (tid == 0) {
+          cut->below = below;
+          cut->prefix = prefix | ((uint32_t)digit << shift);
+          cut->mask = mask | (255u << shift);
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+// Skip-and-continue budget fill on top of the stop-at-first-misfit prefix.
+// Walking the selection order and taking every unit that still fits is the
+// same as repeatedly taking the first unit in that order (smallest key, then
+// smallest id) among the unmarked ones whose length fits what is left: a
+// unit passed over earlier did not fit a larger remainder. Units of length 0
+// always fit and are marked at once. Marks one bit per unit in `mark`.
+template <typename Prefix, typename KeyOf, typename LenOf>
+__device__ void skip_fill(int U, int budget, int u0, int u1, int32_t tie_ex, Prefix is_prefix,
+                          KeyOf keyof, LenOf lenof, uint32_t *mark, int32_t *wt) {
+  const int tid = threadIdx.x, nth = blockDim.x;
+  __shared__ unsigned long long s_best;
+  __shared__ int32_t s_left, s_tot;
+  for (int w = tid; w < (U + 31) / 32; w += nth) mark[w] = 0;
+  __syncthreads();
+  int32_t run = tie_ex, toks = 0;
+  for (int u = u0; u < u1; ++u)
+    if (is_prefix(u, run)) {
+      atomicOr(&mark[u >> 5], 1u << (u & 31));
+      toks += lenof(u);
+    }
+  block_scan_excl(toks, wt, &s_tot);  // (its barriers also publish the marks)
+  if (tid == 0) s_left = budget - s_tot;
+  __syncthreads();
+  for (int u = tid; u < U; u += nth)
+    if (lenof(u) == 0 && !((mark[u >> 5] >> (u & 31)) & 1u)) atomicOr(&mark[u >> 5], 1u << (u & 31));
+  __syncthreads();
+  for (int it = 0; it < U; ++it) {
+    const int32_t left = s_left;
+    unsigned long long best = ~0ull;
+    for (int u = tid; u < U; u += nth) {
+      const int32_t len = lenof(u);
+      if (len <= left && !((mark[u >> 5] >> (u & 31)) & 1u)) {
+        const unsigned long long c = ((unsigned long long)keyof(u) << 32) | (uint32_t)u;
+        best = c < best ? c : best;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const unsigned long long y = __shfl_xor_sync(kFull, best, o);
+      best = y < best ? y : best;
+    }
+    if (tid == 0) s_best = ~0ull;
+    __syncthreads();
+    if ((tid & 31) == 0 && best != ~0ull) atomicMin(&s_best, best);
+    __syncthreads();
+    const unsigned long long b = s_best;
+    if (b == ~0ull) break;
+    const int u = (int)(uint32_t)b;
+    if (tid == 0) {
+      mark[u >> 5] |= 1u << (u & 31);
+      s_left = left - lenof(u);
+    }
+    __syncthreads();
+  }
+}
+
 // Keys, lengths and first pool rows of the units go into shared memory in one
 // round of loads (very large unit tables stay in global memory), unless the
 // caller already put the keys there (keys_in_smem); scg: the step's scores.
@@ -467,74 +625,21 @@ __device__ void select_units(const CtxView &v, int64_t gs, int U, int budget, in
   auto rowof = [&](int u) -> int32_t { return in_smem ? row_s[u] : rwg[u]; };
   __shared__ int32_t whist[kScoreWarps][256];
   __shared__ int32_t wt[64];
-  __shared__ int32_t s_total, s_below, s_all, s_nsel, s_ntok, s_npieces;
-  __shared__ uint32_t s_prefix, s_mask;
-
-  int32_t part = 0;
-  for (int u = tid; u < U; u += nth) part += lenof(u);
-  block_scan_excl(part, wt, &s_total);
-  if (tid == 0) {
-    s_all = s_total <= budget;
-    s_prefix = 0;
-    s_mask = 0;
-    s_below = 0;
-  }
-  __syncthreads();
-  if (!s_all) {
-    for (int pass = 0; pass < 4; ++pass) {
-      const int shift = 24 - 8 * pass;
-      for (int x = tid; x < kScoreWarps * 256; x += nth) (&whist[0][0])[x] = 0;
-      __syncthreads();
-      const uint32_t prefix = s_prefix, mask = s_mask;
-      for (int u = tid; u < U; u += nth) {
-        const uint32_t key = keyof(u);
-        if ((key & mask) == prefix) atomicAdd(&whist[wid][(key >> shift) & 255u], lenof(u));
-      }
-      __syncthreads();
-      for (int bin = tid; bin < 256; bin += nth) {
-        int32_t tot = 0;
-        for (int w = 0; w < kScoreWarps; ++w) tot += whist[w][bin];
-        whist[0][bin] = tot;
-      }
-      __syncthreads();
-      if (tid < 32) {
-        // warp scan over the 256 bins (8 per lane): the bin where the running
-        // weight first exceeds the budget
-        int32_t loc[8], sum = 0;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) { loc[e] = whist[0][tid * 8 + e]; sum += loc[e]; }
-        int32_t inc = sum;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int32_t y = __shfl_up_sync(kFull, inc, o);
-          if (tid >= o) inc += y;
-        }
-        int found = -1;
-        int32_t run = s_below + inc - sum;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          if (found < 0 && run + loc[e] > budget) found = e;
-          if (found < 0) run += loc[e];
-        }
-        const unsigned hit = __ballot_sync(kFull, found >= 0);
-        const int src = hit ? __ffs(hit) - 1 : 31;
-        const int digit = __shfl_sync(kFull, tid * 8 + (found >= 0 ? found : 7), src);
-        const int32_t below = __shfl_sync(kFull, run, src);
-        if (tid == 0) {
-          s_below = below;
-          s_prefix = prefix | ((uint32_t)digit << shift);
-          s_mask = mask | (255u << shift);
-        }
-      }
-      __syncthreads();
-    }
-  }
-  const bool all = s_all != 0;
-  const uint32_t kstar = s_prefix;
-  const int32_t below = s_below;
+  __shared__ int32_t s_nsel, s_ntok, s_npieces;
+  __shared__ RadixCut rc;
+  radix_cut(U, budget, keyof, lenof, whist, wt, &rc);
+  const bool all = rc.all != 0;
+  const uint32_t kstar = rc.prefix;
+  const int32_t below = rc.below;
   const int per = (U + nth - 1) / nth;
   const int u0 = tid * per, u1 = min(U, u0 + per);
-  auto is_sel = [&](int u, int32_t &run) -> bool {
+  // skip-and-continue fill: the prefix below is extended unit by unit in
+  // shared-memory marks (up to kSelSmemUnits units)
+  __shared__ uint32_t s_mark[kSelSmemUnits / 32];
+  const bool skip = v.pol_fill == kFillSkip && !all && in_smem;
+  if (v.pol_fill == kFillSkip && !all && !in_smem && tid == 0) set_err(v.err, kErrCapacity);
+  auto marked = [&](int u) -> bool { return (s_mark[u >> 5] >> (u & 31)) & 1u; };
+  auto is_prefix = [&](int u, int32_t &run) -> bool {
     if (all) return true;
     const uint32_t key = keyof(u);
     if (key < kstar) return true;
@@ -544,12 +649,14 @@ __device__ void select_units(const CtxView &v, int64_t gs, int U, int budget, in
     }
     return false;
   };
+  auto is_sel = [&](int u, int32_t &run) -> bool { return skip ? marked(u) : is_prefix(u, run); };
   // exclusive id-order prefix of the tied units' lengths
   int32_t tl = 0;
   if (!all)
     for (int u = u0; u < u1; ++u)
       if (keyof(u) == kstar) tl += lenof(u);
   const int32_t tie_ex = block_scan_excl(tl, wt, nullptr);
+  if (skip) skip_fill(U, budget, u0, u1, tie_ex, is_prefix, keyof, lenof, s_mark, wt);
   int32_t cnt = 0, toks = 0;
   {
     int32_t run = tie_ex;
@@ -649,6 +756,374 @@ __device__ void select_units(const CtxView &v, int64_t gs, int U, int budget, in
   }
 }
 
+// Per-query-head selection, the baseline of the group-consistent one ("LouisKV
+// ... Long Input-Output Sequences", 关键设计 3 其二 and 消融实验: selecting per
+// head makes the heads of a group fetch overlapping sets). Each of the G
+// query heads of the slice scores every unit with its own query, s_u = q_h .
+// c_u (the fp32 FMA chain of the group score with q_h in place of the group
+// sum), and takes its own budget selection (prefix or skip fill, radix cut
+// as in select_units). The plan lists the union of the heads' units in id
+// order with the mask of heads that chose each, the per-head counts, and the
+// union's token rows with the mask in the top byte, from which the attention
+// masks every head's scores to its own selection. Units in shared memory only
+// (at most kSelSmemUnits; more is a capacity error). Shared memory: keys,
+// lengths and rows (kSelSmemBytes), then head masks, skip marks and the
+// radix histograms (kSelHeadSmemBytes in all).
+constexpr size_t kSelHeadSmemBytes = kSelSmemBytes + kSelSmemUnits + kSelSmemUnits / 8 +
+                                     (size_t)kScoreWarps * 256 * 4;
+
+template <int DT>
+__device__ void select_heads(const CtxView &v, int64_t gs, int U, int budget, int ps, const void *q,
+                             int64_t qoff) {
+  const int tid = threadIdx.x, nth = blockDim.x;
+  extern __shared__ __align__(16) uint32_t sel_smem[];
+  uint32_t *key_s = sel_smem;
+  int32_t *len_s = (int32_t *)(sel_smem + kSelSmemUnits);
+  int32_t *row_s = (int32_t *)(sel_smem + 2 * kSelSmemUnits);
+  uint8_t *hm = (uint8_t *)(sel_smem + 3 * kSelSmemUnits);
+  uint32_t *mark = sel_smem + 3 * kSelSmemUnits + kSelSmemUnits / 4;
+  int32_t(*whist)[256] = reinterpret_cast<int32_t(*)[256]>(mark + kSelSmemUnits / 32);
+  __shared__ int32_t wt[64];
+  __shared__ RadixCut rc;
+  __shared__ float qs[kHeadDim];
+  __shared__ int32_t s_cnt, s_tok, s_nsel, s_ntok;
+  int32_t *hn = plan_hsel_n(v, ps, gs), *ht = plan_hsel_tok(v, ps, gs);
+  if (U > kSelSmemUnits) {
+    if (tid == 0) {
+      set_err(v.err, kErrCapacity);
+      *plan_nsel(v, ps, gs) = 0;
+      *plan_ntok(v, ps, gs) = 0;
+      for (int g = 0; g < v.G; ++g) hn[g] = ht[g] = 0;
+    }
+    return;
+  }
+  const int32_t *lng = v.unit_len + gs * v.u_cap, *rwg = v.unit_row + gs * v.u_cap;
+  for (int u = tid; u < U; u += nth) {
+    len_s[u] = lng[u];
+    row_s[u] = rwg[u];
+    hm[u] = 0;
+  }
+  const int per = (U + nth - 1) / nth;
+  const int u0 = tid * per, u1 = min(U, u0 + per);
+  auto keyof = [&](int u) -> uint32_t { return key_s[u]; };
+  auto lenof = [&](int u) -> int32_t { return len_s[u]; };
+  constexpr int nvec = kHeadDim * elem_bytes<DT>() / 16;
+  const uint4 *rows = (const uint4 *)((const char *)v.cent_op + gs * v.u_cap * kHeadDim * elem_bytes<DT>());
+  for (int g = 0; g < v.G; ++g) {
+    __syncthreads();  // the previous head is done with the keys and the query
+    if (tid < kHeadDim) qs[tid] = load_elem<DT>(q, qoff + (int64_t)g * kHeadDim + tid);
+    __syncthreads();
+    for (int u = tid; u < U; u += nth) {
+      float sc = 0.f;
+#pragma unroll
+      for (int j = 0; j < nvec; ++j) {
+        const uint4 cur = __ldg(rows + (int64_t)u * nvec + j);
+        const uint32_t w[4] = {cur.x, cur.y, cur.z, cur.w};
+        if constexpr (DT == 1) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            sc = __fmaf_rn(qs[j * 8 + 2 * e], __uint_as_float(w[e] << 16), sc);
+            sc = __fmaf_rn(qs[j * 8 + 2 * e + 1], __uint_as_float(w[e] & 0xffff0000u), sc);
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) sc = __fmaf_rn(qs[j * 4 + e], __uint_as_float(w[e]), sc);
+        }
+      }
+      key_s[u] = desc_key(sc);
+    }
+    __syncthreads();
+    radix_cut(U, budget, keyof, lenof, whist, wt, &rc);
+    const bool all = rc.all != 0;
+    const uint32_t kstar = rc.prefix;
+    const int32_t below = rc.below;
+    auto is_prefix = [&](int u, int32_t &run) -> bool {
+      if (all) return true;
+      const uint32_t key = key_s[u];
+      if (key < kstar) return true;
+      if (key == kstar) {
+        run += len_s[u];
+        return below + run <= budget;
+      }
+      return false;
+    };
+    int32_t tl = 0;
+    if (!all)
+      for (int u = u0; u < u1; ++u)
+        if (key_s[u] == kstar) tl += len_s[u];
+    const int32_t tie_ex = block_scan_excl(tl, wt, nullptr);
+    const bool skip = v.pol_fill == kFillSkip && !all;
+    if (skip) skip_fill(U, budget, u0, u1, tie_ex, is_prefix, keyof, lenof, mark, wt);
+    int32_t cnt = 0, toks = 0, run = tie_ex;
+    for (int u = u0; u < u1; ++u) {
+      const bool on = skip ? ((mark[u >> 5] >> (u & 31)) & 1u) != 0 : is_prefix(u, run);
+      if (on) {
+        hm[u] |= (uint8_t)(1u << g);
+        ++cnt;
+        toks += len_s[u];
+      }
+    }
+    block_scan_excl2(cnt, toks, wt, &s_cnt, &s_tok);
+    if (tid == 0) {
+      hn[g] = s_cnt;
+      ht[g] = s_tok;
+      atomicAdd((unsigned long long *)&v.counters[kCntSelUnits], (unsigned long long)s_cnt);
+      atomicAdd((unsigned long long *)&v.counters[kCntSelTokens], (unsigned long long)s_tok);
+      if (s_tok > budget) set_err(v.err, kErrInternal);
+    }
+  }
+  __syncthreads();
+  // the union, in id order
+  int32_t cnt = 0, toks = 0;
+  for (int u = u0; u < u1; ++u)
+    if (hm[u]) {
+      ++cnt;
+      toks += len_s[u];
+    }
+  const int2 ex = block_scan_excl2(cnt, toks, wt, &s_nsel, &s_ntok);
+  int32_t *sel_out = plan_sel(v, ps, gs);
+  uint8_t *msk_out = plan_sel_mask(v, ps, gs);
+  int32_t *tok_rows = plan_sel_rows(v, ps, gs);
+  int32_t kk = ex.x, cum = ex.y;
+  for (int u = u0; u < u1; ++u) {
+    const uint32_t m = hm[u];
+    if (!m) continue;
+    sel_out[kk] = u;
+    msk_out[kk] = (uint8_t)m;
+    const int32_t len = len_s[u], row = row_s[u];
+    for (int32_t j = 0; j < len && cum + j < v.sel_cap; ++j) tok_rows[cum + j] = (row + j) | (int32_t)(m << kRowBits);
+    cum += len;
+    ++kk;
+  }
+  if (tid == 0) {
+    *plan_nsel(v, ps, gs) = s_nsel;
+    *plan_ntok(v, ps, gs) = s_ntok;
+    if (s_ntok > v.sel_cap) set_err(v.err, kErrInternal);
+  }
+}
+
+// ParisKV-style token selection of one (slice, step) (ParisKV technical
+// summary, 核心算法创新 2: a coarse collision vote, then a rerank of the
+// candidates on the compact codes). The region is every prefill token and
+// every decode token that left the local buffer. The rotated group query
+// qr = H D qbar is formed in single precision by the fast Hadamard
+// butterfly; in each subspace the rho sign patterns p with the highest
+// sim_p = sum_j +-qr_j (ties to the lower p) vote rho - r for the tokens in
+// their bucket; the n_cand tokens with the highest vote sums (ties to the
+// lower token) are reranked by est = sum_b w_b <v_b, qr_b>; the budget best
+// by (est desc, token asc) are selected. The plan lists their pool rows in
+// token order (as units and as per-token rows: every "unit" is one token).
+// Shared memory: candidate keys, pattern similarities (later the radix
+// histograms), candidate tokens, votes and the vote-sum histogram.
+constexpr size_t kSelParisSmemBytes = kSelSmemBytes + kParisSub * 256 + 256 * 4;
+
+template <int DT>
+__device__ void select_paris(const CtxView &v, int64_t lb, int64_t gs, int budget, int ps, const void *q,
+                             int64_t qoff, int win_start) {
+  const int tid = threadIdx.x, nth = blockDim.x, lane = tid & 31, wid = tid >> 5;
+  extern __shared__ __align__(16) uint32_t sel_smem[];
+  uint32_t *key_s = sel_smem;
+  float *sim = reinterpret_cast<float *>(sel_smem + kSelSmemUnits);
+  int32_t(*whist)[256] = reinterpret_cast<int32_t(*)[256]>(sel_smem + kSelSmemUnits);
+  int32_t *cand = reinterpret_cast<int32_t *>(sel_smem + 2 * kSelSmemUnits);
+  uint8_t *vote = reinterpret_cast<uint8_t *>(sel_smem + 3 * kSelSmemUnits);
+  int32_t *hist = reinterpret_cast<int32_t *>(vote + kParisSub * 256);
+  __shared__ float qr[kHeadDim], levs[8];
+  __shared__ int32_t wt[64];
+  __shared__ RadixCut rc;
+  __shared__ int32_t s_cut, s_need, s_nc, s_nsel, s_dummy;
+  const int64_t N = v.st[lb].n_prefill;  // constant since the build
+  const int64_t R = N + win_start;
+  const int rho = v.paris_rho;
+  // 1. the rotated group query
+  if (tid < kHeadDim) {
+    float acc = load_elem<DT>(q, qoff + tid);
+    for (int g = 1; g < v.G; ++g) acc = __fadd_rn(acc, load_elem<DT>(q, qoff + (int64_t)g * kHeadDim + tid));
+    qr[tid] = ((v.paris_sign[tid >> 6] >> (tid & 63)) & 1ull) ? -acc : acc;
+  }
+  if (tid < 8) levs[tid] = v.paris_lev[tid];
+  for (int x = tid; x < 256; x += nth) hist[x] = 0;
+  __syncthreads();
+  for (int h = 1; h < kHeadDim; h <<= 1) {
+    if (tid < kHeadDim / 2) {
+      const int j = (tid / h) * 2 * h + (tid % h);
+      const float a = qr[j], b = qr[j + h];
+      qr[j] = __fadd_rn(a, b);
+      qr[j + h] = __fsub_rn(a, b);
+    }
+    __syncthreads();
+  }
+  // 2. similarities of the 256 sign patterns of every subspace, then the
+  //    rho best of each (a warp per subspace, ties to the lower pattern)
+  for (int x = tid; x < kParisSub * 256; x += nth) {
+    const int b = x >> 8, p = x & 255;
+    float sacc = 0.f;
+#pragma unroll
+    for (int j = 0; j < kParisDim; ++j) {
+      const float xq = qr[b * kParisDim + j];
+      sacc = __fadd_rn(sacc, ((p >> j) & 1) ? -xq : xq);
+    }
+    sim[x] = sacc;
+    vote[x] = 0;
+  }
+  __syncthreads();
+  for (int b = wid; b < kParisSub; b += nth / 32) {
+    for (int r = 0; r < rho; ++r) {
+      float bs = -INFINITY;
+      int bp = 256;
+      for (int k = 0; k < 8; ++k) {
+        const int p = lane + 32 * k;
+        const float sp = sim[b * 256 + p];
+        if (!vote[b * 256 + p] && (sp > bs || (sp == bs && p < bp))) {
+          bs = sp;
+          bp = p;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o; o >>= 1) {
+        const float os = __shfl_xor_sync(kFull, bs, o);
+        const int op = __shfl_xor_sync(kFull, bp, o);
+        if (os > bs || (os == bs && op < bp)) {
+          bs = os;
+          bp = op;
+        }
+      }
+      if (lane == 0) vote[b * 256 + bp] = (uint8_t)(rho - r);
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+  const uint8_t *bk = v.pk_bucket + gs * v.pool_rows * kParisSub;
+  auto row_of = [&](int64_t r) -> int64_t { return r < N ? r : v.n_cap + (r - N); };
+  auto coarse = [&](int64_t r) -> int {
+    const uint4 x = __ldg(reinterpret_cast<const uint4 *>(bk + row_of(r) * kParisSub));
+    const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
+    int c = 0;
+#pragma unroll
+    for (int b = 0; b < kParisSub; ++b) c += vote[b * 256 + ((w4[b >> 2] >> (8 * (b & 3))) & 255u)];
+    return c;
+  };
+  // 3. histogram of the vote sums, the cut score and how many ties it takes
+  for (int64_t r = tid; r < R; r += nth) atomicAdd(&hist[coarse(r)], 1);
+  __syncthreads();
+  if (tid == 0) {
+    const int nc = v.paris_n_cand;
+    int cut = 0, need = 1 << 30, above = 0;
+    if (R > nc) {
+      for (int x = 255; x >= 0; --x) {
+        if (above + hist[x] >= nc) {
+          cut = x;
+          need = nc - above;
+          break;
+        }
+        above += hist[x];
+      }
+    }
+    s_cut = cut;
+    s_need = need;
+  }
+  __syncthreads();
+  // 4. the candidates in token order: every token above the cut, the first
+  //    `need` at it
+  const int64_t per = (R + nth - 1) / nth;
+  const int64_t r0 = (int64_t)tid * per, r1 = min(R, r0 + per);
+  const int cut = s_cut, need = s_need;
+  int32_t n_gt = 0, n_eq = 0;
+  for (int64_t r = r0; r < r1; ++r) {
+    const int c = coarse(r);
+    n_gt += c > cut;
+    n_eq += c == cut;
+  }
+  const int2 ex = block_scan_excl2(n_gt, n_eq, wt, &s_dummy, &s_nc);
+  const int32_t take_eq = max(0, min(n_eq, need - ex.y));
+  const int32_t c_ex = block_scan_excl(n_gt + take_eq, wt, &s_nc);
+  {
+    int32_t k = c_ex, eq_seen = 0;
+    for (int64_t r = r0; r < r1; ++r) {
+      const int c = coarse(r);
+      if (c > cut || (c == cut && eq_seen++ < take_eq)) cand[k++] = (int32_t)r;
+    }
+  }
+  __syncthreads();
+  const int nc = min(s_nc, kParisMaxCand);
+  // 5. rerank on the codes: est = sum_b w_b dot_b, dot_b = sum_j v_j qr_j
+  for (int c = tid; c < nc; c += nth) {
+    const int64_t row = gs * v.pool_rows + row_of(cand[c]);
+    const uint4 bx = __ldg(reinterpret_cast<const uint4 *>(v.pk_bucket + row * kParisSub));
+    const uint32_t bw[4] = {bx.x, bx.y, bx.z, bx.w};
+    const uint4 *cp = reinterpret_cast<const uint4 *>(v.pk_code + row * 64);
+    const float4 *wp = reinterpret_cast<const float4 *>(v.pk_w + row * kParisSub);
+    float est = 0.f;
+#pragma unroll
+    for (int b4 = 0; b4 < 4; ++b4) {
+      const uint4 cx = __ldg(cp + b4);
+      const float4 wx = __ldg(wp + b4);
+      const uint32_t cw[4] = {cx.x, cx.y, cx.z, cx.w};
+      const float ww[4] = {wx.x, wx.y, wx.z, wx.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int b = 4 * b4 + e;
+        const uint32_t bits = (bw[b >> 2] >> (8 * (b & 3))) & 255u;
+        float dot = 0.f;
+#pragma unroll
+        for (int j = 0; j < kParisDim; ++j) {
+          const float lv = levs[(cw[e] >> (4 * j)) & 15u];
+          dot = __fmaf_rn(((bits >> j) & 1u) ? -lv : lv, qr[b * kParisDim + j], dot);
+        }
+        est = __fmaf_rn(ww[e], dot, est);
+      }
+    }
+    key_s[c] = desc_key(est);
+  }
+  __syncthreads();
+  // 6. the budget best candidates (every candidate is one token)
+  auto keyof = [&](int c) -> uint32_t { return key_s[c]; };
+  auto one = [&](int) -> int32_t { return 1; };
+  radix_cut(nc, budget, keyof, one, whist, wt, &rc);
+  const bool all = rc.all != 0;
+  const uint32_t kstar = rc.prefix;
+  const int32_t below = rc.below;
+  const int cper = (nc + nth - 1) / nth;
+  const int c0 = tid * cper, c1 = min(nc, c0 + cper);
+  int32_t tl = 0;
+  if (!all)
+    for (int c = c0; c < c1; ++c) tl += key_s[c] == kstar;
+  const int32_t tie_ex = block_scan_excl(tl, wt, nullptr);
+  auto chosen = [&](int c, int32_t &run) -> bool {
+    if (all) return true;
+    const uint32_t key = key_s[c];
+    if (key < kstar) return true;
+    if (key == kstar) return below + (++run) <= budget;
+    return false;
+  };
+  int32_t cnt = 0;
+  {
+    int32_t run = tie_ex;
+    for (int c = c0; c < c1; ++c) cnt += chosen(c, run);
+  }
+  const int32_t o_ex = block_scan_excl(cnt, wt, &s_nsel);
+  {
+    int32_t run = tie_ex, k = o_ex;
+    int32_t *sel_out = plan_sel(v, ps, gs), *tok_rows = plan_sel_rows(v, ps, gs);
+    for (int c = c0; c < c1; ++c)
+      if (chosen(c, run)) {
+        const int32_t row = (int32_t)row_of(cand[c]);
+        if (k < v.u_cap) sel_out[k] = row;
+        if (k < v.sel_cap) tok_rows[k] = row;
+        ++k;
+      }
+  }
+  if (tid == 0) {
+    *plan_nsel(v, ps, gs) = s_nsel;
+    *plan_ntok(v, ps, gs) = s_nsel;
+    atomicAdd((unsigned long long *)&v.counters[kCntScoreUnits], (unsigned long long)R);
+    atomicAdd((unsigned long long *)&v.counters[kCntSelUnits], (unsigned long long)s_nsel);
+    atomicAdd((unsigned long long *)&v.counters[kCntSelTokens], (unsigned long long)s_nsel);
+    if (s_nsel > budget || s_nsel > v.sel_cap || s_nsel > v.u_cap || s_nc > kParisMaxCand)
+      set_err(v.err, kErrInternal);
+  }
+}
+
 // kScoreSplit CTAs of kScoreThreads per (seq, layer, kv head) and step. On a
 // step without retrieval the first only records the step's descriptor for
 // the attention (the plan in force and its token count). On a retrieval step
@@ -683,6 +1158,19 @@ __global__ void __launch_bounds__(kScoreThreads, 3) k_select(CtxView v, StepArgs
   __shared__ int s_last;
   const int H = v.Hkv * v.G;
   const int64_t qoff = (((int64_t)b * a.nl + li) * H + (int64_t)h * v.G) * kHeadDim;
+  if (v.paris) {  // one CTA runs the token pipeline of the slice
+    if (blockIdx.y != 0) return;
+    if constexpr (DT == 1) select_paris<DT>(v, lb, gs, a.budget, view.z, q, qoff, view.y);
+    if (tid == 0) *desc = make_int4(view.x, view.y, view.z, *plan_ntok(v, view.z, gs));
+    return;
+  }
+  if (v.pol_per_head) {  // one CTA scores and selects for every head of the slice
+    if (blockIdx.y != 0) return;
+    if (tid == 0) atomicAdd((unsigned long long *)&v.counters[kCntScoreUnits], (unsigned long long)U * v.G);
+    select_heads<DT>(v, gs, U, a.budget, view.z, q, qoff);
+    if (tid == 0) *desc = make_int4(view.x, view.y, view.z, *plan_ntok(v, view.z, gs));
+    return;
+  }
   if (tid < kHeadDim) {
     float acc = load_elem<DT>(q, qoff + tid);
     for (int g = 1; g < v.G; ++g) acc = __fadd_rn(acc, load_elem<DT>(q, qoff + (int64_t)g * kHeadDim + tid));
@@ -753,6 +1241,15 @@ __global__ void __launch_bounds__(kScoreThreads, 3) k_select_chunk(CtxView v, St
   __shared__ float qbar[kHeadDim];
   const int H = v.Hkv * v.G;
   const int64_t qoff = (((int64_t)b * a.nl + li) * H + (int64_t)h * v.G) * kHeadDim;
+  if (v.paris) {
+    if constexpr (DT == 1) select_paris<DT>(v, lb, gs, a.budget, view.z, q, qoff, view.y);
+    return;
+  }
+  if (v.pol_per_head) {
+    if (tid == 0) atomicAdd((unsigned long long *)&v.counters[kCntScoreUnits], (unsigned long long)U * v.G);
+    select_heads<DT>(v, gs, U, a.budget, view.z, q, qoff);
+    return;
+  }
   if (tid < kHeadDim) {
     float acc = load_elem<DT>(q, qoff + tid);
     for (int g = 1; g < v.G; ++g) acc = __fadd_rn(acc, load_elem<DT>(q, qoff + (int64_t)g * kHeadDim + tid));
@@ -1736,6 +2233,7 @@ __global__ void __launch_bounds__(32 * NW, MINB) k_attn_stream(CtxView v, StepAr
   __shared__ int32_t idx_w[NW][kStreamIdxWin];   // each warp's window of the token-row table
   __shared__ __align__(16) float S_w[NW][16][G];  // each warp's softmax weights of a tile
   __shared__ __align__(8) uint64_t full_w[NW][NS];  // a stage's copies have landed
+  __shared__ uint8_t hmask_w[NW][NS][16];  // per-query-head selection: heads that take each row
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int w = blockIdx.x * NW + wid;
   const int per_l = v.B * v.Hkv;
@@ -1811,14 +2309,35 @@ __global__ void __launch_bounds__(32 * NW, MINB) k_attn_stream(CtxView v, StepAr
   const int64_t k_out = t_s[sl] - a.base_t;
   // the slice's first warp reports the selection in force (it does not
   // depend on the attention)
+  const bool per_head = v.pol_per_head != 0;
   if (active && kw == 0) {
     const int ns = *plan_nsel(v, ps, gs);
-    if (a.selected_units) {
-      const int32_t *sel = plan_sel(v, ps, gs);
-      int32_t *dst = a.selected_units + k_out * a.stride_sel + so * v.u_cap;
-      for (int x = lane; x < ns; x += 32) dst[x] = sel[x];
+    const int32_t *sel = plan_sel(v, ps, gs);
+    if (!per_head) {
+      if (a.selected_units) {
+        int32_t *dst = a.selected_units + k_out * a.stride_sel + so * v.u_cap;
+        for (int x = lane; x < ns; x += 32) dst[x] = sel[x];
+      }
+      if (lane == 0 && a.n_selected) a.n_selected[k_out * a.stride_nsel + so] = ns;
+    } else {
+      // each query head's own selection: the union entries carrying its bit
+      const uint8_t *mk = plan_sel_mask(v, ps, gs);
+      const int32_t *hn = plan_hsel_n(v, ps, gs);
+      for (int g = 0; g < G; ++g) {
+        if (a.selected_units) {
+          int32_t *dst = a.selected_units + k_out * a.stride_sel + (so * G + g) * v.u_cap;
+          int base = 0;
+          for (int x0 = 0; x0 < ns; x0 += 32) {
+            const int x = x0 + lane;
+            const bool on = x < ns && ((mk[x] >> g) & 1);
+            const unsigned bal = __ballot_sync(kFull, on);
+            if (on) dst[base + __popc(bal & ((1u << lane) - 1))] = sel[x];
+            base += __popc(bal);
+          }
+        }
+        if (lane == 0 && a.n_selected) a.n_selected[k_out * a.stride_nsel + so * G + g] = hn[g];
+      }
     }
-    if (lane == 0 && a.n_selected) a.n_selected[k_out * a.stride_nsel + so] = ns;
   }
 
   // row sources: local-buffer row f and selected token j
@@ -1882,6 +2401,10 @@ __global__ void __launch_bounds__(32 * NW, MINB) k_attn_stream(CtxView v, StepAr
     uint64_t *bar = &full_w[wid][i % NS];
     int32_t row = 0;
     if (lane < nrow) row = (wt_ || !tok_rows) ? base + lane : idx[base + lane - jwin];
+    if (per_head && lane < 16) {  // the heads of each selected row (all heads for the buffer)
+      hmask_w[wid][i % NS][lane] = wt_ ? 0xffu : (uint8_t)((uint32_t)row >> kRowBits);
+      row &= kRowMask;
+    }
     const int32_t prev = __shfl_up_sync(kFull, row, 1);
     const unsigned starts = __ballot_sync(kFull, lane < nrow && (lane == 0 || row != prev + 1));
     if (nrow < 16) {  // zero the rows past the tile's end (generic proxy)
@@ -1984,6 +2507,13 @@ __global__ void __launch_bounds__(32 * NW, MINB) k_attn_stream(CtxView v, StepAr
     if (nrow < 16) {  // rows past the tile's end score -inf
       if (gq >= nrow) s[0] = s[1] = -INFINITY;
       if (gq + 8 >= nrow) s[2] = s[3] = -INFINITY;
+    }
+    if (per_head) {  // a head sees only the rows of its own selection (and the buffer)
+      const uint32_t m0 = hmask_w[wid][i % NS][gq], m1 = hmask_w[wid][i % NS][gq + 8];
+      if (!((m0 >> hb) & 1u)) s[0] = -INFINITY;
+      if (!((m0 >> (hb + 1)) & 1u)) s[1] = -INFINITY;
+      if (!((m1 >> hb) & 1u)) s[2] = -INFINITY;
+      if (!((m1 >> (hb + 1)) & 1u)) s[3] = -INFINITY;
     }
     // online softmax; rescale only when a maximum moves
     float c[2];
@@ -2343,7 +2873,7 @@ struct StreamCfg {
 };
 constexpr StreamCfg kStreamCfgs[] = {{8, 3, 1}, {4, 2, 3}, {4, 3, 2}, {8, 2, 1}};
 static int g_stream_single = 0, g_stream_pipe = 1;
-static int g_stream_pipe_div = 3;  // a pipelined launch takes 1 / this of the resident warps
+static int g_stream_pipe_div = 6;  // a pipelined launch takes 1 / this of the resident warps
 static int g_stream_blocks[4] = {1, 1, 1, 1};  // resident CTAs per SM of each configuration
 static int g_sms = 152;
 
@@ -2395,7 +2925,8 @@ static void launch_stream_c(const CtxView &v, const StepArgs &a, int slices, int
                             cudaStream_t st) {
   constexpr StreamCfg cf = kStreamCfgs[C];
   int64_t W = (int64_t)g_stream_blocks[C] * g_sms * cf.nw / (concurrent > 1 ? g_stream_pipe_div : 1);
-  const int64_t rows_cap = (int64_t)slices * ((a.budget + v.L + kStreamRowsPerWarp - 1) / kStreamRowsPerWarp);
+  const int64_t sel_max = (int64_t)(v.pol_per_head ? v.G : 1) * a.budget;  // a per-head union: up to G budgets
+  const int64_t rows_cap = (int64_t)slices * ((sel_max + v.L + kStreamRowsPerWarp - 1) / kStreamRowsPerWarp);
   if (W > rows_cap) W = rows_cap;
   if (W < slices) W = slices;
   if (W > v.w_cap) W = v.w_cap;
@@ -2452,9 +2983,10 @@ static cudaError_t prep_attn() {
     const int x = atoi(env);
     g_attn_split = (x >= 1 && x <= kAttnMaxSplit) ? x : 0;
   }
-  e = cudaFuncSetAttribute(k_select<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSelSmemBytes);
+  e = cudaFuncSetAttribute(k_select<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSelHeadSmemBytes);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(k_select_chunk<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSelSmemBytes);
+  e = cudaFuncSetAttribute(k_select_chunk<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kSelHeadSmemBytes);
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(k_step_boundary<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)(2 * kMaxHeads * kQPitch * elem_bytes<DT>()));
@@ -2485,6 +3017,7 @@ static cudaError_t decode_t(const CtxView &v, const StepArgs &a, int n_steps, cu
   prof.begin(kPBoundary, st);
   launch_pdl(k_step_boundary<DT>, dim3(a.nl * v.B), dim3(kBoundaryThreads),
              (size_t)2 * H * kQPitch * elem_bytes<DT>(), st, v, a, n_steps);
+  if (v.paris) launch_pdl(k_paris_append, dim3(a.nl * v.B, n_steps), dim3(32 * v.Hkv), 0, st, v, a);
   prof.end(st);
   // pipelined: the selection lane follows the boundary kernel, each step's
   // attention follows its selection on a side stream
@@ -2502,7 +3035,8 @@ static cudaError_t decode_t(const CtxView &v, const StepArgs &a, int n_steps, cu
     // then the steps' attentions (step i's on attn[i % kAttnStreams], so it
     // follows step i - kAttnStreams's, whose scratch slot it may share)
     prof.begin(kPSelect, ss);
-    launch_pdl(k_select_chunk<DT>, dim3(slices, n_steps), dim3(kScoreThreads), kSelSmemBytes, ss, v, a);
+    launch_pdl(k_select_chunk<DT>, dim3(slices, n_steps), dim3(kScoreThreads),
+               v.pol_per_head ? kSelHeadSmemBytes : v.paris ? kSelParisSmemBytes : kSelSmemBytes, ss, v, a);
     prof.end(ss);
     if (pipe) {
       e = cudaEventRecord(pipe->sel_done, ss);
@@ -2540,7 +3074,8 @@ static cudaError_t decode_t(const CtxView &v, const StepArgs &a, int n_steps, cu
       if (e != cudaSuccess) return e;
     }
     prof.begin(kPSelect, ss);
-    launch_pdl(k_select<DT>, dim3(slices, kScoreSplit), dim3(kScoreThreads), kSelSmemBytes, ss, v, ai);
+    launch_pdl(k_select<DT>, dim3(slices, kScoreSplit), dim3(kScoreThreads),
+               v.pol_per_head ? kSelHeadSmemBytes : v.paris ? kSelParisSmemBytes : kSelSmemBytes, ss, v, ai);
     prof.end(ss);
     if (v.offload) {
       prof.begin(kPGather, ss);

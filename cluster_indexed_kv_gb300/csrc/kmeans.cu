@@ -1200,6 +1200,8 @@ __global__ void k_reset_layer(CtxView v, int layer, int32_t c) {
       for (int p = 0; p < v.plan_ring; ++p) {  // every plan slot starts empty
         *plan_nsel(v, p, gs) = 0;
         *plan_ntok(v, p, gs) = 0;
+        if (v.hsel_n)
+          for (int g = 0; g < kMaxGroup; ++g) plan_hsel_n(v, p, gs)[g] = plan_hsel_tok(v, p, gs)[g] = 0;
       }
       for (int p = 0; p < kRing; ++p) v.attn_count[p * v.S_all + gs] = 0;
     }
@@ -1391,6 +1393,49 @@ cudaError_t launch_load_index(const CtxView &v, int layer, const KmeansScratch &
   return load_index_t<0>(v, layer, ks, keys, values, n, c, assign, cent, stream, prof);
 }
 
+// Page-mean index [CTkvr, 1.1: block-level indexes mean-pool runs of
+// consecutive tokens]: token i of every slice is in unit i / page; the units'
+// index vectors come from the same exact-sum update as a Lloyd round (every
+// page has at least one token, so none keeps a stale value).
+__global__ void k_page_assign(int64_t n, int32_t page, int64_t n_cap, int64_t gs0, int32_t *assign) {
+  const int64_t gs = gs0 + blockIdx.y;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+    assign[gs * n_cap + i] = (int32_t)(i / page);
+}
+
+template <int DT>
+static cudaError_t page_index_t(const CtxView &v, int layer, const KmeansScratch &ks, const void *keys,
+                                const void *values, int64_t n, int32_t page, cudaStream_t st, Prof &prof) {
+  const int S = v.B * v.Hkv;
+  const int64_t gs0 = (int64_t)layer * S;
+  const int c_cap = v.u_cap - v.t_cap;
+  const int32_t c = (int32_t)((n + page - 1) / page);
+  const int c_pad = (c + kTcN - 1) / kTcN * kTcN;
+  {
+    cudaError_t e = kmeans_kernel_attributes<DT>();
+    if (e != cudaSuccess) return e;
+  }
+  prof.begin(kPKmInit, st);
+  k_page_assign<<<dim3(64, S), 256, 0, st>>>(n, page, v.n_cap, gs0, v.assign);
+  prof.end(st);
+  cudaError_t e = group_and_pool<DT>(v, layer, ks, n, c, gs0, S, st, prof);
+  if (e != cudaSuccess) return e;
+  prof.begin(kPKmUpdate, st);
+  k_update<DT><<<update_grid<DT>(), kUpdThreads, 0, st>>>(keys, n, v.n_cap, c, c_cap, v.u_cap, gs0, v.perm,
+                                                         ks.count, ks.offs, v.cent32, ks.n_inexact, S);
+  prof.end(st);
+  prof.begin(kPKmOperand, st);
+  cudaMemsetAsync(ks.cstat, 0, sizeof(float) * 2 * S, st);
+  launch_prepare<DT>(v, c, c_pad, ks.c2_pitch, gs0, S, ks.c2, ks.cstat, st);
+  prof.end(st);
+  return finish_pool<DT>(v, layer, ks, keys, values, n, c, gs0, S, st, prof);
+}
+
+cudaError_t launch_page_index(const CtxView &v, int layer, const KmeansScratch &ks, const void *keys,
+                              const void *values, int64_t n, int32_t page, cudaStream_t stream, Prof &prof) {
+  if (v.dtype == 1) return page_index_t<1>(v, layer, ks, keys, values, n, page, stream, prof);
+  return page_index_t<0>(v, layer, ks, keys, values, n, page, stream, prof);
+}
 
 // ---------------------------------------------------------------- allocation-free K-means
 

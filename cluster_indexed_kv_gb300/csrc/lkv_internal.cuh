@@ -42,6 +42,7 @@ struct DecState {
   float r;             // this step's r_t
   int32_t seg_slow;    // open segment holds a value outside the exact-sum range
   int32_t plan;        // selection-plan slot (0..plan_ring-1) in force; a retrieval step advances it
+  int32_t n_prefill;   // prefill tokens (read by the ParisKV-style selector)
 };
 
 // Everything a kernel needs to find the context's data. Per-slice arrays are
@@ -102,7 +103,31 @@ struct CtxView {
   int32_t max_chunks;
   int32_t *err;               // device error bits (shared by all layers)
   int64_t *counters;          // [kCounters] work counters (see CounterId)
+  // retrieval policy (all zero: the method; see lkv_policy)
+  int32_t pol_trigger;        // 0 r_t < tau, 1 every step, 2 every pol_interval-th step
+  int32_t pol_interval;
+  int32_t pol_fill;           // 0 stop at the first unit that does not fit, 1 skip it and go on
+  int32_t pol_page;           // 0: segments close at retrieval steps; P: once they hold P tokens
+  int32_t pol_per_head;       // 1: a selection per query head (the attention reads their union)
+  // per-query-head selection only (allocated when that policy is first set):
+  uint8_t *sel_mask;          // [plan_ring][slice][u_cap] query heads that selected each listed unit
+  int32_t *hsel_n;            // [plan_ring][slice][kMaxGroup] units selected by each query head
+  int32_t *hsel_tok;          // [plan_ring][slice][kMaxGroup] their tokens
+  // ParisKV-style token selector (all layers; set by lkv_build_paris)
+  int32_t paris;              // 1: retrievals select tokens by the coarse-to-fine pipeline
+  int32_t paris_rho;          // sign centroids per subspace that vote (1..15)
+  int32_t paris_n_cand;       // candidates kept for the rerank (1..4096)
+  uint64_t paris_sign[2];     // bit j set: coordinate j of the key / query is negated
+  float paris_thr[7];         // prior thresholds on x^2
+  float paris_lev[8];         // prior bin means of |x|
+  uint8_t *pk_bucket;         // [slice][pool_rows][16] bucket (sign pattern) per subspace
+  uint8_t *pk_code;           // [slice][pool_rows][64] 3-bit magnitude levels, two per byte
+  float *pk_w;                // [slice][pool_rows][16] calibrated scale per subspace
 };
+
+// Retrieval triggers and budget fills of the policy.
+enum : int32_t { kTrigAdaptive = 0, kTrigEvery = 1, kTrigInterval = 2 };
+enum : int32_t { kFillPrefix = 0, kFillSkip = 1 };
 
 // Plan-slot views of the selection plan (plan_ring slots).
 __host__ __device__ __forceinline__ int32_t *plan_sel(const CtxView &v, int p, int64_t gs) {
@@ -117,6 +142,19 @@ __host__ __device__ __forceinline__ int32_t *plan_ntok(const CtxView &v, int p, 
 __host__ __device__ __forceinline__ int32_t *plan_sel_rows(const CtxView &v, int p, int64_t gs) {
   return v.sel_rows + ((int64_t)p * v.S_all + gs) * v.sel_cap;
 }
+__host__ __device__ __forceinline__ uint8_t *plan_sel_mask(const CtxView &v, int p, int64_t gs) {
+  return v.sel_mask + ((int64_t)p * v.S_all + gs) * v.u_cap;
+}
+__host__ __device__ __forceinline__ int32_t *plan_hsel_n(const CtxView &v, int p, int64_t gs) {
+  return v.hsel_n + ((int64_t)p * v.S_all + gs) * kMaxGroup;
+}
+__host__ __device__ __forceinline__ int32_t *plan_hsel_tok(const CtxView &v, int p, int64_t gs) {
+  return v.hsel_tok + ((int64_t)p * v.S_all + gs) * kMaxGroup;
+}
+// Per-query-head selection stores the union's token rows with the mask of
+// the heads that selected them in the top byte (pool rows stay below 2^24).
+constexpr int kRowBits = 24;
+constexpr int32_t kRowMask = (1 << kRowBits) - 1;
 __host__ __device__ __forceinline__ int4 *plan_chunk_pieces(const CtxView &v, int p, int64_t gs) {
   return v.chunk_pieces + ((int64_t)p * v.S_all + gs) * v.max_chunks * 64;
 }
@@ -269,6 +307,18 @@ cudaError_t launch_kmeans_build(const CtxView &v, int layer, const KmeansScratch
                                 const void *keys, const void *values, int64_t n,
                                 int32_t c, int32_t iters, bool use_tc,
                                 cudaStream_t stream, Prof &prof);
+// Page-mean index of one layer: unit j holds prefill tokens [j*page,
+// (j+1)*page) of every slice, its index vector the mean of their keys.
+cudaError_t launch_page_index(const CtxView &v, int layer, const KmeansScratch &ks,
+                              const void *keys, const void *values, int64_t n, int32_t page,
+                              cudaStream_t stream, Prof &prof);
+// ParisKV-style index of one layer: the pool in token order (no clusters)
+// and every prefill token's metadata.
+cudaError_t launch_paris_index(const CtxView &v, int layer, const KmeansScratch &ks,
+                               const void *keys, const void *values, int64_t n,
+                               cudaStream_t stream, Prof &prof);
+// Prior thresholds (x^2) and bin means of |x| for m = 8 (host, closed form).
+void paris_levels_host(float thr[7], float lev[8]);
 // Pool and unit table from a given assignment and fp32 centroids.
 cudaError_t launch_load_index(const CtxView &v, int layer, const KmeansScratch &ks,
                               const void *keys, const void *values, int64_t n,

@@ -107,6 +107,24 @@ lkv_status lkv_build_index(lkv_ctx *ctx, int32_t layer, const void *keys,
                            const void *values, int64_t n_tokens,
                            int32_t n_clusters, int32_t iters, uint64_t seed);
 
+/* lkv_build_index pipelined behind a producer [LouisKV notes, 关键设计 2 and
+ * 关键设计 3 其一: the clustering (and the offload of the pool) overlaps the
+ * prefill forward pass instead of blocking it]. The context's stream first
+ * waits for ready_event (a cudaEvent_t recorded by the producer once this
+ * layer's keys and values are complete, or NULL), then runs the build of
+ * lkv_build_index; done_event (a cudaEvent_t, or NULL) is recorded on the
+ * context's stream when the build has finished reading keys and values, so
+ * the producer may reuse those buffers after waiting for it. With the context
+ * on its own stream the build of layer l runs beside the producer's work on
+ * layer l + 1; builds of several layers run one after another (they share the
+ * K-means scratch). Events stay owned by the caller. Same result and errors as
+ * lkv_build_index, plus LKV_ECUDA if an event cannot be waited on or
+ * recorded. */
+lkv_status lkv_build_index_async(lkv_ctx *ctx, int32_t layer, const void *keys,
+                                 const void *values, int64_t n_tokens,
+                                 int32_t n_clusters, int32_t iters, uint64_t seed,
+                                 void *ready_event, void *done_event);
+
 /* Teacher-forced index: same as lkv_build_index but with the assignment and
  * fp32 centroids given instead of computed (for parity runs from an external
  * index). assign: device int32 [B][H_kv][n_tokens], values in [0, n_clusters);
@@ -181,6 +199,111 @@ lkv_status lkv_decode_steps(lkv_ctx *ctx, int32_t layer, int32_t n_layers,
                             const void *v_new, float tau, int32_t budget,
                             int32_t local_buf, float *out, int32_t *selected_units,
                             int32_t *n_selected, uint8_t *boundary, float *r_out);
+
+/* Retrieval policy of a context: the method itself (all fields zero, the
+ * default) or one of the baselines the pages measure it against [LouisKV
+ * notes, 研究背景与动机: earlier systems retrieve at every decode token and
+ * manage KV in fixed pages; 消融实验: adaptive vs fixed retrieval step,
+ * fine-grained vs page units, group-consistent selection]:
+ *   trigger   LKV_TRIGGER_ADAPTIVE: retrieve at t = 0 or when r_t < tau.
+ *             LKV_TRIGGER_EVERY: at every step. LKV_TRIGGER_INTERVAL: when
+ *             t % interval == 0. r_t is computed and reported (r_out) under
+ *             every trigger; tau matters only to the adaptive one.
+ *   interval  >= 1 with LKV_TRIGGER_INTERVAL, else ignored.
+ *   fill      LKV_FILL_PREFIX: units are taken in (score desc, id asc) order
+ *             until the first that does not fit. LKV_FILL_SKIP: a unit that
+ *             does not fit is skipped and the walk goes on, so every later
+ *             unit that still fits is taken (a slice with more than 4096 units
+ *             falls back to the prefix and lkv_sync reports LKV_ECAPACITY).
+ *   page      0: an output segment closes at each retrieval step (step 2 of
+ *             lkv_decode_step). P >= 1: it closes as soon as it holds P tokens
+ *             whatever the trigger (fixed pages of the output; combine with
+ *             lkv_build_pages for page units of the input).
+ *   per_head  0: group-consistent selection (one per KV head from the sum of
+ *             its query heads). 1: one selection per query head, scored with
+ *             that head's own query (s_u = q_h . c_u) and filled to the budget
+ *             on its own; each head attends its own selection and the local
+ *             buffer (the rows are read once for the union of the group's
+ *             selections). The decode outputs selected_units and n_selected
+ *             then have one record per query head: [..][H][max_clusters +
+ *             max_steps] and [..][H]. Needs an HBM pool, bf16, group 4 or 8,
+ *             at most 1024 slices, max_prefill + max_steps < 2^24 and at most
+ *             4096 units in a slice (LKV_ECAPACITY from lkv_sync beyond);
+ *             the first call with per_head = 1 allocates the per-head
+ *             records (LKV_ENOMEM).
+ * The policy applies to the decode calls that follow (graphs captured before
+ * are dropped; the call waits for the context's stream). Errors: LKV_EINVAL,
+ * LKV_ENOMEM, LKV_ECUDA. */
+enum { LKV_TRIGGER_ADAPTIVE = 0, LKV_TRIGGER_EVERY = 1, LKV_TRIGGER_INTERVAL = 2 };
+enum { LKV_FILL_PREFIX = 0, LKV_FILL_SKIP = 1 };
+typedef struct lkv_policy {
+  int32_t trigger;
+  int32_t interval;
+  int32_t fill;
+  int32_t page;
+  int32_t per_head;
+} lkv_policy;
+lkv_status lkv_set_policy(lkv_ctx *ctx, const lkv_policy *policy);
+
+/* Page-unit index for one layer, in place of lkv_build_index (the units of
+ * the page-granular baselines [CTkvr, 1.1: block indexes mean-pool runs of
+ * consecutive tokens]): unit j of every (sequence, KV head) holds prefill
+ * tokens [j*page, (j+1)*page) (the last may be shorter), its index vector the
+ * mean of their keys with the centroid arithmetic of lkv_build_index. Units:
+ * ceil(n_tokens / page), at most max_clusters. keys, values as in
+ * lkv_build_index. Resets the layer's decode state. Errors: LKV_EINVAL,
+ * LKV_ECUDA. */
+lkv_status lkv_build_pages(lkv_ctx *ctx, int32_t layer, const void *keys,
+                           const void *values, int64_t n_tokens, int32_t page);
+
+/* ParisKV-style token selector, a second workload on the same pool and
+ * attention [ParisKV technical summary, 核心算法创新 1-2]. The prefill of the
+ * layer is not clustered: its rows go to the pool in token order, and every
+ * token (prefill, and each decode token as it is appended) gets compact
+ * metadata of its key: the key, as exact integers k * 2^40 (bf16 values of
+ * magnitude 2^-33 .. 2^22), is rotated by H diag(D) (H the 128 x 128
+ * Sylvester-Hadamard matrix, D random signs from splitmix64(seed): bit j % 64
+ * of output j / 64 set means -1) and split into 16 subspaces of 8; per
+ * subspace the bucket is the sign pattern (the nearest of the 256 analytic
+ * centroids), the code holds 3 magnitude bits per coordinate (how many of the
+ * prior's 7 thresholds, lkv_paris_levels, the squared coordinate of the unit
+ * subspace direction reaches), and w = <y_b, v_b> / <v_b, v_b> / (2^40 *
+ * sqrt(128)) scales the dequantised direction v_b (signs times the prior's
+ * bin means). At a retrieval step of a (sequence, layer, KV head), over the
+ * prefill tokens and the decode tokens that left the local buffer: the
+ * group's summed query (fp32 adds in head order) is rotated by the same D
+ * and H (single-precision butterfly, strides 1, 2, ..., 64); in every
+ * subspace the rho sign patterns with the largest sum of +-q (ties to the
+ * lower pattern) give the tokens in their bucket rho, rho - 1, ..., 1 votes;
+ * the n_cand tokens with the most votes (ties to the lower token) are
+ * reranked by est = sum_b w_b <v_b, q_b> (fp32 fused multiply-adds, b and
+ * then coordinate order); the `budget` best by (est desc, token asc) are the
+ * selection, and every head of the group attends them and the local buffer.
+ * Retrieval steps, segments and the local buffer follow the context's policy
+ * as with clusters. selected_units then lists pool rows (prefill token i at
+ * row i, decode token t at max_prefill + t), ascending.
+ * keys, values: device bf16 [B][H_kv][n_tokens][d]. rho 1..15, n_cand
+ * 1..4096; the first call fixes rho, n_cand and seed for the context (a
+ * later call with others is LKV_EINVAL), allocates the metadata of every
+ * pool row (144 bytes per row, LKV_ENOMEM) and drops captured graphs. The
+ * context must be bf16, with an HBM pool, group 4 or 8, at most 1024
+ * slices, max_clusters + max_steps >= max_budget, and no layer built by
+ * lkv_build_index, lkv_build_pages or lkv_load_index (and those calls are
+ * LKV_EINVAL on it afterwards); per-query-head selection does not apply.
+ * Errors: LKV_EINVAL, LKV_ENOMEM, LKV_ECUDA. */
+typedef struct lkv_paris_params {
+  int32_t rho;
+  int32_t n_cand;
+  uint64_t seed;
+} lkv_paris_params;
+lkv_status lkv_build_paris(lkv_ctx *ctx, int32_t layer, const void *keys, const void *values,
+                           int64_t n_tokens, const lkv_paris_params *params);
+
+/* The ParisKV-style prior tables (host only, no GPU): for a coordinate x of
+ * a uniform unit vector in R^8, thr[l-1] = float(t_l^2) where P(|x| < t_l) =
+ * l / 8 (l = 1..7), and lev[l] = float(E[|x| : t_l <= |x| < t_{l+1}]) for
+ * l = 0..7 (t_0 = 0, t_8 = 1). Errors: LKV_EINVAL (null pointer). */
+lkv_status lkv_paris_levels(float *thr, float *lev);
 
 /* Which kernel screens the K-means distances before the exact settlement.
  * LKV_FILTER_TENSOR (the default): tcgen05 tensor-core tiles, used for bf16

@@ -85,3 +85,15 @@ def test_binding_fails_loudly_without_library(tmp_path):
             _lib.load(str(tmp_path / "missing.so"))
         finally:
             _lib._lib = None
+
+
+def test_paris_prior_tables_match_the_oracle(libpath):
+    """lkv_paris_levels is host-only: the library's closed-form tables equal
+    the oracle's Simpson/bisection tables bit for bit (both are the float
+    roundings of the same prior quantiles and bin means)."""
+    import numpy as np
+    import oracle
+    thr, lev = _lib.lkv_paris_levels()
+    othr, olev = oracle.paris_levels(8)
+    assert np.array_equal(np.array(thr, np.float32).view(np.uint32), othr.view(np.uint32))
+    assert np.array_equal(np.array(lev, np.float32).view(np.uint32), olev.view(np.uint32))
