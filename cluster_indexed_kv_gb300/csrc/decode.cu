@@ -773,7 +773,7 @@ constexpr size_t kSelHeadSmemBytes = kSelSmemBytes + kSelSmemUnits + kSelSmemUni
                                      (size_t)kScoreWarps * 256 * 4;
 
 template <int DT>
-__device__ void select_heads(const CtxView &v, int64_t gs, int U, int budget, int ps, const void *q,
+__device__ __noinline__ void select_heads(const CtxView &v, int64_t gs, int U, int budget, int ps, const void *q,
                              int64_t qoff) {
   const int tid = threadIdx.x, nth = blockDim.x;
   extern __shared__ __align__(16) uint32_t sel_smem[];
@@ -918,8 +918,8 @@ __device__ void select_heads(const CtxView &v, int64_t gs, int U, int budget, in
 constexpr size_t kSelParisSmemBytes = kSelSmemBytes + kParisSub * 256 + 256 * 4;
 
 template <int DT>
-__device__ void select_paris(const CtxView &v, int64_t lb, int64_t gs, int budget, int ps, const void *q,
-                             int64_t qoff, int win_start) {
+__device__ __noinline__ void select_paris(const CtxView &v, int64_t lb, int64_t gs, int budget, int ps, int slot,
+                             const void *q, int64_t qoff, int win_start) {
   const int tid = threadIdx.x, nth = blockDim.x, lane = tid & 31, wid = tid >> 5;
   extern __shared__ __align__(16) uint32_t sel_smem[];
   uint32_t *key_s = sel_smem;
@@ -1003,8 +1003,35 @@ __device__ void select_paris(const CtxView &v, int64_t lb, int64_t gs, int budge
     for (int b = 0; b < kParisSub; ++b) c += vote[b * 256 + ((w4[b >> 2] >> (8 * (b & 3))) & 255u)];
     return c;
   };
-  // 3. histogram of the vote sums, the cut score and how many ties it takes
-  for (int64_t r = tid; r < R; r += nth) atomicAdd(&hist[coarse(r)], 1);
+  // 3. every region token's vote sum, kept as a byte in the step slot's
+  //    scratch; their histogram (per warp, then summed); the cut score and
+  //    how many ties it takes
+  uint8_t *sc = v.pk_score + ((int64_t)slot * v.S_all + gs) * v.pool_rows;
+  for (int x = tid; x < kScoreWarps * 256; x += nth) (&whist[0][0])[x] = 0;
+  __syncthreads();
+  {
+    constexpr int kU = 4;  // tokens in flight per thread
+    for (int64_t r0_ = (int64_t)tid; r0_ < R; r0_ += (int64_t)kU * nth) {
+      int c[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int64_t r = r0_ + (int64_t)u * nth;
+        c[u] = r < R ? coarse(r) : -1;
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u)
+        if (c[u] >= 0) {
+          sc[r0_ + (int64_t)u * nth] = (uint8_t)c[u];
+          atomicAdd(&whist[wid][c[u]], 1);
+        }
+    }
+  }
+  __syncthreads();
+  for (int x = tid; x < 256; x += nth) {
+    int32_t tot = 0;
+    for (int w = 0; w < kScoreWarps; ++w) tot += whist[w][x];
+    hist[x] = tot;
+  }
   __syncthreads();
   if (tid == 0) {
     const int nc = v.paris_n_cand;
@@ -1030,7 +1057,7 @@ __device__ void select_paris(const CtxView &v, int64_t lb, int64_t gs, int budge
   const int cut = s_cut, need = s_need;
   int32_t n_gt = 0, n_eq = 0;
   for (int64_t r = r0; r < r1; ++r) {
-    const int c = coarse(r);
+    const int c = sc[r];
     n_gt += c > cut;
     n_eq += c == cut;
   }
@@ -1040,7 +1067,7 @@ __device__ void select_paris(const CtxView &v, int64_t lb, int64_t gs, int budge
   {
     int32_t k = c_ex, eq_seen = 0;
     for (int64_t r = r0; r < r1; ++r) {
-      const int c = coarse(r);
+      const int c = sc[r];
       if (c > cut || (c == cut && eq_seen++ < take_eq)) cand[k++] = (int32_t)r;
     }
   }
@@ -1160,7 +1187,7 @@ __global__ void __launch_bounds__(kScoreThreads, 3) k_select(CtxView v, StepArgs
   const int64_t qoff = (((int64_t)b * a.nl + li) * H + (int64_t)h * v.G) * kHeadDim;
   if (v.paris) {  // one CTA runs the token pipeline of the slice
     if (blockIdx.y != 0) return;
-    if constexpr (DT == 1) select_paris<DT>(v, lb, gs, a.budget, view.z, q, qoff, view.y);
+    if constexpr (DT == 1) select_paris<DT>(v, lb, gs, a.budget, view.z, a.slot, q, qoff, view.y);
     if (tid == 0) *desc = make_int4(view.x, view.y, view.z, *plan_ntok(v, view.z, gs));
     return;
   }
@@ -1242,7 +1269,7 @@ __global__ void __launch_bounds__(kScoreThreads, 3) k_select_chunk(CtxView v, St
   const int H = v.Hkv * v.G;
   const int64_t qoff = (((int64_t)b * a.nl + li) * H + (int64_t)h * v.G) * kHeadDim;
   if (v.paris) {
-    if constexpr (DT == 1) select_paris<DT>(v, lb, gs, a.budget, view.z, q, qoff, view.y);
+    if constexpr (DT == 1) select_paris<DT>(v, lb, gs, a.budget, view.z, slot, q, qoff, view.y);
     return;
   }
   if (v.pol_per_head) {

@@ -123,6 +123,7 @@ struct CtxView {
   uint8_t *pk_bucket;         // [slice][pool_rows][16] bucket (sign pattern) per subspace
   uint8_t *pk_code;           // [slice][pool_rows][64] 3-bit magnitude levels, two per byte
   float *pk_w;                // [slice][pool_rows][16] calibrated scale per subspace
+  uint8_t *pk_score;          // [kSlots][slice][pool_rows] vote sums of a step's region tokens
 };
 
 // Retrieval triggers and budget fills of the policy.

@@ -285,7 +285,8 @@ lkv_status lkv_build_pages(lkv_ctx *ctx, int32_t layer, const void *keys,
  * keys, values: device bf16 [B][H_kv][n_tokens][d]. rho 1..15, n_cand
  * 1..4096; the first call fixes rho, n_cand and seed for the context (a
  * later call with others is LKV_EINVAL), allocates the metadata of every
- * pool row (144 bytes per row, LKV_ENOMEM) and drops captured graphs. The
+ * pool row (144 bytes per row) and the vote scratch of the 128 step slots
+ * (128 bytes per row) (LKV_ENOMEM), and drops captured graphs. The
  * context must be bf16, with an HBM pool, group 4 or 8, at most 1024
  * slices, max_clusters + max_steps >= max_budget, and no layer built by
  * lkv_build_index, lkv_build_pages or lkv_load_index (and those calls are
