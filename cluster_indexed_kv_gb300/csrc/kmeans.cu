@@ -497,6 +497,26 @@ __device__ __forceinline__ Top3 top3_union(const Top3 &a, const Top3 &b) {
   return r;
 }
 
+// 16 columns of the thread's TMEM lane, without waiting for them: the
+// registers are valid after tc_wait_ld16 on the same array, which names them
+// as read-write operands so that the compiler cannot use them earlier.
+__device__ __forceinline__ void tmem_ld16_async(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tc_wait_ld16(uint32_t (&r)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                 "+r"(r[15])
+               :
+               : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
@@ -629,34 +649,48 @@ k_assign_tc(const __grid_constant__ CUtensorMap keys_map, const __grid_constant_
       const float4 *c2s = (const float4 *)(c2 + (int64_t)sl * c2_pitch + qtr * 64);
       for (int ch = 0; ch < nch; ++ch, ++gc) {
         const int ti = gc & 1;
-        float p1 = INFINITY, p2 = INFINITY;  // the two smallest of this chunk's 64 columns
+        // the two smallest of this chunk's 64 columns, in two independent
+        // streams (even and odd value pairs) so that consecutive min/max
+        // operations do not wait on one another; the columns come in four
+        // groups of 16, the TMEM load of the next group in flight while the
+        // current one is reduced
+        float p1a = INFINITY, p2a = INFINITY, p1b = INFINITY, p2b = INFINITY;
+        uint32_t ra[16], rb[16];
+        if (!abort_s) tc_wait(&acc_full[ti], (gc >> 1) & 1, &abort_s);
+        __syncwarp();
+        tc_fence_after();
+        const uint32_t tacc = tbase + ti * kTcN;
+        tmem_ld16_async(tacc, ra);
+        auto group = [&](const uint32_t(&r)[16], int g) {
+          // |c|^2 of the 16 columns (FLT_MAX past the last cluster)
+          float4 cc[4];
 #pragma unroll
-        for (int g = 0; g < 2; ++g) {
-          // |c|^2 of the 32 columns (FLT_MAX past the last cluster), requested
-          // before the accumulator wait so the two latencies overlap
-          float4 cc[8];
+          for (int e = 0; e < 4; ++e) cc[e] = __ldg(c2s + ch * (kTcN / 4) + g * 4 + e);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) cc[e] = __ldg(c2s + ch * (kTcN / 4) + g * 8 + e);
-          if (g == 0) {
-            if (!abort_s) tc_wait(&acc_full[ti], (gc >> 1) & 1, &abort_s);
-            __syncwarp();
-            tc_fence_after();
-          }
-          uint32_t r[32];
-          tmem_ld32(tbase + ti * kTcN + g * 32, r);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
+          for (int e = 0; e < 4; ++e) {
             const float2 lo = fma2(make_float2(-2.f, -2.f),
                                    make_float2(__uint_as_float(r[4 * e]), __uint_as_float(r[4 * e + 1])),
                                    make_float2(cc[e].x, cc[e].y));
             const float2 hi = fma2(make_float2(-2.f, -2.f),
                                    make_float2(__uint_as_float(r[4 * e + 2]), __uint_as_float(r[4 * e + 3])),
                                    make_float2(cc[e].z, cc[e].w));
-            const uint32_t l0 = g * 32 + 4 * e;
-            top2_pair(p1, p2, pack6_mul(lo.x, l0, m26, m64), pack6_mul(lo.y, l0 + 1, m26, m64));
-            top2_pair(p1, p2, pack6_mul(hi.x, l0 + 2, m26, m64), pack6_mul(hi.y, l0 + 3, m26, m64));
+            const uint32_t l0 = g * 16 + 4 * e;
+            top2_pair(p1a, p2a, pack6_mul(lo.x, l0, m26, m64), pack6_mul(lo.y, l0 + 1, m26, m64));
+            top2_pair(p1b, p2b, pack6_mul(hi.x, l0 + 2, m26, m64), pack6_mul(hi.y, l0 + 3, m26, m64));
           }
-        }
+        };
+        tc_wait_ld16(ra);
+        tmem_ld16_async(tacc + 16, rb);
+        group(ra, 0);
+        tc_wait_ld16(rb);
+        tmem_ld16_async(tacc + 32, ra);
+        group(rb, 1);
+        tc_wait_ld16(ra);
+        tmem_ld16_async(tacc + 48, rb);
+        group(ra, 2);
+        tc_wait_ld16(rb);
+        group(rb, 3);
+        const float p1 = fminf(p1a, p1b), p2 = min3f(fmaxf(p1a, p1b), p2a, p2b);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) tc_arrive(&acc_empty[ti]);
