@@ -267,6 +267,18 @@ def attn_roofline(kern, ctr, w, eb):
     return n_attn, ms_attn, alg, sec, alg / sec / 1e9
 
 
+def graph_attention(ctr, w, eb, dec_ms, hbm_peak):
+    """The attention's algorithmic bytes over the whole timed decode (device
+    row counters of every step, so the filling of the local buffer is
+    counted as it happened) divided by the timed decode time: the rate at
+    which the decode graph, with its attentions overlapping, reads K/V rows."""
+    b = ctr["attn_rows"] * 2 * 128 * eb + ctr["attn_slices"] * w.group * 128 * (eb + 4)
+    a = b / (dec_ms / 1e3) / 1e9
+    return {"bound": "hbm", "achieved": a, "peak": hbm_peak, "unit": "GB/s", "frac": a / hbm_peak,
+            "alg_bytes": b, "note": "all timed bench steps; the selection and boundary kernels' "
+                                    "own traffic comes on top"}
+
+
 def selection_rooflines(kern, ctr, w, eb, hbm_peak, peak_kind):
     """HBM roofline of the scoring + selection kernel from a profiled pass in
     which every slice retrieves. Per slice it reads one centroid-operand row
@@ -346,7 +358,7 @@ def run_ours(args, rank, world, local):
         torch.distributed.barrier()
     wall = time.perf_counter() - t_wall
     clk = clocks.stop()
-    kern, _ = ctx.profile(reset=True)
+    kern, ctr_timed = ctx.profile(reset=True)
     launches = int(sum(v[0] for v in kern.values()))
     trig = float(bnd.float().mean().item())
     st = ctx.decode_state(0, 0)
@@ -394,6 +406,24 @@ def run_ours(args, rank, world, local):
         ctx.set_profiling(False)
         sel_lane = selection_rooflines(kern_s, ctr_s, w, eb, hbm_peak, peak_kind)
         sel_lane["steps"] = f"decode steps {t0}..{t0 + sel_T - 1}, tau 2.0 (every slice retrieves)"
+        # the chunked selection that the decode graph runs: one launch scores
+        # and selects the retrievals of 64 steps side by side
+        t1 = t0 + sel_T
+        if t1 + 128 <= T:
+            ctx.set_profiling(True)
+            ctx.profile(reset=True)
+            ctx.decode_steps(0, q[t1:t1 + 128], kn[t1:t1 + 128], vn[t1:t1 + 128], 2.0, w.budget,
+                             out[t1:t1 + 128], n_layers=NL)
+            kern_c, ctr_c = ctx.profile(reset=True)
+            ctx.set_profiling(False)
+            ch = selection_rooflines(kern_c, ctr_c, w, eb, hbm_peak, peak_kind)["k_select"]
+            ch["kernel"] = "k_select_chunk"
+            ch["us_per_step"] = ch["avg_launch_us"] / 64
+            ch["note"] = ("64 steps per launch, every slice retrieving at every step, no L2 flush "
+                          "inside the launch: the steps of a chunk score the same centroid table, "
+                          "so most of its rows come from L2")
+            sel_lane["k_select_chunk"] = ch
+            sel_lane["chunk_steps"] = f"decode steps {t1}..{t1 + 127}, tau 2.0, profiled chunk launches"
 
     # ---- K-means distance contraction on the tensor cores: one build with
     # CUDA events around every kernel (L2 overwritten first; the keys, 537 MB,
@@ -436,6 +466,7 @@ def run_ours(args, rank, world, local):
             "peak_source": f"{peak_kind} bf16_tflops (cuBLAS burst)",
             "flops_per_launch": km_flops, "avg_launch_us": km_s * 1e6, "launches": int(n_km)},
         "roofline_selection_lane": sel_lane,
+        "graph_attention": graph_attention(ctr_timed, w, eb, dec_ms, hbm_peak),
         "kernel_breakdown_us": breakdown,
         "build_breakdown_us": build_breakdown,
         "gpu_launches": launches,

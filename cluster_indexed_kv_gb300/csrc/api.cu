@@ -508,23 +508,38 @@ lkv_status lkv_decode_steps(lkv_ctx *c, int32_t layer, int32_t nl, int32_t n_ste
   lkv::StepArgs a = step_args(c, layer, nl, true, q, k_new, v_new, tau, budget, out,
                               selected_units, n_selected, boundary, r_out);
   cudaError_t e = cudaSuccess;
-  constexpr int kGraphSteps = lkv::kSlots;  // one captured graph: two boundary chunks
-  if (c->prof.timing || n_steps < kGraphSteps) {
+  if (c->prof.timing && c->v.chunk_sel) {
+    // profiled: the graph's kernels (a boundary and a selection launch per
+    // chunk of steps, then the steps' attentions) one after another on the
+    // context stream, each bracketed by events
+    for (int i = 0; i < n_steps && e == cudaSuccess; i += lkv::kChunk) {
+      lkv::StepArgs ai = a;
+      ai.slot = 0;
+      e = lkv::launch_decode_steps(c->v, ai, std::min(lkv::kChunk, n_steps - i), c->stream, c->prof);
+    }
+  } else if (c->prof.timing) {
     for (int i = 0; i < n_steps && e == cudaSuccess; ++i) e = lkv::launch_decode_steps(c->v, a, 1, c->stream, c->prof);
   } else {
-    cudaGraphExec_t exec = nullptr;
-    e = step_graph(c, a, kGraphSteps, &exec);
-    const int reps = n_steps / kGraphSteps, tail = n_steps % kGraphSteps;
-    for (int r = 0; r < reps && e == cudaSuccess; ++r) e = cudaGraphLaunch(exec, c->stream);
-    if (e == cudaSuccess && c->prof.counting) {
-      // per graph: a boundary launch per chunk; selection, attention (and the
-      // offload gather) per step
-      c->prof.launches[lkv::kPBoundary] += (int64_t)reps * (kGraphSteps / lkv::kChunk);
-      c->prof.launches[lkv::kPSelect] += (int64_t)reps * (c->v.chunk_sel ? kGraphSteps / lkv::kChunk : kGraphSteps);
-      c->prof.launches[lkv::kPAttn] += (int64_t)reps * kGraphSteps;
-      if (c->v.offload) c->prof.launches[lkv::kPGather] += (int64_t)reps * kGraphSteps;
+    // captured graphs of 128 steps (two boundary chunks), then one of 64 for
+    // what is left of at least 64, then single steps
+    int done = 0;
+    for (const int gl : {lkv::kSlots, lkv::kChunk}) {
+      const int reps = (n_steps - done) / gl;
+      if (reps == 0 || e != cudaSuccess) continue;
+      cudaGraphExec_t exec = nullptr;
+      e = step_graph(c, a, gl, &exec);
+      for (int r = 0; r < reps && e == cudaSuccess; ++r) e = cudaGraphLaunch(exec, c->stream);
+      if (e == cudaSuccess && c->prof.counting) {
+        // per graph: a boundary launch per chunk; selection (per chunk or per
+        // step), attention and the offload gather per step
+        c->prof.launches[lkv::kPBoundary] += (int64_t)reps * (gl / lkv::kChunk);
+        c->prof.launches[lkv::kPSelect] += (int64_t)reps * (c->v.chunk_sel ? gl / lkv::kChunk : gl);
+        c->prof.launches[lkv::kPAttn] += (int64_t)reps * gl;
+        if (c->v.offload) c->prof.launches[lkv::kPGather] += (int64_t)reps * gl;
+      }
+      done += reps * gl;
     }
-    for (int i = 0; i < tail && e == cudaSuccess; ++i) e = lkv::launch_decode_steps(c->v, a, 1, c->stream, c->prof);
+    for (int i = done; i < n_steps && e == cudaSuccess; ++i) e = lkv::launch_decode_steps(c->v, a, 1, c->stream, c->prof);
   }
   if (e != cudaSuccess) return cuda_fail(c, e, "lkv_decode_steps");
   for (int l = layer; l < layer + nl; ++l) c->steps[l] += n_steps;

@@ -182,17 +182,23 @@ lkv_status lkv_decode_step(lkv_ctx *ctx, int32_t layer, int32_t n_layers,
  *   out [n_steps][B][n_layers][H][d], selected_units
  *   [n_steps][B][n_layers][H_kv][max_clusters + max_steps], n_selected
  *   [n_steps][B][n_layers][H_kv], boundary and r_out [n_steps][B][n_layers].
- * The steps run from a captured CUDA graph of 128 steps (cached per argument
- * set), so the host issues one launch per 128 steps; the steps left over run
- * one at a time. Inside the graph one kernel runs the boundary tests and
+ * The steps run from captured CUDA graphs of 128 steps, then one of 64 for
+ * a remainder of at least 64 (cached per argument set), so the host issues
+ * one launch per 128 steps; fewer than 64 left over run one at a time. Inside the graph one kernel runs the boundary tests and
  * segment bookkeeping of 64 steps at a time (they depend on the inputs
- * only), and the attention of a step runs concurrently with the selections
- * of up to 22 following steps (they never read what it writes);
- * the boundary flags, r_t and selections are those of lkv_decode_step, and
- * the attention outputs agree with it within fp32 rounding (the grid over
- * which a slice's partial softmax sums are split can differ). With profiling
- * enabled (lkv_set_profiling) the steps are launched one kernel at a time
- * instead. All layers of the call must have taken the same number of steps
+ * only); then, for an HBM pool (bf16, 4 or 8 query heads per KV head, at
+ * most 1024 slices), one kernel scores and selects every retrieval of those
+ * 64 steps side by side, and each step's attention runs on one of 16 side
+ * streams, overlapping the attentions of other steps and the next chunk's
+ * boundary and selection work (otherwise each step's selection runs on its
+ * own, as in lkv_decode_step). The boundary flags, r_t and selections are
+ * those of lkv_decode_step, and the attention outputs agree with it within
+ * fp32 rounding (the split of a slice's rows over warps can differ). With
+ * profiling enabled (lkv_set_profiling) the same kernels are launched one
+ * after another on the context's stream (a boundary and a selection launch
+ * per 64 steps where the chunked selection applies, else per step), each
+ * bracketed by CUDA events. All layers of the call must have taken the same
+ * number of steps
  * (LKV_EINVAL). Errors as lkv_decode_step. */
 lkv_status lkv_decode_steps(lkv_ctx *ctx, int32_t layer, int32_t n_layers,
                             int32_t n_steps, const void *q, const void *k_new,
