@@ -183,6 +183,11 @@ def oracle_kmeans_sample(keys_bits, c, n_keys):
     return time.perf_counter() - t0
 
 
+# Arm "CPU part" numbers of /proc/cpuinfo (implementer 0x41) that name a core
+_ARM_PARTS = {"0xd4f": "Arm Neoverse-V2", "0xd40": "Arm Neoverse-V1", "0xd0c": "Arm Neoverse-N1",
+              "0xd49": "Arm Neoverse-N2"}
+
+
 def host_cpu():
     """(logical CPUs, CPU model) of this host."""
     model = None
@@ -192,6 +197,8 @@ def host_cpu():
                 k, _, v = line.partition(":")
                 if k.strip() in ("model name", "Model", "CPU part") and v.strip():
                     model = v.strip()
+                    if k.strip() == "CPU part" and model in _ARM_PARTS:
+                        model = f"{_ARM_PARTS[model]} (CPU part {model})"
                     if k.strip() == "model name":
                         break
     except OSError:
