@@ -658,7 +658,8 @@ lkv_status lkv_build_paris(lkv_ctx *c, int32_t layer, const void *keys, const vo
     uint8_t *bk = (uint8_t *)dalloc(c, rows * lkv::kParisSub, &st);
     uint8_t *code = (uint8_t *)dalloc(c, rows * 64, &st);
     float *w = (float *)dalloc(c, rows * lkv::kParisSub * 4, &st);
-    uint8_t *score = (uint8_t *)dalloc(c, (int64_t)lkv::kSlots * rows, &st);
+    const int64_t pitch = (v.pool_rows + 15) / 16 * 16;
+    uint8_t *score = (uint8_t *)dalloc(c, (int64_t)lkv::kSlots * v.S_all * pitch, &st);
     if (st != LKV_OK) return st;
     for (GraphEntry &g : c->graphs)
       if (g.exec) cudaGraphExecDestroy(g.exec);
@@ -673,6 +674,7 @@ lkv_status lkv_build_paris(lkv_ctx *c, int32_t layer, const void *keys, const vo
     v.pk_code = code;
     v.pk_w = w;
     v.pk_score = score;
+    v.pk_pitch = pitch;
     v.paris = 1;
     c->paris_seed = p->seed;
   }

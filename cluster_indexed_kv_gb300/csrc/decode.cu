@@ -1006,11 +1006,11 @@ __device__ __noinline__ void select_paris(const CtxView &v, int64_t lb, int64_t 
   // 3. every region token's vote sum, kept as a byte in the step slot's
   //    scratch; their histogram (per warp, then summed); the cut score and
   //    how many ties it takes
-  uint8_t *sc = v.pk_score + ((int64_t)slot * v.S_all + gs) * v.pool_rows;
+  uint8_t *sc = v.pk_score + ((int64_t)slot * v.S_all + gs) * v.pk_pitch;
   for (int x = tid; x < kScoreWarps * 256; x += nth) (&whist[0][0])[x] = 0;
   __syncthreads();
   {
-    constexpr int kU = 4;  // tokens in flight per thread
+    constexpr int kU = 8;  // tokens in flight per thread
     for (int64_t r0_ = (int64_t)tid; r0_ < R; r0_ += (int64_t)kU * nth) {
       int c[kU];
 #pragma unroll
@@ -1052,23 +1052,39 @@ __device__ __noinline__ void select_paris(const CtxView &v, int64_t lb, int64_t 
   __syncthreads();
   // 4. the candidates in token order: every token above the cut, the first
   //    `need` at it
-  const int64_t per = (R + nth - 1) / nth;
-  const int64_t r0 = (int64_t)tid * per, r1 = min(R, r0 + per);
+  //    (a thread's range is a whole number of 16-byte words of the vote
+  //    bytes, read one word at a time; the scratch row pitch is a multiple
+  //    of 16, so a word past R stays inside the row)
+  const int64_t per = ((R + nth - 1) / nth + 15) / 16 * 16;
+  const int64_t r0 = min(R, (int64_t)tid * per), r1 = min(R, r0 + per);
   const int cut = s_cut, need = s_need;
+  auto vote_byte = [](const uint4 &x, int b) -> int {
+    const uint32_t wv = b < 8 ? (b < 4 ? x.x : x.y) : (b < 12 ? x.z : x.w);
+    return (int)((wv >> (8 * (b & 3))) & 255u);
+  };
   int32_t n_gt = 0, n_eq = 0;
-  for (int64_t r = r0; r < r1; ++r) {
-    const int c = sc[r];
-    n_gt += c > cut;
-    n_eq += c == cut;
+  for (int64_t r = r0; r < r1; r += 16) {
+    const uint4 x = *reinterpret_cast<const uint4 *>(sc + r);
+#pragma unroll
+    for (int b = 0; b < 16; ++b) {
+      const int c = vote_byte(x, b);
+      const bool in = r + b < r1;
+      n_gt += in && c > cut;
+      n_eq += in && c == cut;
+    }
   }
   const int2 ex = block_scan_excl2(n_gt, n_eq, wt, &s_dummy, &s_nc);
   const int32_t take_eq = max(0, min(n_eq, need - ex.y));
   const int32_t c_ex = block_scan_excl(n_gt + take_eq, wt, &s_nc);
   {
     int32_t k = c_ex, eq_seen = 0;
-    for (int64_t r = r0; r < r1; ++r) {
-      const int c = sc[r];
-      if (c > cut || (c == cut && eq_seen++ < take_eq)) cand[k++] = (int32_t)r;
+    for (int64_t r = r0; r < r1; r += 16) {
+      const uint4 x = *reinterpret_cast<const uint4 *>(sc + r);
+#pragma unroll
+      for (int b = 0; b < 16; ++b) {
+        const int c = vote_byte(x, b);
+        if (r + b < r1 && (c > cut || (c == cut && eq_seen++ < take_eq))) cand[k++] = (int32_t)(r + b);
+      }
     }
   }
   __syncthreads();

@@ -123,7 +123,8 @@ struct CtxView {
   uint8_t *pk_bucket;         // [slice][pool_rows][16] bucket (sign pattern) per subspace
   uint8_t *pk_code;           // [slice][pool_rows][64] 3-bit magnitude levels, two per byte
   float *pk_w;                // [slice][pool_rows][16] calibrated scale per subspace
-  uint8_t *pk_score;          // [kSlots][slice][pool_rows] vote sums of a step's region tokens
+  uint8_t *pk_score;          // [kSlots][slice][pk_pitch] vote sums of a step's region tokens
+  int64_t pk_pitch;           // pool_rows rounded up to a multiple of 16
 };
 
 // Retrieval triggers and budget fills of the policy.
