@@ -399,15 +399,24 @@ static int hadamard_sign(int32_t i, int32_t j) {
   return par ? -1 : 1;
 }
 
-void lkvo_paris_encode(const uint16_t *key, int32_t d, const int8_t *sign, int32_t m,
-                       const float *thr, const float *lev, uint8_t *bucket_out,
-                       uint8_t *level_out, float *w_out) {
+/* the rotation's signs H_ij D_j, [d][d] */
+static int8_t *paris_matrix(int32_t d, const int8_t *sign) {
+  int8_t *hd = (int8_t *)malloc((size_t)d * d);
+  if (!hd) return NULL;
+  for (int32_t i = 0; i < d; ++i)
+    for (int32_t j = 0; j < d; ++j) hd[(size_t)i * d + j] = (int8_t)(hadamard_sign(i, j) * sign[j]);
+  return hd;
+}
+
+static void paris_encode_hd(const uint16_t *key, int32_t d, const int8_t *hd, int32_t m,
+                            const float *thr, const float *lev, uint8_t *bucket_out,
+                            uint8_t *level_out, float *w_out) {
   int64_t *k40 = (int64_t *)malloc((size_t)d * sizeof *k40);
   int64_t *y = (int64_t *)malloc((size_t)d * sizeof *y);
   for (int32_t j = 0; j < d; ++j) k40[j] = (int64_t)((double)lkvo_bf16_to_f32(key[j]) * 0x1p40);
   for (int32_t i = 0; i < d; ++i) {
     int64_t acc = 0;
-    for (int32_t j = 0; j < d; ++j) acc += (int64_t)(hadamard_sign(i, j) * sign[j]) * k40[j];
+    for (int32_t j = 0; j < d; ++j) acc += (int64_t)hd[(size_t)i * d + j] * k40[j];
     y[i] = acc;
   }
   for (int32_t b = 0; b < d / m; ++b) {
@@ -436,6 +445,15 @@ void lkvo_paris_encode(const uint16_t *key, int32_t d, const int8_t *sign, int32
   free(y);
 }
 
+void lkvo_paris_encode(const uint16_t *key, int32_t d, const int8_t *sign, int32_t m,
+                       const float *thr, const float *lev, uint8_t *bucket_out,
+                       uint8_t *level_out, float *w_out) {
+  int8_t *hd = paris_matrix(d, sign);
+  if (!hd) return;
+  paris_encode_hd(key, d, hd, m, thr, lev, bucket_out, level_out, w_out);
+  free(hd);
+}
+
 void lkvo_paris_rotate_query(const void *q, int dtype, int32_t g, int32_t d,
                              const int8_t *sign, float *qrot_out) {
   for (int32_t j = 0; j < d; ++j) {
@@ -452,12 +470,18 @@ void lkvo_paris_rotate_query(const void *q, int dtype, int32_t g, int32_t d,
       }
 }
 
-/* (value desc, id asc) for the int and float rankings */
-static int better_i(const int32_t *v, int64_t a, int64_t b) {
-  return v[a] != v[b] ? v[a] > v[b] : a < b;
+/* rankings by (value desc, id asc), sorted with the C library's qsort */
+typedef struct { int32_t v; int64_t id; } rank_i;
+typedef struct { float v; int64_t id; } rank_f;
+static int cmp_rank_i(const void *pa, const void *pb) {
+  const rank_i *a = (const rank_i *)pa, *b = (const rank_i *)pb;
+  if (a->v != b->v) return a->v > b->v ? -1 : 1;
+  return a->id < b->id ? -1 : (a->id > b->id);
 }
-static int better_f(const float *v, int64_t a, int64_t b) {
-  return v[a] != v[b] ? v[a] > v[b] : a < b;
+static int cmp_rank_f(const void *pa, const void *pb) {
+  const rank_f *a = (const rank_f *)pa, *b = (const rank_f *)pb;
+  if (a->v != b->v) return a->v > b->v ? -1 : 1;
+  return a->id < b->id ? -1 : (a->id > b->id);
 }
 
 int64_t lkvo_paris_select(const float *qrot, int32_t d, int32_t m, int32_t rho,
@@ -470,7 +494,7 @@ int64_t lkvo_paris_select(const float *qrot, int32_t d, int32_t m, int32_t rho,
   float *sim = (float *)malloc((size_t)np * sizeof *sim);
   int32_t *coarse = (int32_t *)calloc((size_t)(n > 0 ? n : 1), sizeof *coarse);
   float *est = (float *)calloc((size_t)(n > 0 ? n : 1), sizeof *est);
-  int64_t *order = (int64_t *)malloc((size_t)(n > 0 ? n : 1) * sizeof *order);
+  rank_i *order = (rank_i *)malloc((size_t)(n > 0 ? n : 1) * sizeof *order);
   /* the rho best sign centroids of each subspace and their votes */
   for (int32_t b = 0; b < nb; ++b) {
     for (int32_t p = 0; p < np; ++p) {
@@ -495,18 +519,15 @@ int64_t lkvo_paris_select(const float *qrot, int32_t d, int32_t m, int32_t rho,
     for (int32_t b = 0; b < nb; ++b) c += vote[(size_t)b * np + bucket[(size_t)i * nb + b]];
     coarse[i] = c;
   }
-  /* candidates: the n_cand best coarse scores (insertion sort of all ids) */
+  /* candidates: the n_cand best coarse scores */
   for (int64_t i = 0; i < n; ++i) {
-    int64_t p = i;
-    while (p > 0 && better_i(coarse, i, order[p - 1])) {
-      order[p] = order[p - 1];
-      --p;
-    }
-    order[p] = i;
+    order[i].v = coarse[i];
+    order[i].id = i;
   }
+  qsort(order, (size_t)n, sizeof *order, cmp_rank_i);
   const int64_t nc = n_cand < n ? n_cand : n;
   for (int64_t c = 0; c < nc; ++c) {
-    const int64_t i = order[c];
+    const int64_t i = order[c].id;
     float e = 0.0f;
     for (int32_t b = 0; b < nb; ++b) {
       float dot = 0.0f;
@@ -521,18 +542,14 @@ int64_t lkvo_paris_select(const float *qrot, int32_t d, int32_t m, int32_t rho,
     est[i] = e;
   }
   /* the budget best candidates by the estimate */
-  int64_t *cand = (int64_t *)malloc((size_t)(nc > 0 ? nc : 1) * sizeof *cand);
+  rank_f *cand = (rank_f *)malloc((size_t)(nc > 0 ? nc : 1) * sizeof *cand);
   for (int64_t c = 0; c < nc; ++c) {
-    const int64_t i = order[c];
-    int64_t p = c;
-    while (p > 0 && better_f(est, i, cand[p - 1])) {
-      cand[p] = cand[p - 1];
-      --p;
-    }
-    cand[p] = i;
+    cand[c].v = est[order[c].id];
+    cand[c].id = order[c].id;
   }
+  qsort(cand, (size_t)nc, sizeof *cand, cmp_rank_f);
   const int64_t k = budget < nc ? budget : nc;
-  for (int64_t c = 0; c < k; ++c) sel_out[c] = cand[c];
+  for (int64_t c = 0; c < k; ++c) sel_out[c] = cand[c].id;
   if (coarse_out) memcpy(coarse_out, coarse, (size_t)n * sizeof *coarse);
   if (est_out) memcpy(est_out, est, (size_t)n * sizeof *est);
   free(vote); free(sim); free(coarse); free(est); free(order); free(cand);
@@ -607,13 +624,16 @@ int lkvo_decode(const lkvo_decode_args *a, lkvo_decode_result *r) {
     if (!psign || !pbk || !plv || !pw || !pq || !psel) goto done;
     lkvo_paris_signs(a->paris_seed, d, psign);
     lkvo_paris_levels(8, pthr, plev);
+    int8_t *hd = paris_matrix(d, psign);
+    if (!hd) goto done;
     for (int32_t kh = 0; kh < hkv; ++kh)
       for (int64_t i = 0; i < n + T; ++i) {
         const uint16_t *kr = i < n ? (const uint16_t *)a->keys + ((size_t)kh * n + i) * d
                                    : (const uint16_t *)a->k_new + ((size_t)(i - n) * hkv + kh) * d;
         const size_t x = (size_t)kh * (n + T) + i;
-        lkvo_paris_encode(kr, d, psign, 8, pthr, plev, pbk + x * pnb, plv + x * d, pw + x * pnb);
+        paris_encode_hd(kr, d, hd, 8, pthr, plev, pbk + x * pnb, plv + x * d, pw + x * pnb);
       }
+    free(hd);
   }
 
   for (int32_t kh = 0; kh < hkv && !paris; ++kh) {

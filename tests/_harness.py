@@ -124,16 +124,19 @@ def compare_segments(ctx, w, o, b, li, layer):
 
 # ---------------------------------------------------------------- graph path at full size
 
-def run_graph(ctx, w, q, kn, vn, *, seqs, tau=None, budget=None, chunk=512, keep_out=True):
+def run_graph(ctx, w, q, kn, vn, *, seqs, tau=None, budget=None, chunk=512, keep_out=True,
+              per_head=False):
     """A whole run through lkv_decode_steps (the pipelined CUDA graph that the
     benchmark times), in chunks of `chunk` steps. Returns host arrays:
-    boundary [T,B], r [T,B], n_sel [T,B,Hkv] for every sequence; for the
-    sequences in `seqs`, out {b: [T,H,d]} and the selections at retrieval
-    steps sel {(t, b, h): ascending ids}."""
+    boundary [T,B], r [T,B], n_sel [T,B,Hs] for every sequence (Hs = Hkv, or
+    H with per-head selection records); for the sequences in `seqs`, out
+    {b: [T,H,d]} and the selections at retrieval steps sel {(t, b, h):
+    ascending ids}."""
     tau = w.tau if tau is None else tau
     budget = w.budget if budget is None else budget
     T, B = q.shape[0], q.shape[1]
-    Hkv, H = w.n_kv_heads, w.n_heads
+    H = w.n_heads
+    Hkv = H if per_head else w.n_kv_heads
     dev = q.device
     out = torch.empty(T, B, 1, H, 128, dtype=torch.float32, device=dev)
     bnd = torch.zeros(T, B, 1, dtype=torch.uint8, device=dev)
