@@ -274,6 +274,22 @@ def attn_roofline(kern, ctr, w, eb):
     return n_attn, ms_attn, alg, sec, alg / sec / 1e9
 
 
+def timed_decode(torch, ctx, q, kn, vn, tau, budget, out, warm, n, **kw):
+    """Decode steps warm .. warm + n - 1 through the graph path, timed with
+    CUDA events on the context stream, after an untimed call for steps
+    0 .. warm - 1 (which also captures the decode graphs, so the timed call
+    only replays them). Returns steps/s."""
+    ctx.decode_steps(0, q[:warm], kn[:warm], vn[:warm], tau, budget, out[:warm], **kw)
+    ctx.sync()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sl = slice(warm, warm + n)
+    e0.record(ctx.stream)
+    ctx.decode_steps(0, q[sl], kn[sl], vn[sl], tau, budget, out[sl], **kw)
+    e1.record(ctx.stream)
+    e1.synchronize()
+    return n / (e0.elapsed_time(e1) / 1e3)
+
+
 def graph_attention(ctr, w, eb, dec_ms, hbm_peak):
     """The attention's algorithmic bytes over the whole timed decode (device
     row counters of every step, so the filling of the local buffer is
@@ -482,15 +498,15 @@ def run_ours(args, rank, world, local):
 
     # ---- end to end through the C ABI with host buffers: every decode step's
     # inputs come from pinned host memory and its outputs go back to it. The
-    # steps go in chunks of 256; a chunk's host-to-device copy (its own
-    # stream) overlaps the previous chunk's decode, and its device-to-host
-    # copy (a third stream) overlaps the next one.
+    # steps go in chunks of 512 (one decode graph each); a chunk's
+    # host-to-device copy (its own stream) overlaps the previous chunk's
+    # decode, and its device-to-host copy (a third stream) overlaps the next.
     if not args.no_e2e:
         qh, knh, vnh = (x.cpu().pin_memory() for x in (q, kn, vn))
         outh = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
         h2d = (q[0].numel() + kn[0].numel() + vn[0].numel()) * eb
         d2h = out[0].numel() * 4
-        chunk = 256
+        chunk = 512
         build_all()
         ctx.sync()
         torch.cuda.synchronize()
@@ -548,8 +564,8 @@ def offload_probe(torch, hbm_peak):
     import synth
     import cluster_indexed_kv_gb300 as lkv
     from cluster_indexed_kv_gb300 import _lib
-    w = synth.WORKLOADS["offload"].replace(n_layers=1, iters=2, n_steps=384)
-    T1, T2 = 256, 128
+    W0, T1, T2 = 128, 256, 128
+    w = synth.WORKLOADS["offload"].replace(n_layers=1, iters=2, n_steps=W0 + T1 + T2)
     K, V = synth.prefill(w, 0, "cuda")
     q, kn, vn, _ = synth.decode_inputs(w, "cuda")
     ctx = lkv.Context(batch=1, n_layers=1, n_kv_heads=w.n_kv_heads, group=w.group,
@@ -560,15 +576,10 @@ def offload_probe(torch, hbm_peak):
     del K, V
     out = torch.empty(w.n_steps, 1, 1, w.n_heads, 128, device="cuda")
     ctx.sync()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(ctx.stream)
-    ctx.decode_steps(0, q[:T1], kn[:T1], vn[:T1], w.tau, w.budget, out[:T1])
-    e1.record(ctx.stream)
-    e1.synchronize()
-    steps_per_s = T1 / (e0.elapsed_time(e1) / 1e3)
+    steps_per_s = timed_decode(torch, ctx, q, kn, vn, w.tau, w.budget, out, W0, T1)
     ctx.set_profiling(True)
     ctx.profile(reset=True)
-    for t in range(T1, T1 + T2):
+    for t in range(W0 + T1, W0 + T1 + T2):
         ctx.decode_step(0, q[t], kn[t], vn[t], 2.0, w.budget, out[t])
     kern, ctr = ctx.profile(reset=True)
     ctx.close()
@@ -616,8 +627,8 @@ def multi_layer_probe(torch, w0, hbm_peak, peak_kind):
     overwritten before every step."""
     import synth
     import cluster_indexed_kv_gb300 as lkv
-    NL, T1, T2 = 4, 1024, 64
-    w = w0.replace(n_layers=NL, n_steps=T1 + T2)
+    NL, W0, T1, T2 = 4, 512, 1024, 64
+    w = w0.replace(n_layers=NL, n_steps=W0 + T1 + T2)
     ctx = lkv.Context(batch=w.batch, n_layers=NL, n_kv_heads=w.n_kv_heads, group=w.group,
                       dtype=w.torch_dtype, local_buf=w.local_buf, max_clusters=w.n_clusters,
                       max_prefill=w.n_prefill, max_steps=w.n_steps, max_budget=w.budget)
@@ -628,16 +639,11 @@ def multi_layer_probe(torch, w0, hbm_peak, peak_kind):
     q, kn, vn, _ = synth.decode_inputs(w, "cuda")
     out = torch.empty(w.n_steps, w.batch, NL, w.n_heads, 128, device="cuda")
     ctx.sync()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(ctx.stream)
-    ctx.decode_steps(0, q[:T1], kn[:T1], vn[:T1], w.tau, w.budget, out[:T1], n_layers=NL)
-    e1.record(ctx.stream)
-    e1.synchronize()
-    steps_per_s = T1 / (e0.elapsed_time(e1) / 1e3)
+    steps_per_s = timed_decode(torch, ctx, q, kn, vn, w.tau, w.budget, out, W0, T1, n_layers=NL)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
     ctx.set_profiling(True)
     ctx.profile(reset=True)
-    for t in range(T1, T1 + T2):
+    for t in range(W0 + T1, W0 + T1 + T2):
         flush.fill_(float(t))
         ctx.decode_step(0, q[t], kn[t], vn[t], w.tau, w.budget, out[t], n_layers=NL)
     kern, ctr = ctx.profile(reset=True)
@@ -645,7 +651,8 @@ def multi_layer_probe(torch, w0, hbm_peak, peak_kind):
     n_attn, _, alg, sec, achieved = attn_roofline(kern, ctr, w, 2)
     return {"workload": f"b8_32k x {NL} layers (one decode call per step for all layers)",
             "decode_steps_per_s": steps_per_s, "tokens_per_s": steps_per_s * w.batch,
-            "decode_note": f"steps 0..{T1 - 1} through the pipelined graph",
+            "decode_note": f"steps {W0}..{W0 + T1 - 1} through the pipelined graph (graphs "
+                           f"captured by the untimed steps before)",
             "attn_roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak,
                               "unit": "GB/s", "frac": achieved / hbm_peak,
                               "alg_bytes_per_launch": alg, "avg_launch_us": sec * 1e6,
@@ -659,14 +666,15 @@ def policy_probe(torch, w0):
     and boundary segments), retrieval at every step, at every 32nd step, and
     the page-granular every-step baseline (16-token pages of the input, as
     many units as clusters, and 16-token output pages). Per policy: decode
-    steps/s through the pipelined graph (steps 0..1535), then 256 single-step
+    steps/s through the pipelined graph (steps 512..2047, after untimed
+    steps 0..511 that capture the graphs), then 256 single-step
     launches with CUDA events around every kernel (L2 overwritten before
     every step) for the share of the step that goes to scoring + selection
     (the retrieval; the K/V rows are read where they lie by the attention)."""
     import synth
     import cluster_indexed_kv_gb300 as lkv
-    T1, T2 = 1536, 256
-    w = w0.replace(n_steps=T1 + T2, iters=4)
+    W0, T1, T2 = 512, 1536, 256
+    w = w0.replace(n_steps=W0 + T1 + T2, iters=4)
     K, V = synth.prefill(w, 0, "cuda")
     q, kn, vn, _ = synth.decode_inputs(w, "cuda")
     out = torch.empty(w.n_steps, w.batch, 1, w.n_heads, 128, device="cuda")
@@ -688,15 +696,10 @@ def policy_probe(torch, w0):
         ctx.set_policy(**pol)
         bnd = torch.zeros(w.n_steps, w.batch, 1, dtype=torch.uint8, device="cuda")
         ctx.sync()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(ctx.stream)
-        ctx.decode_steps(0, q[:T1], kn[:T1], vn[:T1], w.tau, w.budget, out[:T1], boundary=bnd[:T1])
-        e1.record(ctx.stream)
-        e1.synchronize()
-        sps = T1 / (e0.elapsed_time(e1) / 1e3)
+        sps = timed_decode(torch, ctx, q, kn, vn, w.tau, w.budget, out, W0, T1, boundary=bnd)
         ctx.set_profiling(True)
         ctx.profile(reset=True)
-        for t in range(T1, T1 + T2):
+        for t in range(W0 + T1, W0 + T1 + T2):
             flush.fill_(float(t))
             ctx.decode_step(0, q[t], kn[t], vn[t], w.tau, w.budget, out[t], boundary=bnd[t])
         kern, ctr = ctx.profile(reset=True)
@@ -710,7 +713,7 @@ def policy_probe(torch, w0):
                       "attended_rows_per_step": ctr["attn_rows"] / T2,
                       "attended_bytes_per_step": ctr["attn_rows"] * 2 * 128 * 2 / T2,
                       "selected_tokens_per_retrieval": ctr["sel_tokens"] / max(
-                          1, int(bnd[T1:].sum().item()) * w.n_kv_heads)}
+                          1, int(bnd[W0 + T1:].sum().item()) * w.n_kv_heads)}
     return {"workload": "b8_32k (4 Lloyd rounds for the clustered rows)", "policies": rows,
             "note": "share = scoring+selection kernel time / all decode kernel time of the "
                     "single-step launches (the pages' breakdown also counts the host transfer "
@@ -724,36 +727,32 @@ def paris_probe(torch, w0):
     """The ParisKV-style token selector on the 32K-input, batch-8 workload
     (same inputs, budget 1024 tokens, rho 4, 2560 candidates = 7.8% of the
     prefill): decode steps/s through the pipelined graph with the method's
-    adaptive trigger and with retrieval at every step, then 128 single-step
+    adaptive trigger and with retrieval at every step (steps 512..2047, after
+    untimed steps that capture the graphs), then 128 single-step
     launches at every step (L2 overwritten before each) for the selection
     kernel's time and its HBM roofline (bucket bytes of every region token,
     codes and scales of every candidate, 16 + 128 bytes)."""
     import synth
     import cluster_indexed_kv_gb300 as lkv
-    T1, T2 = 1536, 128
-    w = w0.replace(n_steps=2 * T1 + T2)
+    W0, T1, T2 = 512, 1536, 128
+    w = w0.replace(n_steps=W0 + T1 + T2)
     K, V = synth.prefill(w, 0, "cuda")
     q, kn, vn, _ = synth.decode_inputs(w, "cuda")
     out = torch.empty(w.n_steps, w.batch, 1, w.n_heads, 128, device="cuda")
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
     res = {"workload": "b8_32k, ParisKV-style selector (rho 4, 2560 candidates, budget 1024 tokens)"}
-    for name, pol, t0 in (("adaptive", dict(), 0), ("every_step", dict(trigger="every"), T1)):
+    for name, pol in (("adaptive", dict()), ("every_step", dict(trigger="every"))):
         ctx = lkv.Context(batch=w.batch, n_layers=1, n_kv_heads=w.n_kv_heads, group=w.group,
                           dtype=w.torch_dtype, local_buf=w.local_buf, max_clusters=w.n_clusters,
                           max_prefill=w.n_prefill, max_steps=w.n_steps, max_budget=w.budget)
         ctx.build_paris(0, K, V, rho=4, n_cand=2560, seed=1)
         ctx.set_policy(**pol)
         ctx.sync()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(ctx.stream)
-        ctx.decode_steps(0, q[:T1], kn[:T1], vn[:T1], w.tau, w.budget, out[:T1])
-        e1.record(ctx.stream)
-        e1.synchronize()
-        res[f"decode_steps_per_s_{name}"] = T1 / (e0.elapsed_time(e1) / 1e3)
+        res[f"decode_steps_per_s_{name}"] = timed_decode(torch, ctx, q, kn, vn, w.tau, w.budget, out, W0, T1)
         if name == "every_step":
             ctx.set_profiling(True)
             ctx.profile(reset=True)
-            for t in range(T1, T1 + T2):
+            for t in range(W0 + T1, W0 + T1 + T2):
                 flush.fill_(float(t))
                 ctx.decode_step(0, q[t], kn[t], vn[t], w.tau, w.budget, out[t])
             kern, ctr = ctx.profile(reset=True)

@@ -107,6 +107,12 @@ static void free_all(lkv_ctx *c) {
     c->pipe.attn[i] = nullptr;
     c->pipe.attn_done[i] = nullptr;
   }
+  for (int i = 0; i < 3; ++i) {
+    if (c->pipe.chunk_done[i]) cudaEventDestroy(c->pipe.chunk_done[i]);
+    c->pipe.chunk_done[i] = nullptr;
+  }
+  if (c->pipe.join) cudaStreamDestroy(c->pipe.join);
+  c->pipe.join = nullptr;
   if (c->pipe.sel_done) cudaEventDestroy(c->pipe.sel_done);
   if (c->pipe.b_done) cudaEventDestroy(c->pipe.b_done);
   if (c->pipe.sel) cudaStreamDestroy(c->pipe.sel);
@@ -220,7 +226,7 @@ lkv_status lkv_create(const lkv_config *cfg, lkv_ctx **out) {
   v.aview = (int4 *)dalloc(c, lkv::kSlots * LB * sizeof(int4), &st);
   v.adesc = (int4 *)dalloc(c, lkv::kSlots * S_all * sizeof(int4), &st);
   v.segsum = (int64_t *)dalloc(c, S_all * d * 8, &st);
-  v.scores = (float *)dalloc(c, (v.chunk_sel ? lkv::kSlots : 1) * S_all * u_cap * 4, &st);
+  v.scores = (float *)dalloc(c, (v.chunk_sel ? lkv::kChunk : 1) * S_all * u_cap * 4, &st);
   // the selection plan, one copy per plan slot
   v.sel = (int32_t *)dalloc(c, R * S_all * u_cap * 4, &st);
   v.n_sel = (int32_t *)dalloc(c, R * S_all * 4, &st);
@@ -287,6 +293,9 @@ lkv_status lkv_create(const lkv_config *cfg, lkv_ctx **out) {
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->pipe.sel_done, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->pipe.b_done, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&c->pipe.sel, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&c->pipe.join, cudaStreamNonBlocking);
+  for (int i = 0; i < 3; ++i)
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->pipe.chunk_done[i], cudaEventDisableTiming);
   if (e == cudaSuccess) e = lkv::prepare_kernels(k.dtype, k.group);
   if (e == cudaSuccess) e = cudaStreamSynchronize(c->stream);
   if (e != cudaSuccess) {
@@ -476,6 +485,8 @@ static cudaError_t step_graph(lkv_ctx *c, const lkv::StepArgs &a, int steps, cud
     e = cudaStreamWaitEvent(c->capture, c->pipe.attn_done[(steps - 1 - i) % lkv::kAttnStreams], 0);
   if (e == cudaSuccess && steps > 0) e = cudaEventRecord(c->pipe.sel_done, c->pipe.sel);
   if (e == cudaSuccess && steps > 0) e = cudaStreamWaitEvent(c->capture, c->pipe.sel_done, 0);
+  if (e == cudaSuccess && steps > 0 && c->v.chunk_sel)  // the join lane's last record
+    e = cudaStreamWaitEvent(c->capture, c->pipe.chunk_done[((steps - 1) / lkv::kChunk) % 3], 0);
   cudaError_t e2 = cudaStreamEndCapture(c->capture, &graph);
   if (e == cudaSuccess) e = e2;
   cudaGraphExec_t exec = nullptr;
@@ -520,10 +531,10 @@ lkv_status lkv_decode_steps(lkv_ctx *c, int32_t layer, int32_t nl, int32_t n_ste
   } else if (c->prof.timing) {
     for (int i = 0; i < n_steps && e == cudaSuccess; ++i) e = lkv::launch_decode_steps(c->v, a, 1, c->stream, c->prof);
   } else {
-    // captured graphs of 128 steps (two boundary chunks), then one of 64 for
-    // what is left of at least 64, then single steps
+    // captured graphs of 512 steps (eight boundary chunks), then of 128 and
+    // of 64 for what is left, then single steps
     int done = 0;
-    for (const int gl : {lkv::kSlots, lkv::kChunk}) {
+    for (const int gl : {lkv::kSlots, 2 * lkv::kChunk, lkv::kChunk}) {
       const int reps = (n_steps - done) / gl;
       if (reps == 0 || e != cudaSuccess) continue;
       cudaGraphExec_t exec = nullptr;
@@ -659,7 +670,7 @@ lkv_status lkv_build_paris(lkv_ctx *c, int32_t layer, const void *keys, const vo
     uint8_t *code = (uint8_t *)dalloc(c, rows * 64, &st);
     float *w = (float *)dalloc(c, rows * lkv::kParisSub * 4, &st);
     const int64_t pitch = (v.pool_rows + 15) / 16 * 16;
-    uint8_t *score = (uint8_t *)dalloc(c, (int64_t)lkv::kSlots * v.S_all * pitch, &st);
+    uint8_t *score = (uint8_t *)dalloc(c, (int64_t)lkv::kChunk * v.S_all * pitch, &st);
     if (st != LKV_OK) return st;
     for (GraphEntry &g : c->graphs)
       if (g.exec) cudaGraphExecDestroy(g.exec);

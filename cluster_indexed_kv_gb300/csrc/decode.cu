@@ -1006,7 +1006,7 @@ __device__ __noinline__ void select_paris(const CtxView &v, int64_t lb, int64_t 
   // 3. every region token's vote sum, kept as a byte in the step slot's
   //    scratch; their histogram (per warp, then summed); the cut score and
   //    how many ties it takes
-  uint8_t *sc = v.pk_score + ((int64_t)slot * v.S_all + gs) * v.pk_pitch;
+  uint8_t *sc = v.pk_score + ((int64_t)(slot % kChunk) * v.S_all + gs) * v.pk_pitch;
   for (int x = tid; x < kScoreWarps * 256; x += nth) (&whist[0][0])[x] = 0;
   __syncthreads();
   {
@@ -1301,7 +1301,7 @@ __global__ void __launch_bounds__(kScoreThreads, 3) k_select_chunk(CtxView v, St
   __syncthreads();
   extern __shared__ __align__(16) uint32_t sel_smem[];
   const bool in_smem = U <= kSelSmemUnits;
-  float *scg = v.scores + ((int64_t)slot * v.S_all + gs) * v.u_cap;
+  float *scg = v.scores + ((int64_t)(slot % kChunk) * v.S_all + gs) * v.u_cap;
   constexpr int nvec = kHeadDim * elem_bytes<DT>() / 16;
   const uint4 *rows = (const uint4 *)((const char *)v.cent_op + gs * v.u_cap * kHeadDim * elem_bytes<DT>());
   for (int u = tid; u < U; u += nth) {
@@ -3077,6 +3077,11 @@ static cudaError_t decode_t(const CtxView &v, const StepArgs &a, int n_steps, cu
     // chunk selection: every retrieval of the n_steps steps in one launch,
     // then the steps' attentions (step i's on attn[i % kAttnStreams], so it
     // follows step i - kAttnStreams's, whose scratch slot it may share)
+    const int chunk = pipe ? pipe->step / kChunk : 0;
+    if (pipe && chunk >= 2) {  // chunk - 2's attentions are done (plan ring, see Pipe)
+      e = cudaStreamWaitEvent(ss, pipe->chunk_done[(chunk - 2) % 3], 0);
+      if (e != cudaSuccess) return e;
+    }
     prof.begin(kPSelect, ss);
     launch_pdl(k_select_chunk<DT>, dim3(slices, n_steps), dim3(kScoreThreads),
                v.pol_per_head ? kSelHeadSmemBytes : v.paris ? kSelParisSmemBytes : kSelSmemBytes, ss, v, a);
@@ -3103,6 +3108,12 @@ static cudaError_t decode_t(const CtxView &v, const StepArgs &a, int n_steps, cu
         e = cudaEventRecord(pipe->attn_done[step % kAttnStreams], as);
         if (e != cudaSuccess) return e;
       }
+    }
+    if (pipe) {  // every attention of this chunk, joined
+      for (int s = 0; s < kAttnStreams && s < n_steps && e == cudaSuccess; ++s)
+        e = cudaStreamWaitEvent(pipe->join, pipe->attn_done[(pipe->step + n_steps - 1 - s) % kAttnStreams], 0);
+      if (e == cudaSuccess) e = cudaEventRecord(pipe->chunk_done[chunk % 3], pipe->join);
+      if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
   }

@@ -17,7 +17,7 @@ constexpr int kAttnChunk = 64;     // tokens per attention work item
 constexpr int kRing = 32;          // plan slots and attention scratch slots (see Pipe)
 constexpr int kAttnStreams = 16;   // attention streams of a pipelined capture
 constexpr int kChunk = 64;         // decode steps whose boundary tests one launch runs
-constexpr int kSlots = 2 * kChunk; // step slots (queries, views): the steps of one captured graph
+constexpr int kSlots = 8 * kChunk; // step slots (queries, views): the steps of one captured graph
 constexpr int kAttnMaxSplit = 8;   // CTAs per slice in one attention launch, at most
 constexpr int kStreamMaxSlices = 1024;  // slices of one call the streaming attention takes
 
@@ -82,7 +82,7 @@ struct CtxView {
                               // written by the selection kernel on every step
   int64_t *segsum;            // [slice][d] exact fixed-point sums (bf16) or
                               // doubles reinterpreted (fp32)
-  float *scores;              // chunk selection: [kSlots][slice][u_cap] per step slot, else [slice][u_cap]
+  float *scores;              // chunk selection: [kChunk][slice][u_cap] per step of the chunk, else [slice][u_cap]
   // the selection plan, one copy per plan slot: [plan_ring][slice]...
   int32_t plan_ring;          // plan slots: 2 * kChunk + 1 with chunk selection, else kRing
   int32_t chunk_sel;          // one selection launch per chunk of steps (see launch_decode_steps)
@@ -123,7 +123,7 @@ struct CtxView {
   uint8_t *pk_bucket;         // [slice][pool_rows][16] bucket (sign pattern) per subspace
   uint8_t *pk_code;           // [slice][pool_rows][64] 3-bit magnitude levels, two per byte
   float *pk_w;                // [slice][pool_rows][16] calibrated scale per subspace
-  uint8_t *pk_score;          // [kSlots][slice][pk_pitch] vote sums of a step's region tokens
+  uint8_t *pk_score;          // [kChunk][slice][pk_pitch] vote sums of a step's region tokens (by step slot mod kChunk)
   int64_t pk_pitch;           // pool_rows rounded up to a multiple of 16
 };
 
@@ -367,6 +367,13 @@ struct StepArgs {
 //    boundary kernel only writes units above the unit count a pending
 //    selection reads;
 //  - step i's attention on attn[i % kAttnStreams], after its selection (sel_done).
+// With chunk selection the selection lane runs one launch per chunk instead,
+// each after its chunk's boundary kernel and the previous chunk's selection,
+// and chunk j's selection also waits until every attention of chunk j - 2
+// has finished (chunk_done): the attentions still running then belong to
+// chunk j - 1, whose steps and chunk j's are at most 2 * kChunk retrievals
+// apart, so with plan_ring = 2 * kChunk + 1 no plan slot that a running
+// attention reads is written.
 constexpr int kSelWaitStride = 8;
 static_assert(kAttnStreams + kSelWaitStride - 1 < kRing, "plan ring too small for the attentions in flight");
 struct Pipe {
@@ -374,6 +381,11 @@ struct Pipe {
   cudaStream_t attn[kAttnStreams];
   cudaEvent_t b_done, sel_done;
   cudaEvent_t attn_done[kAttnStreams];
+  // chunk selection: chunk j's attentions all done (joined on `join`), in
+  // three rotating events; chunk j + 2's selection waits for it (see
+  // launch_decode_steps)
+  cudaStream_t join;
+  cudaEvent_t chunk_done[3];
   int step;  // index of the chunk's first step in the capture
 };
 
