@@ -274,17 +274,21 @@ def attn_roofline(kern, ctr, w, eb):
     return n_attn, ms_attn, alg, sec, alg / sec / 1e9
 
 
-def timed_decode(torch, ctx, q, kn, vn, tau, budget, out, warm, n, **kw):
+def timed_decode(torch, ctx, q, kn, vn, tau, budget, out, warm, n, boundary=None, **kw):
     """Decode steps warm .. warm + n - 1 through the graph path, timed with
     CUDA events on the context stream, after an untimed call for steps
     0 .. warm - 1 (which also captures the decode graphs, so the timed call
-    only replays them). Returns steps/s."""
-    ctx.decode_steps(0, q[:warm], kn[:warm], vn[:warm], tau, budget, out[:warm], **kw)
+    only replays them). Every per-step buffer is passed from the call's own
+    first step, as a caller walking full-length buffers chunk by chunk does:
+    then both calls present the same graph arguments. Returns steps/s."""
+    b0 = {} if boundary is None else {"boundary": boundary[:warm]}
+    ctx.decode_steps(0, q[:warm], kn[:warm], vn[:warm], tau, budget, out[:warm], **b0, **kw)
     ctx.sync()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sl = slice(warm, warm + n)
+    b1 = {} if boundary is None else {"boundary": boundary[sl]}
     e0.record(ctx.stream)
-    ctx.decode_steps(0, q[sl], kn[sl], vn[sl], tau, budget, out[sl], **kw)
+    ctx.decode_steps(0, q[sl], kn[sl], vn[sl], tau, budget, out[sl], **b1, **kw)
     e1.record(ctx.stream)
     e1.synchronize()
     return n / (e0.elapsed_time(e1) / 1e3)
@@ -498,7 +502,7 @@ def run_ours(args, rank, world, local):
 
     # ---- end to end through the C ABI with host buffers: every decode step's
     # inputs come from pinned host memory and its outputs go back to it. The
-    # steps go in chunks of 512 (one decode graph each); a chunk's
+    # steps go in chunks of 2048 (one decode graph each); a chunk's
     # host-to-device copy (its own stream) overlaps the previous chunk's
     # decode, and its device-to-host copy (a third stream) overlaps the next.
     if not args.no_e2e:
@@ -506,33 +510,38 @@ def run_ours(args, rank, world, local):
         outh = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
         h2d = (q[0].numel() + kn[0].numel() + vn[0].numel()) * eb
         d2h = out[0].numel() * 4
-        chunk = 512
-        build_all()
-        ctx.sync()
-        torch.cuda.synchronize()
+        chunk = 2048
         s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
-        ea, eb_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        ea.record(s_in)
-        starts = list(range(0, T, chunk))
-        for c0 in starts:
-            n = min(chunk, T - c0)
-            with torch.cuda.stream(s_in):
-                q[c0:c0 + n].copy_(qh[c0:c0 + n], non_blocking=True)
-                kn[c0:c0 + n].copy_(knh[c0:c0 + n], non_blocking=True)
-                vn[c0:c0 + n].copy_(vnh[c0:c0 + n], non_blocking=True)
-                inputs_in = torch.cuda.Event()
-                inputs_in.record(s_in)
-            stream.wait_event(inputs_in)
-            ctx.decode_steps(0, q[c0:c0 + n], kn[c0:c0 + n], vn[c0:c0 + n], w.tau, w.budget,
-                             out[c0:c0 + n], n_layers=NL)
-            decoded = torch.cuda.Event()
-            decoded.record(stream)
-            s_out.wait_event(decoded)
-            with torch.cuda.stream(s_out):
-                outh[c0:c0 + n].copy_(out[c0:c0 + n], non_blocking=True)
-        eb_.record(s_out)
-        eb_.synchronize()
-        result["e2e"] = {"value": world * T / (ea.elapsed_time(eb_) / 1e3), "unit": UNIT,
+
+        def e2e_pass():
+            build_all()
+            ctx.sync()
+            torch.cuda.synchronize()
+            ea, eb_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ea.record(s_in)
+            for c0 in range(0, T, chunk):
+                n = min(chunk, T - c0)
+                with torch.cuda.stream(s_in):
+                    q[c0:c0 + n].copy_(qh[c0:c0 + n], non_blocking=True)
+                    kn[c0:c0 + n].copy_(knh[c0:c0 + n], non_blocking=True)
+                    vn[c0:c0 + n].copy_(vnh[c0:c0 + n], non_blocking=True)
+                    inputs_in = torch.cuda.Event()
+                    inputs_in.record(s_in)
+                stream.wait_event(inputs_in)
+                ctx.decode_steps(0, q[c0:c0 + n], kn[c0:c0 + n], vn[c0:c0 + n], w.tau, w.budget,
+                                 out[c0:c0 + n], n_layers=NL)
+                decoded = torch.cuda.Event()
+                decoded.record(stream)
+                s_out.wait_event(decoded)
+                with torch.cuda.stream(s_out):
+                    outh[c0:c0 + n].copy_(out[c0:c0 + n], non_blocking=True)
+            eb_.record(s_out)
+            eb_.synchronize()
+            return ea.elapsed_time(eb_)
+
+        e2e_pass()  # untimed: captures the decode graphs this call sequence uses
+        e2e_ms = e2e_pass()
+        result["e2e"] = {"value": world * T / (e2e_ms / 1e3), "unit": UNIT,
                          "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
     want_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
     idx0 = ctx.get_index(0, 0, 0, w.n_prefill) if want_cpu else None

@@ -222,9 +222,13 @@ lkv_status lkv_create(const lkv_config *cfg, lkv_ctx **out) {
   v.perm = (int32_t *)dalloc(c, S_all * n_cap * 4, &st);
   v.st = (DecState *)dalloc(c, LB * sizeof(DecState), &st);
   v.q_prev = dalloc(c, LB * H * d * es, &st);
-  v.q_attn = (float *)dalloc(c, lkv::kSlots * LB * H * d * 4, &st);  // per step slot
-  v.aview = (int4 *)dalloc(c, lkv::kSlots * LB * sizeof(int4), &st);
-  v.adesc = (int4 *)dalloc(c, lkv::kSlots * S_all * sizeof(int4), &st);
+  // step slots: a captured graph of up to kMaxSlots steps, no longer than
+  // the context's steps need
+  v.n_slots = (int32_t)std::min<int64_t>(lkv::kMaxSlots, ((int64_t)t_cap + lkv::kChunk - 1) / lkv::kChunk * lkv::kChunk);
+  const int64_t NS = v.n_slots;
+  v.q_attn = (float *)dalloc(c, NS * LB * H * d * 4, &st);  // per step slot
+  v.aview = (int4 *)dalloc(c, NS * LB * sizeof(int4), &st);
+  v.adesc = (int4 *)dalloc(c, NS * S_all * sizeof(int4), &st);
   v.segsum = (int64_t *)dalloc(c, S_all * d * 8, &st);
   v.scores = (float *)dalloc(c, (v.chunk_sel ? lkv::kChunk : 1) * S_all * u_cap * 4, &st);
   // the selection plan, one copy per plan slot
@@ -262,6 +266,7 @@ lkv_status lkv_create(const lkv_config *cfg, lkv_ctx **out) {
   ks.knorm = (float *)dalloc(c, S * n_cap * 4, &st);
   ks.c2_pitch = (c_cap + 255) / 256 * 256;
   ks.c2 = (float *)dalloc(c, S * ks.c2_pitch * 4, &st);
+  ks.c2b = (uint16_t *)dalloc(c, S * ks.c2_pitch * 32, &st);
   ks.cstat = (float *)dalloc(c, S * 2 * 4, &st);
   ks.cnt_part = (int32_t *)dalloc(c, S * lkv::kMaxParts * c_cap * 4, &st);
   ks.count = (int32_t *)dalloc(c, S * c_cap * 4, &st);
@@ -531,10 +536,12 @@ lkv_status lkv_decode_steps(lkv_ctx *c, int32_t layer, int32_t nl, int32_t n_ste
   } else if (c->prof.timing) {
     for (int i = 0; i < n_steps && e == cudaSuccess; ++i) e = lkv::launch_decode_steps(c->v, a, 1, c->stream, c->prof);
   } else {
-    // captured graphs of 512 steps (eight boundary chunks), then of 128 and
-    // of 64 for what is left, then single steps
+    // captured graphs of 2048 steps (32 boundary chunks, as far as the step
+    // slots reach), then of 512, 128 and 64 for what is left, then single
+    // steps
     int done = 0;
-    for (const int gl : {lkv::kSlots, 2 * lkv::kChunk, lkv::kChunk}) {
+    for (const int gl : {lkv::kMaxSlots, 8 * lkv::kChunk, 2 * lkv::kChunk, lkv::kChunk}) {
+      if (gl > c->v.n_slots) continue;
       const int reps = (n_steps - done) / gl;
       if (reps == 0 || e != cudaSuccess) continue;
       cudaGraphExec_t exec = nullptr;

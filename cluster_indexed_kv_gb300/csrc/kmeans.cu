@@ -69,7 +69,7 @@ constexpr int kPrepPerCta = 64;
 template <int DT>
 __global__ void __launch_bounds__(256)
 k_prepare_operand(const float *cent32, void *cent_op, int32_t c, int32_t c_pad, int32_t c2_pitch,
-                  int32_t u_cap, int64_t gs0, float *c2, float *cstat) {
+                  int32_t u_cap, int64_t gs0, float *c2, float *cstat, uint16_t *c2b) {
   __shared__ float wmax[8][2];
   const int s = blockIdx.y;
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -83,6 +83,9 @@ k_prepare_operand(const float *cent32, void *cent_op, int32_t c, int32_t c_pad, 
       // finite value no distance reaches) and zero operand rows, so the
       // padded columns of a chunk stay finite and never win
       if (lane == 0) c2[(int64_t)s * c2_pitch + j] = FLT_MAX;
+      // the tensor-core filter's -|c|^2 / 2 row: a value no filter value reaches
+      if (c2b && lane < 8)
+        reinterpret_cast<uint32_t *>(c2b + ((int64_t)s * c2_pitch + j) * 16)[lane] = lane == 0 ? 0xf1800000u >> 16 : 0u;
       if (j < u_cap) {
         if constexpr (DT == 1) *(uint2 *)((uint16_t *)cent_op + base) = make_uint2(0u, 0u);
         else *(float4 *)((float *)cent_op + base) = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -109,6 +112,15 @@ k_prepare_operand(const float *cent32, void *cent_op, int32_t c, int32_t c_pad, 
 #pragma unroll
     for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
     if (lane == 0) c2[(int64_t)s * c2_pitch + j] = acc;
+    if (c2b && lane < 8) {
+      // -|c|^2 / 2 as a bf16 pair (high part and rounded remainder) for the
+      // tensor-core filter's extra product with a row of ones
+      const float hv = -0.5f * acc;
+      const uint16_t hi = f32_to_bf16_bits(hv);
+      const uint16_t lo = f32_to_bf16_bits(hv - bf16_bits_to_f32(hi));
+      reinterpret_cast<uint32_t *>(c2b + ((int64_t)s * c2_pitch + j) * 16)[lane] =
+          lane == 0 ? (uint32_t)hi | ((uint32_t)lo << 16) : 0u;
+    }
     cmax = fmaxf(cmax, sqrtf(acc));
     c2max = fmaxf(c2max, acc);
   }
@@ -124,9 +136,9 @@ k_prepare_operand(const float *cent32, void *cent_op, int32_t c, int32_t c_pad, 
 
 template <int DT>
 static void launch_prepare(const CtxView &v, int32_t c, int32_t c_pad, int32_t c2_pitch, int64_t gs0,
-                           int S, float *c2, float *cstat, cudaStream_t st) {
+                           int S, float *c2, float *cstat, cudaStream_t st, uint16_t *c2b = nullptr) {
   k_prepare_operand<DT><<<dim3((c_pad + kPrepPerCta - 1) / kPrepPerCta, S), 256, 0, st>>>(
-      v.cent32, v.cent_op, c, c_pad, c2_pitch, v.u_cap, gs0, c2, cstat);
+      v.cent32, v.cent_op, c, c_pad, c2_pitch, v.u_cap, gs0, c2, cstat, c2b);
 }
 
 // ---------------------------------------------------------------- assignment
@@ -365,16 +377,22 @@ constexpr int kTcWarps = 2 + kTcEpiWarps;
 constexpr int kTcThreads = kTcWarps * 32;
 constexpr uint32_t kTcABytes = kTcM * kHeadDim * 2;  // 32 KB: two 64-column halves of 16 KB
 constexpr uint32_t kTcBBytes = kTcN * kHeadDim * 2;  // 64 KB: two halves of 32 KB
-constexpr size_t kTcSmem = 2 * kTcABytes + 2 * kTcBBytes + 1024;
+// The extra K block of each chunk: a 16-column bf16 tile of ones (A) against
+// each centroid's -|c~|^2 / 2 split into a bf16 high part and remainder (B),
+// rows of 32 bytes in the 32-byte swizzle
+constexpr uint32_t kTcB1Bytes = kTcN * 32;           // 8 KB
+constexpr uint32_t kTcA1Bytes = kTcM * 32;           // 4 KB
+constexpr size_t kTcSmem = 2 * kTcABytes + 2 * kTcBBytes + 2 * kTcB1Bytes + kTcA1Bytes + 1024;
 constexpr uint32_t kTcIdesc = (1u << 4)            // fp32 accumulator
                               | (1u << 7)          // A bf16
                               | (1u << 10)         // B bf16
                               | ((uint32_t)(kTcN >> 3) << 17) | ((uint32_t)(kTcM >> 4) << 24);
 constexpr uint64_t kTcWaitNs = 2000000000ull;
 // Filter margin: 2^-13 bounds the tensor-core fp32 accumulation error of a
-// 128-term bf16 dot product with a wide safety factor; 2^-16 covers the
-// column id carried in the low mantissa bits of each value.
-constexpr float kTcEps = 0x1p-13f + 0x1p-16f;
+// 128-term bf16 dot product with a wide safety factor; 2^-15 covers the
+// column id carried in the low mantissa bits of each value (2^-17) and the
+// bf16 pair that stands for |c~|^2 / 2 (2^-17 of it).
+constexpr float kTcEps = 0x1p-13f + 0x1p-15f;
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -432,6 +450,16 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   d |= (uint64_t)2 << 61;            // 128-byte swizzle
   return d;
 }
+// The same for the 32-byte-row tiles of the extra K block (32-byte swizzle:
+// rows of 32 bytes, 8-row groups 256 bytes apart).
+__device__ __forceinline__ uint64_t sw32_desc(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;           // leading byte offset (unused for this layout)
+  d |= (uint64_t)(256 >> 4) << 32;  // stride byte offset: 8 rows x 32 bytes
+  d |= (uint64_t)1 << 46;           // descriptor version
+  d |= (uint64_t)6 << 61;           // 32-byte swizzle
+  return d;
+}
 __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t accumulate) {
   asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
                " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}"
@@ -477,6 +505,17 @@ __device__ __forceinline__ void top2_pair(float &c1, float &c2, float q, float r
   const float m = fminf(q, r), M = fmaxf(q, r);
   c2 = min3f(c2, fmaxf(c1, m), M);
   c1 = fminf(c1, m);
+}
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+// The mirror image: the two largest values (c1 >= c2) absorb {q, r}.
+__device__ __forceinline__ void top2max_pair(float &c1, float &c2, float q, float r) {
+  const float M = fmaxf(q, r), m = fminf(q, r);
+  c2 = max3f(c2, fminf(c1, M), m);
+  c1 = fmaxf(c1, M);
 }
 // Merge of two candidate lists with explicit column ids. The first two
 // entries of each list are exact; the third may be a lower bound of the
@@ -531,7 +570,7 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 
 __global__ void __launch_bounds__(kTcThreads, 1)
 k_assign_tc(const __grid_constant__ CUtensorMap keys_map, const __grid_constant__ CUtensorMap cent_map,
-            int64_t n, int32_t c, int32_t u_cap, const float *c2, int32_t c2_pitch, const float *knorm,
+            const __grid_constant__ CUtensorMap c2b_map, int64_t n, int32_t c, int32_t u_cap, const float *knorm,
             int64_t n_cap, const float *cstat, float eps, int32_t *assign, int64_t gs0, int n_slices,
             int4 *amb, int32_t *amb_count, int32_t *amb_crowd, int32_t amb_cap, int32_t *err,
             uint32_t m26, uint32_t m64) {
@@ -544,6 +583,7 @@ k_assign_tc(const __grid_constant__ CUtensorMap keys_map, const __grid_constant_
   __shared__ int32_t xj[3][kTcM][2];
   const uint32_t base = (smem_addr(tc_smem_raw) + 1023u) & ~1023u;
   const uint32_t A0 = base, B0 = base + 2 * kTcABytes;
+  const uint32_t B1 = B0 + 2 * kTcBBytes, A1 = B1 + 2 * kTcB1Bytes;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tiles = (int)((n + kTcM - 1) / kTcM);
   const int n_items = n_slices * tiles;
@@ -561,6 +601,13 @@ k_assign_tc(const __grid_constant__ CUtensorMap keys_map, const __grid_constant_
     tc_mbar_init(&mma_done, 1);
     abort_s = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  // the ones of the extra K block (every element 1.0 in bf16; the layout
+  // does not matter), made visible to the tensor cores' async proxy
+  {
+    uint32_t *a1 = reinterpret_cast<uint32_t *>(tc_smem_raw + (A1 - smem_addr(tc_smem_raw)));
+    for (int x = threadIdx.x; x < (int)(kTcA1Bytes / 4); x += blockDim.x) a1[x] = 0x3f803f80u;
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   if (warp == 1) {  // tensor memory: two 128 x 256 fp32 accumulators
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
@@ -589,11 +636,12 @@ k_assign_tc(const __grid_constant__ CUtensorMap keys_map, const __grid_constant_
         for (int ch = 0; ch < nch; ++ch, ++gc) {
           const int bi = gc & 1;
           if (!tc_wait(&b_empty[bi], ((gc >> 1) & 1) ^ 1, &abort_s)) break;
-          tc_expect_tx(&b_full[bi], kTcBBytes);
+          tc_expect_tx(&b_full[bi], kTcBBytes + kTcB1Bytes);
           // rows past the slice's table read as zeros
           const int zb = (int)(gs0 + sl);
           tma_load_3d(B0 + bi * kTcBBytes, &cent_map, 0, ch * kTcN, zb, &b_full[bi]);
           tma_load_3d(B0 + bi * kTcBBytes + kTcBBytes / 2, &cent_map, 64, ch * kTcN, zb, &b_full[bi]);
+          tma_load_3d(B1 + bi * kTcB1Bytes, &c2b_map, 0, ch * kTcN, sl, &b_full[bi]);
           b_last[bi] = gc;
         }
       }
@@ -624,6 +672,9 @@ k_assign_tc(const __grid_constant__ CUtensorMap keys_map, const __grid_constant_
             const uint32_t bo = B0 + bi * kTcBBytes + (k >> 2) * (kTcBBytes / 2) + (k & 3) * 32;
             tc_mma(d, sw128_desc(ao), sw128_desc(bo), k > 0 ? 1u : 0u);
           }
+          // + ones . (-|c~|^2 / 2): the accumulator holds k.c~ - |c~|^2 / 2,
+          // which is (|k|^2 - e) / 2 for the squared distance e
+          tc_mma(d, sw32_desc(A1), sw32_desc(B1 + bi * kTcB1Bytes), 1u);
           tc_commit(&b_empty[bi]);
           tc_commit(&acc_full[ti]);
         }
@@ -646,15 +697,14 @@ k_assign_tc(const __grid_constant__ CUtensorMap keys_map, const __grid_constant_
       Top3 top;
       top.v1 = top.v2 = top.v3 = INFINITY;
       top.j1 = top.j2 = 0x7fffffff;
-      const float4 *c2s = (const float4 *)(c2 + (int64_t)sl * c2_pitch + qtr * 64);
       for (int ch = 0; ch < nch; ++ch, ++gc) {
         const int ti = gc & 1;
-        // the two smallest of this chunk's 64 columns, in two independent
-        // streams (even and odd value pairs) so that consecutive min/max
-        // operations do not wait on one another; the columns come in four
-        // groups of 16, the TMEM load of the next group in flight while the
-        // current one is reduced
-        float p1a = INFINITY, p2a = INFINITY, p1b = INFINITY, p2b = INFINITY;
+        // the two largest of this chunk's 64 values k.c~ - |c~|^2 / 2, in two
+        // independent streams (even and odd value pairs) so that consecutive
+        // min/max operations do not wait on one another; the columns come in
+        // four groups of 16, the TMEM load of the next group in flight while
+        // the current one is reduced
+        float p1a = -INFINITY, p2a = -INFINITY, p1b = -INFINITY, p2b = -INFINITY;
         uint32_t ra[16], rb[16];
         if (!abort_s) tc_wait(&acc_full[ti], (gc >> 1) & 1, &abort_s);
         __syncwarp();
@@ -662,21 +712,13 @@ k_assign_tc(const __grid_constant__ CUtensorMap keys_map, const __grid_constant_
         const uint32_t tacc = tbase + ti * kTcN;
         tmem_ld16_async(tacc, ra);
         auto group = [&](const uint32_t(&r)[16], int g) {
-          // |c|^2 of the 16 columns (FLT_MAX past the last cluster)
-          float4 cc[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) cc[e] = __ldg(c2s + ch * (kTcN / 4) + g * 4 + e);
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const float2 lo = fma2(make_float2(-2.f, -2.f),
-                                   make_float2(__uint_as_float(r[4 * e]), __uint_as_float(r[4 * e + 1])),
-                                   make_float2(cc[e].x, cc[e].y));
-            const float2 hi = fma2(make_float2(-2.f, -2.f),
-                                   make_float2(__uint_as_float(r[4 * e + 2]), __uint_as_float(r[4 * e + 3])),
-                                   make_float2(cc[e].z, cc[e].w));
             const uint32_t l0 = g * 16 + 4 * e;
-            top2_pair(p1a, p2a, pack6_mul(lo.x, l0, m26, m64), pack6_mul(lo.y, l0 + 1, m26, m64));
-            top2_pair(p1b, p2b, pack6_mul(hi.x, l0 + 2, m26, m64), pack6_mul(hi.y, l0 + 3, m26, m64));
+            top2max_pair(p1a, p2a, pack6_mul(__uint_as_float(r[4 * e]), l0, m26, m64),
+                         pack6_mul(__uint_as_float(r[4 * e + 1]), l0 + 1, m26, m64));
+            top2max_pair(p1b, p2b, pack6_mul(__uint_as_float(r[4 * e + 2]), l0 + 2, m26, m64),
+                         pack6_mul(__uint_as_float(r[4 * e + 3]), l0 + 3, m26, m64));
           }
         };
         tc_wait_ld16(ra);
@@ -690,19 +732,21 @@ k_assign_tc(const __grid_constant__ CUtensorMap keys_map, const __grid_constant_
         group(ra, 2);
         tc_wait_ld16(rb);
         group(rb, 3);
-        const float p1 = fminf(p1a, p1b), p2 = min3f(fmaxf(p1a, p1b), p2a, p2b);
+        const float q1 = fmaxf(p1a, p1b), q2 = max3f(fminf(p1a, p1b), p2a, p2b);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) tc_arrive(&acc_empty[ti]);
-        // fold the chunk's two into the running list with column ids; the
-        // chunk's third smallest is at least p2, so p2 stands in as a lower
-        // bound for it (a key is certified to have at most two candidates
-        // only when that bound clears the margin)
+        // fold the chunk's two into the running list with column ids, as
+        // e - |k|^2 = -2 (k.c~ - |c~|^2 / 2) (exact scaling); the chunk's
+        // third smallest is at least p2, so p2 stands in as a lower bound
+        // for it (a key is certified to have at most two candidates only
+        // when that bound clears the margin)
+        const float p1 = -2.f * q1, p2 = -2.f * q2;
         const int jb = ch * kTcN + qtr * 64;
         Top3 cur;
         cur.v1 = p1; cur.v2 = p2; cur.v3 = p2;
-        cur.j1 = p1 < INFINITY ? jb + (int)(__float_as_uint(p1) & 63u) : 0x7fffffff;
-        cur.j2 = p2 < INFINITY ? jb + (int)(__float_as_uint(p2) & 63u) : 0x7fffffff;
+        cur.j1 = q1 > -INFINITY ? jb + (int)(__float_as_uint(q1) & 63u) : 0x7fffffff;
+        cur.j2 = q2 > -INFINITY ? jb + (int)(__float_as_uint(q2) & 63u) : 0x7fffffff;
         top = top3_union(top, cur);
       }
       // merge the four column quarters of each key, then decide
@@ -765,6 +809,20 @@ static bool make_map(CUtensorMap *map, const void *base, uint64_t rows, uint32_t
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, slices ? 3 : 2, const_cast<void *>(base), dims,
              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// bf16 tensor map over the filter's -|c~|^2 / 2 rows: `slices` tables of
+// `rows` rows of 16 elements, boxes of 16 x 256 with 32-byte swizzle.
+static bool make_c2b_map(CUtensorMap *map, const void *base, uint64_t rows, uint64_t slices) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {16, (cuuint64_t)rows, (cuuint64_t)slices};
+  const cuuint64_t strides[2] = {32, 32 * rows};
+  const cuuint32_t box[3] = {16, (cuuint32_t)kTcN, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Exact settlement of the queued keys: warp per entry.
@@ -1319,11 +1377,12 @@ static cudaError_t kmeans_build_t(const CtxView &v, int layer, const KmeansScrat
   }
   // tensor-core filter (bf16 keys): TMA descriptors of the keys and of the
   // whole centroid-operand table, one persistent CTA per SM
-  CUtensorMap keys_map, cent_map;
+  CUtensorMap keys_map, cent_map, c2b_map;
   int tc_grid = 0;
   if (DT == 1 && use_tc) {
-    if (!make_map(&keys_map, keys, (uint64_t)S * (uint64_t)n, kTcM) ||
-        !make_map(&cent_map, v.cent_op, (uint64_t)v.u_cap, kTcN, (uint64_t)(gs0 + S))) {
+    if (!ks.c2b || !make_map(&keys_map, keys, (uint64_t)S * (uint64_t)n, kTcM) ||
+        !make_map(&cent_map, v.cent_op, (uint64_t)v.u_cap, kTcN, (uint64_t)(gs0 + S)) ||
+        !make_c2b_map(&c2b_map, ks.c2b, (uint64_t)ks.c2_pitch, (uint64_t)S)) {
       use_tc = false;
     } else {
       int dev = 0, sms = 0;
@@ -1343,12 +1402,12 @@ static cudaError_t kmeans_build_t(const CtxView &v, int layer, const KmeansScrat
   for (int it = 0; it < iters; ++it) {
     prof.begin(kPKmOperand, st);
     cudaMemsetAsync(ks.cstat, 0, sizeof(float) * 2 * S, st);
-    launch_prepare<DT>(v, c, c_pad, ks.c2_pitch, gs0, S, ks.c2, ks.cstat, st);
+    launch_prepare<DT>(v, c, c_pad, ks.c2_pitch, gs0, S, ks.c2, ks.cstat, st, use_tc ? ks.c2b : nullptr);
     cudaMemsetAsync(ks.amb_count, 0, 2 * sizeof(int32_t), st);  // both ends of the queue
     prof.end(st);
     prof.begin(use_tc ? kPKmAssignTc : kPKmAssign, st);
     if (use_tc) {
-      k_assign_tc<<<tc_grid, kTcThreads, kTcSmem, st>>>(keys_map, cent_map, n, c, v.u_cap, ks.c2, ks.c2_pitch,
+      k_assign_tc<<<tc_grid, kTcThreads, kTcSmem, st>>>(keys_map, cent_map, c2b_map, n, c, v.u_cap,
                                                         ks.knorm, v.n_cap, ks.cstat, kTcEps, v.assign,
                                                         gs0, S, ks.amb, ks.amb_count, ks.amb_count + 1,
                                                         (int32_t)amb_cap, v.err, 1u << 26, 64u);

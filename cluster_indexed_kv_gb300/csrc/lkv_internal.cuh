@@ -17,7 +17,7 @@ constexpr int kAttnChunk = 64;     // tokens per attention work item
 constexpr int kRing = 32;          // plan slots and attention scratch slots (see Pipe)
 constexpr int kAttnStreams = 16;   // attention streams of a pipelined capture
 constexpr int kChunk = 64;         // decode steps whose boundary tests one launch runs
-constexpr int kSlots = 8 * kChunk; // step slots (queries, views): the steps of one captured graph
+constexpr int kMaxSlots = 32 * kChunk;  // step slots (queries, views) at most: the steps of the longest graph
 constexpr int kAttnMaxSplit = 8;   // CTAs per slice in one attention launch, at most
 constexpr int kStreamMaxSlices = 1024;  // slices of one call the streaming attention takes
 
@@ -76,9 +76,10 @@ struct CtxView {
   int32_t *perm;              // [slice][n_cap]
   DecState *st;               // [lb]
   void *q_prev;               // [lb][H][d] (dtype)
-  float *q_attn;              // [kSlots step slots][lb][H][d] queries * log2(e)/sqrt(d), fp32
-  int4 *aview;                // [kSlots][lb] (t, win_start, plan slot, 2 * units + flag)
-  int4 *adesc;                // [kSlots][slice] (t, win_start, plan slot, selected tokens),
+  int32_t n_slots;            // step slots: max_steps rounded up to kChunk, at most kMaxSlots
+  float *q_attn;              // [n_slots step slots][lb][H][d] queries * log2(e)/sqrt(d), fp32
+  int4 *aview;                // [n_slots][lb] (t, win_start, plan slot, 2 * units + flag)
+  int4 *adesc;                // [n_slots][slice] (t, win_start, plan slot, selected tokens),
                               // written by the selection kernel on every step
   int64_t *segsum;            // [slice][d] exact fixed-point sums (bf16) or
                               // doubles reinterpreted (fp32)
@@ -293,6 +294,7 @@ struct KmeansScratch {
   float *knorm;        // [S][n_cap]
   float *c2;           // [S][c2_pitch]: |c|^2 of the operand centroids
   int32_t c2_pitch;    // c_cap rounded up to a multiple of 256
+  uint16_t *c2b;       // [S][c2_pitch][16] bf16: -|c|^2 / 2 as a high part and remainder, then zeros
   float *cstat;        // [S][2]: max |c|, max |c|^2
   int32_t *cnt_part;   // [S][kMaxParts][c_cap] counts, then running offsets
   int32_t *count;      // [S][c_cap]
@@ -346,7 +348,7 @@ struct StepArgs {
   float *r_out;                    // [B][nl] or null
   int32_t l0;                      // first layer of this call
   int32_t slot;                    // step slot (queries, views): the step's index in a
-                                   // captured graph (0 .. kSlots - 1), else 0; the
+                                   // captured graph (0 .. n_slots - 1), else 0; the
                                    // attention's scratch is slot mod kRing
   int32_t nl;                      // layers in this call
 };

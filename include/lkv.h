@@ -182,9 +182,10 @@ lkv_status lkv_decode_step(lkv_ctx *ctx, int32_t layer, int32_t n_layers,
  *   out [n_steps][B][n_layers][H][d], selected_units
  *   [n_steps][B][n_layers][H_kv][max_clusters + max_steps], n_selected
  *   [n_steps][B][n_layers][H_kv], boundary and r_out [n_steps][B][n_layers].
- * The steps run from captured CUDA graphs of 512 steps, then of 128 and of
- * 64 for what is left (cached per argument set), so the host issues one
- * launch per 512 steps; fewer than 64 left over run one at a time. Inside the graph one kernel runs the boundary tests and
+ * The steps run from captured CUDA graphs of 2048, 512, 128 and 64 steps,
+ * longest first, each no longer than the context's step slots (max_steps
+ * rounded up to 64, at most 2048), cached per argument set, so the host
+ * issues one launch per graph; fewer than 64 left over run one at a time. Inside the graph one kernel runs the boundary tests and
  * segment bookkeeping of 64 steps at a time (they depend on the inputs
  * only); then, for an HBM pool (bf16, 4 or 8 query heads per KV head, at
  * most 1024 slices), one kernel scores and selects every retrieval of those

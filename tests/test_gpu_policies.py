@@ -209,3 +209,10 @@ def test_per_head_rejected_without_streaming_attention():
         ctx.set_policy(per_head=True)
     assert e.value.status == _lib.LKV_EINVAL
     ctx.close()
+
+
+def test_graph_of_2048_steps_matches_oracle():
+    """One call of 2100 steps replays a 2048-step graph (32 chunks, so the
+    selection of chunk j waits for the attentions of chunk j - 2) and runs
+    the last 52 steps singly; every decision and output matches the oracle."""
+    _check(_workload(local_buf=24, jump_p=0.08), 2100, dict())
