@@ -699,12 +699,17 @@ k_assign_tc(const __grid_constant__ CUtensorMap keys_map, const __grid_constant_
       top.j1 = top.j2 = 0x7fffffff;
       for (int ch = 0; ch < nch; ++ch, ++gc) {
         const int ti = gc & 1;
-        // the two largest of this chunk's 64 values k.c~ - |c~|^2 / 2, in two
-        // independent streams (even and odd value pairs) so that consecutive
-        // min/max operations do not wait on one another; the columns come in
-        // four groups of 16, the TMEM load of the next group in flight while
-        // the current one is reduced
-        float p1a = -INFINITY, p2a = -INFINITY, p1b = -INFINITY, p2b = -INFINITY;
+        // the two largest of this chunk's 64 values k.c~ - |c~|^2 / 2. The
+        // values form an 8 x 8 grid (row = 8 consecutive columns); with the
+        // row maxima R and column maxima Cm, the largest value is max R and
+        // the second largest is exactly max(second largest of R, second
+        // largest of Cm): it lies either in another row than the largest
+        // (then it is that row's maximum) or in the same row and another
+        // column (then it is that column's maximum), and no other row or
+        // column maximum exceeds it. The columns come in four groups of 16
+        // (two grid rows), the TMEM load of the next group in flight while
+        // the current one is reduced.
+        float R[8], Cm[8];
         uint32_t ra[16], rb[16];
         if (!abort_s) tc_wait(&acc_full[ti], (gc >> 1) & 1, &abort_s);
         __syncwarp();
@@ -712,13 +717,15 @@ k_assign_tc(const __grid_constant__ CUtensorMap keys_map, const __grid_constant_
         const uint32_t tacc = tbase + ti * kTcN;
         tmem_ld16_async(tacc, ra);
         auto group = [&](const uint32_t(&r)[16], int g) {
+          float x[16];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const uint32_t l0 = g * 16 + 4 * e;
-            top2max_pair(p1a, p2a, pack6_mul(__uint_as_float(r[4 * e]), l0, m26, m64),
-                         pack6_mul(__uint_as_float(r[4 * e + 1]), l0 + 1, m26, m64));
-            top2max_pair(p1b, p2b, pack6_mul(__uint_as_float(r[4 * e + 2]), l0 + 2, m26, m64),
-                         pack6_mul(__uint_as_float(r[4 * e + 3]), l0 + 3, m26, m64));
+          for (int k = 0; k < 16; ++k) x[k] = pack6_mul(__uint_as_float(r[k]), g * 16 + k, m26, m64);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) Cm[c] = g == 0 ? fmaxf(x[c], x[8 + c]) : max3f(Cm[c], x[c], x[8 + c]);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const float *y = x + 8 * h;
+            R[2 * g + h] = max3f(max3f(y[0], y[1], y[2]), max3f(y[3], y[4], y[5]), fmaxf(y[6], y[7]));
           }
         };
         tc_wait_ld16(ra);
@@ -732,7 +739,16 @@ k_assign_tc(const __grid_constant__ CUtensorMap keys_map, const __grid_constant_
         group(ra, 2);
         tc_wait_ld16(rb);
         group(rb, 3);
-        const float q1 = fmaxf(p1a, p1b), q2 = max3f(fminf(p1a, p1b), p2a, p2b);
+        // the two largest of R and of Cm (pairwise: the first pair seeds the
+        // list, each further pair is merged into it)
+        float r1 = fmaxf(R[0], R[1]), r2 = fminf(R[0], R[1]);
+        float c1 = fmaxf(Cm[0], Cm[1]), c2 = fminf(Cm[0], Cm[1]);
+#pragma unroll
+        for (int k = 2; k < 8; k += 2) {
+          top2max_pair(r1, r2, R[k], R[k + 1]);
+          top2max_pair(c1, c2, Cm[k], Cm[k + 1]);
+        }
+        const float q1 = r1, q2 = fmaxf(r2, c2);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) tc_arrive(&acc_empty[ti]);
