@@ -350,6 +350,10 @@ __global__ void __launch_bounds__(kBoundaryThreads, 2) k_step_boundary(CtxView v
   //    (a segment closed during this step restarted the sum at zero)
   const bool restarted = st.n_closed != n_closed0;
   int slow = 0;
+  // a segment spans at most L tokens: with every |key| below 2^(e_hi - 126)
+  // its sum of magnitudes stays below 2^13, so the exact sum is also the
+  // token-order double sum
+  const uint32_t e_hi = min(131u, 139u - (32u - (uint32_t)__clz(max(v.L, 1) - 1)));
 #pragma unroll
   for (int r = 0; r < kMaxPer; ++r) {
     const int x = tid + r * nth;
@@ -361,7 +365,7 @@ __global__ void __launch_bounds__(kBoundaryThreads, 2) k_step_boundary(CtxView v
     if constexpr (DT == 1) {
       ((uint16_t *)v.dec_k)[di] = (uint16_t)(kbits[r] >> 16);
       ((uint16_t *)v.dec_v)[di] = (uint16_t)(kbits[r] & 0xffffu);
-      ssum[r] = prev + bf16_fixed40((uint16_t)(kbits[r] >> 16), &slow);
+      ssum[r] = prev + bf16_fixed40((uint16_t)(kbits[r] >> 16), &slow, e_hi);
     } else {
       ((float *)v.dec_k)[di] = __uint_as_float(kbits[r]);
       ((float *)v.dec_v)[di] = __uint_as_float(vbits[DT == 1 ? 0 : r]);

@@ -1133,8 +1133,24 @@ __global__ void k_scatter(const int32_t *assign, int64_t n, int64_t n_cap, int32
 // the loads overlap; the sums still take the members in token order. A
 // persistent grid whose warps take clusters in turn keeps a long cluster from
 // holding up others.
+//
+// bf16 member sums are formed exactly in 2^-40 fixed point. That is the
+// token-order double sum too while every partial sum fits 53 bits. Every
+// partial sum is a multiple of 2^(e_min - 134), e_min the smallest biased
+// exponent among the nonzero members, and at most the sum of magnitudes A:
+// it fits when A < 2^(e_min - 81). A cluster of at most 256 members (each
+// below 32, e_min >= 94) always qualifies; a larger one is checked with its
+// e_min and a float sum of magnitudes. Any other cluster is summed in
+// double precision in token order.
+//
+// The mean is sum / count rounded to double, then to float. It is formed
+// without a double division: with y = RN(1/count), q = RN(sum * y) is
+// within an ulp of the quotient, and q + (sum - count q) y rounded once
+// (two FMAs, the remainder exact) is the correctly rounded quotient
+// (Markstein's theorem on division by a correctly rounded reciprocal).
 constexpr int kUpdBatch = 8;
 constexpr int kUpdThreads = 256;
+constexpr int32_t kUpdExactCount = 256;
 
 template <int DT>
 __device__ __forceinline__ void load4(const void *keys, int64_t row, int lane, float (&x)[4],
@@ -1144,6 +1160,51 @@ __device__ __forceinline__ void load4(const void *keys, int64_t row, int lane, f
   } else {
     const float4 f = __ldg((const float4 *)((const float *)keys + row * kHeadDim + lane * 4));
     x[0] = f.x; x[1] = f.y; x[2] = f.z; x[3] = f.w;
+  }
+}
+
+__device__ __forceinline__ float mean_rn(double sum, double cnt, double y) {
+  const double q = __dmul_rn(sum, y);
+  const double r = __fma_rn(-q, cnt, sum);
+  return __double2float_rn(__fma_rn(r, y, q));
+}
+
+__device__ __forceinline__ uint32_t bf16_exp_nz(uint32_t bits16) {
+  const uint32_t e = (bits16 >> 7) & 0xffu;
+  return (bits16 & 0x7fffu) ? e : 255u;  // zeros do not set the grid
+}
+
+// Exact fixed-point sums of a cluster's bf16 members (this lane's four
+// dimensions); big (warp-uniform): also the smallest biased exponent of the
+// nonzero members and the float sum of magnitudes.
+__device__ __forceinline__ void fixed_sums(const void *keys, const int32_t *pm, int32_t cnt, int64_t row0,
+                                           int lane, bool big, int64_t (&acc)[4], int &oor, uint32_t &e_min,
+                                           float &asum) {
+  for (int32_t m0 = 0; m0 < cnt; m0 += kUpdBatch) {
+    const int nb = min(kUpdBatch, cnt - m0);
+    const int32_t mine = lane < nb ? __ldg(pm + m0 + lane) : 0;
+    uint2 raw[kUpdBatch];
+    float unused[4];
+#pragma unroll
+    for (int b = 0; b < kUpdBatch; ++b) {
+      const int32_t i = __shfl_sync(0xffffffffu, mine, b);
+      if (b < nb) load4<1>(keys, row0 + i, lane, unused, raw[b]);
+    }
+#pragma unroll
+    for (int b = 0; b < kUpdBatch; ++b) {
+      if (b < nb) {
+        acc[0] += bf16_fixed40((uint16_t)(raw[b].x & 0xffffu), &oor);
+        acc[1] += bf16_fixed40((uint16_t)(raw[b].x >> 16), &oor);
+        acc[2] += bf16_fixed40((uint16_t)(raw[b].y & 0xffffu), &oor);
+        acc[3] += bf16_fixed40((uint16_t)(raw[b].y >> 16), &oor);
+        if (big) {
+          e_min = min(e_min, min(min(bf16_exp_nz(raw[b].x), bf16_exp_nz(raw[b].x >> 16)),
+                                 min(bf16_exp_nz(raw[b].y), bf16_exp_nz(raw[b].y >> 16))));
+          asum += (__uint_as_float((raw[b].x & 0x7fffu) << 16) + __uint_as_float((raw[b].x >> 16 & 0x7fffu) << 16)) +
+                  (__uint_as_float((raw[b].y & 0x7fffu) << 16) + __uint_as_float((raw[b].y >> 16 & 0x7fffu) << 16));
+        }
+      }
+    }
   }
 }
 
@@ -1163,30 +1224,22 @@ __global__ void __launch_bounds__(kUpdThreads, 3) k_update(const void *keys, int
   const int64_t gs = gs0 + s;
   const int32_t *pm = perm + gs * n_cap + base;
   const int64_t row0 = (int64_t)s * n;
+  const double cd = (double)cnt, y = __drcp_rn(cd);
   double sum[4] = {0.0, 0.0, 0.0, 0.0};
   bool slow = (DT == 0);
   if constexpr (DT == 1) {
     int64_t acc[4] = {0, 0, 0, 0};
     int oor = 0;
-    for (int32_t m0 = 0; m0 < cnt; m0 += kUpdBatch) {
-      const int nb = min(kUpdBatch, cnt - m0);
-      const int32_t mine = lane < nb ? __ldg(pm + m0 + lane) : 0;
-      uint2 raw[kUpdBatch];
-      float unused[4];
-#pragma unroll
-      for (int b = 0; b < kUpdBatch; ++b) {
-        const int32_t i = __shfl_sync(0xffffffffu, mine, b);
-        if (b < nb) load4<DT>(keys, row0 + i, lane, unused, raw[b]);
-      }
-#pragma unroll
-      for (int b = 0; b < kUpdBatch; ++b) {
-        if (b < nb) {
-          acc[0] += bf16_fixed40((uint16_t)(raw[b].x & 0xffffu), &oor);
-          acc[1] += bf16_fixed40((uint16_t)(raw[b].x >> 16), &oor);
-          acc[2] += bf16_fixed40((uint16_t)(raw[b].y & 0xffffu), &oor);
-          acc[3] += bf16_fixed40((uint16_t)(raw[b].y >> 16), &oor);
-        }
-      }
+    uint32_t e_min = 255u;
+    float asum = 0.f;
+    const bool big = cnt > kUpdExactCount;
+    fixed_sums(keys, pm, cnt, row0, lane, big, acc, oor, e_min, asum);
+    if (big && e_min < 255u) {
+      // the float sum of 4 cnt magnitudes is at least (1 - 4 cnt 2^-24) A,
+      // so at least 7/8 A for cnt < 2^19: below 7/8 of the limit, A is
+      // below the limit
+      const float lim = __uint_as_float((e_min - 81u + 127u) << 23) * 0.875f;
+      if (!(asum < lim) || cnt >= (1 << 19)) oor = 1;
     }
     slow = __any_sync(0xffffffffu, oor) != 0;
     if (!slow) {
@@ -1237,8 +1290,8 @@ __global__ void __launch_bounds__(kUpdThreads, 3) k_update(const void *keys, int
     }
   }
   float *dst = cent32 + (gs * u_cap + j) * kHeadDim + lane * 4;
-#pragma unroll
-  for (int e = 0; e < 4; ++e) dst[e] = __double2float_rn(__ddiv_rn(sum[e], (double)cnt));
+  *(float4 *)dst = make_float4(mean_rn(sum[0], cd, y), mean_rn(sum[1], cd, y), mean_rn(sum[2], cd, y),
+                               mean_rn(sum[3], cd, y));
   }
 }
 

@@ -268,13 +268,17 @@ __device__ __forceinline__ uint32_t desc_key(float s) {
 
 // Exact fixed-point accumulation of bf16 values: v * 2^40 as int64 is exact
 // for 2^-33 <= |v| < 32 (biased exponent 94..131) and the sum of up to 2^18
-// such terms cannot overflow. Values outside that range (other than zero)
-// set *slow so the caller can fall back to double-precision token-order sums.
-__device__ __forceinline__ int64_t bf16_fixed40(uint16_t bits, int *slow) {
+// such terms cannot overflow. Values outside 94..e_hi (other than zero) set
+// *slow so the caller can fall back to double-precision token-order sums.
+// The exact sum equals a token-order double sum only while every partial
+// sum fits 53 bits, i.e. stays below 2^13 in magnitude: callers bound the
+// sum of magnitudes, either through e_hi and the number of terms or with a
+// running sum of |v|.
+__device__ __forceinline__ int64_t bf16_fixed40(uint16_t bits, int *slow, uint32_t e_hi = 131u) {
   uint32_t e = (bits >> 7) & 0xffu;
   uint32_t m = bits & 0x7fu;
   if (e == 0 && m == 0) return 0;
-  if (e < 94u || e > 131u) { *slow = 1; return 0; }
+  if (e < 94u || e > e_hi) { *slow = 1; return 0; }
   int64_t mag = (int64_t)(128u + m) << (e - 94u);
   return (bits & 0x8000u) ? -mag : mag;
 }

@@ -11,6 +11,23 @@ import synth
 ATOL, RTOL = 2e-3, 1e-2   # attention outputs: bf16 in, fp32 accumulate
 
 
+def rounding_update_keys():
+    """1024 bf16 keys in two far-apart groups of 512 (all dimensions 16, and
+    all -16). In token order, dimension 0 of the first group holds 497 x 16,
+    10 x 24 and 2^-11 (partial sums reach 2^13 = 8192 + 2^-11), then
+    -2^-33, 2^-33 + 2^-40, -2^-33, 2^-33 + 2^-40. A double-precision sum in
+    token order rounds each 2^-40 away (a tie to even at 2^13) and ends at
+    8192 + 2^-11, whose mean 16 + 2^-20 is a float midpoint that rounds to
+    16. The exact sum carries 2^-39 more, and its mean rounds to 16 + 2^-19.
+    Returns (keys [1024, 128] float32, an init seed that draws one key from
+    each group)."""
+    keys = np.full((1024, 128), 16.0, np.float32)
+    keys[512:] = -16.0
+    col = [16.0] * 497 + [24.0] * 10 + [2.0 ** -11] + [-2.0 ** -33, 2.0 ** -33 + 2.0 ** -40] * 2
+    keys[:512, 0] = np.array(col, np.float64).astype(np.float32)
+    return keys, 8
+
+
 def make_ctx(w: synth.Workload, max_steps=None, max_budget=None):
     import cluster_indexed_kv_gb300 as lkv
     return lkv.Context(batch=w.batch, n_layers=w.n_layers, n_kv_heads=w.n_kv_heads,

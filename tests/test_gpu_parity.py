@@ -74,6 +74,30 @@ def test_kmeans_duplicate_keys_tie_to_lowest():
     ctx.close()
 
 
+def test_kmeans_update_sums_in_token_order_past_2_13():
+    """A cluster of 512 members whose dimension-0 partial sums pass 2^13 and
+    whose small members fall below the double-precision ulp there: the
+    token-order double sum rounds, the exact fixed-point sum does not, and
+    the two means differ in their last float bit. The update must give the
+    token-order result (here 16.0), bit for bit with the oracle."""
+    keys, seed = H.rounding_update_keys()
+    w = synth.WORKLOADS["long_in"].replace(n_kv_heads=1, batch=1, n_prefill=1024, n_clusters=2,
+                                           iters=3)
+    K = torch.from_numpy(keys).to(torch.bfloat16).reshape(1, 1, 1024, 128).cuda()
+    V = torch.zeros_like(K)
+    ctx = H.make_ctx(w)
+    ctx.build_index(0, K, V, 2, 3, seed)
+    g = ctx.get_index(0, 0, 0, 1024)
+    o = oracle.kmeans(synth.to_oracle(K[0, 0]), 2, 3, seed)
+    st = ctx.decode_state(0, 0)
+    ctx.close()
+    assert np.array_equal(g["assign"], o["assign"])
+    assert np.array_equal(g["centroids"].view(np.uint32), o["cent"].view(np.uint32))
+    a = int(o["assign"][0])
+    assert o["cent"][a, 0] == np.float32(16.0)
+    assert st["n_inexact"] >= 1  # the cluster left the fixed-point path
+
+
 def _decode_check(w, *, tau=None, budget=None, T=None, seqs=None, teacher=True, build_seed=3):
     T = T or w.n_steps
     dev = "cuda"

@@ -123,6 +123,26 @@ def test_update_is_member_mean_and_empty_keeps_centroid():
         assert np.array_equal(centb[j], want)
 
 
+def test_update_sums_in_token_order_not_exactly():
+    """The member sums are double-precision sums in token order, rounded at
+    every step (the plain reading of "fp64 member sums"), not the exact sum
+    rounded once. On this construction the two give means one float ulp
+    apart: 16.0 from the token-order sum, 16 + 2^-19 from the exact one."""
+    from fractions import Fraction
+    from tests import _harness as H
+    keys, _ = H.rounding_update_keys()
+    kb = bf16(keys)
+    assert np.array_equal(unbf16(kb), keys)  # every value is a bf16
+    a = np.repeat(np.arange(2, dtype=np.int32), 512)
+    cent, cnt, inexact = oracle.update(kb, a, np.zeros((2, 128), np.float32))
+    assert cnt.tolist() == [512, 512]
+    assert inexact == 2  # the two additions of 2^-33 + 2^-40 round (ties to even)
+    assert cent[0, 0] == np.float32(16.0)
+    exact = sum(Fraction(float(x)) for x in keys[:512, 0]) / 512
+    assert np.float32(float(exact)) == np.float32(16.0 + 2.0 ** -19)
+    assert np.all(cent[0, 1:] == 16.0) and np.all(cent[1] == -16.0)
+
+
 def test_well_separated_mixture_recovers_partition():
     # textbook case: components far apart, one initial centroid per component
     # -> one Lloyd round returns the generating partition and its means
