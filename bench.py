@@ -274,6 +274,53 @@ def attn_roofline(kern, ctr, w, eb):
     return n_attn, ms_attn, alg, sec, alg / sec / 1e9
 
 
+def read_ceiling(torch, nbytes, flush, hbm_peak, reps=16):
+    """Event-timed single launches of lkv_read_ceiling over nbytes of device
+    memory, L2 overwritten before each (as in the attention's roofline
+    pass): the rate one launch that reads that many bytes reaches."""
+    from cluster_indexed_kv_gb300 import _lib
+    nbytes = int(nbytes) // 16 * 16
+    buf = torch.ones(nbytes // 4, dtype=torch.int32, device="cuda")
+    st = torch.cuda.current_stream()
+    ms = 0.0
+    for r in range(reps + 2):
+        flush.fill_(float(r))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        _lib.lkv_read_ceiling(buf.data_ptr(), nbytes, st.cuda_stream)
+        e1.record(st)
+        e1.synchronize()
+        if r >= 2:
+            ms += e0.elapsed_time(e1)
+    sec = ms / reps / 1e3
+    del buf
+    return {"bytes": nbytes, "avg_launch_us": sec * 1e6, "achieved": nbytes / sec / 1e9,
+            "frac_of_hbm": nbytes / sec / 1e9 / hbm_peak, "unit": "GB/s",
+            "kernel": "lkv_read_ceiling: plain 16-byte loads over a grid that fills the GPU",
+            "l2": "256 MB written before every launch"}
+
+
+def in_graph_attention(g_bytes, g_sec, launches, hbm_peak):
+    """The attention as the timed decode graph runs it: algorithmic bytes
+    per step over the decode time per step, and the DRAM bytes per step of
+    a whole 512-step graph from the committed ncu record (cache control
+    off). Consecutive steps attend nearly the same rows (the selection
+    changes only at retrieval steps), so most of them come from L2: the
+    algorithmic rate is not an HBM rate."""
+    dram = ncu_traffic("lkv_attn_graph", g_bytes)
+    out = {"achieved_alg": g_bytes / g_sec / 1e9, "frac_alg_of_hbm": g_bytes / g_sec / 1e9 / hbm_peak,
+           "unit": "GB/s", "alg_bytes_per_step": g_bytes, "us_per_step": g_sec * 1e6,
+           "steps": launches, "dram_bytes_per_step": dram,
+           "timing": "CUDA events on the context stream around the timed decode graphs; about nine "
+                     "attentions overlap, and the time per step includes the boundary and "
+                     "selection kernels"}
+    if dram is not None:
+        out["dram_GBps"] = dram / g_sec / 1e9
+        out["dram_frac_of_hbm"] = dram / g_sec / 1e9 / hbm_peak
+        out["l2_served_frac"] = 1.0 - dram / g_bytes
+    return out
+
+
 def timed_decode(torch, ctx, q, kn, vn, tau, budget, out, warm, n, boundary=None, **kw):
     """Decode steps warm .. warm + n - 1 through the graph path, timed with
     CUDA events on the context stream, after an untimed call for steps
@@ -354,7 +401,10 @@ def run_ours(args, rank, world, local):
     def one_step():
         build_all()
         ev["mid"].record(stream)
+        # an NVTX range around the decode lets a profiler select its graphs
+        torch.cuda.nvtx.range_push("decode_steps")
         ctx.decode_steps(0, q, kn, vn, w.tau, w.budget, out, n_layers=NL, boundary=bnd)
+        torch.cuda.nvtx.range_pop()
 
     ev["mid"] = torch.cuda.Event(enable_timing=True)
     for _ in range(args.warmup):
@@ -415,6 +465,7 @@ def run_ours(args, rank, world, local):
     eb = 2 if w.dtype == "bf16" else 4
     n_attn, ms_attn, alg_bytes, attn_s, achieved = attn_roofline(kern_p, ctr, w, eb)
     g_launches = T * K_steps  # one attention launch per step covers all NL layers
+    ceiling = read_ceiling(torch, alg_bytes, flush, hbm_peak)
     g_bytes, g_sec = graph_attention(ctr_timed, w, eb, dec_ms, g_launches)
     breakdown = {k: {"launches": int(v[0]), "avg_us": round(v[1] / v[0] * 1e3, 2)}
                  for k, v in kern_p.items() if v[0]}
@@ -480,24 +531,15 @@ def run_ours(args, rank, world, local):
         "kmeans_mkeys_per_s": mkeys,
         "decode_ms_per_bench_step": dec_ms / K_steps, "build_ms_per_bench_step": build_ms / K_steps,
         "trigger_rate": trig, "kmeans_refined_keys_total": st["n_refined"],
-        "roofline": {"kernel": "lkv_attn", "bound": "hbm", "achieved": g_bytes / g_sec / 1e9,
-                     "peak": hbm_peak, "unit": "GB/s", "frac": g_bytes / g_sec / 1e9 / hbm_peak,
-                     "traffic": ncu_traffic("lkv_attn_graph", g_bytes),
+        "roofline": {"kernel": "lkv_attn", "bound": "hbm", "achieved": achieved, "peak": hbm_peak,
+                     "unit": "GB/s", "frac": achieved / hbm_peak,
+                     "traffic": ncu_traffic("lkv_attn", alg_bytes),
                      "peak_source": f"{peak_kind} hbm_gbs (burst copy)",
-                     "alg_bytes_per_launch": g_bytes, "avg_launch_us": g_sec * 1e6,
-                     "launches": g_launches,
-                     "timing": "CUDA events on the context stream around the timed decode graphs; "
-                               "launches overlap about nine deep, so the time per launch is the "
-                               "timed decode time over the launches, with the boundary and "
-                               "selection kernels' time inside it",
-                     "l2": "the rows of a step (49 MB) do not stay in L2 across the steps "
-                           "behind it; ncu's record of graph nodes reads them from DRAM",
-                     "isolated_launch": {
-                         "achieved": achieved, "frac": achieved / hbm_peak,
-                         "traffic": ncu_traffic("lkv_attn", alg_bytes),
-                         "alg_bytes_per_launch": alg_bytes, "avg_launch_us": attn_s * 1e6,
-                         "launches": int(n_attn),
-                         "l2": "single-step launches, 256 MB written before every step"}},
+                     "alg_bytes_per_launch": alg_bytes, "avg_launch_us": attn_s * 1e6,
+                     "launches": int(n_attn), "l2": "single-step launches, 256 MB written before every step",
+                     "single_launch_read_ceiling": ceiling,
+                     "frac_of_single_launch_ceiling": achieved / ceiling["achieved"],
+                     "in_graph": in_graph_attention(g_bytes, g_sec, g_launches, hbm_peak)},
         "roofline_kmeans_assign": {
             "kernel": "k_assign_tc" if km_kernel == "kmeans_assign_tc" else "k_assign_simt",
             "bound": "tensor", "achieved": km_tf, "peak": tc_peak, "unit": "TFLOP/s",

@@ -21,7 +21,7 @@ EXPORTED = ("lkv_create", "lkv_destroy", "lkv_build_index", "lkv_load_index",
             "lkv_decode_step", "lkv_decode_steps", "lkv_get_index", "lkv_get_decode_state",
             "lkv_sync", "lkv_last_error", "lkv_set_profiling", "lkv_get_profile",
             "lkv_kmeans_static", "lkv_kmeans_static_status", "lkv_set_kmeans_filter",
-            "lkv_diag_wait_timeout", "lkv_uva_read", "lkv_set_policy", "lkv_build_pages",
+            "lkv_diag_wait_timeout", "lkv_uva_read", "lkv_read_ceiling", "lkv_set_policy", "lkv_build_pages",
             "lkv_build_index_async", "lkv_build_paris", "lkv_paris_levels")
 LKV_FILTER_TENSOR, LKV_FILTER_SIMT = 0, 1
 LKV_TRIGGER_ADAPTIVE, LKV_TRIGGER_EVERY, LKV_TRIGGER_INTERVAL = 0, 1, 2
@@ -114,6 +114,8 @@ def load(path: str = LIB_PATH):
         L.lkv_kmeans_static_status.restype = st
         L.lkv_uva_read.argtypes = [vp, vp, i64, vp]
         L.lkv_uva_read.restype = st
+        L.lkv_read_ceiling.argtypes = [vp, i64, vp]
+        L.lkv_read_ceiling.restype = st
         L.lkv_diag_wait_timeout.argtypes = [vp, i64]
         L.lkv_diag_wait_timeout.restype = st
         L.lkv_set_policy.argtypes = [vp, C.POINTER(lkv_policy)]
@@ -243,6 +245,10 @@ def lkv_kmeans_static_status(stream_ptr) -> None:
 
 def lkv_uva_read(host_ptr, dev_ptr, nbytes: int, stream_ptr) -> None:
     _check(load().lkv_uva_read(host_ptr, dev_ptr, nbytes, stream_ptr), None)
+
+
+def lkv_read_ceiling(dev_ptr, nbytes: int, stream_ptr) -> None:
+    _check(load().lkv_read_ceiling(dev_ptr, nbytes, stream_ptr), None)
 
 
 def lkv_diag_wait_timeout(ctx, limit_ns: int) -> None:

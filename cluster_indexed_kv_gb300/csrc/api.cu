@@ -783,6 +783,26 @@ lkv_status lkv_uva_read(const void *host_src, void *dev_dst, int64_t bytes, void
   return LKV_OK;
 }
 
+lkv_status lkv_read_ceiling(const void *dev_src, int64_t bytes, void *stream) {
+  if (!dev_src || bytes < 0 || bytes % 16 != 0 || (uintptr_t)dev_src % 16 != 0) {
+    lkv::set_unbound_error("lkv_read_ceiling: null pointer, or size/address not a multiple of 16");
+    return LKV_EINVAL;
+  }
+  cudaPointerAttributes attr{};
+  cudaError_t e = cudaPointerGetAttributes(&attr, dev_src);
+  if (e != cudaSuccess || attr.type != cudaMemoryTypeDevice) {
+    cudaGetLastError();
+    lkv::set_unbound_error("lkv_read_ceiling: dev_src is not device memory");
+    return LKV_EINVAL;
+  }
+  e = lkv::launch_read_ceiling(dev_src, bytes, (cudaStream_t)stream);
+  if (e != cudaSuccess) {
+    lkv::set_unbound_error((std::string("lkv_read_ceiling: ") + cudaGetErrorString(e)).c_str());
+    return LKV_ECUDA;
+  }
+  return LKV_OK;
+}
+
 lkv_status lkv_diag_wait_timeout(lkv_ctx *c, int64_t limit_ns) {
   lkv_status s = check_usable(c);
   if (s != LKV_OK) return s;

@@ -2823,6 +2823,42 @@ cudaError_t launch_uva_read(const void *host_src, void *dev_dst, int64_t bytes, 
   return cudaGetLastError();
 }
 
+// Single-launch read ceiling of device memory: the same grid and load
+// pattern as k_uva_read, reads only (each thread folds its loads into one
+// word, stored only when it matches a value no input of the measurement
+// gives, so the loads cannot be dropped). A decode step's attention reads
+// its rows in one launch; this kernel reads the same number of bytes
+// contiguously, so its event-timed rate bounds what one launch of that size
+// reaches.
+__device__ uint32_t g_read_sink;
+
+__global__ void __launch_bounds__(256) k_read_ceiling(const uint4 *src, int64_t n16) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  uint32_t acc = 0;
+  for (; i + 7 * stride < n16; i += 8 * stride) {
+    uint4 r[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) r[e] = __ldcg(src + i + e * stride);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc ^= r[e].x ^ r[e].y ^ r[e].z ^ r[e].w;
+  }
+  for (; i < n16; i += stride) {
+    const uint4 r = __ldcg(src + i);
+    acc ^= r.x ^ r.y ^ r.z ^ r.w;
+  }
+  if (acc == 0x9e3779b9u) g_read_sink = acc;
+}
+
+cudaError_t launch_read_ceiling(const void *src, int64_t bytes, cudaStream_t st) {
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  k_read_ceiling<<<sms * 8, 256, 0, st>>>((const uint4 *)src, bytes / 16);
+  return cudaGetLastError();
+}
+
 // ---------------------------------------------------------------- failure-path check
 
 // One CTA waits on an mbarrier that nothing completes. The wait gives up

@@ -403,6 +403,7 @@ cudaError_t launch_decode_steps(const CtxView &v, const StepArgs &a, int n_steps
 // Streaming read of `bytes` (a multiple of 16) of pinned host memory into
 // device memory by plain 16-byte loads over UVA (the host-link ceiling).
 cudaError_t launch_uva_read(const void *host_src, void *dev_dst, int64_t bytes, cudaStream_t stream);
+cudaError_t launch_read_ceiling(const void *src, int64_t bytes, cudaStream_t stream);
 // One CTA whose bounded wait on a barrier nobody completes runs out after
 // limit_ns and records kErrTimeout (tests the failure path).
 cudaError_t launch_diag_wait(const CtxView &v, uint64_t limit_ns, cudaStream_t stream);

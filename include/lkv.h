@@ -424,6 +424,16 @@ lkv_status lkv_get_decode_state(lkv_ctx *ctx, int32_t layer, int32_t seq,
  * lkv_last_error(NULL)). */
 lkv_status lkv_uva_read(const void *host_src, void *dev_dst, int64_t bytes, void *stream);
 
+/* Single-launch read ceiling of device memory (no counterpart in the pages):
+ * one kernel reads `bytes` of device memory at dev_src with plain 16-byte
+ * loads over a grid that fills the GPU, and writes nothing the caller sees.
+ * A decode step's attention reads its rows in one launch; timing this call
+ * with CUDA events on the same number of bytes (L2 overwritten first) gives
+ * the rate one launch of that size reaches. dev_src: device memory, 16-byte
+ * aligned; bytes a multiple of 16. Asynchronous on `stream` (cudaStream_t or
+ * NULL). Errors: LKV_EINVAL, LKV_ECUDA (text via lkv_last_error(NULL)). */
+lkv_status lkv_read_ceiling(const void *dev_src, int64_t bytes, void *stream);
+
 /* Failure-path check (no counterpart in the pages): launches, on the
  * context's stream, one CTA that waits on a barrier that nothing completes.
  * The wait gives up after limit_ns nanoseconds (0..1e9, else LKV_EINVAL) and

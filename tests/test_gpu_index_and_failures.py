@@ -150,3 +150,15 @@ def test_uva_read_copies_pinned_host_memory():
     with pytest.raises(_lib.LKVError) as e:
         _lib.lkv_uva_read(pageable.data_ptr(), dst.data_ptr(), 64, None)
     assert e.value.status == _lib.LKV_EINVAL
+
+
+def test_read_ceiling_reads_device_memory_and_checks_arguments():
+    n = (5 << 20) + 32  # not a multiple of the grid's 8-deep stride
+    src = torch.randint(0, 255, (n,), dtype=torch.uint8, device="cuda")
+    _lib.lkv_read_ceiling(src.data_ptr(), n, None)
+    torch.cuda.synchronize()
+    host = torch.zeros(64, dtype=torch.uint8)
+    for args in ((host.data_ptr(), 64), (src.data_ptr(), 24), (src.data_ptr() + 8, 64)):
+        with pytest.raises(_lib.LKVError) as e:
+            _lib.lkv_read_ceiling(args[0], args[1], None)
+        assert e.value.status == _lib.LKV_EINVAL
