@@ -217,7 +217,9 @@ __device__ __forceinline__ void assign_decide(const Top3 &t, int32_t c, float kn
   const bool valid = t.j1 < c && (c == 1 || t.j2 < c);
   *assign_row = t.j1 < c ? t.j1 : 0;
   if (c == 1 || (valid && t.v2 - t.v1 > beta2)) return;
-  const bool crowded = !valid || ((c > 2) && !(t.v3 - t.v1 > beta2));
+  // (the tensor-core filter's indices can name another cell only where two
+  // values lie within 2^-20 relative of each other, far inside 2^-6 beta)
+  const bool crowded = !valid || ((c > 2) && !(t.v3 - t.v1 > beta2 * (1.f + 0x1p-6f)));
   const int slot = atomicAdd(crowded ? amb_crowd : amb_count, 1);
   if (slot < amb_cap)
     amb[crowded ? amb_cap - 1 - slot : slot] = make_int4(s, (int)row, t.j1, t.j2);
@@ -366,10 +368,10 @@ k_assign_simt(const void *keys, int64_t n, int32_t c, const void *cent_op,
 // TMEM, two accumulators so MMAs of chunk n+1 overlap the epilogue of chunk
 // n). Warp 0 issues the TMA loads (128B-swizzled K-major tiles), warp 1 the
 // MMAs and owns the tensor memory, warps 2..17 read the accumulators (four
-// warps per TMEM lane quadrant, one per 64-column quarter of a chunk), form
-// e_j = |c~_j|^2 - 2 k.c~_j and keep the three smallest per key; the same
-// certified decision as the SIMT filter follows (eps covers the tensor-core
-// fp32 accumulation error with a wide margin).
+// warps per TMEM lane quadrant, one per 64-column quarter of a chunk), keep
+// the two best per 64-column block and fold them, as e_j - |k|^2, into each
+// key's best three; the same certified decision as the SIMT filter follows
+// (eps covers the tensor-core fp32 accumulation error with a wide margin).
 constexpr int kTcM = 128;
 constexpr int kTcN = 256;
 constexpr int kTcEpiWarps = 16;
@@ -390,8 +392,8 @@ constexpr uint32_t kTcIdesc = (1u << 4)            // fp32 accumulator
 constexpr uint64_t kTcWaitNs = 2000000000ull;
 // Filter margin: 2^-13 bounds the tensor-core fp32 accumulation error of a
 // 128-term bf16 dot product with a wide safety factor; 2^-15 covers the
-// column id carried in the low mantissa bits of each value (2^-17) and the
-// bf16 pair that stands for |c~|^2 / 2 (2^-17 of it).
+// row or column index carried in the low mantissa bits of the maxima
+// (2^-20) and the bf16 pair that stands for |c~|^2 / 2 (2^-17 of it).
 constexpr float kTcEps = 0x1p-13f + 0x1p-15f;
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
@@ -480,16 +482,16 @@ __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
   return d;
 }
 
-// Branch-free candidate tracking for the tensor-core filter. A value carries
-// its column's position among the thread's 64 columns of a chunk in the low
-// six mantissa bits (a relative change below 2^-17, covered by the filter's
-// margin), so the two smallest values keep their columns without separate
-// index bookkeeping. The bits are formed with integer multiplies,
-// (e >> 6) * 64 + local, with the multipliers 2^26 and 64 passed in at run
-// time: the min/max network already loads the ALU pipe, and multiplies issue
-// on the FMA pipe (measured faster than a single logic operation on the ALU).
-__device__ __forceinline__ float pack6_mul(float e, uint32_t local, uint32_t m26, uint32_t m64) {
-  return __uint_as_float(__umulhi(__float_as_uint(e), m26) * m64 + local);
+// Index tracking for the tensor-core filter. A row or column maximum of a
+// chunk's 8 x 8 grid of values carries its row or column index in the low
+// three mantissa bits (a relative change below 2^-20, covered by the filter's
+// margin), so the top-2 network keeps the indices without separate
+// bookkeeping. The bits are formed with integer multiplies,
+// (e >> 3) * 8 + local, with the multipliers 2^29 and 8 passed in at run
+// time: the min/max network loads the ALU pipe, and multiplies issue on the
+// FMA pipe (measured faster than a single logic operation on the ALU).
+__device__ __forceinline__ float pack3_mul(float e, uint32_t local, uint32_t m29, uint32_t m8) {
+  return __uint_as_float(__umulhi(__float_as_uint(e), m29) * m8 + local);
 }
 __device__ __forceinline__ float min3f(float a, float b, float c) {
   float d;
@@ -573,7 +575,7 @@ k_assign_tc(const __grid_constant__ CUtensorMap keys_map, const __grid_constant_
             const __grid_constant__ CUtensorMap c2b_map, int64_t n, int32_t c, int32_t u_cap, const float *knorm,
             int64_t n_cap, const float *cstat, float eps, int32_t *assign, int64_t gs0, int n_slices,
             int4 *amb, int32_t *amb_count, int32_t *amb_crowd, int32_t amb_cap, int32_t *err,
-            uint32_t m26, uint32_t m64) {
+            uint32_t m29, uint32_t m8) {
   extern __shared__ unsigned char tc_smem_raw[];
   __shared__ __align__(8) uint64_t a_full[2], a_empty[2], b_full[2], b_empty[2], acc_full[2], acc_empty[2];
   __shared__ __align__(8) uint64_t mma_done;
@@ -700,15 +702,21 @@ k_assign_tc(const __grid_constant__ CUtensorMap keys_map, const __grid_constant_
       for (int ch = 0; ch < nch; ++ch, ++gc) {
         const int ti = gc & 1;
         // the two largest of this chunk's 64 values k.c~ - |c~|^2 / 2. The
-        // values form an 8 x 8 grid (row = 8 consecutive columns); with the
-        // row maxima R and column maxima Cm, the largest value is max R and
-        // the second largest is exactly max(second largest of R, second
-        // largest of Cm): it lies either in another row than the largest
-        // (then it is that row's maximum) or in the same row and another
-        // column (then it is that column's maximum), and no other row or
-        // column maximum exceeds it. The columns come in four groups of 16
-        // (two grid rows), the TMEM load of the next group in flight while
-        // the current one is reduced.
+        // values form an 8 x 8 grid (row = 8 consecutive columns) with row
+        // maxima R and column maxima Cm, taken on the raw values. The largest
+        // value M is max R, at (row of max R, column of max Cm). The second
+        // largest x2 is exactly max(second of R, second of Cm): in another
+        // row than M it is that row's maximum and sits in M's column unless
+        // it is also its own column's maximum; in M's row it is its column's
+        // maximum. Only the 16 maxima carry their row or column index (low
+        // three mantissa bits, a relative change below 2^-20, inside the
+        // filter's margin). Where two values of the chunk lie within that
+        // change of each other the indices may name another cell; such a
+        // key's two best values are then within the margin, so it is not
+        // certified, and its chunk's second value, standing in for the
+        // third, sends it to the full exact scan. The columns come in four
+        // groups of 16 (two grid rows), the TMEM load of the next group in
+        // flight while the current one is reduced.
         float R[8], Cm[8];
         uint32_t ra[16], rb[16];
         if (!abort_s) tc_wait(&acc_full[ti], (gc >> 1) & 1, &abort_s);
@@ -717,15 +725,17 @@ k_assign_tc(const __grid_constant__ CUtensorMap keys_map, const __grid_constant_
         const uint32_t tacc = tbase + ti * kTcN;
         tmem_ld16_async(tacc, ra);
         auto group = [&](const uint32_t(&r)[16], int g) {
-          float x[16];
 #pragma unroll
-          for (int k = 0; k < 16; ++k) x[k] = pack6_mul(__uint_as_float(r[k]), g * 16 + k, m26, m64);
-#pragma unroll
-          for (int c = 0; c < 8; ++c) Cm[c] = g == 0 ? fmaxf(x[c], x[8 + c]) : max3f(Cm[c], x[c], x[8 + c]);
+          for (int c = 0; c < 8; ++c) {
+            const float a0 = __uint_as_float(r[c]), a1 = __uint_as_float(r[8 + c]);
+            Cm[c] = g == 0 ? fmaxf(a0, a1) : max3f(Cm[c], a0, a1);
+          }
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            const float *y = x + 8 * h;
-            R[2 * g + h] = max3f(max3f(y[0], y[1], y[2]), max3f(y[3], y[4], y[5]), fmaxf(y[6], y[7]));
+            const uint32_t *y = r + 8 * h;
+            R[2 * g + h] = max3f(max3f(__uint_as_float(y[0]), __uint_as_float(y[1]), __uint_as_float(y[2])),
+                                 max3f(__uint_as_float(y[3]), __uint_as_float(y[4]), __uint_as_float(y[5])),
+                                 fmaxf(__uint_as_float(y[6]), __uint_as_float(y[7])));
           }
         };
         tc_wait_ld16(ra);
@@ -739,6 +749,14 @@ k_assign_tc(const __grid_constant__ CUtensorMap keys_map, const __grid_constant_
         group(ra, 2);
         tc_wait_ld16(rb);
         group(rb, 3);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) tc_arrive(&acc_empty[ti]);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          R[k] = pack3_mul(R[k], k, m29, m8);
+          Cm[k] = pack3_mul(Cm[k], k, m29, m8);
+        }
         // the two largest of R and of Cm (pairwise: the first pair seeds the
         // list, each further pair is merged into it)
         float r1 = fmaxf(R[0], R[1]), r2 = fminf(R[0], R[1]);
@@ -749,9 +767,12 @@ k_assign_tc(const __grid_constant__ CUtensorMap keys_map, const __grid_constant_
           top2max_pair(c1, c2, Cm[k], Cm[k + 1]);
         }
         const float q1 = r1, q2 = fmaxf(r2, c2);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) tc_arrive(&acc_empty[ti]);
+        const uint32_t i1 = __float_as_uint(r1) & 7u, k1 = __float_as_uint(c1) & 7u;
+        const uint32_t i2r = __float_as_uint(r2) & 7u, k2c = __float_as_uint(c2) & 7u;
+        const uint32_t hr = __float_as_uint(r2) >> 3, hc = __float_as_uint(c2) >> 3;
+        // x2's cell: (its row, M's column), (M's row, its column), or, when
+        // it is both a row and a column maximum, (its row, its column)
+        const uint32_t cell2 = hr == hc ? 8u * i2r + k2c : (r2 > c2 ? 8u * i2r + k1 : 8u * i1 + k2c);
         // fold the chunk's two into the running list with column ids, as
         // e - |k|^2 = -2 (k.c~ - |c~|^2 / 2) (exact scaling); the chunk's
         // third smallest is at least p2, so p2 stands in as a lower bound
@@ -761,8 +782,8 @@ k_assign_tc(const __grid_constant__ CUtensorMap keys_map, const __grid_constant_
         const int jb = ch * kTcN + qtr * 64;
         Top3 cur;
         cur.v1 = p1; cur.v2 = p2; cur.v3 = p2;
-        cur.j1 = q1 > -INFINITY ? jb + (int)(__float_as_uint(q1) & 63u) : 0x7fffffff;
-        cur.j2 = q2 > -INFINITY ? jb + (int)(__float_as_uint(q2) & 63u) : 0x7fffffff;
+        cur.j1 = q1 > -INFINITY ? jb + (int)(8u * i1 + k1) : 0x7fffffff;
+        cur.j2 = q2 > -INFINITY ? jb + (int)cell2 : 0x7fffffff;
         top = top3_union(top, cur);
       }
       // merge the four column quarters of each key, then decide
@@ -1479,7 +1500,7 @@ static cudaError_t kmeans_build_t(const CtxView &v, int layer, const KmeansScrat
       k_assign_tc<<<tc_grid, kTcThreads, kTcSmem, st>>>(keys_map, cent_map, c2b_map, n, c, v.u_cap,
                                                         ks.knorm, v.n_cap, ks.cstat, kTcEps, v.assign,
                                                         gs0, S, ks.amb, ks.amb_count, ks.amb_count + 1,
-                                                        (int32_t)amb_cap, v.err, 1u << 26, 64u);
+                                                        (int32_t)amb_cap, v.err, 1u << 29, 8u);
     } else {
       k_assign_simt<DT><<<dim3((unsigned)((n + kAsTile - 1) / kAsTile), S), kAsThreads, kAsSmem, st>>>(
           keys, n, c, v.cent_op, v.u_cap, ks.c2, ks.c2_pitch, ks.knorm, v.n_cap, ks.cstat, eps,
