@@ -1190,6 +1190,51 @@ __device__ __forceinline__ float mean_rn(double sum, double cnt, double y) {
   return __double2float_rn(__fma_rn(r, y, q));
 }
 
+// Fast exact accumulation of one bf16 value (the low 16 bits of b) in 2^-35
+// fixed point: v * 2^35 = +-(128 + m) << (e - 99) for biased exponents
+// 99..131 (2^-28 <= |v| < 32), a shift of at most 32, so the 64-bit value
+// is one 32-bit shift (lo) and one funnel shift (hi, the sign-extended
+// mantissa's upper word). A nonzero value outside that range sets *oor
+// (the caller then takes the 2^-40 path) and adds nothing.
+__device__ __forceinline__ void fixed35_add(uint32_t b, int64_t &acc, int &oor) {
+  const uint32_t e = (b >> 7) & 0xffu;
+  const uint32_t sh = e - 99u;
+  const bool in = sh <= 32u;
+  if (!in && (b & 0x7fffu) != 0u) oor = 1;
+  const int32_t m = in ? (int32_t)((b & 0x7fu) | 0x80u) : 0;
+  const int32_t ms = (b & 0x8000u) ? -m : m;
+  const uint32_t sx = (uint32_t)(ms >> 31);
+  uint32_t lo, hi;
+  asm("shl.b32 %0, %1, %2;" : "=r"(lo) : "r"((uint32_t)ms), "r"(sh));
+  asm("shf.l.clamp.b32 %0, %1, %2, %3;" : "=r"(hi) : "r"((uint32_t)ms), "r"(sx), "r"(sh));
+  acc += (int64_t)(((uint64_t)hi << 32) | lo);
+}
+
+// fixed35_add over a cluster of at most kUpdExactCount members
+__device__ __forceinline__ void fixed35_sums(const void *keys, const int32_t *pm, int32_t cnt, int64_t row0,
+                                             int lane, int64_t (&acc)[4], int &oor) {
+  for (int32_t m0 = 0; m0 < cnt; m0 += kUpdBatch) {
+    const int nb = min(kUpdBatch, cnt - m0);
+    const int32_t mine = lane < nb ? __ldg(pm + m0 + lane) : 0;
+    uint2 raw[kUpdBatch];
+    float unused[4];
+#pragma unroll
+    for (int b = 0; b < kUpdBatch; ++b) {
+      const int32_t i = __shfl_sync(0xffffffffu, mine, b);
+      if (b < nb) load4<1>(keys, row0 + i, lane, unused, raw[b]);
+    }
+#pragma unroll
+    for (int b = 0; b < kUpdBatch; ++b) {
+      if (b < nb) {
+        fixed35_add(raw[b].x & 0xffffu, acc[0], oor);
+        fixed35_add(raw[b].x >> 16, acc[1], oor);
+        fixed35_add(raw[b].y & 0xffffu, acc[2], oor);
+        fixed35_add(raw[b].y >> 16, acc[3], oor);
+      }
+    }
+  }
+}
+
 __device__ __forceinline__ uint32_t bf16_exp_nz(uint32_t bits16) {
   const uint32_t e = (bits16 >> 7) & 0xffu;
   return (bits16 & 0x7fffu) ? e : 255u;  // zeros do not set the grid
@@ -1198,7 +1243,7 @@ __device__ __forceinline__ uint32_t bf16_exp_nz(uint32_t bits16) {
 // Exact fixed-point sums of a cluster's bf16 members (this lane's four
 // dimensions); big (warp-uniform): also the smallest biased exponent of the
 // nonzero members and the float sum of magnitudes.
-__device__ __forceinline__ void fixed_sums(const void *keys, const int32_t *pm, int32_t cnt, int64_t row0,
+__device__ __noinline__ void fixed_sums(const void *keys, const int32_t *pm, int32_t cnt, int64_t row0,
                                            int lane, bool big, int64_t (&acc)[4], int &oor, uint32_t &e_min,
                                            float &asum) {
   for (int32_t m0 = 0; m0 < cnt; m0 += kUpdBatch) {
@@ -1230,7 +1275,7 @@ __device__ __forceinline__ void fixed_sums(const void *keys, const int32_t *pm, 
 }
 
 template <int DT>
-__global__ void __launch_bounds__(kUpdThreads, 3) k_update(const void *keys, int64_t n, int64_t n_cap, int32_t c,
+__global__ void __launch_bounds__(kUpdThreads, 2) k_update(const void *keys, int64_t n, int64_t n_cap, int32_t c,
                          int32_t c_cap, int32_t u_cap, int64_t gs0, const int32_t *perm,
                          const int32_t *count, const int32_t *offs, float *cent32,
                          int64_t *n_inexact, int n_slices) {
@@ -1254,8 +1299,23 @@ __global__ void __launch_bounds__(kUpdThreads, 3) k_update(const void *keys, int
     uint32_t e_min = 255u;
     float asum = 0.f;
     const bool big = cnt > kUpdExactCount;
-    fixed_sums(keys, pm, cnt, row0, lane, big, acc, oor, e_min, asum);
-    if (big && e_min < 255u) {
+    // small clusters: the 2^-35 path first, the 2^-40 path if a member lies
+    // below its range
+    bool done = false;
+    if (!big) {
+      int oor35 = 0;
+      fixed35_sums(keys, pm, cnt, row0, lane, acc, oor35);
+      done = __any_sync(0xffffffffu, oor35) == 0;
+      if (done) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sum[e] = __dmul_rn(__ll2double_rn(acc[e]), 0x1p-35);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[e] = 0;
+      }
+    }
+    if (!done) fixed_sums(keys, pm, cnt, row0, lane, big, acc, oor, e_min, asum);
+    if (!done && big && e_min < 255u) {
       // the float sum of 4 cnt magnitudes is at least (1 - 4 cnt 2^-24) A,
       // so at least 7/8 A for cnt < 2^19: below 7/8 of the limit, A is
       // below the limit
@@ -1264,8 +1324,10 @@ __global__ void __launch_bounds__(kUpdThreads, 3) k_update(const void *keys, int
     }
     slow = __any_sync(0xffffffffu, oor) != 0;
     if (!slow) {
+      if (!done) {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) sum[e] = fixed40_to_double(acc[e]);
+        for (int e = 0; e < 4; ++e) sum[e] = fixed40_to_double(acc[e]);
+      }
     } else if (lane == 0) {
       atomicAdd((unsigned long long *)n_inexact, 1ull);
     }
