@@ -1184,6 +1184,17 @@ __device__ __forceinline__ void load4(const void *keys, int64_t row, int lane, f
   }
 }
 
+// RN(1/count) for the counts of the fast path, rounded once by the compiler's
+// IEEE division at compile time (a warp-uniform constant-memory read instead
+// of a double-precision reciprocal per cluster)
+struct RcpTable {
+  double v[kUpdExactCount + 1];
+  constexpr RcpTable() : v() {
+    for (int i = 1; i <= kUpdExactCount; ++i) v[i] = 1.0 / i;
+  }
+};
+__constant__ RcpTable c_rcp = RcpTable();
+
 __device__ __forceinline__ float mean_rn(double sum, double cnt, double y) {
   const double q = __dmul_rn(sum, y);
   const double r = __fma_rn(-q, cnt, sum);
@@ -1290,7 +1301,7 @@ __global__ void __launch_bounds__(kUpdThreads, 2) k_update(const void *keys, int
   const int64_t gs = gs0 + s;
   const int32_t *pm = perm + gs * n_cap + base;
   const int64_t row0 = (int64_t)s * n;
-  const double cd = (double)cnt, y = __drcp_rn(cd);
+  const double cd = (double)cnt, y = cnt <= kUpdExactCount ? c_rcp.v[cnt] : __drcp_rn(cd);
   double sum[4] = {0.0, 0.0, 0.0, 0.0};
   bool slow = (DT == 0);
   if constexpr (DT == 1) {
@@ -1307,8 +1318,19 @@ __global__ void __launch_bounds__(kUpdThreads, 2) k_update(const void *keys, int
       fixed35_sums(keys, pm, cnt, row0, lane, acc, oor35);
       done = __any_sync(0xffffffffu, oor35) == 0;
       if (done) {
+        // the mean of the 2^-35 sum with the scale folded into the
+        // reciprocal and the count (both exact): q = RN(S y 2^-35), then
+        // q + (S - count 2^35 q) y 2^-35, the same correctly rounded value
+        const double y35 = y * 0x1p-35, c35 = cd * 0x1p35;
+        float mf[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) sum[e] = __dmul_rn(__ll2double_rn(acc[e]), 0x1p-35);
+        for (int e = 0; e < 4; ++e) {
+          const double sd = __ll2double_rn(acc[e]);
+          const double q = __dmul_rn(sd, y35);
+          mf[e] = __double2float_rn(__fma_rn(__fma_rn(-q, c35, sd), y35, q));
+        }
+        *(float4 *)(cent32 + (gs * u_cap + j) * kHeadDim + lane * 4) = make_float4(mf[0], mf[1], mf[2], mf[3]);
+        continue;
       } else {
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[e] = 0;
