@@ -1224,15 +1224,24 @@ __device__ __forceinline__ void fixed35_add(uint32_t b, int64_t &acc, int &oor) 
 // fixed35_add over a cluster of at most kUpdExactCount members
 __device__ __forceinline__ void fixed35_sums(const void *keys, const int32_t *pm, int32_t cnt, int64_t row0,
                                              int lane, int64_t (&acc)[4], int &oor) {
+  int32_t mine = lane < min(kUpdBatch, cnt) ? __ldg(pm + lane) : 0;
   for (int32_t m0 = 0; m0 < cnt; m0 += kUpdBatch) {
     const int nb = min(kUpdBatch, cnt - m0);
-    const int32_t mine = lane < nb ? __ldg(pm + m0 + lane) : 0;
     uint2 raw[kUpdBatch];
     float unused[4];
 #pragma unroll
     for (int b = 0; b < kUpdBatch; ++b) {
       const int32_t i = __shfl_sync(0xffffffffu, mine, b);
       if (b < nb) load4<1>(keys, row0 + i, lane, unused, raw[b]);
+    }
+    // the next batch: its member ids now, its rows into L2 while this batch
+    // is summed (lane b takes both 128-byte halves of row b)
+    const int nb1 = min(kUpdBatch, cnt - m0 - kUpdBatch);
+    const int32_t next = lane < nb1 ? __ldg(pm + m0 + kUpdBatch + lane) : 0;
+    if (lane < nb1) {
+      const char *p = (const char *)keys + (row0 + next) * (int64_t)(kHeadDim * 2);
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(p + 128));
     }
 #pragma unroll
     for (int b = 0; b < kUpdBatch; ++b) {
@@ -1243,6 +1252,7 @@ __device__ __forceinline__ void fixed35_sums(const void *keys, const int32_t *pm
         fixed35_add(raw[b].y >> 16, acc[3], oor);
       }
     }
+    mine = next;
   }
 }
 
