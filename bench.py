@@ -319,7 +319,32 @@ def read_ceiling(torch, nbytes, flush, hbm_peak, reps=16):
             "l2": "256 MB written, then 256 MB read, before every launch"}
 
 
-def in_graph_attention(g_bytes, g_sec, launches, hbm_peak):
+def l2_read_ceiling(torch, nbytes, reps=32):
+    """Sustained rate at which lkv_read_ceiling reads nbytes of device memory
+    that L2 holds: two untimed launches, then `reps` launches back to back
+    between one pair of CUDA events (so launch gaps are hidden, as the
+    overlapped launches of the decode graph hide them). The timed decode
+    graph's attention reads most of its rows from L2, so this is its
+    ceiling."""
+    from cluster_indexed_kv_gb300 import _lib
+    nbytes = int(nbytes) // 16 * 16
+    buf = torch.ones(nbytes // 4, dtype=torch.int32, device="cuda")
+    st = torch.cuda.current_stream()
+    for _ in range(2):
+        _lib.lkv_read_ceiling(buf.data_ptr(), nbytes, st.cuda_stream)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for _ in range(reps):
+        _lib.lkv_read_ceiling(buf.data_ptr(), nbytes, st.cuda_stream)
+    e1.record(st)
+    e1.synchronize()
+    sec = e0.elapsed_time(e1) / reps / 1e3
+    del buf
+    return {"bytes": nbytes, "avg_launch_us": sec * 1e6, "achieved": nbytes / sec / 1e9, "unit": "GB/s",
+            "kernel": f"lkv_read_ceiling over a buffer that L2 holds, {reps} launches back to back"}
+
+
+def in_graph_attention(g_bytes, g_sec, launches, hbm_peak, l2c=None):
     """The attention as the timed decode graph runs it: algorithmic bytes
     per step over the decode time per step, and the DRAM bytes per step of
     a whole 512-step graph from the committed ncu record (cache control
@@ -337,6 +362,9 @@ def in_graph_attention(g_bytes, g_sec, launches, hbm_peak):
         out["dram_GBps"] = dram / g_sec / 1e9
         out["dram_frac_of_hbm"] = dram / g_sec / 1e9 / hbm_peak
         out["l2_served_frac"] = 1.0 - dram / g_bytes
+    if l2c is not None:
+        out["l2_read_ceiling"] = l2c
+        out["frac_alg_of_l2_ceiling"] = g_bytes / g_sec / 1e9 / l2c["achieved"]
     return out
 
 
@@ -485,6 +513,7 @@ def run_ours(args, rank, world, local):
     n_attn, ms_attn, alg_bytes, attn_s, achieved = attn_roofline(kern_p, ctr, w, eb)
     g_launches = T * K_steps  # one attention launch per step covers all NL layers
     ceiling = read_ceiling(torch, alg_bytes, flush, hbm_peak)
+    l2c = l2_read_ceiling(torch, alg_bytes)
     g_bytes, g_sec = graph_attention(ctr_timed, w, eb, dec_ms, g_launches)
     breakdown = {k: {"launches": int(v[0]), "avg_us": round(v[1] / v[0] * 1e3, 2)}
                  for k, v in kern_p.items() if v[0]}
@@ -558,7 +587,7 @@ def run_ours(args, rank, world, local):
                      "launches": int(n_attn), "l2": "single-step launches; before every step 256 MB written, then 256 MB read",
                      "single_launch_read_ceiling": ceiling,
                      "frac_of_single_launch_ceiling": achieved / ceiling["achieved"],
-                     "in_graph": in_graph_attention(g_bytes, g_sec, g_launches, hbm_peak)},
+                     "in_graph": in_graph_attention(g_bytes, g_sec, g_launches, hbm_peak, l2c)},
         "roofline_kmeans_assign": {
             "kernel": "k_assign_tc" if km_kernel == "kmeans_assign_tc" else "k_assign_simt",
             "bound": "tensor", "achieved": km_tf, "peak": tc_peak, "unit": "TFLOP/s",
