@@ -16,9 +16,11 @@
 // for every cluster when a third one is also within 2 beta).
 //
 // Update: members are grouped by a stable counting sort (token order within a
-// cluster); the member sum of bf16 keys is formed exactly in 2^-40 fixed
-// point (double-precision token-order sum when a value is out of that range,
-// and always for fp32 keys); centroid = float(sum / count) in double.
+// cluster); the member sum of bf16 keys is formed exactly in fixed point
+// (2^-35, else 2^-40), which equals the token-order double sum whenever no
+// partial sum can round; otherwise, and always for fp32 keys, it is the
+// double-precision token-order sum itself; centroid = float(sum / count) in
+// double.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
