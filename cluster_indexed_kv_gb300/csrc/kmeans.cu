@@ -923,35 +923,40 @@ __device__ __forceinline__ float scan32(const float (&k4)[4], const char *cb, in
   return v[0];
 }
 
-// Keys with two candidates: a warp per queue entry, the two exact distances
-// computed by lanes 0 and 1 (each sequentially over the dimensions, the
-// oracle's order), the smaller wins, the lower id on a tie.
+// Keys with two candidates: a lane pair per queue entry, 16 entries per warp;
+// the two exact distances are computed by the pair's two lanes (each
+// sequentially over the dimensions, the oracle's order), the smaller wins,
+// the lower id on a tie. (The double-precision unit runs a warp instruction
+// at a time whatever its active lanes, so every lane carries a distance.)
 template <int DT>
 __global__ void k_refine_pairs(const void *keys, int64_t n, const void *cent_op, int32_t u_cap,
                                int32_t *assign, int64_t n_cap, int64_t gs0, const int4 *amb,
                                const int32_t *amb_count, int32_t amb_cap, int64_t *n_refined) {
   const int lane = threadIdx.x & 31;
-  const int warps = gridDim.x * (blockDim.x / 32);
-  const int w0 = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x / 32);
+  const int64_t w0 = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   const int total = min(*amb_count, amb_cap);
   if (blockIdx.x == 0 && threadIdx.x == 0) atomicAdd((unsigned long long *)n_refined, (unsigned long long)total);
   const int eb = elem_bytes<DT>();
-  for (int w = w0; w < total; w += warps) {
-    const int4 e = amb[w];
-    const int64_t gs = gs0 + e.x;
-    const int64_t row = e.y;
+  for (int64_t w = w0; w * 16 < total; w += warps) {
+    const int64_t q = w * 16 + (lane >> 1);
+    const bool on = q < total;
     double best = INFINITY;
     int32_t bj = 0x7fffffff;
-    if (lane < 2) {
+    int64_t gs = 0, row = 0;
+    if (on) {
+      const int4 e = amb[q];
+      gs = gs0 + e.x;
+      row = e.y;
       const char *key_row = (const char *)keys + ((int64_t)e.x * n + row) * kHeadDim * eb;
       const char *cb = (const char *)cent_op + gs * u_cap * (int64_t)kHeadDim * eb;
-      bj = lane == 0 ? e.z : e.w;
+      bj = (lane & 1) ? e.w : e.z;
       best = sqdist64<DT>(key_row, cb + (int64_t)bj * kHeadDim * eb);
     }
     const double ob = __shfl_xor_sync(0xffffffffu, best, 1);
     const int32_t oj = __shfl_xor_sync(0xffffffffu, bj, 1);
     if (ob < best || (ob == best && oj < bj)) bj = oj;
-    if (lane == 0) assign[gs * n_cap + row] = bj;
+    if (on && (lane & 1) == 0) assign[gs * n_cap + row] = bj;
   }
 }
 
@@ -964,6 +969,7 @@ __global__ void k_refine_pairs(const void *keys, int64_t n, const void *cent_op,
 // single-precision distance is within a factor 1 + 2^-13 of the smallest one
 // (plus 2^-100 for underflowing terms); only those get the exact distance.
 constexpr int kCrowdThreads = 256;
+constexpr int kCrowdCand = 1024;  // candidates compacted per entry (more: the per-thread scan)
 
 template <int DT>
 __global__ void __launch_bounds__(kCrowdThreads)
@@ -971,6 +977,8 @@ k_refine_crowded(const void *keys, int64_t n, int32_t c, const void *cent_op, in
                  int32_t *assign, int64_t n_cap, int64_t gs0, const int4 *amb,
                  const int32_t *amb_crowd, int32_t amb_cap, int64_t *n_refined) {
   extern __shared__ float d32[];  // [c]
+  __shared__ int32_t cand[kCrowdCand];
+  __shared__ int s_nc;
   __shared__ float wmin[kCrowdThreads / 32];
   __shared__ double wbest[kCrowdThreads / 32];
   __shared__ int32_t wj[kCrowdThreads / 32];
@@ -1001,12 +1009,31 @@ k_refine_crowded(const void *keys, int64_t n, int32_t c, const void *cent_op, in
 #pragma unroll
     for (int w = 0; w < nw; ++w) m = fminf(m, wmin[w]);
     const float thr = fmaf(m, 0x1p-13f, m) + 0x1p-100f;
+    // the candidates, compacted into adjacent threads (the double-precision
+    // unit runs a warp instruction at a time whatever its active lanes)
+    if (threadIdx.x == 0) s_nc = 0;
+    __syncthreads();
+    for (int j = threadIdx.x; j < c; j += kCrowdThreads)
+      if (d32[j] <= thr) {
+        const int k = atomicAdd(&s_nc, 1);
+        if (k < kCrowdCand) cand[k] = j;
+      }
+    __syncthreads();
+    const int nc = s_nc;
     double best = INFINITY;
     int32_t bj = 0x7fffffff;
-    for (int j = threadIdx.x; j < c; j += kCrowdThreads) {
-      if (d32[j] <= thr) {
+    if (nc <= kCrowdCand) {
+      for (int i = threadIdx.x; i < nc; i += kCrowdThreads) {
+        const int j = cand[i];
         const double d64 = sqdist64<DT>(key_row, cb + (int64_t)j * kHeadDim * eb);
-        if (d64 < best) { best = d64; bj = j; }  // ascending j: keeps lowest on ties
+        if (d64 < best || (d64 == best && j < bj)) { best = d64; bj = j; }
+      }
+    } else {
+      for (int j = threadIdx.x; j < c; j += kCrowdThreads) {
+        if (d32[j] <= thr) {
+          const double d64 = sqdist64<DT>(key_row, cb + (int64_t)j * kHeadDim * eb);
+          if (d64 < best) { best = d64; bj = j; }  // ascending j: keeps lowest on ties
+        }
       }
     }
 #pragma unroll
