@@ -98,11 +98,14 @@ def test_kmeans_update_sums_in_token_order_past_2_13():
     assert st["n_inexact"] >= 1  # the cluster left the fixed-point path
 
 
-def _decode_check(w, *, tau=None, budget=None, T=None, seqs=None, teacher=True, build_seed=3):
+def _decode_check(w, *, tau=None, budget=None, T=None, seqs=None, teacher=True, build_seed=3,
+                  key_scale=1.0):
     T = T or w.n_steps
     dev = "cuda"
     K, V = synth.prefill(w, 0, dev)
     q, kn, vn, _ = synth.decode_inputs(w, dev, n_steps=T)
+    if key_scale != 1.0:
+        kn = (kn.float() * key_scale).to(kn.dtype)
     ctx = H.make_ctx(w, max_steps=T, max_budget=max(budget or w.budget, 1))
     ctx.build_index(0, K, V, w.n_clusters, w.iters, build_seed)
     ctx.sync()
@@ -127,6 +130,45 @@ def _decode_check(w, *, tau=None, budget=None, T=None, seqs=None, teacher=True, 
 def test_decode_tiny_fp32_full():
     rep = _decode_check(synth.WORKLOADS["tiny"], teacher=False)
     assert rep[0]["n_boundary"] >= 1
+
+
+def test_kmeans_update_tiny_and_zero_members():
+    """Members below the fast path's range: |v| < 2^-28 sends a cluster of at
+    most 256 members to the 2^-40 sums, |v| < 2^-33 to the double-precision
+    token-order sums, and signed zeros add nothing. Centroids stay bit-exact
+    with the oracle on every path."""
+    w = synth.WORKLOADS["long_in"].replace(n_kv_heads=1, batch=1, n_prefill=1024, n_components=16,
+                                           n_clusters=16, iters=3)
+    K, V = synth.prefill(w, 0, "cuda")
+    Kf = K.float()
+    idx = torch.arange(1024, device="cuda")
+    Kf[0, 0, idx % 7 == 0, 0] = 2.0 ** -30
+    Kf[0, 0, idx % 11 == 0, 1] = -(2.0 ** -36)
+    Kf[0, 0, idx % 5 == 0, 2] = 0.0
+    Kf[0, 0, idx % 13 == 0, 3] = -0.0
+    K = Kf.to(torch.bfloat16)
+    ctx = H.make_ctx(w)
+    ctx.build_index(0, K, V, 16, 3, 9)
+    g = ctx.get_index(0, 0, 0, 1024)
+    st = ctx.decode_state(0, 0)
+    ctx.close()
+    o = oracle.kmeans(synth.to_oracle(K[0, 0]), 16, 3, 9)
+    assert int(g["unit_len"].max()) <= 256  # every cluster takes the fast path first
+    assert np.array_equal(g["assign"], o["assign"])
+    assert np.array_equal(g["centroids"].view(np.uint32), o["cent"].view(np.uint32))
+    assert st["n_inexact"] > 0  # the 2^-36 members took the double-precision path
+
+
+def test_decode_segment_means_with_large_keys():
+    """Decode keys scaled so that some reach 16..32: with L = 512 a segment
+    that holds one leaves the fixed-point sum for the token-order double sum
+    (the exponent bound that keeps every partial sum exact). The segment
+    means stay bit-exact with the oracle either way."""
+    w = synth.WORKLOADS["long_out"].replace(batch=2, n_kv_heads=2, n_prefill=700, n_components=30,
+                                            n_clusters=30, iters=5, local_buf=512, budget=200,
+                                            jump_p=0.08)
+    rep = _decode_check(w, tau=0.9, T=640, key_scale=12.0)
+    assert all(r["n_evicted"] >= 1 for r in rep)
 
 
 def test_decode_bf16_evictions_and_forced_cuts():
